@@ -1,0 +1,361 @@
+"""Pins for the CPU oracle: the worked example printed on the HugeCTR page,
+closed forms, special cases that reduce to library routines, brute force on
+tiny inputs, and invariants.  None of these re-type the oracle's code."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.conftest import load_golden
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# --------------------------------------------------------------- fp16 codec
+def test_half_to_double_matches_numpy_for_every_bit_pattern(oracle_lib):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_double_to_half_matches_numpy_rounding(oracle_lib):
+    rng = np.random.default_rng(1)
+    halves = np.arange(0, 0x7c00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mids = (halves[:-1] + halves[1:]) / 2          # exact ties: nearest-even decides
+    vals = np.concatenate([
+        halves, mids, -mids, np.nextafter(mids, 0), np.nextafter(mids, 1),
+        rng.normal(0, 0.01, 20000), rng.normal(0, 100, 5000),
+        np.ldexp(rng.uniform(0.5, 1, 5000), rng.integers(-30, 17, 5000)),
+        [65504.0, 65519.99, 65520.0, 1e9, -1e9, 2.0 ** -25, 2.0 ** -26, 3 * 2.0 ** -26, 0.0, -0.0],
+    ])
+    ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.double_to_half(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------- HugeCTR worked example
+def test_preprocess_matches_hugectr_worked_example(oracle_lib):
+    g = load_golden("hugectr_worked_example.txt")
+    tab = oracle.Tables([g["E"][0]], [8])
+    idx = np.array(g["rows"], np.int64)
+    off = np.array(g["offsets"], np.int64)
+    pp = oracle.preprocess(tab, g["B"][0], idx, off)
+    assert pp["sorted_keys"].tolist() == g["sorted_rows"]
+    assert pp["sorted_bags"].tolist() == g["sorted_bags"]
+    assert pp["run_starts"].tolist() == g["run_starts"]
+    assert len(pp["unique_keys"]) == g["count"][0]
+    # The page's intermediate arrays agree with the oracle's runs: a flag marks
+    # each run start, and its inclusive prefix sum numbers the runs.
+    flags = [int(i in pp["run_starts"][:-1]) for i in range(len(idx))]
+    assert flags == g["flags"]
+    assert np.cumsum(flags).tolist() == g["flag_scan"]
+    # The sample id of every sorted lookup, read through the sort permutation,
+    # is its bag: the expansion step of the page.
+    assert [g["sample_id"][p] for p in pp["sorted_pos"]] == g["sorted_bags"]
+    # keys -> rows by the tens digit, as the page maps them
+    assert [k // 10 for k in g["keys"]] == g["rows"]
+
+
+# ------------------------------------------------------------- random cases
+def _tiny_problem(seed, T=3, B=5, maxL=6, E=(7, 4, 9), D=(8, 16, 8), weighted=False,
+                  dtype=np.int64, invalid=False):
+    rng = np.random.default_rng(seed)
+    E = np.asarray(E[:T]); D = np.asarray(D[:T])
+    L = rng.integers(0, maxL + 1, T * B)
+    off = np.concatenate([[0], np.cumsum(L)]).astype(dtype)
+    idx = np.concatenate([rng.integers(0, E[t], L[t * B:(t + 1) * B].sum()) for t in range(T)])
+    if invalid and len(idx):
+        bad = rng.random(len(idx)) < 0.15
+        idx[bad] = rng.choice([-1, -7, 10 ** 6], bad.sum())
+    idx = idx.astype(dtype)
+    tab = oracle.Tables(E, D)
+    W = (rng.normal(0, 0.5, int((E * D).sum()))).astype(np.float16)
+    G = rng.normal(0, 1, (B, int(D.sum()))).astype(np.float32)
+    psw = rng.uniform(0, 1, len(idx)).astype(np.float32) if weighted else None
+    return tab, B, idx, off, W, G, psw
+
+
+def _lookups(tab, B, idx, off):
+    """(t, b, position, row) for every lookup, read straight from the CSR arrays."""
+    out = []
+    for bag in range(tab.T * B):
+        t, b = divmod(bag, B)
+        for i in range(int(off[bag]), int(off[bag + 1])):
+            out.append((t, b, i, int(idx[i])))
+    return out
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_preprocess_brute_force(oracle_lib, seed):
+    tab, B, idx, off, *_ = _tiny_problem(seed, invalid=seed % 2 == 1)
+    pp = oracle.preprocess(tab, B, idx, off)
+    look = [(int(tab.hash_base[t]) + r, b, i) for t, b, i, r in _lookups(tab, B, idx, off)
+            if 0 <= r < tab.E[t]]
+    keys = sorted({k for k, _, _ in look})
+    # O(n * R): for each key in increasing order, list its lookups by position.
+    exp_keys, exp_bags, exp_pos, starts = [], [], [], []
+    for k in keys:
+        starts.append(len(exp_keys))
+        for kk, b, i in sorted(look, key=lambda x: x[2]):
+            if kk == k:
+                exp_keys.append(k); exp_bags.append(b); exp_pos.append(i)
+    starts.append(len(exp_keys))
+    assert pp["sorted_keys"].tolist() == exp_keys
+    assert pp["sorted_bags"].tolist() == exp_bags
+    assert pp["sorted_pos"].tolist() == exp_pos
+    assert pp["unique_keys"].tolist() == keys
+    assert pp["run_starts"].tolist() == starts
+    # invariants: sum of run lengths = number of valid lookups; keys strictly increase
+    assert int(np.diff(pp["run_starts"]).sum()) == len(look)
+    assert np.all(np.diff(pp["unique_keys"].astype(np.int64)) > 0)
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("weighted", [False, True])
+def test_forward_brute_force_exact_rational(oracle_lib, seed, weighted):
+    tab, B, idx, off, W, G, psw = _tiny_problem(seed, weighted=weighted, dtype=np.int32,
+                                                invalid=seed == 3)
+    out = oracle.forward(tab, B, W, idx, off, psw)
+    exp = np.zeros_like(out, dtype=object)
+    exp[:] = Fraction(0)
+    for t, b, i, r in _lookups(tab, B, idx, off):
+        if not 0 <= r < tab.E[t]:
+            continue
+        c = Fraction(float(psw[i])) if weighted else Fraction(1)
+        base = int(tab.w_offsets[t]) + r * int(tab.D[t])
+        for d in range(int(tab.D[t])):
+            exp[b, int(tab.D_offsets[t]) + d] += c * Fraction(float(W[base + d]))
+    exact = np.array([[float(x) for x in row] for row in exp])
+    # the double sum is rounded once to fp32: within half an fp32 ulp of exact
+    ulp = np.spacing(np.abs(exact).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(out.astype(np.float64) - exact) <= 0.5 * ulp + 1e-300)
+
+
+def test_forward_closed_forms(oracle_lib):
+    tab = oracle.Tables([5, 3], [8, 16])
+    rng = np.random.default_rng(0)
+    W = rng.normal(0, 1, int(tab.w_offsets[-1])).astype(np.float16)
+    B = 4
+    # table 0: bag0 one-hot row 2; bag1 row 4 repeated 2048 times; bag2 empty; bag3 rows 0,1
+    # table 1: bag0 one-hot row 1; bag1 empty; bag2 row 2 x3; bag3 row 0
+    bags = [[2], [4] * 2048, [], [0, 1], [1], [], [2, 2, 2], [0]]
+    idx = np.array([r for bg in bags for r in bg], np.int64)
+    off = np.concatenate([[0], np.cumsum([len(b) for b in bags])]).astype(np.int64)
+    out = oracle.forward(tab, B, W, idx, off)
+    row = lambda t, r: W[tab.w_offsets[t] + r * tab.D[t]: tab.w_offsets[t] + (r + 1) * tab.D[t]]
+    assert np.array_equal(out[0, :8], row(0, 2).astype(np.float32))
+    assert np.array_equal(out[1, :8], 2048 * row(0, 4).astype(np.float32))
+    assert np.array_equal(out[2, :8], np.zeros(8, np.float32))
+    assert np.array_equal(out[0, 8:], row(1, 1).astype(np.float32))
+    assert np.array_equal(out[1, 8:], np.zeros(16, np.float32))
+    assert np.array_equal(out[2, 8:], 3 * row(1, 2).astype(np.float32))
+    # a per-sample weight scales its single row: one rounding of an exact product
+    psw = np.full(len(idx), 1.0, np.float32)
+    assert np.array_equal(oracle.forward(tab, B, W, idx, off, psw), out)
+    psw[0] = 0.3
+    o2 = oracle.forward(tab, B, W, idx, off, psw)
+    assert np.array_equal(o2[0, :8],
+                          (np.float64(np.float32(0.3)) * row(0, 2).astype(np.float64))
+                          .astype(np.float32))
+
+
+def test_forward_skips_out_of_range_rows(oracle_lib):
+    tab, B, idx, off, W, G, psw = _tiny_problem(11)
+    bad_idx = idx.copy()
+    bad_idx[::5] = -3
+    keep = np.ones(len(idx), bool)
+    keep[::5] = False
+    # drop those lookups from the CSR by hand
+    new_off = np.array([keep[:o].sum() for o in off], np.int64)
+    assert np.array_equal(oracle.forward(tab, B, W, bad_idx, off),
+                          oracle.forward(tab, B, W, idx[keep], new_off))
+
+
+# ------------------------------------------------------------------ backward
+def _single_row_problem(D, grad_row, w0, m0=0.0, lr=0.01, eps=1e-8, reps=1, E=3, row=1):
+    tab = oracle.Tables([E], [D])
+    W = np.zeros(E * D, np.float16)
+    W[row * D:(row + 1) * D] = w0
+    m = np.zeros(E, np.float32)
+    m[row] = m0
+    G = np.asarray(grad_row, np.float32).reshape(1, D)
+    idx = np.array([row] * reps, np.int64)
+    off = np.array([0, reps], np.int64)
+    W2, m2 = oracle.backward_rowwise_adagrad(tab, 1, idx, off, G, W, m, lr, eps)
+    return W2.reshape(E, D), m2
+
+
+@pytest.mark.parametrize("c", [0.75, -2.5, 1e-3])
+@pytest.mark.parametrize("eps", [1e-8, 0.5])
+def test_adagrad_constant_gradient_closed_form(oracle_lib, c, eps):
+    # g_d = c for all d, m0 = 0:  m = mean(c^2) = c^2,  w -= lr*c/(|c| + eps)
+    D, lr = 12, 0.01
+    w0 = np.float16(0.125)
+    W2, m2 = _single_row_problem(D, [c] * D, w0, lr=lr, eps=eps)
+    c32 = np.float64(np.float32(c))          # the gradient is stored in fp32
+    assert m2[1] == np.float32(c32 * c32)
+    exp = np.float16(float(w0) - np.float64(np.float32(lr)) * c32 /
+                     (np.sqrt(np.float64(np.float32(c32 * c32))) + np.float64(np.float32(eps))))
+    assert np.all(W2[1] == exp)
+    assert np.all(W2[0] == 0) and np.all(W2[2] == 0) and m2[0] == 0 and m2[2] == 0
+    # eps under the square root would give a different value when eps is large
+    if eps == 0.5 and abs(c) >= 0.5:
+        inside = np.float16(float(w0) - lr * c / np.sqrt(c * c + eps))
+        assert inside != exp
+
+
+def test_adagrad_second_step_accumulates(oracle_lib):
+    # from m0 = c^2 with the same gradient: m = 2c^2, step = lr*c/(sqrt(2)|c| + eps)
+    D, c, lr, eps = 8, 1.5, 0.05, 1e-8
+    W2, m2 = _single_row_problem(D, [c] * D, np.float16(1.0), m0=c * c, lr=lr, eps=eps)
+    assert m2[1] == np.float32(2 * c * c)
+    exp = np.float16(1.0 - lr * c / (np.sqrt(np.float64(np.float32(2 * c * c))) + eps))
+    assert np.all(W2[1] == exp)
+
+
+def test_adagrad_mean_uses_true_width(oracle_lib):
+    # half the entries c, half 0 over D=6: mean(g^2) = c^2/2; zero entries keep w
+    c = 2.0
+    W2, m2 = _single_row_problem(6, [c, c, c, 0, 0, 0], np.float16(0.5), lr=0.1)
+    assert m2[1] == np.float32(c * c / 2)
+    exp = np.float16(0.5 - 0.1 * c / (c / np.sqrt(2.0) + np.float64(np.float32(1e-8))))
+    assert np.all(W2[1, :3] == exp) and np.all(W2[1, 3:] == np.float16(0.5))
+
+
+def test_adagrad_D1_equals_elementwise_hugectr_rule(oracle_lib):
+    # For D = 1 the row mean is the element itself, so row-wise Adagrad equals the
+    # element-wise rule of the HugeCTR Adagrad kernel: acc += g*g; w -= lr*g/(sqrt(acc)+eps).
+    rng = np.random.default_rng(3)
+    lr, eps = 0.05, 1e-3
+    tab = oracle.Tables([4], [1])
+    W = rng.normal(0, 1, 4).astype(np.float16)
+    m = np.zeros(4, np.float32)
+    acc = np.zeros(4, np.float64)
+    w_el = W.astype(np.float64)
+    for step in range(4):
+        idx = rng.integers(0, 4, 6).astype(np.int64)
+        off = np.array([0, 2, 6], np.int64)
+        G = rng.normal(0, 1, (2, 1)).astype(np.float32)
+        W, m = oracle.backward_rowwise_adagrad(tab, 2, idx, off, G, W, m, lr, eps)
+        g = np.zeros(4)
+        for i, r in enumerate(idx):
+            g[r] += G[0 if i < 2 else 1, 0]
+        for r in range(4):
+            if (idx == r).any():
+                acc[r] = np.float32(acc[r] + g[r] * g[r])
+                w_el[r] = np.float16(w_el[r] - lr * g[r] / (np.sqrt(acc[r]) + np.float32(eps)))
+        assert np.array_equal(m.astype(np.float64), acc)
+        assert np.array_equal(W, w_el.astype(np.float16))
+
+
+def test_duplicate_rows_in_a_bag_count_per_occurrence(oracle_lib):
+    # The page's example: a slot "30,20,20,20" updates row 2 with three copies of
+    # the bag gradient and row 3 with one.
+    tab = oracle.Tables([6], [4])
+    G = np.array([[1.0, -2.0, 0.5, 3.0]], np.float32)
+    idx = np.array([3, 2, 2, 2], np.int64)
+    off = np.array([0, 4], np.int64)
+    keys, g = oracle.row_gradients(tab, 1, idx, off, G)
+    assert keys.tolist() == [2, 3]
+    assert np.array_equal(g[0], 3 * G[0].astype(np.float64))
+    assert np.array_equal(g[1], G[0].astype(np.float64))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_row_gradients_brute_force_exact(oracle_lib, seed):
+    tab, B, idx, off, W, G, psw = _tiny_problem(seed + 20, weighted=True, invalid=seed == 1)
+    keys, g = oracle.row_gradients(tab, B, idx, off, G, psw)
+    exp = {}
+    for t, b, i, r in _lookups(tab, B, idx, off):
+        if not 0 <= r < tab.E[t]:
+            continue
+        k = int(tab.hash_base[t]) + r
+        D = int(tab.D[t])
+        row = exp.setdefault(k, [Fraction(0)] * D)
+        for d in range(D):
+            row[d] += Fraction(float(psw[i])) * Fraction(float(G[b, int(tab.D_offsets[t]) + d]))
+    assert keys.tolist() == sorted(exp)
+    for j, k in enumerate(keys):
+        e = np.array([float(x) for x in exp[int(k)]])
+        assert np.allclose(g[j, :len(e)], e, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_backward_invariants(oracle_lib, seed):
+    tab, B, idx, off, W, G, psw = _tiny_problem(seed + 40, weighted=seed % 2 == 0)
+    rng = np.random.default_rng(seed)
+    m0 = rng.uniform(0, 2, int(tab.hash_base[-1])).astype(np.float32)
+    W2, m2 = oracle.backward_rowwise_adagrad(tab, B, idx, off, G, W, m0, 0.01, 1e-8, psw)
+    keys, g = oracle.row_gradients(tab, B, idx, off, G, psw)
+    touched = np.zeros(int(tab.hash_base[-1]), bool)
+    touched[keys] = True
+    # untouched rows: weights and momentum bit-identical
+    for t in range(tab.T):
+        D, E = int(tab.D[t]), int(tab.E[t])
+        for r in range(E):
+            k = int(tab.hash_base[t]) + r
+            sl = slice(int(tab.w_offsets[t]) + r * D, int(tab.w_offsets[t]) + (r + 1) * D)
+            if not touched[k]:
+                assert W2[sl].view(np.uint16).tolist() == W[sl].view(np.uint16).tolist()
+                assert m2[k].view(np.uint32) == m0[k].view(np.uint32)
+    # every touched row updated exactly once: the momentum increment is the mean
+    # square of the row's summed gradient (per-lookup updates would differ)
+    for j, k in enumerate(keys):
+        t = int(np.searchsorted(tab.hash_base, k, side="right") - 1)
+        D = int(tab.D[t])
+        inc = np.mean(g[j, :D] ** 2)
+        assert abs(float(m2[k]) - (float(m0[k]) + inc)) <= 2e-7 * (float(m0[k]) + inc)
+    # gradient mass: summed over runs equals summed over lookups
+    mass_runs = sum(g[j, :int(tab.D[np.searchsorted(tab.hash_base, k, side='right') - 1])].sum()
+                    for j, k in enumerate(keys))
+    mass_lookups = 0.0
+    for t, b, i, r in _lookups(tab, B, idx, off):
+        c = psw[i] if psw is not None else 1.0
+        mass_lookups += float(c) * float(
+            G[b, int(tab.D_offsets[t]):int(tab.D_offsets[t + 1])].astype(np.float64).sum())
+    assert abs(mass_runs - mass_lookups) <= 1e-9 * max(1.0, abs(mass_lookups))
+
+
+def test_backward_selected_agrees_with_full(oracle_lib):
+    tab, B, idx, off, W, G, psw = _tiny_problem(77, weighted=True)
+    m0 = np.linspace(0, 1, int(tab.hash_base[-1])).astype(np.float32)
+    W2, m2 = oracle.backward_rowwise_adagrad(tab, B, idx, off, G, W, m0, 0.02, 1e-6, psw)
+    maxD = int(tab.D.max())
+    sel = np.arange(int(tab.hash_base[-1]), dtype=np.uint32)
+    w_rows = np.zeros((len(sel), maxD), np.float16)
+    for k in sel:
+        t = int(np.searchsorted(tab.hash_base, k, side="right") - 1)
+        D = int(tab.D[t]); r = int(k) - int(tab.hash_base[t])
+        w_rows[k, :D] = W[tab.w_offsets[t] + r * D: tab.w_offsets[t] + (r + 1) * D]
+    ws, ms, cnt = oracle.backward_selected(tab, B, idx, off, G, 0.02, 1e-6, sel, w_rows, m0[sel],
+                                           psw)
+    assert np.array_equal(ms.view(np.uint32), m2[sel].view(np.uint32))
+    for k in sel:
+        t = int(np.searchsorted(tab.hash_base, k, side="right") - 1)
+        D = int(tab.D[t]); r = int(k) - int(tab.hash_base[t])
+        assert np.array_equal(ws[k, :D].view(np.uint16),
+                              W2[tab.w_offsets[t] + r * D: tab.w_offsets[t] + (r + 1) * D]
+                              .view(np.uint16))
+    assert int(cnt.sum()) == len(idx)
+
+
+def test_repair_offsets_examples(oracle_lib):
+    # first entry forced to 0, entries clamped to [0, n], then made non-decreasing
+    got, changed = oracle.repair_offsets(np.array([3, 5, 3, 12, 8], np.int64), 10)
+    assert got.tolist() == [0, 5, 5, 10, 10] and changed == 4
+    got, changed = oracle.repair_offsets(np.array([0, -4, 2, 2, 9], np.int32), 9)
+    assert got.tolist() == [0, 0, 2, 2, 9] and changed == 1
+    ok = np.array([0, 1, 1, 4], np.int64)
+    got, changed = oracle.repair_offsets(ok, 4)
+    assert got.tolist() == ok.tolist() and changed == 0
+
+
+def test_oracle_rejects_bad_offsets(oracle_lib):
+    tab = oracle.Tables([4], [8])
+    with pytest.raises(ValueError):
+        oracle.forward(tab, 2, np.zeros(32, np.float16), np.zeros(3, np.int64),
+                       np.array([0, 2, 1], np.int64))
