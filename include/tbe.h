@@ -1,0 +1,199 @@
+/*
+ * tbe.h -- C ABI of the GB300 (sm_103a) Table Batched Embedding library.
+ *
+ * Table Batched Embedding (TBE) pools lookups from many embedding tables in
+ * one launch and trains them with a backward that regroups lookups by row and
+ * applies exactly one exact row-wise Adagrad update per touched row.
+ *
+ * Sources (page titles and sections):
+ *  - "Modernizing Table Batched Embeddings with FBTriton", sections
+ *    "Why redesign a sparse operator?" (what TBE combines), "Forward: keep a
+ *    narrowly specialized path beside the general one" (generic gather-pool,
+ *    fp32 accumulation of fp16 weights, int32 index option, small-table
+ *    histogram path and its eligibility, bounds checks off by default),
+ *    "Backward: invert 'which rows did this sample use?'" (transpose, sort,
+ *    run-length encoding into runs, short/long runs, fenced last-chunk
+ *    update), "Fewer reads and synchronizations can beat more parallel work"
+ *    (device-resident counts, no read-back), "Fusion boundaries are also
+ *    engineering interfaces" (per-sample weights scale each contribution
+ *    before grouping; the optimizer is the backward's epilogue).
+ *  - "HugeCTR DistributedSlotSparseEmbeddingHash backward" (eqicode.com):
+ *    CSR bags (row_offset / value), the sample-id expansion, radix sort by
+ *    row with end_bit, run flags + prefix sum + run starts with a sentinel,
+ *    and the Adagrad accumulator-then-weight order with eps outside the root.
+ *
+ * Data layout (all device buffers are owned by the caller):
+ *  - T tables; table t has E_t rows of width D_t (D_t a multiple of 8, at
+ *    most 1024).  Weights are fp16, one flat buffer; table t starts at element
+ *    weights_offsets[t], its rows are contiguous with stride D_t.
+ *  - Momentum: fp32 [sum E_t], one value per row, row r of table t at
+ *    hash_base[t] + r.
+ *  - Bags are table-major: bag (t,b) has id t*B+b.  offsets: [T*B+1] of the
+ *    index type, indices: [n], lookups of bag (t,b) at positions
+ *    offsets[t*B+b] .. offsets[t*B+b+1]-1.  A lookup's row must lie in
+ *    [0, E_t); any other value is skipped (contributes nothing), whether or
+ *    not checks are enabled.
+ *  - Pooled output and its gradient: fp32 row-major [B, sum D_t]; table t's
+ *    pooled vector for bag b is at columns D_offsets[t] .. D_offsets[t+1]-1.
+ *  - Optional per-sample weights: fp32 [n].
+ *
+ * Ordering and synchronisation: every call only enqueues work on the given
+ * stream (a cudaStream_t passed as void*; NULL = legacy default stream) and
+ * returns.  No call allocates device memory and no call on the hot path
+ * synchronises with the host; tbe_read_status is the one explicit sync.
+ *
+ * Errors: argument problems are reported synchronously through tbe_status
+ * before anything is enqueued.  Data problems found on the device (indices
+ * out of range, malformed offsets) set bits in a status word that lives in
+ * the workspace; tbe_read_status copies it to the host.
+ */
+#ifndef TBE_H_
+#define TBE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tbe_status {
+  TBE_OK = 0,
+  TBE_EINVAL = 1,       /* null pointer, negative size, dtype mismatch */
+  TBE_EWORKSPACE = 2,   /* workspace null or smaller than tbe_workspace_size */
+  TBE_EUNSUPPORTED = 3, /* well-formed but outside what the kernels cover */
+  TBE_ECUDA = 4         /* a CUDA call or launch returned an error */
+} tbe_status;
+
+/* element types */
+enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3 };
+
+/* call flags */
+#define TBE_F_CHECK_BOUNDS (1u << 0)    /* validate offsets (separate kernel) and indices,
+                                           report problems in the status word */
+#define TBE_F_REPAIR_OFFSETS (1u << 1)  /* also repair offsets into a workspace copy:
+                                           o'[0]=0, o'[i]=max(o'[i-1], clamp(o[i],0,n)) */
+#define TBE_F_FORCE_GENERIC (1u << 2)   /* forward: never take the small-table path */
+#define TBE_F_LONG_TWO_LAUNCH (1u << 3) /* backward: long runs write partial sums and a
+                                           second kernel applies the update (instead of
+                                           the fenced last-arriver update) */
+#define TBE_F_PREPROCESSED (1u << 4)    /* backward: the workspace already holds the
+                                           sorted runs of these indices/offsets from
+                                           tbe_preprocess on the same stream */
+
+/* workspace-size flags */
+#define TBE_WS_WEIGHTED (1u << 0)       /* reserve room for per-sample weights */
+
+/* device status bits (tbe_read_status) */
+#define TBE_ERR_INDEX_RANGE (1 << 0)    /* a lookup's row was outside [0, E_t) */
+#define TBE_ERR_OFFSETS (1 << 1)        /* offsets not 0 = o[0] <= ... <= o[T*B] <= n */
+
+/* Problem description.  The three int64 arrays are device pointers with T+1
+ * entries each (cumulative sums starting at 0); the scalar totals are their
+ * last entries, repeated here so that the host never reads device memory. */
+typedef struct tbe_desc {
+  int32_t T;                        /* number of tables, >= 1 */
+  int32_t B;                        /* bags per table (batch size), >= 1 */
+  int32_t weights_dtype;            /* TBE_DT_F16 */
+  int32_t index_dtype;              /* TBE_DT_I32 or TBE_DT_I64; offsets use it too */
+  const int64_t* D_offsets;         /* device [T+1]: sum of D_t' for t' < t */
+  const int64_t* hash_base;         /* device [T+1]: sum of E_t' for t' < t */
+  const int64_t* weights_offsets;   /* device [T+1]: sum of E_t' * D_t' for t' < t */
+  int64_t total_D;                  /* D_offsets[T] */
+  int64_t total_E;                  /* hash_base[T]; must be < 2^32 - 1 */
+  int32_t max_D;                    /* max_t D_t */
+  int32_t min_D;                    /* min_t D_t */
+} tbe_desc;
+
+/* Device pointers into a workspace after tbe_preprocess, for inspection.
+ * Counts marked (device) live in device memory and are never read back by the
+ * library. */
+typedef struct tbe_ws_view {
+  const uint32_t* sorted_keys;  /* [n] linear keys hash_base[t]+row, ascending; invalid
+                                   lookups carry key total_E and sort last */
+  const uint32_t* sorted_bags;  /* [n] bag b (within its table) of each sorted lookup */
+  const float* sorted_psw;      /* [n] per-sample weight of each sorted lookup, or NULL */
+  const uint32_t* unique_keys;  /* [R] key of each run */
+  const uint32_t* run_starts;   /* [R+1] first sorted position of each run; [R] = n_valid */
+  const uint32_t* counts;       /* (device) [0] R runs, [1] n_valid lookups,
+                                   [2] long runs, [3] long-run chunks */
+  const uint32_t* long_runs;    /* [counts[2]] run id of each long run (SL >= long_threshold) */
+  int32_t long_threshold;       /* run length from which a run takes the chunked path */
+  int32_t chunk;                /* lookups per chunk on the chunked path */
+} tbe_ws_view;
+
+/* Bytes of workspace needed for calls with at most n_max lookups.
+ * ws_flags: TBE_WS_WEIGHTED if per-sample weights will be passed.
+ * The caller allocates the workspace (16-byte aligned) and zero-fills it once
+ * before its first use; the library keeps the status word at its start and
+ * overwrites everything else on every call that needs it.
+ * Errors: TBE_EINVAL (null desc/bytes, n_max < 0), TBE_EUNSUPPORTED
+ * (n_max >= 2^32 or total_E >= 2^32 - 1). */
+tbe_status tbe_workspace_size(const tbe_desc* d, int64_t n_max, uint32_t ws_flags,
+                              size_t* bytes);
+
+/* Pooled forward ("Forward: keep a narrowly specialized path beside the
+ * general one"):
+ *   out[b, D_offsets[t] + c] = sum over lookups i of bag (t,b) with a valid row
+ *                              of psw_i * W_t[indices[i], c]   (psw_i = 1 if NULL)
+ * accumulated in fp32.  An empty bag yields zeros.  One table with E <= 64,
+ * 64 <= D <= 128, no per-sample weights and an average bag length >= 64 takes
+ * the tensor-core histogram path (counts per bag times the table) unless
+ * TBE_F_FORCE_GENERIC; every other problem takes the generic gather-pool.
+ * weights: fp16 device; indices/offsets: device, index_dtype; n: lookups
+ * (length of indices); per_sample_weights: fp32 device [n] or NULL;
+ * out: fp32 device [B, total_D], fully overwritten.  Workspace: the status
+ * word plus (TBE_F_REPAIR_OFFSETS) the repaired offsets; ws_bytes must be at
+ * least tbe_workspace_size(d, n, ...).
+ * Errors: TBE_EINVAL, TBE_EWORKSPACE, TBE_EUNSUPPORTED (dtype, D_t), TBE_ECUDA. */
+tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indices,
+                       const void* offsets, int64_t n, const float* per_sample_weights,
+                       float* out, void* workspace, size_t ws_bytes, void* stream,
+                       uint32_t flags);
+
+/* Backward preprocessing only ("Backward: invert ..." and the HugeCTR steps
+ * 1-4): expand every lookup to (key = hash_base[t] + row, bag b, psw), radix
+ * sort by key (stable, int32 keys), run-length encode into runs, and classify
+ * runs into short and long with the long-run task list compacted on the
+ * device.  Results stay in the workspace (see tbe_workspace_view); a later
+ * tbe_backward_rowwise_adagrad with TBE_F_PREPROCESSED consumes them.
+ * Errors as tbe_forward. */
+tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* offsets, int64_t n,
+                          const float* per_sample_weights, void* workspace, size_t ws_bytes,
+                          void* stream, uint32_t flags);
+
+/* Backward with exact row-wise Adagrad ("Backward: invert ...", "Fusion
+ * boundaries ...", the HugeCTR Adagrad kernel in row-wise form).  For every
+ * touched row r of table t, with the run of its lookups i:
+ *   g_c   = sum_i psw_i * grad_out[b_i, D_offsets[t] + c]        (fp32)
+ *   m_r  <- m_r + (1/D_t) * sum_c g_c^2
+ *   W_t[r, c] <- fp16_rn(W_t[r, c] - lr * g_c / (sqrt(m_r) + eps))
+ * exactly once per touched row; untouched rows are not written.
+ * grad_out: fp32 device [B, total_D]; weights (fp16) and momentum (fp32
+ * [total_E]) are updated in place.  Without TBE_F_PREPROCESSED the call runs
+ * tbe_preprocess first.  No host synchronisation, no device-to-host copy.
+ * Errors as tbe_forward. */
+tbe_status tbe_backward_rowwise_adagrad(const tbe_desc* d, const float* grad_out,
+                                        const void* indices, const void* offsets, int64_t n,
+                                        const float* per_sample_weights, void* weights,
+                                        float* momentum, float lr, float eps, void* workspace,
+                                        size_t ws_bytes, void* stream, uint32_t flags);
+
+/* Fill *view with device pointers into a workspace sized for n lookups.
+ * Errors: TBE_EINVAL. */
+tbe_status tbe_workspace_view(const tbe_desc* d, int64_t n, uint32_t ws_flags, void* workspace,
+                              tbe_ws_view* view);
+
+/* Copy the device status word to *status_bits (a TBE_ERR_* mask) and clear it.
+ * Synchronises the stream: never call it inside a timed or captured region.
+ * Errors: TBE_EINVAL, TBE_ECUDA. */
+tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits);
+
+/* Library build identification: a static string. */
+const char* tbe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TBE_H_ */

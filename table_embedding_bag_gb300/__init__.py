@@ -1,0 +1,243 @@
+"""Thin Python binding of libtbe.so, the GB300 Table Batched Embedding library.
+
+Every function here only marshals arguments (device pointers from torch
+tensors, the current CUDA stream) into the C ABI declared in include/tbe.h;
+every step of the computation runs in the library's CUDA kernels.  There is
+no CPU fallback: if libtbe.so is missing or fails to load, the functions
+raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import _build
+
+__all__ = [
+    "build", "TBEDesc", "Workspace", "TBEError", "tbe_workspace_size", "tbe_forward",
+    "tbe_preprocess", "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status",
+    "tbe_version", "TableBatchedEmbedding", "lib_path",
+    "TBE_F_CHECK_BOUNDS", "TBE_F_REPAIR_OFFSETS", "TBE_F_FORCE_GENERIC", "TBE_F_LONG_TWO_LAUNCH",
+    "TBE_F_PREPROCESSED", "TBE_WS_WEIGHTED", "TBE_ERR_INDEX_RANGE", "TBE_ERR_OFFSETS",
+]
+
+TBE_OK, TBE_EINVAL, TBE_EWORKSPACE, TBE_EUNSUPPORTED, TBE_ECUDA = range(5)
+TBE_DT_F16, TBE_DT_I32, TBE_DT_I64 = 1, 2, 3
+TBE_F_CHECK_BOUNDS = 1 << 0
+TBE_F_REPAIR_OFFSETS = 1 << 1
+TBE_F_FORCE_GENERIC = 1 << 2
+TBE_F_LONG_TWO_LAUNCH = 1 << 3
+TBE_F_PREPROCESSED = 1 << 4
+TBE_WS_WEIGHTED = 1 << 0
+TBE_ERR_INDEX_RANGE = 1 << 0
+TBE_ERR_OFFSETS = 1 << 1
+_STATUS_NAMES = {1: "TBE_EINVAL", 2: "TBE_EWORKSPACE", 3: "TBE_EUNSUPPORTED", 4: "TBE_ECUDA"}
+
+lib_path = _build.LIB
+build = _build.build
+
+
+class TBEError(RuntimeError):
+    def __init__(self, call, code):
+        super().__init__(f"{call} failed: {_STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+class tbe_desc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("B", ctypes.c_int32),
+                ("weights_dtype", ctypes.c_int32), ("index_dtype", ctypes.c_int32),
+                ("D_offsets", ctypes.c_void_p), ("hash_base", ctypes.c_void_p),
+                ("weights_offsets", ctypes.c_void_p), ("total_D", ctypes.c_int64),
+                ("total_E", ctypes.c_int64), ("max_D", ctypes.c_int32),
+                ("min_D", ctypes.c_int32)]
+
+
+class tbe_ws_view(ctypes.Structure):
+    _fields_ = [("sorted_keys", ctypes.c_void_p), ("sorted_bags", ctypes.c_void_p),
+                ("sorted_psw", ctypes.c_void_p), ("unique_keys", ctypes.c_void_p),
+                ("run_starts", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("long_runs", ctypes.c_void_p), ("long_threshold", ctypes.c_int32),
+                ("chunk", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(lib_path):
+            raise RuntimeError(f"{lib_path} is not built; run table_embedding_bag_gb300.build()")
+        lib = ctypes.CDLL(lib_path)
+        P, i64, u32, f32, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint32,
+                                ctypes.c_float, ctypes.c_size_t)
+        D = ctypes.POINTER(tbe_desc)
+        lib.tbe_workspace_size.argtypes = [D, i64, u32, ctypes.POINTER(sz)]
+        lib.tbe_forward.argtypes = [D, P, P, P, i64, P, P, P, sz, P, u32]
+        lib.tbe_preprocess.argtypes = [D, P, P, i64, P, P, sz, P, u32]
+        lib.tbe_backward_rowwise_adagrad.argtypes = [D, P, P, P, i64, P, P, P, f32, f32, P, sz, P,
+                                                     u32]
+        lib.tbe_workspace_view.argtypes = [D, i64, u32, P, ctypes.POINTER(tbe_ws_view)]
+        lib.tbe_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+        lib.tbe_version.restype = ctypes.c_char_p
+        for f in ("tbe_workspace_size", "tbe_forward", "tbe_preprocess",
+                  "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ok(call, code):
+    if code != TBE_OK:
+        raise TBEError(call, code)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class TBEDesc:
+    """Problem description: per-table rows E_t and widths D_t, bags per table B,
+    index dtype.  Holds the three cumulative int64 arrays on the device."""
+
+    def __init__(self, E, D, B, index_dtype=torch.int64, device="cuda"):
+        self.E = np.asarray(E, dtype=np.int64)
+        self.D = np.asarray(D, dtype=np.int64)
+        if self.E.ndim != 1 or self.E.shape != self.D.shape or len(self.E) == 0:
+            raise ValueError("E and D must be equal-length 1-d sequences")
+        if np.any(self.D % 8) or np.any(self.D < 8) or np.any(self.D > 1024):
+            raise ValueError("every D_t must be a multiple of 8 in [8, 1024]")
+        self.T, self.B = len(self.E), int(B)
+        self.index_dtype = index_dtype
+        cum = lambda a: np.concatenate([[0], np.cumsum(a)]).astype(np.int64)
+        self.D_offsets_h = cum(self.D)
+        self.hash_base_h = cum(self.E)
+        self.weights_offsets_h = cum(self.E * self.D)
+        dev = torch.device(device)
+        self.D_offsets = torch.from_numpy(self.D_offsets_h).to(dev)
+        self.hash_base = torch.from_numpy(self.hash_base_h).to(dev)
+        self.weights_offsets = torch.from_numpy(self.weights_offsets_h).to(dev)
+        self.total_D = int(self.D_offsets_h[-1])
+        self.total_E = int(self.hash_base_h[-1])
+        self.num_weights = int(self.weights_offsets_h[-1])
+        self.c = tbe_desc(self.T, self.B, TBE_DT_F16,
+                          TBE_DT_I32 if index_dtype == torch.int32 else TBE_DT_I64,
+                          self.D_offsets.data_ptr(), self.hash_base.data_ptr(),
+                          self.weights_offsets.data_ptr(), self.total_D, self.total_E,
+                          int(self.D.max()), int(self.D.min()))
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def tbe_workspace_size(desc: TBEDesc, n_max: int, weighted: bool = False) -> int:
+    out = ctypes.c_size_t(0)
+    _ok("tbe_workspace_size", _load().tbe_workspace_size(
+        desc.ref, int(n_max), TBE_WS_WEIGHTED if weighted else 0, ctypes.byref(out)))
+    return out.value
+
+
+class Workspace:
+    """Device workspace for calls with at most n_max lookups."""
+
+    def __init__(self, desc: TBEDesc, n_max: int, weighted: bool = False, device="cuda"):
+        self.nbytes = tbe_workspace_size(desc, n_max, weighted)
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
+        self.weighted = weighted
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+
+def _check_tensors(desc, indices, offsets):
+    if indices.dtype != desc.index_dtype or offsets.dtype != desc.index_dtype:
+        raise TypeError(f"indices and offsets must be {desc.index_dtype}")
+    if offsets.numel() != desc.T * desc.B + 1:
+        raise ValueError("offsets must have T*B+1 entries")
+    if not (indices.is_contiguous() and offsets.is_contiguous()):
+        raise ValueError("indices and offsets must be contiguous")
+
+
+def tbe_forward(desc: TBEDesc, weights, indices, offsets, per_sample_weights, out, ws: Workspace,
+                flags: int = 0, stream=None):
+    """Pooled forward into out (fp32 [B, sum D]); see tbe_forward in include/tbe.h."""
+    _check_tensors(desc, indices, offsets)
+    _ok("tbe_forward", _load().tbe_forward(
+        desc.ref, _ptr(weights), _ptr(indices), _ptr(offsets), indices.numel(),
+        _ptr(per_sample_weights), _ptr(out), ws.ptr, ws.nbytes, _stream(stream), flags))
+    return out
+
+
+def tbe_preprocess(desc: TBEDesc, indices, offsets, per_sample_weights, ws: Workspace,
+                   flags: int = 0, stream=None):
+    _check_tensors(desc, indices, offsets)
+    _ok("tbe_preprocess", _load().tbe_preprocess(
+        desc.ref, _ptr(indices), _ptr(offsets), indices.numel(), _ptr(per_sample_weights),
+        ws.ptr, ws.nbytes, _stream(stream), flags))
+
+
+def tbe_backward_rowwise_adagrad(desc: TBEDesc, grad_out, indices, offsets, per_sample_weights,
+                                 weights, momentum, lr, eps, ws: Workspace, flags: int = 0,
+                                 stream=None):
+    """Backward with one exact row-wise Adagrad update per touched row, in place
+    on weights and momentum; see include/tbe.h."""
+    _check_tensors(desc, indices, offsets)
+    _ok("tbe_backward_rowwise_adagrad", _load().tbe_backward_rowwise_adagrad(
+        desc.ref, _ptr(grad_out), _ptr(indices), _ptr(offsets), indices.numel(),
+        _ptr(per_sample_weights), _ptr(weights), _ptr(momentum), float(lr), float(eps), ws.ptr,
+        ws.nbytes, _stream(stream), flags))
+
+
+def tbe_workspace_view(desc: TBEDesc, n: int, ws: Workspace) -> dict:
+    """Device pointers into the workspace (sorted keys, runs, ...) as ints."""
+    v = tbe_ws_view()
+    _ok("tbe_workspace_view", _load().tbe_workspace_view(
+        desc.ref, int(n), TBE_WS_WEIGHTED if ws.weighted else 0, ws.ptr, ctypes.byref(v)))
+    return {name: getattr(v, name) for name, _ in tbe_ws_view._fields_}
+
+
+def tbe_read_status(ws: Workspace, stream=None) -> int:
+    """Read and clear the device status word (synchronises the stream)."""
+    v = ctypes.c_int32(0)
+    _ok("tbe_read_status", _load().tbe_read_status(ws.ptr, _stream(stream), ctypes.byref(v)))
+    return v.value
+
+
+def tbe_version() -> str:
+    return _load().tbe_version().decode()
+
+
+class TableBatchedEmbedding:
+    """Owns fp16 weights, fp32 row-wise momentum and a workspace for one
+    problem shape; forward() and backward() call the C ABI."""
+
+    def __init__(self, E, D, B, n_max, index_dtype=torch.int64, weighted=False, weights=None,
+                 momentum=None, lr=0.01, eps=1e-8, device="cuda"):
+        self.desc = TBEDesc(E, D, B, index_dtype, device)
+        self.ws = Workspace(self.desc, n_max, weighted, device)
+        self.weights = weights if weights is not None else torch.zeros(
+            self.desc.num_weights, dtype=torch.float16, device=device)
+        self.momentum = momentum if momentum is not None else torch.zeros(
+            self.desc.total_E, dtype=torch.float32, device=device)
+        self.lr, self.eps = lr, eps
+        self.out = torch.empty(self.desc.B, self.desc.total_D, dtype=torch.float32, device=device)
+
+    def forward(self, indices, offsets, per_sample_weights=None, flags=0):
+        return tbe_forward(self.desc, self.weights, indices, offsets, per_sample_weights,
+                           self.out, self.ws, flags)
+
+    def backward(self, grad_out, indices, offsets, per_sample_weights=None, flags=0):
+        tbe_backward_rowwise_adagrad(self.desc, grad_out, indices, offsets, per_sample_weights,
+                                     self.weights, self.momentum, self.lr, self.eps, self.ws,
+                                     flags)

@@ -1,0 +1,179 @@
+// Internal helpers shared by the CUDA translation units of the TBE library.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "tbe.h"
+
+namespace tbe {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Lookup threshold from which a run takes the chunked (cooperative) path and
+// the number of lookups per chunk.  The FBTriton backward uses 256 for both;
+// they stay equal here, so a long run always has at least one full chunk.
+constexpr int kLongThreshold = 256;
+constexpr int kChunk = 256;
+// Fan-in of the last-arriver reduction tree over a long run's chunk partials.
+constexpr int kFanIn = 32;
+// Widest supported table row (elements); rows are moved in 16-byte vectors.
+constexpr int kMaxD = 1024;
+
+// Radix sort: threads per CTA, keys per thread, digit width bound.
+constexpr int kSortThreads = 256;
+constexpr int kSortItems = 16;
+constexpr int kSortTile = kSortThreads * kSortItems;
+constexpr int kMaxRadixBits = 9;
+constexpr int kMaxSortCtas = 1024;
+
+// Workspace header: status word and device-resident counters.
+enum Counter : int {
+  kCntRuns = 0,      // R: runs with a valid key
+  kCntValid = 1,     // n_valid: sorted lookups with a valid key
+  kCntLong = 2,      // long runs
+  kCntChunks = 3,    // chunks of long runs
+  kCntTree = 4,      // internal reduction-tree nodes
+  kCntTasks = 5,     // short-run warp tasks
+  kNumCounters = 8,
+};
+
+struct WsLayout {
+  size_t status;       // int32 status word
+  size_t counts;       // uint32 [kNumCounters]
+  size_t table_runs;   // uint32 [T+1] first run of each table
+  size_t table_tasks;  // uint32 [T+1] prefix of short-run warp tasks per table
+  size_t keys[2];      // uint32 [n]
+  size_t vals[2];      // uint32 [n]
+  size_t psw[2];       // float [n] (weighted only)
+  size_t radix_counts; // uint32 [2^kMaxRadixBits * kMaxSortCtas]
+  size_t cta_counts;   // uint32 [kMaxSortCtas + 1]
+  size_t unique_keys;  // uint32 [n + 1]
+  size_t run_starts;   // uint32 [n + 2]
+  size_t long_run;     // uint32 [max_long]
+  size_t long_chunk0;  // uint32 [max_long] first chunk of each long run
+  size_t long_tree0;   // uint32 [max_long] first tree node of each long run
+  size_t chunk_task;   // uint32 [max_chunks] long run of each chunk
+  size_t tree_cnt;     // uint32 [max_tree] arrivals still expected at each tree node
+  size_t partials;     // float [max_chunks * max_D]
+  size_t tree_part;    // float [max_tree * max_D]
+  size_t offsets_fix;  // index type [T*B+1] repaired offsets
+  size_t fix_scratch;  // int64 [blocks] block maxima for the repair scan
+  size_t total;
+  int64_t max_long, max_chunks, max_tree;
+  bool weighted;
+};
+
+// Number of reduction-tree nodes above nch leaves (the root included when
+// nch > 1): levels ceil(nch/F), ceil(ceil(nch/F)/F), ... down to 1.
+__host__ __device__ inline int64_t tree_nodes(int64_t nch) {
+  int64_t total = 0;
+  while (nch > 1) {
+    nch = (nch + kFanIn - 1) / kFanIn;
+    total += nch;
+  }
+  return total;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags);
+
+inline int index_bytes(const tbe_desc* d) { return d->index_dtype == TBE_DT_I32 ? 4 : 8; }
+
+// ------------------------------------------------------------ device helpers
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ void set_status(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+template <typename IndexT>
+__device__ __forceinline__ int64_t load_index(const IndexT* p, int64_t i) {
+  return static_cast<int64_t>(__ldg(p + i));
+}
+
+// Offsets of bag `bag` clamped into [0, n] with end >= start, so that no
+// lookup outside indices[0, n) is ever touched whatever the offsets hold.
+template <typename IndexT>
+__device__ __forceinline__ void bag_range(const IndexT* offsets, int64_t bag, int64_t n,
+                                          int64_t* start, int64_t* end) {
+  int64_t s = load_index(offsets, bag);
+  int64_t e = load_index(offsets, bag + 1);
+  s = s < 0 ? 0 : (s > n ? n : s);
+  e = e < s ? s : (e > n ? n : e);
+  *start = s;
+  *end = e;
+}
+
+// Eight fp16 values packed in a uint4 -> fp32, scaled and accumulated.
+__device__ __forceinline__ void acc_half8(float* acc, uint4 v, float w) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __half22float2(h[i]);
+    acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+    acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+  }
+}
+
+__device__ __forceinline__ uint4 ldg_u4(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ float4 ldg_f4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+}  // namespace tbe
+
+namespace tbe {
+
+// ------------------------------------------------------------------- scans
+struct OpSum {
+  template <typename T>
+  __device__ __forceinline__ T operator()(T a, T b) const { return a + b; }
+};
+struct OpMax {
+  template <typename T>
+  __device__ __forceinline__ T operator()(T a, T b) const { return a > b ? a : b; }
+};
+
+template <typename T, typename Op>
+__device__ __forceinline__ T warp_inclusive_scan(T v, Op op) {
+  const unsigned lane = lane_id();
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T y = __shfl_up_sync(kFull, v, o);
+    if (lane >= static_cast<unsigned>(o)) v = op(v, y);
+  }
+  return v;
+}
+
+// Inclusive scan over the CTA (blockDim.x a multiple of 32, at most 1024).
+// smem must hold 33 elements.  *total receives the CTA aggregate.  Contains
+// __syncthreads; every thread of the CTA must call it.
+template <typename T, typename Op>
+__device__ T block_inclusive_scan(T v, Op op, T identity, T* smem, T* total = nullptr) {
+  const unsigned lane = lane_id();
+  const unsigned warp = threadIdx.x >> 5;
+  const unsigned nwarps = blockDim.x >> 5;
+  v = warp_inclusive_scan(v, op);
+  if (lane == 31) smem[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    T w = lane < nwarps ? smem[lane] : identity;
+    w = warp_inclusive_scan(w, op);
+    smem[lane] = w;  // inclusive per-warp prefix
+  }
+  __syncthreads();
+  if (warp > 0) v = op(smem[warp - 1], v);
+  if (total) *total = smem[nwarps - 1];
+  __syncthreads();
+  return v;
+}
+
+}  // namespace tbe

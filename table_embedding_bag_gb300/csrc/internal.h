@@ -1,0 +1,45 @@
+// Host-side interfaces between the translation units of the TBE library.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tbe.h"
+
+namespace tbe {
+
+struct WsLayout;
+
+// One call's launch context.
+struct Launch {
+  const tbe_desc* d;
+  int64_t n;           // lookups
+  cudaStream_t s;
+  int num_sms;
+};
+
+// forward.cu
+cudaError_t launch_forward_generic(const Launch& L, const void* weights, const void* indices,
+                                   const void* offsets, const float* psw, float* out,
+                                   int* status);
+cudaError_t launch_check_offsets(const Launch& L, const void* offsets, bool repair, void* fixed,
+                                 int64_t* scratch, int* status);
+int64_t repair_scratch_blocks(int64_t nb1);
+
+// forward_small.cu: tensor-core histogram path for one small table.
+bool small_table_eligible(const tbe_desc* d, int64_t n, bool weighted);
+cudaError_t launch_forward_small(const Launch& L, const void* weights, const void* indices,
+                                 const void* offsets, float* out, int* status);
+
+// preprocess.cu: expand, radix sort, run-length encode, classify.
+cudaError_t launch_preprocess(const Launch& L, const WsLayout& W, char* ws, const void* indices,
+                              const void* offsets, const float* psw, bool check);
+// Sorted arrays end up in buffer (passes % 2); the layout needs to know which.
+int radix_passes(const tbe_desc* d);
+
+// update.cu: short-run and long-run row-wise Adagrad.
+cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const float* grad_out,
+                          void* weights, float* momentum, float lr, float eps, bool two_launch);
+
+}  // namespace tbe

@@ -1,0 +1,556 @@
+// Backward preprocessing: expand, radix sort, run-length encode, classify.
+//
+// "Modernizing Table Batched Embeddings with FBTriton", section "Backward:
+// invert 'which rows did this sample use?'": transposition, sorting and
+// run-length encoding turn the bags' lookups into runs, one per unique
+// (table,row), listing the samples that touched it; section "Fewer reads and
+// synchronizations can beat more parallel work": the number of long runs is
+// known only on the device, so task lists are compacted on the GPU and later
+// kernels read the counts from device memory (never copied to the host).
+// "HugeCTR DistributedSlotSparseEmbeddingHash backward" (eqicode.com),
+// steps 1-4: expand each lookup's sample id, radix-sort (row, sample) pairs
+// over only the bits the row range needs (end_bit), flag run starts, prefix-
+// sum the flags and scatter run starts with a sentinel entry.
+//
+// GB300 design:
+//  * keys are 32-bit linear keys hash_base[t] + row (the index range of every
+//    supported problem is below 2^32); values are the bag b within its table;
+//    per-sample weights ride along as a second value.
+//  * LSD radix sort over ceil(log2(total_E+1)) bits in passes of at most 9
+//    bits.  Each pass is reduce-then-scan over persistent CTAs that own
+//    contiguous tile ranges: a digit histogram per CTA, one scan, then a
+//    downsweep that ranks every 4096-key tile stably in shared memory
+//    (warp match + per-warp digit counters) and writes each digit's keys as
+//    one contiguous segment, so global stores stay coalesced.
+//  * invalid lookups get the key total_E and sort after every valid key.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tbe {
+namespace {
+
+constexpr int kRleThreads = 256;
+constexpr int kRleItems = 4;
+constexpr int kRleTile = kRleThreads * kRleItems;
+
+// ------------------------------------------------------------------ expand
+template <typename IndexT, bool kWeighted>
+__global__ void __launch_bounds__(256)
+    expand_kernel(const IndexT* __restrict__ indices, const IndexT* __restrict__ offsets,
+                  const float* __restrict__ psw, const int64_t* __restrict__ hash_base, int64_t n,
+                  int T, int B, uint32_t sentinel, uint32_t* __restrict__ keys,
+                  uint32_t* __restrict__ vals, float* __restrict__ psw_out, int* status) {
+  const int warps = blockDim.x >> 5;
+  const int64_t nbags = static_cast<int64_t>(T) * B;
+  const unsigned lane = lane_id();
+  bool bad = false;
+  for (int64_t bag = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5); bag < nbags;
+       bag += static_cast<int64_t>(gridDim.x) * warps) {
+    const int t = static_cast<int>(bag / B);
+    const uint32_t b = static_cast<uint32_t>(bag - static_cast<int64_t>(t) * B);
+    const int64_t h0 = __ldg(hash_base + t);
+    const int64_t E = __ldg(hash_base + t + 1) - h0;
+    int64_t s, e;
+    bag_range(offsets, bag, n, &s, &e);
+    for (int64_t i = s + lane; i < e; i += 32) {
+      const int64_t r = load_index(indices, i);
+      const bool ok = r >= 0 && r < E;
+      bad |= !ok;
+      keys[i] = ok ? static_cast<uint32_t>(h0 + r) : sentinel;
+      vals[i] = b;
+      if (kWeighted) psw_out[i] = __ldg(psw + i);
+    }
+  }
+  if (status && __any_sync(kFull, bad) && lane == 0) set_status(status, TBE_ERR_INDEX_RANGE);
+}
+
+// Lookups after the last bag (positions offsets[T*B] .. n-1) belong to no bag.
+template <typename IndexT>
+__global__ void fill_tail_kernel(const IndexT* __restrict__ offsets, int64_t nb, int64_t n,
+                                 uint32_t sentinel, uint32_t* __restrict__ keys,
+                                 uint32_t* __restrict__ vals, float* __restrict__ psw_out) {
+  int64_t o = load_index(offsets, nb);
+  o = o < 0 ? 0 : (o > n ? n : o);
+  for (int64_t i = o + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    keys[i] = sentinel;
+    vals[i] = 0;
+    if (psw_out) psw_out[i] = 0.f;
+  }
+}
+
+// -------------------------------------------------------------- radix sort
+struct SortGeom {
+  int ctas;           // persistent CTAs
+  int64_t tiles;      // kSortTile-key tiles
+  int64_t per_cta;    // tiles per CTA
+};
+
+__device__ __forceinline__ void cta_range(const SortGeom& g, int64_t n, int64_t* b, int64_t* e) {
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * g.per_cta;
+  const int64_t t1 = t0 + g.per_cta < g.tiles ? t0 + g.per_cta : g.tiles;
+  *b = t0 * kSortTile;
+  *e = t1 * kSortTile < n ? t1 * kSortTile : n;
+  if (*b > n) *b = n;
+}
+
+// Per-CTA digit histogram; counts stored digit-major: counts[d * ctas + cta].
+__global__ void __launch_bounds__(kSortThreads)
+    radix_upsweep_kernel(const uint32_t* __restrict__ keys, int64_t n, SortGeom g, int shift,
+                         int width, uint32_t* __restrict__ counts) {
+  __shared__ uint32_t hist[kSortThreads / 32][1 << kMaxRadixBits];
+  const int nd = 1 << width;
+  const uint32_t mask = static_cast<uint32_t>(nd - 1);
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < (kSortThreads / 32) * nd; i += kSortThreads)
+    hist[i / nd][i % nd] = 0;
+  __syncthreads();
+  int64_t b, e;
+  cta_range(g, n, &b, &e);
+  // b is a multiple of the tile size, hence 16-byte aligned.
+  int64_t i = b + static_cast<int64_t>(threadIdx.x) * 4;
+  for (; i + 3 < e; i += kSortThreads * 4) {
+    const uint4 k = __ldg(reinterpret_cast<const uint4*>(keys + i));
+    atomicAdd(&hist[warp][(k.x >> shift) & mask], 1u);
+    atomicAdd(&hist[warp][(k.y >> shift) & mask], 1u);
+    atomicAdd(&hist[warp][(k.z >> shift) & mask], 1u);
+    atomicAdd(&hist[warp][(k.w >> shift) & mask], 1u);
+  }
+  for (; i < e; ++i) atomicAdd(&hist[warp][(__ldg(keys + i) >> shift) & mask], 1u);
+  __syncthreads();
+  for (int d = threadIdx.x; d < nd; d += kSortThreads) {
+    uint32_t s = 0;
+#pragma unroll
+    for (int w = 0; w < kSortThreads / 32; ++w) s += hist[w][d];
+    counts[static_cast<int64_t>(d) * g.ctas + blockIdx.x] = s;
+  }
+}
+
+// Single CTA: exclusive scan over `total` counts in place (digit-major order
+// yields, for each (digit, cta), the first output position of that CTA's keys
+// of that digit).  Optionally writes the grand total to *sum_out.
+__global__ void __launch_bounds__(1024)
+    exclusive_scan_kernel(uint32_t* __restrict__ data, int64_t total, uint32_t* sum_out) {
+  __shared__ uint32_t sm[33];
+  const int64_t per = (total + blockDim.x - 1) / blockDim.x;
+  const int64_t b = threadIdx.x * per;
+  const int64_t e = b + per < total ? b + per : total;
+  uint32_t s = 0;
+  for (int64_t i = b; i < e; ++i) s += data[i];
+  uint32_t agg;
+  const uint32_t inc = block_inclusive_scan(s, OpSum(), 0u, sm, &agg);
+  uint32_t run = inc - s;
+  for (int64_t i = b; i < e; ++i) {
+    const uint32_t v = data[i];
+    data[i] = run;
+    run += v;
+  }
+  if (sum_out && threadIdx.x == 0) *sum_out = agg;
+}
+
+struct DownSmem {
+  uint32_t run_off[1 << kMaxRadixBits];              // next output position per digit
+  uint32_t tile_cnt[1 << kMaxRadixBits];
+  uint32_t tile_start[1 << kMaxRadixBits];
+  uint32_t wcnt[kSortThreads / 32][1 << kMaxRadixBits];
+  uint32_t keys[kSortTile];
+  uint32_t vals[kSortTile];
+  float psw[kSortTile];
+  uint32_t scan[33];
+};
+
+template <bool kWeighted>
+__global__ void __launch_bounds__(kSortThreads)
+    radix_downsweep_kernel(const uint32_t* __restrict__ keys_in,
+                           const uint32_t* __restrict__ vals_in,
+                           const float* __restrict__ psw_in, uint32_t* __restrict__ keys_out,
+                           uint32_t* __restrict__ vals_out, float* __restrict__ psw_out,
+                           int64_t n, SortGeom g, int shift, int width,
+                           const uint32_t* __restrict__ counts) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  DownSmem& sm = *reinterpret_cast<DownSmem*>(smem_raw);
+  const int nd = 1 << width;
+  const uint32_t mask = static_cast<uint32_t>(nd - 1);
+  const int warp = threadIdx.x >> 5;
+  const unsigned lane = lane_id();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int d = threadIdx.x; d < nd; d += kSortThreads)
+    sm.run_off[d] = counts[static_cast<int64_t>(d) * g.ctas + blockIdx.x];
+  int64_t b, e;
+  cta_range(g, n, &b, &e);
+  __syncthreads();
+
+  for (int64_t tb = b; tb < e; tb += kSortTile) {
+    const int valid = static_cast<int>(e - tb < kSortTile ? e - tb : kSortTile);
+    for (int d = lane; d < nd; d += 32) sm.wcnt[warp][d] = 0;
+    __syncwarp();
+    // Rank this warp's 512 keys (16 rounds of 32 consecutive keys) stably
+    // among keys of the same digit within the warp.
+    uint32_t key[kSortItems];
+    uint32_t rank[kSortItems];
+#pragma unroll
+    for (int r = 0; r < kSortItems; ++r) {
+      const int p = warp * (kSortItems * 32) + r * 32 + static_cast<int>(lane);
+      // Keys past the end take the largest digit: they rank after every
+      // valid key of the tile and are never written out.
+      key[r] = p < valid ? __ldg(keys_in + tb + p) : 0xffffffffu;
+      const uint32_t d = (key[r] >> shift) & mask;
+      const unsigned peers = __match_any_sync(kFull, d);
+      const uint32_t before = sm.wcnt[warp][d];
+      __syncwarp();
+      if (lane == 31u - __clz(peers)) sm.wcnt[warp][d] = before + __popc(peers);
+      __syncwarp();
+      rank[r] = before + __popc(peers & lt_mask);
+    }
+    __syncthreads();
+    // Exclusive prefix over warps per digit, and the tile's digit counts.
+    for (int d = threadIdx.x; d < nd; d += kSortThreads) {
+      uint32_t s = 0;
+#pragma unroll
+      for (int w = 0; w < kSortThreads / 32; ++w) {
+        const uint32_t c = sm.wcnt[w][d];
+        sm.wcnt[w][d] = s;
+        s += c;
+      }
+      sm.tile_cnt[d] = s;
+    }
+    __syncthreads();
+    {
+      // Exclusive scan of the tile counts over digits (two digits per thread).
+      const int d0 = threadIdx.x * 2;
+      const uint32_t c0 = d0 < nd ? sm.tile_cnt[d0] : 0u;
+      const uint32_t c1 = d0 + 1 < nd ? sm.tile_cnt[d0 + 1] : 0u;
+      const uint32_t inc = block_inclusive_scan(c0 + c1, OpSum(), 0u, sm.scan);
+      if (d0 < nd) sm.tile_start[d0] = inc - c0 - c1;
+      if (d0 + 1 < nd) sm.tile_start[d0 + 1] = inc - c1;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kSortItems; ++r) {
+      const int p = warp * (kSortItems * 32) + r * 32 + static_cast<int>(lane);
+      const uint32_t d = (key[r] >> shift) & mask;
+      const uint32_t pos = sm.tile_start[d] + sm.wcnt[warp][d] + rank[r];
+      sm.keys[pos] = key[r];
+      if (p < valid) {
+        sm.vals[pos] = __ldg(vals_in + tb + p);
+        if (kWeighted) sm.psw[pos] = __ldg(psw_in + tb + p);
+      }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < valid; i += kSortThreads) {
+      const uint32_t k = sm.keys[i];
+      const uint32_t d = (k >> shift) & mask;
+      const uint32_t dst = sm.run_off[d] + (static_cast<uint32_t>(i) - sm.tile_start[d]);
+      keys_out[dst] = k;
+      vals_out[dst] = sm.vals[i];
+      if (kWeighted) psw_out[dst] = sm.psw[i];
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < nd; d += kSortThreads) sm.run_off[d] += sm.tile_cnt[d];
+    __syncthreads();
+  }
+}
+
+// --------------------------------------------------------------------- RLE
+// A run starts at i when key[i] is valid and differs from key[i-1].
+__device__ __forceinline__ bool run_start(const uint32_t* keys, int64_t i, uint32_t k,
+                                          uint32_t sentinel) {
+  return k < sentinel && (i == 0 || __ldg(keys + i - 1) != k);
+}
+
+__global__ void __launch_bounds__(kRleThreads)
+    rle_count_kernel(const uint32_t* __restrict__ keys, int64_t n, SortGeom g, uint32_t sentinel,
+                     uint32_t* __restrict__ cta_counts) {
+  __shared__ uint32_t sm[33];
+  int64_t b, e;
+  cta_range(g, n, &b, &e);
+  uint32_t c = 0;
+  for (int64_t i = b + threadIdx.x; i < e; i += kRleThreads) c += run_start(keys, i, __ldg(keys + i), sentinel);
+  uint32_t total;
+  block_inclusive_scan(c, OpSum(), 0u, sm, &total);
+  if (threadIdx.x == 0) cta_counts[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kRleThreads)
+    rle_write_kernel(const uint32_t* __restrict__ keys, int64_t n, SortGeom g, uint32_t sentinel,
+                     const uint32_t* __restrict__ cta_base, uint32_t* __restrict__ unique_keys,
+                     uint32_t* __restrict__ run_starts, uint32_t* __restrict__ counters) {
+  __shared__ uint32_t sm[33];
+  int64_t b, e;
+  cta_range(g, n, &b, &e);
+  uint32_t carry = cta_base[blockIdx.x];
+  const uint32_t R = cta_base[g.ctas];
+  for (int64_t tb = b; tb < e; tb += kRleTile) {
+    const int64_t i0 = tb + static_cast<int64_t>(threadIdx.x) * kRleItems;
+    uint32_t k[kRleItems];
+    bool f[kRleItems];
+    uint32_t c = 0;
+#pragma unroll
+    for (int j = 0; j < kRleItems; ++j) {
+      const int64_t i = i0 + j;
+      k[j] = i < e ? __ldg(keys + i) : sentinel;
+      f[j] = i < e && run_start(keys, i, k[j], sentinel);
+      c += f[j];
+    }
+    uint32_t total;
+    const uint32_t inc = block_inclusive_scan(c, OpSum(), 0u, sm, &total);
+    uint32_t r = carry + inc - c;
+#pragma unroll
+    for (int j = 0; j < kRleItems; ++j) {
+      const int64_t i = i0 + j;
+      if (f[j]) {
+        unique_keys[r] = k[j];
+        run_starts[r] = static_cast<uint32_t>(i);
+        ++r;
+      }
+      // End of the valid keys: the first invalid key, or the end of the array.
+      if (i < e) {
+        const bool first_invalid = k[j] >= sentinel && (i == 0 || __ldg(keys + i - 1) < sentinel);
+        const bool last_valid = i == n - 1 && k[j] < sentinel;
+        if (first_invalid || last_valid) {
+          const uint32_t nv = first_invalid ? static_cast<uint32_t>(i) : static_cast<uint32_t>(n);
+          run_starts[R] = nv;
+          counters[kCntValid] = nv;
+        }
+      }
+    }
+    carry += total;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) counters[kCntRuns] = R;
+}
+
+// ---------------------------------------------------------------- classify
+__device__ __forceinline__ int short_groups(int D) {
+  // lanes per row for fp32 gradient rows moved as float4: next_pow2(D/4), at most 32
+  const int nv = D >> 2;
+  int S = 1;
+  while (S < nv && S < 32) S <<= 1;
+  return 32 / S;
+}
+
+// One CTA: first run of every table (binary search of its first key among
+// the unique keys) and the prefix of short-run warp tasks per table.
+__global__ void __launch_bounds__(1024)
+    table_runs_kernel(const uint32_t* __restrict__ unique_keys, const uint32_t* __restrict__ counters,
+                      const int64_t* __restrict__ hash_base, const int64_t* __restrict__ D_offsets,
+                      int T, uint32_t* __restrict__ table_runs, uint32_t* __restrict__ table_tasks,
+                      uint32_t* __restrict__ counters_out) {
+  __shared__ uint32_t sm[33];
+  const uint32_t R = counters[kCntRuns];
+  for (int t = threadIdx.x; t <= T; t += blockDim.x) {
+    const uint32_t target = static_cast<uint32_t>(__ldg(hash_base + t));
+    uint32_t lo = 0, hi = R;
+    while (lo < hi) {
+      const uint32_t mid = (lo + hi) >> 1;
+      if (unique_keys[mid] < target) lo = mid + 1; else hi = mid;
+    }
+    table_runs[t] = t == T ? R : lo;
+  }
+  __syncthreads();
+  uint32_t carry = 0;
+  for (int base = 0; base < T; base += blockDim.x) {
+    const int t = base + threadIdx.x;
+    uint32_t c = 0;
+    if (t < T) {
+      const int D = static_cast<int>(__ldg(D_offsets + t + 1) - __ldg(D_offsets + t));
+      const int G = short_groups(D);
+      c = (table_runs[t + 1] - table_runs[t] + G - 1) / G;
+    }
+    uint32_t total;
+    const uint32_t inc = block_inclusive_scan(c, OpSum(), 0u, sm, &total);
+    if (t < T) table_tasks[t] = carry + inc - c;
+    carry += total;
+  }
+  if (threadIdx.x == 0) {
+    table_tasks[T] = carry;
+    counters_out[kCntTasks] = carry;
+  }
+}
+
+// Long runs (SL >= kLongThreshold): compacted into a list on the device, each
+// with a contiguous range of chunk slots and of reduction-tree nodes.
+__global__ void __launch_bounds__(256)
+    classify_kernel(const uint32_t* __restrict__ run_starts, uint32_t* __restrict__ counters,
+                    uint32_t* __restrict__ long_run, uint32_t* __restrict__ long_chunk0,
+                    uint32_t* __restrict__ long_tree0) {
+  const uint32_t R = counters[kCntRuns];
+  for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < R; j += gridDim.x * blockDim.x) {
+    const uint32_t SL = run_starts[j + 1] - run_starts[j];
+    if (SL >= static_cast<uint32_t>(kLongThreshold)) {
+      const uint32_t nch = (SL + kChunk - 1) / kChunk;
+      const uint32_t slot = atomicAdd(&counters[kCntLong], 1u);
+      long_run[slot] = j;
+      long_chunk0[slot] = atomicAdd(&counters[kCntChunks], nch);
+      long_tree0[slot] = atomicAdd(&counters[kCntTree], static_cast<uint32_t>(tree_nodes(nch)));
+    }
+  }
+}
+
+// One warp per long run: chunk -> run map, and the arrival counters of the
+// run's reduction tree (children per node).
+__global__ void __launch_bounds__(256)
+    chunk_fill_kernel(const uint32_t* __restrict__ run_starts, const uint32_t* __restrict__ counters,
+                      const uint32_t* __restrict__ long_run, const uint32_t* __restrict__ long_chunk0,
+                      const uint32_t* __restrict__ long_tree0, uint32_t* __restrict__ chunk_task,
+                      uint32_t* __restrict__ tree_cnt) {
+  const uint32_t nlong = counters[kCntLong];
+  const unsigned lane = lane_id();
+  const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
+  for (uint32_t k = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; k < nlong; k += warps) {
+    const uint32_t j = long_run[k];
+    const uint32_t SL = run_starts[j + 1] - run_starts[j];
+    const uint32_t nch = (SL + kChunk - 1) / kChunk;
+    const uint32_t c0 = long_chunk0[k];
+    for (uint32_t c = lane; c < nch; c += 32) chunk_task[c0 + c] = k;
+    uint32_t node = long_tree0[k];
+    uint32_t below = nch;
+    while (below > 1) {
+      const uint32_t here = (below + kFanIn - 1) / kFanIn;
+      for (uint32_t i = lane; i < here; i += 32) {
+        const uint32_t kids = below - i * kFanIn;
+        tree_cnt[node + i] = kids < static_cast<uint32_t>(kFanIn) ? kids : kFanIn;
+      }
+      node += here;
+      below = here;
+    }
+  }
+}
+
+int key_bits(const tbe_desc* d) {
+  // keys range over [0, total_E], total_E being the invalid-lookup key
+  const uint64_t maxkey = static_cast<uint64_t>(d->total_E);
+  int bits = 0;
+  while (bits < 32 && (maxkey >> bits) != 0) ++bits;
+  return bits < 1 ? 1 : bits;
+}
+
+SortGeom sort_geom(int64_t n, int num_sms) {
+  SortGeom g;
+  g.tiles = (n + kSortTile - 1) / kSortTile;
+  int64_t ctas = 2LL * num_sms;
+  if (ctas > kMaxSortCtas) ctas = kMaxSortCtas;
+  if (ctas > g.tiles) ctas = g.tiles;
+  if (ctas < 1) ctas = 1;
+  g.per_cta = (g.tiles + ctas - 1) / ctas;
+  g.ctas = static_cast<int>((g.tiles + g.per_cta - 1) / g.per_cta);
+  if (g.ctas < 1) g.ctas = 1;
+  return g;
+}
+
+template <typename IndexT>
+cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const IndexT* indices,
+                         const IndexT* offsets, const float* psw, bool check) {
+  const tbe_desc* d = L.d;
+  const int64_t n = L.n;
+  cudaStream_t s = L.s;
+  int* status = check ? reinterpret_cast<int*>(ws + W.status) : nullptr;
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws + W.counts);
+  const uint32_t sentinel = static_cast<uint32_t>(d->total_E);
+  const bool weighted = psw != nullptr;
+  uint32_t* keys[2] = {reinterpret_cast<uint32_t*>(ws + W.keys[0]),
+                       reinterpret_cast<uint32_t*>(ws + W.keys[1])};
+  uint32_t* vals[2] = {reinterpret_cast<uint32_t*>(ws + W.vals[0]),
+                       reinterpret_cast<uint32_t*>(ws + W.vals[1])};
+  float* pw[2] = {weighted ? reinterpret_cast<float*>(ws + W.psw[0]) : nullptr,
+                  weighted ? reinterpret_cast<float*>(ws + W.psw[1]) : nullptr};
+  uint32_t* uk = reinterpret_cast<uint32_t*>(ws + W.unique_keys);
+  uint32_t* rs = reinterpret_cast<uint32_t*>(ws + W.run_starts);
+
+  cudaError_t err = cudaMemsetAsync(counters, 0, kNumCounters * sizeof(uint32_t), s);
+  if (err != cudaSuccess) return err;
+  err = cudaMemsetAsync(rs, 0, sizeof(uint32_t), s);
+  if (err != cudaSuccess) return err;
+
+  if (n > 0) {
+    const int64_t nbags = static_cast<int64_t>(d->T) * d->B;
+    int64_t blocks = (nbags + 7) / 8;
+    if (blocks > (1 << 22)) blocks = 1 << 22;
+    if (weighted)
+      expand_kernel<IndexT, true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+          indices, offsets, psw, d->hash_base, n, d->T, d->B, sentinel, keys[0], vals[0], pw[0],
+          status);
+    else
+      expand_kernel<IndexT, false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+          indices, offsets, psw, d->hash_base, n, d->T, d->B, sentinel, keys[0], vals[0], pw[0],
+          status);
+    fill_tail_kernel<IndexT><<<64, 256, 0, s>>>(offsets, nbags, n, sentinel, keys[0], vals[0],
+                                                pw[0]);
+
+    const SortGeom g = sort_geom(n, L.num_sms);
+    const int bits = key_bits(d);
+    const int passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
+    const int rb = (bits + passes - 1) / passes;
+    uint32_t* counts = reinterpret_cast<uint32_t*>(ws + W.radix_counts);
+    const size_t smem = sizeof(DownSmem);
+    for (int p = 0; p < passes; ++p) {
+      const int shift = p * rb;
+      const int width = rb < bits - shift ? rb : bits - shift;
+      const int src = p & 1, dst = src ^ 1;
+      radix_upsweep_kernel<<<g.ctas, kSortThreads, 0, s>>>(keys[src], n, g, shift, width, counts);
+      exclusive_scan_kernel<<<1, 1024, 0, s>>>(counts, static_cast<int64_t>(1 << width) * g.ctas,
+                                               nullptr);
+      if (weighted)
+        radix_downsweep_kernel<true><<<g.ctas, kSortThreads, smem, s>>>(
+            keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], n, g, shift, width,
+            counts);
+      else
+        radix_downsweep_kernel<false><<<g.ctas, kSortThreads, smem, s>>>(
+            keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], n, g, shift, width,
+            counts);
+    }
+    const int fin = passes & 1;
+    uint32_t* cta_counts = reinterpret_cast<uint32_t*>(ws + W.cta_counts);
+    rle_count_kernel<<<g.ctas, kRleThreads, 0, s>>>(keys[fin], n, g, sentinel, cta_counts);
+    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_counts, g.ctas, cta_counts + g.ctas);
+    rle_write_kernel<<<g.ctas, kRleThreads, 0, s>>>(keys[fin], n, g, sentinel, cta_counts, uk, rs,
+                                                    counters);
+  }
+  table_runs_kernel<<<1, 1024, 0, s>>>(uk, counters, d->hash_base, d->D_offsets, d->T,
+                                       reinterpret_cast<uint32_t*>(ws + W.table_runs),
+                                       reinterpret_cast<uint32_t*>(ws + W.table_tasks), counters);
+  if (n > 0) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 8LL * L.num_sms) blocks = 8LL * L.num_sms;
+    classify_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        rs, counters, reinterpret_cast<uint32_t*>(ws + W.long_run),
+        reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
+        reinterpret_cast<uint32_t*>(ws + W.long_tree0));
+    int64_t fb = (W.max_long * 32 + 255) / 256;
+    if (fb > 8LL * L.num_sms) fb = 8LL * L.num_sms;
+    if (fb < 1) fb = 1;
+    chunk_fill_kernel<<<static_cast<unsigned>(fb), 256, 0, s>>>(
+        rs, counters, reinterpret_cast<uint32_t*>(ws + W.long_run),
+        reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
+        reinterpret_cast<uint32_t*>(ws + W.long_tree0),
+        reinterpret_cast<uint32_t*>(ws + W.chunk_task),
+        reinterpret_cast<uint32_t*>(ws + W.tree_cnt));
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int radix_passes(const tbe_desc* d) {
+  const int bits = key_bits(d);
+  return (bits + kMaxRadixBits - 1) / kMaxRadixBits;
+}
+
+cudaError_t prepare_preprocess_kernels() {
+  const int smem = static_cast<int>(sizeof(DownSmem));
+  cudaError_t e = cudaFuncSetAttribute(radix_downsweep_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(radix_downsweep_kernel<false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+cudaError_t launch_preprocess(const Launch& L, const WsLayout& W, char* ws, const void* indices,
+                              const void* offsets, const float* psw, bool check) {
+  if (L.d->index_dtype == TBE_DT_I32)
+    return preprocess_t<int32_t>(L, W, ws, static_cast<const int32_t*>(indices),
+                                 static_cast<const int32_t*>(offsets), psw, check);
+  return preprocess_t<int64_t>(L, W, ws, static_cast<const int64_t*>(indices),
+                               static_cast<const int64_t*>(offsets), psw, check);
+}
+
+}  // namespace tbe

@@ -1,0 +1,239 @@
+// C ABI entry points: argument validation, workspace layout and launch order.
+// The operations themselves are specified in include/tbe.h.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace tbe {
+
+cudaError_t prepare_preprocess_kernels();
+
+WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.weighted = (ws_flags & TBE_WS_WEIGHTED) != 0;
+  const size_t un = static_cast<size_t>(n);
+  L.status = take(64);
+  L.counts = take(kNumCounters * sizeof(uint32_t));
+  L.table_runs = take((d->T + 1) * sizeof(uint32_t));
+  L.table_tasks = take((d->T + 1) * sizeof(uint32_t));
+  for (int i = 0; i < 2; ++i) L.keys[i] = take(un * 4);
+  for (int i = 0; i < 2; ++i) L.vals[i] = take(un * 4);
+  for (int i = 0; i < 2; ++i) L.psw[i] = L.weighted ? take(un * 4) : 0;
+  L.radix_counts = take(sizeof(uint32_t) * (1u << kMaxRadixBits) * kMaxSortCtas);
+  L.cta_counts = take(sizeof(uint32_t) * (kMaxSortCtas + 1));
+  L.unique_keys = take((un + 1) * 4);
+  L.run_starts = take((un + 2) * 4);
+  L.max_long = n / kLongThreshold + 1;
+  L.max_chunks = n / kChunk + L.max_long + 1;
+  L.max_tree = L.max_chunks / (kFanIn - 1) + 8 * L.max_long + 1;
+  L.long_run = take(L.max_long * 4);
+  L.long_chunk0 = take(L.max_long * 4);
+  L.long_tree0 = take(L.max_long * 4);
+  L.chunk_task = take(L.max_chunks * 4);
+  L.tree_cnt = take(L.max_tree * 4);
+  L.partials = take(static_cast<size_t>(L.max_chunks) * d->max_D * 4);
+  L.tree_part = take(static_cast<size_t>(L.max_tree) * d->max_D * 4);
+  const int64_t nb1 = static_cast<int64_t>(d->T) * d->B + 1;
+  L.offsets_fix = take(nb1 * index_bytes(d));
+  L.fix_scratch = take(repair_scratch_blocks(nb1) * sizeof(int64_t));
+  L.total = off;
+  return L;
+}
+
+namespace {
+
+tbe_status check_desc(const tbe_desc* d) {
+  if (!d) return TBE_EINVAL;
+  if (d->T < 1 || d->B < 1 || !d->D_offsets || !d->hash_base || !d->weights_offsets)
+    return TBE_EINVAL;
+  if (d->weights_dtype != TBE_DT_F16) return TBE_EUNSUPPORTED;
+  if (d->index_dtype != TBE_DT_I32 && d->index_dtype != TBE_DT_I64) return TBE_EUNSUPPORTED;
+  if (d->min_D < 8 || d->max_D > kMaxD || d->min_D > d->max_D || (d->min_D & 7) ||
+      (d->max_D & 7) || d->total_D < d->max_D || (d->total_D & 7))
+    return TBE_EUNSUPPORTED;
+  if (d->total_E < 1 || d->total_E >= 0xffffffffLL) return TBE_EUNSUPPORTED;
+  if (static_cast<int64_t>(d->B) * d->T >= 0x7fffffffLL) return TBE_EUNSUPPORTED;
+  return TBE_OK;
+}
+
+tbe_status check_n(int64_t n) {
+  if (n < 0) return TBE_EINVAL;
+  if (n >= 0xfffffff0LL) return TBE_EUNSUPPORTED;
+  return TBE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sms() {
+  static int sms[64] = {0};
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::call_once(once[dev], [dev]() {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+      v = 148;
+    sms[dev] = v;
+    prepare_preprocess_kernels();
+  });
+  return sms[dev];
+}
+
+tbe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TBE_OK : TBE_ECUDA; }
+
+// Offsets check / repair shared by every entry point.  Returns the offsets
+// pointer the kernels should read.
+tbe_status run_checks(const Launch& L, const WsLayout& W, char* ws, const void* offsets,
+                      uint32_t flags, const void** offsets_eff, int** status) {
+  *offsets_eff = offsets;
+  *status = nullptr;
+  if (!(flags & (TBE_F_CHECK_BOUNDS | TBE_F_REPAIR_OFFSETS))) return TBE_OK;
+  *status = reinterpret_cast<int*>(ws + W.status);
+  const bool repair = (flags & TBE_F_REPAIR_OFFSETS) != 0;
+  cudaError_t e = launch_check_offsets(L, offsets, repair, ws + W.offsets_fix,
+                                       reinterpret_cast<int64_t*>(ws + W.fix_scratch), *status);
+  if (e != cudaSuccess) return TBE_ECUDA;
+  if (repair) *offsets_eff = ws + W.offsets_fix;
+  return TBE_OK;
+}
+
+tbe_status common_args(const tbe_desc* d, const void* indices, const void* offsets, int64_t n,
+                       void* workspace, size_t ws_bytes, bool weighted, WsLayout* W) {
+  tbe_status st = check_desc(d);
+  if (st != TBE_OK) return st;
+  st = check_n(n);
+  if (st != TBE_OK) return st;
+  if (!offsets || (n > 0 && !indices)) return TBE_EINVAL;
+  if (!workspace || !aligned16(workspace)) return TBE_EWORKSPACE;
+  *W = make_layout(d, n, weighted ? TBE_WS_WEIGHTED : 0u);
+  if (ws_bytes < W->total) return TBE_EWORKSPACE;
+  return TBE_OK;
+}
+
+}  // namespace
+}  // namespace tbe
+
+using namespace tbe;
+
+extern "C" {
+
+tbe_status tbe_workspace_size(const tbe_desc* d, int64_t n_max, uint32_t ws_flags,
+                              size_t* bytes) {
+  if (!bytes) return TBE_EINVAL;
+  tbe_status st = check_desc(d);
+  if (st != TBE_OK) return st;
+  st = check_n(n_max);
+  if (st != TBE_OK) return st;
+  *bytes = make_layout(d, n_max, ws_flags).total;
+  return TBE_OK;
+}
+
+tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indices,
+                       const void* offsets, int64_t n, const float* per_sample_weights,
+                       float* out, void* workspace, size_t ws_bytes, void* stream,
+                       uint32_t flags) {
+  WsLayout W;
+  // The forward needs only the status word and the repaired offsets, but the
+  // workspace contract is the same for every entry point.
+  tbe_status st = common_args(d, indices, offsets, n, workspace, ws_bytes, false, &W);
+  if (st != TBE_OK) return st;
+  if (!weights || !out || !aligned16(weights) || !aligned16(out)) return TBE_EINVAL;
+  const Launch L{d, n, static_cast<cudaStream_t>(stream), device_sms()};
+  char* ws = static_cast<char*>(workspace);
+  const void* off_eff;
+  int* status;
+  st = run_checks(L, W, ws, offsets, flags, &off_eff, &status);
+  if (st != TBE_OK) return st;
+  if (!(flags & TBE_F_FORCE_GENERIC) && small_table_eligible(d, n, per_sample_weights != nullptr))
+    return from_cuda(launch_forward_small(L, weights, indices, off_eff, out, status));
+  return from_cuda(
+      launch_forward_generic(L, weights, indices, off_eff, per_sample_weights, out, status));
+}
+
+tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* offsets, int64_t n,
+                          const float* per_sample_weights, void* workspace, size_t ws_bytes,
+                          void* stream, uint32_t flags) {
+  WsLayout W;
+  tbe_status st = common_args(d, indices, offsets, n, workspace, ws_bytes,
+                              per_sample_weights != nullptr, &W);
+  if (st != TBE_OK) return st;
+  const Launch L{d, n, static_cast<cudaStream_t>(stream), device_sms()};
+  char* ws = static_cast<char*>(workspace);
+  const void* off_eff;
+  int* status;
+  st = run_checks(L, W, ws, offsets, flags, &off_eff, &status);
+  if (st != TBE_OK) return st;
+  return from_cuda(launch_preprocess(L, W, ws, indices, off_eff, per_sample_weights,
+                                     status != nullptr));
+}
+
+tbe_status tbe_backward_rowwise_adagrad(const tbe_desc* d, const float* grad_out,
+                                        const void* indices, const void* offsets, int64_t n,
+                                        const float* per_sample_weights, void* weights,
+                                        float* momentum, float lr, float eps, void* workspace,
+                                        size_t ws_bytes, void* stream, uint32_t flags) {
+  WsLayout W;
+  tbe_status st = common_args(d, indices, offsets, n, workspace, ws_bytes,
+                              per_sample_weights != nullptr, &W);
+  if (st != TBE_OK) return st;
+  if (!grad_out || !weights || !momentum || !aligned16(grad_out) || !aligned16(weights))
+    return TBE_EINVAL;
+  const Launch L{d, n, static_cast<cudaStream_t>(stream), device_sms()};
+  char* ws = static_cast<char*>(workspace);
+  if (!(flags & TBE_F_PREPROCESSED)) {
+    const void* off_eff;
+    int* status;
+    st = run_checks(L, W, ws, offsets, flags, &off_eff, &status);
+    if (st != TBE_OK) return st;
+    st = from_cuda(launch_preprocess(L, W, ws, indices, off_eff, per_sample_weights,
+                                     status != nullptr));
+    if (st != TBE_OK) return st;
+  }
+  return from_cuda(launch_update(L, W, ws, grad_out, weights, momentum, lr, eps,
+                                 (flags & TBE_F_LONG_TWO_LAUNCH) != 0));
+}
+
+tbe_status tbe_workspace_view(const tbe_desc* d, int64_t n, uint32_t ws_flags, void* workspace,
+                              tbe_ws_view* view) {
+  if (!view || !workspace) return TBE_EINVAL;
+  tbe_status st = check_desc(d);
+  if (st != TBE_OK) return st;
+  st = check_n(n);
+  if (st != TBE_OK) return st;
+  const WsLayout W = make_layout(d, n, ws_flags);
+  const char* ws = static_cast<const char*>(workspace);
+  const int fin = radix_passes(d) & 1;
+  view->sorted_keys = reinterpret_cast<const uint32_t*>(ws + W.keys[fin]);
+  view->sorted_bags = reinterpret_cast<const uint32_t*>(ws + W.vals[fin]);
+  view->sorted_psw = W.weighted ? reinterpret_cast<const float*>(ws + W.psw[fin]) : nullptr;
+  view->unique_keys = reinterpret_cast<const uint32_t*>(ws + W.unique_keys);
+  view->run_starts = reinterpret_cast<const uint32_t*>(ws + W.run_starts);
+  view->counts = reinterpret_cast<const uint32_t*>(ws + W.counts);
+  view->long_runs = reinterpret_cast<const uint32_t*>(ws + W.long_run);
+  view->long_threshold = kLongThreshold;
+  view->chunk = kChunk;
+  return TBE_OK;
+}
+
+tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits) {
+  if (!workspace || !status_bits) return TBE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return TBE_ECUDA;
+  *status_bits = v;
+  return TBE_OK;
+}
+
+const char* tbe_version(void) { return "tbe-gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

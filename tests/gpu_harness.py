@@ -1,0 +1,118 @@
+"""Helpers for tests that run the CUDA path and the oracle on the same inputs.
+
+Inputs come from workloads (seeded); the CUDA path is reached only through
+the C-ABI binding; the oracle only through oracle/.  Nothing here computes a
+TBE result itself.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import table_embedding_bag_gb300 as tbe
+
+
+def ws_array(ws, ptr, count, dtype=torch.int32):
+    """Copy `count` 4-byte elements at device address ptr (inside ws) to numpy."""
+    off = ptr - ws.buf.data_ptr()
+    assert 0 <= off and off + 4 * count <= ws.nbytes
+    a = ws.buf[off:off + 4 * count].view(dtype).cpu().numpy()
+    return a.view(np.uint32) if dtype == torch.int32 else a
+
+
+def host(w):
+    """Host numpy copies of a workload's arrays (psw None when unweighted)."""
+    t = lambda x: None if x is None else x.detach().cpu().numpy()
+    return dict(indices=t(w.indices), offsets=t(w.offsets), psw=t(w.psw), weights=t(w.weights),
+                momentum=t(w.momentum), grad_out=t(w.grad_out))
+
+
+class Run:
+    """One TBE problem on the GPU through the C ABI."""
+
+    def __init__(self, w, device="cuda"):
+        self.w = w
+        self.desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, device)
+        self.ws = tbe.Workspace(self.desc, max(w.n, 1), w.psw is not None, device)
+        d = lambda x: None if x is None else x.to(device).contiguous()
+        self.indices, self.offsets, self.psw = d(w.indices), d(w.offsets), d(w.psw)
+        self.weights = d(w.weights).clone()
+        self.momentum = d(w.momentum).clone()
+        self.grad_out = d(w.grad_out)
+        self.out = torch.empty(w.B, self.desc.total_D, dtype=torch.float32, device=device)
+
+    def forward(self, flags=0):
+        tbe.tbe_forward(self.desc, self.weights, self.indices, self.offsets, self.psw, self.out,
+                        self.ws, flags)
+        torch.cuda.synchronize()
+        return self.out.cpu().numpy()
+
+    def preprocess(self, flags=0):
+        tbe.tbe_preprocess(self.desc, self.indices, self.offsets, self.psw, self.ws, flags)
+        torch.cuda.synchronize()
+        v = tbe.tbe_workspace_view(self.desc, max(self.w.n, 1), self.ws)
+        counts = ws_array(self.ws, v["counts"], 8)
+        R, nv = int(counts[0]), int(counts[1])
+        res = dict(R=R, n_valid=nv, n_long=int(counts[2]), n_chunks=int(counts[3]),
+                   sorted_keys=ws_array(self.ws, v["sorted_keys"], self.w.n),
+                   sorted_bags=ws_array(self.ws, v["sorted_bags"], self.w.n),
+                   unique_keys=ws_array(self.ws, v["unique_keys"], R),
+                   run_starts=ws_array(self.ws, v["run_starts"], R + 1),
+                   long_runs=ws_array(self.ws, v["long_runs"], int(counts[2])),
+                   long_threshold=v["long_threshold"], chunk=v["chunk"])
+        if v["sorted_psw"]:
+            res["sorted_psw"] = ws_array(self.ws, v["sorted_psw"], self.w.n, torch.float32)
+        return res
+
+    def backward(self, flags=0):
+        tbe.tbe_backward_rowwise_adagrad(self.desc, self.grad_out, self.indices, self.offsets,
+                                         self.psw, self.weights, self.momentum, self.w.lr,
+                                         self.w.eps, self.ws, flags)
+        torch.cuda.synchronize()
+        return self.weights.cpu().numpy(), self.momentum.cpu().numpy()
+
+    def status(self):
+        return tbe.tbe_read_status(self.ws)
+
+
+def tables(w):
+    return oracle.Tables(w.E, w.D)
+
+
+# ------------------------------------------------------------- comparisons
+def assert_forward_close(out, ref, abs_terms, rel=1e-5):
+    """|out - ref| <= rel * sum|terms| elementwise (sum|terms| from the oracle on |W|, |psw|)."""
+    err = np.abs(out.astype(np.float64) - ref.astype(np.float64))
+    tol = rel * abs_terms.astype(np.float64) + 1e-30
+    bad = err > tol
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} forward outputs off; worst err "
+                           f"{err.max():.3e} at {np.unravel_index(np.argmax(err - tol), err.shape)}")
+
+
+def assert_momentum_close(m, ref, rel=1e-5):
+    err = np.abs(m.astype(np.float64) - ref.astype(np.float64))
+    tol = rel * np.abs(ref.astype(np.float64)) + 1e-30
+    bad = err > tol
+    assert not bad.any(), f"{bad.sum()} momentum values off; worst rel {np.max(err / (tol / rel)):.3e}"
+
+
+def assert_weights_within_ulp(w, ref, ulps=1):
+    """fp16 values within `ulps` units in the last place of the oracle's value."""
+    a = w.astype(np.float64)
+    b = ref.astype(np.float64)
+    ulp = np.spacing(np.abs(ref).astype(np.float16)).astype(np.float64)
+    bad = np.abs(a - b) > ulps * ulp
+    assert not bad.any(), f"{bad.sum()} of {bad.size} weights beyond {ulps} ulp"
+
+
+def row_mask(tab, keys):
+    """Boolean mask over the flat weights of the rows with the given linear keys."""
+    mask = np.zeros(int(tab.w_offsets[-1]), bool)
+    for k in np.asarray(keys, dtype=np.int64):
+        t = int(np.searchsorted(tab.hash_base, k, side="right") - 1)
+        r = int(k - tab.hash_base[t])
+        D = int(tab.D[t])
+        s = int(tab.w_offsets[t]) + r * D
+        mask[s:s + D] = True
+    return mask

@@ -1,0 +1,106 @@
+"""The C-ABI library builds, loads without a GPU, exports every function that
+include/tbe.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import table_embedding_bag_gb300 as tbe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tbe.build()
+    return ctypes.CDLL(tbe.lib_path)
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tbe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tbe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted([
+        "tbe_backward_rowwise_adagrad", "tbe_forward", "tbe_preprocess", "tbe_read_status",
+        "tbe_version", "tbe_workspace_size", "tbe_workspace_view"])
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_string(lib):
+    lib.tbe_version.restype = ctypes.c_char_p
+    assert b"sm_103a" in lib.tbe_version()
+
+
+def _desc(T=2, B=4, E=(10, 20), D=(8, 16), index=tbe.TBE_DT_I64):
+    fake = 0x1000  # never dereferenced by the host-side checks
+    return tbe.tbe_desc(T, B, tbe.TBE_DT_F16, index, fake, fake, fake, sum(D), sum(E), max(D),
+                        min(D))
+
+
+def _ws_size(lib, d, n, flags=0):
+    out = ctypes.c_size_t(0)
+    lib.tbe_workspace_size.argtypes = [ctypes.POINTER(tbe.tbe_desc), ctypes.c_int64,
+                                       ctypes.c_uint32, ctypes.POINTER(ctypes.c_size_t)]
+    rc = lib.tbe_workspace_size(ctypes.byref(d), n, flags, ctypes.byref(out))
+    return rc, out.value
+
+
+def test_workspace_size_grows_with_lookups_and_weights(lib):
+    d = _desc()
+    rc0, s0 = _ws_size(lib, d, 0)
+    rc1, s1 = _ws_size(lib, d, 1 << 20)
+    rc2, s2 = _ws_size(lib, d, 1 << 20, tbe.TBE_WS_WEIGHTED)
+    assert rc0 == rc1 == rc2 == tbe.TBE_OK
+    assert 0 < s0 < s1 < s2
+    assert s2 - s1 >= 2 * 4 * (1 << 20)  # two per-sample-weight buffers
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("T", 0, tbe.TBE_EINVAL), ("B", 0, tbe.TBE_EINVAL), ("weights_dtype", 9, tbe.TBE_EUNSUPPORTED),
+    ("index_dtype", 9, tbe.TBE_EUNSUPPORTED), ("max_D", 2048, tbe.TBE_EUNSUPPORTED),
+    ("min_D", 4, tbe.TBE_EUNSUPPORTED), ("total_E", 1 << 32, tbe.TBE_EUNSUPPORTED),
+    ("D_offsets", None, tbe.TBE_EINVAL)])
+def test_bad_descriptors_rejected(lib, field, value, code):
+    d = _desc()
+    setattr(d, field, value)
+    assert _ws_size(lib, d, 100)[0] == code
+
+
+def test_bad_sizes_rejected(lib):
+    assert _ws_size(lib, _desc(), -1)[0] == tbe.TBE_EINVAL
+    assert _ws_size(lib, _desc(), 1 << 33)[0] == tbe.TBE_EUNSUPPORTED
+
+
+def test_small_workspace_rejected_before_any_launch(lib):
+    d = _desc()
+    P = ctypes.c_void_p
+    lib.tbe_forward.argtypes = [ctypes.POINTER(tbe.tbe_desc), P, P, P, ctypes.c_int64, P, P, P,
+                                ctypes.c_size_t, P, ctypes.c_uint32]
+    fake = P(0x1000)
+    rc = lib.tbe_forward(ctypes.byref(d), fake, fake, fake, 10, None, fake, fake, 16, None, 0)
+    assert rc == tbe.TBE_EWORKSPACE
+    rc = lib.tbe_forward(ctypes.byref(d), fake, fake, fake, 10, None, fake, None, 1 << 30, None, 0)
+    assert rc == tbe.TBE_EWORKSPACE
+    rc = lib.tbe_forward(ctypes.byref(d), fake, fake, None, 10, None, fake, fake, 1 << 30, None, 0)
+    assert rc == tbe.TBE_EINVAL
+    lib.tbe_backward_rowwise_adagrad.argtypes = [
+        ctypes.POINTER(tbe.tbe_desc), P, P, P, ctypes.c_int64, P, P, P, ctypes.c_float,
+        ctypes.c_float, P, ctypes.c_size_t, P, ctypes.c_uint32]
+    rc = lib.tbe_backward_rowwise_adagrad(ctypes.byref(d), fake, fake, fake, 10, None, fake, fake,
+                                          0.01, 1e-8, fake, 8, None, 0)
+    assert rc == tbe.TBE_EWORKSPACE
+
+
+def test_package_refuses_to_run_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(tbe, "lib_path", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(tbe, "_lib", None)
+    with pytest.raises(RuntimeError):
+        tbe.tbe_version()
