@@ -107,19 +107,26 @@ typedef struct tbe_desc {
 
 /* Device pointers into a workspace after tbe_preprocess, for inspection.
  * Counts marked (device) live in device memory and are never read back by the
- * library. */
+ * library.  A run is the set of sorted lookups of one (table,row); inside a
+ * run, a pair is the set of its lookups that come from one bag (they share
+ * one gradient row, so the update gathers it once and scales it by the
+ * pair's multiplicity or, with per-sample weights, by their sum). */
 typedef struct tbe_ws_view {
   const uint32_t* sorted_keys;  /* [n] linear keys hash_base[t]+row, ascending; invalid
                                    lookups carry key total_E and sort last */
-  const uint32_t* sorted_bags;  /* [n] bag b (within its table) of each sorted lookup */
+  const uint32_t* sorted_bags;  /* [n] bag b (within its table) of each sorted lookup;
+                                   ascending within a run (the sort is stable) */
   const float* sorted_psw;      /* [n] per-sample weight of each sorted lookup, or NULL */
   const uint32_t* unique_keys;  /* [R] key of each run */
   const uint32_t* run_starts;   /* [R+1] first sorted position of each run; [R] = n_valid */
-  const uint32_t* counts;       /* (device) [0] R runs, [1] n_valid lookups,
-                                   [2] long runs, [3] long-run chunks */
-  const uint32_t* long_runs;    /* [counts[2]] run id of each long run (SL >= long_threshold) */
-  int32_t long_threshold;       /* run length from which a run takes the chunked path */
-  int32_t chunk;                /* lookups per chunk on the chunked path */
+  const uint32_t* counts;       /* (device) [0] R runs, [1] n_valid lookups, [2] long runs,
+                                   [3] long-run chunks, [6] P pairs */
+  const uint32_t* long_runs;    /* [counts[2]] run id of each long run, in no set order */
+  int32_t long_threshold;       /* pairs from which a run takes the chunked path */
+  int32_t chunk;                /* pairs per chunk on the chunked path */
+  const uint32_t* run_pairs;    /* [R+1] first pair of each run; [R] = P */
+  const uint32_t* pair_starts;  /* [P+1] first sorted position of each pair; [P] = n_valid */
+  const uint32_t* pair_bags;    /* [P] bag of each pair */
 } tbe_ws_view;
 
 /* Bytes of workspace needed for calls with at most n_max lookups.

@@ -60,7 +60,8 @@ class tbe_ws_view(ctypes.Structure):
                 ("sorted_psw", ctypes.c_void_p), ("unique_keys", ctypes.c_void_p),
                 ("run_starts", ctypes.c_void_p), ("counts", ctypes.c_void_p),
                 ("long_runs", ctypes.c_void_p), ("long_threshold", ctypes.c_int32),
-                ("chunk", ctypes.c_int32)]
+                ("chunk", ctypes.c_int32), ("run_pairs", ctypes.c_void_p),
+                ("pair_starts", ctypes.c_void_p), ("pair_bags", ctypes.c_void_p)]
 
 
 _lib = None

@@ -13,9 +13,11 @@ namespace tbe {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-// Lookup threshold from which a run takes the chunked (cooperative) path and
-// the number of lookups per chunk.  The FBTriton backward uses 256 for both;
-// they stay equal here, so a long run always has at least one full chunk.
+// Work threshold from which a run takes the chunked (cooperative) path and
+// the work per chunk.  Work is counted in distinct (row, bag) pairs: every
+// lookup of a bag into the same row shares one gradient-row gather.  The
+// FBTriton backward uses 256 lookups for both; they stay equal here, so a
+// long run always has at least one full chunk.
 constexpr int kLongThreshold = 256;
 constexpr int kChunk = 256;
 // Fan-in of the last-arriver reduction tree over a long run's chunk partials.
@@ -38,6 +40,7 @@ enum Counter : int {
   kCntChunks = 3,    // chunks of long runs
   kCntTree = 4,      // internal reduction-tree nodes
   kCntTasks = 5,     // short-run warp tasks
+  kCntPairs = 6,     // P: distinct (key, bag) pairs among the valid sorted lookups
   kNumCounters = 8,
 };
 
@@ -52,7 +55,10 @@ struct WsLayout {
   size_t radix_counts; // uint32 [2^kMaxRadixBits * kMaxSortCtas]
   size_t cta_counts;   // uint32 [kMaxSortCtas + 1]
   size_t unique_keys;  // uint32 [n + 1]
-  size_t run_starts;   // uint32 [n + 2]
+  size_t run_starts;   // uint32 [n + 2] first sorted position of each run
+  size_t run_pairs;    // uint32 [n + 2] first pair of each run
+  size_t pair_starts;  // uint32 [n + 2] first sorted position of each (key, bag) pair
+  size_t pair_bags;    // uint32 [n + 1] bag of each pair
   size_t long_run;     // uint32 [max_long]
   size_t long_chunk0;  // uint32 [max_long] first chunk of each long run
   size_t long_tree0;   // uint32 [max_long] first tree node of each long run

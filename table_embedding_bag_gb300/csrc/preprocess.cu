@@ -30,7 +30,7 @@ namespace tbe {
 namespace {
 
 constexpr int kRleThreads = 256;
-constexpr int kRleItems = 4;
+constexpr int kRleItems = 8;
 constexpr int kRleTile = kRleThreads * kRleItems;
 
 // ------------------------------------------------------------------ expand
@@ -252,71 +252,148 @@ __global__ void __launch_bounds__(kSortThreads)
 }
 
 // --------------------------------------------------------------------- RLE
-// A run starts at i when key[i] is valid and differs from key[i-1].
-__device__ __forceinline__ bool run_start(const uint32_t* keys, int64_t i, uint32_t k,
-                                          uint32_t sentinel) {
-  return k < sentinel && (i == 0 || __ldg(keys + i - 1) != k);
+// Two levels over the sorted lookups: a run starts where the key changes (a
+// new table row), a pair starts where the key or the bag changes.  Lookups
+// with the invalid key start nothing.  Each thread owns kRleItems consecutive
+// lookups; the lookup before its first one comes from the neighbouring lane
+// (or, for lane 0, from memory).
+struct RleItems {
+  uint32_t k[kRleItems];
+  uint32_t b[kRleItems];
+  bool run_head[kRleItems];
+  bool pair_head[kRleItems];
+};
+
+__device__ __forceinline__ void rle_flags(const uint32_t* __restrict__ keys,
+                                          const uint32_t* __restrict__ bags, int64_t i0,
+                                          int64_t e, uint32_t sentinel, RleItems& it) {
+  if (i0 + kRleItems <= e) {
+#pragma unroll
+    for (int j = 0; j < kRleItems; j += 4) {
+      const uint4 kk = __ldg(reinterpret_cast<const uint4*>(keys + i0 + j));
+      const uint4 bb = __ldg(reinterpret_cast<const uint4*>(bags + i0 + j));
+      it.k[j] = kk.x; it.k[j + 1] = kk.y; it.k[j + 2] = kk.z; it.k[j + 3] = kk.w;
+      it.b[j] = bb.x; it.b[j + 1] = bb.y; it.b[j + 2] = bb.z; it.b[j + 3] = bb.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kRleItems; ++j) {
+      const bool in = i0 + j < e;
+      it.k[j] = in ? __ldg(keys + i0 + j) : sentinel;
+      it.b[j] = in ? __ldg(bags + i0 + j) : 0u;
+    }
+  }
+  uint32_t pk = __shfl_up_sync(kFull, it.k[kRleItems - 1], 1);
+  uint32_t pb = __shfl_up_sync(kFull, it.b[kRleItems - 1], 1);
+  bool first = false;  // no lookup before this one
+  if (lane_id() == 0) {
+    if (i0 > 0 && i0 - 1 < e) {
+      pk = __ldg(keys + i0 - 1);
+      pb = __ldg(bags + i0 - 1);
+    } else if (i0 == 0) {
+      first = true;
+    } else {
+      pk = sentinel;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kRleItems; ++j) {
+    const bool valid = it.k[j] < sentinel;
+    const bool newkey = first || it.k[j] != pk;
+    it.run_head[j] = valid && newkey;
+    it.pair_head[j] = valid && (newkey || it.b[j] != pb);
+    first = false;
+    pk = it.k[j];
+    pb = it.b[j];
+  }
 }
 
 __global__ void __launch_bounds__(kRleThreads)
-    rle_count_kernel(const uint32_t* __restrict__ keys, int64_t n, SortGeom g, uint32_t sentinel,
-                     uint32_t* __restrict__ cta_counts) {
-  __shared__ uint32_t sm[33];
+    rle_count_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ bags,
+                     int64_t n, SortGeom g, uint32_t sentinel, uint32_t* __restrict__ cta_runs,
+                     uint32_t* __restrict__ cta_pairs) {
+  __shared__ unsigned long long sm[33];
   int64_t b, e;
   cta_range(g, n, &b, &e);
-  uint32_t c = 0;
-  for (int64_t i = b + threadIdx.x; i < e; i += kRleThreads) c += run_start(keys, i, __ldg(keys + i), sentinel);
-  uint32_t total;
-  block_inclusive_scan(c, OpSum(), 0u, sm, &total);
-  if (threadIdx.x == 0) cta_counts[blockIdx.x] = total;
+  unsigned long long c = 0;  // runs in the high word, pairs in the low word
+  for (int64_t tb = b; tb < e; tb += kRleTile) {
+    RleItems it;
+    rle_flags(keys, bags, tb + static_cast<int64_t>(threadIdx.x) * kRleItems, e, sentinel, it);
+#pragma unroll
+    for (int j = 0; j < kRleItems; ++j)
+      c += (static_cast<unsigned long long>(it.run_head[j]) << 32) | it.pair_head[j];
+  }
+  unsigned long long total;
+  block_inclusive_scan(c, OpSum(), 0ull, sm, &total);
+  if (threadIdx.x == 0) {
+    cta_runs[blockIdx.x] = static_cast<uint32_t>(total >> 32);
+    cta_pairs[blockIdx.x] = static_cast<uint32_t>(total);
+  }
 }
 
 __global__ void __launch_bounds__(kRleThreads)
-    rle_write_kernel(const uint32_t* __restrict__ keys, int64_t n, SortGeom g, uint32_t sentinel,
-                     const uint32_t* __restrict__ cta_base, uint32_t* __restrict__ unique_keys,
-                     uint32_t* __restrict__ run_starts, uint32_t* __restrict__ counters) {
+    rle_write_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ bags,
+                     int64_t n, SortGeom g, uint32_t sentinel,
+                     const uint32_t* __restrict__ run_base, const uint32_t* __restrict__ pair_base,
+                     uint32_t* __restrict__ unique_keys, uint32_t* __restrict__ run_starts,
+                     uint32_t* __restrict__ run_pairs, uint32_t* __restrict__ pair_starts,
+                     uint32_t* __restrict__ pair_bags, uint32_t* __restrict__ counters) {
   __shared__ uint32_t sm[33];
   int64_t b, e;
   cta_range(g, n, &b, &e);
-  uint32_t carry = cta_base[blockIdx.x];
-  const uint32_t R = cta_base[g.ctas];
+  uint32_t r = run_base[blockIdx.x];
+  uint32_t p = pair_base[blockIdx.x];
+  const uint32_t R = run_base[g.ctas];
+  const uint32_t P = pair_base[g.ctas];
   for (int64_t tb = b; tb < e; tb += kRleTile) {
     const int64_t i0 = tb + static_cast<int64_t>(threadIdx.x) * kRleItems;
-    uint32_t k[kRleItems];
-    bool f[kRleItems];
-    uint32_t c = 0;
+    RleItems it;
+    rle_flags(keys, bags, i0, e, sentinel, it);
+    uint32_t c = 0;  // runs << 16 | pairs: at most kRleTile each per tile
 #pragma unroll
-    for (int j = 0; j < kRleItems; ++j) {
-      const int64_t i = i0 + j;
-      k[j] = i < e ? __ldg(keys + i) : sentinel;
-      f[j] = i < e && run_start(keys, i, k[j], sentinel);
-      c += f[j];
-    }
+    for (int j = 0; j < kRleItems; ++j) c += (static_cast<uint32_t>(it.run_head[j]) << 16) | it.pair_head[j];
     uint32_t total;
     const uint32_t inc = block_inclusive_scan(c, OpSum(), 0u, sm, &total);
-    uint32_t r = carry + inc - c;
+    const uint32_t exc = inc - c;
+    uint32_t rr = r + (exc >> 16);
+    uint32_t pp = p + (exc & 0xffffu);
 #pragma unroll
     for (int j = 0; j < kRleItems; ++j) {
       const int64_t i = i0 + j;
-      if (f[j]) {
-        unique_keys[r] = k[j];
-        run_starts[r] = static_cast<uint32_t>(i);
-        ++r;
+      if (it.pair_head[j]) {
+        pair_starts[pp] = static_cast<uint32_t>(i);
+        pair_bags[pp] = it.b[j];
+        if (it.run_head[j]) {
+          unique_keys[rr] = it.k[j];
+          run_starts[rr] = static_cast<uint32_t>(i);
+          run_pairs[rr] = pp;
+          ++rr;
+        }
+        ++pp;
       }
       // End of the valid keys: the first invalid key, or the end of the array.
       if (i < e) {
-        const bool first_invalid = k[j] >= sentinel && (i == 0 || __ldg(keys + i - 1) < sentinel);
-        const bool last_valid = i == n - 1 && k[j] < sentinel;
+        const bool invalid = it.k[j] >= sentinel;
+        const bool prev_valid = i == 0 ? false
+                                : (j > 0 ? it.k[j - 1] < sentinel : __ldg(keys + i - 1) < sentinel);
+        const bool first_invalid = invalid && (i == 0 || prev_valid);
+        const bool last_valid = !invalid && i == n - 1;
         if (first_invalid || last_valid) {
           const uint32_t nv = first_invalid ? static_cast<uint32_t>(i) : static_cast<uint32_t>(n);
           run_starts[R] = nv;
+          pair_starts[P] = nv;
+          run_pairs[R] = P;
           counters[kCntValid] = nv;
         }
       }
     }
-    carry += total;
+    r += total >> 16;
+    p += total & 0xffffu;
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) counters[kCntRuns] = R;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    counters[kCntRuns] = R;
+    counters[kCntPairs] = P;
+  }
 }
 
 // ---------------------------------------------------------------- classify
@@ -367,15 +444,15 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-// Long runs (SL >= kLongThreshold): compacted into a list on the device, each
-// with a contiguous range of chunk slots and of reduction-tree nodes.
+// Long runs (at least kLongThreshold pairs): compacted into a list on the
+// device, each with a contiguous range of chunk slots and of tree nodes.
 __global__ void __launch_bounds__(256)
-    classify_kernel(const uint32_t* __restrict__ run_starts, uint32_t* __restrict__ counters,
+    classify_kernel(const uint32_t* __restrict__ run_pairs, uint32_t* __restrict__ counters,
                     uint32_t* __restrict__ long_run, uint32_t* __restrict__ long_chunk0,
                     uint32_t* __restrict__ long_tree0) {
   const uint32_t R = counters[kCntRuns];
   for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < R; j += gridDim.x * blockDim.x) {
-    const uint32_t SL = run_starts[j + 1] - run_starts[j];
+    const uint32_t SL = run_pairs[j + 1] - run_pairs[j];
     if (SL >= static_cast<uint32_t>(kLongThreshold)) {
       const uint32_t nch = (SL + kChunk - 1) / kChunk;
       const uint32_t slot = atomicAdd(&counters[kCntLong], 1u);
@@ -389,7 +466,7 @@ __global__ void __launch_bounds__(256)
 // One warp per long run: chunk -> run map, and the arrival counters of the
 // run's reduction tree (children per node).
 __global__ void __launch_bounds__(256)
-    chunk_fill_kernel(const uint32_t* __restrict__ run_starts, const uint32_t* __restrict__ counters,
+    chunk_fill_kernel(const uint32_t* __restrict__ run_pairs, const uint32_t* __restrict__ counters,
                       const uint32_t* __restrict__ long_run, const uint32_t* __restrict__ long_chunk0,
                       const uint32_t* __restrict__ long_tree0, uint32_t* __restrict__ chunk_task,
                       uint32_t* __restrict__ tree_cnt) {
@@ -398,7 +475,7 @@ __global__ void __launch_bounds__(256)
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   for (uint32_t k = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; k < nlong; k += warps) {
     const uint32_t j = long_run[k];
-    const uint32_t SL = run_starts[j + 1] - run_starts[j];
+    const uint32_t SL = run_pairs[j + 1] - run_pairs[j];
     const uint32_t nch = (SL + kChunk - 1) / kChunk;
     const uint32_t c0 = long_chunk0[k];
     for (uint32_t c = lane; c < nch; c += 32) chunk_task[c0 + c] = k;
@@ -460,6 +537,10 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
   if (err != cudaSuccess) return err;
   err = cudaMemsetAsync(rs, 0, sizeof(uint32_t), s);
   if (err != cudaSuccess) return err;
+  err = cudaMemsetAsync(ws + W.run_pairs, 0, sizeof(uint32_t), s);
+  if (err != cudaSuccess) return err;
+  err = cudaMemsetAsync(ws + W.pair_starts, 0, sizeof(uint32_t), s);
+  if (err != cudaSuccess) return err;
 
   if (n > 0) {
     const int64_t nbags = static_cast<int64_t>(d->T) * d->B;
@@ -499,11 +580,17 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
             counts);
     }
     const int fin = passes & 1;
-    uint32_t* cta_counts = reinterpret_cast<uint32_t*>(ws + W.cta_counts);
-    rle_count_kernel<<<g.ctas, kRleThreads, 0, s>>>(keys[fin], n, g, sentinel, cta_counts);
-    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_counts, g.ctas, cta_counts + g.ctas);
-    rle_write_kernel<<<g.ctas, kRleThreads, 0, s>>>(keys[fin], n, g, sentinel, cta_counts, uk, rs,
-                                                    counters);
+    uint32_t* cta_runs = reinterpret_cast<uint32_t*>(ws + W.cta_counts);
+    uint32_t* cta_pairs = cta_runs + (kMaxSortCtas + 1);
+    rle_count_kernel<<<g.ctas, kRleThreads, 0, s>>>(keys[fin], vals[fin], n, g, sentinel, cta_runs,
+                                                    cta_pairs);
+    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_runs, g.ctas, cta_runs + g.ctas);
+    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_pairs, g.ctas, cta_pairs + g.ctas);
+    rle_write_kernel<<<g.ctas, kRleThreads, 0, s>>>(
+        keys[fin], vals[fin], n, g, sentinel, cta_runs, cta_pairs, uk, rs,
+        reinterpret_cast<uint32_t*>(ws + W.run_pairs),
+        reinterpret_cast<uint32_t*>(ws + W.pair_starts),
+        reinterpret_cast<uint32_t*>(ws + W.pair_bags), counters);
   }
   table_runs_kernel<<<1, 1024, 0, s>>>(uk, counters, d->hash_base, d->D_offsets, d->T,
                                        reinterpret_cast<uint32_t*>(ws + W.table_runs),
@@ -512,14 +599,14 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     int64_t blocks = (n + 255) / 256;
     if (blocks > 8LL * L.num_sms) blocks = 8LL * L.num_sms;
     classify_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        rs, counters, reinterpret_cast<uint32_t*>(ws + W.long_run),
+        reinterpret_cast<uint32_t*>(ws + W.run_pairs), counters, reinterpret_cast<uint32_t*>(ws + W.long_run),
         reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
         reinterpret_cast<uint32_t*>(ws + W.long_tree0));
     int64_t fb = (W.max_long * 32 + 255) / 256;
     if (fb > 8LL * L.num_sms) fb = 8LL * L.num_sms;
     if (fb < 1) fb = 1;
     chunk_fill_kernel<<<static_cast<unsigned>(fb), 256, 0, s>>>(
-        rs, counters, reinterpret_cast<uint32_t*>(ws + W.long_run),
+        reinterpret_cast<uint32_t*>(ws + W.run_pairs), counters, reinterpret_cast<uint32_t*>(ws + W.long_run),
         reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
         reinterpret_cast<uint32_t*>(ws + W.long_tree0),
         reinterpret_cast<uint32_t*>(ws + W.chunk_task),

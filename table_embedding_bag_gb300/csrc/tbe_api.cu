@@ -27,9 +27,12 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   for (int i = 0; i < 2; ++i) L.vals[i] = take(un * 4);
   for (int i = 0; i < 2; ++i) L.psw[i] = L.weighted ? take(un * 4) : 0;
   L.radix_counts = take(sizeof(uint32_t) * (1u << kMaxRadixBits) * kMaxSortCtas);
-  L.cta_counts = take(sizeof(uint32_t) * (kMaxSortCtas + 1));
+  L.cta_counts = take(sizeof(uint32_t) * 2 * (kMaxSortCtas + 1));
   L.unique_keys = take((un + 1) * 4);
   L.run_starts = take((un + 2) * 4);
+  L.run_pairs = take((un + 2) * 4);
+  L.pair_starts = take((un + 2) * 4);
+  L.pair_bags = take((un + 1) * 4);
   L.max_long = n / kLongThreshold + 1;
   L.max_chunks = n / kChunk + L.max_long + 1;
   L.max_tree = L.max_chunks / (kFanIn - 1) + 8 * L.max_long + 1;
@@ -217,6 +220,9 @@ tbe_status tbe_workspace_view(const tbe_desc* d, int64_t n, uint32_t ws_flags, v
   view->run_starts = reinterpret_cast<const uint32_t*>(ws + W.run_starts);
   view->counts = reinterpret_cast<const uint32_t*>(ws + W.counts);
   view->long_runs = reinterpret_cast<const uint32_t*>(ws + W.long_run);
+  view->run_pairs = reinterpret_cast<const uint32_t*>(ws + W.run_pairs);
+  view->pair_starts = reinterpret_cast<const uint32_t*>(ws + W.pair_starts);
+  view->pair_bags = reinterpret_cast<const uint32_t*>(ws + W.pair_bags);
   view->long_threshold = kLongThreshold;
   view->chunk = kChunk;
   return TBE_OK;

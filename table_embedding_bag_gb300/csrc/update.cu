@@ -2,10 +2,10 @@
 // step per touched row.
 //
 // "Modernizing Table Batched Embeddings with FBTriton", section "Backward:
-// invert 'which rows did this sample use?'": runs shorter than 256 lookups are
-// handled by one program that gathers, accumulates in registers, updates and
-// plain-stores the row (it owns the row exclusively); longer runs are split
-// into chunks of 256 lookups that write partial sums; in the fused variant
+// invert 'which rows did this sample use?'": short runs are handled by one
+// program that gathers, accumulates in registers, updates and plain-stores
+// the row (it owns the row exclusively); long runs are split into chunks
+// that write partial sums; in the fused variant
 // each chunk writes its partial, executes a device-scope fence and decrements
 // the run's remaining count, and only the last chunk to finish updates the
 // row, while the default variant finishes in a second kernel.  Section
@@ -16,6 +16,11 @@
 // first and the weight step divides by sqrt(new accumulator) + eps.
 //
 // GB300 design:
+//  * work is counted in pairs: the lookups of one run that come from the
+//    same bag read the same gradient row, so each pair gathers that row once
+//    and scales it by the pair's multiplicity (or the sum of its per-sample
+//    weights).  On skewed inputs a hot row is hit many times per bag, and
+//    this removes most of its gathers;
 //  * the gradient rows are fp32; a row of D floats is D/4 float4 vectors on
 //    S = next_pow2(D/4) lanes (at most 32), so one warp serves G = 32/S short
 //    runs of the same table at once (tasks never straddle tables);
@@ -39,10 +44,11 @@ struct UpdArgs {
   const int64_t* D_offsets;
   const int64_t* hash_base;
   const int64_t* w_offsets;
-  const uint32_t* sorted_bags;
   const float* sorted_psw;
   const uint32_t* unique_keys;
-  const uint32_t* run_starts;
+  const uint32_t* run_pairs;
+  const uint32_t* pair_starts;
+  const uint32_t* pair_bags;
   const uint32_t* counters;
   const uint32_t* table_runs;
   const uint32_t* table_tasks;
@@ -70,6 +76,23 @@ __device__ __forceinline__ int find_table(const V* first, int T, V x) {
     if (__ldg(first + mid) <= x) lo = mid; else hi = mid - 1;
   }
   return lo;
+}
+
+// Bag and coefficient of pair k: every lookup of the pair reads the same
+// gradient row, so the row is gathered once and scaled by the number of
+// lookups or, with per-sample weights, by their sum (in lookup order).
+template <bool kWeighted>
+__device__ __forceinline__ void load_pair(const UpdArgs& a, uint32_t k, uint32_t* bag, float* coef) {
+  const uint32_t s = a.pair_starts[k];
+  const uint32_t e = a.pair_starts[k + 1];
+  *bag = a.pair_bags[k];
+  if (kWeighted) {
+    float c = 0.f;
+    for (uint32_t i = s; i < e; ++i) c += a.sorted_psw[i];
+    *coef = c;
+  } else {
+    *coef = static_cast<float>(e - s);
+  }
 }
 
 // Row-wise Adagrad on one row (key, row r of table t) with the summed
@@ -121,10 +144,10 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, int t, uint32_t j0,
   const int D = static_cast<int>(__ldg(a.D_offsets + t + 1) - d0);
   const int nv = D >> 2;
   const uint32_t j = j0 + g;
-  uint32_t s = 0, SL = 0;
+  uint32_t s = 0, SL = 0;  // first pair and pair count of this group's run
   if (j < j_end) {
-    s = a.run_starts[j];
-    SL = a.run_starts[j + 1] - s;
+    s = a.run_pairs[j];
+    SL = a.run_pairs[j + 1] - s;
     if (SL >= static_cast<uint32_t>(kLongThreshold)) SL = 0;  // chunked path owns it
   }
   const uint32_t max_len = __reduce_max_sync(kFull, SL);
@@ -136,10 +159,7 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, int t, uint32_t j0,
   for (uint32_t base = 0; base < max_len; base += S) {
     uint32_t my_b = 0xffffffffu;
     float my_w = 0.f;
-    if (base + sl < SL) {
-      my_b = a.sorted_bags[s + base + sl];
-      my_w = kWeighted ? a.sorted_psw[s + base + sl] : 1.f;
-    }
+    if (base + sl < SL) load_pair<kWeighted>(a, s + base + sl, &my_b, &my_w);
 #pragma unroll
     for (int u0 = 0; u0 < S; u0 += U) {
       if (base + u0 >= max_len) break;  // warp-uniform
@@ -199,8 +219,8 @@ __global__ void __launch_bounds__(256) short_runs_kernel(UpdArgs a) {
 }
 
 // -------------------------------------------------------------- long runs
-// Sum lookups [s, e) of one run over the whole warp: group g takes every G-th
-// lookup; the groups meet in a butterfly so every lane ends with its columns.
+// Sum pairs [s, e) of one run over the whole warp: group g takes every G-th
+// pair; the groups meet in a butterfly so every lane ends with its columns.
 template <int S, int NC, bool kWeighted>
 __device__ __forceinline__ void sum_lookups(const UpdArgs& a, int64_t d0, int nv, uint32_t s,
                                             uint32_t e, float (&acc)[NC][4]) {
@@ -217,10 +237,7 @@ __device__ __forceinline__ void sum_lookups(const UpdArgs& a, int64_t d0, int nv
     const int cnt = static_cast<int>(e - base < 32u ? e - base : 32u);
     uint32_t my_b = 0xffffffffu;
     float my_w = 0.f;
-    if (lane < cnt) {
-      my_b = a.sorted_bags[base + lane];
-      my_w = kWeighted ? a.sorted_psw[base + lane] : 1.f;
-    }
+    if (lane < cnt) load_pair<kWeighted>(a, base + lane, &my_b, &my_w);
 #pragma unroll
     for (int u0 = 0; u0 < S; u0 += U) {
       if (G * u0 >= cnt) break;  // warp-uniform
@@ -328,8 +345,8 @@ __device__ __forceinline__ void long_chunk(const UpdArgs& a, uint32_t q, bool tw
   const uint32_t k = a.chunk_task[q];
   const uint32_t j = a.long_run[k];
   const uint32_t c = q - a.long_chunk0[k];
-  const uint32_t rs0 = a.run_starts[j];
-  const uint32_t SL = a.run_starts[j + 1] - rs0;
+  const uint32_t rs0 = a.run_pairs[j];
+  const uint32_t SL = a.run_pairs[j + 1] - rs0;
   const uint32_t nch = (SL + kChunk - 1) / kChunk;
   const uint32_t s = rs0 + c * kChunk;
   const uint32_t e = s + kChunk < rs0 + SL ? s + kChunk : rs0 + SL;
@@ -401,7 +418,7 @@ __global__ void __launch_bounds__(256) long_chunks_kernel(UpdArgs a, bool two_la
 template <int S, int NC>
 __device__ __forceinline__ void finish_run(const UpdArgs& a, uint32_t k) {
   const uint32_t j = a.long_run[k];
-  const uint32_t SL = a.run_starts[j + 1] - a.run_starts[j];
+  const uint32_t SL = a.run_pairs[j + 1] - a.run_pairs[j];
   const uint32_t nch = (SL + kChunk - 1) / kChunk;
   const uint32_t key = a.unique_keys[j];
   const int t = find_table(a.hash_base, a.T, static_cast<int64_t>(key));
@@ -445,10 +462,11 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   a.D_offsets = d->D_offsets;
   a.hash_base = d->hash_base;
   a.w_offsets = d->weights_offsets;
-  a.sorted_bags = reinterpret_cast<const uint32_t*>(ws + W.vals[fin]);
   a.sorted_psw = W.weighted ? reinterpret_cast<const float*>(ws + W.psw[fin]) : nullptr;
   a.unique_keys = reinterpret_cast<const uint32_t*>(ws + W.unique_keys);
-  a.run_starts = reinterpret_cast<const uint32_t*>(ws + W.run_starts);
+  a.run_pairs = reinterpret_cast<const uint32_t*>(ws + W.run_pairs);
+  a.pair_starts = reinterpret_cast<const uint32_t*>(ws + W.pair_starts);
+  a.pair_bags = reinterpret_cast<const uint32_t*>(ws + W.pair_bags);
   a.counters = reinterpret_cast<const uint32_t*>(ws + W.counts);
   a.table_runs = reinterpret_cast<const uint32_t*>(ws + W.table_runs);
   a.table_tasks = reinterpret_cast<const uint32_t*>(ws + W.table_tasks);

@@ -53,8 +53,11 @@ class Run:
         torch.cuda.synchronize()
         v = tbe.tbe_workspace_view(self.desc, max(self.w.n, 1), self.ws)
         counts = ws_array(self.ws, v["counts"], 8)
-        R, nv = int(counts[0]), int(counts[1])
-        res = dict(R=R, n_valid=nv, n_long=int(counts[2]), n_chunks=int(counts[3]),
+        R, nv, P = int(counts[0]), int(counts[1]), int(counts[6])
+        res = dict(R=R, n_valid=nv, n_long=int(counts[2]), n_chunks=int(counts[3]), P=P,
+                   run_pairs=ws_array(self.ws, v["run_pairs"], R + 1),
+                   pair_starts=ws_array(self.ws, v["pair_starts"], P + 1),
+                   pair_bags=ws_array(self.ws, v["pair_bags"], P),
                    sorted_keys=ws_array(self.ws, v["sorted_keys"], self.w.n),
                    sorted_bags=ws_array(self.ws, v["sorted_bags"], self.w.n),
                    unique_keys=ws_array(self.ws, v["unique_keys"], R),
@@ -116,3 +119,17 @@ def row_mask(tab, keys):
         s = int(tab.w_offsets[t]) + r * D
         mask[s:s + D] = True
     return mask
+
+
+def pair_structure(sorted_keys, sorted_bags, run_starts):
+    """Pairs read off sorted arrays: a pair starts where the key or the bag
+    changes.  Returns (pair_starts[P+1], pair_bags[P], run_pairs[R+1])."""
+    k = np.asarray(sorted_keys, dtype=np.int64)
+    b = np.asarray(sorted_bags, dtype=np.int64)
+    n = len(k)
+    head = np.ones(n, bool)
+    if n:
+        head[1:] = (k[1:] != k[:-1]) | (b[1:] != b[:-1])
+    ps = np.concatenate([np.nonzero(head)[0], [n]]).astype(np.int64)
+    rp = np.searchsorted(ps, np.asarray(run_starts, dtype=np.int64))
+    return ps, b[ps[:-1]], rp

@@ -66,23 +66,23 @@ def test_row_widths(D):
     check_all(custom([50], [D], 16, bags, weighted=True))
 
 
-@pytest.mark.parametrize("SL", [1, 255, 256, 257, 511, 512, 513, 8191, 8192, 8193])
-def test_run_lengths_around_chunk_boundaries(SL):
-    # row 3 appears SL times spread over 64 bags; other rows once or twice
-    rng = np.random.default_rng(SL)
-    B = 64
-    rows = [3] * SL + list(rng.integers(4, 10, 50))
-    rng.shuffle(rows)
-    cuts = np.sort(rng.integers(0, len(rows), B - 1))
-    bags = [list(x) for x in np.split(np.array(rows), cuts)]
+@pytest.mark.parametrize("P", [1, 255, 256, 257, 511, 512, 513, 8191, 8192, 8193])
+def test_run_lengths_around_chunk_boundaries(P):
+    # row 3 is looked up by P distinct bags (a few of them twice); the work of
+    # a run is counted in distinct bags, so P sits on the chunk boundaries
+    rng = np.random.default_rng(P)
+    B = P + 7
+    bags = [[int(r)] for r in rng.integers(4, 10, B)]
+    for b in range(P):
+        bags[b] = [3] * (1 + (b % 5 == 0)) + bags[b]
     for flags in (0, tbe.TBE_F_LONG_TWO_LAUNCH):
-        check_all(custom([10], [64], B, bags, seed=SL), flags)
+        check_all(custom([10], [64], B, bags, seed=P, weighted=P % 2 == 1), flags)
 
 
 def test_deep_reduction_tree():
-    # 1.1M lookups of one row: ~4300 chunks -> tree levels 135, 5, 1
-    B = 4096
-    bags = [[7] * 268 + [1]] * B
+    # one row looked up by 1.2M distinct bags: ~4700 chunks -> tree levels 147, 5, 1
+    B = 1200000
+    bags = [[7]] * B
     w = custom([9], [128], B, bags, seed=1)
     check_all(w)
     check_all(w, tbe.TBE_F_LONG_TWO_LAUNCH)

@@ -82,8 +82,13 @@ def test_fullsize_sort_properties(full):
     assert rs[0] == 0 and rs[-1] == n and np.all(np.diff(rs) > 0)
     assert np.all(np.diff(uk) > 0) and np.array_equal(k[rs[:-1]], uk)
     assert got["R"] == int(np.count_nonzero(np.diff(k))) + 1
-    sl = np.diff(rs)
-    assert np.array_equal(np.sort(got["long_runs"]), np.nonzero(sl >= got["long_threshold"])[0])
+    ps, pb, rp = H.pair_structure(k, bags.numpy(), rs)
+    assert got["P"] == len(pb)
+    assert np.array_equal(got["pair_starts"].astype(np.int64), ps)
+    assert np.array_equal(got["run_pairs"].astype(np.int64), rp)
+    npairs = np.diff(rp)
+    assert np.array_equal(np.sort(got["long_runs"]),
+                          np.nonzero(npairs >= got["long_threshold"])[0])
 
 
 @pytest.mark.parametrize("two_launch", [False, True])
@@ -91,9 +96,9 @@ def test_fullsize_backward_sampled_rows(full, two_launch):
     w = full
     run = H.Run(w)
     pre = run.preprocess()
-    rs = pre["run_starts"].astype(np.int64)
+    rp = pre["run_pairs"].astype(np.int64)
     uk = pre["unique_keys"].astype(np.int64)
-    sl = np.diff(rs)
+    sl = np.diff(rp)
     rng = np.random.default_rng(2)
     # the longest runs (deepest reduction trees), random touched rows, and a
     # few untouched rows

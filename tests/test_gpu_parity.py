@@ -65,12 +65,18 @@ def test_preprocess_bit_exact(case):
     assert np.array_equal(got["run_starts"].astype(np.int64), ref["run_starts"])
     if hw["psw"] is not None:
         assert np.array_equal(got["sorted_psw"][:nv], hw["psw"][ref["sorted_pos"]])
-    # device-side classification: exactly the runs of at least long_threshold lookups
-    sl = np.diff(ref["run_starts"])
-    exp_long = np.nonzero(sl >= got["long_threshold"])[0]
+    # pairs: a new pair wherever the key or the bag changes
+    ps, pb, rp = H.pair_structure(ref["sorted_keys"], ref["sorted_bags"], ref["run_starts"])
+    assert got["P"] == len(pb)
+    assert np.array_equal(got["pair_starts"].astype(np.int64), ps)
+    assert np.array_equal(got["pair_bags"].astype(np.int64), pb)
+    assert np.array_equal(got["run_pairs"].astype(np.int64), rp)
+    # device-side classification: exactly the runs of at least long_threshold pairs
+    npairs = np.diff(rp)
+    exp_long = np.nonzero(npairs >= got["long_threshold"])[0]
     assert np.array_equal(np.sort(got["long_runs"]), exp_long)
     chunk = got["chunk"]
-    assert got["n_chunks"] == int(((sl[exp_long] + chunk - 1) // chunk).sum())
+    assert got["n_chunks"] == int(((npairs[exp_long] + chunk - 1) // chunk).sum())
 
 
 @pytest.mark.parametrize("two_launch", [False, True])
