@@ -49,6 +49,10 @@ def parse():
                    help="bags of table 0 in the CPU-oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    # smaller variants of the hot-row recipe, for profiling captures only
+    p.add_argument("--tables", type=int, default=None)
+    p.add_argument("--rows", type=int, default=None)
+    p.add_argument("--bags", type=int, default=None)
     return p.parse_args()
 
 
@@ -146,7 +150,8 @@ def run_native(args, world, rank, local):
     import workloads
 
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = workloads.make("hot", device=dev, seed=rank)
+    E_scale = None if args.rows is None else args.rows / workloads.SPECS["hot"].E
+    w = workloads.make("hot", device=dev, seed=rank, T=args.tables, B=args.bags, E_scale=E_scale)
     desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, dev)
     ws = tbe.Workspace(desc, w.n, False, dev)
     weights, momentum = w.weights, w.momentum
@@ -326,7 +331,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "n_lookups": w.n, "global_batch": w.B * world,
+        "config": {"workload": WORKLOAD if (args.tables, args.rows, args.bags) == (None,) * 3 else
+                   f"reduced hot-row recipe T={w.T} E={int(w.E[0])} B={w.B} (profiling case)",
+                   "n_lookups": w.n, "global_batch": w.B * world,
                    "parallelism": f"replicas x{world} (independent batches)",
                    "l2": "inputs larger than L2 (indices 1.7 GB, weights 20.5 GB); no flush",
                    "storage": "fp16 weights, fp32 momentum/gradients"},

@@ -25,6 +25,11 @@ constexpr int kFanIn = 32;
 // Widest supported table row (elements); rows are moved in 16-byte vectors.
 constexpr int kMaxD = 1024;
 
+// Long-run chunks are processed in order of the first bag they touch, binned
+// into at most this many bag bands, so that the warps in flight gather
+// gradient rows from a narrow band of bags and the band stays in L2.
+constexpr int kBagBands = 2048;
+
 // Radix sort: threads per CTA, keys per thread, digit width bound.
 constexpr int kSortThreads = 256;
 constexpr int kSortItems = 16;
@@ -63,6 +68,9 @@ struct WsLayout {
   size_t long_chunk0;  // uint32 [max_long] first chunk of each long run
   size_t long_tree0;   // uint32 [max_long] first tree node of each long run
   size_t chunk_task;   // uint32 [max_chunks] long run of each chunk
+  size_t chunk_band;   // uint32 [max_chunks] bag band of each chunk
+  size_t chunk_order;  // uint32 [max_chunks] chunks sorted by bag band
+  size_t band_count;   // uint32 [kBagBands] chunks per band, then band cursors
   size_t tree_cnt;     // uint32 [max_tree] arrivals still expected at each tree node
   size_t partials;     // float [max_chunks * max_D]
   size_t tree_part;    // float [max_tree * max_D]
@@ -124,6 +132,18 @@ __device__ __forceinline__ void acc_half8(float* acc, uint4 v, float w) {
     acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
     acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
   }
+}
+
+// Eight fp16 values accumulated into fp32 without a weight: f32(h) + acc,
+// rounded once, the same result as converting and then adding.
+__device__ __forceinline__ void add_half8(float* acc, uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
+        : "r"(w[i]));
 }
 
 __device__ __forceinline__ uint4 ldg_u4(const void* p) {

@@ -10,32 +10,35 @@
 // vectors; S = next_pow2(D_t/8) lanes (at most 32) cover one row, so a warp
 // holds G = 32/S lookups of the bag at once and every lane keeps U row
 // vectors in flight.  The G partial sums meet through a shuffle butterfly.
-// Narrow tables therefore do not leave lanes sized for the widest table idle.
+// Narrow tables therefore do not leave lanes sized for the widest table idle;
+// rows wider than 256 values take several 256-column passes.  Unweighted
+// bags accumulate with the mixed-precision add (f16 operand, f32 sum).
 #include "common.cuh"
 #include "internal.h"
 
 namespace tbe {
 namespace {
 
-template <int S, int NC, typename IndexT, bool kWeighted>
-__device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t E, int D,
+// Pool one bag over the row columns [vec0*8, (vec0 + min(S, nvec - vec0))*8):
+// lane sl of each group owns the 16-byte vector vec0 + sl.  Rows wider than
+// 32 vectors (256 fp16) are pooled in several such column passes, so no lane
+// ever holds more than eight accumulators.
+template <int S, typename IndexT, bool kWeighted>
+__device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t E, int D, int vec0,
                                          const IndexT* __restrict__ indices,
                                          const float* __restrict__ psw, int64_t start,
                                          int64_t end, float* __restrict__ out_row,
                                          int* status) {
   constexpr int G = 32 / S;
-  // Row vectors in flight per lane per step: bounded so that U*NC <= 4.
-  constexpr int U0 = 4 / NC > 0 ? 4 / NC : 1;
-  constexpr int U = U0 < S ? U0 : S;
+  constexpr int U = S < 4 ? S : 4;  // row vectors in flight per lane per step
   const int lane = static_cast<int>(lane_id());
   const int g = lane / S;
   const int sl = lane % S;
-  const int nvec = D >> 3;
-  float acc[NC][8];
+  const int vec = vec0 + sl;
+  const bool col_ok = vec < (D >> 3);
+  float acc[8];
 #pragma unroll
-  for (int c = 0; c < NC; ++c)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[c][i] = 0.f;
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   bool bad = false;
 
   for (int64_t base = start; base < end; base += 32) {
@@ -54,25 +57,21 @@ __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t 
 #pragma unroll
     for (int u0 = 0; u0 < S; u0 += U) {
       if (G * u0 >= cnt) break;  // warp-uniform
-      uint4 v[U][NC];
+      uint4 v[U];
       float wv[U];
 #pragma unroll
       for (int uu = 0; uu < U; ++uu) {
         const int k = g + G * (u0 + uu);  // < 32 because u0 + uu < S
         const uint32_t r = __shfl_sync(kFull, my_r, k);
         wv[uu] = kWeighted ? __shfl_sync(kFull, my_w, k) : 1.f;
-        const bool ok = (okmask >> k) & 1u;
-        const __half* row = Wt + static_cast<int64_t>(r) * D;
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          const int vec = sl + c * S;
-          v[uu][c] = (ok && vec < nvec) ? ldg_u4(row + vec * 8) : make_uint4(0, 0, 0, 0);
-        }
+        const bool ok = ((okmask >> k) & 1u) && col_ok;
+        v[uu] = ok ? ldg_u4(Wt + static_cast<int64_t>(r) * D + vec * 8) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int uu = 0; uu < U; ++uu)
-#pragma unroll
-        for (int c = 0; c < NC; ++c) acc_half8(acc[c], v[uu][c], wv[uu]);
+      for (int uu = 0; uu < U; ++uu) {
+        if (kWeighted) acc_half8(acc, v[uu], wv[uu]);
+        else add_half8(acc, v[uu]);
+      }
     }
   }
 
@@ -80,26 +79,18 @@ __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t 
 #pragma unroll
   for (int off = S; off < 32; off <<= 1)
 #pragma unroll
-    for (int c = 0; c < NC; ++c)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[c][i] += __shfl_xor_sync(kFull, acc[c][i], off);
+    for (int i = 0; i < 8; ++i) acc[i] += __shfl_xor_sync(kFull, acc[i], off);
 
-  if (g == 0) {
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const int vec = sl + c * S;
-      if (vec < nvec) {
-        float4* o = reinterpret_cast<float4*>(out_row + vec * 8);
-        __stcs(o, make_float4(acc[c][0], acc[c][1], acc[c][2], acc[c][3]));
-        __stcs(o + 1, make_float4(acc[c][4], acc[c][5], acc[c][6], acc[c][7]));
-      }
-    }
+  if (g == 0 && col_ok) {
+    float4* o = reinterpret_cast<float4*>(out_row + vec * 8);
+    __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
+    __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
   }
   if (status && __any_sync(kFull, bad) && lane == 0) set_status(status, TBE_ERR_INDEX_RANGE);
 }
 
 template <typename IndexT, bool kWeighted>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
     forward_generic_kernel(const __half* __restrict__ W, const int64_t* __restrict__ D_offsets,
                            const int64_t* __restrict__ hash_base,
                            const int64_t* __restrict__ w_offsets,
@@ -122,21 +113,18 @@ __global__ void __launch_bounds__(256)
     float* orow = out + b * total_D + d0;
     const int nvec = D >> 3;
     if (nvec <= 1)
-      pool_bag<1, 1, IndexT, kWeighted>(Wt, E, D, indices, psw, s, e, orow, status);
+      pool_bag<1, IndexT, kWeighted>(Wt, E, D, 0, indices, psw, s, e, orow, status);
     else if (nvec <= 2)
-      pool_bag<2, 1, IndexT, kWeighted>(Wt, E, D, indices, psw, s, e, orow, status);
+      pool_bag<2, IndexT, kWeighted>(Wt, E, D, 0, indices, psw, s, e, orow, status);
     else if (nvec <= 4)
-      pool_bag<4, 1, IndexT, kWeighted>(Wt, E, D, indices, psw, s, e, orow, status);
+      pool_bag<4, IndexT, kWeighted>(Wt, E, D, 0, indices, psw, s, e, orow, status);
     else if (nvec <= 8)
-      pool_bag<8, 1, IndexT, kWeighted>(Wt, E, D, indices, psw, s, e, orow, status);
+      pool_bag<8, IndexT, kWeighted>(Wt, E, D, 0, indices, psw, s, e, orow, status);
     else if (nvec <= 16)
-      pool_bag<16, 1, IndexT, kWeighted>(Wt, E, D, indices, psw, s, e, orow, status);
-    else if (nvec <= 32)
-      pool_bag<32, 1, IndexT, kWeighted>(Wt, E, D, indices, psw, s, e, orow, status);
-    else if (nvec <= 64)
-      pool_bag<32, 2, IndexT, kWeighted>(Wt, E, D, indices, psw, s, e, orow, status);
+      pool_bag<16, IndexT, kWeighted>(Wt, E, D, 0, indices, psw, s, e, orow, status);
     else
-      pool_bag<32, 4, IndexT, kWeighted>(Wt, E, D, indices, psw, s, e, orow, status);
+      for (int vec0 = 0; vec0 < nvec; vec0 += 32)
+        pool_bag<32, IndexT, kWeighted>(Wt, E, D, vec0, indices, psw, s, e, orow, status);
   }
 }
 

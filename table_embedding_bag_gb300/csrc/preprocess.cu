@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(1024)
   if (sum_out && threadIdx.x == 0) *sum_out = agg;
 }
 
+template <bool kWeighted>
 struct DownSmem {
   uint32_t run_off[1 << kMaxRadixBits];              // next output position per digit
   uint32_t tile_cnt[1 << kMaxRadixBits];
@@ -155,12 +156,12 @@ struct DownSmem {
   uint32_t wcnt[kSortThreads / 32][1 << kMaxRadixBits];
   uint32_t keys[kSortTile];
   uint32_t vals[kSortTile];
-  float psw[kSortTile];
+  float psw[kWeighted ? kSortTile : 1];
   uint32_t scan[33];
 };
 
 template <bool kWeighted>
-__global__ void __launch_bounds__(kSortThreads)
+__global__ void __launch_bounds__(kSortThreads, 3)
     radix_downsweep_kernel(const uint32_t* __restrict__ keys_in,
                            const uint32_t* __restrict__ vals_in,
                            const float* __restrict__ psw_in, uint32_t* __restrict__ keys_out,
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(kSortThreads)
                            int64_t n, SortGeom g, int shift, int width,
                            const uint32_t* __restrict__ counts) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  DownSmem& sm = *reinterpret_cast<DownSmem*>(smem_raw);
+  DownSmem<kWeighted>& sm = *reinterpret_cast<DownSmem<kWeighted>*>(smem_raw);
   const int nd = 1 << width;
   const uint32_t mask = static_cast<uint32_t>(nd - 1);
   const int warp = threadIdx.x >> 5;
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kSortThreads)
     // Rank this warp's 512 keys (16 rounds of 32 consecutive keys) stably
     // among keys of the same digit within the warp.
     uint32_t key[kSortItems];
-    uint32_t rank[kSortItems];
+    uint32_t rank[kSortItems / 2];  // two 16-bit ranks per word (a rank is below 512)
 #pragma unroll
     for (int r = 0; r < kSortItems; ++r) {
       const int p = warp * (kSortItems * 32) + r * 32 + static_cast<int>(lane);
@@ -200,7 +201,8 @@ __global__ void __launch_bounds__(kSortThreads)
       __syncwarp();
       if (lane == 31u - __clz(peers)) sm.wcnt[warp][d] = before + __popc(peers);
       __syncwarp();
-      rank[r] = before + __popc(peers & lt_mask);
+      const uint32_t rk = before + __popc(peers & lt_mask);
+      if (r & 1) rank[r >> 1] |= rk << 16; else rank[r >> 1] = rk;
     }
     __syncthreads();
     // Exclusive prefix over warps per digit, and the tile's digit counts.
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(kSortThreads)
     for (int r = 0; r < kSortItems; ++r) {
       const int p = warp * (kSortItems * 32) + r * 32 + static_cast<int>(lane);
       const uint32_t d = (key[r] >> shift) & mask;
-      const uint32_t pos = sm.tile_start[d] + sm.wcnt[warp][d] + rank[r];
+      const uint32_t pos = sm.tile_start[d] + sm.wcnt[warp][d] + ((rank[r >> 1] >> (16 * (r & 1))) & 0xffffu);
       sm.keys[pos] = key[r];
       if (p < valid) {
         sm.vals[pos] = __ldg(vals_in + tb + p);
@@ -493,6 +495,36 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Processing order of the long-run chunks: binned by the first bag each
+// chunk gathers (counting sort over bag bands; order within a band is free).
+__global__ void __launch_bounds__(256)
+    chunk_band_count_kernel(const uint32_t* __restrict__ counters,
+                            const uint32_t* __restrict__ chunk_task,
+                            const uint32_t* __restrict__ long_run,
+                            const uint32_t* __restrict__ long_chunk0,
+                            const uint32_t* __restrict__ run_pairs,
+                            const uint32_t* __restrict__ pair_bags, int band_shift,
+                            uint32_t* __restrict__ chunk_band, uint32_t* __restrict__ band_count) {
+  const uint32_t nchunks = counters[kCntChunks];
+  for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < nchunks; q += gridDim.x * blockDim.x) {
+    const uint32_t k = chunk_task[q];
+    const uint32_t first = run_pairs[long_run[k]] + (q - long_chunk0[k]) * kChunk;
+    uint32_t band = pair_bags[first] >> band_shift;
+    band = band < kBagBands ? band : kBagBands - 1;
+    chunk_band[q] = band;
+    atomicAdd(&band_count[band], 1u);
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    chunk_band_scatter_kernel(const uint32_t* __restrict__ counters,
+                              const uint32_t* __restrict__ chunk_band,
+                              uint32_t* __restrict__ band_cursor, uint32_t* __restrict__ chunk_order) {
+  const uint32_t nchunks = counters[kCntChunks];
+  for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < nchunks; q += gridDim.x * blockDim.x)
+    chunk_order[atomicAdd(&band_cursor[chunk_band[q]], 1u)] = q;
+}
+
 int key_bits(const tbe_desc* d) {
   // keys range over [0, total_E], total_E being the invalid-lookup key
   const uint64_t maxkey = static_cast<uint64_t>(d->total_E);
@@ -501,10 +533,10 @@ int key_bits(const tbe_desc* d) {
   return bits < 1 ? 1 : bits;
 }
 
-SortGeom sort_geom(int64_t n, int num_sms) {
+SortGeom sort_geom(int64_t n, int num_sms, int per_sm = 2) {
   SortGeom g;
   g.tiles = (n + kSortTile - 1) / kSortTile;
-  int64_t ctas = 2LL * num_sms;
+  int64_t ctas = static_cast<int64_t>(per_sm) * num_sms;
   if (ctas > kMaxSortCtas) ctas = kMaxSortCtas;
   if (ctas > g.tiles) ctas = g.tiles;
   if (ctas < 1) ctas = 1;
@@ -557,12 +589,12 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     fill_tail_kernel<IndexT><<<64, 256, 0, s>>>(offsets, nbags, n, sentinel, keys[0], vals[0],
                                                 pw[0]);
 
-    const SortGeom g = sort_geom(n, L.num_sms);
+    const SortGeom g = sort_geom(n, L.num_sms, 3);
     const int bits = key_bits(d);
     const int passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
     const int rb = (bits + passes - 1) / passes;
     uint32_t* counts = reinterpret_cast<uint32_t*>(ws + W.radix_counts);
-    const size_t smem = sizeof(DownSmem);
+    const size_t smem = weighted ? sizeof(DownSmem<true>) : sizeof(DownSmem<false>);
     for (int p = 0; p < passes; ++p) {
       const int shift = p * rb;
       const int width = rb < bits - shift ? rb : bits - shift;
@@ -580,14 +612,15 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
             counts);
     }
     const int fin = passes & 1;
+    const SortGeom gr = sort_geom(n, L.num_sms, 6);
     uint32_t* cta_runs = reinterpret_cast<uint32_t*>(ws + W.cta_counts);
     uint32_t* cta_pairs = cta_runs + (kMaxSortCtas + 1);
-    rle_count_kernel<<<g.ctas, kRleThreads, 0, s>>>(keys[fin], vals[fin], n, g, sentinel, cta_runs,
-                                                    cta_pairs);
-    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_runs, g.ctas, cta_runs + g.ctas);
-    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_pairs, g.ctas, cta_pairs + g.ctas);
-    rle_write_kernel<<<g.ctas, kRleThreads, 0, s>>>(
-        keys[fin], vals[fin], n, g, sentinel, cta_runs, cta_pairs, uk, rs,
+    rle_count_kernel<<<gr.ctas, kRleThreads, 0, s>>>(keys[fin], vals[fin], n, gr, sentinel,
+                                                     cta_runs, cta_pairs);
+    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_runs, gr.ctas, cta_runs + gr.ctas);
+    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_pairs, gr.ctas, cta_pairs + gr.ctas);
+    rle_write_kernel<<<gr.ctas, kRleThreads, 0, s>>>(
+        keys[fin], vals[fin], n, gr, sentinel, cta_runs, cta_pairs, uk, rs,
         reinterpret_cast<uint32_t*>(ws + W.run_pairs),
         reinterpret_cast<uint32_t*>(ws + W.pair_starts),
         reinterpret_cast<uint32_t*>(ws + W.pair_bags), counters);
@@ -611,6 +644,23 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
         reinterpret_cast<uint32_t*>(ws + W.long_tree0),
         reinterpret_cast<uint32_t*>(ws + W.chunk_task),
         reinterpret_cast<uint32_t*>(ws + W.tree_cnt));
+    int band_shift = 0;
+    while ((static_cast<int64_t>(d->B - 1) >> band_shift) >= kBagBands) ++band_shift;
+    uint32_t* band_count = reinterpret_cast<uint32_t*>(ws + W.band_count);
+    err = cudaMemsetAsync(band_count, 0, kBagBands * sizeof(uint32_t), s);
+    if (err != cudaSuccess) return err;
+    int64_t cb = (W.max_chunks + 255) / 256;
+    if (cb > 8LL * L.num_sms) cb = 8LL * L.num_sms;
+    if (cb < 1) cb = 1;
+    chunk_band_count_kernel<<<static_cast<unsigned>(cb), 256, 0, s>>>(
+        counters, reinterpret_cast<uint32_t*>(ws + W.chunk_task),
+        reinterpret_cast<uint32_t*>(ws + W.long_run), reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
+        reinterpret_cast<uint32_t*>(ws + W.run_pairs), reinterpret_cast<uint32_t*>(ws + W.pair_bags),
+        band_shift, reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count);
+    exclusive_scan_kernel<<<1, 1024, 0, s>>>(band_count, kBagBands, nullptr);
+    chunk_band_scatter_kernel<<<static_cast<unsigned>(cb), 256, 0, s>>>(
+        counters, reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count,
+        reinterpret_cast<uint32_t*>(ws + W.chunk_order));
   }
   return cudaGetLastError();
 }
@@ -623,12 +673,13 @@ int radix_passes(const tbe_desc* d) {
 }
 
 cudaError_t prepare_preprocess_kernels() {
-  const int smem = static_cast<int>(sizeof(DownSmem));
   cudaError_t e = cudaFuncSetAttribute(radix_downsweep_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(DownSmem<true>)));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(radix_downsweep_kernel<false>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(sizeof(DownSmem<false>)));
 }
 
 cudaError_t launch_preprocess(const Launch& L, const WsLayout& W, char* ws, const void* indices,

@@ -56,6 +56,7 @@ struct UpdArgs {
   const uint32_t* long_chunk0;
   const uint32_t* long_tree0;
   const uint32_t* chunk_task;
+  const uint32_t* chunk_order;
   uint32_t* tree_cnt;
   float* partials;
   float* tree_part;
@@ -395,7 +396,8 @@ template <bool kWeighted>
 __global__ void __launch_bounds__(256) long_chunks_kernel(UpdArgs a, bool two_launch) {
   const uint32_t nchunks = a.counters[kCntChunks];
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
-  for (uint32_t q = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; q < nchunks; q += warps) {
+  for (uint32_t qi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; qi < nchunks; qi += warps) {
+    const uint32_t q = a.chunk_order[qi];
     const uint32_t k = a.chunk_task[q];
     const uint32_t key = a.unique_keys[a.long_run[k]];
     const int t = find_table(a.hash_base, a.T, static_cast<int64_t>(key));
@@ -474,6 +476,7 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   a.long_chunk0 = reinterpret_cast<const uint32_t*>(ws + W.long_chunk0);
   a.long_tree0 = reinterpret_cast<const uint32_t*>(ws + W.long_tree0);
   a.chunk_task = reinterpret_cast<const uint32_t*>(ws + W.chunk_task);
+  a.chunk_order = reinterpret_cast<const uint32_t*>(ws + W.chunk_order);
   a.tree_cnt = reinterpret_cast<uint32_t*>(ws + W.tree_cnt);
   a.partials = reinterpret_cast<float*>(ws + W.partials);
   a.tree_part = reinterpret_cast<float*>(ws + W.tree_part);
