@@ -37,9 +37,13 @@ def _stale(target, inputs):
     return any(os.path.getmtime(p) > t for p in inputs)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every .cu in parallel, then link the shared library."""
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib=None, objdir=None) -> str:
+    """Compile every .cu in parallel, then link the shared library (by default
+    libtbe.so in the package; `lib`/`objdir` redirect a build with other
+    `extra_flags`, e.g. -DTBE_CHUNK_PAIRS=512)."""
     nvcc = _nvcc()
+    LIB = lib or globals()["LIB"]
+    OBJDIR = objdir or globals()["OBJDIR"]
     os.makedirs(OBJDIR, exist_ok=True)
     deps = _deps()
     jobs = []

@@ -9,6 +9,32 @@
 
 #include "tbe.h"
 
+// Build-time tuning knobs (defaults are the measured choices on GB300):
+//   TBE_CHUNK_PAIRS   pairs per long-run chunk and the long-run threshold
+//   TBE_LONG_VECS     row vectors in flight per lane on long-run chunks
+//   TBE_LONG_MINB     resident CTAs per SM the long-run kernel is built for
+//   TBE_SHORT_VECS    row vectors in flight per lane on short runs
+//   TBE_FWD_UNROLL    row vectors in flight per lane in the forward
+//   TBE_SHORT_MINB, TBE_FWD_MINB  resident CTAs per SM for those kernels
+#ifndef TBE_SHORT_MINB
+#define TBE_SHORT_MINB 3
+#endif
+#ifndef TBE_FWD_MINB
+#define TBE_FWD_MINB 5
+#endif
+#ifndef TBE_LONG_VECS
+#define TBE_LONG_VECS 8
+#endif
+#ifndef TBE_LONG_MINB
+#define TBE_LONG_MINB 3
+#endif
+#ifndef TBE_SHORT_VECS
+#define TBE_SHORT_VECS 4
+#endif
+#ifndef TBE_FWD_UNROLL
+#define TBE_FWD_UNROLL 4
+#endif
+
 namespace tbe {
 
 constexpr unsigned kFull = 0xffffffffu;
@@ -16,10 +42,14 @@ constexpr unsigned kFull = 0xffffffffu;
 // Work threshold from which a run takes the chunked (cooperative) path and
 // the work per chunk.  Work is counted in distinct (row, bag) pairs: every
 // lookup of a bag into the same row shares one gradient-row gather.  The
-// FBTriton backward uses 256 lookups for both; they stay equal here, so a
-// long run always has at least one full chunk.
-constexpr int kLongThreshold = 256;
-constexpr int kChunk = 256;
+// FBTriton backward uses 256 lookups for both; here both are 128 pairs (the
+// fastest on GB300 in a sweep of 128/256/512), and they stay equal, so a long
+// run always has at least one full chunk.
+#ifndef TBE_CHUNK_PAIRS
+#define TBE_CHUNK_PAIRS 128
+#endif
+constexpr int kLongThreshold = TBE_CHUNK_PAIRS;
+constexpr int kChunk = TBE_CHUNK_PAIRS;
 // Fan-in of the last-arriver reduction tree over a long run's chunk partials.
 constexpr int kFanIn = 32;
 // Widest supported table row (elements); rows are moved in 16-byte vectors.
@@ -67,9 +97,10 @@ struct WsLayout {
   size_t long_run;     // uint32 [max_long]
   size_t long_chunk0;  // uint32 [max_long] first chunk of each long run
   size_t long_tree0;   // uint32 [max_long] first tree node of each long run
-  size_t chunk_task;   // uint32 [max_chunks] long run of each chunk
+  size_t long_info;    // LongRunInfo [max_long]
+  size_t chunk_desc;   // ChunkDesc [max_chunks], chunk-id order
   size_t chunk_band;   // uint32 [max_chunks] bag band of each chunk
-  size_t chunk_order;  // uint32 [max_chunks] chunks sorted by bag band
+  size_t chunk_order;  // ChunkDesc [max_chunks], sorted by bag band
   size_t band_count;   // uint32 [kBagBands] chunks per band, then band cursors
   size_t tree_cnt;     // uint32 [max_tree] arrivals still expected at each tree node
   size_t partials;     // float [max_chunks * max_D]
@@ -80,6 +111,29 @@ struct WsLayout {
   int64_t max_long, max_chunks, max_tree;
   bool weighted;
 };
+
+// One chunk of a long run: pairs [first, end) of long run `run`, chunk index c.
+struct __align__(16) ChunkDesc {
+  uint32_t first, end, run, c;
+};
+
+// One long run: its key and table, chunk count, first chunk slot and first
+// reduction-tree node.
+struct __align__(16) LongRunInfo {
+  uint32_t key, table, nch, chunk0, tree0, pad0, pad1, pad2;
+};
+
+// Lanes per gradient row for the update kernels (fp32 rows moved as float4,
+// nv = D/4 vectors): small rows take next_pow2(nv) lanes; wider rows give each
+// lane up to four vectors so that a warp serves several runs at once.
+__host__ __device__ inline int update_lanes(int nv) {
+  int p = 1;
+  while (p < nv) p <<= 1;
+  if (p <= 8) return p;
+  int S = p / 4;
+  if (S < 8) S = 8;
+  return S > 32 ? 32 : S;
+}
 
 // Number of reduction-tree nodes above nch leaves (the root included when
 // nch > 1): levels ceil(nch/F), ceil(ceil(nch/F)/F), ... down to 1.

@@ -19,23 +19,32 @@
 namespace tbe {
 namespace {
 
+// A row of zeros (kMaxD fp16 values): the gather target of lookups that are
+// out of range or past a bag's end.  Static device memory is zero at module
+// load and nothing writes it.
+__device__ __align__(16) uint4 g_zero_row[kMaxD / 8];
+
 // Pool one bag over the row columns [vec0*8, (vec0 + min(S, nvec - vec0))*8):
 // lane sl of each group owns the 16-byte vector vec0 + sl.  Rows wider than
 // 32 vectors (256 fp16) are pooled in several such column passes, so no lane
-// ever holds more than eight accumulators.
+// ever holds more than eight accumulators.  The lane that loads a lookup's
+// index resolves it to a row address once; a lookup that is out of range or
+// past the bag's end resolves to a row of zeros, so the gather loop has no
+// per-lookup branch (a skipped lookup also gets weight 0).
 template <int S, typename IndexT, bool kWeighted>
 __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t E, int D, int vec0,
                                          const IndexT* __restrict__ indices,
                                          const float* __restrict__ psw, int64_t start,
-                                         int64_t end, float* __restrict__ out_row,
-                                         int* status) {
+                                         int64_t end, float* __restrict__ out_row, int* status) {
   constexpr int G = 32 / S;
-  constexpr int U = S < 4 ? S : 4;  // row vectors in flight per lane per step
+  constexpr int U = S < TBE_FWD_UNROLL ? S : TBE_FWD_UNROLL;  // row vectors in flight per lane
   const int lane = static_cast<int>(lane_id());
   const int g = lane / S;
   const int sl = lane % S;
   const int vec = vec0 + sl;
   const bool col_ok = vec < (D >> 3);
+  // lanes past the row's last vector read the row's first one and drop it
+  const int col = col_ok ? vec * 8 : 0;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -43,17 +52,20 @@ __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t 
 
   for (int64_t base = start; base < end; base += 32) {
     const int cnt = static_cast<int>(end - base < 32 ? end - base : 32);
-    uint32_t my_r = 0;
-    float my_w = 1.f;
-    bool my_ok = false;
+    const __half* my_row = reinterpret_cast<const __half*>(g_zero_row);
+    float my_w = 0.f;
     if (lane < cnt) {
       const int64_t r = load_index(indices, base + lane);
-      my_ok = r >= 0 && r < E;
-      bad |= !my_ok;
-      my_r = my_ok ? static_cast<uint32_t>(r) : 0u;
-      if (kWeighted) my_w = __ldg(psw + base + lane);
+      const bool ok = r >= 0 && r < E;
+      bad |= !ok;
+      if (ok) {
+        my_row = Wt + r * D;
+        if (kWeighted) my_w = __ldg(psw + base + lane);
+      }
     }
-    const unsigned okmask = __ballot_sync(kFull, my_ok);
+    const uint64_t my_addr = reinterpret_cast<uint64_t>(my_row);
+    const uint32_t my_lo = static_cast<uint32_t>(my_addr);
+    const uint32_t my_hi = static_cast<uint32_t>(my_addr >> 32);
 #pragma unroll
     for (int u0 = 0; u0 < S; u0 += U) {
       if (G * u0 >= cnt) break;  // warp-uniform
@@ -62,10 +74,10 @@ __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t 
 #pragma unroll
       for (int uu = 0; uu < U; ++uu) {
         const int k = g + G * (u0 + uu);  // < 32 because u0 + uu < S
-        const uint32_t r = __shfl_sync(kFull, my_r, k);
-        wv[uu] = kWeighted ? __shfl_sync(kFull, my_w, k) : 1.f;
-        const bool ok = ((okmask >> k) & 1u) && col_ok;
-        v[uu] = ok ? ldg_u4(Wt + static_cast<int64_t>(r) * D + vec * 8) : make_uint4(0, 0, 0, 0);
+        const uint64_t a = static_cast<uint64_t>(__shfl_sync(kFull, my_lo, k)) |
+                           (static_cast<uint64_t>(__shfl_sync(kFull, my_hi, k)) << 32);
+        if (kWeighted) wv[uu] = __shfl_sync(kFull, my_w, k);
+        v[uu] = ldg_u4(reinterpret_cast<const __half*>(a) + col);
       }
 #pragma unroll
       for (int uu = 0; uu < U; ++uu) {
@@ -90,7 +102,7 @@ __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t 
 }
 
 template <typename IndexT, bool kWeighted>
-__global__ void __launch_bounds__(256, 4)
+__global__ void __launch_bounds__(256, TBE_FWD_MINB)
     forward_generic_kernel(const __half* __restrict__ W, const int64_t* __restrict__ D_offsets,
                            const int64_t* __restrict__ hash_base,
                            const int64_t* __restrict__ w_offsets,

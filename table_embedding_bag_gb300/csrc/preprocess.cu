@@ -399,14 +399,6 @@ __global__ void __launch_bounds__(kRleThreads)
 }
 
 // ---------------------------------------------------------------- classify
-__device__ __forceinline__ int short_groups(int D) {
-  // lanes per row for fp32 gradient rows moved as float4: next_pow2(D/4), at most 32
-  const int nv = D >> 2;
-  int S = 1;
-  while (S < nv && S < 32) S <<= 1;
-  return 32 / S;
-}
-
 // One CTA: first run of every table (binary search of its first key among
 // the unique keys) and the prefix of short-run warp tasks per table.
 __global__ void __launch_bounds__(1024)
@@ -432,7 +424,7 @@ __global__ void __launch_bounds__(1024)
     uint32_t c = 0;
     if (t < T) {
       const int D = static_cast<int>(__ldg(D_offsets + t + 1) - __ldg(D_offsets + t));
-      const int G = short_groups(D);
+      const int G = 32 / update_lanes(D >> 2);
       c = (table_runs[t + 1] - table_runs[t] + G - 1) / G;
     }
     uint32_t total;
@@ -465,22 +457,49 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// One warp per long run: chunk -> run map, and the arrival counters of the
-// run's reduction tree (children per node).
+// One warp per long run: its info record, the descriptors of its chunks, and
+// the arrival counters of its reduction tree (children per node).
 __global__ void __launch_bounds__(256)
     chunk_fill_kernel(const uint32_t* __restrict__ run_pairs, const uint32_t* __restrict__ counters,
+                      const uint32_t* __restrict__ unique_keys,
+                      const int64_t* __restrict__ hash_base, int T,
                       const uint32_t* __restrict__ long_run, const uint32_t* __restrict__ long_chunk0,
-                      const uint32_t* __restrict__ long_tree0, uint32_t* __restrict__ chunk_task,
-                      uint32_t* __restrict__ tree_cnt) {
+                      const uint32_t* __restrict__ long_tree0, LongRunInfo* __restrict__ info,
+                      ChunkDesc* __restrict__ chunk_desc, uint32_t* __restrict__ tree_cnt) {
   const uint32_t nlong = counters[kCntLong];
   const unsigned lane = lane_id();
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   for (uint32_t k = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; k < nlong; k += warps) {
     const uint32_t j = long_run[k];
-    const uint32_t SL = run_pairs[j + 1] - run_pairs[j];
-    const uint32_t nch = (SL + kChunk - 1) / kChunk;
+    const uint32_t p0 = run_pairs[j];
+    const uint32_t np = run_pairs[j + 1] - p0;
+    const uint32_t nch = (np + kChunk - 1) / kChunk;
     const uint32_t c0 = long_chunk0[k];
-    for (uint32_t c = lane; c < nch; c += 32) chunk_task[c0 + c] = k;
+    const uint32_t key = unique_keys[j];
+    if (lane == 0) {
+      int lo = 0, hi = T - 1;  // table of the key
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(hash_base + mid) <= static_cast<int64_t>(key)) lo = mid; else hi = mid - 1;
+      }
+      LongRunInfo r;
+      r.key = key;
+      r.table = static_cast<uint32_t>(lo);
+      r.nch = nch;
+      r.chunk0 = c0;
+      r.tree0 = long_tree0[k];
+      r.pad0 = j;
+      r.pad1 = r.pad2 = 0;
+      info[k] = r;
+    }
+    for (uint32_t c = lane; c < nch; c += 32) {
+      ChunkDesc cd;
+      cd.first = p0 + c * kChunk;
+      cd.end = cd.first + kChunk < p0 + np ? cd.first + kChunk : p0 + np;
+      cd.run = k;
+      cd.c = c;
+      chunk_desc[c0 + c] = cd;
+    }
     uint32_t node = long_tree0[k];
     uint32_t below = nch;
     while (below > 1) {
@@ -499,17 +518,12 @@ __global__ void __launch_bounds__(256)
 // chunk gathers (counting sort over bag bands; order within a band is free).
 __global__ void __launch_bounds__(256)
     chunk_band_count_kernel(const uint32_t* __restrict__ counters,
-                            const uint32_t* __restrict__ chunk_task,
-                            const uint32_t* __restrict__ long_run,
-                            const uint32_t* __restrict__ long_chunk0,
-                            const uint32_t* __restrict__ run_pairs,
+                            const ChunkDesc* __restrict__ chunk_desc,
                             const uint32_t* __restrict__ pair_bags, int band_shift,
                             uint32_t* __restrict__ chunk_band, uint32_t* __restrict__ band_count) {
   const uint32_t nchunks = counters[kCntChunks];
   for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < nchunks; q += gridDim.x * blockDim.x) {
-    const uint32_t k = chunk_task[q];
-    const uint32_t first = run_pairs[long_run[k]] + (q - long_chunk0[k]) * kChunk;
-    uint32_t band = pair_bags[first] >> band_shift;
+    uint32_t band = pair_bags[chunk_desc[q].first] >> band_shift;
     band = band < kBagBands ? band : kBagBands - 1;
     chunk_band[q] = band;
     atomicAdd(&band_count[band], 1u);
@@ -518,11 +532,12 @@ __global__ void __launch_bounds__(256)
 
 __global__ void __launch_bounds__(256)
     chunk_band_scatter_kernel(const uint32_t* __restrict__ counters,
+                              const ChunkDesc* __restrict__ chunk_desc,
                               const uint32_t* __restrict__ chunk_band,
-                              uint32_t* __restrict__ band_cursor, uint32_t* __restrict__ chunk_order) {
+                              uint32_t* __restrict__ band_cursor, ChunkDesc* __restrict__ chunk_order) {
   const uint32_t nchunks = counters[kCntChunks];
   for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < nchunks; q += gridDim.x * blockDim.x)
-    chunk_order[atomicAdd(&band_cursor[chunk_band[q]], 1u)] = q;
+    chunk_order[atomicAdd(&band_cursor[chunk_band[q]], 1u)] = chunk_desc[q];
 }
 
 int key_bits(const tbe_desc* d) {
@@ -639,10 +654,12 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     if (fb > 8LL * L.num_sms) fb = 8LL * L.num_sms;
     if (fb < 1) fb = 1;
     chunk_fill_kernel<<<static_cast<unsigned>(fb), 256, 0, s>>>(
-        reinterpret_cast<uint32_t*>(ws + W.run_pairs), counters, reinterpret_cast<uint32_t*>(ws + W.long_run),
+        reinterpret_cast<uint32_t*>(ws + W.run_pairs), counters, uk, d->hash_base, d->T,
+        reinterpret_cast<uint32_t*>(ws + W.long_run),
         reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
         reinterpret_cast<uint32_t*>(ws + W.long_tree0),
-        reinterpret_cast<uint32_t*>(ws + W.chunk_task),
+        reinterpret_cast<LongRunInfo*>(ws + W.long_info),
+        reinterpret_cast<ChunkDesc*>(ws + W.chunk_desc),
         reinterpret_cast<uint32_t*>(ws + W.tree_cnt));
     int band_shift = 0;
     while ((static_cast<int64_t>(d->B - 1) >> band_shift) >= kBagBands) ++band_shift;
@@ -653,14 +670,14 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     if (cb > 8LL * L.num_sms) cb = 8LL * L.num_sms;
     if (cb < 1) cb = 1;
     chunk_band_count_kernel<<<static_cast<unsigned>(cb), 256, 0, s>>>(
-        counters, reinterpret_cast<uint32_t*>(ws + W.chunk_task),
-        reinterpret_cast<uint32_t*>(ws + W.long_run), reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
-        reinterpret_cast<uint32_t*>(ws + W.run_pairs), reinterpret_cast<uint32_t*>(ws + W.pair_bags),
-        band_shift, reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count);
+        counters, reinterpret_cast<ChunkDesc*>(ws + W.chunk_desc),
+        reinterpret_cast<uint32_t*>(ws + W.pair_bags), band_shift,
+        reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count);
     exclusive_scan_kernel<<<1, 1024, 0, s>>>(band_count, kBagBands, nullptr);
     chunk_band_scatter_kernel<<<static_cast<unsigned>(cb), 256, 0, s>>>(
-        counters, reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count,
-        reinterpret_cast<uint32_t*>(ws + W.chunk_order));
+        counters, reinterpret_cast<ChunkDesc*>(ws + W.chunk_desc),
+        reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count,
+        reinterpret_cast<ChunkDesc*>(ws + W.chunk_order));
   }
   return cudaGetLastError();
 }

@@ -39,9 +39,10 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   L.long_run = take(L.max_long * 4);
   L.long_chunk0 = take(L.max_long * 4);
   L.long_tree0 = take(L.max_long * 4);
-  L.chunk_task = take(L.max_chunks * 4);
+  L.long_info = take(L.max_long * sizeof(LongRunInfo));
+  L.chunk_desc = take(L.max_chunks * sizeof(ChunkDesc));
   L.chunk_band = take(L.max_chunks * 4);
-  L.chunk_order = take(L.max_chunks * 4);
+  L.chunk_order = take(L.max_chunks * sizeof(ChunkDesc));
   L.band_count = take(kBagBands * 4);
   L.tree_cnt = take(L.max_tree * 4);
   L.partials = take(static_cast<size_t>(L.max_chunks) * d->max_D * 4);

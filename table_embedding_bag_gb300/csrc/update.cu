@@ -5,15 +5,15 @@
 // invert 'which rows did this sample use?'": short runs are handled by one
 // program that gathers, accumulates in registers, updates and plain-stores
 // the row (it owns the row exclusively); long runs are split into chunks
-// that write partial sums; in the fused variant
-// each chunk writes its partial, executes a device-scope fence and decrements
-// the run's remaining count, and only the last chunk to finish updates the
-// row, while the default variant finishes in a second kernel.  Section
-// "Fusion boundaries are also engineering interfaces": per-sample weights
-// scale each contribution before grouping, and the optimizer is the
-// epilogue of the backward.  "HugeCTR DistributedSlotSparseEmbeddingHash
-// backward" (eqicode.com), the Adagrad kernel: the accumulator is updated
-// first and the weight step divides by sqrt(new accumulator) + eps.
+// that write partial sums; in the fused variant each chunk writes its
+// partial, executes a device-scope fence and decrements the run's remaining
+// count, and only the last chunk to finish updates the row, while the
+// default variant finishes in a second kernel.  Section "Fusion boundaries
+// are also engineering interfaces": per-sample weights scale each
+// contribution before grouping, and the optimizer is the epilogue of the
+// backward.  "HugeCTR DistributedSlotSparseEmbeddingHash backward"
+// (eqicode.com), the Adagrad kernel: the accumulator is updated first and the
+// weight step divides by sqrt(new accumulator) + eps.
 //
 // GB300 design:
 //  * work is counted in pairs: the lookups of one run that come from the
@@ -21,9 +21,14 @@
 //    and scales it by the pair's multiplicity (or the sum of its per-sample
 //    weights).  On skewed inputs a hot row is hit many times per bag, and
 //    this removes most of its gathers;
-//  * the gradient rows are fp32; a row of D floats is D/4 float4 vectors on
-//    S = next_pow2(D/4) lanes (at most 32), so one warp serves G = 32/S short
-//    runs of the same table at once (tasks never straddle tables);
+//  * the gradient rows are fp32, moved as float4: a row of D floats is
+//    nv = D/4 vectors on S lanes with NC = nv/S vectors each (update_lanes),
+//    so one warp serves G = 32/S runs of a table at once; a lane keeps up to
+//    8 row vectors in flight on long-run chunks and 4 on short runs, whose
+//    memory latency is hidden by running several of them per warp;
+//  * table metadata sits in shared memory; a short run's weights row and
+//    momentum are fetched at the start, in the shadow of its gradient
+//    gathers; a long-run chunk is one 16-byte descriptor;
 //  * a long run's chunk partials meet in a tree of fan-in 32: the last of a
 //    node's children to arrive (fence, then atomic decrement) sums them in
 //    child order and climbs; the root's last arriver applies the update.  A
@@ -36,6 +41,8 @@
 
 namespace tbe {
 namespace {
+
+constexpr int kSmemTables = 256;  // tables whose metadata is cached in shared memory
 
 struct UpdArgs {
   const float* grad_out;
@@ -52,11 +59,8 @@ struct UpdArgs {
   const uint32_t* counters;
   const uint32_t* table_runs;
   const uint32_t* table_tasks;
-  const uint32_t* long_run;
-  const uint32_t* long_chunk0;
-  const uint32_t* long_tree0;
-  const uint32_t* chunk_task;
-  const uint32_t* chunk_order;
+  const LongRunInfo* long_info;
+  const ChunkDesc* chunk_order;
   uint32_t* tree_cnt;
   float* partials;
   float* tree_part;
@@ -68,13 +72,45 @@ struct UpdArgs {
   float eps;
 };
 
-// Largest t with table_first[t] <= x (table_first has T+1 ascending entries).
-template <typename V>
-__device__ __forceinline__ int find_table(const V* first, int T, V x) {
+// Table metadata, in shared memory when the problem has few enough tables.
+struct Meta {
+  const int64_t* d_off;
+  const int64_t* hb;
+  const int64_t* w_off;
+  const uint32_t* tasks;
+  const uint32_t* runs;
+};
+
+struct MetaSmem {
+  int64_t d_off[kSmemTables + 1];
+  int64_t hb[kSmemTables + 1];
+  int64_t w_off[kSmemTables + 1];
+  uint32_t tasks[kSmemTables + 1];
+  uint32_t runs[kSmemTables + 1];
+};
+
+__device__ __forceinline__ Meta load_meta(const UpdArgs& a, MetaSmem& sm, bool with_tasks) {
+  if (a.T > kSmemTables)
+    return Meta{a.D_offsets, a.hash_base, a.w_offsets, a.table_tasks, a.table_runs};
+  for (int t = threadIdx.x; t <= a.T; t += blockDim.x) {
+    sm.d_off[t] = a.D_offsets[t];
+    sm.hb[t] = a.hash_base[t];
+    sm.w_off[t] = a.w_offsets[t];
+    if (with_tasks) {
+      sm.tasks[t] = a.table_tasks[t];
+      sm.runs[t] = a.table_runs[t];
+    }
+  }
+  __syncthreads();
+  return Meta{sm.d_off, sm.hb, sm.w_off, sm.tasks, sm.runs};
+}
+
+// Largest t with first[t] <= x (first has T+1 ascending entries).
+__device__ __forceinline__ int find_table(const uint32_t* first, int T, uint32_t x) {
   int lo = 0, hi = T - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(first + mid) <= x) lo = mid; else hi = mid - 1;
+    if (first[mid] <= x) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -84,24 +120,61 @@ __device__ __forceinline__ int find_table(const V* first, int T, V x) {
 // lookups or, with per-sample weights, by their sum (in lookup order).
 template <bool kWeighted>
 __device__ __forceinline__ void load_pair(const UpdArgs& a, uint32_t k, uint32_t* bag, float* coef) {
-  const uint32_t s = a.pair_starts[k];
-  const uint32_t e = a.pair_starts[k + 1];
-  *bag = a.pair_bags[k];
+  const uint32_t s = __ldg(a.pair_starts + k);
+  const uint32_t e = __ldg(a.pair_starts + k + 1);
+  *bag = __ldg(a.pair_bags + k);
   if (kWeighted) {
     float c = 0.f;
-    for (uint32_t i = s; i < e; ++i) c += a.sorted_psw[i];
+    for (uint32_t i = s; i < e; ++i) c += __ldg(a.sorted_psw + i);
     *coef = c;
   } else {
     *coef = static_cast<float>(e - s);
   }
 }
 
-// Row-wise Adagrad on one row (key, row r of table t) with the summed
-// gradient held by the S lanes of a group: lane sl owns columns
-// (sl + c*S)*4 .. +3 for c < NC.
+// This lane's vectors of gradient row b (columns d0 + (sl + c*S)*4 ..).
 template <int S, int NC>
-__device__ __forceinline__ void adagrad_row(const UpdArgs& a, float (&g)[NC][4], int D,
-                                            uint32_t key, int t, bool active) {
+__device__ __forceinline__ void gather_row(const UpdArgs& a, int64_t d0, int nv, uint32_t b,
+                                           float4 (&v)[NC], bool ok) {
+  const int sl = static_cast<int>(lane_id()) % S;
+  const float* grow = a.grad_out + static_cast<int64_t>(b) * a.total_D + d0;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int vec = sl + c * S;
+    v[c] = (ok && vec < nv) ? ldg_f4(grow + vec * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+template <int NC>
+__device__ __forceinline__ void fma_rows(float (&acc)[NC][4], const float4 (&v)[NC], float w) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    acc[c][0] = fmaf(w, v[c].x, acc[c][0]);
+    acc[c][1] = fmaf(w, v[c].y, acc[c][1]);
+    acc[c][2] = fmaf(w, v[c].z, acc[c][2]);
+    acc[c][3] = fmaf(w, v[c].w, acc[c][3]);
+  }
+}
+
+template <int S, int NC>
+__device__ __forceinline__ void load_row(const __half* row, int nv, uint2 (&w_raw)[NC], bool active) {
+  const int sl = static_cast<int>(lane_id()) % S;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int vec = sl + c * S;
+    w_raw[c] = (active && vec < nv) ? *reinterpret_cast<const uint2*>(row + vec * 4)
+                                    : make_uint2(0u, 0u);
+  }
+}
+
+// Row-wise Adagrad on one row with the summed gradient held by the S lanes
+// of a group (lane sl owns vectors sl + c*S).  w_raw / m_old are the row's
+// fp16 weights (4 per vector) and momentum, already loaded.  Every lane of
+// the warp must call it (the sum of squares is a group shuffle).
+template <int S, int NC>
+__device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4], int D,
+                                              uint32_t key, __half* row, const uint2 (&w_raw)[NC],
+                                              float m_old, bool active) {
   const int sl = static_cast<int>(lane_id()) % S;
   const int nv = D >> 2;
   float ss = 0.f;
@@ -113,132 +186,135 @@ __device__ __forceinline__ void adagrad_row(const UpdArgs& a, float (&g)[NC][4],
 #pragma unroll
   for (int off = 1; off < S; off <<= 1) ss += __shfl_xor_sync(kFull, ss, off);
   if (!active) return;
-  const float m_new = a.momentum[key] + ss / static_cast<float>(D);
+  const float m_new = m_old + ss / static_cast<float>(D);
   const float denom = sqrtf(m_new) + a.eps;
-  const int64_t r = static_cast<int64_t>(key) - __ldg(a.hash_base + t);
-  __half* row = a.W + __ldg(a.w_offsets + t) + r * D;
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     const int vec = sl + c * S;
     if (vec < nv) {
-      uint2* p = reinterpret_cast<uint2*>(row + vec * 4);
-      uint2 raw = *p;
+      uint2 raw = w_raw[c];
       __half2* h = reinterpret_cast<__half2*>(&raw);
       const float2 w01 = __half22float2(h[0]);
       const float2 w23 = __half22float2(h[1]);
       h[0] = __floats2half2_rn(w01.x - a.lr * g[c][0] / denom, w01.y - a.lr * g[c][1] / denom);
       h[1] = __floats2half2_rn(w23.x - a.lr * g[c][2] / denom, w23.y - a.lr * g[c][3] / denom);
-      *p = raw;
+      *reinterpret_cast<uint2*>(row + vec * 4) = raw;
     }
   }
   if (sl == 0) a.momentum[key] = m_new;
 }
 
 // ------------------------------------------------------------- short runs
+// Group g of the warp owns run j0 + g: its pairs are loaded S at a time, one
+// per lane of the group, and gathered U at a time.
 template <int S, int NC, bool kWeighted>
-__device__ __forceinline__ void short_task(const UpdArgs& a, int t, uint32_t j0, uint32_t j_end) {
-  constexpr int U = 4 / NC > 0 ? (4 / NC < S ? 4 / NC : S) : 1;
+__device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, int t, uint32_t j0,
+                                           uint32_t j_end) {
+  // Row vectors in flight per lane: short runs hold few pairs, so the warp's
+  // G concurrent runs, not a deep unroll, hide the latency.
+  constexpr int U = TBE_SHORT_VECS / NC > 0 ? (TBE_SHORT_VECS / NC < S ? TBE_SHORT_VECS / NC : S) : 1;
   const int lane = static_cast<int>(lane_id());
   const int g = lane / S;
   const int sl = lane % S;
-  const int64_t d0 = __ldg(a.D_offsets + t);
-  const int D = static_cast<int>(__ldg(a.D_offsets + t + 1) - d0);
+  const int64_t d0 = m.d_off[t];
+  const int D = static_cast<int>(m.d_off[t + 1] - d0);
   const int nv = D >> 2;
   const uint32_t j = j0 + g;
-  uint32_t s = 0, SL = 0;  // first pair and pair count of this group's run
+  uint32_t p0 = 0, np = 0;
+  uint32_t key = 0;
   if (j < j_end) {
-    s = a.run_pairs[j];
-    SL = a.run_pairs[j + 1] - s;
-    if (SL >= static_cast<uint32_t>(kLongThreshold)) SL = 0;  // chunked path owns it
+    p0 = __ldg(a.run_pairs + j);
+    np = __ldg(a.run_pairs + j + 1) - p0;
+    key = __ldg(a.unique_keys + j);
+    if (np >= static_cast<uint32_t>(kLongThreshold)) np = 0;  // chunked path owns it
   }
-  const uint32_t max_len = __reduce_max_sync(kFull, SL);
+  const bool active = np > 0;
+  __half* row = a.W + m.w_off[t] + (active ? (static_cast<int64_t>(key) - m.hb[t]) * D : 0);
+  uint2 w_raw[NC];
+  load_row<S, NC>(row, nv, w_raw, active);
+  const float m_old = active ? a.momentum[key] : 0.f;
+  const uint32_t max_np = __reduce_max_sync(kFull, np);
   float acc[NC][4];
 #pragma unroll
   for (int c = 0; c < NC; ++c)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[c][i] = 0.f;
-  for (uint32_t base = 0; base < max_len; base += S) {
+  for (uint32_t base = 0; base < max_np; base += S) {
     uint32_t my_b = 0xffffffffu;
     float my_w = 0.f;
-    if (base + sl < SL) load_pair<kWeighted>(a, s + base + sl, &my_b, &my_w);
+    if (base + sl < np) load_pair<kWeighted>(a, p0 + base + sl, &my_b, &my_w);
 #pragma unroll
     for (int u0 = 0; u0 < S; u0 += U) {
-      if (base + u0 >= max_len) break;  // warp-uniform
+      if (base + u0 >= max_np) break;  // warp-uniform
       float4 v[U][NC];
       float wv[U];
 #pragma unroll
       for (int uu = 0; uu < U; ++uu) {
         const uint32_t b = __shfl_sync(kFull, my_b, u0 + uu, S);
         wv[uu] = __shfl_sync(kFull, my_w, u0 + uu, S);
-        const bool ok = b < static_cast<uint32_t>(a.B);  // also false past the run's end
-        const float* grow = a.grad_out + static_cast<int64_t>(b) * a.total_D + d0;
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          const int vec = sl + c * S;
-          v[uu][c] = (ok && vec < nv) ? ldg_f4(grow + vec * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        gather_row<S, NC>(a, d0, nv, b, v[uu], b < static_cast<uint32_t>(a.B));
       }
 #pragma unroll
-      for (int uu = 0; uu < U; ++uu)
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          acc[c][0] = fmaf(wv[uu], v[uu][c].x, acc[c][0]);
-          acc[c][1] = fmaf(wv[uu], v[uu][c].y, acc[c][1]);
-          acc[c][2] = fmaf(wv[uu], v[uu][c].z, acc[c][2]);
-          acc[c][3] = fmaf(wv[uu], v[uu][c].w, acc[c][3]);
-        }
+      for (int uu = 0; uu < U; ++uu) fma_rows<NC>(acc, v[uu], wv[uu]);
     }
   }
-  const uint32_t key = SL > 0 ? a.unique_keys[j] : 0u;
-  adagrad_row<S, NC>(a, acc, D, key, t, SL > 0);
+  adagrad_apply<S, NC>(a, acc, D, key, row, w_raw, m_old, active);
 }
 
-template <bool kWeighted>
-__global__ void __launch_bounds__(256) short_runs_kernel(UpdArgs a) {
+// kWide: the instantiation for rows wider than 512 values (eight vectors per
+// lane); the other one skips them, so that its register budget stays small.
+template <bool kWeighted, bool kWide>
+__global__ void __launch_bounds__(256, TBE_SHORT_MINB) short_runs_kernel(UpdArgs a) {
+  __shared__ MetaSmem msm;
+  const Meta m = load_meta(a, msm, true);
   const uint32_t ntasks = a.counters[kCntTasks];
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   for (uint32_t task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntasks;
        task += warps) {
-    const int t = find_table(a.table_tasks, a.T, task);
-    const int D = static_cast<int>(__ldg(a.D_offsets + t + 1) - __ldg(a.D_offsets + t));
+    const int t = find_table(m.tasks, a.T, task);
+    const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
     if (D < 8 || D > kMaxD || (D & 7)) continue;  // widths the vector path cannot move
     const int nv = D >> 2;
-    int S = 1;
-    while (S < nv && S < 32) S <<= 1;
+    if ((nv > 128) != kWide) continue;
+    const int S = update_lanes(nv);
     const uint32_t G = 32 / S;
-    const uint32_t j0 = a.table_runs[t] + (task - a.table_tasks[t]) * G;
-    const uint32_t j_end = a.table_runs[t + 1];
-    if (nv <= 2) short_task<2, 1, kWeighted>(a, t, j0, j_end);
-    else if (nv <= 4) short_task<4, 1, kWeighted>(a, t, j0, j_end);
-    else if (nv <= 8) short_task<8, 1, kWeighted>(a, t, j0, j_end);
-    else if (nv <= 16) short_task<16, 1, kWeighted>(a, t, j0, j_end);
-    else if (nv <= 32) short_task<32, 1, kWeighted>(a, t, j0, j_end);
-    else if (nv <= 64) short_task<32, 2, kWeighted>(a, t, j0, j_end);
-    else if (nv <= 128) short_task<32, 4, kWeighted>(a, t, j0, j_end);
-    else short_task<32, 8, kWeighted>(a, t, j0, j_end);
+    const uint32_t j0 = m.runs[t] + (task - m.tasks[t]) * G;
+    const uint32_t j_end = m.runs[t + 1];
+    if (kWide) short_task<32, 8, kWeighted>(a, m, t, j0, j_end);
+    else if (nv <= 2) short_task<2, 1, kWeighted>(a, m, t, j0, j_end);
+    else if (nv <= 4) short_task<4, 1, kWeighted>(a, m, t, j0, j_end);
+    else if (nv <= 8) short_task<8, 1, kWeighted>(a, m, t, j0, j_end);
+    else if (nv <= 16) short_task<8, 2, kWeighted>(a, m, t, j0, j_end);
+    else if (nv <= 32) short_task<8, 4, kWeighted>(a, m, t, j0, j_end);
+    else if (nv <= 64) short_task<16, 4, kWeighted>(a, m, t, j0, j_end);
+    else short_task<32, 4, kWeighted>(a, m, t, j0, j_end);
   }
 }
 
 // -------------------------------------------------------------- long runs
-// Sum pairs [s, e) of one run over the whole warp: group g takes every G-th
-// pair; the groups meet in a butterfly so every lane ends with its columns.
+// Sum pairs [s, e) over the whole warp: group g takes every G-th pair of each
+// batch of 32; the next batch's pair data is fetched while this batch's rows
+// are gathered.  The groups meet in a butterfly so every lane ends with its
+// columns of the sum.
 template <int S, int NC, bool kWeighted>
-__device__ __forceinline__ void sum_lookups(const UpdArgs& a, int64_t d0, int nv, uint32_t s,
-                                            uint32_t e, float (&acc)[NC][4]) {
+__device__ __forceinline__ void sum_pairs(const UpdArgs& a, int64_t d0, int nv, uint32_t s,
+                                          uint32_t e, float (&acc)[NC][4]) {
   constexpr int G = 32 / S;
-  constexpr int U = 4 / NC > 0 ? (4 / NC < S ? 4 / NC : S) : 1;
+  constexpr int U = TBE_LONG_VECS / NC > 0 ? (TBE_LONG_VECS / NC < S ? TBE_LONG_VECS / NC : S) : 1;
   const int lane = static_cast<int>(lane_id());
   const int g = lane / S;
-  const int sl = lane % S;
 #pragma unroll
   for (int c = 0; c < NC; ++c)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[c][i] = 0.f;
+  uint32_t my_b = 0xffffffffu;
+  float my_w = 0.f;
+  if (s + lane < e) load_pair<kWeighted>(a, s + lane, &my_b, &my_w);
   for (uint32_t base = s; base < e; base += 32) {
     const int cnt = static_cast<int>(e - base < 32u ? e - base : 32u);
-    uint32_t my_b = 0xffffffffu;
-    float my_w = 0.f;
-    if (lane < cnt) load_pair<kWeighted>(a, base + lane, &my_b, &my_w);
+    uint32_t nx_b = 0xffffffffu;
+    float nx_w = 0.f;
+    if (base + 32 + lane < e) load_pair<kWeighted>(a, base + 32 + lane, &nx_b, &nx_w);
 #pragma unroll
     for (int u0 = 0; u0 < S; u0 += U) {
       if (G * u0 >= cnt) break;  // warp-uniform
@@ -249,24 +325,13 @@ __device__ __forceinline__ void sum_lookups(const UpdArgs& a, int64_t d0, int nv
         const int k = g + G * (u0 + uu);
         const uint32_t b = __shfl_sync(kFull, my_b, k);
         wv[uu] = __shfl_sync(kFull, my_w, k);
-        const bool ok = b < static_cast<uint32_t>(a.B);
-        const float* grow = a.grad_out + static_cast<int64_t>(b) * a.total_D + d0;
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          const int vec = sl + c * S;
-          v[uu][c] = (ok && vec < nv) ? ldg_f4(grow + vec * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        gather_row<S, NC>(a, d0, nv, b, v[uu], b < static_cast<uint32_t>(a.B));
       }
 #pragma unroll
-      for (int uu = 0; uu < U; ++uu)
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          acc[c][0] = fmaf(wv[uu], v[uu][c].x, acc[c][0]);
-          acc[c][1] = fmaf(wv[uu], v[uu][c].y, acc[c][1]);
-          acc[c][2] = fmaf(wv[uu], v[uu][c].z, acc[c][2]);
-          acc[c][3] = fmaf(wv[uu], v[uu][c].w, acc[c][3]);
-        }
+      for (int uu = 0; uu < U; ++uu) fma_rows<NC>(acc, v[uu], wv[uu]);
     }
+    my_b = nx_b;
+    my_w = nx_w;
   }
 #pragma unroll
   for (int off = S; off < 32; off <<= 1)
@@ -341,50 +406,55 @@ __device__ __forceinline__ bool arrive_last(uint32_t* counter) {
   return prev == 1u;
 }
 
+// The whole warp applies the update of one long run's row (every lane holds
+// the summed gradient; group 0's lanes write).
+template <int S, int NC>
+__device__ __forceinline__ void finish_long_row(const UpdArgs& a, const Meta& m,
+                                                const LongRunInfo& ri, float (&acc)[NC][4]) {
+  const int t = static_cast<int>(ri.table);
+  const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
+  __half* row = a.W + m.w_off[t] + (static_cast<int64_t>(ri.key) - m.hb[t]) * D;
+  const bool writer = static_cast<int>(lane_id()) < S;
+  uint2 w_raw[NC];
+  load_row<S, NC>(row, D >> 2, w_raw, writer);
+  const float m_old = a.momentum[ri.key];
+  adagrad_apply<S, NC>(a, acc, D, ri.key, row, w_raw, m_old, writer);
+}
+
 template <int S, int NC, bool kWeighted>
-__device__ __forceinline__ void long_chunk(const UpdArgs& a, uint32_t q, bool two_launch) {
-  const uint32_t k = a.chunk_task[q];
-  const uint32_t j = a.long_run[k];
-  const uint32_t c = q - a.long_chunk0[k];
-  const uint32_t rs0 = a.run_pairs[j];
-  const uint32_t SL = a.run_pairs[j + 1] - rs0;
-  const uint32_t nch = (SL + kChunk - 1) / kChunk;
-  const uint32_t s = rs0 + c * kChunk;
-  const uint32_t e = s + kChunk < rs0 + SL ? s + kChunk : rs0 + SL;
-  const uint32_t key = a.unique_keys[j];
-  const int t = find_table(a.hash_base, a.T, static_cast<int64_t>(key));
-  const int64_t d0 = __ldg(a.D_offsets + t);
-  const int D = static_cast<int>(__ldg(a.D_offsets + t + 1) - d0);
+__device__ __forceinline__ void long_chunk(const UpdArgs& a, const Meta& m, const ChunkDesc& cd,
+                                           const LongRunInfo& ri, bool two_launch) {
+  const int t = static_cast<int>(ri.table);
+  const int64_t d0 = m.d_off[t];
+  const int D = static_cast<int>(m.d_off[t + 1] - d0);
   const int nv = D >> 2;
   float acc[NC][4];
-  sum_lookups<S, NC, kWeighted>(a, d0, nv, s, e, acc);
-  if (nch == 1 && !two_launch) {
-    adagrad_row<S, NC>(a, acc, D, key, t, true);
+  sum_pairs<S, NC, kWeighted>(a, d0, nv, cd.first, cd.end, acc);
+  if (ri.nch == 1 && !two_launch) {
+    finish_long_row<S, NC>(a, m, ri, acc);
     return;
   }
-  const uint32_t c0 = a.long_chunk0[k];
-  store_partial<S, NC>(a.partials + static_cast<int64_t>(c0 + c) * a.max_D, nv, acc);
+  store_partial<S, NC>(a.partials + static_cast<int64_t>(ri.chunk0 + cd.c) * a.max_D, nv, acc);
   if (two_launch) return;
   // Climb the run's reduction tree while this warp is the last arriver.
-  const uint32_t tree0 = a.long_tree0[k];
   uint32_t level_off = 0;   // first node of the current level within the run's tree
-  uint32_t below = nch;     // nodes on the level below
-  uint32_t i = c / kFanIn;  // node index on the current level
+  uint32_t below = ri.nch;  // nodes on the level below
+  uint32_t i = cd.c / kFanIn;
   for (;;) {
     const uint32_t here = (below + kFanIn - 1) / kFanIn;
-    if (!arrive_last(a.tree_cnt + tree0 + level_off + i)) return;
+    if (!arrive_last(a.tree_cnt + ri.tree0 + level_off + i)) return;
     const uint32_t first = i * kFanIn;
     const uint32_t kids = below - first < static_cast<uint32_t>(kFanIn) ? below - first : kFanIn;
-    const float* src = level_off == 0 && below == nch
-                           ? a.partials + static_cast<int64_t>(c0 + first) * a.max_D
-                           : a.tree_part + static_cast<int64_t>(tree0 + level_off - below + first) *
+    const float* src = level_off == 0 && below == ri.nch
+                           ? a.partials + static_cast<int64_t>(ri.chunk0 + first) * a.max_D
+                           : a.tree_part + static_cast<int64_t>(ri.tree0 + level_off - below + first) *
                                                a.max_D;
     sum_partials<S, NC>(src, a.max_D, kids, nv, acc);
     if (here == 1) {
-      adagrad_row<S, NC>(a, acc, D, key, t, true);
+      finish_long_row<S, NC>(a, m, ri, acc);
       return;
     }
-    store_partial<S, NC>(a.tree_part + static_cast<int64_t>(tree0 + level_off + i) * a.max_D, nv,
+    store_partial<S, NC>(a.tree_part + static_cast<int64_t>(ri.tree0 + level_off + i) * a.max_D, nv,
                          acc);
     level_off += here;
     below = here;
@@ -392,62 +462,64 @@ __device__ __forceinline__ void long_chunk(const UpdArgs& a, uint32_t q, bool tw
   }
 }
 
-template <bool kWeighted>
-__global__ void __launch_bounds__(256) long_chunks_kernel(UpdArgs a, bool two_launch) {
+template <bool kWeighted, bool kWide>
+__global__ void __launch_bounds__(256, TBE_LONG_MINB) long_chunks_kernel(UpdArgs a, bool two_launch) {
+  __shared__ MetaSmem msm;
+  const Meta m = load_meta(a, msm, false);
   const uint32_t nchunks = a.counters[kCntChunks];
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   for (uint32_t qi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; qi < nchunks; qi += warps) {
-    const uint32_t q = a.chunk_order[qi];
-    const uint32_t k = a.chunk_task[q];
-    const uint32_t key = a.unique_keys[a.long_run[k]];
-    const int t = find_table(a.hash_base, a.T, static_cast<int64_t>(key));
-    const int D = static_cast<int>(__ldg(a.D_offsets + t + 1) - __ldg(a.D_offsets + t));
+    const ChunkDesc cd = a.chunk_order[qi];
+    const LongRunInfo ri = a.long_info[cd.run];
+    const int t = static_cast<int>(ri.table);
+    const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
     if (D < 8 || D > kMaxD || (D & 7)) continue;
     const int nv = D >> 2;
-    if (nv <= 2) long_chunk<2, 1, kWeighted>(a, q, two_launch);
-    else if (nv <= 4) long_chunk<4, 1, kWeighted>(a, q, two_launch);
-    else if (nv <= 8) long_chunk<8, 1, kWeighted>(a, q, two_launch);
-    else if (nv <= 16) long_chunk<16, 1, kWeighted>(a, q, two_launch);
-    else if (nv <= 32) long_chunk<32, 1, kWeighted>(a, q, two_launch);
-    else if (nv <= 64) long_chunk<32, 2, kWeighted>(a, q, two_launch);
-    else if (nv <= 128) long_chunk<32, 4, kWeighted>(a, q, two_launch);
-    else long_chunk<32, 8, kWeighted>(a, q, two_launch);
+    if ((nv > 128) != kWide) continue;
+    if (kWide) long_chunk<32, 8, kWeighted>(a, m, cd, ri, two_launch);
+    else if (nv <= 2) long_chunk<2, 1, kWeighted>(a, m, cd, ri, two_launch);
+    else if (nv <= 4) long_chunk<4, 1, kWeighted>(a, m, cd, ri, two_launch);
+    else if (nv <= 8) long_chunk<8, 1, kWeighted>(a, m, cd, ri, two_launch);
+    else if (nv <= 16) long_chunk<8, 2, kWeighted>(a, m, cd, ri, two_launch);
+    else if (nv <= 32) long_chunk<8, 4, kWeighted>(a, m, cd, ri, two_launch);
+    else if (nv <= 64) long_chunk<16, 4, kWeighted>(a, m, cd, ri, two_launch);
+    else long_chunk<32, 4, kWeighted>(a, m, cd, ri, two_launch);
   }
 }
 
 // Two-launch variant, second kernel: one warp per long run sums the run's
 // chunk partials in chunk order and applies the update.
 template <int S, int NC>
-__device__ __forceinline__ void finish_run(const UpdArgs& a, uint32_t k) {
-  const uint32_t j = a.long_run[k];
-  const uint32_t SL = a.run_pairs[j + 1] - a.run_pairs[j];
-  const uint32_t nch = (SL + kChunk - 1) / kChunk;
-  const uint32_t key = a.unique_keys[j];
-  const int t = find_table(a.hash_base, a.T, static_cast<int64_t>(key));
-  const int D = static_cast<int>(__ldg(a.D_offsets + t + 1) - __ldg(a.D_offsets + t));
+__device__ __forceinline__ void finish_run(const UpdArgs& a, const Meta& m, const LongRunInfo& ri) {
+  const int t = static_cast<int>(ri.table);
+  const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
   float acc[NC][4];
-  sum_partials<S, NC>(a.partials + static_cast<int64_t>(a.long_chunk0[k]) * a.max_D, a.max_D, nch,
+  sum_partials<S, NC>(a.partials + static_cast<int64_t>(ri.chunk0) * a.max_D, a.max_D, ri.nch,
                       D >> 2, acc);
-  adagrad_row<S, NC>(a, acc, D, key, t, true);
+  finish_long_row<S, NC>(a, m, ri, acc);
 }
 
-__global__ void __launch_bounds__(256) long_finish_kernel(UpdArgs a) {
+template <bool kWide>
+__global__ void __launch_bounds__(256, 3) long_finish_kernel(UpdArgs a) {
+  __shared__ MetaSmem msm;
+  const Meta m = load_meta(a, msm, false);
   const uint32_t nlong = a.counters[kCntLong];
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   for (uint32_t k = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; k < nlong; k += warps) {
-    const uint32_t key = a.unique_keys[a.long_run[k]];
-    const int t = find_table(a.hash_base, a.T, static_cast<int64_t>(key));
-    const int D = static_cast<int>(__ldg(a.D_offsets + t + 1) - __ldg(a.D_offsets + t));
+    const LongRunInfo ri = a.long_info[k];
+    const int t = static_cast<int>(ri.table);
+    const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
     if (D < 8 || D > kMaxD || (D & 7)) continue;
     const int nv = D >> 2;
-    if (nv <= 2) finish_run<2, 1>(a, k);
-    else if (nv <= 4) finish_run<4, 1>(a, k);
-    else if (nv <= 8) finish_run<8, 1>(a, k);
-    else if (nv <= 16) finish_run<16, 1>(a, k);
-    else if (nv <= 32) finish_run<32, 1>(a, k);
-    else if (nv <= 64) finish_run<32, 2>(a, k);
-    else if (nv <= 128) finish_run<32, 4>(a, k);
-    else finish_run<32, 8>(a, k);
+    if ((nv > 128) != kWide) continue;
+    if (kWide) finish_run<32, 8>(a, m, ri);
+    else if (nv <= 2) finish_run<2, 1>(a, m, ri);
+    else if (nv <= 4) finish_run<4, 1>(a, m, ri);
+    else if (nv <= 8) finish_run<8, 1>(a, m, ri);
+    else if (nv <= 16) finish_run<8, 2>(a, m, ri);
+    else if (nv <= 32) finish_run<8, 4>(a, m, ri);
+    else if (nv <= 64) finish_run<16, 4>(a, m, ri);
+    else finish_run<32, 4>(a, m, ri);
   }
 }
 
@@ -472,11 +544,8 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   a.counters = reinterpret_cast<const uint32_t*>(ws + W.counts);
   a.table_runs = reinterpret_cast<const uint32_t*>(ws + W.table_runs);
   a.table_tasks = reinterpret_cast<const uint32_t*>(ws + W.table_tasks);
-  a.long_run = reinterpret_cast<const uint32_t*>(ws + W.long_run);
-  a.long_chunk0 = reinterpret_cast<const uint32_t*>(ws + W.long_chunk0);
-  a.long_tree0 = reinterpret_cast<const uint32_t*>(ws + W.long_tree0);
-  a.chunk_task = reinterpret_cast<const uint32_t*>(ws + W.chunk_task);
-  a.chunk_order = reinterpret_cast<const uint32_t*>(ws + W.chunk_order);
+  a.long_info = reinterpret_cast<const LongRunInfo*>(ws + W.long_info);
+  a.chunk_order = reinterpret_cast<const ChunkDesc*>(ws + W.chunk_order);
   a.tree_cnt = reinterpret_cast<uint32_t*>(ws + W.tree_cnt);
   a.partials = reinterpret_cast<float*>(ws + W.partials);
   a.tree_part = reinterpret_cast<float*>(ws + W.tree_part);
@@ -489,11 +558,19 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   if (L.n == 0) return cudaSuccess;
   const unsigned blocks = static_cast<unsigned>(L.num_sms) * 8u;
   const bool weighted = a.sorted_psw != nullptr;
-  if (weighted) short_runs_kernel<true><<<blocks, 256, 0, L.s>>>(a);
-  else short_runs_kernel<false><<<blocks, 256, 0, L.s>>>(a);
-  if (weighted) long_chunks_kernel<true><<<blocks, 256, 0, L.s>>>(a, two_launch);
-  else long_chunks_kernel<false><<<blocks, 256, 0, L.s>>>(a, two_launch);
-  if (two_launch) long_finish_kernel<<<blocks, 256, 0, L.s>>>(a);
+  const bool wide = d->max_D > 512;  // rows of more than 128 float4 vectors
+  if (weighted) short_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a);
+  else short_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a);
+  if (wide && weighted) short_runs_kernel<true, true><<<blocks, 256, 0, L.s>>>(a);
+  if (wide && !weighted) short_runs_kernel<false, true><<<blocks, 256, 0, L.s>>>(a);
+  if (weighted) long_chunks_kernel<true, false><<<blocks, 256, 0, L.s>>>(a, two_launch);
+  else long_chunks_kernel<false, false><<<blocks, 256, 0, L.s>>>(a, two_launch);
+  if (wide && weighted) long_chunks_kernel<true, true><<<blocks, 256, 0, L.s>>>(a, two_launch);
+  if (wide && !weighted) long_chunks_kernel<false, true><<<blocks, 256, 0, L.s>>>(a, two_launch);
+  if (two_launch) {
+    long_finish_kernel<false><<<blocks, 256, 0, L.s>>>(a);
+    if (wide) long_finish_kernel<true><<<blocks, 256, 0, L.s>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -116,10 +116,12 @@ def _lengths(spec: Spec, B: int, g, device):
 
 
 def zipf_cdf(E: int, alpha: float, device):
-    """Cumulative distribution of the truncated Zipf law P(k) ~ k^-alpha, k=1..E."""
-    k = torch.arange(1, E + 1, dtype=torch.float64, device=device)
+    """Cumulative distribution of the truncated Zipf law P(k) ~ k^-alpha, k=1..E.
+    Summed on the host in a fixed order (a parallel device scan may round
+    differently from run to run), then moved to `device`."""
+    k = torch.arange(1, E + 1, dtype=torch.float64)
     c = torch.cumsum(k.pow_(-alpha), 0)
-    return c.div_(c[-1].clone())
+    return c.div_(c[-1].clone()).to(device)
 
 
 def _rows(spec: Spec, E: int, count: int, g, device):
