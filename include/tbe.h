@@ -87,6 +87,8 @@ enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3 };
 /* device status bits (tbe_read_status) */
 #define TBE_ERR_INDEX_RANGE (1 << 0)    /* a lookup's row was outside [0, E_t) */
 #define TBE_ERR_OFFSETS (1 << 1)        /* offsets not 0 = o[0] <= ... <= o[T*B] <= n */
+#define TBE_ERR_TIMEOUT (1 << 2)        /* a bounded device wait gave up: the call's results
+                                           are incomplete (reported whatever the flags) */
 
 /* Problem description.  The three int64 arrays are device pointers with T+1
  * entries each (cumulative sums starting at 0); the scalar totals are their

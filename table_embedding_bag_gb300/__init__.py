@@ -34,6 +34,7 @@ TBE_F_PREPROCESSED = 1 << 4
 TBE_WS_WEIGHTED = 1 << 0
 TBE_ERR_INDEX_RANGE = 1 << 0
 TBE_ERR_OFFSETS = 1 << 1
+TBE_ERR_TIMEOUT = 1 << 2
 _STATUS_NAMES = {1: "TBE_EINVAL", 2: "TBE_EWORKSPACE", 3: "TBE_EUNSUPPORTED", 4: "TBE_ECUDA"}
 
 lib_path = _build.LIB

@@ -1,16 +1,330 @@
-// Small-table forward on the tensor cores (placeholder until the tcgen05
-// kernel lands: no problem is eligible yet, so every call takes the generic
-// gather-pool path).
+// Small-table forward on the 5th-generation tensor cores.
+//
+// "Modernizing Table Batched Embeddings with FBTriton", section "Forward:
+// keep a narrowly specialized path beside the general one": for one small
+// table, count how often each row occurs in each bag, then multiply the
+// counts by the table, turning irregular reads into tensor-core work;
+// eligibility is one table with E <= 64, 64 <= D <= 128, bags of at least 64
+// lookups, fp16 weights, fp32 output and no per-sample weights.
+//
+// GB300 design (one CTA per tile of 128 bags, persistent over tiles):
+//  * the table is staged once per CTA in shared memory as the B operand
+//    (N = D rows of K = 64 fp16, K-major, no swizzle; rows E..63 are zero);
+//  * each warp builds the histogram H[bag][row] of its bags with shared-memory
+//    atomics, converted to fp16 into the A operand (M = 128 bags x K = 64).
+//    A count c is split into c_hi = c & ~2047 and c_lo = c & 2047, both exact
+//    in fp16; the c_hi operand is multiplied only when some count reaches
+//    2048, so the result is exact in the counts whatever the bag length;
+//  * one thread issues tcgen05.mma (kind::f16, fp32 accumulate) into a
+//    128 x D fp32 accumulator in tensor memory and commits to an mbarrier;
+//    the warps then move the accumulator out with tcgen05.ld and store the
+//    pooled rows.  Every wait on the mbarrier is bounded: on time-out the CTA
+//    records an error in the status word, drains its MMAs (also bounded),
+//    frees its tensor memory and stops.
 #include "common.cuh"
 #include "internal.h"
 
 namespace tbe {
+namespace {
 
-bool small_table_eligible(const tbe_desc*, int64_t, bool) { return false; }
+constexpr int kM = 128;              // bags per tile (MMA M)
+constexpr int kK = 64;               // table rows (MMA K, zero-padded)
+constexpr int kThreads = 256;        // 8 warps
+constexpr int kCoreBytes = 128;      // 8 rows x 16 bytes
+constexpr int kLBO = kCoreBytes;     // next 8 K-elements of the same 8 rows
+constexpr int kSBO = (kK / 8) * kCoreBytes;  // next 8 rows (1024 bytes)
+constexpr int kTmemCols = 128;       // fp32 accumulator columns (>= D, power of two)
+constexpr uint32_t kSpinLimit = 1u << 26;
 
-cudaError_t launch_forward_small(const Launch&, const void*, const void*, const void*, float*,
-                                 int*) {
-  return cudaErrorNotSupported;
+struct SmallSmem {
+  alignas(1024) __half a_lo[kM * kK];  // H & 2047, canonical K-major layout
+  alignas(1024) __half a_hi[kM * kK];  // H & ~2047
+  alignas(1024) __half b[128 * kK];    // W^T rows (N = D <= 128), canonical K-major
+  uint32_t counts[kM * kK];            // integer histogram of the tile
+  alignas(8) unsigned long long mbar;
+  uint32_t tmem_base;
+  int need_hi;
+  int timed_out;
+};
+
+// Byte offset of element (row, k) of a K-major operand in the canonical
+// no-swizzle layout: 8x8 core matrices of 128 contiguous bytes, K-adjacent
+// cores kLBO apart, 8-row groups kSBO apart.
+__device__ __forceinline__ int canon_offset(int row, int k) {
+  return (row >> 3) * kSBO + (k >> 3) * kLBO + (row & 7) * 16 + (k & 7) * 2;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// tcgen05 shared-memory matrix descriptor: start address, leading and stride
+// byte offsets (all >> 4), descriptor version 1, no swizzle.
+__device__ __forceinline__ uint64_t make_desc(const void* smem_ptr) {
+  const uint64_t addr = smem_u32(smem_ptr);
+  return ((addr & 0x3ffffull) >> 4) | (static_cast<uint64_t>(kLBO >> 4) << 16) |
+         (static_cast<uint64_t>(kSBO >> 4) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__device__ __forceinline__ uint32_t make_idesc(int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; false if the phase did not complete within the limit.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i > 64) __nanosleep(64);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(unsigned long long* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 consecutive fp32 accumulator columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <typename IndexT>
+__global__ void __launch_bounds__(kThreads, 1)
+    forward_small_kernel(const __half* __restrict__ W, const IndexT* __restrict__ indices,
+                         const IndexT* __restrict__ offsets, int64_t n, int B, int E, int D,
+                         float* __restrict__ out, int64_t ld_out, int* status, int* error_word) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  SmallSmem& sm = *reinterpret_cast<SmallSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const unsigned lane = lane_id();
+
+  // Table -> B operand: element (n, k) = W[k][n] for k < E, zero otherwise.
+  for (int i = tid; i < 128 * kK; i += kThreads) {
+    const int nn = i / kK, k = i % kK;
+    const __half v = (nn < D && k < E) ? W[static_cast<int64_t>(k) * D + nn] : __float2half(0.f);
+    *reinterpret_cast<__half*>(reinterpret_cast<unsigned char*>(sm.b) + canon_offset(nn, k)) = v;
+  }
+  if (warp == 0) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+            smem_u32(&sm.tmem_base)),
+        "r"(kTmemCols)
+        : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    mbar_init(&sm.mbar, 1);
+    sm.timed_out = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+  const uint32_t idesc = make_idesc(D <= 64 ? 64 : 128);
+  const int n_mma = D <= 64 ? 64 : 128;
+  uint32_t phase = 0;
+  uint32_t drain_phase = 0;
+  bool bad = false;
+  const int64_t tiles = (static_cast<int64_t>(B) + kM - 1) / kM;
+
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int64_t bag0 = tile * kM;
+    // 1. histogram of the tile's bags (warp w takes bags w, w+8, ...)
+    for (int i = tid; i < kM * kK; i += kThreads) sm.counts[i] = 0;
+    if (tid == 0) sm.need_hi = 0;
+    __syncthreads();
+    for (int lb = warp; lb < kM; lb += kThreads / 32) {
+      const int64_t bag = bag0 + lb;
+      if (bag >= B) break;
+      int64_t s, e;
+      bag_range(offsets, bag, n, &s, &e);
+      for (int64_t i = s + lane; i < e; i += 32) {
+        const int64_t r = load_index(indices, i);
+        if (r >= 0 && r < E) atomicAdd(&sm.counts[lb * kK + static_cast<int>(r)], 1u);
+        else bad = true;
+      }
+    }
+    __syncthreads();
+    // 2. counts -> fp16 A operands (exact split at 2048)
+    int hi_here = 0;
+    for (int i = tid; i < kM * kK; i += kThreads) {
+      const int m = i / kK, k = i % kK;
+      const uint32_t c = sm.counts[i];
+      const int off = canon_offset(m, k);
+      *reinterpret_cast<__half*>(reinterpret_cast<unsigned char*>(sm.a_lo) + off) =
+          __uint2half_rn(c & 2047u);
+      *reinterpret_cast<__half*>(reinterpret_cast<unsigned char*>(sm.a_hi) + off) =
+          __uint2half_rn(c & ~2047u);
+      hi_here |= c > 2047u;
+    }
+    if (__syncthreads_or(hi_here) && tid == 0) sm.need_hi = 1;
+    fence_proxy_async();  // make the generic-proxy smem writes visible to the tensor core
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    // 3. one thread issues the MMAs (K = 64 in four steps of 16)
+    if (tid == 0) {
+      const int parts = sm.need_hi ? 2 : 1;
+      uint32_t acc = 0;
+      for (int part = 0; part < parts; ++part) {
+        const __half* a = part == 0 ? sm.a_lo : sm.a_hi;
+#pragma unroll
+        for (int ks = 0; ks < kK / 16; ++ks) {
+          const uint64_t ad = make_desc(reinterpret_cast<const unsigned char*>(a) + ks * 2 * kLBO);
+          const uint64_t bd =
+              make_desc(reinterpret_cast<const unsigned char*>(sm.b) + ks * 2 * kLBO);
+          mma_f16(tmem, ad, bd, idesc, acc);
+          acc = 1;
+        }
+      }
+      mma_commit(&sm.mbar);
+    }
+    __syncwarp();
+    // 4. wait for the accumulator, then store the pooled rows
+    const bool done = mbar_wait(&sm.mbar, phase);
+    drain_phase = phase;
+    phase ^= 1u;
+    if (!done) atomicOr(&sm.timed_out, 1);
+    fence_after_sync();
+    __syncthreads();
+    if (sm.timed_out) break;
+    {
+      const int lane_grp = warp & 3;               // TMEM lanes 32*lane_grp ..
+      const int col_half = warp >> 2;              // warps 4..7 take the upper columns
+      const int m = lane_grp * 32 + static_cast<int>(lane);
+      const int64_t bag = bag0 + m;
+      for (int c0 = col_half * 32; c0 < n_mma; c0 += 64) {
+        float v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(lane_grp * 32) << 16) + static_cast<uint32_t>(c0), v);
+        if (bag < B) {
+          float* o = out + bag * ld_out;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            if (c0 + j < D) __stcs(reinterpret_cast<float4*>(o + c0 + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+        }
+      }
+    }
+    fence_before_sync();
+    __syncthreads();  // accumulator and A buffers free for the next tile
+    fence_after_sync();
+  }
+
+  if (sm.timed_out) {
+    // Drain: give outstanding MMAs a bounded time to finish before the
+    // tensor memory is released.
+    if (tid == 0) {
+      atomicOr(error_word, TBE_ERR_TIMEOUT);
+      mbar_wait(&sm.mbar, drain_phase);
+    }
+    __syncthreads();
+  }
+  if (status && __any_sync(kFull, bad) && lane == 0) set_status(status, TBE_ERR_INDEX_RANGE);
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+}
+
+constexpr size_t kSmallSmemBytes = sizeof(SmallSmem) + 1024;
+
+template <typename IndexT>
+cudaError_t launch_small_t(const Launch& L, const __half* W, const IndexT* indices,
+                           const IndexT* offsets, float* out, int* status, int* error_word) {
+  const tbe_desc* d = L.d;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(forward_small_kernel<IndexT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmallSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int64_t tiles = (static_cast<int64_t>(d->B) + kM - 1) / kM;
+  int64_t grid = L.num_sms;
+  if (grid > tiles) grid = tiles;
+  if (grid < 1) grid = 1;
+  forward_small_kernel<IndexT><<<static_cast<unsigned>(grid), kThreads, kSmallSmemBytes, L.s>>>(
+      W, indices, offsets, L.n, d->B, static_cast<int>(d->total_E), static_cast<int>(d->total_D),
+      out, d->total_D, status, error_word);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool small_table_eligible(const tbe_desc* d, int64_t n, bool weighted) {
+  if (weighted || d->T != 1 || d->weights_dtype != TBE_DT_F16) return false;
+  if (d->total_E < 1 || d->total_E > kK) return false;
+  if (d->total_D < 64 || d->total_D > 128 || (d->total_D & 15)) return false;
+  return n >= 64LL * d->B;  // bags of at least 64 lookups on average
+}
+
+cudaError_t launch_forward_small(const Launch& L, const void* weights, const void* indices,
+                                 const void* offsets, float* out, int* status, int* error_word) {
+  const __half* W = static_cast<const __half*>(weights);
+  if (L.d->index_dtype == TBE_DT_I32)
+    return launch_small_t<int32_t>(L, W, static_cast<const int32_t*>(indices),
+                                   static_cast<const int32_t*>(offsets), out, status, error_word);
+  return launch_small_t<int64_t>(L, W, static_cast<const int64_t*>(indices),
+                                 static_cast<const int64_t*>(offsets), out, status, error_word);
 }
 
 }  // namespace tbe

@@ -30,7 +30,7 @@ int64_t repair_scratch_blocks(int64_t nb1);
 // forward_small.cu: tensor-core histogram path for one small table.
 bool small_table_eligible(const tbe_desc* d, int64_t n, bool weighted);
 cudaError_t launch_forward_small(const Launch& L, const void* weights, const void* indices,
-                                 const void* offsets, float* out, int* status);
+                                 const void* offsets, float* out, int* status, int* error_word);
 
 // preprocess.cu: expand, radix sort, run-length encode, classify.
 cudaError_t launch_preprocess(const Launch& L, const WsLayout& W, char* ws, const void* indices,

@@ -148,20 +148,51 @@ __global__ void __launch_bounds__(1024)
   if (sum_out && threadIdx.x == 0) *sum_out = agg;
 }
 
+// 16-byte asynchronous global -> shared copy; bytes beyond src_bytes are
+// zero-filled and not read from global memory.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 template <bool kWeighted>
 struct DownSmem {
-  uint32_t run_off[1 << kMaxRadixBits];              // next output position per digit
+  // Two tile buffers: one being loaded while the other is ranked, permuted
+  // in place into digit order and written out.
+  uint32_t keys[2][kSortTile];
+  uint32_t vals[2][kSortTile];
+  float psw[2][kWeighted ? kSortTile : 4];
+  uint32_t run_off[1 << kMaxRadixBits];  // next output position per digit
   uint32_t tile_cnt[1 << kMaxRadixBits];
   uint32_t tile_start[1 << kMaxRadixBits];
   uint32_t wcnt[kSortThreads / 32][1 << kMaxRadixBits];
-  uint32_t keys[kSortTile];
-  uint32_t vals[kSortTile];
-  float psw[kWeighted ? kSortTile : 1];
   uint32_t scan[33];
 };
 
+// Queue the copies of tile [tb, tb + valid) into buffer `buf`.
 template <bool kWeighted>
-__global__ void __launch_bounds__(kSortThreads, 3)
+__device__ __forceinline__ void load_tile_async(DownSmem<kWeighted>& sm, int buf,
+                                                const uint32_t* keys_in, const uint32_t* vals_in,
+                                                const float* psw_in, int64_t tb, int valid) {
+  for (int c = threadIdx.x; c < kSortTile / 4; c += kSortThreads) {
+    const int rem = valid - 4 * c;
+    const int bytes = rem >= 4 ? 16 : (rem > 0 ? rem * 4 : 0);
+    const int64_t src = rem > 0 ? tb + 4 * c : 0;  // no global read when bytes == 0
+    cp_async16(&sm.keys[buf][4 * c], keys_in + src, bytes);
+    cp_async16(&sm.vals[buf][4 * c], vals_in + src, bytes);
+    if (kWeighted) cp_async16(&sm.psw[buf][4 * c], psw_in + src, bytes);
+  }
+}
+
+template <bool kWeighted>
+__global__ void __launch_bounds__(kSortThreads, 2)
     radix_downsweep_kernel(const uint32_t* __restrict__ keys_in,
                            const uint32_t* __restrict__ vals_in,
                            const float* __restrict__ psw_in, uint32_t* __restrict__ keys_out,
@@ -179,12 +210,23 @@ __global__ void __launch_bounds__(kSortThreads, 3)
     sm.run_off[d] = counts[static_cast<int64_t>(d) * g.ctas + blockIdx.x];
   int64_t b, e;
   cta_range(g, n, &b, &e);
-  __syncthreads();
+  if (b < e) {
+    load_tile_async(sm, 0, keys_in, vals_in, psw_in, b,
+                    static_cast<int>(e - b < kSortTile ? e - b : kSortTile));
+  }
+  cp_async_commit();
 
-  for (int64_t tb = b; tb < e; tb += kSortTile) {
+  int cur = 0;
+  for (int64_t tb = b; tb < e; tb += kSortTile, cur ^= 1) {
     const int valid = static_cast<int>(e - tb < kSortTile ? e - tb : kSortTile);
+    const int64_t nb = tb + kSortTile;
+    if (nb < e)
+      load_tile_async(sm, cur ^ 1, keys_in, vals_in, psw_in, nb,
+                      static_cast<int>(e - nb < kSortTile ? e - nb : kSortTile));
+    cp_async_commit();
+    cp_async_wait<1>();  // this tile's copies are done (the next tile's may still run)
     for (int d = lane; d < nd; d += 32) sm.wcnt[warp][d] = 0;
-    __syncwarp();
+    __syncthreads();
     // Rank this warp's 512 keys (16 rounds of 32 consecutive keys) stably
     // among keys of the same digit within the warp.
     uint32_t key[kSortItems];
@@ -194,7 +236,7 @@ __global__ void __launch_bounds__(kSortThreads, 3)
       const int p = warp * (kSortItems * 32) + r * 32 + static_cast<int>(lane);
       // Keys past the end take the largest digit: they rank after every
       // valid key of the tile and are never written out.
-      key[r] = p < valid ? __ldg(keys_in + tb + p) : 0xffffffffu;
+      key[r] = p < valid ? sm.keys[cur][p] : 0xffffffffu;
       const uint32_t d = (key[r] >> shift) & mask;
       const unsigned peers = __match_any_sync(kFull, d);
       const uint32_t before = sm.wcnt[warp][d];
@@ -226,31 +268,41 @@ __global__ void __launch_bounds__(kSortThreads, 3)
       if (d0 < nd) sm.tile_start[d0] = inc - c0 - c1;
       if (d0 + 1 < nd) sm.tile_start[d0 + 1] = inc - c1;
     }
-    __syncthreads();
+    // Take this thread's values out of the buffer, then write keys and
+    // values back in digit order (the block scan above ended on a barrier,
+    // and the reads below finish before the barrier that precedes the writes).
+    uint32_t val[kSortItems];
+    float pw[kWeighted ? kSortItems : 1];
 #pragma unroll
     for (int r = 0; r < kSortItems; ++r) {
       const int p = warp * (kSortItems * 32) + r * 32 + static_cast<int>(lane);
+      val[r] = sm.vals[cur][p];
+      if (kWeighted) pw[r] = sm.psw[cur][p];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kSortItems; ++r) {
       const uint32_t d = (key[r] >> shift) & mask;
-      const uint32_t pos = sm.tile_start[d] + sm.wcnt[warp][d] + ((rank[r >> 1] >> (16 * (r & 1))) & 0xffffu);
-      sm.keys[pos] = key[r];
-      if (p < valid) {
-        sm.vals[pos] = __ldg(vals_in + tb + p);
-        if (kWeighted) sm.psw[pos] = __ldg(psw_in + tb + p);
-      }
+      const uint32_t pos = sm.tile_start[d] + sm.wcnt[warp][d] +
+                           ((rank[r >> 1] >> (16 * (r & 1))) & 0xffffu);
+      sm.keys[cur][pos] = key[r];
+      sm.vals[cur][pos] = val[r];
+      if (kWeighted) sm.psw[cur][pos] = pw[r];
     }
     __syncthreads();
     for (int i = threadIdx.x; i < valid; i += kSortThreads) {
-      const uint32_t k = sm.keys[i];
+      const uint32_t k = sm.keys[cur][i];
       const uint32_t d = (k >> shift) & mask;
       const uint32_t dst = sm.run_off[d] + (static_cast<uint32_t>(i) - sm.tile_start[d]);
       keys_out[dst] = k;
-      vals_out[dst] = sm.vals[i];
-      if (kWeighted) psw_out[dst] = sm.psw[i];
+      vals_out[dst] = sm.vals[cur][i];
+      if (kWeighted) psw_out[dst] = sm.psw[cur][i];
     }
     __syncthreads();
     for (int d = threadIdx.x; d < nd; d += kSortThreads) sm.run_off[d] += sm.tile_cnt[d];
-    __syncthreads();
+    // The next iteration's barrier orders these updates before their use.
   }
+  cp_async_wait<0>();
 }
 
 // --------------------------------------------------------------------- RLE
@@ -604,7 +656,7 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     fill_tail_kernel<IndexT><<<64, 256, 0, s>>>(offsets, nbags, n, sentinel, keys[0], vals[0],
                                                 pw[0]);
 
-    const SortGeom g = sort_geom(n, L.num_sms, 3);
+    const SortGeom g = sort_geom(n, L.num_sms, 2);
     const int bits = key_bits(d);
     const int passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
     const int rb = (bits + passes - 1) / passes;

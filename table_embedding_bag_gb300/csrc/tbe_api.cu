@@ -23,9 +23,10 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   L.counts = take(kNumCounters * sizeof(uint32_t));
   L.table_runs = take((d->T + 1) * sizeof(uint32_t));
   L.table_tasks = take((d->T + 1) * sizeof(uint32_t));
-  for (int i = 0; i < 2; ++i) L.keys[i] = take(un * 4);
-  for (int i = 0; i < 2; ++i) L.vals[i] = take(un * 4);
-  for (int i = 0; i < 2; ++i) L.psw[i] = L.weighted ? take(un * 4) : 0;
+  // sort buffers keep 64 spare bytes: whole 16-byte tile copies stay inside
+  for (int i = 0; i < 2; ++i) L.keys[i] = take(un * 4 + 64);
+  for (int i = 0; i < 2; ++i) L.vals[i] = take(un * 4 + 64);
+  for (int i = 0; i < 2; ++i) L.psw[i] = L.weighted ? take(un * 4 + 64) : 0;
   L.radix_counts = take(sizeof(uint32_t) * (1u << kMaxRadixBits) * kMaxSortCtas);
   L.cta_counts = take(sizeof(uint32_t) * 2 * (kMaxSortCtas + 1));
   L.unique_keys = take((un + 1) * 4);
@@ -159,7 +160,8 @@ tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indic
   st = run_checks(L, W, ws, offsets, flags, &off_eff, &status);
   if (st != TBE_OK) return st;
   if (!(flags & TBE_F_FORCE_GENERIC) && small_table_eligible(d, n, per_sample_weights != nullptr))
-    return from_cuda(launch_forward_small(L, weights, indices, off_eff, out, status));
+    return from_cuda(launch_forward_small(L, weights, indices, off_eff, out, status,
+                                          reinterpret_cast<int*>(ws + W.status)));
   return from_cuda(
       launch_forward_generic(L, weights, indices, off_eff, per_sample_weights, out, status));
 }
