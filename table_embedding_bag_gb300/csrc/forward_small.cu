@@ -10,8 +10,10 @@
 // GB300 design (one CTA per tile of 128 bags, persistent over tiles):
 //  * the table is staged once per CTA in shared memory as the B operand
 //    (N = D rows of K = 64 fp16, K-major, no swizzle; rows E..63 are zero);
-//  * each warp builds the histogram H[bag][row] of its bags with shared-memory
-//    atomics, converted to fp16 into the A operand (M = 128 bags x K = 64).
+//  * the CTA streams the tile's index range (contiguous: 128 consecutive
+//    bags) with 8 loads in flight per thread and builds the histogram
+//    H[bag][row] with shared-memory atomics, then converts it to fp16 into
+//    the A operand (M = 128 bags x K = 64);
 //    A count c is split into c_hi = c & ~2047 and c_lo = c & 2047, both exact
 //    in fp16; the c_hi operand is multiplied only when some count reaches
 //    2048, so the result is exact in the counts whatever the bag length;
@@ -41,6 +43,7 @@ struct SmallSmem {
   alignas(1024) __half a_hi[kM * kK];  // H & ~2047
   alignas(1024) __half b[128 * kK];    // W^T rows (N = D <= 128), canonical K-major
   uint32_t counts[kM * kK];            // integer histogram of the tile
+  int64_t bag_off[kM + 1];             // the tile's bag offsets, clamped to [0, n]
   alignas(8) unsigned long long mbar;
   uint32_t tmem_base;
   int need_hi;
@@ -143,7 +146,7 @@ __device__ __forceinline__ void fence_proxy_async() {
 }
 
 template <typename IndexT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     forward_small_kernel(const __half* __restrict__ W, const IndexT* __restrict__ indices,
                          const IndexT* __restrict__ offsets, int64_t n, int B, int E, int D,
                          float* __restrict__ out, int64_t ld_out, int* status, int* error_word) {
@@ -186,19 +189,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int64_t bag0 = tile * kM;
-    // 1. histogram of the tile's bags (warp w takes bags w, w+8, ...)
+    // 1. histogram of the tile's bags.  The tile's lookups are one contiguous
+    //    range of indices; every thread keeps kLoads index loads in flight
+    //    and finds each lookup's bag by binary search in the tile offsets.
     for (int i = tid; i < kM * kK; i += kThreads) sm.counts[i] = 0;
+    for (int j = tid; j <= kM; j += kThreads) {
+      const int64_t bag = bag0 + j < B ? bag0 + j : B;
+      int64_t o = load_index(offsets, bag);
+      o = o < 0 ? 0 : (o > n ? n : o);
+      sm.bag_off[j] = o;
+    }
     if (tid == 0) sm.need_hi = 0;
     __syncthreads();
-    for (int lb = warp; lb < kM; lb += kThreads / 32) {
-      const int64_t bag = bag0 + lb;
-      if (bag >= B) break;
-      int64_t s, e;
-      bag_range(offsets, bag, n, &s, &e);
-      for (int64_t i = s + lane; i < e; i += 32) {
-        const int64_t r = load_index(indices, i);
-        if (r >= 0 && r < E) atomicAdd(&sm.counts[lb * kK + static_cast<int>(r)], 1u);
-        else bad = true;
+    {
+      const int64_t p0 = sm.bag_off[0];
+      const int64_t p1 = sm.bag_off[kM];
+      constexpr int kLoads = 8;
+      for (int64_t base = p0; base < p1; base += static_cast<int64_t>(kThreads) * kLoads) {
+        int64_t r[kLoads];
+#pragma unroll
+        for (int u = 0; u < kLoads; ++u) {
+          const int64_t p = base + u * kThreads + tid;
+          r[u] = p < p1 ? load_index(indices, p) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kLoads; ++u) {
+          const int64_t p = base + u * kThreads + tid;
+          if (p >= p1) continue;
+          int lo = 0, hi = kM - 1;  // largest bag j with bag_off[j] <= p
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sm.bag_off[mid] <= p) lo = mid; else hi = mid - 1;
+          }
+          if (p >= sm.bag_off[lo + 1]) continue;  // in no bag of the tile
+          if (r[u] >= 0 && r[u] < E) atomicAdd(&sm.counts[lo * kK + static_cast<int>(r[u])], 1u);
+          else bad = true;
+        }
       }
     }
     __syncthreads();
@@ -299,7 +325,7 @@ cudaError_t launch_small_t(const Launch& L, const __half* W, const IndexT* indic
     attr_set[dev] = true;
   }
   const int64_t tiles = (static_cast<int64_t>(d->B) + kM - 1) / kM;
-  int64_t grid = L.num_sms;
+  int64_t grid = 2LL * L.num_sms;
   if (grid > tiles) grid = tiles;
   if (grid < 1) grid = 1;
   forward_small_kernel<IndexT><<<static_cast<unsigned>(grid), kThreads, kSmallSmemBytes, L.s>>>(
