@@ -138,9 +138,12 @@ def _rows(spec: Spec, E: int, count: int, g, device):
 
 
 def make(name: str, device="cpu", seed: int = 0, B: int | None = None, T: int | None = None,
-         E_scale: float | None = None) -> Workload:
+         E_scale: float | None = None, compact: bool = False) -> Workload:
     """Draw a workload.  B, T and E_scale shrink a recipe for oracle-sized tests
-    (E_scale multiplies every table's row count, keeping at least one row)."""
+    (E_scale multiplies every table's row count, keeping at least one row).
+    compact=True keeps only the rows the lookups touch, renumbered per table
+    in increasing order (the lookups are drawn from the full tables first), so
+    that a few bags of a huge table need no huge weight array."""
     spec = SPECS[name]
     T = spec.T if T is None else T
     B = spec.B if B is None else B
@@ -157,6 +160,11 @@ def make(name: str, device="cpu", seed: int = 0, B: int | None = None, T: int | 
         rows.append(_rows(spec, int(E[t]), cnt, g, device))
         if spec.weighted:
             psws.append(torch.rand(cnt, dtype=torch.float32, generator=g, device=device))
+    if compact:
+        for t in range(T):
+            uniq, inv = torch.unique(rows[t], return_inverse=True)
+            rows[t] = inv
+            E[t] = max(1, int(uniq.numel()))
     L = torch.cat(lengths)
     offsets = torch.zeros(T * B + 1, dtype=torch.int64, device=device)
     torch.cumsum(L, 0, out=offsets[1:])
