@@ -62,7 +62,9 @@ typedef enum tbe_status {
   TBE_EINVAL = 1,       /* null pointer, negative size, dtype mismatch */
   TBE_EWORKSPACE = 2,   /* workspace null or smaller than tbe_workspace_size */
   TBE_EUNSUPPORTED = 3, /* well-formed but outside what the kernels cover */
-  TBE_ECUDA = 4         /* a CUDA call or launch returned an error */
+  TBE_ECUDA = 4,        /* a CUDA call or launch returned an error */
+  TBE_ETOO_LARGE = 5    /* the problem needs more scratch than the fixed array of
+                           tbe_backward_rowwise_adagrad_noalloc holds */
 } tbe_status;
 
 /* element types */
@@ -197,6 +199,43 @@ tbe_status tbe_workspace_view(const tbe_desc* d, int64_t n, uint32_t ws_flags, v
  * Synchronises the stream: never call it inside a timed or captured region.
  * Errors: TBE_EINVAL, TBE_ECUDA. */
 tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits);
+
+/* Size of the library-owned scratch used by tbe_backward_rowwise_adagrad_noalloc. */
+#define TBE_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* Backward with exact row-wise Adagrad that allocates nothing, not even a
+ * caller-provided workspace.  The pages have no counterpart: this entry point
+ * exists for callers that must not allocate device memory when they call the
+ * backward -- runtimes that hand out all device memory up front from their
+ * own pools (a serving engine or a training loop with a static memory plan),
+ * and code that cannot afford cudaMalloc/cudaFree, which may synchronise the
+ * whole device and fragment such a plan.
+ *
+ * It computes exactly what tbe_backward_rowwise_adagrad computes, with the
+ * same kernels, but its scratch is a fixed array of TBE_NOALLOC_SCRATCH_BYTES
+ * (32 MiB) inside the library, held by every GPU that loads the library until
+ * the process exits.  Problems whose scratch would be larger -- roughly more
+ * than 400k lookups of 128-wide rows, fewer for wider rows or per-sample
+ * weights -- are rejected
+ * with TBE_ETOO_LARGE before anything is enqueued.  No cudaMalloc, cudaFree or
+ * other allocating call is made.
+ *
+ * The first call on each device does the set-up (looks up the device address
+ * of the array); make that first call before any stream capture.  Every call
+ * shares the one array and it keeps the previous call's contents; everything
+ * that must start at zero is cleared by the call itself.  Calls whose work
+ * overlaps on the GPU (different streams, or several host threads) race on
+ * the array: serialise them.
+ *
+ * Arguments as tbe_backward_rowwise_adagrad without workspace; flags may be 0
+ * or TBE_F_LONG_TWO_LAUNCH (no bounds reporting: the status word lives in the
+ * caller's workspace elsewhere; invalid rows are still skipped).
+ * Errors: TBE_EINVAL, TBE_EUNSUPPORTED, TBE_ETOO_LARGE, TBE_ECUDA. */
+tbe_status tbe_backward_rowwise_adagrad_noalloc(const tbe_desc* d, const float* grad_out,
+                                                const void* indices, const void* offsets,
+                                                int64_t n, const float* per_sample_weights,
+                                                void* weights, float* momentum, float lr,
+                                                float eps, void* stream, uint32_t flags);
 
 /* Library build identification: a static string. */
 const char* tbe_version(void);

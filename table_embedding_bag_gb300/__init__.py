@@ -19,12 +19,14 @@ from . import _build
 __all__ = [
     "build", "TBEDesc", "Workspace", "TBEError", "tbe_workspace_size", "tbe_forward",
     "tbe_preprocess", "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status",
-    "tbe_version", "TableBatchedEmbedding", "lib_path",
+    "tbe_version", "TableBatchedEmbedding", "lib_path", "tbe_backward_rowwise_adagrad_noalloc",
+    "TBE_NOALLOC_SCRATCH_BYTES", "TBE_ETOO_LARGE",
     "TBE_F_CHECK_BOUNDS", "TBE_F_REPAIR_OFFSETS", "TBE_F_FORCE_GENERIC", "TBE_F_LONG_TWO_LAUNCH",
     "TBE_F_PREPROCESSED", "TBE_WS_WEIGHTED", "TBE_ERR_INDEX_RANGE", "TBE_ERR_OFFSETS",
 ]
 
-TBE_OK, TBE_EINVAL, TBE_EWORKSPACE, TBE_EUNSUPPORTED, TBE_ECUDA = range(5)
+TBE_OK, TBE_EINVAL, TBE_EWORKSPACE, TBE_EUNSUPPORTED, TBE_ECUDA, TBE_ETOO_LARGE = range(6)
+TBE_NOALLOC_SCRATCH_BYTES = 32 << 20
 TBE_DT_F16, TBE_DT_I32, TBE_DT_I64 = 1, 2, 3
 TBE_F_CHECK_BOUNDS = 1 << 0
 TBE_F_REPAIR_OFFSETS = 1 << 1
@@ -35,7 +37,8 @@ TBE_WS_WEIGHTED = 1 << 0
 TBE_ERR_INDEX_RANGE = 1 << 0
 TBE_ERR_OFFSETS = 1 << 1
 TBE_ERR_TIMEOUT = 1 << 2
-_STATUS_NAMES = {1: "TBE_EINVAL", 2: "TBE_EWORKSPACE", 3: "TBE_EUNSUPPORTED", 4: "TBE_ECUDA"}
+_STATUS_NAMES = {1: "TBE_EINVAL", 2: "TBE_EWORKSPACE", 3: "TBE_EUNSUPPORTED", 4: "TBE_ECUDA",
+                 5: "TBE_ETOO_LARGE"}
 
 lib_path = _build.LIB
 build = _build.build
@@ -83,10 +86,13 @@ def _load():
         lib.tbe_backward_rowwise_adagrad.argtypes = [D, P, P, P, i64, P, P, P, f32, f32, P, sz, P,
                                                      u32]
         lib.tbe_workspace_view.argtypes = [D, i64, u32, P, ctypes.POINTER(tbe_ws_view)]
+        lib.tbe_backward_rowwise_adagrad_noalloc.argtypes = [D, P, P, P, i64, P, P, P, f32, f32,
+                                                             P, u32]
         lib.tbe_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         lib.tbe_version.restype = ctypes.c_char_p
         for f in ("tbe_workspace_size", "tbe_forward", "tbe_preprocess",
-                  "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status"):
+                  "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status",
+                  "tbe_backward_rowwise_adagrad_noalloc"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -199,6 +205,19 @@ def tbe_backward_rowwise_adagrad(desc: TBEDesc, grad_out, indices, offsets, per_
         desc.ref, _ptr(grad_out), _ptr(indices), _ptr(offsets), indices.numel(),
         _ptr(per_sample_weights), _ptr(weights), _ptr(momentum), float(lr), float(eps), ws.ptr,
         ws.nbytes, _stream(stream), flags))
+
+
+def tbe_backward_rowwise_adagrad_noalloc(desc: TBEDesc, grad_out, indices, offsets,
+                                         per_sample_weights, weights, momentum, lr, eps,
+                                         flags: int = 0, stream=None):
+    """The backward without any workspace: for callers that must not allocate
+    device memory at call time (see tbe_backward_rowwise_adagrad_noalloc in
+    include/tbe.h for the scratch limit and the rules on overlapping calls)."""
+    _check_tensors(desc, indices, offsets)
+    _ok("tbe_backward_rowwise_adagrad_noalloc", _load().tbe_backward_rowwise_adagrad_noalloc(
+        desc.ref, _ptr(grad_out), _ptr(indices), _ptr(offsets), indices.numel(),
+        _ptr(per_sample_weights), _ptr(weights), _ptr(momentum), float(lr), float(eps),
+        _stream(stream), flags))
 
 
 def tbe_workspace_view(desc: TBEDesc, n: int, ws: Workspace) -> dict:

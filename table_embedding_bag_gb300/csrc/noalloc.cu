@@ -1,0 +1,97 @@
+// Backward with row-wise Adagrad for callers that cannot allocate device
+// memory: the scratch lives in a fixed array inside the library instead of a
+// caller-provided workspace.  The kernels are the ones tbe_backward_rowwise_
+// adagrad runs; only where the scratch comes from differs.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace tbe {
+namespace {
+
+// Library-owned scratch for tbe_backward_rowwise_adagrad_noalloc.  Every GPU
+// that loads the library holds this array until the process exits.  In host
+// code the symbol is only a stand-in: its device address comes from
+// cudaGetSymbolAddress, taken once per device in scratch_ptr().
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TBE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+cudaError_t prepare_preprocess_kernels();
+namespace {
+
+// Set-up, once per device and with that device current: the device address
+// of the scratch, and the shared-memory attributes of the sort kernels.
+// Returns the scratch address on the current device, or nullptr on failure.
+char* scratch_ptr() {
+  static char* ptrs[kMaxDevices] = {nullptr};
+  static std::once_flag once[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::call_once(once[dev], [dev]() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return;
+    if (prepare_preprocess_kernels() != cudaSuccess) return;
+    ptrs[dev] = static_cast<char*>(p);
+  });
+  return ptrs[dev];
+}
+
+// Same checks as the workspace entry points, except that the workspace is the
+// library's own array.
+tbe_status check_args(const tbe_desc* d, const void* indices, const void* offsets, int64_t n) {
+  if (!d) return TBE_EINVAL;
+  if (d->T < 1 || d->B < 1 || !d->D_offsets || !d->hash_base || !d->weights_offsets)
+    return TBE_EINVAL;
+  if (d->weights_dtype != TBE_DT_F16) return TBE_EUNSUPPORTED;
+  if (d->index_dtype != TBE_DT_I32 && d->index_dtype != TBE_DT_I64) return TBE_EUNSUPPORTED;
+  if (d->min_D < 8 || d->max_D > kMaxD || d->min_D > d->max_D || (d->min_D & 7) ||
+      (d->max_D & 7) || d->total_D < d->max_D || (d->total_D & 7))
+    return TBE_EUNSUPPORTED;
+  if (d->total_E < 1 || d->total_E >= 0xffffffffLL) return TBE_EUNSUPPORTED;
+  if (static_cast<int64_t>(d->B) * d->T >= 0x7fffffffLL) return TBE_EUNSUPPORTED;
+  if (n < 0) return TBE_EINVAL;
+  if (n >= 0xfffffff0LL) return TBE_EUNSUPPORTED;
+  if (!offsets || (n > 0 && !indices)) return TBE_EINVAL;
+  return TBE_OK;
+}
+
+int sm_count() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+    return 148;
+  return v;
+}
+
+}  // namespace
+}  // namespace tbe
+
+using namespace tbe;
+
+extern "C" tbe_status tbe_backward_rowwise_adagrad_noalloc(
+    const tbe_desc* d, const float* grad_out, const void* indices, const void* offsets, int64_t n,
+    const float* per_sample_weights, void* weights, float* momentum, float lr, float eps,
+    void* stream, uint32_t flags) {
+  tbe_status st = check_args(d, indices, offsets, n);
+  if (st != TBE_OK) return st;
+  if (!grad_out || !weights || !momentum) return TBE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(grad_out) & 15u) || (reinterpret_cast<uintptr_t>(weights) & 15u))
+    return TBE_EINVAL;
+  if (flags & ~TBE_F_LONG_TWO_LAUNCH) return TBE_EINVAL;
+  const WsLayout W = make_layout(d, n, per_sample_weights ? TBE_WS_WEIGHTED : 0u);
+  if (W.total > TBE_NOALLOC_SCRATCH_BYTES) return TBE_ETOO_LARGE;
+  char* scratch = scratch_ptr();
+  if (!scratch) return TBE_ECUDA;
+  const Launch L{d, n, static_cast<cudaStream_t>(stream), sm_count()};
+  // Everything the kernels read before writing is reset by launch_preprocess
+  // (counters, first run and pair entries, band counts); the status word is
+  // not used because bounds reporting is not offered here.
+  cudaError_t e = launch_preprocess(L, W, scratch, indices, offsets, per_sample_weights, false);
+  if (e != cudaSuccess) return TBE_ECUDA;
+  e = launch_update(L, W, scratch, grad_out, weights, momentum, lr, eps,
+                    (flags & TBE_F_LONG_TWO_LAUNCH) != 0);
+  return e == cudaSuccess ? TBE_OK : TBE_ECUDA;
+}

@@ -25,8 +25,9 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "tbe_backward_rowwise_adagrad", "tbe_forward", "tbe_preprocess", "tbe_read_status",
-        "tbe_version", "tbe_workspace_size", "tbe_workspace_view"])
+        "tbe_backward_rowwise_adagrad", "tbe_backward_rowwise_adagrad_noalloc", "tbe_forward",
+        "tbe_preprocess", "tbe_read_status", "tbe_version", "tbe_workspace_size",
+        "tbe_workspace_view"])
 
 
 def test_every_declared_symbol_is_exported(lib):
