@@ -20,7 +20,7 @@
 #define TBE_SHORT_MINB 3
 #endif
 #ifndef TBE_FWD_MINB
-#define TBE_FWD_MINB 5
+#define TBE_FWD_MINB 4
 #endif
 #ifndef TBE_LONG_VECS
 #define TBE_LONG_VECS 8

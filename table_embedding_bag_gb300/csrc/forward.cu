@@ -50,17 +50,26 @@ __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t 
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   bool bad = false;
 
+  // The next batch's index (and weight) is loaded while this batch's rows are
+  // gathered, so a batch waits on one memory round trip instead of two.
+  int64_t nx_r = start + lane < end ? load_index(indices, start + lane) : 0;
+  float nx_w = (kWeighted && start + lane < end) ? __ldg(psw + start + lane) : 0.f;
   for (int64_t base = start; base < end; base += 32) {
     const int cnt = static_cast<int>(end - base < 32 ? end - base : 32);
+    const int64_t r = nx_r;
+    const float w_in = nx_w;
+    if (base + 32 + lane < end) {
+      nx_r = load_index(indices, base + 32 + lane);
+      if (kWeighted) nx_w = __ldg(psw + base + 32 + lane);
+    }
     const __half* my_row = reinterpret_cast<const __half*>(g_zero_row);
     float my_w = 0.f;
     if (lane < cnt) {
-      const int64_t r = load_index(indices, base + lane);
       const bool ok = r >= 0 && r < E;
       bad |= !ok;
       if (ok) {
         my_row = Wt + r * D;
-        if (kWeighted) my_w = __ldg(psw + base + lane);
+        if (kWeighted) my_w = w_in;
       }
     }
     const uint64_t my_addr = reinterpret_cast<uint64_t>(my_row);

@@ -94,7 +94,7 @@ __device__ __forceinline__ void cta_range(const SortGeom& g, int64_t n, int64_t*
   if (*b > n) *b = n;
 }
 
-// Per-CTA digit histogram; counts stored digit-major: counts[d * ctas + cta].
+// Per-CTA digit histogram; counts stored CTA-major: counts[cta * 2^width + d].
 __global__ void __launch_bounds__(kSortThreads)
     radix_upsweep_kernel(const uint32_t* __restrict__ keys, int64_t n, SortGeom g, int shift,
                          int width, uint32_t* __restrict__ counts) {
@@ -122,8 +122,37 @@ __global__ void __launch_bounds__(kSortThreads)
     uint32_t s = 0;
 #pragma unroll
     for (int w = 0; w < kSortThreads / 32; ++w) s += hist[w][d];
-    counts[static_cast<int64_t>(d) * g.ctas + blockIdx.x] = s;
+    counts[static_cast<int64_t>(blockIdx.x) * nd + d] = s;
   }
+}
+
+// Output position of every (digit, CTA) in digit-major order: for digit d and
+// CTA c, the keys of smaller digits plus the keys of digit d in CTAs before c.
+// One CTA, one thread per digit walking the CTAs (loads are coalesced across
+// threads), then a scan of the digit totals.  In place on counts[c][d].
+__global__ void __launch_bounds__(1 << kMaxRadixBits)
+    radix_scan_kernel(uint32_t* __restrict__ counts, int ctas, int nd) {
+  __shared__ uint32_t sm[33];
+  const int d = threadIdx.x;
+  uint32_t run = 0;
+  if (d < nd) {
+    constexpr int kAhead = 8;  // loads issued before the stores they precede
+    for (int c0 = 0; c0 < ctas; c0 += kAhead) {
+      uint32_t v[kAhead];
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u)
+        v[u] = c0 + u < ctas ? counts[static_cast<int64_t>(c0 + u) * nd + d] : 0u;
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) {
+        if (c0 + u < ctas) counts[static_cast<int64_t>(c0 + u) * nd + d] = run;
+        run += v[u];
+      }
+    }
+  }
+  const uint32_t inc = block_inclusive_scan(run, OpSum(), 0u, sm);
+  const uint32_t base = inc - run;
+  if (d < nd)
+    for (int c = 0; c < ctas; ++c) counts[static_cast<int64_t>(c) * nd + d] += base;
 }
 
 // Single CTA: exclusive scan over `total` counts in place (digit-major order
@@ -207,7 +236,7 @@ __global__ void __launch_bounds__(kSortThreads, 2)
   const unsigned lane = lane_id();
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int d = threadIdx.x; d < nd; d += kSortThreads)
-    sm.run_off[d] = counts[static_cast<int64_t>(d) * g.ctas + blockIdx.x];
+    sm.run_off[d] = counts[static_cast<int64_t>(blockIdx.x) * nd + d];
   int64_t b, e;
   cta_range(g, n, &b, &e);
   if (b < e) {
@@ -306,21 +335,24 @@ __global__ void __launch_bounds__(kSortThreads, 2)
 }
 
 // --------------------------------------------------------------------- RLE
-// Two levels over the sorted lookups: a run starts where the key changes (a
-// new table row), a pair starts where the key or the bag changes.  Lookups
-// with the invalid key start nothing.  Each thread owns kRleItems consecutive
-// lookups; the lookup before its first one comes from the neighbouring lane
-// (or, for lane 0, from memory).
+// Two levels over the sorted lookups: runs (one per table row) and pairs (the
+// lookups of a run from one bag).  Each thread owns kRleItems consecutive
+// lookups; the loads of the next tile are issued before the current tile is
+// processed.
 struct RleItems {
   uint32_t k[kRleItems];
   uint32_t b[kRleItems];
+  uint32_t pk, pb;  // the lookup before the first one (lane 0: from memory)
+  bool first;       // no lookup before the first one
   bool run_head[kRleItems];
   bool pair_head[kRleItems];
 };
 
-__device__ __forceinline__ void rle_flags(const uint32_t* __restrict__ keys,
-                                          const uint32_t* __restrict__ bags, int64_t i0,
-                                          int64_t e, uint32_t sentinel, RleItems& it) {
+// Issue the loads of a thread's kRleItems lookups starting at i0 (and, on
+// lane 0, of the lookup before them); rle_heads consumes them later.
+__device__ __forceinline__ void rle_load(const uint32_t* __restrict__ keys,
+                                         const uint32_t* __restrict__ bags, int64_t i0, int64_t e,
+                                         uint32_t sentinel, RleItems& it) {
   if (i0 + kRleItems <= e) {
 #pragma unroll
     for (int j = 0; j < kRleItems; j += 4) {
@@ -337,18 +369,30 @@ __device__ __forceinline__ void rle_flags(const uint32_t* __restrict__ keys,
       it.b[j] = in ? __ldg(bags + i0 + j) : 0u;
     }
   }
-  uint32_t pk = __shfl_up_sync(kFull, it.k[kRleItems - 1], 1);
-  uint32_t pb = __shfl_up_sync(kFull, it.b[kRleItems - 1], 1);
-  bool first = false;  // no lookup before this one
+  it.first = false;
+  it.pk = sentinel;
+  it.pb = 0;
   if (lane_id() == 0) {
     if (i0 > 0 && i0 - 1 < e) {
-      pk = __ldg(keys + i0 - 1);
-      pb = __ldg(bags + i0 - 1);
+      it.pk = __ldg(keys + i0 - 1);
+      it.pb = __ldg(bags + i0 - 1);
     } else if (i0 == 0) {
-      first = true;
-    } else {
-      pk = sentinel;
+      it.first = true;
     }
+  }
+}
+
+// A run starts where the key changes (a new table row), a pair where the key
+// or the bag changes; lookups with the invalid key start nothing.  The
+// lookup before a thread's first one is its neighbour lane's last one.
+__device__ __forceinline__ void rle_heads(RleItems& it, uint32_t sentinel) {
+  uint32_t pk = __shfl_up_sync(kFull, it.k[kRleItems - 1], 1);
+  uint32_t pb = __shfl_up_sync(kFull, it.b[kRleItems - 1], 1);
+  bool first = false;
+  if (lane_id() == 0) {
+    pk = it.pk;
+    pb = it.pb;
+    first = it.first;
   }
 #pragma unroll
   for (int j = 0; j < kRleItems; ++j) {
@@ -370,9 +414,14 @@ __global__ void __launch_bounds__(kRleThreads)
   int64_t b, e;
   cta_range(g, n, &b, &e);
   unsigned long long c = 0;  // runs in the high word, pairs in the low word
+  RleItems it, nx;
+  if (b < e) rle_load(keys, bags, b + static_cast<int64_t>(threadIdx.x) * kRleItems, e, sentinel, nx);
   for (int64_t tb = b; tb < e; tb += kRleTile) {
-    RleItems it;
-    rle_flags(keys, bags, tb + static_cast<int64_t>(threadIdx.x) * kRleItems, e, sentinel, it);
+    it = nx;
+    if (tb + kRleTile < e)  // next tile's loads in flight while this one is counted
+      rle_load(keys, bags, tb + kRleTile + static_cast<int64_t>(threadIdx.x) * kRleItems, e,
+               sentinel, nx);
+    rle_heads(it, sentinel);
 #pragma unroll
     for (int j = 0; j < kRleItems; ++j)
       c += (static_cast<unsigned long long>(it.run_head[j]) << 32) | it.pair_head[j];
@@ -399,10 +448,17 @@ __global__ void __launch_bounds__(kRleThreads)
   uint32_t p = pair_base[blockIdx.x];
   const uint32_t R = run_base[g.ctas];
   const uint32_t P = pair_base[g.ctas];
+  RleItems it, nx;
+  if (b < e) rle_load(keys, bags, b + static_cast<int64_t>(threadIdx.x) * kRleItems, e, sentinel, nx);
   for (int64_t tb = b; tb < e; tb += kRleTile) {
     const int64_t i0 = tb + static_cast<int64_t>(threadIdx.x) * kRleItems;
-    RleItems it;
-    rle_flags(keys, bags, i0, e, sentinel, it);
+    it = nx;
+    if (tb + kRleTile < e)  // next tile's loads in flight while this one is written
+      rle_load(keys, bags, i0 + kRleTile, e, sentinel, nx);
+    const bool first_here = it.first;
+    const uint32_t up_key = __shfl_up_sync(kFull, it.k[kRleItems - 1], 1);  // all lanes
+    const uint32_t before_key = lane_id() == 0 ? it.pk : up_key;
+    rle_heads(it, sentinel);
     uint32_t c = 0;  // runs << 16 | pairs: at most kRleTile each per tile
 #pragma unroll
     for (int j = 0; j < kRleItems; ++j) c += (static_cast<uint32_t>(it.run_head[j]) << 16) | it.pair_head[j];
@@ -428,9 +484,8 @@ __global__ void __launch_bounds__(kRleThreads)
       // End of the valid keys: the first invalid key, or the end of the array.
       if (i < e) {
         const bool invalid = it.k[j] >= sentinel;
-        const bool prev_valid = i == 0 ? false
-                                : (j > 0 ? it.k[j - 1] < sentinel : __ldg(keys + i - 1) < sentinel);
-        const bool first_invalid = invalid && (i == 0 || prev_valid);
+        const uint32_t prev = j > 0 ? it.k[j - 1] : before_key;
+        const bool first_invalid = invalid && ((j == 0 && first_here) || prev < sentinel);
         const bool last_valid = !invalid && i == n - 1;
         if (first_invalid || last_valid) {
           const uint32_t nv = first_invalid ? static_cast<uint32_t>(i) : static_cast<uint32_t>(n);
@@ -667,8 +722,7 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
       const int width = rb < bits - shift ? rb : bits - shift;
       const int src = p & 1, dst = src ^ 1;
       radix_upsweep_kernel<<<g.ctas, kSortThreads, 0, s>>>(keys[src], n, g, shift, width, counts);
-      exclusive_scan_kernel<<<1, 1024, 0, s>>>(counts, static_cast<int64_t>(1 << width) * g.ctas,
-                                               nullptr);
+      radix_scan_kernel<<<1, 1 << kMaxRadixBits, 0, s>>>(counts, g.ctas, 1 << width);
       if (weighted)
         radix_downsweep_kernel<true><<<g.ctas, kSortThreads, smem, s>>>(
             keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], n, g, shift, width,

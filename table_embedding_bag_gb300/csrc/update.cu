@@ -205,29 +205,53 @@ __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4
 }
 
 // ------------------------------------------------------------- short runs
-// Group g of the warp owns run j0 + g: its pairs are loaded S at a time, one
+// A warp task: G consecutive runs of table t, run j0 + g for lane group g.
+// Its run data is fetched one task ahead (see short_runs_kernel).
+struct ShortTask {
+  int t;       // table, -1 when there is no task
+  int nv;      // float4 vectors per gradient row
+  uint32_t p0; // this lane group's first pair
+  uint32_t np; // and pair count (0: no run, or a long run)
+  uint32_t key;
+};
+
+__device__ __forceinline__ ShortTask fetch_task(const UpdArgs& a, const Meta& m, uint32_t task,
+                                                uint32_t ntasks) {
+  ShortTask st{-1, 0, 0, 0, 0};
+  if (task >= ntasks) return st;
+  const int t = find_table(m.tasks, a.T, task);
+  const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
+  if (D < 8 || D > kMaxD || (D & 7)) return st;  // widths the vector path cannot move
+  st.t = t;
+  st.nv = D >> 2;
+  const int S = update_lanes(st.nv);
+  const uint32_t G = 32 / S;
+  const uint32_t j = m.runs[t] + (task - m.tasks[t]) * G + lane_id() / S;
+  if (j < m.runs[t + 1]) {
+    st.p0 = __ldg(a.run_pairs + j);
+    st.np = __ldg(a.run_pairs + j + 1) - st.p0;
+    st.key = __ldg(a.unique_keys + j);
+  }
+  return st;
+}
+
+// Group g of the warp owns one run: its pairs are loaded S at a time, one
 // per lane of the group, and gathered U at a time.
 template <int S, int NC, bool kWeighted>
-__device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, int t, uint32_t j0,
-                                           uint32_t j_end) {
+__device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, const ShortTask& st) {
   // Row vectors in flight per lane: short runs hold few pairs, so the warp's
   // G concurrent runs, not a deep unroll, hide the latency.
   constexpr int U = TBE_SHORT_VECS / NC > 0 ? (TBE_SHORT_VECS / NC < S ? TBE_SHORT_VECS / NC : S) : 1;
   const int lane = static_cast<int>(lane_id());
-  const int g = lane / S;
   const int sl = lane % S;
+  const int t = st.t;
   const int64_t d0 = m.d_off[t];
   const int D = static_cast<int>(m.d_off[t + 1] - d0);
   const int nv = D >> 2;
-  const uint32_t j = j0 + g;
-  uint32_t p0 = 0, np = 0;
-  uint32_t key = 0;
-  if (j < j_end) {
-    p0 = __ldg(a.run_pairs + j);
-    np = __ldg(a.run_pairs + j + 1) - p0;
-    key = __ldg(a.unique_keys + j);
-    if (np >= static_cast<uint32_t>(kLongThreshold)) np = 0;  // chunked path owns it
-  }
+  const uint32_t p0 = st.p0;
+  const uint32_t key = st.key;
+  // the chunked path owns runs of kLongThreshold pairs or more
+  const uint32_t np = st.np >= static_cast<uint32_t>(kLongThreshold) ? 0u : st.np;
   const bool active = np > 0;
   __half* row = a.W + m.w_off[t] + (active ? (static_cast<int64_t>(key) - m.hb[t]) * D : 0);
   uint2 w_raw[NC];
@@ -263,31 +287,30 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, int 
 
 // kWide: the instantiation for rows wider than 512 values (eight vectors per
 // lane); the other one skips them, so that its register budget stays small.
+// kWide: the instantiation for rows wider than 512 values (eight vectors per
+// lane); the other one skips them, so that its register budget stays small.
 template <bool kWeighted, bool kWide>
 __global__ void __launch_bounds__(256, TBE_SHORT_MINB) short_runs_kernel(UpdArgs a) {
   __shared__ MetaSmem msm;
   const Meta m = load_meta(a, msm, true);
   const uint32_t ntasks = a.counters[kCntTasks];
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
-  for (uint32_t task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; task < ntasks;
-       task += warps) {
-    const int t = find_table(m.tasks, a.T, task);
-    const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
-    if (D < 8 || D > kMaxD || (D & 7)) continue;  // widths the vector path cannot move
-    const int nv = D >> 2;
-    if ((nv > 128) != kWide) continue;
-    const int S = update_lanes(nv);
-    const uint32_t G = 32 / S;
-    const uint32_t j0 = m.runs[t] + (task - m.tasks[t]) * G;
-    const uint32_t j_end = m.runs[t + 1];
-    if (kWide) short_task<32, 8, kWeighted>(a, m, t, j0, j_end);
-    else if (nv <= 2) short_task<2, 1, kWeighted>(a, m, t, j0, j_end);
-    else if (nv <= 4) short_task<4, 1, kWeighted>(a, m, t, j0, j_end);
-    else if (nv <= 8) short_task<8, 1, kWeighted>(a, m, t, j0, j_end);
-    else if (nv <= 16) short_task<8, 2, kWeighted>(a, m, t, j0, j_end);
-    else if (nv <= 32) short_task<8, 4, kWeighted>(a, m, t, j0, j_end);
-    else if (nv <= 64) short_task<16, 4, kWeighted>(a, m, t, j0, j_end);
-    else short_task<32, 4, kWeighted>(a, m, t, j0, j_end);
+  uint32_t task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  ShortTask cur = fetch_task(a, m, task, ntasks);
+  for (; task < ntasks; task += warps) {
+    const ShortTask next = fetch_task(a, m, task + warps, ntasks);  // one task ahead
+    const int nv = cur.nv;
+    if (cur.t >= 0 && (nv > 128) == kWide) {
+      if (kWide) short_task<32, 8, kWeighted>(a, m, cur);
+      else if (nv <= 2) short_task<2, 1, kWeighted>(a, m, cur);
+      else if (nv <= 4) short_task<4, 1, kWeighted>(a, m, cur);
+      else if (nv <= 8) short_task<8, 1, kWeighted>(a, m, cur);
+      else if (nv <= 16) short_task<8, 2, kWeighted>(a, m, cur);
+      else if (nv <= 32) short_task<8, 4, kWeighted>(a, m, cur);
+      else if (nv <= 64) short_task<16, 4, kWeighted>(a, m, cur);
+      else short_task<32, 4, kWeighted>(a, m, cur);
+    }
+    cur = next;
   }
 }
 
@@ -392,17 +415,16 @@ __device__ __forceinline__ void store_partial(float* dst, int nv, const float (&
 
 // Publish this warp's stores, then take one arrival off `counter`.  Returns
 // true for the last arriver, which may then read every other arriver's data.
+// Release: every lane fences its own stores before lane 0's decrement.
+// Acquire: only the last arriver fences again before reading.
 __device__ __forceinline__ bool arrive_last(uint32_t* counter) {
   __threadfence();
   __syncwarp();
   uint32_t prev = 0;
-  if (lane_id() == 0) {
-    prev = atomicSub(counter, 1u);
-    __threadfence();
-  }
+  if (lane_id() == 0) prev = atomicSub(counter, 1u);
   prev = __shfl_sync(kFull, prev, 0);
+  if (prev == 1u) __threadfence();
   __syncwarp();
-  __threadfence();
   return prev == 1u;
 }
 
