@@ -133,6 +133,28 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def profiled_traffic():
+    """DRAM bytes of one forward_generic_kernel launch on this workload, from
+    the committed ncu summary, if the kernel's sources are unchanged since
+    the capture (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "forward_generic_hot_row.md")
+    srcs = [os.path.join(ROOT, "table_embedding_bag_gb300", "csrc", f)
+            for f in ("forward.cu", "common.cuh")]
+    try:
+        text = open(path).read()
+        h = hashlib.sha1()
+        for f in srcs:
+            h.update(open(f, "rb").read())
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines()
+                  if line.startswith(("traffic_bytes_per_launch:", "source_sha1:")))
+    if fields.get("source_sha1", "").strip() != h.hexdigest()[:16]:
+        return None
+    return int(fields["traffic_bytes_per_launch"])
+
+
 def algorithmic_bytes(w, R):
     """Byte models of one step (see the design notes): `min` counts every
     distinct row once (the least DRAM traffic any implementation needs),
@@ -342,7 +364,8 @@ def main():
         "runs": {"R": r["R"], "long_runs": r["n_long"], "long_chunks": r["n_chunks"]},
         "roofline": {"kernel": "forward_generic_kernel (tbe_forward)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "peak_source": peak_src,
+                     "traffic": profiled_traffic() if args.tables is None else None,
+                     "peak_source": peak_src,
                      "bytes_model": "min: indices+offsets+distinct rows once+output",
                      "per_use_GBps": ab["fwd_per_use"] / fwd_s / 1e9},
         "clocks": r["clocks"],
