@@ -76,6 +76,7 @@ enum Counter : int {
   kCntTree = 4,      // internal reduction-tree nodes
   kCntTasks = 5,     // short-run warp tasks
   kCntPairs = 6,     // P: distinct (key, bag) pairs among the valid sorted lookups
+  kCntSortN = 7,     // entries in the sort (written on the device before the sort)
   kNumCounters = 8,
 };
 

@@ -80,15 +80,22 @@ __global__ void fill_tail_kernel(const IndexT* __restrict__ offsets, int64_t nb,
 }
 
 // -------------------------------------------------------------- radix sort
+// Persistent CTAs over the sorted range.  The number of entries is read from
+// device memory (counters[kCntSortN]), so it can be decided on the device;
+// the grid is sized on the host from an upper bound.
 struct SortGeom {
-  int ctas;           // persistent CTAs
-  int64_t tiles;      // kSortTile-key tiles
-  int64_t per_cta;    // tiles per CTA
+  int ctas;              // persistent CTAs
+  const uint32_t* n_dev; // entries to process
 };
 
+__device__ __forceinline__ int64_t geom_n(const SortGeom& g) { return static_cast<int64_t>(*g.n_dev); }
+
+// Tile range of this CTA: contiguous kSortTile-key tiles, split evenly.
 __device__ __forceinline__ void cta_range(const SortGeom& g, int64_t n, int64_t* b, int64_t* e) {
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * g.per_cta;
-  const int64_t t1 = t0 + g.per_cta < g.tiles ? t0 + g.per_cta : g.tiles;
+  const int64_t tiles = (n + kSortTile - 1) / kSortTile;
+  const int64_t per_cta = (tiles + g.ctas - 1) / g.ctas;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * per_cta;
+  const int64_t t1 = t0 + per_cta < tiles ? t0 + per_cta : tiles;
   *b = t0 * kSortTile;
   *e = t1 * kSortTile < n ? t1 * kSortTile : n;
   if (*b > n) *b = n;
@@ -96,8 +103,9 @@ __device__ __forceinline__ void cta_range(const SortGeom& g, int64_t n, int64_t*
 
 // Per-CTA digit histogram; counts stored CTA-major: counts[cta * 2^width + d].
 __global__ void __launch_bounds__(kSortThreads)
-    radix_upsweep_kernel(const uint32_t* __restrict__ keys, int64_t n, SortGeom g, int shift,
+    radix_upsweep_kernel(const uint32_t* __restrict__ keys, SortGeom g, int shift,
                          int width, uint32_t* __restrict__ counts) {
+  const int64_t n = geom_n(g);
   __shared__ uint32_t hist[kSortThreads / 32][1 << kMaxRadixBits];
   const int nd = 1 << width;
   const uint32_t mask = static_cast<uint32_t>(nd - 1);
@@ -226,8 +234,9 @@ __global__ void __launch_bounds__(kSortThreads, 2)
                            const uint32_t* __restrict__ vals_in,
                            const float* __restrict__ psw_in, uint32_t* __restrict__ keys_out,
                            uint32_t* __restrict__ vals_out, float* __restrict__ psw_out,
-                           int64_t n, SortGeom g, int shift, int width,
+                           SortGeom g, int shift, int width,
                            const uint32_t* __restrict__ counts) {
+  const int64_t n = geom_n(g);
   extern __shared__ __align__(16) unsigned char smem_raw[];
   DownSmem<kWeighted>& sm = *reinterpret_cast<DownSmem<kWeighted>*>(smem_raw);
   const int nd = 1 << width;
@@ -408,8 +417,9 @@ __device__ __forceinline__ void rle_heads(RleItems& it, uint32_t sentinel) {
 
 __global__ void __launch_bounds__(kRleThreads)
     rle_count_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ bags,
-                     int64_t n, SortGeom g, uint32_t sentinel, uint32_t* __restrict__ cta_runs,
+                     SortGeom g, uint32_t sentinel, uint32_t* __restrict__ cta_runs,
                      uint32_t* __restrict__ cta_pairs) {
+  const int64_t n = geom_n(g);
   __shared__ unsigned long long sm[33];
   int64_t b, e;
   cta_range(g, n, &b, &e);
@@ -436,12 +446,13 @@ __global__ void __launch_bounds__(kRleThreads)
 
 __global__ void __launch_bounds__(kRleThreads)
     rle_write_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restrict__ bags,
-                     int64_t n, SortGeom g, uint32_t sentinel,
+                     SortGeom g, uint32_t sentinel,
                      const uint32_t* __restrict__ run_base, const uint32_t* __restrict__ pair_base,
                      uint32_t* __restrict__ unique_keys, uint32_t* __restrict__ run_starts,
                      uint32_t* __restrict__ run_pairs, uint32_t* __restrict__ pair_starts,
                      uint32_t* __restrict__ pair_bags, uint32_t* __restrict__ counters) {
   __shared__ uint32_t sm[33];
+  const int64_t n = geom_n(g);
   int64_t b, e;
   cta_range(g, n, &b, &e);
   uint32_t r = run_base[blockIdx.x];
@@ -655,18 +666,21 @@ int key_bits(const tbe_desc* d) {
   return bits < 1 ? 1 : bits;
 }
 
-SortGeom sort_geom(int64_t n, int num_sms, int per_sm = 2) {
+// Grid of the sort / RLE kernels for at most n entries.
+SortGeom sort_geom(int64_t n, int num_sms, int per_sm, const uint32_t* n_dev) {
   SortGeom g;
-  g.tiles = (n + kSortTile - 1) / kSortTile;
+  const int64_t tiles = (n + kSortTile - 1) / kSortTile;
   int64_t ctas = static_cast<int64_t>(per_sm) * num_sms;
   if (ctas > kMaxSortCtas) ctas = kMaxSortCtas;
-  if (ctas > g.tiles) ctas = g.tiles;
+  if (ctas > tiles) ctas = tiles;
   if (ctas < 1) ctas = 1;
-  g.per_cta = (g.tiles + ctas - 1) / ctas;
-  g.ctas = static_cast<int>((g.tiles + g.per_cta - 1) / g.per_cta);
-  if (g.ctas < 1) g.ctas = 1;
+  g.ctas = static_cast<int>(ctas);
+  g.n_dev = n_dev;
   return g;
 }
+
+// One thread: the number of entries to sort (every lookup).
+__global__ void set_sort_n_kernel(uint32_t* counters, uint32_t n) { counters[kCntSortN] = n; }
 
 template <typename IndexT>
 cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const IndexT* indices,
@@ -710,8 +724,9 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
           status);
     fill_tail_kernel<IndexT><<<64, 256, 0, s>>>(offsets, nbags, n, sentinel, keys[0], vals[0],
                                                 pw[0]);
+    set_sort_n_kernel<<<1, 1, 0, s>>>(counters, static_cast<uint32_t>(n));
 
-    const SortGeom g = sort_geom(n, L.num_sms, 2);
+    const SortGeom g = sort_geom(n, L.num_sms, 2, counters + kCntSortN);
     const int bits = key_bits(d);
     const int passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
     const int rb = (bits + passes - 1) / passes;
@@ -721,27 +736,27 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
       const int shift = p * rb;
       const int width = rb < bits - shift ? rb : bits - shift;
       const int src = p & 1, dst = src ^ 1;
-      radix_upsweep_kernel<<<g.ctas, kSortThreads, 0, s>>>(keys[src], n, g, shift, width, counts);
+      radix_upsweep_kernel<<<g.ctas, kSortThreads, 0, s>>>(keys[src], g, shift, width, counts);
       radix_scan_kernel<<<1, 1 << kMaxRadixBits, 0, s>>>(counts, g.ctas, 1 << width);
       if (weighted)
         radix_downsweep_kernel<true><<<g.ctas, kSortThreads, smem, s>>>(
-            keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], n, g, shift, width,
+            keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], g, shift, width,
             counts);
       else
         radix_downsweep_kernel<false><<<g.ctas, kSortThreads, smem, s>>>(
-            keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], n, g, shift, width,
+            keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], g, shift, width,
             counts);
     }
     const int fin = passes & 1;
-    const SortGeom gr = sort_geom(n, L.num_sms, 6);
+    const SortGeom gr = sort_geom(n, L.num_sms, 6, counters + kCntSortN);
     uint32_t* cta_runs = reinterpret_cast<uint32_t*>(ws + W.cta_counts);
     uint32_t* cta_pairs = cta_runs + (kMaxSortCtas + 1);
-    rle_count_kernel<<<gr.ctas, kRleThreads, 0, s>>>(keys[fin], vals[fin], n, gr, sentinel,
+    rle_count_kernel<<<gr.ctas, kRleThreads, 0, s>>>(keys[fin], vals[fin], gr, sentinel,
                                                      cta_runs, cta_pairs);
     exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_runs, gr.ctas, cta_runs + gr.ctas);
     exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_pairs, gr.ctas, cta_pairs + gr.ctas);
     rle_write_kernel<<<gr.ctas, kRleThreads, 0, s>>>(
-        keys[fin], vals[fin], n, gr, sentinel, cta_runs, cta_pairs, uk, rs,
+        keys[fin], vals[fin], gr, sentinel, cta_runs, cta_pairs, uk, rs,
         reinterpret_cast<uint32_t*>(ws + W.run_pairs),
         reinterpret_cast<uint32_t*>(ws + W.pair_starts),
         reinterpret_cast<uint32_t*>(ws + W.pair_bags), counters);
