@@ -131,6 +131,9 @@ typedef struct tbe_ws_view {
   const uint32_t* run_pairs;    /* [R+1] first pair of each run; [R] = P */
   const uint32_t* pair_starts;  /* [P+1] first sorted position of each pair; [P] = n_valid */
   const uint32_t* pair_bags;    /* [P] bag of each pair */
+  const uint32_t* hot_keys;     /* [T][hot_slots] hot rows of each table (linear keys, sorted) */
+  const uint32_t* hot_n;        /* [T] hot rows per table */
+  int32_t hot_slots;            /* hot rows a table can have */
 } tbe_ws_view;
 
 /* Bytes of workspace needed for calls with at most n_max lookups.
@@ -223,7 +226,8 @@ tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits);
  * The first call on each device does the set-up (looks up the device address
  * of the array); make that first call before any stream capture.  Every call
  * shares the one array and it keeps the previous call's contents; everything
- * that must start at zero is cleared by the call itself.  Calls whose work
+ * that must start at zero is cleared by the call itself, including the
+ * hot-row set (see tbe_backward_rowwise_adagrad), so each call stands alone.  Calls whose work
  * overlaps on the GPU (different streams, or several host threads) race on
  * the array: serialise them.
  *

@@ -65,7 +65,9 @@ class tbe_ws_view(ctypes.Structure):
                 ("run_starts", ctypes.c_void_p), ("counts", ctypes.c_void_p),
                 ("long_runs", ctypes.c_void_p), ("long_threshold", ctypes.c_int32),
                 ("chunk", ctypes.c_int32), ("run_pairs", ctypes.c_void_p),
-                ("pair_starts", ctypes.c_void_p), ("pair_bags", ctypes.c_void_p)]
+                ("pair_starts", ctypes.c_void_p), ("pair_bags", ctypes.c_void_p),
+                ("hot_keys", ctypes.c_void_p), ("hot_n", ctypes.c_void_p),
+                ("hot_slots", ctypes.c_int32)]
 
 
 _lib = None

@@ -55,6 +55,18 @@ constexpr int kFanIn = 32;
 // Widest supported table row (elements); rows are moved in 16-byte vectors.
 constexpr int kMaxD = 1024;
 
+// Hot rows: per table, up to kHot rows (the most looked-up ones of the
+// previous backward) bypass the sort; their gradients are histogram(bag x hot
+// row)^T x grad_out.  The histogram is kept only if it fits kHotBudgetBytes,
+// and tables wider than kHotMaxD take no hot rows.
+constexpr int kHot = 64;
+constexpr int kHotTileBags = 128;  // bags per expand CTA (one table)
+constexpr int kHotMaxD = 256;
+constexpr size_t kHotBudgetBytes = size_t(2) << 30;
+constexpr int kHotCtaTarget = 320;  // CTAs of the hot-gradient kernel
+constexpr int kHotMinPartBags = 256;  // fewest bags per hot-gradient CTA
+constexpr int kHotBuckets = 256;    // log-scale buckets of lookup counts (8 per octave)
+
 // Long-run chunks are processed in order of the first bag they touch, binned
 // into at most this many bag bands, so that the warps in flight gather
 // gradient rows from a narrow band of bags and the band stays in L2.
@@ -106,10 +118,24 @@ struct WsLayout {
   size_t tree_cnt;     // uint32 [max_tree] arrivals still expected at each tree node
   size_t partials;     // float [max_chunks * max_D]
   size_t tree_part;    // float [max_tree * max_D]
+  size_t hot_keys;     // uint32 [T][kHot] hot rows (linear keys), kept across calls
+  size_t hot_n;        // uint32 [T] hot rows per table, kept across calls
+  size_t hot_cnt;      // uint32 [T][kHot] lookups of each hot row in this call
+  size_t hot_hist;     // float [T][kHot][B] per-bag weight of each hot row (if enabled)
+  size_t hot_part;     // float [T][hot_parts][kHot][kHotMaxD] partial hot gradients
+  size_t bag_cold;     // uint32 [T*B] cold lookups per bag
+  size_t tile_cold;    // uint32 [hot_tiles + 1] cold lookups per expand tile, then prefix
+  size_t sel_hist;     // uint32 [T][kHotBuckets] refresh: count buckets per table
+  size_t sel_thresh;   // uint32 [T] refresh: lowest bucket kept
+  size_t sel_keys;     // uint32 [T][kHot] refresh: the next hot set
+  size_t sel_n;        // uint32 [T]
   size_t offsets_fix;  // index type [T*B+1] repaired offsets
   size_t fix_scratch;  // int64 [blocks] block maxima for the repair scan
   size_t total;
   int64_t max_long, max_chunks, max_tree;
+  int64_t hot_tiles;   // expand CTAs: T * ceil(B / kHotTileBags)
+  int hot_parts;       // bag partitions per table in the hot-gradient kernel
+  bool hot_enabled;    // histogram fits the budget
   bool weighted;
 };
 

@@ -86,9 +86,15 @@ extern "C" tbe_status tbe_backward_rowwise_adagrad_noalloc(
   char* scratch = scratch_ptr();
   if (!scratch) return TBE_ECUDA;
   const Launch L{d, n, static_cast<cudaStream_t>(stream), sm_count()};
-  // Everything the kernels read before writing is reset by launch_preprocess
-  // (counters, first run and pair entries, band counts); the status word is
-  // not used because bounds reporting is not offered here.
+  // Each call stands alone: the hot-row set a previous call left in the
+  // scratch (possibly for another problem) is cleared, so no call's result
+  // depends on an earlier one.  Everything else the kernels read before
+  // writing is reset by launch_preprocess (counters, first run and pair
+  // entries, band counts); the status word is not used because bounds
+  // reporting is not offered here.
+  if (cudaMemsetAsync(scratch + W.hot_n, 0, static_cast<size_t>(d->T) * sizeof(uint32_t),
+                      L.s) != cudaSuccess)
+    return TBE_ECUDA;
   cudaError_t e = launch_preprocess(L, W, scratch, indices, offsets, per_sample_weights, false);
   if (e != cudaSuccess) return TBE_ECUDA;
   e = launch_update(L, W, scratch, grad_out, weights, momentum, lr, eps,

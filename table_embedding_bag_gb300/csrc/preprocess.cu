@@ -23,6 +23,8 @@
 //    (warp match + per-warp digit counters) and writes each digit's keys as
 //    one contiguous segment, so global stores stay coalesced.
 //  * invalid lookups get the key total_E and sort after every valid key.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -34,48 +36,234 @@ constexpr int kRleItems = 8;
 constexpr int kRleTile = kRleThreads * kRleItems;
 
 // ------------------------------------------------------------------ expand
-template <typename IndexT, bool kWeighted>
-__global__ void __launch_bounds__(256)
-    expand_kernel(const IndexT* __restrict__ indices, const IndexT* __restrict__ offsets,
-                  const float* __restrict__ psw, const int64_t* __restrict__ hash_base, int64_t n,
-                  int T, int B, uint32_t sentinel, uint32_t* __restrict__ keys,
-                  uint32_t* __restrict__ vals, float* __restrict__ psw_out, int* status) {
-  const int warps = blockDim.x >> 5;
-  const int64_t nbags = static_cast<int64_t>(T) * B;
-  const unsigned lane = lane_id();
-  bool bad = false;
-  for (int64_t bag = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5); bag < nbags;
-       bag += static_cast<int64_t>(gridDim.x) * warps) {
-    const int t = static_cast<int>(bag / B);
-    const uint32_t b = static_cast<uint32_t>(bag - static_cast<int64_t>(t) * B);
-    const int64_t h0 = __ldg(hash_base + t);
-    const int64_t E = __ldg(hash_base + t + 1) - h0;
-    int64_t s, e;
-    bag_range(offsets, bag, n, &s, &e);
-    for (int64_t i = s + lane; i < e; i += 32) {
-      const int64_t r = load_index(indices, i);
-      const bool ok = r >= 0 && r < E;
-      bad |= !ok;
-      keys[i] = ok ? static_cast<uint32_t>(h0 + r) : sentinel;
-      vals[i] = b;
-      if (kWeighted) psw_out[i] = __ldg(psw + i);
+// One CTA per tile of kHotTileBags consecutive bags of one table.  A lookup
+// whose row is in the table's hot set adds its weight (1 without per-sample
+// weights) to the tile's histogram hot_hist[t][slot][bag]; every other valid
+// lookup is cold and goes to the sort.  Out-of-range lookups go nowhere.
+// Pass 1 (count) fills the histogram and counts cold lookups per bag and per
+// tile; a scan of the tile counts gives each tile's first sort position;
+// pass 2 (write) writes the cold lookups in position order, so the sort's
+// input order, and hence its stability, is the lookup order.
+
+// Hot-set membership: an open-addressing hash of the table's hot keys in
+// shared memory (twice as many entries as keys, linear probing).
+constexpr int kHotHash = 2 * kHot;
+constexpr uint32_t kEmptyKey = 0xffffffffu;
+
+struct HotHash {
+  uint32_t key[kHotHash];
+  uint8_t slot[kHotHash];
+};
+
+__device__ __forceinline__ uint32_t hot_hash(uint32_t key) {
+  return (key * 2654435761u) >> (32 - 7);  // 7 bits: kHotHash = 128
+}
+
+// Slot of `key` in the hot set, or -1.
+__device__ __forceinline__ int hot_lookup(const HotHash& h, uint32_t key) {
+  uint32_t i = hot_hash(key);
+#pragma unroll 1
+  for (int probe = 0; probe < kHotHash; ++probe) {
+    const uint32_t k = h.key[i];
+    if (k == key) return h.slot[i];
+    if (k == kEmptyKey) return -1;
+    i = (i + 1) & (kHotHash - 1);
+  }
+  return -1;
+}
+
+struct TileInfo {
+  int t;
+  int64_t b0;
+  int nbags;
+};
+
+__device__ __forceinline__ TileInfo tile_info(int B) {
+  const int64_t per_table = (B + kHotTileBags - 1) / kHotTileBags;
+  TileInfo ti;
+  ti.t = static_cast<int>(blockIdx.x / per_table);
+  ti.b0 = (blockIdx.x % per_table) * kHotTileBags;
+  ti.nbags = static_cast<int>(B - ti.b0 < kHotTileBags ? B - ti.b0 : kHotTileBags);
+  return ti;
+}
+
+// Builds the hash of table t's hot set (empty when the histogram is disabled
+// or the table is too wide for the hot path); returns the number of hot rows.
+// Contains __syncthreads.
+__device__ int build_hot_hash(HotHash& h, const uint32_t* hot_keys, const uint32_t* hot_n,
+                              const int64_t* D_offsets, int t, bool enabled) {
+  int nh = 0;
+  if (enabled) {
+    const int D = static_cast<int>(__ldg(D_offsets + t + 1) - __ldg(D_offsets + t));
+    nh = D <= kHotMaxD ? static_cast<int>(min(hot_n[t], static_cast<uint32_t>(kHot))) : 0;
+  }
+  for (int i = threadIdx.x; i < kHotHash; i += blockDim.x) h.key[i] = kEmptyKey;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nh; ++s) {
+      const uint32_t key = hot_keys[t * kHot + s];
+      uint32_t i = hot_hash(key);
+      while (h.key[i] != kEmptyKey && h.key[i] != key) i = (i + 1) & (kHotHash - 1);
+      h.key[i] = key;
+      h.slot[i] = static_cast<uint8_t>(s);
     }
   }
+  __syncthreads();
+  return nh;
+}
+
+template <typename IndexT, bool kWeighted>
+struct ExpandSmem {
+  HotHash hash;
+  uint32_t slot_cnt[kHot];
+  uint32_t warp_cold[8];
+  // per-bag weight of each hot row: exact sums (integer counts, or fp32
+  // weights summed in double), so the result does not depend on atomic order
+  typename std::conditional<kWeighted, double, uint32_t>::type hist[kHot][kHotTileBags];
+};
+
+constexpr int kExpandLoads = 4;  // index loads in flight per lane
+
+template <typename IndexT, bool kWeighted>
+__global__ void __launch_bounds__(256)
+    expand_count_kernel(const IndexT* __restrict__ indices, const IndexT* __restrict__ offsets,
+                        const float* __restrict__ psw, const int64_t* __restrict__ hash_base,
+                        const int64_t* __restrict__ D_offsets, int64_t n, int B,
+                        const uint32_t* __restrict__ hot_keys, const uint32_t* __restrict__ hot_n,
+                        float* __restrict__ hot_hist, uint32_t* __restrict__ hot_cnt,
+                        uint32_t* __restrict__ bag_cold, uint32_t* __restrict__ tile_cold,
+                        int* status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  ExpandSmem<IndexT, kWeighted>& sm = *reinterpret_cast<ExpandSmem<IndexT, kWeighted>*>(smem_raw);
+  const TileInfo ti = tile_info(B);
+  const int warp = threadIdx.x >> 5;
+  const unsigned lane = lane_id();
+  for (int i = threadIdx.x; i < kHot; i += blockDim.x) sm.slot_cnt[i] = 0;
+  for (int i = threadIdx.x; i < kHot * kHotTileBags; i += blockDim.x)
+    sm.hist[i / kHotTileBags][i % kHotTileBags] = 0;
+  const int nh = build_hot_hash(sm.hash, hot_keys, hot_n, D_offsets, ti.t, hot_hist != nullptr);
+  const int64_t h0 = __ldg(hash_base + ti.t);
+  const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
+  bool bad = false;
+  uint32_t cold_w = 0;
+  for (int lb = warp; lb < ti.nbags; lb += 8) {
+    const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
+    int64_t s, e;
+    bag_range(offsets, bag, n, &s, &e);
+    uint32_t cold = 0;
+    for (int64_t base = s; base < e; base += 32 * kExpandLoads) {
+      int64_t r[kExpandLoads];
+#pragma unroll
+      for (int u = 0; u < kExpandLoads; ++u) {
+        const int64_t i = base + u * 32 + lane;
+        r[u] = i < e ? load_index(indices, i) : -2;  // -2: past the bag's end
+      }
+#pragma unroll
+      for (int u = 0; u < kExpandLoads; ++u) {
+        if (base + u * 32 >= e) break;  // warp-uniform
+        const bool inside = r[u] != -2;
+        const bool ok = inside && r[u] >= 0 && r[u] < E;
+        bad |= inside && !ok;
+        const int slot = ok && nh ? hot_lookup(sm.hash, static_cast<uint32_t>(h0 + r[u])) : -1;
+        cold += ok && slot < 0;
+        if constexpr (kWeighted) {
+          // double sums of fp32 weights are exact: atomic order does not matter
+          if (slot >= 0) {
+            atomicAdd(&sm.hist[slot][lb], static_cast<double>(__ldg(psw + base + u * 32 + lane)));
+            atomicAdd(&sm.slot_cnt[slot], 1u);
+          }
+        } else {
+          // one add per distinct hot row of the 32 lookups
+          const unsigned peers = __match_any_sync(kFull, slot);
+          if (slot >= 0 && lane == static_cast<unsigned>(__ffs(peers) - 1)) {
+            const uint32_t c = static_cast<uint32_t>(__popc(peers));
+            atomicAdd(&sm.hist[slot][lb], c);
+            atomicAdd(&sm.slot_cnt[slot], c);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cold += __shfl_xor_sync(kFull, cold, o);
+    if (lane == 0) bag_cold[bag] = cold;
+    cold_w += cold;
+  }
+  if (lane == 0) sm.warp_cold[warp] = cold_w;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t c = 0;
+    for (int w = 0; w < 8; ++w) c += sm.warp_cold[w];
+    tile_cold[blockIdx.x] = c;
+  }
+  for (int i = threadIdx.x; i < nh * kHotTileBags; i += blockDim.x) {
+    const int slot = i / kHotTileBags, lb = i % kHotTileBags;
+    if (lb < ti.nbags)
+      hot_hist[(static_cast<int64_t>(ti.t) * kHot + slot) * B + ti.b0 + lb] =
+          static_cast<float>(sm.hist[slot][lb]);
+  }
+  for (int i = threadIdx.x; i < nh; i += blockDim.x)
+    if (sm.slot_cnt[i]) atomicAdd(&hot_cnt[ti.t * kHot + i], sm.slot_cnt[i]);
   if (status && __any_sync(kFull, bad) && lane == 0) set_status(status, TBE_ERR_INDEX_RANGE);
 }
 
-// Lookups after the last bag (positions offsets[T*B] .. n-1) belong to no bag.
-template <typename IndexT>
-__global__ void fill_tail_kernel(const IndexT* __restrict__ offsets, int64_t nb, int64_t n,
-                                 uint32_t sentinel, uint32_t* __restrict__ keys,
-                                 uint32_t* __restrict__ vals, float* __restrict__ psw_out) {
-  int64_t o = load_index(offsets, nb);
-  o = o < 0 ? 0 : (o > n ? n : o);
-  for (int64_t i = o + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    keys[i] = sentinel;
-    vals[i] = 0;
-    if (psw_out) psw_out[i] = 0.f;
+template <typename IndexT, bool kWeighted>
+__global__ void __launch_bounds__(256)
+    expand_write_kernel(const IndexT* __restrict__ indices, const IndexT* __restrict__ offsets,
+                        const float* __restrict__ psw, const int64_t* __restrict__ hash_base,
+                        const int64_t* __restrict__ D_offsets, int64_t n, int B,
+                        const uint32_t* __restrict__ hot_keys, const uint32_t* __restrict__ hot_n,
+                        bool hot_enabled, const uint32_t* __restrict__ bag_cold,
+                        const uint32_t* __restrict__ tile_base, uint32_t* __restrict__ keys,
+                        uint32_t* __restrict__ vals, float* __restrict__ psw_out) {
+  __shared__ HotHash hash;
+  __shared__ uint32_t bag_base[kHotTileBags];
+  __shared__ uint32_t scan[33];
+  const TileInfo ti = tile_info(B);
+  const int warp = threadIdx.x >> 5;
+  const unsigned lane = lane_id();
+  {
+    // exclusive prefix of the tile's per-bag cold counts
+    const int lb = threadIdx.x;
+    const uint32_t c =
+        lb < ti.nbags ? bag_cold[static_cast<int64_t>(ti.t) * B + ti.b0 + lb] : 0u;
+    const uint32_t inc = block_inclusive_scan(c, OpSum(), 0u, scan);
+    if (lb < kHotTileBags) bag_base[lb] = tile_base[blockIdx.x] + inc - c;
+  }
+  const int nh = build_hot_hash(hash, hot_keys, hot_n, D_offsets, ti.t, hot_enabled);
+  const int64_t h0 = __ldg(hash_base + ti.t);
+  const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int lb = warp; lb < ti.nbags; lb += 8) {
+    const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
+    int64_t s, e;
+    bag_range(offsets, bag, n, &s, &e);
+    uint32_t pos = bag_base[lb];
+    for (int64_t base = s; base < e; base += 32 * kExpandLoads) {
+      int64_t r[kExpandLoads];
+#pragma unroll
+      for (int u = 0; u < kExpandLoads; ++u) {
+        const int64_t i = base + u * 32 + lane;
+        r[u] = i < e ? load_index(indices, i) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kExpandLoads; ++u) {
+        if (base + u * 32 >= e) break;  // warp-uniform
+        bool cold = false;
+        uint32_t key = 0;
+        if (r[u] >= 0 && r[u] < E) {
+          key = static_cast<uint32_t>(h0 + r[u]);
+          cold = !nh || hot_lookup(hash, key) < 0;
+        }
+        const unsigned m = __ballot_sync(kFull, cold);
+        if (cold) {
+          const uint32_t p = pos + __popc(m & lt);
+          keys[p] = key;
+          vals[p] = static_cast<uint32_t>(ti.b0 + lb);
+          if (kWeighted) psw_out[p] = __ldg(psw + base + u * 32 + lane);
+        }
+        pos += __popc(m);
+      }
+    }
   }
 }
 
@@ -679,9 +867,6 @@ SortGeom sort_geom(int64_t n, int num_sms, int per_sm, const uint32_t* n_dev) {
   return g;
 }
 
-// One thread: the number of entries to sort (every lookup).
-__global__ void set_sort_n_kernel(uint32_t* counters, uint32_t n) { counters[kCntSortN] = n; }
-
 template <typename IndexT>
 cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const IndexT* indices,
                          const IndexT* offsets, const float* psw, bool check) {
@@ -710,22 +895,37 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
   err = cudaMemsetAsync(ws + W.pair_starts, 0, sizeof(uint32_t), s);
   if (err != cudaSuccess) return err;
 
-  if (n > 0) {
-    const int64_t nbags = static_cast<int64_t>(d->T) * d->B;
-    int64_t blocks = (nbags + 7) / 8;
-    if (blocks > (1 << 22)) blocks = 1 << 22;
+  // Expand: hot lookups into the histogram, cold ones (in lookup order) to the sort.
+  uint32_t* tile_cold = reinterpret_cast<uint32_t*>(ws + W.tile_cold);
+  {
+    err = cudaMemsetAsync(ws + W.hot_cnt, 0, static_cast<size_t>(d->T) * kHot * 4, s);
+    if (err != cudaSuccess) return err;
+    const uint32_t* hk = reinterpret_cast<const uint32_t*>(ws + W.hot_keys);
+    const uint32_t* hn = reinterpret_cast<const uint32_t*>(ws + W.hot_n);
+    float* hh = W.hot_enabled ? reinterpret_cast<float*>(ws + W.hot_hist) : nullptr;
+    uint32_t* hc = reinterpret_cast<uint32_t*>(ws + W.hot_cnt);
+    uint32_t* bc = reinterpret_cast<uint32_t*>(ws + W.bag_cold);
+    const unsigned tiles = static_cast<unsigned>(W.hot_tiles);
     if (weighted)
-      expand_kernel<IndexT, true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-          indices, offsets, psw, d->hash_base, n, d->T, d->B, sentinel, keys[0], vals[0], pw[0],
-          status);
+      expand_count_kernel<IndexT, true><<<tiles, 256, sizeof(ExpandSmem<IndexT, true>), s>>>(
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hh, hc, bc,
+          tile_cold, status);
     else
-      expand_kernel<IndexT, false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-          indices, offsets, psw, d->hash_base, n, d->T, d->B, sentinel, keys[0], vals[0], pw[0],
-          status);
-    fill_tail_kernel<IndexT><<<64, 256, 0, s>>>(offsets, nbags, n, sentinel, keys[0], vals[0],
-                                                pw[0]);
-    set_sort_n_kernel<<<1, 1, 0, s>>>(counters, static_cast<uint32_t>(n));
+      expand_count_kernel<IndexT, false><<<tiles, 256, sizeof(ExpandSmem<IndexT, false>), s>>>(
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hh, hc, bc,
+          tile_cold, status);
+    exclusive_scan_kernel<<<1, 1024, 0, s>>>(tile_cold, W.hot_tiles, counters + kCntSortN);
+    if (weighted)
+      expand_write_kernel<IndexT, true><<<tiles, 256, 0, s>>>(
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, W.hot_enabled, bc,
+          tile_cold, keys[0], vals[0], pw[0]);
+    else
+      expand_write_kernel<IndexT, false><<<tiles, 256, 0, s>>>(
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, W.hot_enabled, bc,
+          tile_cold, keys[0], vals[0], pw[0]);
+  }
 
+  if (n > 0) {
     const SortGeom g = sort_geom(n, L.num_sms, 2, counters + kCntSortN);
     const int bits = key_bits(d);
     const int passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
@@ -811,7 +1011,15 @@ int radix_passes(const tbe_desc* d) {
 }
 
 cudaError_t prepare_preprocess_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(radix_downsweep_kernel<true>,
+  cudaError_t e = cudaFuncSetAttribute(expand_count_kernel<int32_t, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(ExpandSmem<int32_t, true>)));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(expand_count_kernel<int64_t, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sizeof(ExpandSmem<int64_t, true>)));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(radix_downsweep_kernel<true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sizeof(DownSmem<true>)));
   if (e != cudaSuccess) return e;

@@ -48,7 +48,26 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   L.tree_cnt = take(L.max_tree * 4);
   L.partials = take(static_cast<size_t>(L.max_chunks) * d->max_D * 4);
   L.tree_part = take(static_cast<size_t>(L.max_tree) * d->max_D * 4);
-  const int64_t nb1 = static_cast<int64_t>(d->T) * d->B + 1;
+  const int64_t T = d->T, B = d->B;
+  L.hot_tiles = T * ((B + kHotTileBags - 1) / kHotTileBags);
+  // hot-gradient partitions: about kHotCtaTarget CTAs in all, at least
+  // kHotMinPartBags bags each
+  L.hot_parts = static_cast<int>(kHotCtaTarget / T > 0 ? kHotCtaTarget / T : 1);
+  const int64_t max_parts = (B + kHotMinPartBags - 1) / kHotMinPartBags;
+  if (L.hot_parts > max_parts) L.hot_parts = static_cast<int>(max_parts);
+  L.hot_enabled = static_cast<size_t>(T) * kHot * B * sizeof(float) <= kHotBudgetBytes;
+  L.hot_keys = take(T * kHot * 4);
+  L.hot_n = take(T * 4);
+  L.hot_cnt = take(T * kHot * 4);
+  L.hot_hist = L.hot_enabled ? take(static_cast<size_t>(T) * kHot * B * sizeof(float)) : 0;
+  L.hot_part = L.hot_enabled ? take(static_cast<size_t>(T) * L.hot_parts * kHot * kHotMaxD * 4) : 0;
+  L.bag_cold = take(static_cast<size_t>(T) * B * 4);
+  L.tile_cold = take((L.hot_tiles + 1) * 4);
+  L.sel_hist = take(T * kHotBuckets * 4);
+  L.sel_thresh = take(T * 4);
+  L.sel_keys = take(T * kHot * 4);
+  L.sel_n = take(T * 4);
+  const int64_t nb1 = T * B + 1;
   L.offsets_fix = take(nb1 * index_bytes(d));
   L.fix_scratch = take(repair_scratch_blocks(nb1) * sizeof(int64_t));
   L.total = off;
@@ -229,6 +248,9 @@ tbe_status tbe_workspace_view(const tbe_desc* d, int64_t n, uint32_t ws_flags, v
   view->run_pairs = reinterpret_cast<const uint32_t*>(ws + W.run_pairs);
   view->pair_starts = reinterpret_cast<const uint32_t*>(ws + W.pair_starts);
   view->pair_bags = reinterpret_cast<const uint32_t*>(ws + W.pair_bags);
+  view->hot_keys = reinterpret_cast<const uint32_t*>(ws + W.hot_keys);
+  view->hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n);
+  view->hot_slots = kHot;
   view->long_threshold = kLongThreshold;
   view->chunk = kChunk;
   return TBE_OK;

@@ -545,6 +545,257 @@ __global__ void __launch_bounds__(256, 3) long_finish_kernel(UpdArgs a) {
   }
 }
 
+// --------------------------------------------------------------- hot rows
+// The gradient of a hot row is sum_b hist[t][slot][b] * grad_out[b, D_off[t]:]:
+// one pass over the table's gradient rows serves all its hot rows.  CTA
+// (t, p) sums bag partition p of table t; thread items are 4 hot slots x 8
+// columns, read from shared-memory chunks of 32 bags.
+constexpr int kHotChunk = 32;
+
+template <int kItems>
+__global__ void __launch_bounds__(256)
+    hot_grad_kernel(UpdArgs a, const float* __restrict__ hot_hist,
+                    const uint32_t* __restrict__ hot_n, int parts, float* __restrict__ hot_part) {
+  __shared__ float hs[kHot][kHotChunk];
+  __shared__ __align__(16) float gs[kHotChunk][kHotMaxD];
+  const int t = blockIdx.x / parts;
+  const int p = blockIdx.x % parts;
+  const int nh = static_cast<int>(min(hot_n[t], static_cast<uint32_t>(kHot)));
+  const int64_t d0 = a.D_offsets[t];
+  const int D = static_cast<int>(a.D_offsets[t + 1] - d0);
+  if (nh == 0 || D > kHotMaxD || (D & 7)) return;  // uniform over the CTA
+  const int ndg = D >> 3;                          // column groups of 8
+  const int nsg = (nh + 3) >> 2;                   // slot groups of 4
+  const int64_t B = a.B;
+  const int64_t b_begin = B * p / parts, b_end = B * (p + 1) / parts;
+  float acc[kItems][4][8];
+#pragma unroll
+  for (int k = 0; k < kItems; ++k)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[k][i][j] = 0.f;
+  for (int64_t c0 = b_begin; c0 < b_end; c0 += kHotChunk) {
+    const int cnt = static_cast<int>(b_end - c0 < kHotChunk ? b_end - c0 : kHotChunk);
+    for (int i = threadIdx.x; i < kHot * kHotChunk; i += blockDim.x) {
+      const int slot = i / kHotChunk, j = i % kHotChunk;
+      hs[slot][j] = slot < nh && j < cnt
+                        ? __ldg(hot_hist + (static_cast<int64_t>(t) * kHot + slot) * B + c0 + j)
+                        : 0.f;
+    }
+    const int nq = D >> 2;
+    for (int i = threadIdx.x; i < kHotChunk * nq; i += blockDim.x) {
+      const int j = i / nq, q = i % nq;
+      const float4 v = j < cnt ? ldg_f4(a.grad_out + (c0 + j) * a.total_D + d0 + q * 4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(&gs[j][q * 4]) = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const int item = threadIdx.x + k * blockDim.x;
+      const int sg = item / ndg, dg = item % ndg;
+      if (sg < nsg) {
+        for (int j = 0; j < cnt; ++j) {
+          float h[4], g[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) h[i] = hs[sg * 4 + i][j];
+          const float4 g0 = *reinterpret_cast<const float4*>(&gs[j][dg * 8]);
+          const float4 g1 = *reinterpret_cast<const float4*>(&gs[j][dg * 8 + 4]);
+          g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+          g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) acc[k][i][jj] = fmaf(h[i], g[jj], acc[k][i][jj]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const int item = threadIdx.x + k * blockDim.x;
+    const int sg = item / ndg, dg = item % ndg;
+    if (sg < nsg) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float* dst = hot_part + ((static_cast<int64_t>(t) * parts + p) * kHot + sg * 4 + i) * kHotMaxD +
+                     dg * 8;
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[k][i][0], acc[k][i][1], acc[k][i][2], acc[k][i][3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[k][i][4], acc[k][i][5], acc[k][i][6], acc[k][i][7]);
+      }
+    }
+  }
+}
+
+// One CTA per hot row that was looked up in this call: warp w adds the
+// partitions w, w + 8, ... in order, warp 0 adds the eight warp sums in order
+// (a fixed order, so the result is reproducible), then applies the row-wise
+// Adagrad step.
+__global__ void __launch_bounds__(256)
+    hot_finish_kernel(UpdArgs a, const uint32_t* __restrict__ hot_keys,
+                      const uint32_t* __restrict__ hot_n, const uint32_t* __restrict__ hot_cnt,
+                      int parts, const float* __restrict__ hot_part) {
+  __shared__ __align__(16) float wsum[8][kHotMaxD];
+  const int t = static_cast<int>(blockIdx.x / kHot), slot = static_cast<int>(blockIdx.x % kHot);
+  if (slot >= static_cast<int>(min(hot_n[t], static_cast<uint32_t>(kHot))) ||
+      hot_cnt[blockIdx.x] == 0)
+    return;  // uniform over the CTA
+  const int D = static_cast<int>(a.D_offsets[t + 1] - a.D_offsets[t]);
+  if (D > kHotMaxD || (D & 7)) return;
+  const int warp = threadIdx.x >> 5;
+  const int lane = static_cast<int>(lane_id());
+  const int nv = D >> 2;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int vec = lane + c * 32;
+    if (vec < nv) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float* src = hot_part + (static_cast<int64_t>(t) * parts * kHot + slot) * kHotMaxD + vec * 4;
+#pragma unroll 4
+      for (int p = warp; p < parts; p += 8) {
+        const float4 v = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(p) * kHot * kHotMaxD);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      *reinterpret_cast<float4*>(&wsum[warp][vec * 4]) = acc;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float acc[2][4];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int vec = lane + c * 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[c][i] = 0.f;
+    if (vec < nv)
+      for (int w = 0; w < 8; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(&wsum[w][vec * 4]);
+        acc[c][0] += v.x; acc[c][1] += v.y; acc[c][2] += v.z; acc[c][3] += v.w;
+      }
+  }
+  const uint32_t key = hot_keys[blockIdx.x];
+  __half* row = a.W + a.w_offsets[t] + (static_cast<int64_t>(key) - a.hash_base[t]) * D;
+  uint2 w_raw[2];
+  load_row<32, 2>(row, nv, w_raw, true);
+  const float m_old = a.momentum[key];
+  adagrad_apply<32, 2>(a, acc, D, key, row, w_raw, m_old, true);
+}
+
+// ------------------------------------------------------ hot set refresh
+// The next call's hot rows: per table, the rows with the most lookups in
+// this call (cold runs and current hot rows alike), at most kHot of them and
+// only rows looked up at least min_count times.  Counts go to log-scale
+// buckets (8 per octave); the cut is the lowest bucket whose suffix fits.
+__device__ __forceinline__ int count_bucket(uint32_t c) {
+  const int e = 31 - __clz(c);
+  const uint32_t frac = e >= 3 ? (c >> (e - 3)) & 7u : (c << (3 - e)) & 7u;
+  return e * 8 + static_cast<int>(frac);
+}
+
+// Candidate i: cold runs first, then the current hot slots.
+__device__ __forceinline__ bool hot_candidate(const UpdArgs& a, const Meta& m, uint32_t i,
+                                              uint32_t R, const uint32_t* run_starts,
+                                              const uint32_t* hot_keys, const uint32_t* hot_n,
+                                              const uint32_t* hot_cnt, uint32_t min_count,
+                                              int* t_out, uint32_t* key_out, uint32_t* cnt_out) {
+  int t;
+  uint32_t key, cnt;
+  if (i < R) {
+    key = a.unique_keys[i];
+    cnt = run_starts[i + 1] - run_starts[i];
+    int lo = 0, hi = a.T - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (m.hb[mid] <= static_cast<int64_t>(key)) lo = mid; else hi = mid - 1;
+    }
+    t = lo;
+  } else {
+    const uint32_t w = i - R;
+    t = static_cast<int>(w / kHot);
+    if (w % kHot >= min(hot_n[t], static_cast<uint32_t>(kHot))) return false;
+    key = hot_keys[w];
+    cnt = hot_cnt[w];
+  }
+  if (cnt < min_count || m.d_off[t + 1] - m.d_off[t] > kHotMaxD) return false;
+  *t_out = t;
+  *key_out = key;
+  *cnt_out = cnt;
+  return true;
+}
+
+__global__ void __launch_bounds__(256)
+    hot_hist_kernel(UpdArgs a, const uint32_t* __restrict__ run_starts,
+                    const uint32_t* __restrict__ hot_keys, const uint32_t* __restrict__ hot_n,
+                    const uint32_t* __restrict__ hot_cnt, uint32_t min_count,
+                    uint32_t* __restrict__ sel_hist) {
+  __shared__ MetaSmem msm;
+  const Meta m = load_meta(a, msm, false);
+  const uint32_t R = a.counters[kCntRuns];
+  const uint32_t total = R + static_cast<uint32_t>(a.T) * kHot;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    int t;
+    uint32_t key, cnt;
+    if (hot_candidate(a, m, i, R, run_starts, hot_keys, hot_n, hot_cnt, min_count, &t, &key, &cnt))
+      atomicAdd(&sel_hist[t * kHotBuckets + count_bucket(cnt)], 1u);
+  }
+}
+
+__global__ void hot_thresh_kernel(int T, const uint32_t* __restrict__ sel_hist,
+                                  uint32_t* __restrict__ sel_thresh) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+    uint32_t acc = 0, cut = 0;
+    for (int b = kHotBuckets - 1; b >= 0; --b) {
+      acc += sel_hist[t * kHotBuckets + b];
+      if (acc > static_cast<uint32_t>(kHot)) {
+        cut = static_cast<uint32_t>(b + 1);
+        break;
+      }
+    }
+    sel_thresh[t] = cut;
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    hot_select_kernel(UpdArgs a, const uint32_t* __restrict__ run_starts,
+                      const uint32_t* __restrict__ hot_keys, const uint32_t* __restrict__ hot_n,
+                      const uint32_t* __restrict__ hot_cnt, uint32_t min_count,
+                      const uint32_t* __restrict__ sel_thresh, uint32_t* __restrict__ sel_keys,
+                      uint32_t* __restrict__ sel_n) {
+  __shared__ MetaSmem msm;
+  const Meta m = load_meta(a, msm, false);
+  const uint32_t R = a.counters[kCntRuns];
+  const uint32_t total = R + static_cast<uint32_t>(a.T) * kHot;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    int t;
+    uint32_t key, cnt;
+    if (hot_candidate(a, m, i, R, run_starts, hot_keys, hot_n, hot_cnt, min_count, &t, &key, &cnt) &&
+        static_cast<uint32_t>(count_bucket(cnt)) >= sel_thresh[t]) {
+      const uint32_t slot = atomicAdd(&sel_n[t], 1u);
+      if (slot < static_cast<uint32_t>(kHot)) sel_keys[t * kHot + slot] = key;
+    }
+  }
+}
+
+// The selected keys, sorted per table, become the hot set.
+__global__ void hot_commit_kernel(int T, const uint32_t* __restrict__ sel_keys,
+                                  const uint32_t* __restrict__ sel_n, uint32_t* __restrict__ hot_keys,
+                                  uint32_t* __restrict__ hot_n) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+    const uint32_t nsel = min(sel_n[t], static_cast<uint32_t>(kHot));
+    uint32_t k[kHot];
+    for (uint32_t i = 0; i < nsel; ++i) {
+      uint32_t v = sel_keys[t * kHot + i];
+      uint32_t j = i;
+      for (; j > 0 && k[j - 1] > v; --j) k[j] = k[j - 1];
+      k[j] = v;
+    }
+    for (uint32_t i = 0; i < nsel; ++i) hot_keys[t * kHot + i] = k[i];
+    hot_n[t] = nsel;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const float* grad_out,
@@ -593,6 +844,37 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
     long_finish_kernel<false><<<blocks, 256, 0, L.s>>>(a);
     if (wide) long_finish_kernel<true><<<blocks, 256, 0, L.s>>>(a);
   }
+  // Hot rows: gradient from the histogram, update, then choose the next set.
+  uint32_t* hot_keys = reinterpret_cast<uint32_t*>(ws + W.hot_keys);
+  uint32_t* hot_n = reinterpret_cast<uint32_t*>(ws + W.hot_n);
+  const uint32_t* hot_cnt = reinterpret_cast<const uint32_t*>(ws + W.hot_cnt);
+  if (W.hot_enabled) {
+    float* part = reinterpret_cast<float*>(ws + W.hot_part);
+    const float* hist = reinterpret_cast<const float*>(ws + W.hot_hist);
+    const unsigned hg = static_cast<unsigned>(d->T) * W.hot_parts;
+    if (d->max_D <= 128)
+      hot_grad_kernel<1><<<hg, 256, 0, L.s>>>(a, hist, hot_n, W.hot_parts, part);
+    else
+      hot_grad_kernel<2><<<hg, 256, 0, L.s>>>(a, hist, hot_n, W.hot_parts, part);
+    hot_finish_kernel<<<static_cast<unsigned>(d->T) * kHot, 256, 0, L.s>>>(
+        a, hot_keys, hot_n, hot_cnt, W.hot_parts, part);
+  }
+  if (!W.hot_enabled) return cudaGetLastError();  // no histogram: the hot set stays empty
+  cudaError_t e = cudaMemsetAsync(ws + W.sel_hist, 0, static_cast<size_t>(d->T) * kHotBuckets * 4, L.s);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(ws + W.sel_n, 0, static_cast<size_t>(d->T) * 4, L.s);
+  if (e != cudaSuccess) return e;
+  const uint32_t min_count = d->B / 8 > 32 ? static_cast<uint32_t>(d->B / 8) : 32u;
+  const uint32_t* rs = reinterpret_cast<const uint32_t*>(ws + W.run_starts);
+  uint32_t* sel_hist = reinterpret_cast<uint32_t*>(ws + W.sel_hist);
+  uint32_t* sel_thresh = reinterpret_cast<uint32_t*>(ws + W.sel_thresh);
+  uint32_t* sel_keys = reinterpret_cast<uint32_t*>(ws + W.sel_keys);
+  uint32_t* sel_n = reinterpret_cast<uint32_t*>(ws + W.sel_n);
+  hot_hist_kernel<<<blocks, 256, 0, L.s>>>(a, rs, hot_keys, hot_n, hot_cnt, min_count, sel_hist);
+  hot_thresh_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(d->T, sel_hist, sel_thresh);
+  hot_select_kernel<<<blocks, 256, 0, L.s>>>(a, rs, hot_keys, hot_n, hot_cnt, min_count,
+                                             sel_thresh, sel_keys, sel_n);
+  hot_commit_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(d->T, sel_keys, sel_n, hot_keys, hot_n);
   return cudaGetLastError();
 }
 

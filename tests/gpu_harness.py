@@ -78,6 +78,20 @@ class Run:
     def status(self):
         return tbe.tbe_read_status(self.ws)
 
+    def hot_set(self):
+        """The workspace's hot rows: list (per table) of sorted linear keys."""
+        torch.cuda.synchronize()
+        v = tbe.tbe_workspace_view(self.desc, max(self.w.n, 1), self.ws)
+        T, K = self.desc.T, v["hot_slots"]
+        n = ws_array(self.ws, v["hot_n"], T)
+        keys = ws_array(self.ws, v["hot_keys"], T * K).reshape(T, K)
+        return [keys[t, :n[t]].astype(np.int64) for t in range(T)]
+
+    def reset_state(self):
+        """Weights and momentum back to the workload's values."""
+        self.weights.copy_(self.w.weights.to(self.weights.device))
+        self.momentum.copy_(self.w.momentum.to(self.momentum.device))
+
 
 def tables(w):
     return oracle.Tables(w.E, w.D)

@@ -29,6 +29,9 @@ def test_noalloc_matches_workspace_entry_point_twice(recipe, kw, flags):
     w = workloads.make(recipe, seed=7, **kw)
     ref, got = _pair(w)
     for _ in range(2):  # the second call starts from the scratch the first one left
+        # Each no-allocation call stands alone (no hot rows carried over), so
+        # the workspace entry point gets a fresh workspace for each call too.
+        ref.ws = tbe.Workspace(ref.desc, max(w.n, 1), w.psw is not None)
         tbe.tbe_backward_rowwise_adagrad(ref.desc, ref.grad_out, ref.indices, ref.offsets, ref.psw,
                                          ref.weights, ref.momentum, w.lr, w.eps, ref.ws, flags)
         tbe.tbe_backward_rowwise_adagrad_noalloc(got.desc, got.grad_out, got.indices, got.offsets,
