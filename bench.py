@@ -99,7 +99,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -203,10 +203,12 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = tbe.tbe_kernel_launches()
     t0.record(stream)
     for k in range(args.steps):
         step(evs[k])
     t1.record(stream)
+    launches = tbe.tbe_kernel_launches() - launches0
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
@@ -220,13 +222,11 @@ def run_native(args, world, rank, local):
     off = view["counts"] - ws.buf.data_ptr()
     counts = ws.buf[off:off + 32].view(torch.int32).cpu().numpy().view(np.uint32)
     R, n_long, n_chunks = int(counts[0]), int(counts[2]), int(counts[3])
-    passes = 3
-    launches_per_step = 1 + (2 + 3 * passes + 3 + 3) + 2
     result = {
         "ms": ms, "ms_local": ms_local, "fwd_ms": statistics.median(fwd),
         "pre_ms": statistics.median(pre), "upd_ms": statistics.median(upd),
         "n": w.n, "R": R, "n_long": n_long, "n_chunks": n_chunks, "clocks": clk,
-        "launches": launches_per_step * args.steps, "w": w,
+        "launches": launches, "w": w,
     }
 
     if not args.no_e2e:

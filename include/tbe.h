@@ -244,6 +244,13 @@ tbe_status tbe_backward_rowwise_adagrad_noalloc(const tbe_desc* d, const float* 
 /* Library build identification: a static string. */
 const char* tbe_version(void);
 
+/* Number of CUDA kernels this library has launched in this process, over all
+ * entry points, devices and threads (a relaxed atomic counter, never reset).
+ * Memsets are not counted.  A measurement aid with no counterpart in the
+ * method: the difference of two readings is the kernel count of the calls
+ * made between them. */
+uint64_t tbe_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

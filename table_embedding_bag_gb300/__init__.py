@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "build", "TBEDesc", "Workspace", "TBEError", "tbe_workspace_size", "tbe_forward",
     "tbe_preprocess", "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status",
-    "tbe_version", "TableBatchedEmbedding", "lib_path", "tbe_backward_rowwise_adagrad_noalloc",
+    "tbe_version", "tbe_kernel_launches", "TableBatchedEmbedding", "lib_path", "tbe_backward_rowwise_adagrad_noalloc",
     "TBE_NOALLOC_SCRATCH_BYTES", "TBE_ETOO_LARGE",
     "TBE_F_CHECK_BOUNDS", "TBE_F_REPAIR_OFFSETS", "TBE_F_FORCE_GENERIC", "TBE_F_LONG_TWO_LAUNCH",
     "TBE_F_PREPROCESSED", "TBE_WS_WEIGHTED", "TBE_ERR_INDEX_RANGE", "TBE_ERR_OFFSETS",
@@ -92,6 +92,8 @@ def _load():
                                                              P, u32]
         lib.tbe_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         lib.tbe_version.restype = ctypes.c_char_p
+        lib.tbe_kernel_launches.restype = ctypes.c_uint64
+        lib.tbe_kernel_launches.argtypes = []
         for f in ("tbe_workspace_size", "tbe_forward", "tbe_preprocess",
                   "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status",
                   "tbe_backward_rowwise_adagrad_noalloc"):
@@ -239,6 +241,11 @@ def tbe_read_status(ws: Workspace, stream=None) -> int:
 
 def tbe_version() -> str:
     return _load().tbe_version().decode()
+
+
+def tbe_kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(_load().tbe_kernel_launches())
 
 
 class TableBatchedEmbedding:

@@ -66,6 +66,13 @@ constexpr size_t kHotBudgetBytes = size_t(2) << 30;
 constexpr int kHotCtaTarget = 320;  // CTAs of the hot-gradient kernel
 constexpr int kHotMinPartBags = 256;  // fewest bags per hot-gradient CTA
 constexpr int kHotBuckets = 256;    // log-scale buckets of lookup counts (8 per octave)
+constexpr int kHotHashBits = 10;    // shared-memory hash of a table's hot set: 1024 entries
+constexpr uint32_t kEmptyKey = 0xffffffffu;  // never a key: total_E < 2^32 - 1
+
+// Hash of a hot-set key under the table's multiplier (one-to-one on the set).
+__host__ __device__ __forceinline__ uint32_t hot_hash(uint32_t key, uint32_t mult) {
+  return (key * mult) >> (32 - kHotHashBits);
+}
 
 // Long-run chunks are processed in order of the first bag they touch, binned
 // into at most this many bag bands, so that the warps in flight gather
@@ -120,6 +127,7 @@ struct WsLayout {
   size_t tree_part;    // float [max_tree * max_D]
   size_t hot_keys;     // uint32 [T][kHot] hot rows (linear keys), kept across calls
   size_t hot_n;        // uint32 [T] hot rows per table, kept across calls
+  size_t hot_mult;     // uint32 [T] collision-free hash multiplier of the hot set
   size_t hot_cnt;      // uint32 [T][kHot] lookups of each hot row in this call
   size_t hot_hist;     // float [T][kHot][B] per-bag weight of each hot row (if enabled)
   size_t hot_part;     // float [T][hot_parts][kHot][kHotMaxD] partial hot gradients

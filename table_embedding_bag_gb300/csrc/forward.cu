@@ -245,13 +245,13 @@ cudaError_t launch_forward_t(const Launch& L, const __half* W, const IndexT* ind
   if (blocks > (1 << 22)) blocks = 1 << 22;
   if (blocks < 1) blocks = 1;
   if (psw)
-    forward_generic_kernel<IndexT, true><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
+    { forward_generic_kernel<IndexT, true><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
         W, d->D_offsets, d->hash_base, d->weights_offsets, indices, offsets, psw, L.n, d->T,
-        d->B, d->total_D, out, status);
+        d->B, d->total_D, out, status); note_launch(); }
   else
-    forward_generic_kernel<IndexT, false><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
+    { forward_generic_kernel<IndexT, false><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
         W, d->D_offsets, d->hash_base, d->weights_offsets, indices, offsets, psw, L.n, d->T,
-        d->B, d->total_D, out, status);
+        d->B, d->total_D, out, status); note_launch(); }
   return cudaGetLastError();
 }
 
@@ -261,15 +261,15 @@ cudaError_t launch_offsets_t(const Launch& L, const IndexT* offsets, bool repair
   const int64_t nb = static_cast<int64_t>(L.d->T) * L.d->B;
   int64_t blocks = (nb + 1 + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  check_offsets_kernel<IndexT><<<static_cast<unsigned>(blocks), 256, 0, L.s>>>(offsets, nb, L.n,
-                                                                               status);
+  { check_offsets_kernel<IndexT><<<static_cast<unsigned>(blocks), 256, 0, L.s>>>(offsets, nb, L.n,
+                                                                               status); note_launch(); }
   if (!repair) return cudaGetLastError();
   const int64_t nfix = (nb + 1 + kFixTile - 1) / kFixTile;
-  repair_block_max_kernel<IndexT><<<static_cast<unsigned>(nfix), kFixThreads, 0, L.s>>>(
-      offsets, nb + 1, L.n, scratch);
-  repair_scan_kernel<<<1, 1024, 0, L.s>>>(scratch, nfix);
-  repair_apply_kernel<IndexT><<<static_cast<unsigned>(nfix), kFixThreads, 0, L.s>>>(
-      offsets, nb + 1, L.n, scratch, fixed);
+  { repair_block_max_kernel<IndexT><<<static_cast<unsigned>(nfix), kFixThreads, 0, L.s>>>(
+      offsets, nb + 1, L.n, scratch); note_launch(); }
+  { repair_scan_kernel<<<1, 1024, 0, L.s>>>(scratch, nfix); note_launch(); }
+  { repair_apply_kernel<IndexT><<<static_cast<unsigned>(nfix), kFixThreads, 0, L.s>>>(
+      offsets, nb + 1, L.n, scratch, fixed); note_launch(); }
   return cudaGetLastError();
 }
 

@@ -328,9 +328,9 @@ cudaError_t launch_small_t(const Launch& L, const __half* W, const IndexT* indic
   int64_t grid = 2LL * L.num_sms;
   if (grid > tiles) grid = tiles;
   if (grid < 1) grid = 1;
-  forward_small_kernel<IndexT><<<static_cast<unsigned>(grid), kThreads, kSmallSmemBytes, L.s>>>(
+  { forward_small_kernel<IndexT><<<static_cast<unsigned>(grid), kThreads, kSmallSmemBytes, L.s>>>(
       W, indices, offsets, L.n, d->B, static_cast<int>(d->total_E), static_cast<int>(d->total_D),
-      out, d->total_D, status, error_word);
+      out, d->total_D, status, error_word); note_launch(); }
   return cudaGetLastError();
 }
 

@@ -11,6 +11,9 @@ namespace tbe {
 
 struct WsLayout;
 
+// Counts one kernel launch (read back by tbe_kernel_launches).
+void note_launch();
+
 // One call's launch context.
 struct Launch {
   const tbe_desc* d;

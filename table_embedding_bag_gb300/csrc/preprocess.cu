@@ -45,31 +45,20 @@ constexpr int kRleTile = kRleThreads * kRleItems;
 // pass 2 (write) writes the cold lookups in position order, so the sort's
 // input order, and hence its stability, is the lookup order.
 
-// Hot-set membership: an open-addressing hash of the table's hot keys in
-// shared memory (twice as many entries as keys, linear probing).
-constexpr int kHotHash = 2 * kHot;
-constexpr uint32_t kEmptyKey = 0xffffffffu;
+// Hot-set membership: a collision-free hash of the table's hot keys in
+// shared memory.  When the hot set is chosen, a multiplier is picked for which
+// key -> (key * mult) >> (32 - kHotHashBits) is one-to-one on the set, so a
+// lookup is one 64-bit load: entry = key | slot << 32, empty = kEmptyKey.
+constexpr uint64_t kEmptyEntry = kEmptyKey;
 
 struct HotHash {
-  uint32_t key[kHotHash];
-  uint8_t slot[kHotHash];
+  uint64_t e[1 << kHotHashBits];
 };
 
-__device__ __forceinline__ uint32_t hot_hash(uint32_t key) {
-  return (key * 2654435761u) >> (32 - 7);  // 7 bits: kHotHash = 128
-}
-
 // Slot of `key` in the hot set, or -1.
-__device__ __forceinline__ int hot_lookup(const HotHash& h, uint32_t key) {
-  uint32_t i = hot_hash(key);
-#pragma unroll 1
-  for (int probe = 0; probe < kHotHash; ++probe) {
-    const uint32_t k = h.key[i];
-    if (k == key) return h.slot[i];
-    if (k == kEmptyKey) return -1;
-    i = (i + 1) & (kHotHash - 1);
-  }
-  return -1;
+__device__ __forceinline__ int hot_lookup(const HotHash& h, uint32_t mult, uint32_t key) {
+  const uint64_t e = h.e[hot_hash(key, mult)];
+  return static_cast<uint32_t>(e) == key ? static_cast<int>(e >> 32) : -1;
 }
 
 struct TileInfo {
@@ -90,24 +79,22 @@ __device__ __forceinline__ TileInfo tile_info(int B) {
 // Builds the hash of table t's hot set (empty when the histogram is disabled
 // or the table is too wide for the hot path); returns the number of hot rows.
 // Contains __syncthreads.
-__device__ int build_hot_hash(HotHash& h, const uint32_t* hot_keys, const uint32_t* hot_n,
+__device__ int build_hot_hash(HotHash& h, uint32_t* mult, const uint32_t* hot_keys,
+                              const uint32_t* hot_n, const uint32_t* hot_mult,
                               const int64_t* D_offsets, int t, bool enabled) {
   int nh = 0;
   if (enabled) {
     const int D = static_cast<int>(__ldg(D_offsets + t + 1) - __ldg(D_offsets + t));
     nh = D <= kHotMaxD ? static_cast<int>(min(hot_n[t], static_cast<uint32_t>(kHot))) : 0;
   }
-  for (int i = threadIdx.x; i < kHotHash; i += blockDim.x) h.key[i] = kEmptyKey;
+  const uint32_t m = hot_mult[t];
+  for (int i = threadIdx.x; i < (1 << kHotHashBits); i += blockDim.x) h.e[i] = kEmptyEntry;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < nh; ++s) {
-      const uint32_t key = hot_keys[t * kHot + s];
-      uint32_t i = hot_hash(key);
-      while (h.key[i] != kEmptyKey && h.key[i] != key) i = (i + 1) & (kHotHash - 1);
-      h.key[i] = key;
-      h.slot[i] = static_cast<uint8_t>(s);
-    }
+  if (threadIdx.x < nh) {
+    const uint32_t key = hot_keys[t * kHot + threadIdx.x];
+    h.e[hot_hash(key, m)] = key | (static_cast<uint64_t>(threadIdx.x) << 32);
   }
+  *mult = m;
   __syncthreads();
   return nh;
 }
@@ -115,11 +102,11 @@ __device__ int build_hot_hash(HotHash& h, const uint32_t* hot_keys, const uint32
 template <typename IndexT, bool kWeighted>
 struct ExpandSmem {
   HotHash hash;
-  uint32_t slot_cnt[kHot];
   uint32_t warp_cold[8];
   // per-bag weight of each hot row: exact sums (integer counts, or fp32
-  // weights summed in double), so the result does not depend on atomic order
-  typename std::conditional<kWeighted, double, uint32_t>::type hist[kHot][kHotTileBags];
+  // weights summed in double), so the result does not depend on atomic order.
+  // Rows are padded by one so that one bag's slots fall in different banks.
+  typename std::conditional<kWeighted, double, uint32_t>::type hist[kHot][kHotTileBags + 1];
 };
 
 constexpr int kExpandLoads = 4;  // index loads in flight per lane
@@ -130,7 +117,7 @@ __global__ void __launch_bounds__(256)
                         const float* __restrict__ psw, const int64_t* __restrict__ hash_base,
                         const int64_t* __restrict__ D_offsets, int64_t n, int B,
                         const uint32_t* __restrict__ hot_keys, const uint32_t* __restrict__ hot_n,
-                        float* __restrict__ hot_hist, uint32_t* __restrict__ hot_cnt,
+                        const uint32_t* __restrict__ hot_mult, float* __restrict__ hot_hist, uint32_t* __restrict__ hot_cnt,
                         uint32_t* __restrict__ bag_cold, uint32_t* __restrict__ tile_cold,
                         int* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -138,10 +125,11 @@ __global__ void __launch_bounds__(256)
   const TileInfo ti = tile_info(B);
   const int warp = threadIdx.x >> 5;
   const unsigned lane = lane_id();
-  for (int i = threadIdx.x; i < kHot; i += blockDim.x) sm.slot_cnt[i] = 0;
-  for (int i = threadIdx.x; i < kHot * kHotTileBags; i += blockDim.x)
-    sm.hist[i / kHotTileBags][i % kHotTileBags] = 0;
-  const int nh = build_hot_hash(sm.hash, hot_keys, hot_n, D_offsets, ti.t, hot_hist != nullptr);
+  for (int i = threadIdx.x; i < kHot * (kHotTileBags + 1); i += blockDim.x)
+    sm.hist[i / (kHotTileBags + 1)][i % (kHotTileBags + 1)] = 0;
+  uint32_t mult;
+  const int nh = build_hot_hash(sm.hash, &mult, hot_keys, hot_n, hot_mult, D_offsets, ti.t,
+                                hot_hist != nullptr);
   const int64_t h0 = __ldg(hash_base + ti.t);
   const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
   bool bad = false;
@@ -164,22 +152,18 @@ __global__ void __launch_bounds__(256)
         const bool inside = r[u] != -2;
         const bool ok = inside && r[u] >= 0 && r[u] < E;
         bad |= inside && !ok;
-        const int slot = ok && nh ? hot_lookup(sm.hash, static_cast<uint32_t>(h0 + r[u])) : -1;
+        const int slot =
+            ok && nh ? hot_lookup(sm.hash, mult, static_cast<uint32_t>(h0 + r[u])) : -1;
         cold += ok && slot < 0;
         if constexpr (kWeighted) {
           // double sums of fp32 weights are exact: atomic order does not matter
-          if (slot >= 0) {
+          if (slot >= 0)
             atomicAdd(&sm.hist[slot][lb], static_cast<double>(__ldg(psw + base + u * 32 + lane)));
-            atomicAdd(&sm.slot_cnt[slot], 1u);
-          }
         } else {
           // one add per distinct hot row of the 32 lookups
           const unsigned peers = __match_any_sync(kFull, slot);
-          if (slot >= 0 && lane == static_cast<unsigned>(__ffs(peers) - 1)) {
-            const uint32_t c = static_cast<uint32_t>(__popc(peers));
-            atomicAdd(&sm.hist[slot][lb], c);
-            atomicAdd(&sm.slot_cnt[slot], c);
-          }
+          if (slot >= 0 && lane == static_cast<unsigned>(__ffs(peers) - 1))
+            atomicAdd(&sm.hist[slot][lb], static_cast<uint32_t>(__popc(peers)));
         }
       }
     }
@@ -195,14 +179,19 @@ __global__ void __launch_bounds__(256)
     for (int w = 0; w < 8; ++w) c += sm.warp_cold[w];
     tile_cold[blockIdx.x] = c;
   }
-  for (int i = threadIdx.x; i < nh * kHotTileBags; i += blockDim.x) {
-    const int slot = i / kHotTileBags, lb = i % kHotTileBags;
-    if (lb < ti.nbags)
-      hot_hist[(static_cast<int64_t>(ti.t) * kHot + slot) * B + ti.b0 + lb] =
-          static_cast<float>(sm.hist[slot][lb]);
+  // each warp writes out 8 slots; lookups per slot = bags' counts summed
+  for (int slot = warp; slot < nh; slot += 8) {
+    uint32_t c = 0;
+    for (int lb = lane; lb < ti.nbags; lb += 32) {
+      const auto v = sm.hist[slot][lb];
+      hot_hist[(static_cast<int64_t>(ti.t) * kHot + slot) * B + ti.b0 + lb] = static_cast<float>(v);
+      if constexpr (kWeighted) c += v != 0.0;  // weighted counts nonzero-weight bags only
+      else c += v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+    if (lane == 0 && c) atomicAdd(&hot_cnt[ti.t * kHot + slot], c);
   }
-  for (int i = threadIdx.x; i < nh; i += blockDim.x)
-    if (sm.slot_cnt[i]) atomicAdd(&hot_cnt[ti.t * kHot + i], sm.slot_cnt[i]);
   if (status && __any_sync(kFull, bad) && lane == 0) set_status(status, TBE_ERR_INDEX_RANGE);
 }
 
@@ -212,7 +201,7 @@ __global__ void __launch_bounds__(256)
                         const float* __restrict__ psw, const int64_t* __restrict__ hash_base,
                         const int64_t* __restrict__ D_offsets, int64_t n, int B,
                         const uint32_t* __restrict__ hot_keys, const uint32_t* __restrict__ hot_n,
-                        bool hot_enabled, const uint32_t* __restrict__ bag_cold,
+                        const uint32_t* __restrict__ hot_mult, bool hot_enabled, const uint32_t* __restrict__ bag_cold,
                         const uint32_t* __restrict__ tile_base, uint32_t* __restrict__ keys,
                         uint32_t* __restrict__ vals, float* __restrict__ psw_out) {
   __shared__ HotHash hash;
@@ -229,7 +218,9 @@ __global__ void __launch_bounds__(256)
     const uint32_t inc = block_inclusive_scan(c, OpSum(), 0u, scan);
     if (lb < kHotTileBags) bag_base[lb] = tile_base[blockIdx.x] + inc - c;
   }
-  const int nh = build_hot_hash(hash, hot_keys, hot_n, D_offsets, ti.t, hot_enabled);
+  uint32_t mult;
+  const int nh =
+      build_hot_hash(hash, &mult, hot_keys, hot_n, hot_mult, D_offsets, ti.t, hot_enabled);
   const int64_t h0 = __ldg(hash_base + ti.t);
   const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
   const unsigned lt = (1u << lane) - 1u;
@@ -252,7 +243,7 @@ __global__ void __launch_bounds__(256)
         uint32_t key = 0;
         if (r[u] >= 0 && r[u] < E) {
           key = static_cast<uint32_t>(h0 + r[u]);
-          cold = !nh || hot_lookup(hash, key) < 0;
+          cold = !nh || hot_lookup(hash, mult, key) < 0;
         }
         const unsigned m = __ballot_sync(kFull, cold);
         if (cold) {
@@ -902,27 +893,28 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     if (err != cudaSuccess) return err;
     const uint32_t* hk = reinterpret_cast<const uint32_t*>(ws + W.hot_keys);
     const uint32_t* hn = reinterpret_cast<const uint32_t*>(ws + W.hot_n);
+    const uint32_t* hm = reinterpret_cast<const uint32_t*>(ws + W.hot_mult);
     float* hh = W.hot_enabled ? reinterpret_cast<float*>(ws + W.hot_hist) : nullptr;
     uint32_t* hc = reinterpret_cast<uint32_t*>(ws + W.hot_cnt);
     uint32_t* bc = reinterpret_cast<uint32_t*>(ws + W.bag_cold);
     const unsigned tiles = static_cast<unsigned>(W.hot_tiles);
     if (weighted)
-      expand_count_kernel<IndexT, true><<<tiles, 256, sizeof(ExpandSmem<IndexT, true>), s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hh, hc, bc,
-          tile_cold, status);
+      { expand_count_kernel<IndexT, true><<<tiles, 256, sizeof(ExpandSmem<IndexT, true>), s>>>(
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hm, hh, hc, bc,
+          tile_cold, status); note_launch(); }
     else
-      expand_count_kernel<IndexT, false><<<tiles, 256, sizeof(ExpandSmem<IndexT, false>), s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hh, hc, bc,
-          tile_cold, status);
-    exclusive_scan_kernel<<<1, 1024, 0, s>>>(tile_cold, W.hot_tiles, counters + kCntSortN);
+      { expand_count_kernel<IndexT, false><<<tiles, 256, sizeof(ExpandSmem<IndexT, false>), s>>>(
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hm, hh, hc, bc,
+          tile_cold, status); note_launch(); }
+    { exclusive_scan_kernel<<<1, 1024, 0, s>>>(tile_cold, W.hot_tiles, counters + kCntSortN); note_launch(); }
     if (weighted)
-      expand_write_kernel<IndexT, true><<<tiles, 256, 0, s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, W.hot_enabled, bc,
-          tile_cold, keys[0], vals[0], pw[0]);
+      { expand_write_kernel<IndexT, true><<<tiles, 256, 0, s>>>(
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hm, W.hot_enabled, bc,
+          tile_cold, keys[0], vals[0], pw[0]); note_launch(); }
     else
-      expand_write_kernel<IndexT, false><<<tiles, 256, 0, s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, W.hot_enabled, bc,
-          tile_cold, keys[0], vals[0], pw[0]);
+      { expand_write_kernel<IndexT, false><<<tiles, 256, 0, s>>>(
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hm, W.hot_enabled, bc,
+          tile_cold, keys[0], vals[0], pw[0]); note_launch(); }
   }
 
   if (n > 0) {
@@ -936,52 +928,52 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
       const int shift = p * rb;
       const int width = rb < bits - shift ? rb : bits - shift;
       const int src = p & 1, dst = src ^ 1;
-      radix_upsweep_kernel<<<g.ctas, kSortThreads, 0, s>>>(keys[src], g, shift, width, counts);
-      radix_scan_kernel<<<1, 1 << kMaxRadixBits, 0, s>>>(counts, g.ctas, 1 << width);
+      { radix_upsweep_kernel<<<g.ctas, kSortThreads, 0, s>>>(keys[src], g, shift, width, counts); note_launch(); }
+      { radix_scan_kernel<<<1, 1 << kMaxRadixBits, 0, s>>>(counts, g.ctas, 1 << width); note_launch(); }
       if (weighted)
-        radix_downsweep_kernel<true><<<g.ctas, kSortThreads, smem, s>>>(
+        { radix_downsweep_kernel<true><<<g.ctas, kSortThreads, smem, s>>>(
             keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], g, shift, width,
-            counts);
+            counts); note_launch(); }
       else
-        radix_downsweep_kernel<false><<<g.ctas, kSortThreads, smem, s>>>(
+        { radix_downsweep_kernel<false><<<g.ctas, kSortThreads, smem, s>>>(
             keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], g, shift, width,
-            counts);
+            counts); note_launch(); }
     }
     const int fin = passes & 1;
     const SortGeom gr = sort_geom(n, L.num_sms, 6, counters + kCntSortN);
     uint32_t* cta_runs = reinterpret_cast<uint32_t*>(ws + W.cta_counts);
     uint32_t* cta_pairs = cta_runs + (kMaxSortCtas + 1);
-    rle_count_kernel<<<gr.ctas, kRleThreads, 0, s>>>(keys[fin], vals[fin], gr, sentinel,
-                                                     cta_runs, cta_pairs);
-    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_runs, gr.ctas, cta_runs + gr.ctas);
-    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_pairs, gr.ctas, cta_pairs + gr.ctas);
-    rle_write_kernel<<<gr.ctas, kRleThreads, 0, s>>>(
+    { rle_count_kernel<<<gr.ctas, kRleThreads, 0, s>>>(keys[fin], vals[fin], gr, sentinel,
+                                                     cta_runs, cta_pairs); note_launch(); }
+    { exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_runs, gr.ctas, cta_runs + gr.ctas); note_launch(); }
+    { exclusive_scan_kernel<<<1, 1024, 0, s>>>(cta_pairs, gr.ctas, cta_pairs + gr.ctas); note_launch(); }
+    { rle_write_kernel<<<gr.ctas, kRleThreads, 0, s>>>(
         keys[fin], vals[fin], gr, sentinel, cta_runs, cta_pairs, uk, rs,
         reinterpret_cast<uint32_t*>(ws + W.run_pairs),
         reinterpret_cast<uint32_t*>(ws + W.pair_starts),
-        reinterpret_cast<uint32_t*>(ws + W.pair_bags), counters);
+        reinterpret_cast<uint32_t*>(ws + W.pair_bags), counters); note_launch(); }
   }
-  table_runs_kernel<<<1, 1024, 0, s>>>(uk, counters, d->hash_base, d->D_offsets, d->T,
+  { table_runs_kernel<<<1, 1024, 0, s>>>(uk, counters, d->hash_base, d->D_offsets, d->T,
                                        reinterpret_cast<uint32_t*>(ws + W.table_runs),
-                                       reinterpret_cast<uint32_t*>(ws + W.table_tasks), counters);
+                                       reinterpret_cast<uint32_t*>(ws + W.table_tasks), counters); note_launch(); }
   if (n > 0) {
     int64_t blocks = (n + 255) / 256;
     if (blocks > 8LL * L.num_sms) blocks = 8LL * L.num_sms;
-    classify_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+    { classify_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         reinterpret_cast<uint32_t*>(ws + W.run_pairs), counters, reinterpret_cast<uint32_t*>(ws + W.long_run),
         reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
-        reinterpret_cast<uint32_t*>(ws + W.long_tree0));
+        reinterpret_cast<uint32_t*>(ws + W.long_tree0)); note_launch(); }
     int64_t fb = (W.max_long * 32 + 255) / 256;
     if (fb > 8LL * L.num_sms) fb = 8LL * L.num_sms;
     if (fb < 1) fb = 1;
-    chunk_fill_kernel<<<static_cast<unsigned>(fb), 256, 0, s>>>(
+    { chunk_fill_kernel<<<static_cast<unsigned>(fb), 256, 0, s>>>(
         reinterpret_cast<uint32_t*>(ws + W.run_pairs), counters, uk, d->hash_base, d->T,
         reinterpret_cast<uint32_t*>(ws + W.long_run),
         reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
         reinterpret_cast<uint32_t*>(ws + W.long_tree0),
         reinterpret_cast<LongRunInfo*>(ws + W.long_info),
         reinterpret_cast<ChunkDesc*>(ws + W.chunk_desc),
-        reinterpret_cast<uint32_t*>(ws + W.tree_cnt));
+        reinterpret_cast<uint32_t*>(ws + W.tree_cnt)); note_launch(); }
     int band_shift = 0;
     while ((static_cast<int64_t>(d->B - 1) >> band_shift) >= kBagBands) ++band_shift;
     uint32_t* band_count = reinterpret_cast<uint32_t*>(ws + W.band_count);
@@ -990,15 +982,15 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     int64_t cb = (W.max_chunks + 255) / 256;
     if (cb > 8LL * L.num_sms) cb = 8LL * L.num_sms;
     if (cb < 1) cb = 1;
-    chunk_band_count_kernel<<<static_cast<unsigned>(cb), 256, 0, s>>>(
+    { chunk_band_count_kernel<<<static_cast<unsigned>(cb), 256, 0, s>>>(
         counters, reinterpret_cast<ChunkDesc*>(ws + W.chunk_desc),
         reinterpret_cast<uint32_t*>(ws + W.pair_bags), band_shift,
-        reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count);
-    exclusive_scan_kernel<<<1, 1024, 0, s>>>(band_count, kBagBands, nullptr);
-    chunk_band_scatter_kernel<<<static_cast<unsigned>(cb), 256, 0, s>>>(
+        reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count); note_launch(); }
+    { exclusive_scan_kernel<<<1, 1024, 0, s>>>(band_count, kBagBands, nullptr); note_launch(); }
+    { chunk_band_scatter_kernel<<<static_cast<unsigned>(cb), 256, 0, s>>>(
         counters, reinterpret_cast<ChunkDesc*>(ws + W.chunk_desc),
         reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count,
-        reinterpret_cast<ChunkDesc*>(ws + W.chunk_order));
+        reinterpret_cast<ChunkDesc*>(ws + W.chunk_order)); note_launch(); }
   }
   return cudaGetLastError();
 }

@@ -1,11 +1,16 @@
 // C ABI entry points: argument validation, workspace layout and launch order.
 // The operations themselves are specified in include/tbe.h.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace tbe {
+
+std::atomic<uint64_t> g_kernel_launches{0};
+
+void note_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 
 cudaError_t prepare_preprocess_kernels();
 
@@ -58,6 +63,7 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   L.hot_enabled = static_cast<size_t>(T) * kHot * B * sizeof(float) <= kHotBudgetBytes;
   L.hot_keys = take(T * kHot * 4);
   L.hot_n = take(T * 4);
+  L.hot_mult = take(T * 4);
   L.hot_cnt = take(T * kHot * 4);
   L.hot_hist = L.hot_enabled ? take(static_cast<size_t>(T) * kHot * B * sizeof(float)) : 0;
   L.hot_part = L.hot_enabled ? take(static_cast<size_t>(T) * L.hot_parts * kHot * kHotMaxD * 4) : 0;
@@ -269,5 +275,9 @@ tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits) 
 }
 
 const char* tbe_version(void) { return "tbe-gb300 0.1 (sm_103a)"; }
+
+uint64_t tbe_kernel_launches(void) {
+  return tbe::g_kernel_launches.load(std::memory_order_relaxed);
+}
 
 }  // extern "C"

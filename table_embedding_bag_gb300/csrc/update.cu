@@ -778,12 +778,32 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// The selected keys, sorted per table, become the hot set.
+// The selected keys, sorted per table, become the hot set, together with the
+// first multiplier of a fixed odd sequence whose hash is one-to-one on them.
+// If none of kMultTries is (about one chance in 10^16 for 64 keys in 1024
+// entries), keys that collide under the first multiplier are dropped.
+constexpr int kMultTries = 256;
+
+__device__ __forceinline__ uint32_t mult_candidate(int i) {
+  return (0x9E3779B1u + 2u * static_cast<uint32_t>(i) * 0x3C6EF372u) | 1u;
+}
+
+__device__ bool one_to_one(const uint32_t* k, uint32_t nsel, uint32_t mult) {
+  uint32_t used[(1 << kHotHashBits) / 32];
+  for (int i = 0; i < (1 << kHotHashBits) / 32; ++i) used[i] = 0;
+  for (uint32_t i = 0; i < nsel; ++i) {
+    const uint32_t h = hot_hash(k[i], mult);
+    if (used[h >> 5] & (1u << (h & 31))) return false;
+    used[h >> 5] |= 1u << (h & 31);
+  }
+  return true;
+}
+
 __global__ void hot_commit_kernel(int T, const uint32_t* __restrict__ sel_keys,
                                   const uint32_t* __restrict__ sel_n, uint32_t* __restrict__ hot_keys,
-                                  uint32_t* __restrict__ hot_n) {
+                                  uint32_t* __restrict__ hot_n, uint32_t* __restrict__ hot_mult) {
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
-    const uint32_t nsel = min(sel_n[t], static_cast<uint32_t>(kHot));
+    uint32_t nsel = min(sel_n[t], static_cast<uint32_t>(kHot));
     uint32_t k[kHot];
     for (uint32_t i = 0; i < nsel; ++i) {
       uint32_t v = sel_keys[t * kHot + i];
@@ -791,8 +811,28 @@ __global__ void hot_commit_kernel(int T, const uint32_t* __restrict__ sel_keys,
       for (; j > 0 && k[j - 1] > v; --j) k[j] = k[j - 1];
       k[j] = v;
     }
+    uint32_t mult = 0;
+    bool found = false;
+    for (int i = 0; i < kMultTries && !found; ++i) {
+      mult = mult_candidate(i);
+      found = one_to_one(k, nsel, mult);
+    }
+    if (!found) {
+      mult = mult_candidate(0);
+      uint32_t used[(1 << kHotHashBits) / 32];
+      for (int i = 0; i < (1 << kHotHashBits) / 32; ++i) used[i] = 0;
+      uint32_t kept = 0;
+      for (uint32_t i = 0; i < nsel; ++i) {
+        const uint32_t h = hot_hash(k[i], mult);
+        if (used[h >> 5] & (1u << (h & 31))) continue;
+        used[h >> 5] |= 1u << (h & 31);
+        k[kept++] = k[i];
+      }
+      nsel = kept;
+    }
     for (uint32_t i = 0; i < nsel; ++i) hot_keys[t * kHot + i] = k[i];
     hot_n[t] = nsel;
+    hot_mult[t] = mult;
   }
 }
 
@@ -832,17 +872,17 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   const unsigned blocks = static_cast<unsigned>(L.num_sms) * 8u;
   const bool weighted = a.sorted_psw != nullptr;
   const bool wide = d->max_D > 512;  // rows of more than 128 float4 vectors
-  if (weighted) short_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a);
-  else short_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a);
-  if (wide && weighted) short_runs_kernel<true, true><<<blocks, 256, 0, L.s>>>(a);
-  if (wide && !weighted) short_runs_kernel<false, true><<<blocks, 256, 0, L.s>>>(a);
-  if (weighted) long_chunks_kernel<true, false><<<blocks, 256, 0, L.s>>>(a, two_launch);
-  else long_chunks_kernel<false, false><<<blocks, 256, 0, L.s>>>(a, two_launch);
-  if (wide && weighted) long_chunks_kernel<true, true><<<blocks, 256, 0, L.s>>>(a, two_launch);
-  if (wide && !weighted) long_chunks_kernel<false, true><<<blocks, 256, 0, L.s>>>(a, two_launch);
+  if (weighted) { short_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
+  else { short_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
+  if (wide && weighted) { short_runs_kernel<true, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
+  if (wide && !weighted) { short_runs_kernel<false, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
+  if (weighted) { long_chunks_kernel<true, false><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); }
+  else { long_chunks_kernel<false, false><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); }
+  if (wide && weighted) { long_chunks_kernel<true, true><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); }
+  if (wide && !weighted) { long_chunks_kernel<false, true><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); }
   if (two_launch) {
-    long_finish_kernel<false><<<blocks, 256, 0, L.s>>>(a);
-    if (wide) long_finish_kernel<true><<<blocks, 256, 0, L.s>>>(a);
+    { long_finish_kernel<false><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
+    if (wide) { long_finish_kernel<true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
   }
   // Hot rows: gradient from the histogram, update, then choose the next set.
   uint32_t* hot_keys = reinterpret_cast<uint32_t*>(ws + W.hot_keys);
@@ -853,11 +893,11 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
     const float* hist = reinterpret_cast<const float*>(ws + W.hot_hist);
     const unsigned hg = static_cast<unsigned>(d->T) * W.hot_parts;
     if (d->max_D <= 128)
-      hot_grad_kernel<1><<<hg, 256, 0, L.s>>>(a, hist, hot_n, W.hot_parts, part);
+      { hot_grad_kernel<1><<<hg, 256, 0, L.s>>>(a, hist, hot_n, W.hot_parts, part); note_launch(); }
     else
-      hot_grad_kernel<2><<<hg, 256, 0, L.s>>>(a, hist, hot_n, W.hot_parts, part);
-    hot_finish_kernel<<<static_cast<unsigned>(d->T) * kHot, 256, 0, L.s>>>(
-        a, hot_keys, hot_n, hot_cnt, W.hot_parts, part);
+      { hot_grad_kernel<2><<<hg, 256, 0, L.s>>>(a, hist, hot_n, W.hot_parts, part); note_launch(); }
+    { hot_finish_kernel<<<static_cast<unsigned>(d->T) * kHot, 256, 0, L.s>>>(
+        a, hot_keys, hot_n, hot_cnt, W.hot_parts, part); note_launch(); }
   }
   if (!W.hot_enabled) return cudaGetLastError();  // no histogram: the hot set stays empty
   cudaError_t e = cudaMemsetAsync(ws + W.sel_hist, 0, static_cast<size_t>(d->T) * kHotBuckets * 4, L.s);
@@ -870,11 +910,12 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   uint32_t* sel_thresh = reinterpret_cast<uint32_t*>(ws + W.sel_thresh);
   uint32_t* sel_keys = reinterpret_cast<uint32_t*>(ws + W.sel_keys);
   uint32_t* sel_n = reinterpret_cast<uint32_t*>(ws + W.sel_n);
-  hot_hist_kernel<<<blocks, 256, 0, L.s>>>(a, rs, hot_keys, hot_n, hot_cnt, min_count, sel_hist);
-  hot_thresh_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(d->T, sel_hist, sel_thresh);
-  hot_select_kernel<<<blocks, 256, 0, L.s>>>(a, rs, hot_keys, hot_n, hot_cnt, min_count,
-                                             sel_thresh, sel_keys, sel_n);
-  hot_commit_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(d->T, sel_keys, sel_n, hot_keys, hot_n);
+  { hot_hist_kernel<<<blocks, 256, 0, L.s>>>(a, rs, hot_keys, hot_n, hot_cnt, min_count, sel_hist); note_launch(); }
+  { hot_thresh_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(d->T, sel_hist, sel_thresh); note_launch(); }
+  { hot_select_kernel<<<blocks, 256, 0, L.s>>>(a, rs, hot_keys, hot_n, hot_cnt, min_count,
+                                             sel_thresh, sel_keys, sel_n); note_launch(); }
+  { hot_commit_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(d->T, sel_keys, sel_n, hot_keys, hot_n,
+                                                    reinterpret_cast<uint32_t*>(ws + W.hot_mult)); note_launch(); }
   return cudaGetLastError();
 }
 

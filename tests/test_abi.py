@@ -27,6 +27,7 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "tbe_backward_rowwise_adagrad", "tbe_backward_rowwise_adagrad_noalloc", "tbe_forward",
         "tbe_preprocess", "tbe_read_status", "tbe_version", "tbe_workspace_size",
+        "tbe_kernel_launches",
         "tbe_workspace_view"])
 
 
@@ -81,6 +82,8 @@ def test_bad_sizes_rejected(lib):
 
 
 def test_small_workspace_rejected_before_any_launch(lib):
+    lib.tbe_kernel_launches.restype = ctypes.c_uint64
+    launches0 = lib.tbe_kernel_launches()
     d = _desc()
     P = ctypes.c_void_p
     lib.tbe_forward.argtypes = [ctypes.POINTER(tbe.tbe_desc), P, P, P, ctypes.c_int64, P, P, P,
@@ -98,6 +101,7 @@ def test_small_workspace_rejected_before_any_launch(lib):
     rc = lib.tbe_backward_rowwise_adagrad(ctypes.byref(d), fake, fake, fake, 10, None, fake, fake,
                                           0.01, 1e-8, fake, 8, None, 0)
     assert rc == tbe.TBE_EWORKSPACE
+    assert lib.tbe_kernel_launches() == launches0  # rejected calls launch nothing
 
 
 def test_package_refuses_to_run_without_the_library(monkeypatch, tmp_path):

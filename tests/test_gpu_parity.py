@@ -142,3 +142,20 @@ def test_int32_and_int64_indices_agree():
     W32, m32 = run32.backward()
     assert np.array_equal(W32.view(np.uint16), W64.view(np.uint16))
     assert np.array_equal(m32.view(np.uint32), m64.view(np.uint32))
+
+
+def test_launch_counter_counts_the_kernels_of_a_call():
+    # tiny: two tables, so the generic forward is one kernel; with bounds
+    # checking the offsets check adds one more
+    w = make("tiny")
+    run = H.Run(w)
+    c0 = H.tbe.tbe_kernel_launches()
+    run.forward(flags=0)
+    c1 = H.tbe.tbe_kernel_launches()
+    run.forward(flags=H.tbe.TBE_F_CHECK_BOUNDS)
+    c2 = H.tbe.tbe_kernel_launches()
+    run.preprocess()
+    c3 = H.tbe.tbe_kernel_launches()
+    assert c1 - c0 == 1
+    assert c2 - c1 == 2
+    assert c3 - c2 >= 10  # expand, sort passes, run-length encoding, classify
