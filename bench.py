@@ -180,17 +180,20 @@ def run_native(args, world, rank, local):
     out = torch.empty(w.B, desc.total_D, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    PRE = tbe.TBE_F_PREPROCESSED
+
     def step(ev=None):
+        # one preprocess of the batch's indices serves forward and backward
         if ev is not None:
             ev[0].record(stream)
-        tbe.tbe_forward(desc, weights, w.indices, w.offsets, None, out, ws)
+        tbe.tbe_preprocess(desc, w.indices, w.offsets, None, ws)
         if ev is not None:
             ev[1].record(stream)
-        tbe.tbe_preprocess(desc, w.indices, w.offsets, None, ws)
+        tbe.tbe_forward(desc, weights, w.indices, w.offsets, None, out, ws, PRE)
         if ev is not None:
             ev[2].record(stream)
         tbe.tbe_backward_rowwise_adagrad(desc, w.grad_out, w.indices, w.offsets, None, weights,
-                                         momentum, w.lr, w.eps, ws, tbe.TBE_F_PREPROCESSED)
+                                         momentum, w.lr, w.eps, ws, PRE)
         if ev is not None:
             ev[3].record(stream)
 
@@ -212,20 +215,25 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
+    status = tbe.tbe_read_status(ws)
+    if status & tbe.TBE_ERR_TIMEOUT:
+        raise SystemExit("bench: a kernel's bounded wait timed out during the timed steps "
+                         f"(status {status:#x}); the measurement is invalid")
     ms_local = t0.elapsed_time(t1)
     ms = max_over_ranks(ms_local, world, dev)
-    fwd = [e[0].elapsed_time(e[1]) for e in evs]
-    pre = [e[1].elapsed_time(e[2]) for e in evs]
+    pre = [e[0].elapsed_time(e[1]) for e in evs]
+    fwd = [e[1].elapsed_time(e[2]) for e in evs]
     upd = [e[2].elapsed_time(e[3]) for e in evs]
 
     view = tbe.tbe_workspace_view(desc, w.n, ws)
     off = view["counts"] - ws.buf.data_ptr()
     counts = ws.buf[off:off + 32].view(torch.int32).cpu().numpy().view(np.uint32)
     R, n_long, n_chunks = int(counts[0]), int(counts[2]), int(counts[3])
+    n_cold = int(counts[7])  # lookups left to the sort after the hot rows
     result = {
         "ms": ms, "ms_local": ms_local, "fwd_ms": statistics.median(fwd),
         "pre_ms": statistics.median(pre), "upd_ms": statistics.median(upd),
-        "n": w.n, "R": R, "n_long": n_long, "n_chunks": n_chunks, "clocks": clk,
+        "n": w.n, "R": R, "n_long": n_long, "n_chunks": n_chunks, "n_cold": n_cold, "clocks": clk,
         "launches": launches, "w": w,
     }
 
@@ -243,9 +251,10 @@ def run_native(args, world, rank, local):
             d_idx.copy_(h_idx, non_blocking=True)
             d_off.copy_(h_off, non_blocking=True)
             d_grad.copy_(h_grad, non_blocking=True)
-            tbe.tbe_forward(desc, weights, d_idx, d_off, None, out, ws)
+            tbe.tbe_preprocess(desc, d_idx, d_off, None, ws)
+            tbe.tbe_forward(desc, weights, d_idx, d_off, None, out, ws, PRE)
             tbe.tbe_backward_rowwise_adagrad(desc, d_grad, d_idx, d_off, None, weights, momentum,
-                                             w.lr, w.eps, ws)
+                                             w.lr, w.eps, ws, PRE)
             h_out.copy_(out, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):
@@ -361,7 +370,8 @@ def main():
                    "l2": "inputs larger than L2 (indices 1.7 GB, weights 20.5 GB); no flush",
                    "storage": "fp16 weights, fp32 momentum/gradients"},
         "phases_ms": {"forward": r["fwd_ms"], "preprocess": r["pre_ms"], "update": r["upd_ms"]},
-        "runs": {"R": r["R"], "long_runs": r["n_long"], "long_chunks": r["n_chunks"]},
+        "runs": {"R": r["R"], "long_runs": r["n_long"], "long_chunks": r["n_chunks"],
+                 "cold_lookups": r["n_cold"]},
         "roofline": {"kernel": "forward_generic_kernel (tbe_forward)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": profiled_traffic() if args.tables is None else None,

@@ -79,9 +79,11 @@ enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3 };
 #define TBE_F_LONG_TWO_LAUNCH (1u << 3) /* backward: long runs write partial sums and a
                                            second kernel applies the update (instead of
                                            the fenced last-arriver update) */
-#define TBE_F_PREPROCESSED (1u << 4)    /* backward: the workspace already holds the
-                                           sorted runs of these indices/offsets from
-                                           tbe_preprocess on the same stream */
+#define TBE_F_PREPROCESSED (1u << 4)    /* forward and backward: the workspace already
+                                           holds tbe_preprocess's results for these
+                                           indices/offsets/per-sample weights (same
+                                           stream); see tbe_forward for when the
+                                           forward still reads the indices */
 
 /* workspace-size flags */
 #define TBE_WS_WEIGHTED (1u << 0)       /* reserve room for per-sample weights */
@@ -154,6 +156,15 @@ tbe_status tbe_workspace_size(const tbe_desc* d, int64_t n_max, uint32_t ws_flag
  * 64 <= D <= 128, no per-sample weights and an average bag length >= 64 takes
  * the tensor-core histogram path (counts per bag times the table) unless
  * TBE_F_FORCE_GENERIC; every other problem takes the generic gather-pool.
+ * With TBE_F_PREPROCESSED and bags of at least 64 lookups on average
+ * (n >= 64 T B; shorter bags are pooled from the indices as without the
+ * flag) the forward reads tbe_preprocess's results instead of the indices:
+ * each table's hot rows are pooled as the per-bag histogram
+ * times those rows on the tensor cores (tf32 with an exact remainder term:
+ * the products are exact), the cold lookups are gathered from the per-bag
+ * cold lists; the bounds/offsets flags are then ignored (the preprocess
+ * checked them) and per_sample_weights must be NULL exactly when it was NULL
+ * for the preprocess.
  * weights: fp16 device; indices/offsets: device, index_dtype; n: lookups
  * (length of indices); per_sample_weights: fp32 device [n] or NULL;
  * out: fp32 device [B, total_D], fully overwritten.  Workspace: the status
@@ -169,9 +180,13 @@ tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indic
  * 1-4): expand every lookup to (key = hash_base[t] + row, bag b, psw), radix
  * sort by key (stable, int32 keys), run-length encode into runs, and classify
  * runs into short and long with the long-run task list compacted on the
- * device.  Results stay in the workspace (see tbe_workspace_view); a later
- * tbe_backward_rowwise_adagrad with TBE_F_PREPROCESSED consumes them.
- * Errors as tbe_forward. */
+ * device.  Hot rows: the workspace keeps, per table, up to hot_slots rows
+ * chosen by the previous backward on it (none at first); lookups of those
+ * rows are not sorted but summed per bag into a histogram (counts, or sums of
+ * per-sample weights), and the remaining (cold) lookups are also kept per bag
+ * in lookup order.  Results stay in the workspace (see tbe_workspace_view); a
+ * later tbe_forward or tbe_backward_rowwise_adagrad with TBE_F_PREPROCESSED
+ * consumes them.  Errors as tbe_forward. */
 tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* offsets, int64_t n,
                           const float* per_sample_weights, void* workspace, size_t ws_bytes,
                           void* stream, uint32_t flags);
@@ -185,8 +200,15 @@ tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* of
  * exactly once per touched row; untouched rows are not written.
  * grad_out: fp32 device [B, total_D]; weights (fp16) and momentum (fp32
  * [total_E]) are updated in place.  Without TBE_F_PREPROCESSED the call runs
- * tbe_preprocess first.  No host synchronisation, no device-to-host copy.
- * Errors as tbe_forward. */
+ * tbe_preprocess first.  The gradient of a hot row (see tbe_preprocess) is
+ * its histogram column times grad_out, summed over bag partitions in a fixed
+ * order; every other row's gradient is summed over its sorted run.  Both are
+ * fp32 sums whose rounding order differs, so a row's result can differ in the
+ * last bits between a call where it is hot and one where it is cold.  The call
+ * then chooses the next hot set: per table, the most looked-up rows of this
+ * batch with at least max(B/8, 32) lookups (tables with D_t <= 256 only, and
+ * only while T * hot_slots * B * 4 bytes stay within 2 GiB).
+ * No host synchronisation, no device-to-host copy.  Errors as tbe_forward. */
 tbe_status tbe_backward_rowwise_adagrad(const tbe_desc* d, const float* grad_out,
                                         const void* indices, const void* offsets, int64_t n,
                                         const float* per_sample_weights, void* weights,

@@ -12,8 +12,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtbe.so")
-SOURCES = ["tbe_api.cu", "forward.cu", "forward_small.cu", "preprocess.cu", "update.cu",
-           "noalloc.cu"]
+SOURCES = ["tbe_api.cu", "forward.cu", "forward_small.cu", "forward_hot.cu", "preprocess.cu",
+           "update.cu", "hot_grad.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC]

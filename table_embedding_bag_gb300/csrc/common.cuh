@@ -65,6 +65,7 @@ constexpr int kHotMaxD = 256;
 constexpr size_t kHotBudgetBytes = size_t(2) << 30;
 constexpr int kHotCtaTarget = 320;  // CTAs of the hot-gradient kernel
 constexpr int kHotMinPartBags = 256;  // fewest bags per hot-gradient CTA
+constexpr int kHotFwdMinBagLen = 64;  // preprocessed forward: mean lookups per bag to use it
 constexpr int kHotBuckets = 256;    // log-scale buckets of lookup counts (8 per octave)
 constexpr int kHotHashBits = 10;    // shared-memory hash of a table's hot set: 1024 entries
 constexpr uint32_t kEmptyKey = 0xffffffffu;  // never a key: total_E < 2^32 - 1
@@ -104,9 +105,11 @@ struct WsLayout {
   size_t counts;       // uint32 [kNumCounters]
   size_t table_runs;   // uint32 [T+1] first run of each table
   size_t table_tasks;  // uint32 [T+1] prefix of short-run warp tasks per table
-  size_t keys[2];      // uint32 [n]
-  size_t vals[2];      // uint32 [n]
-  size_t psw[2];       // float [n] (weighted only)
+  // sort buffers: [2] is the expand output, the cold lookups in lookup order
+  // (kept intact for the forward), [0] / [1] the radix passes' ping-pong
+  size_t keys[3];      // uint32 [n] linear keys
+  size_t vals[3];      // uint32 [n] bags
+  size_t psw[3];       // float [n] (weighted only)
   size_t radix_counts; // uint32 [2^kMaxRadixBits * kMaxSortCtas]
   size_t cta_counts;   // uint32 [kMaxSortCtas + 1]
   size_t unique_keys;  // uint32 [n + 1]
@@ -125,9 +128,18 @@ struct WsLayout {
   size_t tree_cnt;     // uint32 [max_tree] arrivals still expected at each tree node
   size_t partials;     // float [max_chunks * max_D]
   size_t tree_part;    // float [max_tree * max_D]
-  size_t hot_keys;     // uint32 [T][kHot] hot rows (linear keys), kept across calls
-  size_t hot_n;        // uint32 [T] hot rows per table, kept across calls
-  size_t hot_mult;     // uint32 [T] collision-free hash multiplier of the hot set
+  // Two hot sets, each uint32 keys [T][kHot] (sorted linear keys), n [T] and
+  // mult [T] (collision-free hash multiplier), kept across calls: `hot_next`
+  // is written by the backward's refresh and copied to `hot_cur` at the start
+  // of every preprocess; the preprocess, the forward and the backward of one
+  // batch all read `hot_cur`.
+  size_t hot_cur;
+  size_t hot_next;
+  size_t hot_set_bytes;
+  size_t hot_keys(size_t set) const { return set; }
+  size_t hot_n(size_t set) const { return set + static_cast<size_t>(T) * kHot * 4; }
+  size_t hot_mult(size_t set) const { return set + static_cast<size_t>(T) * (kHot + 1) * 4; }
+  int64_t T;
   size_t hot_cnt;      // uint32 [T][kHot] lookups of each hot row in this call
   size_t hot_hist;     // float [T][kHot][B] per-bag weight of each hot row (if enabled)
   size_t hot_part;     // float [T][hot_parts][kHot][kHotMaxD] partial hot gradients

@@ -25,6 +25,7 @@
 //    frees its tensor memory and stops.
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace tbe {
 namespace {
@@ -36,7 +37,6 @@ constexpr int kCoreBytes = 128;      // 8 rows x 16 bytes
 constexpr int kLBO = kCoreBytes;     // next 8 K-elements of the same 8 rows
 constexpr int kSBO = (kK / 8) * kCoreBytes;  // next 8 rows (1024 bytes)
 constexpr int kTmemCols = 128;       // fp32 accumulator columns (>= D, power of two)
-constexpr uint32_t kSpinLimit = 1u << 26;
 
 struct SmallSmem {
   alignas(1024) __half a_lo[kM * kK];  // H & 2047, canonical K-major layout
@@ -57,92 +57,8 @@ __device__ __forceinline__ int canon_offset(int row, int k) {
   return (row >> 3) * kSBO + (k >> 3) * kLBO + (row & 7) * 16 + (k & 7) * 2;
 }
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// tcgen05 shared-memory matrix descriptor: start address, leading and stride
-// byte offsets (all >> 4), descriptor version 1, no swizzle.
 __device__ __forceinline__ uint64_t make_desc(const void* smem_ptr) {
-  const uint64_t addr = smem_u32(smem_ptr);
-  return ((addr & 0x3ffffull) >> 4) | (static_cast<uint64_t>(kLBO >> 4) << 16) |
-         (static_cast<uint64_t>(kSBO >> 4) << 32) | (1ull << 46);
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__device__ __forceinline__ uint32_t make_idesc(int n) {
-  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kM >> 4) << 24);
-}
-
-__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait; false if the phase did not complete within the limit.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i > 64) __nanosleep(64);
-  }
-  return false;
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(unsigned long long* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// 32 consecutive fp32 accumulator columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void fence_before_sync() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_after_sync() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  return make_smem_desc(smem_ptr, kLBO, kSBO);
 }
 
 template <typename IndexT>
@@ -163,14 +79,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const __half v = (nn < D && k < E) ? W[static_cast<int64_t>(k) * D + nn] : __float2half(0.f);
     *reinterpret_cast<__half*>(reinterpret_cast<unsigned char*>(sm.b) + canon_offset(nn, k)) = v;
   }
-  if (warp == 0) {
-    asm volatile(
-        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-            smem_u32(&sm.tmem_base)),
-        "r"(kTmemCols)
-        : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
+  if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
   if (tid == 0) {
     mbar_init(&sm.mbar, 1);
     sm.timed_out = 0;
@@ -180,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t idesc = make_idesc(D <= 64 ? 64 : 128);
+  const uint32_t idesc = make_idesc(kFmtF16, kM, D <= 64 ? 64 : 128);
   const int n_mma = D <= 64 ? 64 : 128;
   uint32_t phase = 0;
   uint32_t drain_phase = 0;
@@ -302,10 +211,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
   }
   if (status && __any_sync(kFull, bad) && lane == 0) set_status(status, TBE_ERR_INDEX_RANGE);
-  if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
-                 : "memory");
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 constexpr size_t kSmallSmemBytes = sizeof(SmallSmem) + 1024;

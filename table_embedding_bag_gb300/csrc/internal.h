@@ -35,11 +35,19 @@ bool small_table_eligible(const tbe_desc* d, int64_t n, bool weighted);
 cudaError_t launch_forward_small(const Launch& L, const void* weights, const void* indices,
                                  const void* offsets, float* out, int* status, int* error_word);
 
+// forward_hot.cu: forward from tbe_preprocess's results (hot rows on the
+// tensor cores, cold lookups gathered).
+cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, const void* weights,
+                               const float* psw, float* out);
+
 // preprocess.cu: expand, radix sort, run-length encode, classify.
 cudaError_t launch_preprocess(const Launch& L, const WsLayout& W, char* ws, const void* indices,
                               const void* offsets, const float* psw, bool check);
 // Sorted arrays end up in buffer (passes % 2); the layout needs to know which.
 int radix_passes(const tbe_desc* d);
+
+// hot_grad.cu: partial gradients of the hot rows (tensor cores).
+cudaError_t launch_hot_grad(const Launch& L, const WsLayout& W, char* ws, const float* grad_out);
 
 // update.cu: short-run and long-run row-wise Adagrad.
 cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const float* grad_out,

@@ -92,7 +92,7 @@ extern "C" tbe_status tbe_backward_rowwise_adagrad_noalloc(
   // writing is reset by launch_preprocess (counters, first run and pair
   // entries, band counts); the status word is not used because bounds
   // reporting is not offered here.
-  if (cudaMemsetAsync(scratch + W.hot_n, 0, static_cast<size_t>(d->T) * sizeof(uint32_t),
+  if (cudaMemsetAsync(scratch + W.hot_n(W.hot_next), 0, static_cast<size_t>(d->T) * sizeof(uint32_t),
                       L.s) != cudaSuccess)
     return TBE_ECUDA;
   cudaError_t e = launch_preprocess(L, W, scratch, indices, offsets, per_sample_weights, false);

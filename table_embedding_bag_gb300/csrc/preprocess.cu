@@ -81,7 +81,8 @@ __device__ __forceinline__ TileInfo tile_info(int B) {
 // Contains __syncthreads.
 __device__ int build_hot_hash(HotHash& h, uint32_t* mult, const uint32_t* hot_keys,
                               const uint32_t* hot_n, const uint32_t* hot_mult,
-                              const int64_t* D_offsets, int t, bool enabled) {
+                              const int64_t* D_offsets, int64_t h0, int64_t E, int t,
+                              bool enabled) {
   int nh = 0;
   if (enabled) {
     const int D = static_cast<int>(__ldg(D_offsets + t + 1) - __ldg(D_offsets + t));
@@ -91,8 +92,11 @@ __device__ int build_hot_hash(HotHash& h, uint32_t* mult, const uint32_t* hot_ke
   for (int i = threadIdx.x; i < (1 << kHotHashBits); i += blockDim.x) h.e[i] = kEmptyEntry;
   __syncthreads();
   if (threadIdx.x < nh) {
+    // a key outside the table (a workspace last used for other tables) is
+    // left out: its slot stays empty
     const uint32_t key = hot_keys[t * kHot + threadIdx.x];
-    h.e[hot_hash(key, m)] = key | (static_cast<uint64_t>(threadIdx.x) << 32);
+    if (key >= h0 && key < h0 + E)
+      h.e[hot_hash(key, m)] = key | (static_cast<uint64_t>(threadIdx.x) << 32);
   }
   *mult = m;
   __syncthreads();
@@ -127,11 +131,11 @@ __global__ void __launch_bounds__(256)
   const unsigned lane = lane_id();
   for (int i = threadIdx.x; i < kHot * (kHotTileBags + 1); i += blockDim.x)
     sm.hist[i / (kHotTileBags + 1)][i % (kHotTileBags + 1)] = 0;
-  uint32_t mult;
-  const int nh = build_hot_hash(sm.hash, &mult, hot_keys, hot_n, hot_mult, D_offsets, ti.t,
-                                hot_hist != nullptr);
   const int64_t h0 = __ldg(hash_base + ti.t);
   const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
+  uint32_t mult;
+  const int nh = build_hot_hash(sm.hash, &mult, hot_keys, hot_n, hot_mult, D_offsets, h0, E,
+                                ti.t, hot_hist != nullptr);
   bool bad = false;
   uint32_t cold_w = 0;
   for (int lb = warp; lb < ti.nbags; lb += 8) {
@@ -218,11 +222,11 @@ __global__ void __launch_bounds__(256)
     const uint32_t inc = block_inclusive_scan(c, OpSum(), 0u, scan);
     if (lb < kHotTileBags) bag_base[lb] = tile_base[blockIdx.x] + inc - c;
   }
-  uint32_t mult;
-  const int nh =
-      build_hot_hash(hash, &mult, hot_keys, hot_n, hot_mult, D_offsets, ti.t, hot_enabled);
   const int64_t h0 = __ldg(hash_base + ti.t);
   const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
+  uint32_t mult;
+  const int nh = build_hot_hash(hash, &mult, hot_keys, hot_n, hot_mult, D_offsets, h0, E, ti.t,
+                                hot_enabled);
   const unsigned lt = (1u << lane) - 1u;
   for (int lb = warp; lb < ti.nbags; lb += 8) {
     const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
@@ -868,12 +872,14 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
   uint32_t* counters = reinterpret_cast<uint32_t*>(ws + W.counts);
   const uint32_t sentinel = static_cast<uint32_t>(d->total_E);
   const bool weighted = psw != nullptr;
-  uint32_t* keys[2] = {reinterpret_cast<uint32_t*>(ws + W.keys[0]),
-                       reinterpret_cast<uint32_t*>(ws + W.keys[1])};
-  uint32_t* vals[2] = {reinterpret_cast<uint32_t*>(ws + W.vals[0]),
-                       reinterpret_cast<uint32_t*>(ws + W.vals[1])};
-  float* pw[2] = {weighted ? reinterpret_cast<float*>(ws + W.psw[0]) : nullptr,
-                  weighted ? reinterpret_cast<float*>(ws + W.psw[1]) : nullptr};
+  uint32_t* keys[3];
+  uint32_t* vals[3];
+  float* pw[3];
+  for (int i = 0; i < 3; ++i) {
+    keys[i] = reinterpret_cast<uint32_t*>(ws + W.keys[i]);
+    vals[i] = reinterpret_cast<uint32_t*>(ws + W.vals[i]);
+    pw[i] = weighted ? reinterpret_cast<float*>(ws + W.psw[i]) : nullptr;
+  }
   uint32_t* uk = reinterpret_cast<uint32_t*>(ws + W.unique_keys);
   uint32_t* rs = reinterpret_cast<uint32_t*>(ws + W.run_starts);
 
@@ -891,9 +897,13 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
   {
     err = cudaMemsetAsync(ws + W.hot_cnt, 0, static_cast<size_t>(d->T) * kHot * 4, s);
     if (err != cudaSuccess) return err;
-    const uint32_t* hk = reinterpret_cast<const uint32_t*>(ws + W.hot_keys);
-    const uint32_t* hn = reinterpret_cast<const uint32_t*>(ws + W.hot_n);
-    const uint32_t* hm = reinterpret_cast<const uint32_t*>(ws + W.hot_mult);
+    // this batch's hot set: the one the last backward chose
+    err = cudaMemcpyAsync(ws + W.hot_cur, ws + W.hot_next, W.hot_set_bytes,
+                          cudaMemcpyDeviceToDevice, s);
+    if (err != cudaSuccess) return err;
+    const uint32_t* hk = reinterpret_cast<const uint32_t*>(ws + W.hot_keys(W.hot_cur));
+    const uint32_t* hn = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_cur));
+    const uint32_t* hm = reinterpret_cast<const uint32_t*>(ws + W.hot_mult(W.hot_cur));
     float* hh = W.hot_enabled ? reinterpret_cast<float*>(ws + W.hot_hist) : nullptr;
     uint32_t* hc = reinterpret_cast<uint32_t*>(ws + W.hot_cnt);
     uint32_t* bc = reinterpret_cast<uint32_t*>(ws + W.bag_cold);
@@ -910,11 +920,11 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     if (weighted)
       { expand_write_kernel<IndexT, true><<<tiles, 256, 0, s>>>(
           indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hm, W.hot_enabled, bc,
-          tile_cold, keys[0], vals[0], pw[0]); note_launch(); }
+          tile_cold, keys[2], vals[2], pw[2]); note_launch(); }
     else
       { expand_write_kernel<IndexT, false><<<tiles, 256, 0, s>>>(
           indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hm, W.hot_enabled, bc,
-          tile_cold, keys[0], vals[0], pw[0]); note_launch(); }
+          tile_cold, keys[2], vals[2], pw[2]); note_launch(); }
   }
 
   if (n > 0) {
@@ -927,7 +937,9 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     for (int p = 0; p < passes; ++p) {
       const int shift = p * rb;
       const int width = rb < bits - shift ? rb : bits - shift;
-      const int src = p & 1, dst = src ^ 1;
+      // pass 0 reads the expand output (buffer 2), later passes ping-pong
+      // between 1 and 0, so the sorted result is in buffer passes & 1
+      const int src = p == 0 ? 2 : (p & 1), dst = (p & 1) ^ 1;
       { radix_upsweep_kernel<<<g.ctas, kSortThreads, 0, s>>>(keys[src], g, shift, width, counts); note_launch(); }
       { radix_scan_kernel<<<1, 1 << kMaxRadixBits, 0, s>>>(counts, g.ctas, 1 << width); note_launch(); }
       if (weighted)

@@ -24,14 +24,20 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   };
   L.weighted = (ws_flags & TBE_WS_WEIGHTED) != 0;
   const size_t un = static_cast<size_t>(n);
+  // State kept across calls comes first, at offsets that depend only on T,
+  // so calls with different n (or weightedness) on one workspace agree.
   L.status = take(64);
+  L.T = d->T;
+  L.hot_set_bytes = static_cast<size_t>(d->T) * (kHot + 2) * 4;
+  L.hot_cur = take(L.hot_set_bytes);
+  L.hot_next = take(L.hot_set_bytes);
   L.counts = take(kNumCounters * sizeof(uint32_t));
   L.table_runs = take((d->T + 1) * sizeof(uint32_t));
   L.table_tasks = take((d->T + 1) * sizeof(uint32_t));
   // sort buffers keep 64 spare bytes: whole 16-byte tile copies stay inside
-  for (int i = 0; i < 2; ++i) L.keys[i] = take(un * 4 + 64);
-  for (int i = 0; i < 2; ++i) L.vals[i] = take(un * 4 + 64);
-  for (int i = 0; i < 2; ++i) L.psw[i] = L.weighted ? take(un * 4 + 64) : 0;
+  for (int i = 0; i < 3; ++i) L.keys[i] = take(un * 4 + 64);
+  for (int i = 0; i < 3; ++i) L.vals[i] = take(un * 4 + 64);
+  for (int i = 0; i < 3; ++i) L.psw[i] = L.weighted ? take(un * 4 + 64) : 0;
   L.radix_counts = take(sizeof(uint32_t) * (1u << kMaxRadixBits) * kMaxSortCtas);
   L.cta_counts = take(sizeof(uint32_t) * 2 * (kMaxSortCtas + 1));
   L.unique_keys = take((un + 1) * 4);
@@ -61,9 +67,6 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   const int64_t max_parts = (B + kHotMinPartBags - 1) / kHotMinPartBags;
   if (L.hot_parts > max_parts) L.hot_parts = static_cast<int>(max_parts);
   L.hot_enabled = static_cast<size_t>(T) * kHot * B * sizeof(float) <= kHotBudgetBytes;
-  L.hot_keys = take(T * kHot * 4);
-  L.hot_n = take(T * 4);
-  L.hot_mult = take(T * 4);
   L.hot_cnt = take(T * kHot * 4);
   L.hot_hist = L.hot_enabled ? take(static_cast<size_t>(T) * kHot * B * sizeof(float)) : 0;
   L.hot_part = L.hot_enabled ? take(static_cast<size_t>(T) * L.hot_parts * kHot * kHotMaxD * 4) : 0;
@@ -173,13 +176,20 @@ tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indic
                        float* out, void* workspace, size_t ws_bytes, void* stream,
                        uint32_t flags) {
   WsLayout W;
-  // The forward needs only the status word and the repaired offsets, but the
-  // workspace contract is the same for every entry point.
-  tbe_status st = common_args(d, indices, offsets, n, workspace, ws_bytes, false, &W);
+  // The plain forward needs only the status word and the repaired offsets,
+  // but the workspace contract is the same for every entry point; after a
+  // preprocess the layout must be the one the preprocess used.
+  const bool pre = (flags & TBE_F_PREPROCESSED) != 0;
+  tbe_status st = common_args(d, indices, offsets, n, workspace, ws_bytes,
+                              pre && per_sample_weights != nullptr, &W);
   if (st != TBE_OK) return st;
   if (!weights || !out || !aligned16(weights) || !aligned16(out)) return TBE_EINVAL;
   const Launch L{d, n, static_cast<cudaStream_t>(stream), device_sms()};
   char* ws = static_cast<char*>(workspace);
+  // The preprocessed path pays off when a bag holds enough lookups for its
+  // hot rows to matter; shorter bags are pooled straight from the indices.
+  if (pre && n >= static_cast<int64_t>(kHotFwdMinBagLen) * d->T * d->B)
+    return from_cuda(launch_forward_hot(L, W, ws, weights, per_sample_weights, out));
   const void* off_eff;
   int* status;
   st = run_checks(L, W, ws, offsets, flags, &off_eff, &status);
@@ -254,8 +264,8 @@ tbe_status tbe_workspace_view(const tbe_desc* d, int64_t n, uint32_t ws_flags, v
   view->run_pairs = reinterpret_cast<const uint32_t*>(ws + W.run_pairs);
   view->pair_starts = reinterpret_cast<const uint32_t*>(ws + W.pair_starts);
   view->pair_bags = reinterpret_cast<const uint32_t*>(ws + W.pair_bags);
-  view->hot_keys = reinterpret_cast<const uint32_t*>(ws + W.hot_keys);
-  view->hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n);
+  view->hot_keys = reinterpret_cast<const uint32_t*>(ws + W.hot_keys(W.hot_next));
+  view->hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_next));
   view->hot_slots = kHot;
   view->long_threshold = kLongThreshold;
   view->chunk = kChunk;

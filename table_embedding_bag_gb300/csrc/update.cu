@@ -546,89 +546,8 @@ __global__ void __launch_bounds__(256, 3) long_finish_kernel(UpdArgs a) {
 }
 
 // --------------------------------------------------------------- hot rows
-// The gradient of a hot row is sum_b hist[t][slot][b] * grad_out[b, D_off[t]:]:
-// one pass over the table's gradient rows serves all its hot rows.  CTA
-// (t, p) sums bag partition p of table t; thread items are 4 hot slots x 8
-// columns, read from shared-memory chunks of 32 bags.
-constexpr int kHotChunk = 32;
-
-template <int kItems>
-__global__ void __launch_bounds__(256)
-    hot_grad_kernel(UpdArgs a, const float* __restrict__ hot_hist,
-                    const uint32_t* __restrict__ hot_n, int parts, float* __restrict__ hot_part) {
-  __shared__ float hs[kHot][kHotChunk];
-  __shared__ __align__(16) float gs[kHotChunk][kHotMaxD];
-  const int t = blockIdx.x / parts;
-  const int p = blockIdx.x % parts;
-  const int nh = static_cast<int>(min(hot_n[t], static_cast<uint32_t>(kHot)));
-  const int64_t d0 = a.D_offsets[t];
-  const int D = static_cast<int>(a.D_offsets[t + 1] - d0);
-  if (nh == 0 || D > kHotMaxD || (D & 7)) return;  // uniform over the CTA
-  const int ndg = D >> 3;                          // column groups of 8
-  const int nsg = (nh + 3) >> 2;                   // slot groups of 4
-  const int64_t B = a.B;
-  const int64_t b_begin = B * p / parts, b_end = B * (p + 1) / parts;
-  float acc[kItems][4][8];
-#pragma unroll
-  for (int k = 0; k < kItems; ++k)
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[k][i][j] = 0.f;
-  for (int64_t c0 = b_begin; c0 < b_end; c0 += kHotChunk) {
-    const int cnt = static_cast<int>(b_end - c0 < kHotChunk ? b_end - c0 : kHotChunk);
-    for (int i = threadIdx.x; i < kHot * kHotChunk; i += blockDim.x) {
-      const int slot = i / kHotChunk, j = i % kHotChunk;
-      hs[slot][j] = slot < nh && j < cnt
-                        ? __ldg(hot_hist + (static_cast<int64_t>(t) * kHot + slot) * B + c0 + j)
-                        : 0.f;
-    }
-    const int nq = D >> 2;
-    for (int i = threadIdx.x; i < kHotChunk * nq; i += blockDim.x) {
-      const int j = i / nq, q = i % nq;
-      const float4 v = j < cnt ? ldg_f4(a.grad_out + (c0 + j) * a.total_D + d0 + q * 4)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-      *reinterpret_cast<float4*>(&gs[j][q * 4]) = v;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kItems; ++k) {
-      const int item = threadIdx.x + k * blockDim.x;
-      const int sg = item / ndg, dg = item % ndg;
-      if (sg < nsg) {
-        for (int j = 0; j < cnt; ++j) {
-          float h[4], g[8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) h[i] = hs[sg * 4 + i][j];
-          const float4 g0 = *reinterpret_cast<const float4*>(&gs[j][dg * 8]);
-          const float4 g1 = *reinterpret_cast<const float4*>(&gs[j][dg * 8 + 4]);
-          g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
-          g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) acc[k][i][jj] = fmaf(h[i], g[jj], acc[k][i][jj]);
-        }
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    const int item = threadIdx.x + k * blockDim.x;
-    const int sg = item / ndg, dg = item % ndg;
-    if (sg < nsg) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float* dst = hot_part + ((static_cast<int64_t>(t) * parts + p) * kHot + sg * 4 + i) * kHotMaxD +
-                     dg * 8;
-        *reinterpret_cast<float4*>(dst) = make_float4(acc[k][i][0], acc[k][i][1], acc[k][i][2], acc[k][i][3]);
-        *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[k][i][4], acc[k][i][5], acc[k][i][6], acc[k][i][7]);
-      }
-    }
-  }
-}
-
+// The hot rows' partial gradients come from the tensor-core kernel in
+// hot_grad.cu (hot_part[t][p][slot][c]).
 // One CTA per hot row that was looked up in this call: warp w adds the
 // partitions w, w + 8, ... in order, warp 0 adds the eight warp sums in order
 // (a fixed order, so the result is reproducible), then applies the row-wise
@@ -676,6 +595,7 @@ __global__ void __launch_bounds__(256)
       }
   }
   const uint32_t key = hot_keys[blockIdx.x];
+  if (key < a.hash_base[t] || key >= a.hash_base[t + 1]) return;  // not this table's row
   __half* row = a.W + a.w_offsets[t] + (static_cast<int64_t>(key) - a.hash_base[t]) * D;
   uint2 w_raw[2];
   load_row<32, 2>(row, nv, w_raw, true);
@@ -885,17 +805,13 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
     if (wide) { long_finish_kernel<true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
   }
   // Hot rows: gradient from the histogram, update, then choose the next set.
-  uint32_t* hot_keys = reinterpret_cast<uint32_t*>(ws + W.hot_keys);
-  uint32_t* hot_n = reinterpret_cast<uint32_t*>(ws + W.hot_n);
+  const uint32_t* hot_keys = reinterpret_cast<const uint32_t*>(ws + W.hot_keys(W.hot_cur));
+  const uint32_t* hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_cur));
   const uint32_t* hot_cnt = reinterpret_cast<const uint32_t*>(ws + W.hot_cnt);
   if (W.hot_enabled) {
-    float* part = reinterpret_cast<float*>(ws + W.hot_part);
-    const float* hist = reinterpret_cast<const float*>(ws + W.hot_hist);
-    const unsigned hg = static_cast<unsigned>(d->T) * W.hot_parts;
-    if (d->max_D <= 128)
-      { hot_grad_kernel<1><<<hg, 256, 0, L.s>>>(a, hist, hot_n, W.hot_parts, part); note_launch(); }
-    else
-      { hot_grad_kernel<2><<<hg, 256, 0, L.s>>>(a, hist, hot_n, W.hot_parts, part); note_launch(); }
+    const float* part = reinterpret_cast<const float*>(ws + W.hot_part);
+    cudaError_t e = launch_hot_grad(L, W, ws, grad_out);
+    if (e != cudaSuccess) return e;
     { hot_finish_kernel<<<static_cast<unsigned>(d->T) * kHot, 256, 0, L.s>>>(
         a, hot_keys, hot_n, hot_cnt, W.hot_parts, part); note_launch(); }
   }
@@ -914,8 +830,10 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   { hot_thresh_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(d->T, sel_hist, sel_thresh); note_launch(); }
   { hot_select_kernel<<<blocks, 256, 0, L.s>>>(a, rs, hot_keys, hot_n, hot_cnt, min_count,
                                              sel_thresh, sel_keys, sel_n); note_launch(); }
-  { hot_commit_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(d->T, sel_keys, sel_n, hot_keys, hot_n,
-                                                    reinterpret_cast<uint32_t*>(ws + W.hot_mult)); note_launch(); }
+  { hot_commit_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(
+      d->T, sel_keys, sel_n, reinterpret_cast<uint32_t*>(ws + W.hot_keys(W.hot_next)),
+      reinterpret_cast<uint32_t*>(ws + W.hot_n(W.hot_next)),
+      reinterpret_cast<uint32_t*>(ws + W.hot_mult(W.hot_next))); note_launch(); }
   return cudaGetLastError();
 }
 

@@ -82,3 +82,30 @@ def test_hot_rows_absent_from_the_batch_stay_untouched():
         D = int(w.D[0])
         assert np.array_equal(W_gpu[r * D:(r + 1) * D].view(np.uint16),
                               w.weights[r * D:(r + 1) * D].numpy().view(np.uint16))
+
+
+def test_hot_set_carries_over_between_batches_of_different_sizes():
+    # the hot set lives at a workspace offset that does not depend on n: a
+    # batch with fewer lookups after a larger one still finds (and validates)
+    # it, and the result matches the oracle
+    w_big = make("hot", seed=2)
+    run = H.Run(w_big)
+    run.backward()
+    hot = run.hot_set()
+    assert sum(len(h) for h in hot) > 0
+    B = w_big.B
+    off = w_big.offsets.clone()
+    # second batch: every bag keeps only its first half
+    half = (off[1:] - off[:-1]) // 2
+    keep = torch.cat([torch.arange(int(off[i]), int(off[i]) + int(half[i]))
+                      for i in range(len(half))])
+    idx2 = w_big.indices[keep]
+    off2 = torch.cat([torch.zeros(1, dtype=off.dtype), torch.cumsum(half, 0).to(off.dtype)])
+    w2 = workloads.from_arrays(w_big.E, w_big.D, B, idx2, off2, w_big.weights, w_big.grad_out,
+                               momentum=w_big.momentum, lr=w_big.lr, eps=w_big.eps)
+    assert w2.n < w_big.n
+    run.w = w2
+    run.indices, run.offsets = idx2.cuda(), off2.cuda()
+    run.reset_state()
+    check_step(run, w2)
+    assert run.hot_set()[0].size > 0
