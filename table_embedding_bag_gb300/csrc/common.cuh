@@ -59,20 +59,39 @@ constexpr int kMaxD = 1024;
 // previous backward) bypass the sort; their gradients are histogram(bag x hot
 // row)^T x grad_out.  The histogram is kept only if it fits kHotBudgetBytes,
 // and tables wider than kHotMaxD take no hot rows.
-constexpr int kHot = 64;
+#ifndef TBE_HOT_ROWS
+#define TBE_HOT_ROWS 256
+#endif
+constexpr int kHot = TBE_HOT_ROWS;
 constexpr int kHotTileBags = 128;  // bags per expand CTA (one table)
 constexpr int kHotMaxD = 256;
 constexpr size_t kHotBudgetBytes = size_t(2) << 30;
-constexpr int kHotCtaTarget = 320;  // CTAs of the hot-gradient kernel
+constexpr int kHotCtaTarget = 304;  // CTAs of the hot-gradient kernel: one wave at 2 per SM on 152 SMs
 constexpr int kHotMinPartBags = 256;  // fewest bags per hot-gradient CTA
 constexpr int kHotFwdMinBagLen = 64;  // preprocessed forward: mean lookups per bag to use it
 constexpr int kHotBuckets = 256;    // log-scale buckets of lookup counts (8 per octave)
-constexpr int kHotHashBits = 10;    // shared-memory hash of a table's hot set: 1024 entries
+// A row becomes hot with at least max(B / kHotMinCountDiv, 32) lookups in a
+// batch: its histogram column costs about 12 bytes per bag (written once,
+// read by the forward and the gradient), a cold lookup costs several hundred
+// (row gather, gradient-row gather, sort traffic).
+constexpr int kHotMinCountDiv = 64;
+static_assert(kHot % 64 == 0 && kHot <= 256, "hot slots: multiples of the 64-slot MMA chunk");
+
+// Hot-set membership: a two-choice (cuckoo) hash of the table's hot keys in
+// shared memory, two halves of kCuckooHalf entries.  When the set is chosen,
+// multipliers m1, m2 are found under which every key has a place at
+// h1 = (key * m1) >> s or kCuckooHalf + ((key * m2) >> s), and each key's place
+// is stored with the set, so a lookup is two independent 64-bit shared loads.
+constexpr int kCuckooHalfBits = 9;
+constexpr int kCuckooHalf = 1 << kCuckooHalfBits;
+constexpr int kCuckooSize = 2 * kCuckooHalf;
 constexpr uint32_t kEmptyKey = 0xffffffffu;  // never a key: total_E < 2^32 - 1
 
-// Hash of a hot-set key under the table's multiplier (one-to-one on the set).
-__host__ __device__ __forceinline__ uint32_t hot_hash(uint32_t key, uint32_t mult) {
-  return (key * mult) >> (32 - kHotHashBits);
+__host__ __device__ __forceinline__ uint32_t cuckoo_h1(uint32_t key, uint32_t m1) {
+  return (key * m1) >> (32 - kCuckooHalfBits);
+}
+__host__ __device__ __forceinline__ uint32_t cuckoo_h2(uint32_t key, uint32_t m2) {
+  return kCuckooHalf + ((key * m2) >> (32 - kCuckooHalfBits));
 }
 
 // Long-run chunks are processed in order of the first bag they touch, binned
@@ -128,20 +147,24 @@ struct WsLayout {
   size_t tree_cnt;     // uint32 [max_tree] arrivals still expected at each tree node
   size_t partials;     // float [max_chunks * max_D]
   size_t tree_part;    // float [max_tree * max_D]
-  // Two hot sets, each uint32 keys [T][kHot] (sorted linear keys), n [T] and
-  // mult [T] (collision-free hash multiplier), kept across calls: `hot_next`
-  // is written by the backward's refresh and copied to `hot_cur` at the start
-  // of every preprocess; the preprocess, the forward and the backward of one
-  // batch all read `hot_cur`.
+  // Two hot sets, each uint32 keys [T][kHot] (sorted linear keys), place
+  // [T][kHot] (each key's cuckoo entry), n [T], m1 [T], m2 [T], kept across
+  // calls: `hot_next` is written by the backward's refresh and copied to
+  // `hot_cur` at the start of every preprocess; the preprocess, the forward
+  // and the backward of one batch all read `hot_cur`.
   size_t hot_cur;
   size_t hot_next;
   size_t hot_set_bytes;
   size_t hot_keys(size_t set) const { return set; }
-  size_t hot_n(size_t set) const { return set + static_cast<size_t>(T) * kHot * 4; }
-  size_t hot_mult(size_t set) const { return set + static_cast<size_t>(T) * (kHot + 1) * 4; }
+  size_t hot_place(size_t set) const { return set + static_cast<size_t>(T) * kHot * 4; }
+  size_t hot_n(size_t set) const { return set + static_cast<size_t>(T) * kHot * 8; }
+  size_t hot_m1(size_t set) const { return hot_n(set) + static_cast<size_t>(T) * 4; }
+  size_t hot_m2(size_t set) const { return hot_n(set) + static_cast<size_t>(T) * 8; }
   int64_t T;
   size_t hot_cnt;      // uint32 [T][kHot] lookups of each hot row in this call
-  size_t hot_hist;     // float [T][kHot][B] per-bag weight of each hot row (if enabled)
+  size_t hot_hist;     // float [T][B][kHot] per-bag weight of each hot row (if enabled)
+  size_t hot_scale;    // int8 [T*B] per-bag exponent: histogram row x 2^scale peaks in [2^14, 2^15)
+  size_t cold_off;     // uint32 [T*B + 1] first cold-list entry of each bag
   size_t hot_part;     // float [T][hot_parts][kHot][kHotMaxD] partial hot gradients
   size_t bag_cold;     // uint32 [T*B] cold lookups per bag
   size_t tile_cold;    // uint32 [hot_tiles + 1] cold lookups per expand tile, then prefix

@@ -37,26 +37,142 @@ __global__ void __launch_bounds__(256, TBE_FWD_MINB)
     const int64_t d0 = __ldg(D_offsets + t);
     const int D = static_cast<int>(__ldg(D_offsets + t + 1) - d0);
     if (D < 8 || D > kMaxD || (D & 7)) continue;  // widths the vector path cannot move
-    const int64_t E = __ldg(hash_base + t + 1) - __ldg(hash_base + t);
+    const int64_t h0 = __ldg(hash_base + t);
+    const int64_t E = __ldg(hash_base + t + 1) - h0;
+    const int64_t rbase = 0;
+    const int mode = kPoolStore;
     const __half* Wt = W + __ldg(w_offsets + t);
     int64_t s, e;
     bag_range(offsets, bag, n, &s, &e);
     float* orow = out + b * total_D + d0;
     const int nvec = D >> 3;
     if (nvec <= 1)
-      pool_bag<1, IndexT, kWeighted>(Wt, E, 0, D, 0, indices, psw, s, e, orow, true, status);
+      pool_bag<1, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status);
     else if (nvec <= 2)
-      pool_bag<2, IndexT, kWeighted>(Wt, E, 0, D, 0, indices, psw, s, e, orow, true, status);
+      pool_bag<2, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status);
     else if (nvec <= 4)
-      pool_bag<4, IndexT, kWeighted>(Wt, E, 0, D, 0, indices, psw, s, e, orow, true, status);
+      pool_bag<4, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status);
     else if (nvec <= 8)
-      pool_bag<8, IndexT, kWeighted>(Wt, E, 0, D, 0, indices, psw, s, e, orow, true, status);
+      pool_bag<8, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status);
     else if (nvec <= 16)
-      pool_bag<16, IndexT, kWeighted>(Wt, E, 0, D, 0, indices, psw, s, e, orow, true, status);
+      pool_bag<16, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status);
     else
       for (int vec0 = 0; vec0 < nvec; vec0 += 32)
-        pool_bag<32, IndexT, kWeighted>(Wt, E, 0, D, vec0, indices, psw, s, e, orow, true,
+        pool_bag<32, IndexT, kWeighted>(Wt, E, rbase, D, vec0, indices, psw, s, e, orow, mode,
                                           status);
+  }
+}
+
+// Cold lists after tbe_preprocess: short bags, so a warp pools G = 32 / S
+// consecutive bags at once, one per group of S lanes (S = next_pow2(D / 8)
+// for the widest table, at most 32), which multiplies the loads in flight per
+// warp by G.  Lookups are linear keys (row = key - hash_base[t]); each
+// group's next index batch is loaded while the current one is gathered, and
+// when the bag's hot rows were already pooled into out (hot_n given, the
+// table has hot rows, D_t <= kHotMaxD) the out row is read at the start and
+// added to.  Rows wider than 8 S values take several column passes.
+template <int S, bool kWeighted>
+__global__ void __launch_bounds__(256, TBE_FWD_MINB)
+    forward_cold_kernel(const __half* __restrict__ W, const int64_t* __restrict__ D_offsets,
+                        const int64_t* __restrict__ hash_base, const int64_t* __restrict__ w_offsets,
+                        const uint32_t* __restrict__ keys, const uint32_t* __restrict__ cold_off,
+                        const float* __restrict__ psw, int T, int B, int64_t total_D,
+                        float* __restrict__ out, const uint32_t* __restrict__ hot_n) {
+  constexpr int G = 32 / S;
+  constexpr int U = S < TBE_FWD_UNROLL ? S : TBE_FWD_UNROLL;
+  const int lane = static_cast<int>(lane_id());
+  const int g = lane / S;
+  const int sl = lane % S;
+  const int warps = blockDim.x >> 5;
+  const int64_t nbags = static_cast<int64_t>(T) * B;
+  for (int64_t bag0 = (static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5)) * G;
+       bag0 < nbags; bag0 += static_cast<int64_t>(gridDim.x) * warps * G) {
+    const int64_t bag = bag0 + g;  // this group's bag
+    const bool live = bag < nbags;
+    const int t = live ? static_cast<int>(bag / B) : 0;
+    const int64_t b = bag - static_cast<int64_t>(t) * B;
+    const int64_t d0 = __ldg(D_offsets + t);
+    const int D = static_cast<int>(__ldg(D_offsets + t + 1) - d0);
+    const int64_t h0 = __ldg(hash_base + t);
+    const int64_t E = __ldg(hash_base + t + 1) - h0;
+    const __half* Wt = W + __ldg(w_offsets + t);
+    const bool add = live && hot_n && D <= kHotMaxD && hot_n[t] != 0;
+    const int64_t s = live ? static_cast<int64_t>(__ldg(cold_off + bag)) : 0;
+    const int64_t e = live ? static_cast<int64_t>(__ldg(cold_off + bag + 1)) : 0;
+    float* orow = out + b * total_D + d0;
+    const int nvec = D >> 3;
+    // groups may hold tables of different widths: passes run to the widest
+    int nvec_max = nvec;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) nvec_max = max(nvec_max, __shfl_xor_sync(kFull, nvec_max, o));
+    for (int vec0 = 0; vec0 < nvec_max; vec0 += S) {  // warp-uniform
+      const int vec = vec0 + sl;
+      const bool col_ok = live && vec < nvec;
+      const int col = col_ok ? vec * 8 : 0;
+      float acc[8];
+      if (add && col_ok) {
+        const float4 o0 = reinterpret_cast<const float4*>(orow + col)[0];
+        const float4 o1 = reinterpret_cast<const float4*>(orow + col)[1];
+        acc[0] = o0.x; acc[1] = o0.y; acc[2] = o0.z; acc[3] = o0.w;
+        acc[4] = o1.x; acc[5] = o1.y; acc[6] = o1.z; acc[7] = o1.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      }
+      int64_t p = s;
+      uint32_t nx_key = p + sl < e ? __ldg(keys + p + sl) : 0u;
+      float nx_w = (kWeighted && p + sl < e) ? __ldg(psw + p + sl) : 0.f;
+      for (;;) {
+        const int cnt = static_cast<int>(e - p < S ? (e - p > 0 ? e - p : 0) : S);
+        int cmax = cnt;
+#pragma unroll
+        for (int o = S; o < 32; o <<= 1) cmax = max(cmax, __shfl_xor_sync(kFull, cmax, o));
+        if (cmax == 0) break;  // warp-uniform
+        const uint32_t key = nx_key;
+        const float w_in = nx_w;
+        if (p + S + sl < e) {
+          nx_key = __ldg(keys + p + S + sl);
+          if (kWeighted) nx_w = __ldg(psw + p + S + sl);
+        }
+        const __half* my_row = reinterpret_cast<const __half*>(g_zero_row);
+        float my_w = 0.f;
+        if (sl < cnt) {
+          const int64_t r = static_cast<int64_t>(key) - h0;
+          if (r >= 0 && r < E) {
+            my_row = Wt + r * D;
+            if (kWeighted) my_w = w_in;
+          }
+        }
+        const uint64_t my_addr = reinterpret_cast<uint64_t>(my_row);
+        const uint32_t my_lo = static_cast<uint32_t>(my_addr);
+        const uint32_t my_hi = static_cast<uint32_t>(my_addr >> 32);
+#pragma unroll
+        for (int u0 = 0; u0 < S; u0 += U) {
+          if (u0 >= cmax) break;  // warp-uniform
+          uint4 v[U];
+          float wv[U];
+#pragma unroll
+          for (int uu = 0; uu < U; ++uu) {
+            const int src = g * S + u0 + uu;  // lane of this group holding lookup u0 + uu
+            const uint64_t ad = static_cast<uint64_t>(__shfl_sync(kFull, my_lo, src)) |
+                                (static_cast<uint64_t>(__shfl_sync(kFull, my_hi, src)) << 32);
+            if (kWeighted) wv[uu] = __shfl_sync(kFull, my_w, src);
+            v[uu] = ldg_u4(reinterpret_cast<const __half*>(ad) + col);
+          }
+#pragma unroll
+          for (int uu = 0; uu < U; ++uu) {
+            if (kWeighted) acc_half8(acc, v[uu], wv[uu]);
+            else add_half8(acc, v[uu]);
+          }
+        }
+        p += S;
+      }
+      if (col_ok) {
+        float4* o = reinterpret_cast<float4*>(orow + vec * 8);
+        __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+      }
+    }
   }
 }
 
@@ -195,6 +311,40 @@ cudaError_t launch_forward_generic(const Launch& L, const void* weights, const v
                                      static_cast<const int32_t*>(offsets), psw, out, status);
   return launch_forward_t<int64_t>(L, W, static_cast<const int64_t*>(indices),
                                    static_cast<const int64_t*>(offsets), psw, out, status);
+}
+
+template <int S>
+cudaError_t launch_cold_s(const Launch& L, const __half* W, const uint32_t* keys,
+                          const uint32_t* cold_off, const float* psw, float* out,
+                          const uint32_t* hot_n) {
+  const tbe_desc* d = L.d;
+  const int64_t tasks = (static_cast<int64_t>(d->T) * d->B + (32 / S) - 1) / (32 / S);
+  const int warps = 8;
+  int64_t blocks = (tasks + warps - 1) / warps;
+  if (blocks > (1 << 22)) blocks = 1 << 22;
+  if (blocks < 1) blocks = 1;
+  if (psw)
+    { forward_cold_kernel<S, true><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
+        W, d->D_offsets, d->hash_base, d->weights_offsets, keys, cold_off, psw, d->T, d->B,
+        d->total_D, out, hot_n); note_launch(); }
+  else
+    { forward_cold_kernel<S, false><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
+        W, d->D_offsets, d->hash_base, d->weights_offsets, keys, cold_off, psw, d->T, d->B,
+        d->total_D, out, hot_n); note_launch(); }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_forward_cold(const Launch& L, const void* weights, const uint32_t* cold_keys,
+                                const uint32_t* cold_off, const float* cold_psw, float* out,
+                                const uint32_t* hot_n) {
+  const __half* W = static_cast<const __half*>(weights);
+  const int64_t nvec = L.d->max_D / 8;  // lanes per row for the widest table
+  if (nvec <= 1) return launch_cold_s<1>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
+  if (nvec <= 2) return launch_cold_s<2>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
+  if (nvec <= 4) return launch_cold_s<4>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
+  if (nvec <= 8) return launch_cold_s<8>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
+  if (nvec <= 16) return launch_cold_s<16>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
+  return launch_cold_s<32>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
 }
 
 int64_t repair_scratch_blocks(int64_t nb1) { return (nb1 + kFixTile - 1) / kFixTile; }

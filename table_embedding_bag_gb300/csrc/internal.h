@@ -26,6 +26,11 @@ struct Launch {
 cudaError_t launch_forward_generic(const Launch& L, const void* weights, const void* indices,
                                    const void* offsets, const float* psw, float* out,
                                    int* status);
+// The generic kernel over tbe_preprocess's per-bag cold lists (linear keys);
+// with hot_n, bags of tables with hot rows are added to out.
+cudaError_t launch_forward_cold(const Launch& L, const void* weights, const uint32_t* cold_keys,
+                                const uint32_t* cold_off, const float* cold_psw, float* out,
+                                const uint32_t* hot_n);
 cudaError_t launch_check_offsets(const Launch& L, const void* offsets, bool repair, void* fixed,
                                  int64_t* scratch, int* status);
 int64_t repair_scratch_blocks(int64_t nb1);

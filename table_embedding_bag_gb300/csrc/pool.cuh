@@ -7,6 +7,10 @@
 namespace tbe {
 namespace {
 
+// How pool_bag leaves its sum: stored, or added to what out_row holds.
+constexpr int kPoolStore = 0;
+constexpr int kPoolAdd = 1;
+
 // A row of zeros (kMaxD fp16 values): the gather target of lookups that are
 // out of range or past a bag's end.  Static device memory is zero at module
 // load and nothing writes it.
@@ -25,7 +29,7 @@ template <int S, typename IndexT, bool kWeighted, int kUnroll = TBE_FWD_UNROLL>
 __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t E, int64_t rbase,
                                          int D, int vec0, const IndexT* __restrict__ indices,
                                          const float* __restrict__ psw, int64_t start,
-                                         int64_t end, float* __restrict__ out_row, bool stream,
+                                         int64_t end, float* __restrict__ out_row, int mode,
                                          int* status) {
   constexpr int G = 32 / S;
   constexpr int U = S < kUnroll ? S : kUnroll;  // row vectors in flight per lane
@@ -95,13 +99,14 @@ __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t 
 
   if (g == 0 && col_ok) {
     float4* o = reinterpret_cast<float4*>(out_row + vec * 8);
-    if (stream) {  // written once, not read back: evict first
-      __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
-      __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
-    } else {
-      o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (mode == kPoolAdd) {  // out already holds a partial sum of the bag
+      const float4 a = o[0], b = o[1];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
     }
+    // written once, not read back: evict first
+    __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
+    __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
   }
   if (status && __any_sync(kFull, bad) && lane == 0) set_status(status, TBE_ERR_INDEX_RANGE);
 }

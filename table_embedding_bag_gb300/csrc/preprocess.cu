@@ -45,20 +45,31 @@ constexpr int kRleTile = kRleThreads * kRleItems;
 // pass 2 (write) writes the cold lookups in position order, so the sort's
 // input order, and hence its stability, is the lookup order.
 
-// Hot-set membership: a collision-free hash of the table's hot keys in
-// shared memory.  When the hot set is chosen, a multiplier is picked for which
-// key -> (key * mult) >> (32 - kHotHashBits) is one-to-one on the set, so a
-// lookup is one 64-bit load: entry = key | slot << 32, empty = kEmptyKey.
+// Hot-set membership: the two-choice hash of the table's hot keys (see
+// kCuckooHalf); entry = key | slot << 32, empty = kEmptyKey.
 constexpr uint64_t kEmptyEntry = kEmptyKey;
 
 struct HotHash {
-  uint64_t e[1 << kHotHashBits];
+  uint64_t e[kCuckooSize];
+};
+
+// The table's hot set as the kernels read it.
+struct HotSet {
+  const uint32_t* keys;   // [T][kHot]
+  const uint32_t* place;  // [T][kHot]
+  const uint32_t* n;      // [T]
+  const uint32_t* m1;     // [T]
+  const uint32_t* m2;     // [T]
 };
 
 // Slot of `key` in the hot set, or -1.
-__device__ __forceinline__ int hot_lookup(const HotHash& h, uint32_t mult, uint32_t key) {
-  const uint64_t e = h.e[hot_hash(key, mult)];
-  return static_cast<uint32_t>(e) == key ? static_cast<int>(e >> 32) : -1;
+__device__ __forceinline__ int hot_lookup(const HotHash& h, uint32_t m1, uint32_t m2,
+                                          uint32_t key) {
+  const uint64_t e1 = h.e[cuckoo_h1(key, m1)];
+  const uint64_t e2 = h.e[cuckoo_h2(key, m2)];
+  return static_cast<uint32_t>(e1) == key   ? static_cast<int>(e1 >> 32)
+         : static_cast<uint32_t>(e2) == key ? static_cast<int>(e2 >> 32)
+                                            : -1;
 }
 
 struct TileInfo {
@@ -77,40 +88,45 @@ __device__ __forceinline__ TileInfo tile_info(int B) {
 }
 
 // Builds the hash of table t's hot set (empty when the histogram is disabled
-// or the table is too wide for the hot path); returns the number of hot rows.
-// Contains __syncthreads.
-__device__ int build_hot_hash(HotHash& h, uint32_t* mult, const uint32_t* hot_keys,
-                              const uint32_t* hot_n, const uint32_t* hot_mult,
+// or the table is too wide for the hot path); returns the number of hot
+// slots.  Contains __syncthreads.
+__device__ int build_hot_hash(HotHash& h, uint32_t* m1, uint32_t* m2, const HotSet& hs,
                               const int64_t* D_offsets, int64_t h0, int64_t E, int t,
                               bool enabled) {
   int nh = 0;
   if (enabled) {
     const int D = static_cast<int>(__ldg(D_offsets + t + 1) - __ldg(D_offsets + t));
-    nh = D <= kHotMaxD ? static_cast<int>(min(hot_n[t], static_cast<uint32_t>(kHot))) : 0;
+    nh = D <= kHotMaxD ? static_cast<int>(min(hs.n[t], static_cast<uint32_t>(kHot))) : 0;
   }
-  const uint32_t m = hot_mult[t];
-  for (int i = threadIdx.x; i < (1 << kHotHashBits); i += blockDim.x) h.e[i] = kEmptyEntry;
+  for (int i = threadIdx.x; i < kCuckooSize; i += blockDim.x) h.e[i] = kEmptyEntry;
   __syncthreads();
-  if (threadIdx.x < nh) {
-    // a key outside the table (a workspace last used for other tables) is
-    // left out: its slot stays empty
-    const uint32_t key = hot_keys[t * kHot + threadIdx.x];
-    if (key >= h0 && key < h0 + E)
-      h.e[hot_hash(key, m)] = key | (static_cast<uint64_t>(threadIdx.x) << 32);
+  for (int slot = threadIdx.x; slot < nh; slot += blockDim.x) {
+    // a key outside the table (a workspace last used for other tables) or a
+    // place outside the hash is left out: its slot stays empty
+    const uint32_t key = hs.keys[t * kHot + slot];
+    const uint32_t at = hs.place[t * kHot + slot];
+    if (key >= h0 && key < h0 + E && at < static_cast<uint32_t>(kCuckooSize))
+      h.e[at] = key | (static_cast<uint64_t>(slot) << 32);
   }
-  *mult = m;
+  *m1 = hs.m1[t];
+  *m2 = hs.m2[t];
   __syncthreads();
   return nh;
 }
+
+// Histogram slots written per bag: nh rounded up to the 64-slot MMA chunk.
+__device__ __forceinline__ int hot_slots_padded(int nh) { return (nh + 63) & ~63; }
 
 template <typename IndexT, bool kWeighted>
 struct ExpandSmem {
   HotHash hash;
   uint32_t warp_cold[8];
-  // per-bag weight of each hot row: exact sums (integer counts, or fp32
-  // weights summed in double), so the result does not depend on atomic order.
-  // Rows are padded by one so that one bag's slots fall in different banks.
-  typename std::conditional<kWeighted, double, uint32_t>::type hist[kHot][kHotTileBags + 1];
+  uint32_t slot_cnt[kHot];
+  // the bag each warp is on: per-slot weight (exact sums: integer counts, or
+  // fp32 weights summed in double, so the result does not depend on atomic
+  // order) and, weighted, per-slot lookups
+  typename std::conditional<kWeighted, double, uint32_t>::type row[8][kHot];
+  uint32_t cnt_row[kWeighted ? 8 : 1][kWeighted ? kHot : 1];
 };
 
 constexpr int kExpandLoads = 4;  // index loads in flight per lane
@@ -119,23 +135,30 @@ template <typename IndexT, bool kWeighted>
 __global__ void __launch_bounds__(256)
     expand_count_kernel(const IndexT* __restrict__ indices, const IndexT* __restrict__ offsets,
                         const float* __restrict__ psw, const int64_t* __restrict__ hash_base,
-                        const int64_t* __restrict__ D_offsets, int64_t n, int B,
-                        const uint32_t* __restrict__ hot_keys, const uint32_t* __restrict__ hot_n,
-                        const uint32_t* __restrict__ hot_mult, float* __restrict__ hot_hist, uint32_t* __restrict__ hot_cnt,
-                        uint32_t* __restrict__ bag_cold, uint32_t* __restrict__ tile_cold,
-                        int* status) {
+                        const int64_t* __restrict__ D_offsets, int64_t n, int B, HotSet hs,
+                        float* __restrict__ hot_hist, int8_t* __restrict__ hot_scale,
+                        uint32_t* __restrict__ hot_cnt, uint32_t* __restrict__ bag_cold,
+                        uint32_t* __restrict__ tile_cold, int* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   ExpandSmem<IndexT, kWeighted>& sm = *reinterpret_cast<ExpandSmem<IndexT, kWeighted>*>(smem_raw);
   const TileInfo ti = tile_info(B);
   const int warp = threadIdx.x >> 5;
   const unsigned lane = lane_id();
-  for (int i = threadIdx.x; i < kHot * (kHotTileBags + 1); i += blockDim.x)
-    sm.hist[i / (kHotTileBags + 1)][i % (kHotTileBags + 1)] = 0;
+  for (int i = threadIdx.x; i < 8 * kHot; i += blockDim.x) {
+    sm.row[i / kHot][i % kHot] = 0;
+    if constexpr (kWeighted) sm.cnt_row[i / kHot][i % kHot] = 0;
+  }
+  for (int i = threadIdx.x; i < kHot; i += blockDim.x) sm.slot_cnt[i] = 0;
   const int64_t h0 = __ldg(hash_base + ti.t);
   const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
-  uint32_t mult;
-  const int nh = build_hot_hash(sm.hash, &mult, hot_keys, hot_n, hot_mult, D_offsets, h0, E,
-                                ti.t, hot_hist != nullptr);
+  uint32_t m1, m2;
+  const int nh = build_hot_hash(sm.hash, &m1, &m2, hs, D_offsets, h0, E, ti.t,
+                                hot_hist != nullptr);
+  const int nh_pad = hot_slots_padded(nh);
+  constexpr int kPerLane = kHot / 32;
+  uint32_t cnt[kPerLane];  // lane l: lookups of slots l, l + 32, ... over the tile
+#pragma unroll
+  for (int j = 0; j < kPerLane; ++j) cnt[j] = 0;
   bool bad = false;
   uint32_t cold_w = 0;
   for (int lb = warp; lb < ti.nbags; lb += 8) {
@@ -157,17 +180,19 @@ __global__ void __launch_bounds__(256)
         const bool ok = inside && r[u] >= 0 && r[u] < E;
         bad |= inside && !ok;
         const int slot =
-            ok && nh ? hot_lookup(sm.hash, mult, static_cast<uint32_t>(h0 + r[u])) : -1;
+            ok && nh ? hot_lookup(sm.hash, m1, m2, static_cast<uint32_t>(h0 + r[u])) : -1;
         cold += ok && slot < 0;
         if constexpr (kWeighted) {
           // double sums of fp32 weights are exact: atomic order does not matter
-          if (slot >= 0)
-            atomicAdd(&sm.hist[slot][lb], static_cast<double>(__ldg(psw + base + u * 32 + lane)));
+          if (slot >= 0) {
+            atomicAdd(&sm.row[warp][slot], static_cast<double>(__ldg(psw + base + u * 32 + lane)));
+            atomicAdd(&sm.cnt_row[warp][slot], 1u);
+          }
         } else {
           // one add per distinct hot row of the 32 lookups
           const unsigned peers = __match_any_sync(kFull, slot);
           if (slot >= 0 && lane == static_cast<unsigned>(__ffs(peers) - 1))
-            atomicAdd(&sm.hist[slot][lb], static_cast<uint32_t>(__popc(peers)));
+            atomicAdd(&sm.row[warp][slot], static_cast<uint32_t>(__popc(peers)));
         }
       }
     }
@@ -175,27 +200,51 @@ __global__ void __launch_bounds__(256)
     for (int o = 16; o > 0; o >>= 1) cold += __shfl_xor_sync(kFull, cold, o);
     if (lane == 0) bag_cold[bag] = cold;
     cold_w += cold;
+    if (nh_pad) {
+      // flush the bag's row: histogram entries, per-bag scale, slot counts
+      __syncwarp();
+      float* dst = hot_hist + bag * kHot;
+      float peak = 0.f;
+#pragma unroll
+      for (int j = 0; j < kPerLane; ++j) {
+        const int slot = lane + 32 * j;
+        if (slot < nh_pad) {
+          const auto v = sm.row[warp][slot];
+          const float f = static_cast<float>(v);
+          dst[slot] = f;
+          peak = fmaxf(peak, fabsf(f));
+          if constexpr (kWeighted) {
+            cnt[j] += sm.cnt_row[warp][slot];
+            sm.cnt_row[warp][slot] = 0;
+          } else {
+            cnt[j] += v;
+          }
+          sm.row[warp][slot] = 0;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) peak = fmaxf(peak, __shfl_xor_sync(kFull, peak, o));
+      if (lane == 0) {
+        // exponent taking the bag's largest entry into [2^14, 2^15)
+        int sc = 0;
+        if (peak > 0.f) sc = 14 - ilogbf(peak);
+        hot_scale[bag] = static_cast<int8_t>(sc < -126 ? -126 : (sc > 126 ? 126 : sc));
+      }
+      __syncwarp();
+    }
   }
   if (lane == 0) sm.warp_cold[warp] = cold_w;
+#pragma unroll
+  for (int j = 0; j < kPerLane; ++j)
+    if (cnt[j]) atomicAdd(&sm.slot_cnt[lane + 32 * j], cnt[j]);
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t c = 0;
     for (int w = 0; w < 8; ++w) c += sm.warp_cold[w];
     tile_cold[blockIdx.x] = c;
   }
-  // each warp writes out 8 slots; lookups per slot = bags' counts summed
-  for (int slot = warp; slot < nh; slot += 8) {
-    uint32_t c = 0;
-    for (int lb = lane; lb < ti.nbags; lb += 32) {
-      const auto v = sm.hist[slot][lb];
-      hot_hist[(static_cast<int64_t>(ti.t) * kHot + slot) * B + ti.b0 + lb] = static_cast<float>(v);
-      if constexpr (kWeighted) c += v != 0.0;  // weighted counts nonzero-weight bags only
-      else c += v;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
-    if (lane == 0 && c) atomicAdd(&hot_cnt[ti.t * kHot + slot], c);
-  }
+  for (int i = threadIdx.x; i < nh; i += blockDim.x)
+    if (sm.slot_cnt[i]) atomicAdd(&hot_cnt[ti.t * kHot + i], sm.slot_cnt[i]);
   if (status && __any_sync(kFull, bad) && lane == 0) set_status(status, TBE_ERR_INDEX_RANGE);
 }
 
@@ -203,11 +252,11 @@ template <typename IndexT, bool kWeighted>
 __global__ void __launch_bounds__(256)
     expand_write_kernel(const IndexT* __restrict__ indices, const IndexT* __restrict__ offsets,
                         const float* __restrict__ psw, const int64_t* __restrict__ hash_base,
-                        const int64_t* __restrict__ D_offsets, int64_t n, int B,
-                        const uint32_t* __restrict__ hot_keys, const uint32_t* __restrict__ hot_n,
-                        const uint32_t* __restrict__ hot_mult, bool hot_enabled, const uint32_t* __restrict__ bag_cold,
-                        const uint32_t* __restrict__ tile_base, uint32_t* __restrict__ keys,
-                        uint32_t* __restrict__ vals, float* __restrict__ psw_out) {
+                        const int64_t* __restrict__ D_offsets, int64_t n, int B, HotSet hs,
+                        bool hot_enabled, const uint32_t* __restrict__ bag_cold,
+                        const uint32_t* __restrict__ tile_base, uint32_t* __restrict__ cold_off,
+                        uint32_t* __restrict__ keys, uint32_t* __restrict__ vals,
+                        float* __restrict__ psw_out) {
   __shared__ HotHash hash;
   __shared__ uint32_t bag_base[kHotTileBags];
   __shared__ uint32_t scan[33];
@@ -215,18 +264,23 @@ __global__ void __launch_bounds__(256)
   const int warp = threadIdx.x >> 5;
   const unsigned lane = lane_id();
   {
-    // exclusive prefix of the tile's per-bag cold counts
+    // exclusive prefix of the tile's per-bag cold counts = the bags' first
+    // entries in the cold list
     const int lb = threadIdx.x;
     const uint32_t c =
         lb < ti.nbags ? bag_cold[static_cast<int64_t>(ti.t) * B + ti.b0 + lb] : 0u;
-    const uint32_t inc = block_inclusive_scan(c, OpSum(), 0u, scan);
-    if (lb < kHotTileBags) bag_base[lb] = tile_base[blockIdx.x] + inc - c;
+    uint32_t total;
+    const uint32_t inc = block_inclusive_scan(c, OpSum(), 0u, scan, &total);
+    const uint32_t first = tile_base[blockIdx.x] + inc - c;
+    if (lb < kHotTileBags) bag_base[lb] = first;
+    if (lb < ti.nbags) cold_off[static_cast<int64_t>(ti.t) * B + ti.b0 + lb] = first;
+    if (lb == 0 && blockIdx.x == gridDim.x - 1)
+      cold_off[static_cast<int64_t>(ti.t) * B + ti.b0 + ti.nbags] = tile_base[blockIdx.x] + total;
   }
   const int64_t h0 = __ldg(hash_base + ti.t);
   const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
-  uint32_t mult;
-  const int nh = build_hot_hash(hash, &mult, hot_keys, hot_n, hot_mult, D_offsets, h0, E, ti.t,
-                                hot_enabled);
+  uint32_t m1, m2;
+  const int nh = build_hot_hash(hash, &m1, &m2, hs, D_offsets, h0, E, ti.t, hot_enabled);
   const unsigned lt = (1u << lane) - 1u;
   for (int lb = warp; lb < ti.nbags; lb += 8) {
     const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
@@ -247,7 +301,7 @@ __global__ void __launch_bounds__(256)
         uint32_t key = 0;
         if (r[u] >= 0 && r[u] < E) {
           key = static_cast<uint32_t>(h0 + r[u]);
-          cold = !nh || hot_lookup(hash, mult, key) < 0;
+          cold = !nh || hot_lookup(hash, m1, m2, key) < 0;
         }
         const unsigned m = __ballot_sync(kFull, cold);
         if (cold) {
@@ -901,32 +955,36 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     err = cudaMemcpyAsync(ws + W.hot_cur, ws + W.hot_next, W.hot_set_bytes,
                           cudaMemcpyDeviceToDevice, s);
     if (err != cudaSuccess) return err;
-    const uint32_t* hk = reinterpret_cast<const uint32_t*>(ws + W.hot_keys(W.hot_cur));
-    const uint32_t* hn = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_cur));
-    const uint32_t* hm = reinterpret_cast<const uint32_t*>(ws + W.hot_mult(W.hot_cur));
+    HotSet hs;
+    hs.keys = reinterpret_cast<const uint32_t*>(ws + W.hot_keys(W.hot_cur));
+    hs.place = reinterpret_cast<const uint32_t*>(ws + W.hot_place(W.hot_cur));
+    hs.n = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_cur));
+    hs.m1 = reinterpret_cast<const uint32_t*>(ws + W.hot_m1(W.hot_cur));
+    hs.m2 = reinterpret_cast<const uint32_t*>(ws + W.hot_m2(W.hot_cur));
     float* hh = W.hot_enabled ? reinterpret_cast<float*>(ws + W.hot_hist) : nullptr;
+    int8_t* hsc = reinterpret_cast<int8_t*>(ws + W.hot_scale);
     uint32_t* hc = reinterpret_cast<uint32_t*>(ws + W.hot_cnt);
     uint32_t* bc = reinterpret_cast<uint32_t*>(ws + W.bag_cold);
+    uint32_t* co = reinterpret_cast<uint32_t*>(ws + W.cold_off);
     const unsigned tiles = static_cast<unsigned>(W.hot_tiles);
     if (weighted)
       { expand_count_kernel<IndexT, true><<<tiles, 256, sizeof(ExpandSmem<IndexT, true>), s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hm, hh, hc, bc,
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh, hsc, hc, bc,
           tile_cold, status); note_launch(); }
     else
       { expand_count_kernel<IndexT, false><<<tiles, 256, sizeof(ExpandSmem<IndexT, false>), s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hm, hh, hc, bc,
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh, hsc, hc, bc,
           tile_cold, status); note_launch(); }
     { exclusive_scan_kernel<<<1, 1024, 0, s>>>(tile_cold, W.hot_tiles, counters + kCntSortN); note_launch(); }
     if (weighted)
       { expand_write_kernel<IndexT, true><<<tiles, 256, 0, s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hm, W.hot_enabled, bc,
-          tile_cold, keys[2], vals[2], pw[2]); note_launch(); }
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, W.hot_enabled, bc,
+          tile_cold, co, keys[2], vals[2], pw[2]); note_launch(); }
     else
       { expand_write_kernel<IndexT, false><<<tiles, 256, 0, s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hk, hn, hm, W.hot_enabled, bc,
-          tile_cold, keys[2], vals[2], pw[2]); note_launch(); }
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, W.hot_enabled, bc,
+          tile_cold, co, keys[2], vals[2], pw[2]); note_launch(); }
   }
-
   if (n > 0) {
     const SortGeom g = sort_geom(n, L.num_sms, 2, counters + kCntSortN);
     const int bits = key_bits(d);

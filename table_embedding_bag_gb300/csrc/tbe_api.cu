@@ -28,7 +28,7 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   // so calls with different n (or weightedness) on one workspace agree.
   L.status = take(64);
   L.T = d->T;
-  L.hot_set_bytes = static_cast<size_t>(d->T) * (kHot + 2) * 4;
+  L.hot_set_bytes = static_cast<size_t>(d->T) * (2 * kHot + 3) * 4;
   L.hot_cur = take(L.hot_set_bytes);
   L.hot_next = take(L.hot_set_bytes);
   L.counts = take(kNumCounters * sizeof(uint32_t));
@@ -70,7 +70,9 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   L.hot_cnt = take(T * kHot * 4);
   L.hot_hist = L.hot_enabled ? take(static_cast<size_t>(T) * kHot * B * sizeof(float)) : 0;
   L.hot_part = L.hot_enabled ? take(static_cast<size_t>(T) * L.hot_parts * kHot * kHotMaxD * 4) : 0;
+  L.hot_scale = take(static_cast<size_t>(T) * B);
   L.bag_cold = take(static_cast<size_t>(T) * B * 4);
+  L.cold_off = take((static_cast<size_t>(T) * B + 1) * 4);
   L.tile_cold = take((L.hot_tiles + 1) * 4);
   L.sel_hist = take(T * kHotBuckets * 4);
   L.sel_thresh = take(T * 4);

@@ -698,61 +698,106 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// The selected keys, sorted per table, become the hot set, together with the
-// first multiplier of a fixed odd sequence whose hash is one-to-one on them.
-// If none of kMultTries is (about one chance in 10^16 for 64 keys in 1024
-// entries), keys that collide under the first multiplier are dropped.
-constexpr int kMultTries = 256;
+// The selected keys, sorted per table, become the hot set, together with a
+// place for each key in the two-choice hash (see kCuckooHalf): one CTA per
+// table sorts the keys (bitonic), then one thread inserts them with
+// displacement under the first multiplier pair of a fixed sequence for which
+// every insertion succeeds within kCuckooKicks moves.  At a load of 1/4 the
+// first pair almost always succeeds; if kCuckooTries pairs fail, keys that
+// find no free place without displacement under the first pair are dropped
+// from the set (a smaller set stays correct, only less effective).
+constexpr int kCuckooTries = 64;
+constexpr int kCuckooKicks = 128;
 
-__device__ __forceinline__ uint32_t mult_candidate(int i) {
+__device__ __forceinline__ uint32_t odd_mult(int i) {
   return (0x9E3779B1u + 2u * static_cast<uint32_t>(i) * 0x3C6EF372u) | 1u;
 }
 
-__device__ bool one_to_one(const uint32_t* k, uint32_t nsel, uint32_t mult) {
-  uint32_t used[(1 << kHotHashBits) / 32];
-  for (int i = 0; i < (1 << kHotHashBits) / 32; ++i) used[i] = 0;
-  for (uint32_t i = 0; i < nsel; ++i) {
-    const uint32_t h = hot_hash(k[i], mult);
-    if (used[h >> 5] & (1u << (h & 31))) return false;
-    used[h >> 5] |= 1u << (h & 31);
+// Inserts key into tab (kEmptyKey = free); false if kicks run out (the table
+// then holds some other key displaced out, so the caller starts over).
+__device__ bool cuckoo_insert(uint32_t* tab, uint32_t key, uint32_t m1, uint32_t m2,
+                              bool displace) {
+  uint32_t cur = key;
+  uint32_t pos = cuckoo_h1(cur, m1);
+  if (tab[pos] == kEmptyKey) { tab[pos] = cur; return true; }
+  pos = cuckoo_h2(cur, m2);
+  if (tab[pos] == kEmptyKey) { tab[pos] = cur; return true; }
+  if (!displace) return false;
+  for (int kick = 0; kick < kCuckooKicks; ++kick) {
+    const uint32_t out = tab[pos];
+    tab[pos] = cur;
+    cur = out;
+    // the displaced key moves to its other place
+    pos = pos == cuckoo_h1(cur, m1) ? cuckoo_h2(cur, m2) : cuckoo_h1(cur, m1);
+    if (tab[pos] == kEmptyKey) { tab[pos] = cur; return true; }
   }
-  return true;
+  return false;
 }
 
-__global__ void hot_commit_kernel(int T, const uint32_t* __restrict__ sel_keys,
-                                  const uint32_t* __restrict__ sel_n, uint32_t* __restrict__ hot_keys,
-                                  uint32_t* __restrict__ hot_n, uint32_t* __restrict__ hot_mult) {
-  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
-    uint32_t nsel = min(sel_n[t], static_cast<uint32_t>(kHot));
-    uint32_t k[kHot];
-    for (uint32_t i = 0; i < nsel; ++i) {
-      uint32_t v = sel_keys[t * kHot + i];
-      uint32_t j = i;
-      for (; j > 0 && k[j - 1] > v; --j) k[j] = k[j - 1];
-      k[j] = v;
-    }
-    uint32_t mult = 0;
-    bool found = false;
-    for (int i = 0; i < kMultTries && !found; ++i) {
-      mult = mult_candidate(i);
-      found = one_to_one(k, nsel, mult);
-    }
-    if (!found) {
-      mult = mult_candidate(0);
-      uint32_t used[(1 << kHotHashBits) / 32];
-      for (int i = 0; i < (1 << kHotHashBits) / 32; ++i) used[i] = 0;
-      uint32_t kept = 0;
-      for (uint32_t i = 0; i < nsel; ++i) {
-        const uint32_t h = hot_hash(k[i], mult);
-        if (used[h >> 5] & (1u << (h & 31))) continue;
-        used[h >> 5] |= 1u << (h & 31);
-        k[kept++] = k[i];
+__global__ void __launch_bounds__(kHot)
+    hot_commit_kernel(const uint32_t* __restrict__ sel_keys, const uint32_t* __restrict__ sel_n,
+                      uint32_t* __restrict__ hot_keys, uint32_t* __restrict__ hot_place,
+                      uint32_t* __restrict__ hot_n, uint32_t* __restrict__ hot_m1,
+                      uint32_t* __restrict__ hot_m2) {
+  __shared__ uint32_t k[kHot];
+  __shared__ uint32_t tab[kCuckooSize];
+  __shared__ uint32_t scan[33];
+  __shared__ uint32_t mults[2];
+  const int t = blockIdx.x;
+  const int i = threadIdx.x;
+  const uint32_t nsel = min(sel_n[t], static_cast<uint32_t>(kHot));
+  k[i] = i < static_cast<int>(nsel) ? sel_keys[t * kHot + i] : kEmptyKey;
+  // bitonic sort of kHot keys, ascending (padding kEmptyKey sorts last)
+  for (int size = 2; size <= kHot; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      const int j = i ^ stride;
+      if (j > i) {
+        const bool up = (i & size) == 0;
+        const uint32_t a = k[i], b = k[j];
+        if ((a > b) == up) { k[i] = b; k[j] = a; }
       }
-      nsel = kept;
     }
-    for (uint32_t i = 0; i < nsel; ++i) hot_keys[t * kHot + i] = k[i];
-    hot_n[t] = nsel;
-    hot_mult[t] = mult;
+  __syncthreads();
+  if (i == 0) {
+    bool ok = false;
+    uint32_t m1 = odd_mult(0), m2 = odd_mult(1);
+    for (int tr = 0; tr < kCuckooTries && !ok; ++tr) {
+      m1 = odd_mult(2 * tr);
+      m2 = odd_mult(2 * tr + 1);
+      for (int e = 0; e < kCuckooSize; ++e) tab[e] = kEmptyKey;
+      ok = true;
+      for (uint32_t s = 0; s < nsel && ok; ++s) ok = cuckoo_insert(tab, k[s], m1, m2, true);
+    }
+    if (!ok) {
+      m1 = odd_mult(0);
+      m2 = odd_mult(1);
+      for (int e = 0; e < kCuckooSize; ++e) tab[e] = kEmptyKey;
+      for (uint32_t s = 0; s < nsel; ++s) cuckoo_insert(tab, k[s], m1, m2, false);
+    }
+    mults[0] = m1;
+    mults[1] = m2;
+  }
+  __syncthreads();
+  const uint32_t m1 = mults[0], m2 = mults[1];
+  // keep the placed keys in sorted order with their places
+  uint32_t place = kCuckooSize;
+  if (i < static_cast<int>(nsel)) {
+    const uint32_t key = k[i];
+    if (tab[cuckoo_h1(key, m1)] == key) place = cuckoo_h1(key, m1);
+    else if (tab[cuckoo_h2(key, m2)] == key) place = cuckoo_h2(key, m2);
+  }
+  const uint32_t kept = place < static_cast<uint32_t>(kCuckooSize) ? 1u : 0u;
+  uint32_t total;
+  const uint32_t inc = block_inclusive_scan(kept, OpSum(), 0u, scan, &total);
+  if (kept) {
+    hot_keys[t * kHot + inc - 1] = k[i];
+    hot_place[t * kHot + inc - 1] = place;
+  }
+  if (i == 0) {
+    hot_n[t] = total;
+    hot_m1[t] = m1;
+    hot_m2[t] = m2;
   }
 }
 
@@ -820,7 +865,8 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(ws + W.sel_n, 0, static_cast<size_t>(d->T) * 4, L.s);
   if (e != cudaSuccess) return e;
-  const uint32_t min_count = d->B / 8 > 32 ? static_cast<uint32_t>(d->B / 8) : 32u;
+  const uint32_t min_count =
+      d->B / kHotMinCountDiv > 32 ? static_cast<uint32_t>(d->B / kHotMinCountDiv) : 32u;
   const uint32_t* rs = reinterpret_cast<const uint32_t*>(ws + W.run_starts);
   uint32_t* sel_hist = reinterpret_cast<uint32_t*>(ws + W.sel_hist);
   uint32_t* sel_thresh = reinterpret_cast<uint32_t*>(ws + W.sel_thresh);
@@ -830,10 +876,12 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   { hot_thresh_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(d->T, sel_hist, sel_thresh); note_launch(); }
   { hot_select_kernel<<<blocks, 256, 0, L.s>>>(a, rs, hot_keys, hot_n, hot_cnt, min_count,
                                              sel_thresh, sel_keys, sel_n); note_launch(); }
-  { hot_commit_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(
-      d->T, sel_keys, sel_n, reinterpret_cast<uint32_t*>(ws + W.hot_keys(W.hot_next)),
+  { hot_commit_kernel<<<static_cast<unsigned>(d->T), kHot, 0, L.s>>>(
+      sel_keys, sel_n, reinterpret_cast<uint32_t*>(ws + W.hot_keys(W.hot_next)),
+      reinterpret_cast<uint32_t*>(ws + W.hot_place(W.hot_next)),
       reinterpret_cast<uint32_t*>(ws + W.hot_n(W.hot_next)),
-      reinterpret_cast<uint32_t*>(ws + W.hot_mult(W.hot_next))); note_launch(); }
+      reinterpret_cast<uint32_t*>(ws + W.hot_m1(W.hot_next)),
+      reinterpret_cast<uint32_t*>(ws + W.hot_m2(W.hot_next))); note_launch(); }
   return cudaGetLastError();
 }
 
