@@ -375,29 +375,36 @@ __global__ void __launch_bounds__(kSortThreads)
 // CTA c, the keys of smaller digits plus the keys of digit d in CTAs before c.
 // One CTA, one thread per digit walking the CTAs (loads are coalesced across
 // threads), then a scan of the digit totals.  In place on counts[c][d].
-__global__ void __launch_bounds__(1 << kMaxRadixBits)
-    radix_scan_kernel(uint32_t* __restrict__ counts, int ctas, int nd) {
-  __shared__ uint32_t sm[33];
-  const int d = threadIdx.x;
-  uint32_t run = 0;
-  if (d < nd) {
-    constexpr int kAhead = 8;  // loads issued before the stores they precede
-    for (int c0 = 0; c0 < ctas; c0 += kAhead) {
-      uint32_t v[kAhead];
+// Digit-parallel scan of the upsweep's counts: one warp per digit d turns
+// counts[c][d] into the exclusive prefix over CTAs c of digit d and writes the
+// digit's total to totals[d]; the downsweep adds the exclusive prefix of the
+// totals over digits (its digit base).  Lane l owns CTAs [l k, (l + 1) k).
+constexpr int kScanPerLane = kMaxSortCtas / 32;
+
+__global__ void __launch_bounds__(256)
+    radix_scan_kernel(uint32_t* __restrict__ counts, int ctas, int nd,
+                      uint32_t* __restrict__ totals) {
+  const int d = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (d >= nd) return;  // warp-uniform
+  const int lane = static_cast<int>(lane_id());
+  const int k = (ctas + 31) / 32;
+  uint32_t v[kScanPerLane];
+  uint32_t sum = 0;
 #pragma unroll
-      for (int u = 0; u < kAhead; ++u)
-        v[u] = c0 + u < ctas ? counts[static_cast<int64_t>(c0 + u) * nd + d] : 0u;
-#pragma unroll
-      for (int u = 0; u < kAhead; ++u) {
-        if (c0 + u < ctas) counts[static_cast<int64_t>(c0 + u) * nd + d] = run;
-        run += v[u];
-      }
-    }
+  for (int j = 0; j < kScanPerLane; ++j) {
+    const int c = lane * k + j;
+    v[j] = (j < k && c < ctas) ? counts[static_cast<int64_t>(c) * nd + d] : 0u;
+    sum += v[j];
   }
-  const uint32_t inc = block_inclusive_scan(run, OpSum(), 0u, sm);
-  const uint32_t base = inc - run;
-  if (d < nd)
-    for (int c = 0; c < ctas; ++c) counts[static_cast<int64_t>(c) * nd + d] += base;
+  const uint32_t inc = warp_inclusive_scan(sum, OpSum());
+  uint32_t run = inc - sum;
+#pragma unroll
+  for (int j = 0; j < kScanPerLane; ++j) {
+    const int c = lane * k + j;
+    if (j < k && c < ctas) counts[static_cast<int64_t>(c) * nd + d] = run;
+    run += v[j];
+  }
+  if (lane == 31) totals[d] = inc;
 }
 
 // Single CTA: exclusive scan over `total` counts in place (digit-major order
@@ -472,7 +479,8 @@ __global__ void __launch_bounds__(kSortThreads, 2)
                            const float* __restrict__ psw_in, uint32_t* __restrict__ keys_out,
                            uint32_t* __restrict__ vals_out, float* __restrict__ psw_out,
                            SortGeom g, int shift, int width,
-                           const uint32_t* __restrict__ counts) {
+                           const uint32_t* __restrict__ counts,
+                           const uint32_t* __restrict__ totals) {
   const int64_t n = geom_n(g);
   extern __shared__ __align__(16) unsigned char smem_raw[];
   DownSmem<kWeighted>& sm = *reinterpret_cast<DownSmem<kWeighted>*>(smem_raw);
@@ -481,8 +489,17 @@ __global__ void __launch_bounds__(kSortThreads, 2)
   const int warp = threadIdx.x >> 5;
   const unsigned lane = lane_id();
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int d = threadIdx.x; d < nd; d += kSortThreads)
-    sm.run_off[d] = counts[static_cast<int64_t>(blockIdx.x) * nd + d];
+  {
+    // output start of each digit: the digit's base (exclusive prefix of the
+    // digit totals) plus this CTA's prefix within the digit
+    const int d0 = threadIdx.x * 2;
+    const uint32_t t0 = d0 < nd ? totals[d0] : 0u;
+    const uint32_t t1 = d0 + 1 < nd ? totals[d0 + 1] : 0u;
+    const uint32_t inc = block_inclusive_scan(t0 + t1, OpSum(), 0u, sm.scan);
+    if (d0 < nd) sm.run_off[d0] = inc - t0 - t1 + counts[static_cast<int64_t>(blockIdx.x) * nd + d0];
+    if (d0 + 1 < nd)
+      sm.run_off[d0 + 1] = inc - t1 + counts[static_cast<int64_t>(blockIdx.x) * nd + d0 + 1];
+  }
   int64_t b, e;
   cta_range(g, n, &b, &e);
   if (b < e) {
@@ -991,6 +1008,7 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     const int passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
     const int rb = (bits + passes - 1) / passes;
     uint32_t* counts = reinterpret_cast<uint32_t*>(ws + W.radix_counts);
+    uint32_t* totals = counts + static_cast<size_t>(kMaxSortCtas) * (1 << kMaxRadixBits);
     const size_t smem = weighted ? sizeof(DownSmem<true>) : sizeof(DownSmem<false>);
     for (int p = 0; p < passes; ++p) {
       const int shift = p * rb;
@@ -999,15 +1017,15 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
       // between 1 and 0, so the sorted result is in buffer passes & 1
       const int src = p == 0 ? 2 : (p & 1), dst = (p & 1) ^ 1;
       { radix_upsweep_kernel<<<g.ctas, kSortThreads, 0, s>>>(keys[src], g, shift, width, counts); note_launch(); }
-      { radix_scan_kernel<<<1, 1 << kMaxRadixBits, 0, s>>>(counts, g.ctas, 1 << width); note_launch(); }
+      { radix_scan_kernel<<<((1 << width) + 7) / 8, 256, 0, s>>>(counts, g.ctas, 1 << width, totals); note_launch(); }
       if (weighted)
         { radix_downsweep_kernel<true><<<g.ctas, kSortThreads, smem, s>>>(
             keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], g, shift, width,
-            counts); note_launch(); }
+            counts, totals); note_launch(); }
       else
         { radix_downsweep_kernel<false><<<g.ctas, kSortThreads, smem, s>>>(
             keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], g, shift, width,
-            counts); note_launch(); }
+            counts, totals); note_launch(); }
     }
     const int fin = passes & 1;
     const SortGeom gr = sort_geom(n, L.num_sms, 6, counters + kCntSortN);

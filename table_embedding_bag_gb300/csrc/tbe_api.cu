@@ -38,7 +38,7 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   for (int i = 0; i < 3; ++i) L.keys[i] = take(un * 4 + 64);
   for (int i = 0; i < 3; ++i) L.vals[i] = take(un * 4 + 64);
   for (int i = 0; i < 3; ++i) L.psw[i] = L.weighted ? take(un * 4 + 64) : 0;
-  L.radix_counts = take(sizeof(uint32_t) * (1u << kMaxRadixBits) * kMaxSortCtas);
+  L.radix_counts = take(sizeof(uint32_t) * (1u << kMaxRadixBits) * (kMaxSortCtas + 1));
   L.cta_counts = take(sizeof(uint32_t) * 2 * (kMaxSortCtas + 1));
   L.unique_keys = take((un + 1) * 4);
   L.run_starts = take((un + 2) * 4);
