@@ -49,6 +49,13 @@ constexpr unsigned kFull = 0xffffffffu;
 #define TBE_CHUNK_PAIRS 128
 #endif
 constexpr int kLongThreshold = TBE_CHUNK_PAIRS;
+// Runs of at least kMediumRun pairs (and fewer than kLongThreshold) are
+// updated by a whole warp each instead of sharing a warp with other runs.
+#ifndef TBE_MEDIUM_RUN
+#define TBE_MEDIUM_RUN 16
+#endif
+constexpr int kMediumRun = TBE_MEDIUM_RUN;
+static_assert(kMediumRun <= TBE_CHUNK_PAIRS, "medium runs lie below the long threshold");
 constexpr int kChunk = TBE_CHUNK_PAIRS;
 // Fan-in of the last-arriver reduction tree over a long run's chunk partials.
 constexpr int kFanIn = 32;
@@ -116,7 +123,8 @@ enum Counter : int {
   kCntTasks = 5,     // short-run warp tasks
   kCntPairs = 6,     // P: distinct (key, bag) pairs among the valid sorted lookups
   kCntSortN = 7,     // entries in the sort (written on the device before the sort)
-  kNumCounters = 8,
+  kCntMedium = 8,    // medium runs (kMediumRun <= pairs < kLongThreshold)
+  kNumCounters = 9,
 };
 
 struct WsLayout {
@@ -136,6 +144,7 @@ struct WsLayout {
   size_t run_pairs;    // uint32 [n + 2] first pair of each run
   size_t pair_starts;  // uint32 [n + 2] first sorted position of each (key, bag) pair
   size_t pair_bags;    // uint32 [n + 1] bag of each pair
+  size_t medium_run;   // uint32 [max_medium] medium runs (any order)
   size_t long_run;     // uint32 [max_long]
   size_t long_chunk0;  // uint32 [max_long] first chunk of each long run
   size_t long_tree0;   // uint32 [max_long] first tree node of each long run
@@ -175,7 +184,7 @@ struct WsLayout {
   size_t offsets_fix;  // index type [T*B+1] repaired offsets
   size_t fix_scratch;  // int64 [blocks] block maxima for the repair scan
   size_t total;
-  int64_t max_long, max_chunks, max_tree;
+  int64_t max_long, max_chunks, max_tree, max_medium;
   int64_t hot_tiles;   // expand CTAs: T * ceil(B / kHotTileBags)
   int hot_parts;       // bag partitions per table in the hot-gradient kernel
   bool hot_enabled;    // histogram fits the budget

@@ -815,10 +815,24 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(256)
     classify_kernel(const uint32_t* __restrict__ run_pairs, uint32_t* __restrict__ counters,
                     uint32_t* __restrict__ long_run, uint32_t* __restrict__ long_chunk0,
-                    uint32_t* __restrict__ long_tree0) {
+                    uint32_t* __restrict__ long_tree0, uint32_t* __restrict__ medium_run) {
   const uint32_t R = counters[kCntRuns];
-  for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < R; j += gridDim.x * blockDim.x) {
-    const uint32_t SL = run_pairs[j + 1] - run_pairs[j];
+  const uint32_t stride = gridDim.x * blockDim.x;
+  // whole warps iterate together (the medium list takes one atomic per warp)
+  const uint32_t R_up = (R + 31u) & ~31u;
+  for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < R_up; j += stride) {
+    const uint32_t SL = j < R ? run_pairs[j + 1] - run_pairs[j] : 0u;
+    const bool medium = SL >= static_cast<uint32_t>(kMediumRun) &&
+                        SL < static_cast<uint32_t>(kLongThreshold);
+    const unsigned mm = __ballot_sync(kFull, medium);
+    if (mm) {
+      const unsigned lane = lane_id();
+      const int leader = __ffs(mm) - 1;
+      uint32_t first = 0;
+      if (static_cast<int>(lane) == leader) first = atomicAdd(&counters[kCntMedium], __popc(mm));
+      first = __shfl_sync(kFull, first, leader);
+      if (medium) medium_run[first + __popc(mm & ((1u << lane) - 1u))] = j;
+    }
     if (SL >= static_cast<uint32_t>(kLongThreshold)) {
       const uint32_t nch = (SL + kChunk - 1) / kChunk;
       const uint32_t slot = atomicAdd(&counters[kCntLong], 1u);
@@ -1050,7 +1064,8 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     { classify_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         reinterpret_cast<uint32_t*>(ws + W.run_pairs), counters, reinterpret_cast<uint32_t*>(ws + W.long_run),
         reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
-        reinterpret_cast<uint32_t*>(ws + W.long_tree0)); note_launch(); }
+        reinterpret_cast<uint32_t*>(ws + W.long_tree0),
+        reinterpret_cast<uint32_t*>(ws + W.medium_run)); note_launch(); }
     int64_t fb = (W.max_long * 32 + 255) / 256;
     if (fb > 8LL * L.num_sms) fb = 8LL * L.num_sms;
     if (fb < 1) fb = 1;

@@ -48,6 +48,8 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   L.max_long = n / kLongThreshold + 1;
   L.max_chunks = n / kChunk + L.max_long + 1;
   L.max_tree = L.max_chunks / (kFanIn - 1) + 8 * L.max_long + 1;
+  L.max_medium = n / kMediumRun + 1;
+  L.medium_run = take(L.max_medium * 4);
   L.long_run = take(L.max_long * 4);
   L.long_chunk0 = take(L.max_long * 4);
   L.long_tree0 = take(L.max_long * 4);

@@ -250,8 +250,9 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, cons
   const int nv = D >> 2;
   const uint32_t p0 = st.p0;
   const uint32_t key = st.key;
-  // the chunked path owns runs of kLongThreshold pairs or more
-  const uint32_t np = st.np >= static_cast<uint32_t>(kLongThreshold) ? 0u : st.np;
+  // runs of kMediumRun pairs or more belong to medium_runs_kernel and the
+  // chunked path
+  const uint32_t np = st.np >= static_cast<uint32_t>(kMediumRun) ? 0u : st.np;
   const bool active = np > 0;
   __half* row = a.W + m.w_off[t] + (active ? (static_cast<int64_t>(key) - m.hb[t]) * D : 0);
   uint2 w_raw[NC];
@@ -289,6 +290,95 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, cons
 // lane); the other one skips them, so that its register budget stays small.
 // kWide: the instantiation for rows wider than 512 values (eight vectors per
 // lane); the other one skips them, so that its register budget stays small.
+// One medium run with the whole warp.  The row's nv float4 vectors take R
+// lanes (lane l holds vectors l % R + c R, c < NC), the warp's G = 32 / R lane
+// groups take the run's pairs in turn (group g: pairs g, g + G, ...) with
+// U = 8 / NC rows in flight per lane, and a butterfly adds the groups' sums
+// (each group sums its pairs in order; the groups are combined in a fixed
+// pattern).  A run of many pairs costs one round trip per G U pairs.
+template <int R, int NC, bool kWeighted>
+__device__ __forceinline__ void warp_run(const UpdArgs& a, const Meta& m, int t, uint32_t p0,
+                                         uint32_t np, uint32_t key) {
+  constexpr int G = 32 / R;
+  constexpr int U = NC < 8 ? 8 / NC : 1;
+  const int lane = static_cast<int>(lane_id());
+  const int g = lane / R;
+  const int64_t d0 = m.d_off[t];
+  const int D = static_cast<int>(m.d_off[t + 1] - d0);
+  const int nv = D >> 2;
+  __half* row = a.W + m.w_off[t] + (static_cast<int64_t>(key) - m.hb[t]) * D;
+  uint2 w_raw[NC];
+  load_row<R, NC>(row, nv, w_raw, true);
+  const float m_old = a.momentum[key];
+  float acc[NC][4];
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[c][i] = 0.f;
+  for (uint32_t base = 0; base < np; base += 32) {
+    uint32_t my_b = 0xffffffffu;
+    float my_w = 0.f;
+    if (base + lane < np) load_pair<kWeighted>(a, p0 + base + lane, &my_b, &my_w);
+    const uint32_t cnt = np - base < 32u ? np - base : 32u;
+#pragma unroll
+    for (int u0 = 0; u0 < R; u0 += U) {
+      if (static_cast<uint32_t>(u0 * G) >= cnt) break;  // warp-uniform
+      float4 v[U][NC];
+      float wv[U];
+#pragma unroll
+      for (int uu = 0; uu < U; ++uu) {
+        const int k = (u0 + uu) * G + g;  // this group's pair within the batch
+        const uint32_t b = __shfl_sync(kFull, my_b, k & 31);
+        const float w = __shfl_sync(kFull, my_w, k & 31);
+        const bool ok = k < 32 && b < static_cast<uint32_t>(a.B);
+        wv[uu] = ok ? w : 0.f;
+        gather_row<R, NC>(a, d0, nv, b, v[uu], ok);
+      }
+#pragma unroll
+      for (int uu = 0; uu < U; ++uu) fma_rows<NC>(acc, v[uu], wv[uu]);
+    }
+  }
+#pragma unroll
+  for (int off = R; off < 32; off <<= 1)
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[c][i] += __shfl_xor_sync(kFull, acc[c][i], off);
+  adagrad_apply<R, NC>(a, acc, D, key, row, w_raw, m_old, g == 0);
+}
+
+// Medium runs (kMediumRun <= pairs < kLongThreshold, listed by the
+// preprocess): one warp per run.
+template <bool kWeighted>
+__global__ void __launch_bounds__(256, 2) medium_runs_kernel(UpdArgs a, const uint32_t* __restrict__ medium_run) {
+  __shared__ MetaSmem msm;
+  const Meta m = load_meta(a, msm, true);
+  const uint32_t nmed = a.counters[kCntMedium];
+  const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
+  for (uint32_t i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < nmed; i += warps) {
+    const uint32_t j = __ldg(medium_run + i);
+    const uint32_t key = __ldg(a.unique_keys + j);
+    const uint32_t p0 = __ldg(a.run_pairs + j);
+    const uint32_t np = __ldg(a.run_pairs + j + 1) - p0;
+    int lo = 0, hi = a.T - 1;  // table of the key
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (m.hb[mid] <= static_cast<int64_t>(key)) lo = mid; else hi = mid - 1;
+    }
+    const int t = lo;
+    const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
+    if (D < 8 || D > kMaxD || (D & 7)) continue;  // widths the vector path cannot move
+    const int nv = D >> 2;
+    if (nv <= 4) warp_run<4, 1, kWeighted>(a, m, t, p0, np, key);
+    else if (nv <= 8) warp_run<8, 1, kWeighted>(a, m, t, p0, np, key);
+    else if (nv <= 16) warp_run<16, 1, kWeighted>(a, m, t, p0, np, key);
+    else if (nv <= 32) warp_run<32, 1, kWeighted>(a, m, t, p0, np, key);
+    else if (nv <= 64) warp_run<32, 2, kWeighted>(a, m, t, p0, np, key);
+    else if (nv <= 128) warp_run<32, 4, kWeighted>(a, m, t, p0, np, key);
+    else warp_run<32, 8, kWeighted>(a, m, t, p0, np, key);
+  }
+}
+
 template <bool kWeighted, bool kWide>
 __global__ void __launch_bounds__(256, TBE_SHORT_MINB) short_runs_kernel(UpdArgs a) {
   __shared__ MetaSmem msm;
@@ -839,6 +929,9 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   const bool wide = d->max_D > 512;  // rows of more than 128 float4 vectors
   if (weighted) { short_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
   else { short_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
+  const uint32_t* medium = reinterpret_cast<const uint32_t*>(ws + W.medium_run);
+  if (weighted) { medium_runs_kernel<true><<<blocks, 256, 0, L.s>>>(a, medium); note_launch(); }
+  else { medium_runs_kernel<false><<<blocks, 256, 0, L.s>>>(a, medium); note_launch(); }
   if (wide && weighted) { short_runs_kernel<true, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
   if (wide && !weighted) { short_runs_kernel<false, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
   if (weighted) { long_chunks_kernel<true, false><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); }
