@@ -138,7 +138,8 @@ __global__ void __launch_bounds__(256)
                         const int64_t* __restrict__ D_offsets, int64_t n, int B, HotSet hs,
                         float* __restrict__ hot_hist, int8_t* __restrict__ hot_scale,
                         uint32_t* __restrict__ hot_cnt, uint32_t* __restrict__ bag_cold,
-                        uint32_t* __restrict__ tile_cold, int* status) {
+                        uint32_t* __restrict__ tile_cold, uint32_t* __restrict__ sp_keys,
+                        uint32_t* __restrict__ sp_vals, float* __restrict__ sp_psw, int* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   ExpandSmem<IndexT, kWeighted>& sm = *reinterpret_cast<ExpandSmem<IndexT, kWeighted>*>(smem_raw);
   const TileInfo ti = tile_info(B);
@@ -161,11 +162,12 @@ __global__ void __launch_bounds__(256)
   for (int j = 0; j < kPerLane; ++j) cnt[j] = 0;
   bool bad = false;
   uint32_t cold_w = 0;
+  const unsigned lt = (1u << lane) - 1u;
   for (int lb = warp; lb < ti.nbags; lb += 8) {
     const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
     int64_t s, e;
     bag_range(offsets, bag, n, &s, &e);
-    uint32_t cold = 0;
+    uint32_t cold = 0;  // this bag's cold lookups so far (the same in every lane)
     for (int64_t base = s; base < e; base += 32 * kExpandLoads) {
       int64_t r[kExpandLoads];
 #pragma unroll
@@ -179,9 +181,19 @@ __global__ void __launch_bounds__(256)
         const bool inside = r[u] != -2;
         const bool ok = inside && r[u] >= 0 && r[u] < E;
         bad |= inside && !ok;
-        const int slot =
-            ok && nh ? hot_lookup(sm.hash, m1, m2, static_cast<uint32_t>(h0 + r[u])) : -1;
-        cold += ok && slot < 0;
+        const uint32_t key = static_cast<uint32_t>(h0 + r[u]);
+        const int slot = ok && nh ? hot_lookup(sm.hash, m1, m2, key) : -1;
+        // cold lookups go, in lookup order, to the front of the bag's own
+        // range [s, e) of the sparse list
+        const bool is_cold = ok && slot < 0;
+        const unsigned cm = __ballot_sync(kFull, is_cold);
+        if (is_cold) {
+          const int64_t at = s + cold + __popc(cm & lt);
+          sp_keys[at] = key;
+          sp_vals[at] = static_cast<uint32_t>(ti.b0 + lb);
+          if (kWeighted) sp_psw[at] = __ldg(psw + base + u * 32 + lane);
+        }
+        cold += __popc(cm);
         if constexpr (kWeighted) {
           // double sums of fp32 weights are exact: atomic order does not matter
           if (slot >= 0) {
@@ -196,8 +208,6 @@ __global__ void __launch_bounds__(256)
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cold += __shfl_xor_sync(kFull, cold, o);
     if (lane == 0) bag_cold[bag] = cold;
     cold_w += cold;
     if (nh_pad) {
@@ -248,16 +258,19 @@ __global__ void __launch_bounds__(256)
   if (status && __any_sync(kFull, bad) && lane == 0) set_status(status, TBE_ERR_INDEX_RANGE);
 }
 
+// Compaction of the cold lookups: each bag's cold entries, which the count
+// kernel left at the front of the bag's own range of the sparse list, move to
+// the dense list at the bag's first cold entry (tile base + in-tile prefix of
+// the per-bag counts), keeping lookup order; cold_off gets each bag's first
+// entry.  Only the cold entries are read, not the indices.
 template <typename IndexT, bool kWeighted>
 __global__ void __launch_bounds__(256)
-    expand_write_kernel(const IndexT* __restrict__ indices, const IndexT* __restrict__ offsets,
-                        const float* __restrict__ psw, const int64_t* __restrict__ hash_base,
-                        const int64_t* __restrict__ D_offsets, int64_t n, int B, HotSet hs,
-                        bool hot_enabled, const uint32_t* __restrict__ bag_cold,
+    expand_write_kernel(const IndexT* __restrict__ offsets, int64_t n, int B,
+                        const uint32_t* __restrict__ bag_cold,
                         const uint32_t* __restrict__ tile_base, uint32_t* __restrict__ cold_off,
-                        uint32_t* __restrict__ keys, uint32_t* __restrict__ vals,
-                        float* __restrict__ psw_out) {
-  __shared__ HotHash hash;
+                        const uint32_t* __restrict__ sp_keys, const uint32_t* __restrict__ sp_vals,
+                        const float* __restrict__ sp_psw, uint32_t* __restrict__ keys,
+                        uint32_t* __restrict__ vals, float* __restrict__ psw_out) {
   __shared__ uint32_t bag_base[kHotTileBags];
   __shared__ uint32_t scan[33];
   const TileInfo ti = tile_info(B);
@@ -265,7 +278,7 @@ __global__ void __launch_bounds__(256)
   const unsigned lane = lane_id();
   {
     // exclusive prefix of the tile's per-bag cold counts = the bags' first
-    // entries in the cold list
+    // entries in the dense list
     const int lb = threadIdx.x;
     const uint32_t c =
         lb < ti.nbags ? bag_cold[static_cast<int64_t>(ti.t) * B + ti.b0 + lb] : 0u;
@@ -277,41 +290,17 @@ __global__ void __launch_bounds__(256)
     if (lb == 0 && blockIdx.x == gridDim.x - 1)
       cold_off[static_cast<int64_t>(ti.t) * B + ti.b0 + ti.nbags] = tile_base[blockIdx.x] + total;
   }
-  const int64_t h0 = __ldg(hash_base + ti.t);
-  const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
-  uint32_t m1, m2;
-  const int nh = build_hot_hash(hash, &m1, &m2, hs, D_offsets, h0, E, ti.t, hot_enabled);
-  const unsigned lt = (1u << lane) - 1u;
+  __syncthreads();
   for (int lb = warp; lb < ti.nbags; lb += 8) {
     const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
     int64_t s, e;
     bag_range(offsets, bag, n, &s, &e);
-    uint32_t pos = bag_base[lb];
-    for (int64_t base = s; base < e; base += 32 * kExpandLoads) {
-      int64_t r[kExpandLoads];
-#pragma unroll
-      for (int u = 0; u < kExpandLoads; ++u) {
-        const int64_t i = base + u * 32 + lane;
-        r[u] = i < e ? load_index(indices, i) : -1;
-      }
-#pragma unroll
-      for (int u = 0; u < kExpandLoads; ++u) {
-        if (base + u * 32 >= e) break;  // warp-uniform
-        bool cold = false;
-        uint32_t key = 0;
-        if (r[u] >= 0 && r[u] < E) {
-          key = static_cast<uint32_t>(h0 + r[u]);
-          cold = !nh || hot_lookup(hash, m1, m2, key) < 0;
-        }
-        const unsigned m = __ballot_sync(kFull, cold);
-        if (cold) {
-          const uint32_t p = pos + __popc(m & lt);
-          keys[p] = key;
-          vals[p] = static_cast<uint32_t>(ti.b0 + lb);
-          if (kWeighted) psw_out[p] = __ldg(psw + base + u * 32 + lane);
-        }
-        pos += __popc(m);
-      }
+    const uint32_t c = bag_cold[bag];
+    const uint32_t pos = bag_base[lb];
+    for (uint32_t i = lane; i < c; i += 32) {
+      keys[pos + i] = __ldg(sp_keys + s + i);
+      vals[pos + i] = __ldg(sp_vals + s + i);
+      if (kWeighted) psw_out[pos + i] = __ldg(sp_psw + s + i);
     }
   }
 }
@@ -998,23 +987,26 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     uint32_t* bc = reinterpret_cast<uint32_t*>(ws + W.bag_cold);
     uint32_t* co = reinterpret_cast<uint32_t*>(ws + W.cold_off);
     const unsigned tiles = static_cast<unsigned>(W.hot_tiles);
+    // the cold lookups go first to buffer 0 at their bags' own positions,
+    // then, compacted, to buffer 2 (the sort reads buffer 2 before it
+    // writes buffer 0)
     if (weighted)
       { expand_count_kernel<IndexT, true><<<tiles, 256, sizeof(ExpandSmem<IndexT, true>), s>>>(
           indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh, hsc, hc, bc,
-          tile_cold, status); note_launch(); }
+          tile_cold, keys[0], vals[0], pw[0], status); note_launch(); }
     else
       { expand_count_kernel<IndexT, false><<<tiles, 256, sizeof(ExpandSmem<IndexT, false>), s>>>(
           indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh, hsc, hc, bc,
-          tile_cold, status); note_launch(); }
+          tile_cold, keys[0], vals[0], pw[0], status); note_launch(); }
     { exclusive_scan_kernel<<<1, 1024, 0, s>>>(tile_cold, W.hot_tiles, counters + kCntSortN); note_launch(); }
     if (weighted)
       { expand_write_kernel<IndexT, true><<<tiles, 256, 0, s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, W.hot_enabled, bc,
-          tile_cold, co, keys[2], vals[2], pw[2]); note_launch(); }
+          offsets, n, d->B, bc, tile_cold, co, keys[0], vals[0], pw[0], keys[2], vals[2],
+          pw[2]); note_launch(); }
     else
       { expand_write_kernel<IndexT, false><<<tiles, 256, 0, s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, W.hot_enabled, bc,
-          tile_cold, co, keys[2], vals[2], pw[2]); note_launch(); }
+          offsets, n, d->B, bc, tile_cold, co, keys[0], vals[0], pw[0], keys[2], vals[2],
+          pw[2]); note_launch(); }
   }
   if (n > 0) {
     const SortGeom g = sort_geom(n, L.num_sms, 2, counters + kCntSortN);
