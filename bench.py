@@ -133,7 +133,12 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-ROOFLINE_KERNEL_SOURCES = ("forward_hot.cu", "pool.cuh", "tcgen05.cuh", "common.cuh")
+# The step's dominant kernel (largest share of the ncu launch list of this
+# workload, profiles/launches_hot_row_step.md): the long-run chunk kernel of
+# the backward.  Its launches are timed live by the library's kernel probe.
+ROOFLINE_KERNEL = "long_chunks_kernel (tbe_backward_rowwise_adagrad, long runs)"
+ROOFLINE_KERNEL_SOURCES = ("update.cu", "common.cuh")
+ROOFLINE_PROFILE = "long_chunks_hot_row.md"
 
 
 def source_sha1():
@@ -146,10 +151,10 @@ def source_sha1():
 
 
 def profiled_traffic():
-    """DRAM bytes of one forward_hot_kernel launch on this workload, from the
-    committed ncu summary, if the kernel's sources are unchanged since the
-    capture (else None)."""
-    path = os.path.join(ROOT, "profiles", "forward_hot_hot_row.md")
+    """DRAM bytes of one launch of the roofline kernel on this workload, from
+    the committed ncu summary, if the kernel's sources are unchanged since
+    the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", ROOFLINE_PROFILE)
     try:
         text = open(path).read()
         digest = source_sha1()
@@ -162,25 +167,23 @@ def profiled_traffic():
     return int(fields["traffic_bytes_per_launch"])
 
 
-def algorithmic_bytes(w, R, n_cold, n_hot):
-    """Byte models of the forward (see the design notes).
+def long_chunk_bytes(D, long_pairs, chunks, long_runs):
+    """Algorithmic bytes of one long_chunks_kernel launch, counted per use (the
+    per-unit figures of the design notes): per long pair its gradient row
+    (4 D) and pair data (8); per chunk its partial written and read back
+    (2 x 4 D) and its descriptor (16); per long run the weights row read and
+    written (2 x 2 D), the momentum (8) and the run record (32)."""
+    return (long_pairs * (4 * D + 8) + chunks * (2 * 4 * D + 16)
+            + long_runs * (2 * 2 * D + 8 + 32))
 
-    `kernel`: what forward_hot_kernel must move once: the histogram columns of
-    the n_hot hot rows (4 B per bag each), the cold lists (4 B per cold
-    lookup, 4 B per bag of counts), every distinct row it touches once (R cold
-    rows + n_hot hot rows, 2 D bytes) and the pooled output.
-    `problem_min`: the forward problem's compulsory bytes (indices, offsets,
-    distinct rows once, output), whatever the implementation.
-    `per_use`: every lookup's row read as its own transfer."""
-    n = w.n
+
+def forward_problem_bytes(w, rows_touched):
+    """Compulsory bytes of the forward problem: indices, offsets, every
+    distinct row once, the pooled output."""
     nb = w.T * w.B
     D = int(w.D[0])
-    out = w.B * int(w.D.sum()) * 4
-    tiles = w.T * ((w.B + 127) // 128)
-    kernel = n_hot * w.B * 4 + n_cold * 4 + nb * 4 + tiles * 4 + (R + n_hot) * D * 2 + out
-    problem_min = n * INDEX_BYTES + (nb + 1) * INDEX_BYTES + (R + n_hot) * D * 2 + out
-    per_use = n * (INDEX_BYTES + D * 2) + (nb + 1) * INDEX_BYTES + out
-    return {"kernel": kernel, "problem_min": problem_min, "per_use": per_use}
+    return (w.n * INDEX_BYTES + (nb + 1) * INDEX_BYTES + rows_touched * D * 2
+            + w.B * int(w.D.sum()) * 4)
 
 
 def run_native(args, world, rank, local):
@@ -222,12 +225,15 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    tbe.tbe_probe_set(tbe.TBE_PROBE_LONG_CHUNKS)
     launches0 = tbe.tbe_kernel_launches()
     t0.record(stream)
     for k in range(args.steps):
         step(evs[k])
     t1.record(stream)
     launches = tbe.tbe_kernel_launches() - launches0
+    probe_launches, probe_ms = tbe.tbe_probe_read()
+    tbe.tbe_probe_set(tbe.TBE_PROBE_OFF)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
@@ -250,11 +256,21 @@ def run_native(args, world, rank, local):
     # so it is also the set the timed steps used)
     hoff = view["hot_n"] - ws.buf.data_ptr()
     n_hot = int(ws.buf[hoff:hoff + 4 * w.T].view(torch.int32).cpu().numpy().sum())
+
+    def ws_u32(ptr, count):
+        o = ptr - ws.buf.data_ptr()
+        return ws.buf[o:o + 4 * count].view(torch.int32).cpu().numpy().view(np.uint32)
+
+    # pairs of the long runs (the units of the long-run kernel)
+    run_pairs = ws_u32(view["run_pairs"], R + 1).astype(np.int64)
+    long_idx = ws_u32(view["long_runs"], n_long).astype(np.int64)
+    long_pairs = int((run_pairs[long_idx + 1] - run_pairs[long_idx]).sum()) if n_long else 0
     result = {
         "ms": ms, "ms_local": ms_local, "fwd_ms": statistics.median(fwd),
         "pre_ms": statistics.median(pre), "upd_ms": statistics.median(upd),
         "n": w.n, "R": R, "n_long": n_long, "n_chunks": n_chunks, "n_cold": n_cold,
-        "n_hot": n_hot, "clocks": clk,
+        "n_hot": n_hot, "long_pairs": long_pairs, "clocks": clk,
+        "probe_launches": probe_launches, "probe_ms": probe_ms,
         "launches": launches, "w": w,
     }
 
@@ -376,9 +392,11 @@ def main():
         pass
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    ab = algorithmic_bytes(w, r["R"], r["n_cold"], r["n_hot"])
-    fwd_s = r["fwd_ms"] / 1e3
-    achieved = ab["kernel"] / fwd_s / 1e9
+    D = int(w.D[0])
+    kb = long_chunk_bytes(D, r["long_pairs"], r["n_chunks"], r["n_long"])
+    k_launch_ms = r["probe_ms"] / max(r["probe_launches"], 1)
+    achieved = kb / (k_launch_ms / 1e3) / 1e9
+    fwd_problem = forward_problem_bytes(w, r["R"] + r["n_hot"])
     line = {
         "metric": METRIC, "value": value, "unit": "lookups/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
@@ -394,16 +412,19 @@ def main():
         "phases_ms": {"forward": r["fwd_ms"], "preprocess": r["pre_ms"], "update": r["upd_ms"]},
         "runs": {"R": r["R"], "long_runs": r["n_long"], "long_chunks": r["n_chunks"],
                  "cold_lookups": r["n_cold"], "hot_rows": r["n_hot"]},
-        "roofline": {"kernel": "forward_hot_kernel (tbe_forward, TBE_F_PREPROCESSED)",
-                     "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm,
+        "roofline": {"kernel": ROOFLINE_KERNEL, "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": profiled_traffic() if args.tables is None else None,
                      "peak_source": peak_src,
-                     "bytes_model": "hot histogram columns + cold lists + distinct rows once "
-                                    "+ output",
-                     "bytes_per_launch": ab["kernel"],
-                     "problem_min_GBps": ab["problem_min"] / fwd_s / 1e9,
-                     "per_use_GBps": ab["per_use"] / fwd_s / 1e9},
+                     "bytes_model": "per use: gradient row + pair data per long pair, "
+                                    "partial write+read per chunk, weights row r/w + "
+                                    "momentum per long run",
+                     "bytes_per_launch": kb, "launch_ms": k_launch_ms,
+                     "launches_timed": r["probe_launches"],
+                     "units": {"long_pairs": r["long_pairs"], "chunks": r["n_chunks"],
+                               "long_runs": r["n_long"]}},
+        "forward_context": {"phase_ms": r["fwd_ms"],
+                            "problem_min_GBps": fwd_problem / (r["fwd_ms"] / 1e3) / 1e9},
         "clocks": r["clocks"],
         "gpu_launches": r["launches"],
     }

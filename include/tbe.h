@@ -273,6 +273,30 @@ const char* tbe_version(void);
  * made between them. */
 uint64_t tbe_kernel_launches(void);
 
+/* Kernel probe, a measurement aid with no counterpart in the method: times
+ * every launch of one of the library's kernels with a pair of CUDA events
+ * recorded on the launch's stream around it.
+ * tbe_probe_set(kernel) selects the kernel (one of TBE_PROBE_*, or
+ * TBE_PROBE_OFF) and clears the record; up to 256 launches are recorded
+ * after that, later ones are not.  The events are created by the library
+ * on the current device.  tbe_probe_read waits for the recorded events and
+ * returns the number of recorded launches and their summed duration in
+ * milliseconds.  Both are host calls for use outside timed work; probing
+ * adds two event records per probed launch and nothing else.
+ * Errors: TBE_EINVAL (unknown kernel, NULL pointers), TBE_ECUDA. */
+#define TBE_PROBE_OFF 0u
+#define TBE_PROBE_EXPAND_COUNT 1u
+#define TBE_PROBE_RADIX_DOWNSWEEP 2u
+#define TBE_PROBE_FORWARD_HOT 3u
+#define TBE_PROBE_FORWARD_COLD 4u
+#define TBE_PROBE_SHORT_RUNS 5u
+#define TBE_PROBE_MEDIUM_RUNS 6u
+#define TBE_PROBE_LONG_CHUNKS 7u
+#define TBE_PROBE_HOT_GRAD 8u
+#define TBE_PROBE_LAST 8u
+tbe_status tbe_probe_set(uint32_t kernel);
+tbe_status tbe_probe_read(uint32_t* launches, float* total_ms);
+
 #ifdef __cplusplus
 }
 #endif

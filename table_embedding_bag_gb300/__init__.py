@@ -19,7 +19,8 @@ from . import _build
 __all__ = [
     "build", "TBEDesc", "Workspace", "TBEError", "tbe_workspace_size", "tbe_forward",
     "tbe_preprocess", "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status",
-    "tbe_version", "tbe_kernel_launches", "TableBatchedEmbedding", "lib_path", "tbe_backward_rowwise_adagrad_noalloc",
+    "tbe_version", "tbe_kernel_launches", "tbe_probe_set", "tbe_probe_read",
+    "TableBatchedEmbedding", "lib_path", "tbe_backward_rowwise_adagrad_noalloc",
     "TBE_NOALLOC_SCRATCH_BYTES", "TBE_ETOO_LARGE",
     "TBE_F_CHECK_BOUNDS", "TBE_F_REPAIR_OFFSETS", "TBE_F_FORCE_GENERIC", "TBE_F_LONG_TWO_LAUNCH",
     "TBE_F_PREPROCESSED", "TBE_WS_WEIGHTED", "TBE_ERR_INDEX_RANGE", "TBE_ERR_OFFSETS",
@@ -37,6 +38,16 @@ TBE_WS_WEIGHTED = 1 << 0
 TBE_ERR_INDEX_RANGE = 1 << 0
 TBE_ERR_OFFSETS = 1 << 1
 TBE_ERR_TIMEOUT = 1 << 2
+# kernels tbe_probe_set can time
+TBE_PROBE_OFF = 0
+TBE_PROBE_EXPAND_COUNT = 1
+TBE_PROBE_RADIX_DOWNSWEEP = 2
+TBE_PROBE_FORWARD_HOT = 3
+TBE_PROBE_FORWARD_COLD = 4
+TBE_PROBE_SHORT_RUNS = 5
+TBE_PROBE_MEDIUM_RUNS = 6
+TBE_PROBE_LONG_CHUNKS = 7
+TBE_PROBE_HOT_GRAD = 8
 _STATUS_NAMES = {1: "TBE_EINVAL", 2: "TBE_EWORKSPACE", 3: "TBE_EUNSUPPORTED", 4: "TBE_ECUDA",
                  5: "TBE_ETOO_LARGE"}
 
@@ -94,9 +105,12 @@ def _load():
         lib.tbe_version.restype = ctypes.c_char_p
         lib.tbe_kernel_launches.restype = ctypes.c_uint64
         lib.tbe_kernel_launches.argtypes = []
+        lib.tbe_probe_set.argtypes = [u32]
+        lib.tbe_probe_read.argtypes = [ctypes.POINTER(ctypes.c_uint32),
+                                       ctypes.POINTER(ctypes.c_float)]
         for f in ("tbe_workspace_size", "tbe_forward", "tbe_preprocess",
                   "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status",
-                  "tbe_backward_rowwise_adagrad_noalloc"):
+                  "tbe_backward_rowwise_adagrad_noalloc", "tbe_probe_set", "tbe_probe_read"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -246,6 +260,19 @@ def tbe_version() -> str:
 def tbe_kernel_launches() -> int:
     """Kernels the library has launched in this process so far."""
     return int(_load().tbe_kernel_launches())
+
+
+def tbe_probe_set(kernel: int) -> None:
+    """Time every following launch of one kernel (TBE_PROBE_*) with CUDA events."""
+    _ok("tbe_probe_set", _load().tbe_probe_set(kernel))
+
+
+def tbe_probe_read():
+    """(launches, total milliseconds) recorded since tbe_probe_set; waits for the events."""
+    n = ctypes.c_uint32(0)
+    ms = ctypes.c_float(0.0)
+    _ok("tbe_probe_read", _load().tbe_probe_read(ctypes.byref(n), ctypes.byref(ms)))
+    return int(n.value), float(ms.value)
 
 
 class TableBatchedEmbedding:

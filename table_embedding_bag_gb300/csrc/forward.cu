@@ -324,13 +324,13 @@ cudaError_t launch_cold_s(const Launch& L, const __half* W, const uint32_t* keys
   if (blocks > (1 << 22)) blocks = 1 << 22;
   if (blocks < 1) blocks = 1;
   if (psw)
-    { forward_cold_kernel<S, true><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
+    { probe_begin(TBE_PROBE_FORWARD_COLD, L.s); forward_cold_kernel<S, true><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
         W, d->D_offsets, d->hash_base, d->weights_offsets, keys, cold_off, psw, d->T, d->B,
-        d->total_D, out, hot_n); note_launch(); }
+        d->total_D, out, hot_n); note_launch(); probe_end(TBE_PROBE_FORWARD_COLD, L.s); }
   else
-    { forward_cold_kernel<S, false><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
+    { probe_begin(TBE_PROBE_FORWARD_COLD, L.s); forward_cold_kernel<S, false><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
         W, d->D_offsets, d->hash_base, d->weights_offsets, keys, cold_off, psw, d->T, d->B,
-        d->total_D, out, hot_n); note_launch(); }
+        d->total_D, out, hot_n); note_launch(); probe_end(TBE_PROBE_FORWARD_COLD, L.s); }
   return cudaGetLastError();
 }
 

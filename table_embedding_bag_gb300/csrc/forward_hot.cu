@@ -335,7 +335,7 @@ cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, con
     int64_t grid = static_cast<int64_t>(per_sm) * L.num_sms;
     if (grid > tiles) grid = tiles;
     if (grid < 1) grid = 1;
-    { forward_hot_kernel<<<static_cast<unsigned>(grid), kFThreads, smem, L.s>>>(a, tmem_cols); note_launch(); }
+    { probe_begin(TBE_PROBE_FORWARD_HOT, L.s); forward_hot_kernel<<<static_cast<unsigned>(grid), kFThreads, smem, L.s>>>(a, tmem_cols); note_launch(); probe_end(TBE_PROBE_FORWARD_HOT, L.s); }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -299,7 +299,7 @@ cudaError_t launch_hot_grad(const Launch& L, const WsLayout& W, char* ws, const 
   a.parts = W.hot_parts;
   a.max_mtiles = max_mtiles;
   const unsigned grid = static_cast<unsigned>(L.d->T) * static_cast<unsigned>(W.hot_parts);
-  { hot_grad_tc_kernel<<<grid, kGThreads, smem, L.s>>>(a); note_launch(); }
+  { probe_begin(TBE_PROBE_HOT_GRAD, L.s); hot_grad_tc_kernel<<<grid, kGThreads, smem, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_HOT_GRAD, L.s); }
   return cudaGetLastError();
 }
 

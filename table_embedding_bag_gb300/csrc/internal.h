@@ -14,6 +14,10 @@ struct WsLayout;
 // Counts one kernel launch (read back by tbe_kernel_launches).
 void note_launch();
 
+// Kernel probe (tbe_probe_set): events around launches of the selected kernel.
+void probe_begin(uint32_t kernel, cudaStream_t s);
+void probe_end(uint32_t kernel, cudaStream_t s);
+
 // One call's launch context.
 struct Launch {
   const tbe_desc* d;

@@ -991,13 +991,13 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     // then, compacted, to buffer 2 (the sort reads buffer 2 before it
     // writes buffer 0)
     if (weighted)
-      { expand_count_kernel<IndexT, true><<<tiles, 256, sizeof(ExpandSmem<IndexT, true>), s>>>(
+      { probe_begin(TBE_PROBE_EXPAND_COUNT, s); expand_count_kernel<IndexT, true><<<tiles, 256, sizeof(ExpandSmem<IndexT, true>), s>>>(
           indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh, hsc, hc, bc,
-          tile_cold, keys[0], vals[0], pw[0], status); note_launch(); }
+          tile_cold, keys[0], vals[0], pw[0], status); note_launch(); probe_end(TBE_PROBE_EXPAND_COUNT, s); }
     else
-      { expand_count_kernel<IndexT, false><<<tiles, 256, sizeof(ExpandSmem<IndexT, false>), s>>>(
+      { probe_begin(TBE_PROBE_EXPAND_COUNT, s); expand_count_kernel<IndexT, false><<<tiles, 256, sizeof(ExpandSmem<IndexT, false>), s>>>(
           indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh, hsc, hc, bc,
-          tile_cold, keys[0], vals[0], pw[0], status); note_launch(); }
+          tile_cold, keys[0], vals[0], pw[0], status); note_launch(); probe_end(TBE_PROBE_EXPAND_COUNT, s); }
     { exclusive_scan_kernel<<<1, 1024, 0, s>>>(tile_cold, W.hot_tiles, counters + kCntSortN); note_launch(); }
     if (weighted)
       { expand_write_kernel<IndexT, true><<<tiles, 256, 0, s>>>(
@@ -1025,13 +1025,13 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
       { radix_upsweep_kernel<<<g.ctas, kSortThreads, 0, s>>>(keys[src], g, shift, width, counts); note_launch(); }
       { radix_scan_kernel<<<((1 << width) + 7) / 8, 256, 0, s>>>(counts, g.ctas, 1 << width, totals); note_launch(); }
       if (weighted)
-        { radix_downsweep_kernel<true><<<g.ctas, kSortThreads, smem, s>>>(
+        { probe_begin(TBE_PROBE_RADIX_DOWNSWEEP, s); radix_downsweep_kernel<true><<<g.ctas, kSortThreads, smem, s>>>(
             keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], g, shift, width,
-            counts, totals); note_launch(); }
+            counts, totals); note_launch(); probe_end(TBE_PROBE_RADIX_DOWNSWEEP, s); }
       else
-        { radix_downsweep_kernel<false><<<g.ctas, kSortThreads, smem, s>>>(
+        { probe_begin(TBE_PROBE_RADIX_DOWNSWEEP, s); radix_downsweep_kernel<false><<<g.ctas, kSortThreads, smem, s>>>(
             keys[src], vals[src], pw[src], keys[dst], vals[dst], pw[dst], g, shift, width,
-            counts, totals); note_launch(); }
+            counts, totals); note_launch(); probe_end(TBE_PROBE_RADIX_DOWNSWEEP, s); }
     }
     const int fin = passes & 1;
     const SortGeom gr = sort_geom(n, L.num_sms, 6, counters + kCntSortN);

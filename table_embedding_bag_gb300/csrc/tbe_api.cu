@@ -12,6 +12,33 @@ std::atomic<uint64_t> g_kernel_launches{0};
 
 void note_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 
+namespace {
+constexpr int kProbeMax = 256;
+std::mutex g_probe_mu;
+std::atomic<uint32_t> g_probe_kernel{0};
+cudaEvent_t g_probe_ev[kProbeMax][2] = {};
+int g_probe_used = 0;   // launches recorded
+bool g_probe_open = false;
+}  // namespace
+
+void probe_begin(uint32_t kernel, cudaStream_t s) {
+  if (g_probe_kernel.load(std::memory_order_relaxed) != kernel || kernel == 0) return;
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  if (g_probe_used >= kProbeMax || g_probe_open) return;
+  cudaEvent_t* ev = g_probe_ev[g_probe_used];
+  if (!ev[0] && cudaEventCreate(&ev[0]) != cudaSuccess) return;
+  if (!ev[1] && cudaEventCreate(&ev[1]) != cudaSuccess) return;
+  if (cudaEventRecord(ev[0], s) == cudaSuccess) g_probe_open = true;
+}
+
+void probe_end(uint32_t kernel, cudaStream_t s) {
+  if (g_probe_kernel.load(std::memory_order_relaxed) != kernel || kernel == 0) return;
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  if (!g_probe_open) return;
+  g_probe_open = false;
+  if (cudaEventRecord(g_probe_ev[g_probe_used][1], s) == cudaSuccess) ++g_probe_used;
+}
+
 cudaError_t prepare_preprocess_kernels();
 
 WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
@@ -289,6 +316,32 @@ tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits) 
 }
 
 const char* tbe_version(void) { return "tbe-gb300 0.1 (sm_103a)"; }
+
+tbe_status tbe_probe_set(uint32_t kernel) {
+  if (kernel > TBE_PROBE_LAST) return TBE_EINVAL;
+  std::lock_guard<std::mutex> lk(tbe::g_probe_mu);
+  // events are kept for reuse; a new selection clears the record
+  tbe::g_probe_used = 0;
+  tbe::g_probe_open = false;
+  tbe::g_probe_kernel.store(kernel, std::memory_order_relaxed);
+  return TBE_OK;
+}
+
+tbe_status tbe_probe_read(uint32_t* launches, float* total_ms) {
+  if (!launches || !total_ms) return TBE_EINVAL;
+  std::lock_guard<std::mutex> lk(tbe::g_probe_mu);
+  float sum = 0.f;
+  for (int i = 0; i < tbe::g_probe_used; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(tbe::g_probe_ev[i][1]) != cudaSuccess) return TBE_ECUDA;
+    if (cudaEventElapsedTime(&ms, tbe::g_probe_ev[i][0], tbe::g_probe_ev[i][1]) != cudaSuccess)
+      return TBE_ECUDA;
+    sum += ms;
+  }
+  *launches = static_cast<uint32_t>(tbe::g_probe_used);
+  *total_ms = sum;
+  return TBE_OK;
+}
 
 uint64_t tbe_kernel_launches(void) {
   return tbe::g_kernel_launches.load(std::memory_order_relaxed);

@@ -927,17 +927,17 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   const unsigned blocks = static_cast<unsigned>(L.num_sms) * 8u;
   const bool weighted = a.sorted_psw != nullptr;
   const bool wide = d->max_D > 512;  // rows of more than 128 float4 vectors
-  if (weighted) { short_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
-  else { short_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
+  if (weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  else { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   const uint32_t* medium = reinterpret_cast<const uint32_t*>(ws + W.medium_run);
-  if (weighted) { medium_runs_kernel<true><<<blocks, 256, 0, L.s>>>(a, medium); note_launch(); }
-  else { medium_runs_kernel<false><<<blocks, 256, 0, L.s>>>(a, medium); note_launch(); }
-  if (wide && weighted) { short_runs_kernel<true, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
-  if (wide && !weighted) { short_runs_kernel<false, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
-  if (weighted) { long_chunks_kernel<true, false><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); }
-  else { long_chunks_kernel<false, false><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); }
-  if (wide && weighted) { long_chunks_kernel<true, true><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); }
-  if (wide && !weighted) { long_chunks_kernel<false, true><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); }
+  if (weighted) { probe_begin(TBE_PROBE_MEDIUM_RUNS, L.s); medium_runs_kernel<true><<<blocks, 256, 0, L.s>>>(a, medium); note_launch(); probe_end(TBE_PROBE_MEDIUM_RUNS, L.s); }
+  else { probe_begin(TBE_PROBE_MEDIUM_RUNS, L.s); medium_runs_kernel<false><<<blocks, 256, 0, L.s>>>(a, medium); note_launch(); probe_end(TBE_PROBE_MEDIUM_RUNS, L.s); }
+  if (wide && weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  if (wide && !weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  if (weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, false><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  else { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, false><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  if (wide && weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, true><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  if (wide && !weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, true><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
   if (two_launch) {
     { long_finish_kernel<false><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
     if (wide) { long_finish_kernel<true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }

@@ -27,7 +27,7 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "tbe_backward_rowwise_adagrad", "tbe_backward_rowwise_adagrad_noalloc", "tbe_forward",
         "tbe_preprocess", "tbe_read_status", "tbe_version", "tbe_workspace_size",
-        "tbe_kernel_launches",
+        "tbe_kernel_launches", "tbe_probe_set", "tbe_probe_read",
         "tbe_workspace_view"])
 
 
@@ -109,3 +109,11 @@ def test_package_refuses_to_run_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(tbe, "_lib", None)
     with pytest.raises(RuntimeError):
         tbe.tbe_version()
+
+
+def test_probe_selection_and_empty_record(lib):
+    # no GPU needed: selecting a kernel records nothing until it launches
+    assert lib.tbe_probe_set(99) == tbe.TBE_EINVAL
+    assert lib.tbe_probe_set(tbe.TBE_PROBE_LONG_CHUNKS) == tbe.TBE_OK
+    assert tbe.tbe_probe_read() == (0, 0.0)
+    assert lib.tbe_probe_set(tbe.TBE_PROBE_OFF) == tbe.TBE_OK

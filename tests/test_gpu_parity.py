@@ -159,3 +159,17 @@ def test_launch_counter_counts_the_kernels_of_a_call():
     assert c1 - c0 == 1
     assert c2 - c1 == 2
     assert c3 - c2 >= 10  # expand, sort passes, run-length encoding, classify
+
+
+def test_probe_times_the_selected_kernel():
+    w = make("hot")
+    run = H.Run(w)
+    run.backward()  # warm-up: module load, hot set
+    H.tbe.tbe_probe_set(H.tbe.TBE_PROBE_LONG_CHUNKS)
+    run.backward()
+    run.backward()
+    launches, ms = H.tbe.tbe_probe_read()
+    H.tbe.tbe_probe_set(H.tbe.TBE_PROBE_OFF)
+    assert launches == 2 and ms > 0.0
+    run.backward()
+    assert H.tbe.tbe_probe_read() == (0, 0.0)  # switched off
