@@ -240,9 +240,9 @@ tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits);
  * same kernels, but its scratch is a fixed array of TBE_NOALLOC_SCRATCH_BYTES
  * (32 MiB) inside the library, held by every GPU that loads the library until
  * the process exits.  Problems whose scratch would be larger -- roughly more
- * than 400k lookups of 128-wide rows, fewer for wider rows or per-sample
- * weights -- are rejected
- * with TBE_ETOO_LARGE before anything is enqueued.  No cudaMalloc, cudaFree or
+ * than 300k lookups of 128-wide rows at 200 lookups per bag, fewer for wider
+ * rows, shorter bags or per-sample weights -- are rejected with
+ * TBE_ETOO_LARGE before anything is enqueued.  No cudaMalloc, cudaFree or
  * other allocating call is made.
  *
  * The first call on each device does the set-up (looks up the device address
