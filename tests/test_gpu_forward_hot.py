@@ -140,3 +140,25 @@ def test_empty_batch_after_hot_rows_were_learned():
     run.psw = None
     out = forward_preprocessed(run)
     assert not out.any()
+
+
+def test_counts_far_beyond_the_fp16_range():
+    # counts of 40001 and 70000 lookups of one row in a bag: the forward's
+    # scaled three-part fp16 split and the gradient's tf32 remainder terms
+    # must keep forward and backward on the oracle
+    rng = np.random.default_rng(11)
+    bags = [[[7] * 40001 + [3] * 9, [7] * 5 + [3] * 70000, list(rng.integers(0, 50, 100)),
+             [5] * 2048]]
+    w = _custom([50], [64], bags)
+    run = H.Run(w)
+    ref, terms = oracle_forward(w)
+    hot = learn_hot_set(run)
+    assert {3, 5, 7} <= set(hot[0].tolist())
+    H.assert_forward_close(forward_preprocessed(run), ref, terms)
+    hw = H.host(w)
+    W_gpu, m_gpu = run.backward(tbe.TBE_F_PREPROCESSED)
+    W_ref, m_ref = oracle.backward_rowwise_adagrad(H.tables(w), w.B, hw["indices"], hw["offsets"],
+                                                   hw["grad_out"], hw["weights"], hw["momentum"],
+                                                   w.lr, w.eps, hw["psw"])
+    H.assert_momentum_close(m_gpu, m_ref)
+    H.assert_weights_within_ulp(W_gpu, W_ref)
