@@ -186,7 +186,11 @@ tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indic
  * per-sample weights), and the remaining (cold) lookups are also kept per bag
  * in lookup order.  Results stay in the workspace (see tbe_workspace_view); a
  * later tbe_forward or tbe_backward_rowwise_adagrad with TBE_F_PREPROCESSED
- * consumes them.  Errors as tbe_forward. */
+ * consumes them.  The sort chain runs on a stream of the library's own, so
+ * that a forward enqueued next runs concurrently with it; the library's
+ * calls order themselves against it (through events), but reading the
+ * sorted arrays directly needs a device synchronisation first.
+ * Errors as tbe_forward. */
 tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* offsets, int64_t n,
                           const float* per_sample_weights, void* workspace, size_t ws_bytes,
                           void* stream, uint32_t flags);

@@ -941,7 +941,7 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
                          const IndexT* offsets, const float* psw, bool check) {
   const tbe_desc* d = L.d;
   const int64_t n = L.n;
-  cudaStream_t s = L.s;
+  cudaStream_t s = L.s;  // the side stream after the expand
   int* status = check ? reinterpret_cast<int*>(ws + W.status) : nullptr;
   uint32_t* counters = reinterpret_cast<uint32_t*>(ws + W.counts);
   const uint32_t sentinel = static_cast<uint32_t>(d->total_E);
@@ -957,7 +957,13 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
   uint32_t* uk = reinterpret_cast<uint32_t*>(ws + W.unique_keys);
   uint32_t* rs = reinterpret_cast<uint32_t*>(ws + W.run_starts);
 
-  cudaError_t err = cudaMemsetAsync(counters, 0, kNumCounters * sizeof(uint32_t), s);
+  SideFlow* sf = side_flow();
+  if (!sf) return cudaErrorNotReady;
+  // the previous call's side work (sort chain, hot-row update) still reads
+  // the buffers this one rewrites
+  cudaError_t err = cudaStreamWaitEvent(s, sf->done, 0);
+  if (err != cudaSuccess) return err;
+  err = cudaMemsetAsync(counters, 0, kNumCounters * sizeof(uint32_t), s);
   if (err != cudaSuccess) return err;
   err = cudaMemsetAsync(rs, 0, sizeof(uint32_t), s);
   if (err != cudaSuccess) return err;
@@ -1008,6 +1014,12 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
           offsets, n, d->B, bc, tile_cold, co, keys[0], vals[0], pw[0], keys[2], vals[2],
           pw[2]); note_launch(); }
   }
+  // The sort chain (sort, run-length encoding, classification) goes to the
+  // side stream: the forward needs only the expand's outputs and runs
+  // concurrently on the caller's stream; the backward waits for `sorted`.
+  err = fork_to(sf, s);
+  if (err != cudaSuccess) return err;
+  s = sf->side;
   if (n > 0) {
     const SortGeom g = sort_geom(n, L.num_sms, 2, counters + kCntSortN);
     const int bits = key_bits(d);
@@ -1087,6 +1099,10 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
         reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count,
         reinterpret_cast<ChunkDesc*>(ws + W.chunk_order)); note_launch(); }
   }
+  err = cudaEventRecord(sf->sorted, s);
+  if (err != cudaSuccess) return err;
+  err = cudaEventRecord(sf->done, s);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

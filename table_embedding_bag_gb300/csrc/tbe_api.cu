@@ -12,6 +12,31 @@ std::atomic<uint64_t> g_kernel_launches{0};
 
 void note_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 
+SideFlow* side_flow() {
+  static SideFlow flows[64];
+  static std::once_flag once[64];
+  static bool ok[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::call_once(once[dev], [dev]() {
+    SideFlow& f = flows[dev];
+    const unsigned ef = cudaEventDisableTiming;
+    ok[dev] = cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&f.fork, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&f.sorted, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&f.hot, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&f.done, ef) == cudaSuccess;
+  });
+  return ok[dev] ? &flows[dev] : nullptr;
+}
+
+cudaError_t fork_to(SideFlow* f, cudaStream_t s) {
+  cudaError_t e = cudaEventRecord(f->fork, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamWaitEvent(f->side, f->fork, 0);
+}
+
+
 namespace {
 constexpr int kProbeMax = 256;
 std::mutex g_probe_mu;

@@ -924,9 +924,38 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   a.lr = lr;
   a.eps = eps;
   if (L.n == 0) return cudaSuccess;
+  SideFlow* sf = side_flow();
+  if (!sf) return cudaErrorNotReady;
   const unsigned blocks = static_cast<unsigned>(L.num_sms) * 8u;
   const bool weighted = a.sorted_psw != nullptr;
   const bool wide = d->max_D > 512;  // rows of more than 128 float4 vectors
+  // Hot rows on the side stream, concurrently with the cold rows below
+  // (disjoint rows): their gradient needs grad_out (ready on the caller's
+  // stream) and the histogram; the side stream has finished the sort chain
+  // before it starts.
+  const uint32_t* hot_keys = reinterpret_cast<const uint32_t*>(ws + W.hot_keys(W.hot_cur));
+  const uint32_t* hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_cur));
+  const uint32_t* hot_cnt = reinterpret_cast<const uint32_t*>(ws + W.hot_cnt);
+  if (W.hot_enabled) {
+    cudaError_t e = fork_to(sf, L.s);
+    if (e != cudaSuccess) return e;
+    Launch Ls = L;
+    Ls.s = sf->side;
+    const float* part = reinterpret_cast<const float*>(ws + W.hot_part);
+    e = launch_hot_grad(Ls, W, ws, grad_out);
+    if (e != cudaSuccess) return e;
+    { hot_finish_kernel<<<static_cast<unsigned>(d->T) * kHot, 256, 0, Ls.s>>>(
+        a, hot_keys, hot_n, hot_cnt, W.hot_parts, part); note_launch(); }
+    e = cudaEventRecord(sf->hot, Ls.s);
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecord(sf->done, Ls.s);
+    if (e != cudaSuccess) return e;
+  }
+  // the cold rows need the sort chain
+  {
+    cudaError_t e = cudaStreamWaitEvent(L.s, sf->sorted, 0);
+    if (e != cudaSuccess) return e;
+  }
   if (weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   else { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   const uint32_t* medium = reinterpret_cast<const uint32_t*>(ws + W.medium_run);
@@ -942,19 +971,11 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
     { long_finish_kernel<false><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
     if (wide) { long_finish_kernel<true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
   }
-  // Hot rows: gradient from the histogram, update, then choose the next set.
-  const uint32_t* hot_keys = reinterpret_cast<const uint32_t*>(ws + W.hot_keys(W.hot_cur));
-  const uint32_t* hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_cur));
-  const uint32_t* hot_cnt = reinterpret_cast<const uint32_t*>(ws + W.hot_cnt);
-  if (W.hot_enabled) {
-    const float* part = reinterpret_cast<const float*>(ws + W.hot_part);
-    cudaError_t e = launch_hot_grad(L, W, ws, grad_out);
-    if (e != cudaSuccess) return e;
-    { hot_finish_kernel<<<static_cast<unsigned>(d->T) * kHot, 256, 0, L.s>>>(
-        a, hot_keys, hot_n, hot_cnt, W.hot_parts, part); note_launch(); }
-  }
   if (!W.hot_enabled) return cudaGetLastError();  // no histogram: the hot set stays empty
-  cudaError_t e = cudaMemsetAsync(ws + W.sel_hist, 0, static_cast<size_t>(d->T) * kHotBuckets * 4, L.s);
+  // Choose the next hot set, once the hot rows' update has read this one.
+  cudaError_t e = cudaStreamWaitEvent(L.s, sf->hot, 0);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(ws + W.sel_hist, 0, static_cast<size_t>(d->T) * kHotBuckets * 4, L.s);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(ws + W.sel_n, 0, static_cast<size_t>(d->T) * 4, L.s);
   if (e != cudaSuccess) return e;
