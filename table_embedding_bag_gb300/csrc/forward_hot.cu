@@ -76,6 +76,7 @@ struct FwdHotTail {
   uint32_t tmem_base;
   int timed_out;
   int b_table;
+  int64_t row_off[kHot];  // element offset of each hot row in its table, -1: none
   int8_t scale[kFM];
 };
 
@@ -157,21 +158,28 @@ __global__ void __launch_bounds__(kFThreads, 2) forward_hot_kernel(FwdHotArgs a,
       const int64_t h0 = __ldg(a.hash_base + t);
       const int64_t E = __ldg(a.hash_base + t + 1) - h0;
       const __half* Wt = a.W + __ldg(a.w_offsets + t);
+      // the hot rows' offsets first, so the row loads below are independent
+      for (int k = tid; k < nchunks * kFChunk; k += kFThreads) {
+        int64_t off = -1;
+        if (k < nh) {
+          // a key outside the table never had lookups counted: zero row
+          const int64_t row = static_cast<int64_t>(a.hot_keys[t * kHot + k]) - h0;
+          if (row >= 0 && row < E) off = row * D;
+        }
+        tl.row_off[k] = off;
+      }
+      __syncthreads();
       const int ngroups = n_pad / 8;
       const int ncores = ngroups * nchunks * (kFChunk / 8);
+#pragma unroll 4
       for (int cm = warp; cm < ncores; cm += kFThreads / 32) {
         const int ng = cm % ngroups, kg = cm / ngroups;
         const int nn = ng * 8 + lr;
         __half v[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const int k = kg * 8 + lk * 2 + q;
-          v[q] = __float2half(0.f);
-          if (k < nh && nn < D) {
-            // a key outside the table never had lookups counted: zero row
-            const int64_t row = static_cast<int64_t>(a.hot_keys[t * kHot + k]) - h0;
-            if (row >= 0 && row < E) v[q] = Wt[row * D + nn];
-          }
+          const int64_t off = tl.row_off[kg * 8 + lk * 2 + q];
+          v[q] = (off >= 0 && nn < D) ? Wt[off + nn] : __float2half(0.f);
         }
         *reinterpret_cast<__half2*>(b_op + ng * kFSBOB + kg * kFLBO + lane * 4) =
             __halves2half2(v[0], v[1]);
