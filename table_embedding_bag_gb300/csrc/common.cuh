@@ -64,13 +64,21 @@ constexpr int kMaxD = 1024;
 
 // Hot rows: per table, up to kHot rows (the most looked-up ones of the
 // previous backward) bypass the sort; their gradients are histogram(bag x hot
-// row)^T x grad_out.  The histogram is kept only if it fits kHotBudgetBytes,
+// row)^T x grad_out.  The histogram (a byte per entry, plus fp32 rows for
+// the tiles whose entries a byte cannot hold) is kept only if it fits
+// kHotBudgetBytes,
 // and tables wider than kHotMaxD take no hot rows.
 #ifndef TBE_HOT_ROWS
 #define TBE_HOT_ROWS 256
 #endif
 constexpr int kHot = TBE_HOT_ROWS;
 constexpr int kHotTileBags = 128;  // bags per expand CTA (one table)
+// Histogram storage of a tile of kHotTileBags bags: every count of the tile
+// fits a byte (unweighted lookups, at most 255 of one row in a bag), or the
+// tile's rows are fp32 with per-bag scales, or its table has no hot rows.
+constexpr uint8_t kTileBytes = 0;
+constexpr uint8_t kTileWide = 1;
+constexpr uint8_t kTileNoHot = 2;
 constexpr int kHotMaxD = 256;
 constexpr size_t kHotBudgetBytes = size_t(2) << 30;
 constexpr int kHotCtaTarget = 304;  // CTAs of the hot-gradient kernel: one wave at 2 per SM on 152 SMs
@@ -171,8 +179,10 @@ struct WsLayout {
   size_t hot_m2(size_t set) const { return hot_n(set) + static_cast<size_t>(T) * 8; }
   int64_t T;
   size_t hot_cnt;      // uint32 [T][kHot] lookups of each hot row in this call
-  size_t hot_hist;     // float [T][B][kHot] per-bag weight of each hot row (if enabled)
-  size_t hot_scale;    // int8 [T*B] per-bag exponent: histogram row x 2^scale peaks in [2^14, 2^15)
+  size_t hot_hist8;    // uint8 [T][B][kHot] per-bag lookups of each hot row, byte tiles (if enabled)
+  size_t hot_hist;     // float [T][B][kHot] per-bag weight of each hot row, wide tiles (if enabled)
+  size_t hot_scale;    // int8 [T*B] wide tiles: histogram row x 2^scale peaks below 2^15
+  size_t tile_kind;    // uint8 [hot_tiles] kTileBytes / kTileWide / kTileNoHot
   size_t cold_off;     // uint32 [T*B + 1] first cold-list entry of each bag
   size_t hot_part;     // float [T][hot_parts][kHot][kHotMaxD] partial hot gradients
   size_t bag_cold;     // uint32 [T*B] cold lookups per bag

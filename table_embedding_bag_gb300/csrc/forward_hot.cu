@@ -61,8 +61,10 @@ struct FwdHotArgs {
   const int64_t* w_offsets;
   const uint32_t* hot_keys;  // [T][kHot] this batch's hot rows
   const uint32_t* hot_n;     // [T]
-  const float* hot_hist;     // [T][B][kHot]
-  const int8_t* hot_scale;   // [T*B]
+  const uint8_t* hot_hist8;  // [T][B][kHot] byte tiles
+  const float* hot_hist;     // [T][B][kHot] wide tiles
+  const int8_t* hot_scale;   // [T*B] wide tiles
+  const uint8_t* tile_kind;  // [T * ceil(B / kFM)]
   float* out;
   int* error_word;
   int64_t total_D;
@@ -107,6 +109,51 @@ __device__ __forceinline__ void load_chunk(const FwdHotArgs& a, int t, int64_t b
   }
 }
 
+// B operand of table t (once per table and CTA): element (n, k) =
+// W_t[hot row k][n], zero past D or nh.  A warp fills one 128-byte core
+// matrix (8 n x 8 k) per step, lane = 4 (n % 8) + (k % 8) / 2, two k per
+// lane.  row_off (kHot entries of shared memory) takes the hot rows' offsets
+// first, so that the row loads are independent.  Contains __syncthreads; the
+// caller makes sure no MMA still reads b_op.
+__device__ __forceinline__ void stage_hot_rows(const FwdHotArgs& a, int t, int D, int nh,
+                                               int nchunks, int n_pad, unsigned char* b_op,
+                                               int64_t* row_off) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const unsigned lane = lane_id();
+  const int lr = static_cast<int>(lane) >> 2, lk = static_cast<int>(lane) & 3;
+  const int64_t h0 = __ldg(a.hash_base + t);
+  const int64_t E = __ldg(a.hash_base + t + 1) - h0;
+  const __half* Wt = a.W + __ldg(a.w_offsets + t);
+  for (int k = tid; k < nchunks * kFChunk; k += blockDim.x) {
+    int64_t off = -1;
+    if (k < nh) {
+      // a key outside the table never had lookups counted: zero row
+      const int64_t row = static_cast<int64_t>(a.hot_keys[t * kHot + k]) - h0;
+      if (row >= 0 && row < E) off = row * D;
+    }
+    row_off[k] = off;
+  }
+  __syncthreads();
+  const int ngroups = n_pad / 8;
+  const int ncores = ngroups * nchunks * (kFChunk / 8);
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
+#pragma unroll 4
+  for (int cm = warp; cm < ncores; cm += nwarps) {
+    const int ng = cm % ngroups, kg = cm / ngroups;
+    const int nn = ng * 8 + lr;
+    __half v[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int64_t off = row_off[kg * 8 + lk * 2 + q];
+      v[q] = (off >= 0 && nn < D) ? Wt[off + nn] : __float2half(0.f);
+    }
+    *reinterpret_cast<__half2*>(b_op + ng * kFSBOB + kg * kFLBO + lane * 4) =
+        __halves2half2(v[0], v[1]);
+  }
+}
+
+// Wide tiles only (per-sample weights, or counts above 255 in some bag).
 __global__ void __launch_bounds__(kFThreads, 2) forward_hot_kernel(FwdHotArgs a, uint32_t tmem_cols) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -118,6 +165,19 @@ __global__ void __launch_bounds__(kFThreads, 2) forward_hot_kernel(FwdHotArgs a,
   const int warp = tid >> 5;
   const unsigned lane = lane_id();
   const int lr = static_cast<int>(lane) >> 2, lk = static_cast<int>(lane) & 3;
+
+  const int64_t per_table = (a.B + kFM - 1) / kFM;
+  const int64_t tiles = per_table * a.T;
+  const int64_t tile_begin = tiles * blockIdx.x / gridDim.x;
+  const int64_t tile_end = tiles * (blockIdx.x + 1) / gridDim.x;
+  {
+    // nothing to do (the usual case without per-sample weights): leave
+    // before allocating tensor memory
+    int mine = 0;
+    for (int64_t i = tile_begin + tid; i < tile_end; i += kFThreads)
+      mine |= a.tile_kind[i] == kTileWide;
+    if (!__syncthreads_or(mine)) return;
+  }
 
   if (warp == 0) tmem_alloc(&tl.tmem_base, tmem_cols);
   if (tid == 0) {
@@ -133,11 +193,8 @@ __global__ void __launch_bounds__(kFThreads, 2) forward_hot_kernel(FwdHotArgs a,
   uint32_t phase = 0;
   bool pending = false;
 
-  const int64_t per_table = (a.B + kFM - 1) / kFM;
-  const int64_t tiles = per_table * a.T;
-  const int64_t tile_begin = tiles * blockIdx.x / gridDim.x;
-  const int64_t tile_end = tiles * (blockIdx.x + 1) / gridDim.x;
   for (int64_t tile = tile_begin; tile < tile_end; ++tile) {
+    if (a.tile_kind[tile] != kTileWide) continue;  // uniform
     const int t = static_cast<int>(tile / per_table);
     const int64_t d0 = __ldg(a.D_offsets + t);
     const int D = static_cast<int>(__ldg(a.D_offsets + t + 1) - d0);
@@ -151,39 +208,8 @@ __global__ void __launch_bounds__(kFThreads, 2) forward_hot_kernel(FwdHotArgs a,
     float2 x[kFItems];
     load_chunk(a, t, b0, nbags, nh, 0, warp, lr, lk, x);
 
-    // B operand (once per table): element (n, k) = W_t[hot row k][n], zero
-    // past D or nh.  A warp fills one 128-byte core matrix (8 n x 8 k) per
-    // step, lane = 4 (n % 8) + (k % 8) / 2, two k per lane.
     if (tl.b_table != t) {
-      const int64_t h0 = __ldg(a.hash_base + t);
-      const int64_t E = __ldg(a.hash_base + t + 1) - h0;
-      const __half* Wt = a.W + __ldg(a.w_offsets + t);
-      // the hot rows' offsets first, so the row loads below are independent
-      for (int k = tid; k < nchunks * kFChunk; k += kFThreads) {
-        int64_t off = -1;
-        if (k < nh) {
-          // a key outside the table never had lookups counted: zero row
-          const int64_t row = static_cast<int64_t>(a.hot_keys[t * kHot + k]) - h0;
-          if (row >= 0 && row < E) off = row * D;
-        }
-        tl.row_off[k] = off;
-      }
-      __syncthreads();
-      const int ngroups = n_pad / 8;
-      const int ncores = ngroups * nchunks * (kFChunk / 8);
-#pragma unroll 4
-      for (int cm = warp; cm < ncores; cm += kFThreads / 32) {
-        const int ng = cm % ngroups, kg = cm / ngroups;
-        const int nn = ng * 8 + lr;
-        __half v[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int64_t off = tl.row_off[kg * 8 + lk * 2 + q];
-          v[q] = (off >= 0 && nn < D) ? Wt[off + nn] : __float2half(0.f);
-        }
-        *reinterpret_cast<__half2*>(b_op + ng * kFSBOB + kg * kFLBO + lane * 4) =
-            __halves2half2(v[0], v[1]);
-      }
+      stage_hot_rows(a, t, D, nh, nchunks, n_pad, b_op, tl.row_off);
       if (tid == 0) tl.b_table = t;
     }
     if (tid < kFM) tl.scale[tid] = tid < nbags ? a.hot_scale[static_cast<int64_t>(t) * a.B + b0 + tid] : 0;
@@ -284,6 +310,236 @@ __global__ void __launch_bounds__(kFThreads, 2) forward_hot_kernel(FwdHotArgs a,
   if (warp == 0) tmem_dealloc(tmem, tmem_cols);
 }
 
+// ------------------------------------------------------------- byte tiles
+// Tiles whose counts are bytes (no per-sample weights, at most 255 lookups of
+// one hot row in a bag): the tile's 128 x 256 histogram is one contiguous
+// 32 KB block, fetched by one bulk copy into a ring of `stages` buffers,
+// `stages` tiles ahead.  Per tile every thread converts four 16-byte pieces
+// (16 slots of one bag) to fp16, exact, into the A operand (four 64-slot
+// chunks, the layout of the wide kernel); one thread issues the 16 MMAs
+// (K = 256) into one of two accumulators and refills the ring buffer just
+// read; then the warps store the previous tile's accumulator, so that its
+// epilogue overlaps this tile's MMAs.  No scaling: counts and fp16 weights
+// multiply exactly, and the sums are fp32 accumulations.
+constexpr int kBThreads = 512;
+constexpr int kBRawBytes = kFM * kHot;             // 32 KB
+constexpr int kBAOpBytes = kFM * kHot * 2;         // 64 KB: four chunks of kAPartBytes
+constexpr int kBMaxStages = 4;
+static_assert(kHot == 256 && kBAOpBytes == 4 * kAPartBytes, "byte tiles: 256 slots, 4 chunks");
+
+struct FwdBytesTail {
+  alignas(8) unsigned long long full[kBMaxStages];
+  alignas(8) unsigned long long mma_done;
+  uint32_t tmem_base;
+  int timed_out;
+  int b_table;
+  int64_t row_off[kHot];
+};
+
+__host__ __device__ constexpr size_t fwd_bytes_smem_bytes(int n_max, int stages) {
+  return 128 + static_cast<size_t>(n_max) * kHot * 2 + kBAOpBytes +
+         static_cast<size_t>(stages) * kBRawBytes + sizeof(FwdBytesTail);
+}
+
+// Bytes 2 i and 2 i + 1 of w as two fp16 values: 1024 + b is exact in fp16
+// (exponent 10, b in the mantissa), minus 1024 exactly.
+__device__ __forceinline__ uint32_t bytes_to_half2(uint32_t w, uint32_t sel) {
+  const uint32_t x = __byte_perm(w, 0x64646464u, sel);
+  __half2 h = *reinterpret_cast<const __half2*>(&x);
+  h = __hsub2(h, __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400))));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kBThreads, 1)
+    forward_bytes_kernel(FwdHotArgs a, uint32_t tmem_cols, int stages) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  unsigned char* b_op = base;
+  unsigned char* a_op = b_op + static_cast<size_t>(a.n_max) * kHot * 2;
+  unsigned char* raw = a_op + kBAOpBytes;
+  FwdBytesTail& tl = *reinterpret_cast<FwdBytesTail*>(raw + static_cast<size_t>(stages) * kBRawBytes);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const unsigned lane = lane_id();
+
+  const int64_t per_table = (a.B + kFM - 1) / kFM;
+  const int64_t tiles = per_table * a.T;
+  const int64_t tile_begin = tiles * blockIdx.x / gridDim.x;
+  const int64_t tile_end = tiles * (blockIdx.x + 1) / gridDim.x;
+  {
+    int mine = 0;
+    for (int64_t i = tile_begin + tid; i < tile_end; i += kBThreads)
+      mine |= a.tile_kind[i] == kTileBytes;
+    if (!__syncthreads_or(mine)) return;
+  }
+  // the next byte tile at or after `from` (all threads walk the same list)
+  auto next_tile = [&](int64_t from) {
+    while (from < tile_end && a.tile_kind[from] != kTileBytes) ++from;
+    return from;
+  };
+  auto tile_bags = [&](int64_t tile) {
+    const int64_t b0 = (tile % per_table) * kFM;
+    return static_cast<int>(a.B - b0 < kFM ? a.B - b0 : kFM);
+  };
+
+  if (warp == 0) tmem_alloc(&tl.tmem_base, 2 * tmem_cols);
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) mbar_init(&tl.full[i], 1);
+    mbar_init(&tl.mma_done, 1);
+    tl.timed_out = 0;
+    tl.b_table = -1;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tl.tmem_base;
+
+  // producer (thread 0): tiles fetched so far and the next one to fetch
+  int64_t fetch_at = tile_begin;
+  uint32_t fetched = 0;
+  auto fetch = [&](int slot) {
+    fetch_at = next_tile(fetch_at);
+    if (fetch_at >= tile_end) return;
+    const int t = static_cast<int>(fetch_at / per_table);
+    const int64_t b0 = (fetch_at % per_table) * kFM;
+    const uint32_t bytes = static_cast<uint32_t>(tile_bags(fetch_at)) * kHot;
+    mbar_expect_tx(&tl.full[slot], bytes);
+    bulk_copy_g2s(raw + static_cast<size_t>(slot) * kBRawBytes,
+                  a.hot_hist8 + (static_cast<int64_t>(t) * a.B + b0) * kHot, bytes, &tl.full[slot]);
+    ++fetch_at;
+    ++fetched;
+  };
+  if (tid == 0)
+    for (int i = 0; i < stages; ++i) fetch(i);
+
+  uint32_t consumed = 0;   // tiles taken from the ring
+  uint32_t committed = 0;  // tiles whose MMAs were committed
+  uint32_t done = 0;       // tiles whose MMAs are known complete
+  int64_t prev_tile = -1;
+  int prev_t = 0, prev_D = 0, prev_npad = 0;
+
+  // out rows of a finished tile: acc[m][n] for bags m < nbags, columns < D
+  auto epilogue = [&](int64_t tile, int t, int D, int n_pad, uint32_t acc_col) {
+    const int64_t b0 = (tile % per_table) * kFM;
+    const int nbags = tile_bags(tile);
+    const int64_t d0 = __ldg(a.D_offsets + t);
+    const int q = warp & 3;
+    const int m = q * 32 + static_cast<int>(lane);
+    for (int c0 = (warp >> 2) * 32; c0 < n_pad; c0 += (kBThreads / 128) * 32) {
+      float v[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc_col + static_cast<uint32_t>(c0), v);
+      if (m < nbags) {
+        float* o = a.out + (b0 + m) * a.total_D + d0 + c0;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          if (c0 + j < D) *reinterpret_cast<float4*>(o + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
+    }
+  };
+
+  for (int64_t tile = next_tile(tile_begin); tile < tile_end; tile = next_tile(tile + 1)) {
+    const int t = static_cast<int>(tile / per_table);
+    const int64_t d0 = __ldg(a.D_offsets + t);
+    const int D = static_cast<int>(__ldg(a.D_offsets + t + 1) - d0);
+    const int nh = static_cast<int>(min(a.hot_n[t], static_cast<uint32_t>(kHot)));
+    const int n_pad = (D + 15) & ~15;
+    const int nchunks = (nh + kFChunk - 1) / kFChunk;
+    const int slot = static_cast<int>(consumed % static_cast<uint32_t>(stages));
+    // this tile's bytes, and the previous tile's MMAs (A and B are rewritten)
+    bool ok = mbar_wait(&tl.full[slot], (consumed / static_cast<uint32_t>(stages)) & 1u);
+    ++consumed;
+    if (committed > done) {
+      const bool mma_ok = mbar_wait(&tl.mma_done, done & 1u);
+      if (mma_ok) ++done;
+      ok = ok && mma_ok;
+    }
+    fence_after_sync();
+    if (!ok) atomicOr(&tl.timed_out, 1);
+    __syncthreads();
+    if (tl.timed_out) break;
+    if (tl.b_table != t) {
+      // tables with hot rows are at most kHotMaxD wide, so n_pad <= n_max
+      stage_hot_rows(a, t, D, nh, nchunks, n_pad, b_op, tl.row_off);
+      if (tid == 0) tl.b_table = t;
+    }
+    // bytes -> fp16 A operand.  Item (bag m, 16 slots from k0): the eight
+    // lanes of a quarter warp take bags 8 mg .. 8 mg + 7 at rotated slot
+    // groups, so that both the 16-byte reads (row stride 256 bytes) and the
+    // core-matrix writes fall in eight distinct bank groups.
+    const unsigned char* rt = raw + static_cast<size_t>(slot) * kBRawBytes;
+#pragma unroll
+    for (int j = 0; j < (kFM * kHot / 16) / kBThreads; ++j) {
+      const int item = tid + j * kBThreads;
+      const int p = item & 7, r = item >> 3;
+      const int mg = r & 15, kq = r >> 4;
+      const int m = mg * 8 + p;
+      const int k0 = ((kq + p) & 15) * 16;
+      const uint4 w = *reinterpret_cast<const uint4*>(rt + m * kHot + k0);
+      uint4 h0, h1;
+      h0.x = bytes_to_half2(w.x, 0x4140u);
+      h0.y = bytes_to_half2(w.x, 0x4342u);
+      h0.z = bytes_to_half2(w.y, 0x4140u);
+      h0.w = bytes_to_half2(w.y, 0x4342u);
+      h1.x = bytes_to_half2(w.z, 0x4140u);
+      h1.y = bytes_to_half2(w.z, 0x4342u);
+      h1.z = bytes_to_half2(w.w, 0x4140u);
+      h1.w = bytes_to_half2(w.w, 0x4342u);
+      unsigned char* dst = a_op + (k0 >> 6) * kAPartBytes + mg * kFSBOA + ((k0 & 63) >> 3) * kFLBO + p * 16;
+      *reinterpret_cast<uint4*>(dst) = h0;
+      *reinterpret_cast<uint4*>(dst + kFLBO) = h1;
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t acc_col = (committed & 1u) * tmem_cols;
+    if (tid == 0) {
+      const uint32_t idesc = make_idesc(kFmtF16, kFM, n_pad);
+      for (int c = 0; c < nchunks; ++c)
+#pragma unroll
+        for (int ks = 0; ks < kFChunk / 16; ++ks)
+          mma_f16(tmem + acc_col,
+                  make_smem_desc(a_op + c * kAPartBytes + ks * 2 * kFLBO, kFLBO, kFSBOA),
+                  make_smem_desc(b_op + (c * (kFChunk / 8) + ks * 2) * kFLBO, kFLBO, kFSBOB), idesc,
+                  (c | ks) != 0 ? 1u : 0u);
+      mma_commit(&tl.mma_done);
+      // the ring buffer just converted is free: fetch `stages` tiles ahead
+      fence_proxy_async();
+      fetch(slot);
+    }
+    ++committed;
+    if (prev_tile >= 0) epilogue(prev_tile, prev_t, prev_D, prev_npad, ((committed - 2) & 1u) * tmem_cols);
+    prev_tile = tile;
+    prev_t = t;
+    prev_D = D;
+    prev_npad = n_pad;
+    fence_before_sync();
+  }
+  if (!tl.timed_out && committed > done) {
+    const bool ok = mbar_wait(&tl.mma_done, done & 1u);
+    if (ok) ++done;
+    fence_after_sync();
+    if (!ok) atomicOr(&tl.timed_out, 1);
+    __syncthreads();
+    if (!tl.timed_out) epilogue(prev_tile, prev_t, prev_D, prev_npad, ((committed - 1) & 1u) * tmem_cols);
+  }
+  __syncthreads();
+  if (tl.timed_out && tid == 0) {
+    atomicOr(a.error_word, TBE_ERR_TIMEOUT);
+    // drain (bounded): the MMAs committed and the copies issued (the last
+    // tile taken may have timed out on its copy; a completed phase passes)
+    if (committed > done) mbar_wait(&tl.mma_done, done & 1u);
+    for (uint32_t f = consumed > 0 ? consumed - 1 : 0; f < fetched; ++f)
+      mbar_wait(&tl.full[f % static_cast<uint32_t>(stages)], (f / static_cast<uint32_t>(stages)) & 1u);
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 2 * tmem_cols);
+}
+
 }  // namespace
 
 cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, const void* weights,
@@ -298,8 +554,10 @@ cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, con
     a.w_offsets = d->weights_offsets;
     a.hot_keys = reinterpret_cast<const uint32_t*>(ws + W.hot_keys(W.hot_cur));
     a.hot_n = hot_n;
+    a.hot_hist8 = reinterpret_cast<const uint8_t*>(ws + W.hot_hist8);
     a.hot_hist = reinterpret_cast<const float*>(ws + W.hot_hist);
     a.hot_scale = reinterpret_cast<const int8_t*>(ws + W.hot_scale);
+    a.tile_kind = reinterpret_cast<const uint8_t*>(ws + W.tile_kind);
     a.out = out;
     a.error_word = reinterpret_cast<int*>(ws + W.status);
     a.total_D = d->total_D;
@@ -343,7 +601,37 @@ cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, con
     int64_t grid = static_cast<int64_t>(per_sm) * L.num_sms;
     if (grid > tiles) grid = tiles;
     if (grid < 1) grid = 1;
-    { probe_begin(TBE_PROBE_FORWARD_HOT, L.s); forward_hot_kernel<<<static_cast<unsigned>(grid), kFThreads, smem, L.s>>>(a, tmem_cols); note_launch(); probe_end(TBE_PROBE_FORWARD_HOT, L.s); }
+
+    // byte tiles: one CTA per SM, as many ring stages as shared memory holds
+    static size_t bytes_attr[64] = {};
+    static int bytes_stages[64] = {};
+    static int bytes_nmax[64] = {};
+    if (bytes_nmax[dev] != a.n_max) {
+      int optin = 0;
+      e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+      if (e != cudaSuccess) return e;
+      int stages = kBMaxStages;
+      while (stages > 1 && fwd_bytes_smem_bytes(a.n_max, stages) > static_cast<size_t>(optin)) --stages;
+      const size_t bsmem = fwd_bytes_smem_bytes(a.n_max, stages);
+      e = cudaFuncSetAttribute(forward_bytes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(bsmem));
+      if (e != cudaSuccess) return e;
+      bytes_attr[dev] = bsmem;
+      bytes_stages[dev] = stages;
+      bytes_nmax[dev] = a.n_max;
+    }
+    int64_t bgrid = L.num_sms < tiles ? L.num_sms : tiles;
+    if (bgrid < 1) bgrid = 1;
+    // both kernels together are the hot part of the forward
+    probe_begin(TBE_PROBE_FORWARD_HOT, L.s);
+    forward_bytes_kernel<<<static_cast<unsigned>(bgrid), kBThreads, bytes_attr[dev], L.s>>>(
+        a, tmem_cols, bytes_stages[dev]);
+    note_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    forward_hot_kernel<<<static_cast<unsigned>(grid), kFThreads, smem, L.s>>>(a, tmem_cols);
+    note_launch();
+    probe_end(TBE_PROBE_FORWARD_HOT, L.s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -7,12 +7,14 @@
 // built.  For all hot rows of a table at once that is a dense product
 // G^T (D_t x B) times H (B x slots), computed here per partition of the bags.
 //
-// GB300 design: CTA (t, p) owns bags [B p / P, B (p+1) / P) of table t and
+// GB300 design: CTA (t, p) owns the p-th of P runs of whole 32-bag stages of
+// table t (so that a stage never straddles two 128-bag histogram tiles) and
 // accumulates D^T[c][slot] (M = 128 columns per tile, up to two tiles for
 // D_t <= 256; N = the table's hot slots rounded up to 16, at most 256) in
 // tensor memory over stages of 32 bags.  Per stage the threads stage the
 // gradient rows transposed (A, K-major) and the histogram rows transposed
-// (B, K-major), each split into a tf32 high part and an exact fp32
+// (B, K-major; from the byte histogram for byte tiles, the fp32 one for wide
+// tiles), each split into a tf32 high part and an exact fp32
 // remainder, and one thread issues kind::tf32 MMAs for hi*hi + lo*hi + hi*lo
 // (the last only when the histogram has a remainder: per-sample weights, or
 // counts of 2^11 and up).  The next stage's loads are issued before waiting
@@ -51,7 +53,9 @@ __device__ __forceinline__ void split_tf32(float v, float* hi, float* lo) {
 struct HotGradArgs {
   const float* grad_out;
   const int64_t* D_offsets;
-  const float* hot_hist;  // [T][B][kHot]
+  const uint8_t* hot_hist8;  // [T][B][kHot] byte tiles
+  const float* hot_hist;     // [T][B][kHot] wide tiles
+  const uint8_t* tile_kind;  // [T * ceil(B / kHotTileBags)]
   const uint32_t* hot_n;  // [T]
   float* hot_part;        // [T][parts][kHot][kHotMaxD]
   int* error_word;
@@ -82,9 +86,10 @@ struct StageRegs {
   float h[kGBItems];
 };
 
+template <bool kMixed>
 __device__ __forceinline__ void load_stage(const HotGradArgs& a, int t, int64_t d0, int D,
                                            int mtiles, int nh, int n_slots, int64_t c0, int cnt,
-                                           int warp, int lr, int lk, StageRegs& r) {
+                                           bool bytes, int warp, int lr, int lk, StageRegs& r) {
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -99,17 +104,65 @@ __device__ __forceinline__ void load_stage(const HotGradArgs& a, int t, int64_t 
   // B items: core matrix cm = 8 sg + kg (k group fastest, a power of two),
   // rows = hot slots 8 sg .. 8 sg + 7
   const int ngroups = n_slots / 8;
-  const float* hrow = a.hot_hist + (static_cast<int64_t>(t) * a.B + c0 + lk) * kHot + lr;
+  const int64_t hoff = (static_cast<int64_t>(t) * a.B + c0 + lk) * kHot + lr;
+  if (kMixed && bytes) {
+    const uint8_t* hrow = a.hot_hist8 + hoff;
 #pragma unroll
-  for (int j = 0; j < kGBItems; ++j) {
-    const int cm = warp + j * kGWarps;
-    const int kg = cm & (kGStage / 4 - 1), sg = cm >> 3;
-    const int slot = sg * 8 + lr;
-    const int kb = kg * 4 + lk;
-    r.h[j] = (sg < ngroups && slot < nh && kb < cnt) ? __ldg(hrow + kg * 4 * kHot + sg * 8) : 0.f;
+    for (int j = 0; j < kGBItems; ++j) {
+      const int cm = warp + j * kGWarps;
+      const int kg = cm & (kGStage / 4 - 1), sg = cm >> 3;
+      const int slot = sg * 8 + lr;
+      const int kb = kg * 4 + lk;
+      r.h[j] = (sg < ngroups && slot < nh && kb < cnt)
+                   ? static_cast<float>(__ldg(hrow + kg * 4 * kHot + sg * 8))
+                   : 0.f;
+    }
+  } else {
+    const float* hrow = a.hot_hist + hoff;
+#pragma unroll
+    for (int j = 0; j < kGBItems; ++j) {
+      const int cm = warp + j * kGWarps;
+      const int kg = cm & (kGStage / 4 - 1), sg = cm >> 3;
+      const int slot = sg * 8 + lr;
+      const int kb = kg * 4 + lk;
+      r.h[j] = (sg < ngroups && slot < nh && kb < cnt) ? __ldg(hrow + kg * 4 * kHot + sg * 8) : 0.f;
+    }
   }
 }
 
+// Bags [*b_begin, *b_end) of partition p: whole 32-bag stages, so that a
+// stage lies inside one 128-bag histogram tile.
+__device__ __forceinline__ void partition_bags(const HotGradArgs& a, int p, int64_t* b_begin,
+                                               int64_t* b_end) {
+  static_assert(kHotTileBags % kGStage == 0, "stages inside histogram tiles");
+  const int64_t nstages = (a.B + kGStage - 1) / kGStage;
+  *b_begin = nstages * p / a.parts * kGStage;
+  const int64_t e = nstages * (p + 1) / a.parts * kGStage;
+  *b_end = e < a.B ? e : a.B;
+}
+
+// Which kernel takes a partition: its histogram tiles all bytes, all wide (or
+// none), or both.  Contains __syncthreads_or.
+enum PartClass { kPartWide = 0, kPartBytes = 1, kPartMixed = 2 };
+__device__ __forceinline__ int partition_class(const HotGradArgs& a, int t, int64_t b_begin,
+                                               int64_t b_end) {
+  const int64_t per_table = (a.B + kHotTileBags - 1) / kHotTileBags;
+  int any_bytes = 0, any_wide = 0;
+  if (b_begin < b_end)
+    for (int64_t i = b_begin / kHotTileBags + threadIdx.x; i <= (b_end - 1) / kHotTileBags;
+         i += blockDim.x) {
+      const uint8_t k = a.tile_kind[t * per_table + i];
+      any_bytes |= k == kTileBytes;
+      any_wide |= k != kTileBytes;
+    }
+  any_bytes = __syncthreads_or(any_bytes);
+  any_wide = __syncthreads_or(any_wide);
+  return any_bytes ? (any_wide ? kPartMixed : kPartBytes) : kPartWide;
+}
+
+// Partitions with wide tiles (kMixed: with byte tiles too; otherwise every
+// tile wide, or no bags): register-staged, one stage of loads in flight.
+template <bool kMixed>
 __global__ void __launch_bounds__(kGThreads, 2) hot_grad_tc_kernel(HotGradArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -129,8 +182,9 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_tc_kernel(HotGradArgs a
   if (nh == 0 || (D & 7) || mtiles > a.max_mtiles) return;  // uniform over the CTA
   const int n_slots = (nh + 15) & ~15;                      // MMA N
   const uint32_t tmem_cols = mtiles == 1 ? 256u : 512u;     // 256 columns per M tile
-  const int64_t b_begin = static_cast<int64_t>(a.B) * p / a.parts;
-  const int64_t b_end = static_cast<int64_t>(a.B) * (p + 1) / a.parts;
+  int64_t b_begin, b_end;
+  partition_bags(a, p, &b_begin, &b_end);
+  if (partition_class(a, t, b_begin, b_end) != (kMixed ? kPartMixed : kPartWide)) return;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const unsigned lane = lane_id();
@@ -151,11 +205,16 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_tc_kernel(HotGradArgs a
   bool pending = false;
   bool first = true;
 
+  // histogram kind of the stage at bag c (byte or wide tile); read one stage
+  // ahead of its loads, so that it adds no latency in front of them
+  const uint8_t* kinds = a.tile_kind + static_cast<int64_t>(t) * ((a.B + kHotTileBags - 1) / kHotTileBags);
+  auto kind_at = [&](int64_t c) { return c < b_end ? kinds[c / kHotTileBags] : kTileWide; };
   StageRegs r;
+  uint8_t kind_next = kind_at(b_begin + kGStage);
   if (b_begin < b_end)
-    load_stage(a, t, d0, D, mtiles, nh, n_slots, b_begin,
-               static_cast<int>(b_end - b_begin < kGStage ? b_end - b_begin : kGStage), warp, lr,
-               lk, r);
+    load_stage<kMixed>(a, t, d0, D, mtiles, nh, n_slots, b_begin,
+               static_cast<int>(b_end - b_begin < kGStage ? b_end - b_begin : kGStage),
+               kind_at(b_begin) == kTileBytes, warp, lr, lk, r);
   for (int64_t c0 = b_begin; c0 < b_end; c0 += kGStage) {
     // stage the loaded values: core matrix cm sits at (cm % groups) * SBO +
     // (cm / groups) * LBO; inside it element (row % 8, k % 4) is at 4 lane
@@ -192,9 +251,13 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_tc_kernel(HotGradArgs a
     }
     // the next stage's loads overlap this stage's MMAs
     const int64_t c1 = c0 + kGStage;
-    if (c1 < b_end)
-      load_stage(a, t, d0, D, mtiles, nh, n_slots, c1,
-                 static_cast<int>(b_end - c1 < kGStage ? b_end - c1 : kGStage), warp, lr, lk, r);
+    if (c1 < b_end) {
+      const bool bytes = kind_next == kTileBytes;
+      kind_next = kind_at(c1 + kGStage);
+      load_stage<kMixed>(a, t, d0, D, mtiles, nh, n_slots, c1,
+                 static_cast<int>(b_end - c1 < kGStage ? b_end - c1 : kGStage), bytes, warp, lr,
+                 lk, r);
+    }
     const int need_lo = __syncthreads_or(lo_here);
     fence_proxy_async();
     fence_before_sync();
@@ -268,21 +331,232 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_tc_kernel(HotGradArgs a
   if (warp == 0) tmem_dealloc(tmem, tmem_cols);
 }
 
+// ------------------------------------------------------ byte partitions
+// Partitions whose tiles all hold byte counts.  Each 32-bag stage is one
+// bulk copy of the 8 KB byte histogram plus one bulk copy per gradient row
+// (D_t floats) into a ring of kGRing shared buffers, kGRing stages ahead.
+// The threads build the operands from shared memory: the gradient split
+// into tf32 high part and exact remainder (A, K-major; M = columns), the
+// counts as tf32 (B; exact, so no remainder term); one thread issues the
+// MMAs (hi x B + lo x B) into the accumulator in tensor memory.  Operands
+// are single-buffered: the next stage's conversion waits for this stage's
+// MMAs, two CTAs per SM interleave.  Bags past the end of the partition are
+// zero in both operands (their ring rows are not copied).
+constexpr int kGRing = 2;
+constexpr int kGHistBytes = kGStage * kHot;  // 8 KB
+
+struct HotGradBytesTail {
+  alignas(8) unsigned long long full[kGRing];
+  alignas(8) unsigned long long mma_done;
+  uint32_t tmem_base;
+  int timed_out;
+};
+
+// ring stage: byte histogram, then kGStage gradient rows of up to mtiles x 128 floats
+__host__ __device__ constexpr size_t grad_ring_stage_bytes(int mtiles) {
+  return kGHistBytes + static_cast<size_t>(kGStage) * mtiles * kGM * 4;
+}
+__host__ __device__ constexpr size_t hot_grad_bytes_smem_bytes(int mtiles) {
+  return 128 + 2 * static_cast<size_t>(mtiles) * kGATileBytes + kGBBytes +
+         kGRing * grad_ring_stage_bytes(mtiles) + sizeof(HotGradBytesTail);
+}
+
+__global__ void __launch_bounds__(kGThreads, 2) hot_grad_bytes_kernel(HotGradArgs a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  unsigned char* a_hi[2] = {base, base + 2 * kGATileBytes};
+  unsigned char* a_lo[2] = {base + kGATileBytes, base + 3 * kGATileBytes};
+  unsigned char* b_op = base + 2 * a.max_mtiles * kGATileBytes;
+  unsigned char* ring = b_op + kGBBytes;
+  const size_t stage_bytes = grad_ring_stage_bytes(a.max_mtiles);
+  HotGradBytesTail& tl = *reinterpret_cast<HotGradBytesTail*>(ring + kGRing * stage_bytes);
+
+  const int t = blockIdx.x / a.parts;
+  const int p = blockIdx.x % a.parts;
+  const int64_t d0 = a.D_offsets[t];
+  const int D = static_cast<int>(a.D_offsets[t + 1] - d0);
+  const int nh = D <= kHotMaxD ? static_cast<int>(min(a.hot_n[t], static_cast<uint32_t>(kHot))) : 0;
+  const int mtiles = (D + kGM - 1) / kGM;
+  if (nh == 0 || (D & 7) || mtiles > a.max_mtiles) return;  // uniform over the CTA
+  int64_t b_begin, b_end;
+  partition_bags(a, p, &b_begin, &b_end);
+  if (partition_class(a, t, b_begin, b_end) != kPartBytes) return;
+  const int n_slots = (nh + 15) & ~15;
+  const uint32_t tmem_cols = mtiles == 1 ? 256u : 512u;
+  const int nstages = static_cast<int>((b_end - b_begin + kGStage - 1) / kGStage);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const unsigned lane = lane_id();
+
+  if (warp == 0) tmem_alloc(&tl.tmem_base, tmem_cols);
+  if (tid == 0) {
+    for (int i = 0; i < kGRing; ++i) mbar_init(&tl.full[i], 1);
+    mbar_init(&tl.mma_done, 1);
+    tl.timed_out = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tl.tmem_base;
+  const uint32_t idesc = make_idesc(kFmtTF32, kGM, n_slots);
+
+  // warp 0 issues stage i into ring slot i % kGRing
+  auto issue = [&](int i) {
+    const int slot = i % kGRing;
+    const int64_t c0 = b_begin + static_cast<int64_t>(i) * kGStage;
+    const int cnt = static_cast<int>(b_end - c0 < kGStage ? b_end - c0 : kGStage);
+    unsigned char* st = ring + slot * stage_bytes;
+    if (lane == 0)
+      mbar_expect_tx(&tl.full[slot], static_cast<uint32_t>(cnt) * (kHot + D * 4));
+    __syncwarp();
+    if (lane == 0)
+      bulk_copy_g2s(st, a.hot_hist8 + (static_cast<int64_t>(t) * a.B + c0) * kHot,
+                    static_cast<uint32_t>(cnt) * kHot, &tl.full[slot]);
+    if (static_cast<int>(lane) < cnt)
+      bulk_copy_g2s(st + kGHistBytes + lane * D * 4, a.grad_out + (c0 + lane) * a.total_D + d0,
+                    static_cast<uint32_t>(D) * 4, &tl.full[slot]);
+  };
+  if (warp == 0)
+    for (int i = 0; i < kGRing && i < nstages; ++i) issue(i);
+
+  int consumed = 0, committed = 0, done = 0;
+  for (int i = 0; i < nstages; ++i) {
+    const int slot = i % kGRing;
+    bool ok = mbar_wait(&tl.full[slot], static_cast<uint32_t>(i / kGRing) & 1u);
+    ++consumed;
+    if (committed > done) {
+      const bool mma_ok = mbar_wait(&tl.mma_done, static_cast<uint32_t>(done) & 1u);
+      if (mma_ok) ++done;
+      ok = ok && mma_ok;
+    }
+    fence_after_sync();
+    if (!ok) atomicOr(&tl.timed_out, 1);
+    __syncthreads();
+    if (tl.timed_out) break;
+    const int64_t c0 = b_begin + static_cast<int64_t>(i) * kGStage;
+    const int cnt = static_cast<int>(b_end - c0 < kGStage ? b_end - c0 : kGStage);
+    const unsigned char* st = ring + slot * stage_bytes;
+    const float* g = reinterpret_cast<const float*>(st + kGHistBytes);
+    // A: item (column c, bag group kg) reads rows 4 kg .. 4 kg + 3 of column c
+    // (consecutive columns across the warp) and writes one 16-byte row of a
+    // core matrix (eight consecutive columns hit eight bank groups)
+    for (int item = tid; item < mtiles * kGM * (kGStage / 4); item += kGThreads) {
+      const int c = item % (mtiles * kGM);
+      const int kg = item / (mtiles * kGM);
+      float hi[4], lo[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int kb = kg * 4 + q;
+        const float v = (kb < cnt && c < D) ? g[kb * D + c] : 0.f;
+        split_tf32(v, &hi[q], &lo[q]);
+      }
+      const int mt = c / kGM, cc = c % kGM;
+      const uint32_t at = static_cast<uint32_t>((cc / 8) * kGSBO + kg * kGLBO + (cc % 8) * 16);
+      *reinterpret_cast<float4*>(a_hi[mt] + at) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<float4*>(a_lo[mt] + at) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    // B: item (slot n, bag group kg): four counts of slot n as tf32 (exact)
+    for (int item = tid; item < n_slots * (kGStage / 4); item += kGThreads) {
+      const int n = item % n_slots;
+      const int kg = item / n_slots;
+      float v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int kb = kg * 4 + q;
+        v[q] = (kb < cnt && n < nh) ? static_cast<float>(st[kb * kHot + n]) : 0.f;
+      }
+      const uint32_t at = static_cast<uint32_t>((n / 8) * kGSBO + kg * kGLBO + (n % 8) * 16);
+      *reinterpret_cast<float4*>(b_op + at) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (tid == 0) {
+      for (int mt = 0; mt < mtiles; ++mt) {
+        const uint32_t acc_tmem = tmem + static_cast<uint32_t>(mt * 256);
+#pragma unroll
+        for (int ks = 0; ks < kGStage / 8; ++ks) {
+          const uint32_t off = ks * 2 * kGLBO;
+          mma_tf32(acc_tmem, make_smem_desc(a_hi[mt] + off, kGLBO, kGSBO),
+                   make_smem_desc(b_op + off, kGLBO, kGSBO), idesc, (i | ks) != 0 ? 1u : 0u);
+          mma_tf32(acc_tmem, make_smem_desc(a_lo[mt] + off, kGLBO, kGSBO),
+                   make_smem_desc(b_op + off, kGLBO, kGSBO), idesc, 1u);
+        }
+      }
+      mma_commit(&tl.mma_done);
+    }
+    ++committed;
+    // the ring slot just read is free: warp 0 refills it kGRing stages ahead
+    if (warp == 0 && i + kGRing < nstages) {
+      fence_proxy_async();
+      issue(i + kGRing);
+    }
+  }
+  if (!tl.timed_out && committed > done) {
+    const bool ok = mbar_wait(&tl.mma_done, static_cast<uint32_t>(done) & 1u);
+    if (ok) ++done;
+    fence_after_sync();
+    if (!ok) atomicOr(&tl.timed_out, 1);
+  }
+  __syncthreads();
+  float* dst = a.hot_part + (static_cast<int64_t>(t) * a.parts + p) * kHot * kHotMaxD;
+  if (!tl.timed_out) {
+    // D^T[c][slot] -> hot_part[t][p][slot][c], as in the register-staged kernel
+    const int q = warp & 3;
+    const int mt = warp >> 2;
+    if (mt < mtiles) {
+      const int c = mt * kGM + q * 32 + static_cast<int>(lane);
+      for (int s0 = 0; s0 < n_slots; s0 += 32) {
+        float v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 256 + s0), v);
+        if (c < D)
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (s0 + j < nh) dst[(s0 + j) * kHotMaxD + c] = v[j];
+      }
+    }
+  } else if (tid == 0) {
+    atomicOr(a.error_word, TBE_ERR_TIMEOUT);
+    // drain (bounded): committed MMAs, issued copies (the stage that timed
+    // out included; a completed phase passes)
+    if (committed > done) mbar_wait(&tl.mma_done, static_cast<uint32_t>(done) & 1u);
+    const int issued = nstages < consumed - 1 + kGRing ? nstages : consumed - 1 + kGRing;
+    for (int f = consumed > 0 ? consumed - 1 : 0; f < issued; ++f)
+      mbar_wait(&tl.full[f % kGRing], static_cast<uint32_t>(f / kGRing) & 1u);
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, tmem_cols);
+}
+
 }  // namespace
 
 cudaError_t launch_hot_grad(const Launch& L, const WsLayout& W, char* ws, const float* grad_out) {
   const int max_mtiles = L.d->max_D > kGM ? 2 : 1;
   const size_t smem = hot_grad_smem_bytes(max_mtiles);
+  const size_t bsmem = hot_grad_bytes_smem_bytes(max_mtiles);
   static size_t attr_bytes[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (attr_bytes[dev] != smem) {
-    e = cudaFuncSetAttribute(hot_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    for (const void* k : {reinterpret_cast<const void*>(hot_grad_tc_kernel<false>),
+                          reinterpret_cast<const void*>(hot_grad_tc_kernel<true>)}) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+    }
+    e = cudaFuncSetAttribute(hot_grad_bytes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bsmem));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(hot_grad_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(hot_grad_bytes_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_bytes[dev] = smem;
@@ -290,7 +564,9 @@ cudaError_t launch_hot_grad(const Launch& L, const WsLayout& W, char* ws, const 
   HotGradArgs a;
   a.grad_out = grad_out;
   a.D_offsets = L.d->D_offsets;
+  a.hot_hist8 = reinterpret_cast<const uint8_t*>(ws + W.hot_hist8);
   a.hot_hist = reinterpret_cast<const float*>(ws + W.hot_hist);
+  a.tile_kind = reinterpret_cast<const uint8_t*>(ws + W.tile_kind);
   a.hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_cur));
   a.hot_part = reinterpret_cast<float*>(ws + W.hot_part);
   a.error_word = reinterpret_cast<int*>(ws + W.status);
@@ -298,8 +574,17 @@ cudaError_t launch_hot_grad(const Launch& L, const WsLayout& W, char* ws, const 
   a.B = L.d->B;
   a.parts = W.hot_parts;
   a.max_mtiles = max_mtiles;
+  // every partition is taken by exactly one of the three kernels (byte
+  // tiles only, wide tiles only or no bags, both kinds); the others leave
   const unsigned grid = static_cast<unsigned>(L.d->T) * static_cast<unsigned>(W.hot_parts);
-  { probe_begin(TBE_PROBE_HOT_GRAD, L.s); hot_grad_tc_kernel<<<grid, kGThreads, smem, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_HOT_GRAD, L.s); }
+  probe_begin(TBE_PROBE_HOT_GRAD, L.s);
+  hot_grad_bytes_kernel<<<grid, kGThreads, bsmem, L.s>>>(a);
+  note_launch();
+  hot_grad_tc_kernel<false><<<grid, kGThreads, smem, L.s>>>(a);
+  note_launch();
+  hot_grad_tc_kernel<true><<<grid, kGThreads, smem, L.s>>>(a);
+  note_launch();
+  probe_end(TBE_PROBE_HOT_GRAD, L.s);
   return cudaGetLastError();
 }
 

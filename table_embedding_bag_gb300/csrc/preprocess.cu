@@ -38,8 +38,12 @@ constexpr int kRleTile = kRleThreads * kRleItems;
 // ------------------------------------------------------------------ expand
 // One CTA per tile of kHotTileBags consecutive bags of one table.  A lookup
 // whose row is in the table's hot set adds its weight (1 without per-sample
-// weights) to the tile's histogram hot_hist[t][slot][bag]; every other valid
-// lookup is cold and goes to the sort.  Out-of-range lookups go nowhere.
+// weights) to the bag's histogram row; every other valid lookup is cold and
+// goes to the sort.  Out-of-range lookups go nowhere.  Without per-sample
+// weights a bag's row is stored as bytes (hot_hist8) while no count exceeds
+// 255; a tile with any larger count, and every tile with per-sample weights,
+// is wide: all its bags get fp32 rows (hot_hist) with per-bag scales.  The
+// tile's kind (bytes, wide, or no hot rows) goes to tile_kind.
 // Pass 1 (count) fills the histogram and counts cold lookups per bag and per
 // tile; a scan of the tile counts gives each tile's first sort position;
 // pass 2 (write) writes the cold lookups in position order, so the sort's
@@ -114,6 +118,14 @@ __device__ int build_hot_hash(HotHash& h, uint32_t* m1, uint32_t* m2, const HotS
   return nh;
 }
 
+// Per-bag exponent of an fp32 histogram row: the row's largest magnitude
+// times 2^scale lands in [2^14, 2^15).
+__device__ __forceinline__ int8_t bag_scale(float peak) {
+  int sc = 0;
+  if (peak > 0.f) sc = 14 - ilogbf(peak);
+  return static_cast<int8_t>(sc < -126 ? -126 : (sc > 126 ? 126 : sc));
+}
+
 // Histogram slots written per bag: nh rounded up to the 64-slot MMA chunk.
 __device__ __forceinline__ int hot_slots_padded(int nh) { return (nh + 63) & ~63; }
 
@@ -121,11 +133,12 @@ template <typename IndexT, bool kWeighted>
 struct ExpandSmem {
   HotHash hash;
   uint32_t warp_cold[8];
+  uint32_t wide_bags[kHotTileBags / 32];  // bit lb: bag lb has an fp32 row
   uint32_t slot_cnt[kHot];
   // the bag each warp is on: per-slot weight (exact sums: integer counts, or
   // fp32 weights summed in double, so the result does not depend on atomic
   // order) and, weighted, per-slot lookups
-  typename std::conditional<kWeighted, double, uint32_t>::type row[8][kHot];
+  alignas(16) typename std::conditional<kWeighted, double, uint32_t>::type row[8][kHot];
   uint32_t cnt_row[kWeighted ? 8 : 1][kWeighted ? kHot : 1];
 };
 
@@ -136,7 +149,8 @@ __global__ void __launch_bounds__(256)
     expand_count_kernel(const IndexT* __restrict__ indices, const IndexT* __restrict__ offsets,
                         const float* __restrict__ psw, const int64_t* __restrict__ hash_base,
                         const int64_t* __restrict__ D_offsets, int64_t n, int B, HotSet hs,
-                        float* __restrict__ hot_hist, int8_t* __restrict__ hot_scale,
+                        uint8_t* __restrict__ hot_hist8, float* __restrict__ hot_hist,
+                        int8_t* __restrict__ hot_scale, uint8_t* __restrict__ tile_kind,
                         uint32_t* __restrict__ hot_cnt, uint32_t* __restrict__ bag_cold,
                         uint32_t* __restrict__ tile_cold, uint32_t* __restrict__ sp_keys,
                         uint32_t* __restrict__ sp_vals, float* __restrict__ sp_psw, int* status) {
@@ -150,6 +164,7 @@ __global__ void __launch_bounds__(256)
     if constexpr (kWeighted) sm.cnt_row[i / kHot][i % kHot] = 0;
   }
   for (int i = threadIdx.x; i < kHot; i += blockDim.x) sm.slot_cnt[i] = 0;
+  if (threadIdx.x < kHotTileBags / 32) sm.wide_bags[threadIdx.x] = 0;
   const int64_t h0 = __ldg(hash_base + ti.t);
   const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
   uint32_t m1, m2;
@@ -157,7 +172,10 @@ __global__ void __launch_bounds__(256)
                                 hot_hist != nullptr);
   const int nh_pad = hot_slots_padded(nh);
   constexpr int kPerLane = kHot / 32;
-  uint32_t cnt[kPerLane];  // lane l: lookups of slots l, l + 32, ... over the tile
+  static_assert(kPerLane == 8, "byte rows: eight slots per lane");
+  // lookups of this lane's slots over the tile: slots l, l + 32, ... with
+  // per-sample weights, slots 8 l .. 8 l + 7 without
+  uint32_t cnt[kPerLane];
 #pragma unroll
   for (int j = 0; j < kPerLane; ++j) cnt[j] = 0;
   bool bad = false;
@@ -214,31 +232,52 @@ __global__ void __launch_bounds__(256)
       // flush the bag's row: histogram entries, per-bag scale, slot counts
       __syncwarp();
       float* dst = hot_hist + bag * kHot;
-      float peak = 0.f;
+      if constexpr (kWeighted) {
+        float peak = 0.f;
 #pragma unroll
-      for (int j = 0; j < kPerLane; ++j) {
-        const int slot = lane + 32 * j;
-        if (slot < nh_pad) {
-          const auto v = sm.row[warp][slot];
-          const float f = static_cast<float>(v);
-          dst[slot] = f;
-          peak = fmaxf(peak, fabsf(f));
-          if constexpr (kWeighted) {
+        for (int j = 0; j < kPerLane; ++j) {
+          const int slot = lane + 32 * j;
+          if (slot < nh_pad) {
+            const float f = static_cast<float>(sm.row[warp][slot]);
+            dst[slot] = f;
+            peak = fmaxf(peak, fabsf(f));
             cnt[j] += sm.cnt_row[warp][slot];
             sm.cnt_row[warp][slot] = 0;
-          } else {
-            cnt[j] += v;
+            sm.row[warp][slot] = 0;
           }
-          sm.row[warp][slot] = 0;
         }
-      }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) peak = fmaxf(peak, __shfl_xor_sync(kFull, peak, o));
-      if (lane == 0) {
-        // exponent taking the bag's largest entry into [2^14, 2^15)
-        int sc = 0;
-        if (peak > 0.f) sc = 14 - ilogbf(peak);
-        hot_scale[bag] = static_cast<int8_t>(sc < -126 ? -126 : (sc > 126 ? 126 : sc));
+        for (int o = 16; o > 0; o >>= 1) peak = fmaxf(peak, __shfl_xor_sync(kFull, peak, o));
+        if (lane == 0) hot_scale[bag] = bag_scale(peak);
+      } else {
+        // lane l: slots 8 l .. 8 l + 7 (two 16-byte shared loads)
+        uint4* rw = reinterpret_cast<uint4*>(&sm.row[warp][8 * lane]);
+        const uint4 q0 = rw[0], q1 = rw[1];
+        rw[0] = make_uint4(0u, 0u, 0u, 0u);
+        rw[1] = make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t v[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        uint32_t peak = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          cnt[k] += v[k];
+          peak = max(peak, v[k]);
+        }
+        peak = __reduce_max_sync(kFull, peak);
+        if (peak <= 255u) {
+          // slots past nh hold zeros: the whole 256-byte row is written
+          uint2 packed;
+          packed.x = v[0] | (v[1] << 8) | (v[2] << 16) | (v[3] << 24);
+          packed.y = v[4] | (v[5] << 8) | (v[6] << 16) | (v[7] << 24);
+          *reinterpret_cast<uint2*>(hot_hist8 + bag * kHot + 8 * lane) = packed;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (8 * lane + k < nh_pad) dst[8 * lane + k] = static_cast<float>(v[k]);
+          if (lane == 0) {
+            hot_scale[bag] = bag_scale(static_cast<float>(peak));
+            atomicOr(&sm.wide_bags[lb >> 5], 1u << (lb & 31));
+          }
+        }
       }
       __syncwarp();
     }
@@ -246,12 +285,32 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) sm.warp_cold[warp] = cold_w;
 #pragma unroll
   for (int j = 0; j < kPerLane; ++j)
-    if (cnt[j]) atomicAdd(&sm.slot_cnt[lane + 32 * j], cnt[j]);
+    if (cnt[j]) atomicAdd(&sm.slot_cnt[kWeighted ? lane + 32 * j : 8 * lane + j], cnt[j]);
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t c = 0;
     for (int w = 0; w < 8; ++w) c += sm.warp_cold[w];
     tile_cold[blockIdx.x] = c;
+  }
+  if (nh_pad) {
+    bool wide = kWeighted;
+#pragma unroll
+    for (int i = 0; i < kHotTileBags / 32; ++i) wide |= sm.wide_bags[i] != 0;
+    if (!kWeighted && wide) {
+      // a wide tile is read as fp32 rows only: the byte rows written above
+      // (this CTA's own global writes, visible after the barrier) become
+      // fp32 rows with scale 0 (counts of at most 255 are exact as they are)
+      for (int lb = warp; lb < ti.nbags; lb += 8) {
+        if ((sm.wide_bags[lb >> 5] >> (lb & 31)) & 1u) continue;
+        const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
+        for (int slot = lane; slot < nh_pad; slot += 32)
+          hot_hist[bag * kHot + slot] = static_cast<float>(hot_hist8[bag * kHot + slot]);
+        if (lane == 0) hot_scale[bag] = 0;
+      }
+    }
+    if (threadIdx.x == 0) tile_kind[blockIdx.x] = wide ? kTileWide : kTileBytes;
+  } else if (hot_hist != nullptr && threadIdx.x == 0) {
+    tile_kind[blockIdx.x] = kTileNoHot;
   }
   for (int i = threadIdx.x; i < nh; i += blockDim.x)
     if (sm.slot_cnt[i]) atomicAdd(&hot_cnt[ti.t * kHot + i], sm.slot_cnt[i]);
@@ -988,7 +1047,9 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     hs.m1 = reinterpret_cast<const uint32_t*>(ws + W.hot_m1(W.hot_cur));
     hs.m2 = reinterpret_cast<const uint32_t*>(ws + W.hot_m2(W.hot_cur));
     float* hh = W.hot_enabled ? reinterpret_cast<float*>(ws + W.hot_hist) : nullptr;
+    uint8_t* hh8 = W.hot_enabled ? reinterpret_cast<uint8_t*>(ws + W.hot_hist8) : nullptr;
     int8_t* hsc = reinterpret_cast<int8_t*>(ws + W.hot_scale);
+    uint8_t* tk = reinterpret_cast<uint8_t*>(ws + W.tile_kind);
     uint32_t* hc = reinterpret_cast<uint32_t*>(ws + W.hot_cnt);
     uint32_t* bc = reinterpret_cast<uint32_t*>(ws + W.bag_cold);
     uint32_t* co = reinterpret_cast<uint32_t*>(ws + W.cold_off);
@@ -998,11 +1059,11 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     // writes buffer 0)
     if (weighted)
       { probe_begin(TBE_PROBE_EXPAND_COUNT, s); expand_count_kernel<IndexT, true><<<tiles, 256, sizeof(ExpandSmem<IndexT, true>), s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh, hsc, hc, bc,
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh8, hh, hsc, tk, hc, bc,
           tile_cold, keys[0], vals[0], pw[0], status); note_launch(); probe_end(TBE_PROBE_EXPAND_COUNT, s); }
     else
       { probe_begin(TBE_PROBE_EXPAND_COUNT, s); expand_count_kernel<IndexT, false><<<tiles, 256, sizeof(ExpandSmem<IndexT, false>), s>>>(
-          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh, hsc, hc, bc,
+          indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh8, hh, hsc, tk, hc, bc,
           tile_cold, keys[0], vals[0], pw[0], status); note_launch(); probe_end(TBE_PROBE_EXPAND_COUNT, s); }
     { exclusive_scan_kernel<<<1, 1024, 0, s>>>(tile_cold, W.hot_tiles, counters + kCntSortN); note_launch(); }
     if (weighted)

@@ -120,9 +120,11 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   L.hot_parts = static_cast<int>(kHotCtaTarget / T > 0 ? kHotCtaTarget / T : 1);
   const int64_t max_parts = (B + kHotMinPartBags - 1) / kHotMinPartBags;
   if (L.hot_parts > max_parts) L.hot_parts = static_cast<int>(max_parts);
-  L.hot_enabled = static_cast<size_t>(T) * kHot * B * sizeof(float) <= kHotBudgetBytes;
+  L.hot_enabled = static_cast<size_t>(T) * kHot * B * (sizeof(float) + 1) <= kHotBudgetBytes;
   L.hot_cnt = take(T * kHot * 4);
+  L.hot_hist8 = L.hot_enabled ? take(static_cast<size_t>(T) * kHot * B) : 0;
   L.hot_hist = L.hot_enabled ? take(static_cast<size_t>(T) * kHot * B * sizeof(float)) : 0;
+  L.tile_kind = take(L.hot_tiles);
   L.hot_part = L.hot_enabled ? take(static_cast<size_t>(T) * L.hot_parts * kHot * kHotMaxD * 4) : 0;
   L.hot_scale = take(static_cast<size_t>(T) * B);
   L.bag_cold = take(static_cast<size_t>(T) * B * 4);

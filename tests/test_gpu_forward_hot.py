@@ -162,3 +162,37 @@ def test_counts_far_beyond_the_fp16_range():
                                                    w.lr, w.eps, hw["psw"])
     H.assert_momentum_close(m_gpu, m_ref)
     H.assert_weights_within_ulp(W_gpu, W_ref)
+
+
+def test_byte_and_wide_tiles_in_one_table():
+    # 400 bags = three 128-bag tiles and a ragged one of 16.  Table 0: bag
+    # 150 (second tile) and bag 390 (last tile) hold 300 lookups of one row,
+    # past a byte, so those tiles keep fp32 rows; the others are byte tiles.
+    # Table 1 stays in bytes (at most 255 of a row per bag, 255 in bag 7).
+    rng = np.random.default_rng(13)
+    E, D, B = [60, 3000], [64, 128], 400
+    bags = []
+    for t in range(2):
+        tb = []
+        for b in range(B):
+            n = int(rng.integers(60, 140))
+            hot = rng.integers(0, 6, n * 3 // 4)
+            cold = rng.integers(0, E[t], n - n * 3 // 4)
+            tb.append(list(rng.permutation(np.concatenate([hot, cold]))))
+        bags.append(tb)
+    bags[0][150] = bags[0][150] + [5] * 300
+    bags[0][390] = [2] * 300 + bags[0][390]
+    bags[1][7] = [4] * 255 + bags[1][7]
+    w = _custom(E, D, bags)
+    run = H.Run(w)
+    ref, terms = oracle_forward(w)
+    hot = learn_hot_set(run)
+    assert all(len(h) > 0 for h in hot)
+    H.assert_forward_close(forward_preprocessed(run), ref, terms)
+    hw = H.host(w)
+    W_gpu, m_gpu = run.backward(tbe.TBE_F_PREPROCESSED)
+    W_ref, m_ref = oracle.backward_rowwise_adagrad(H.tables(w), w.B, hw["indices"], hw["offsets"],
+                                                   hw["grad_out"], hw["weights"], hw["momentum"],
+                                                   w.lr, w.eps, hw["psw"])
+    H.assert_momentum_close(m_gpu, m_ref)
+    H.assert_weights_within_ulp(W_gpu, W_ref)
