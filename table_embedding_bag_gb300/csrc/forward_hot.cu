@@ -336,9 +336,13 @@ struct FwdBytesTail {
   int64_t row_off[kHot];
 };
 
-__host__ __device__ constexpr size_t fwd_bytes_smem_bytes(int n_max, int stages) {
+// Epilogue transpose buffer: per warp 32 rows x 16 columns of fp32.
+constexpr int kBXposeBytes = (kBThreads / 32) * 32 * 16 * 4;  // 32 KB
+
+__host__ __device__ constexpr size_t fwd_bytes_smem_bytes(int n_max, int stages, bool xpose) {
   return 128 + static_cast<size_t>(n_max) * kHot * 2 + kBAOpBytes +
-         static_cast<size_t>(stages) * kBRawBytes + sizeof(FwdBytesTail);
+         static_cast<size_t>(stages) * kBRawBytes + (xpose ? kBXposeBytes : 0) +
+         sizeof(FwdBytesTail);
 }
 
 // Bytes 2 i and 2 i + 1 of w as two fp16 values: 1024 + b is exact in fp16
@@ -350,6 +354,11 @@ __device__ __forceinline__ uint32_t bytes_to_half2(uint32_t w, uint32_t sel) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// kXpose: the epilogue goes through a per-warp shared buffer so that every
+// global store instruction writes 8 rows x 64 contiguous bytes (full
+// sectors); without it (no room for the buffer: D_t > 128) a lane stores its
+// own row.
+template <bool kXpose>
 __global__ void __launch_bounds__(kBThreads, 1)
     forward_bytes_kernel(FwdHotArgs a, uint32_t tmem_cols, int stages) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -358,7 +367,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
   unsigned char* b_op = base;
   unsigned char* a_op = b_op + static_cast<size_t>(a.n_max) * kHot * 2;
   unsigned char* raw = a_op + kBAOpBytes;
-  FwdBytesTail& tl = *reinterpret_cast<FwdBytesTail*>(raw + static_cast<size_t>(stages) * kBRawBytes);
+  unsigned char* xpose = raw + static_cast<size_t>(stages) * kBRawBytes;
+  FwdBytesTail& tl = *reinterpret_cast<FwdBytesTail*>(xpose + (kXpose ? kBXposeBytes : 0));
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const unsigned lane = lane_id();
@@ -430,7 +440,33 @@ __global__ void __launch_bounds__(kBThreads, 1)
     for (int c0 = (warp >> 2) * 32; c0 < n_pad; c0 += (kBThreads / 128) * 32) {
       float v[32];
       tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc_col + static_cast<uint32_t>(c0), v);
-      if (m < nbags) {
+      if constexpr (kXpose) {
+        // 16 columns at a time: lane = row writes four 16-byte chunks, chunk
+        // c of row r at r * 64 + (c ^ ((r >> 1) & 3)) * 16, so eight
+        // consecutive rows fill eight bank groups; then four lanes per row
+        // read a row's 64 bytes back (eight rows per instruction)
+        unsigned char* xb = xpose + warp * (32 * 16 * 4);
+        const int lr4 = static_cast<int>(lane) >> 2, lc = static_cast<int>(lane) & 3;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<float4*>(xb + lane * 64 + ((c ^ ((lane >> 1) & 3)) * 16)) =
+                make_float4(v[16 * h + 4 * c], v[16 * h + 4 * c + 1], v[16 * h + 4 * c + 2],
+                            v[16 * h + 4 * c + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int r = 8 * k + lr4;
+            const float4 x = *reinterpret_cast<const float4*>(xb + r * 64 + ((lc ^ ((r >> 1) & 3)) * 16));
+            const int mm = q * 32 + r;
+            const int col = c0 + 16 * h + 4 * lc;
+            if (mm < nbags && col < D)
+              *reinterpret_cast<float4*>(a.out + (b0 + mm) * a.total_D + d0 + col) = x;
+          }
+          __syncwarp();
+        }
+      } else if (m < nbags) {
         float* o = a.out + (b0 + m) * a.total_D + d0 + c0;
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
@@ -439,13 +475,15 @@ __global__ void __launch_bounds__(kBThreads, 1)
     }
   };
 
+  int t = -1, D = 0, nh = 0, n_pad = 0, nchunks = 0;  // the current tile's table
   for (int64_t tile = next_tile(tile_begin); tile < tile_end; tile = next_tile(tile + 1)) {
-    const int t = static_cast<int>(tile / per_table);
-    const int64_t d0 = __ldg(a.D_offsets + t);
-    const int D = static_cast<int>(__ldg(a.D_offsets + t + 1) - d0);
-    const int nh = static_cast<int>(min(a.hot_n[t], static_cast<uint32_t>(kHot)));
-    const int n_pad = (D + 15) & ~15;
-    const int nchunks = (nh + kFChunk - 1) / kFChunk;
+    if (tile / per_table != t) {
+      t = static_cast<int>(tile / per_table);
+      D = static_cast<int>(__ldg(a.D_offsets + t + 1) - __ldg(a.D_offsets + t));
+      nh = static_cast<int>(min(a.hot_n[t], static_cast<uint32_t>(kHot)));
+      n_pad = (D + 15) & ~15;
+      nchunks = (nh + kFChunk - 1) / kFChunk;
+    }
     const int slot = static_cast<int>(consumed % static_cast<uint32_t>(stages));
     // this tile's bytes, and the previous tile's MMAs (A and B are rewritten)
     bool ok = mbar_wait(&tl.full[slot], (consumed / static_cast<uint32_t>(stages)) & 1u);
@@ -603,29 +641,38 @@ cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, con
     if (grid < 1) grid = 1;
 
     // byte tiles: one CTA per SM, as many ring stages as shared memory holds
+    // (the transpose buffer when at least two stages fit beside it)
     static size_t bytes_attr[64] = {};
     static int bytes_stages[64] = {};
     static int bytes_nmax[64] = {};
+    static bool bytes_xpose[64] = {};
     if (bytes_nmax[dev] != a.n_max) {
       int optin = 0;
       e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
       if (e != cudaSuccess) return e;
+      const bool xpose = fwd_bytes_smem_bytes(a.n_max, 2, true) <= static_cast<size_t>(optin);
       int stages = kBMaxStages;
-      while (stages > 1 && fwd_bytes_smem_bytes(a.n_max, stages) > static_cast<size_t>(optin)) --stages;
-      const size_t bsmem = fwd_bytes_smem_bytes(a.n_max, stages);
-      e = cudaFuncSetAttribute(forward_bytes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(bsmem));
+      while (stages > 1 && fwd_bytes_smem_bytes(a.n_max, stages, xpose) > static_cast<size_t>(optin))
+        --stages;
+      const size_t bsmem = fwd_bytes_smem_bytes(a.n_max, stages, xpose);
+      e = cudaFuncSetAttribute(xpose ? forward_bytes_kernel<true> : forward_bytes_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bsmem));
       if (e != cudaSuccess) return e;
       bytes_attr[dev] = bsmem;
       bytes_stages[dev] = stages;
+      bytes_xpose[dev] = xpose;
       bytes_nmax[dev] = a.n_max;
     }
     int64_t bgrid = L.num_sms < tiles ? L.num_sms : tiles;
     if (bgrid < 1) bgrid = 1;
     // both kernels together are the hot part of the forward
     probe_begin(TBE_PROBE_FORWARD_HOT, L.s);
-    forward_bytes_kernel<<<static_cast<unsigned>(bgrid), kBThreads, bytes_attr[dev], L.s>>>(
-        a, tmem_cols, bytes_stages[dev]);
+    if (bytes_xpose[dev])
+      forward_bytes_kernel<true><<<static_cast<unsigned>(bgrid), kBThreads, bytes_attr[dev], L.s>>>(
+          a, tmem_cols, bytes_stages[dev]);
+    else
+      forward_bytes_kernel<false><<<static_cast<unsigned>(bgrid), kBThreads, bytes_attr[dev], L.s>>>(
+          a, tmem_cols, bytes_stages[dev]);
     note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

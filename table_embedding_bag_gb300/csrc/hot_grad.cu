@@ -439,36 +439,49 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_bytes_kernel(HotGradArg
     const int cnt = static_cast<int>(b_end - c0 < kGStage ? b_end - c0 : kGStage);
     const unsigned char* st = ring + slot * stage_bytes;
     const float* g = reinterpret_cast<const float*>(st + kGHistBytes);
-    // A: item (column c, bag group kg) reads rows 4 kg .. 4 kg + 3 of column c
-    // (consecutive columns across the warp) and writes one 16-byte row of a
-    // core matrix (eight consecutive columns hit eight bank groups)
-    for (int item = tid; item < mtiles * kGM * (kGStage / 4); item += kGThreads) {
-      const int c = item % (mtiles * kGM);
-      const int kg = item / (mtiles * kGM);
-      float hi[4], lo[4];
+    // A: thread (column cl of each M tile, bag groups kgb + 2 j) reads rows
+    // 4 kg .. 4 kg + 3 of its column (consecutive columns across the warp)
+    // and writes one 16-byte row of a core matrix (eight consecutive columns
+    // hit eight bank groups)
+    static_assert(kGThreads == 2 * kGM, "A: two bag groups per pass");
+    {
+      const int cl = tid & (kGM - 1), kgb = tid >> 7;
+      for (int mt = 0; mt < mtiles; ++mt) {
+        const int c = mt * kGM + cl;
+        const bool col_ok = c < D;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int kb = kg * 4 + q;
-        const float v = (kb < cnt && c < D) ? g[kb * D + c] : 0.f;
-        split_tf32(v, &hi[q], &lo[q]);
+        for (int j = 0; j < kGStage / 8; ++j) {
+          const int kg = kgb + 2 * j;
+          float hi[4], lo[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int kb = kg * 4 + q;
+            const float v = (kb < cnt && col_ok) ? g[kb * D + c] : 0.f;
+            split_tf32(v, &hi[q], &lo[q]);
+          }
+          const uint32_t at = static_cast<uint32_t>((cl >> 3) * kGSBO + kg * kGLBO + (cl & 7) * 16);
+          *reinterpret_cast<float4*>(a_hi[mt] + at) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<float4*>(a_lo[mt] + at) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+        }
       }
-      const int mt = c / kGM, cc = c % kGM;
-      const uint32_t at = static_cast<uint32_t>((cc / 8) * kGSBO + kg * kGLBO + (cc % 8) * 16);
-      *reinterpret_cast<float4*>(a_hi[mt] + at) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<float4*>(a_lo[mt] + at) = make_float4(lo[0], lo[1], lo[2], lo[3]);
     }
-    // B: item (slot n, bag group kg): four counts of slot n as tf32 (exact)
-    for (int item = tid; item < n_slots * (kGStage / 4); item += kGThreads) {
-      const int n = item % n_slots;
-      const int kg = item / n_slots;
-      float v[4];
+    // B: thread n (one hot slot, n_slots <= 256 threads): the four counts of
+    // each bag group as tf32, exact (2^23 + b is a float, minus 2^23)
+    static_assert(kGThreads >= kHot, "B: one slot per thread");
+    if (tid < n_slots) {
+      const int n = tid;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int kb = kg * 4 + q;
-        v[q] = (kb < cnt && n < nh) ? static_cast<float>(st[kb * kHot + n]) : 0.f;
+      for (int kg = 0; kg < kGStage / 4; ++kg) {
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int kb = kg * 4 + q;
+          const uint32_t b = (kb < cnt && n < nh) ? st[kb * kHot + n] : 0u;
+          v[q] = __uint_as_float(0x4b000000u | b) - 8388608.f;
+        }
+        const uint32_t at = static_cast<uint32_t>((n >> 3) * kGSBO + kg * kGLBO + (n & 7) * 16);
+        *reinterpret_cast<float4*>(b_op + at) = make_float4(v[0], v[1], v[2], v[3]);
       }
-      const uint32_t at = static_cast<uint32_t>((n / 8) * kGSBO + kg * kGLBO + (n % 8) * 16);
-      *reinterpret_cast<float4*>(b_op + at) = make_float4(v[0], v[1], v[2], v[3]);
     }
     fence_proxy_async();
     fence_before_sync();
