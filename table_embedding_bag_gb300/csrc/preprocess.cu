@@ -142,7 +142,10 @@ struct ExpandSmem {
   uint32_t cnt_row[kWeighted ? 8 : 1][kWeighted ? kHot : 1];
 };
 
-constexpr int kExpandLoads = 4;  // index loads in flight per lane
+#ifndef TBE_EXPAND_LOADS
+#define TBE_EXPAND_LOADS 8
+#endif
+constexpr int kExpandLoads = TBE_EXPAND_LOADS;  // index loads in flight per lane
 
 template <typename IndexT, bool kWeighted>
 __global__ void __launch_bounds__(256)
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(256)
       for (int u = 0; u < kExpandLoads; ++u) {
         if (base + u * 32 >= e) break;  // warp-uniform
         const bool inside = r[u] != -2;
-        const bool ok = inside && r[u] >= 0 && r[u] < E;
+        const bool ok = static_cast<uint64_t>(r[u]) < static_cast<uint64_t>(E);  // -2 fails too
         bad |= inside && !ok;
         const uint32_t key = static_cast<uint32_t>(h0 + r[u]);
         const int slot = ok && nh ? hot_lookup(sm.hash, m1, m2, key) : -1;
@@ -219,10 +222,10 @@ __global__ void __launch_bounds__(256)
             atomicAdd(&sm.cnt_row[warp][slot], 1u);
           }
         } else {
-          // one add per distinct hot row of the 32 lookups
-          const unsigned peers = __match_any_sync(kFull, slot);
-          if (slot >= 0 && lane == static_cast<unsigned>(__ffs(peers) - 1))
-            atomicAdd(&sm.row[warp][slot], static_cast<uint32_t>(__popc(peers)));
+          // one shared atomic per hot lookup: lanes on the same row are
+          // merged by the shared-memory unit, which measured faster than
+          // combining them first with a warp match
+          if (slot >= 0) atomicAdd(&sm.row[warp][slot], 1u);
         }
       }
     }
