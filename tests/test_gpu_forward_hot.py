@@ -196,3 +196,31 @@ def test_byte_and_wide_tiles_in_one_table():
                                                    w.lr, w.eps, hw["psw"])
     H.assert_momentum_close(m_gpu, m_ref)
     H.assert_weights_within_ulp(W_gpu, W_ref)
+
+
+def test_hot_sets_at_capacity_with_a_cold_remainder():
+    # 300 and 310 rows, each looked up far above the hot threshold: the hot
+    # sets are (nearly) full and the remaining rows stay cold.  Bag 200 of
+    # table 0 has 300 lookups of one row (its tile keeps fp32 rows); table 1
+    # (D = 256) stays in bytes.
+    rng = np.random.default_rng(17)
+    E, D, B = [300, 310], [64, 256], 384
+    bags = [[list(rng.integers(0, E[t], int(rng.integers(80, 160)))) for _ in range(B)]
+            for t in range(2)]
+    bags[0][200] = bags[0][200] + [290] * 300
+    w = _custom(E, D, bags)
+    run = H.Run(w)
+    ref, terms = oracle_forward(w)
+    hot = learn_hot_set(run)
+    slots = tbe.tbe_workspace_view(run.desc, max(w.n, 1), run.ws)["hot_slots"]
+    # the selection cuts at log-scale count buckets, so a set of evenly used
+    # rows need not fill every slot
+    assert all(0 < len(h) <= min(slots, e) for h, e in zip(hot, E))
+    H.assert_forward_close(forward_preprocessed(run), ref, terms)
+    hw = H.host(w)
+    W_gpu, m_gpu = run.backward(tbe.TBE_F_PREPROCESSED)
+    W_ref, m_ref = oracle.backward_rowwise_adagrad(H.tables(w), w.B, hw["indices"], hw["offsets"],
+                                                   hw["grad_out"], hw["weights"], hw["momentum"],
+                                                   w.lr, w.eps, hw["psw"])
+    H.assert_momentum_close(m_gpu, m_ref)
+    H.assert_weights_within_ulp(W_gpu, W_ref)
