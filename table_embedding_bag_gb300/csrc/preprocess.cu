@@ -91,6 +91,19 @@ __device__ __forceinline__ TileInfo tile_info(int B) {
   return ti;
 }
 
+// The tile's nbags + 1 offsets, clamped to [0, n], into shared memory (one
+// coalesced load per CTA instead of a dependent load at every bag); bag lb
+// of the tile then spans [off[lb], max(off[lb + 1], off[lb])), as bag_range
+// gives.  The caller synchronises before reading them.
+template <typename IndexT>
+__device__ __forceinline__ void load_tile_offsets(const IndexT* offsets, const TileInfo& ti, int B,
+                                                  int64_t n, int64_t* off) {
+  for (int i = threadIdx.x; i <= ti.nbags; i += blockDim.x) {
+    const int64_t v = load_index(offsets, static_cast<int64_t>(ti.t) * B + ti.b0 + i);
+    off[i] = v < 0 ? 0 : (v > n ? n : v);
+  }
+}
+
 // Builds the hash of table t's hot set (empty when the histogram is disabled
 // or the table is too wide for the hot path); returns the number of hot
 // slots.  Contains __syncthreads.
@@ -132,6 +145,7 @@ __device__ __forceinline__ int hot_slots_padded(int nh) { return (nh + 63) & ~63
 template <typename IndexT, bool kWeighted>
 struct ExpandSmem {
   HotHash hash;
+  int64_t bag_off[kHotTileBags + 1];  // the tile's offsets, clamped to [0, n]
   uint32_t warp_cold[8];
   uint32_t wide_bags[kHotTileBags / 32];  // bit lb: bag lb has an fp32 row
   uint32_t slot_cnt[kHot];
@@ -168,6 +182,7 @@ __global__ void __launch_bounds__(256)
   }
   for (int i = threadIdx.x; i < kHot; i += blockDim.x) sm.slot_cnt[i] = 0;
   if (threadIdx.x < kHotTileBags / 32) sm.wide_bags[threadIdx.x] = 0;
+  load_tile_offsets(offsets, ti, B, n, sm.bag_off);  // read after build_hot_hash's barriers
   const int64_t h0 = __ldg(hash_base + ti.t);
   const int64_t E = __ldg(hash_base + ti.t + 1) - h0;
   uint32_t m1, m2;
@@ -186,8 +201,8 @@ __global__ void __launch_bounds__(256)
   const unsigned lt = (1u << lane) - 1u;
   for (int lb = warp; lb < ti.nbags; lb += 8) {
     const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
-    int64_t s, e;
-    bag_range(offsets, bag, n, &s, &e);
+    const int64_t s = sm.bag_off[lb];
+    const int64_t e = sm.bag_off[lb + 1] > s ? sm.bag_off[lb + 1] : s;
     uint32_t cold = 0;  // this bag's cold lookups so far (the same in every lane)
     for (int64_t base = s; base < e; base += 32 * kExpandLoads) {
       int64_t r[kExpandLoads];
@@ -335,9 +350,11 @@ __global__ void __launch_bounds__(256)
                         uint32_t* __restrict__ vals, float* __restrict__ psw_out) {
   __shared__ uint32_t bag_base[kHotTileBags];
   __shared__ uint32_t scan[33];
+  __shared__ int64_t bag_off[kHotTileBags + 1];
   const TileInfo ti = tile_info(B);
   const int warp = threadIdx.x >> 5;
   const unsigned lane = lane_id();
+  load_tile_offsets(offsets, ti, B, n, bag_off);  // read after the scan's barriers
   {
     // exclusive prefix of the tile's per-bag cold counts = the bags' first
     // entries in the dense list
@@ -355,8 +372,7 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   for (int lb = warp; lb < ti.nbags; lb += 8) {
     const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
-    int64_t s, e;
-    bag_range(offsets, bag, n, &s, &e);
+    const int64_t s = bag_off[lb];
     const uint32_t c = bag_cold[bag];
     const uint32_t pos = bag_base[lb];
     for (uint32_t i = lane; i < c; i += 32) {
