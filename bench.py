@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import select
 import statistics
 import subprocess
 import sys
@@ -42,7 +43,7 @@ INDEX_BYTES = 8
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=40)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--cpu-bags", type=int, default=16384,
@@ -96,6 +97,7 @@ class Clocks:
     def __init__(self, gpu_index):
         self.proc = None
         self.gpu = gpu_index
+        self.first = ""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.Q}",
@@ -103,6 +105,11 @@ class Clocks:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
+            return
+        # start timing only once sampling is live (its first line is out)
+        ready, _, _ = select.select([self.proc.stdout], [], [], 5.0)
+        if ready:
+            self.first = self.proc.stdout.readline()
 
     def stop(self):
         if self.proc is None:
@@ -115,7 +122,7 @@ class Clocks:
             out, _ = self.proc.communicate()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in (self.first + out).strip().splitlines():
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
