@@ -598,10 +598,12 @@ __global__ void __launch_bounds__(kSortThreads, 2)
       key[r] = p < valid ? sm.keys[cur][p] : 0xffffffffu;
       const uint32_t d = (key[r] >> shift) & mask;
       const unsigned peers = __match_any_sync(kFull, d);
-      const uint32_t before = sm.wcnt[warp][d];
-      __syncwarp();
-      if (lane == 31u - __clz(peers)) sm.wcnt[warp][d] = before + __popc(peers);
-      __syncwarp();
+      // the digit's leader adds the round's count; atomics on one address
+      // return in issue order, so the rounds need no barrier between them
+      const int leader = 31 - __clz(peers);
+      uint32_t old = 0;
+      if (static_cast<int>(lane) == leader) old = atomicAdd(&sm.wcnt[warp][d], __popc(peers));
+      const uint32_t before = __shfl_sync(kFull, old, leader);
       const uint32_t rk = before + __popc(peers & lt_mask);
       if (r & 1) rank[r >> 1] |= rk << 16; else rank[r >> 1] = rk;
     }
@@ -877,36 +879,55 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-// Long runs (at least kLongThreshold pairs): compacted into a list on the
-// device, each with a contiguous range of chunk slots and of tree nodes.
+// Medium runs (kMediumRun <= pairs < kLongThreshold) and long runs (at least
+// kLongThreshold pairs) compacted into lists on the device, each long run
+// with a contiguous range of chunk slots and of tree nodes.  Each block takes
+// a contiguous range of runs in passes of 256; a pass places its runs by
+// block scans and takes its list ranges with one atomic per counter (the
+// lists' order across blocks is arbitrary; every run is independent).
 __global__ void __launch_bounds__(256)
     classify_kernel(const uint32_t* __restrict__ run_pairs, uint32_t* __restrict__ counters,
                     uint32_t* __restrict__ long_run, uint32_t* __restrict__ long_chunk0,
                     uint32_t* __restrict__ long_tree0, uint32_t* __restrict__ medium_run) {
+  __shared__ uint32_t sm32[33];
+  __shared__ unsigned long long sm64[33];
+  __shared__ uint32_t base[4];
   const uint32_t R = counters[kCntRuns];
-  const uint32_t stride = gridDim.x * blockDim.x;
-  // whole warps iterate together (the medium list takes one atomic per warp)
-  const uint32_t R_up = (R + 31u) & ~31u;
-  for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < R_up; j += stride) {
-    const uint32_t SL = j < R ? run_pairs[j + 1] - run_pairs[j] : 0u;
+  const uint32_t per_block = ((R + gridDim.x - 1) / gridDim.x + 255u) & ~255u;
+  const uint32_t j0 = blockIdx.x * per_block;
+  const uint32_t j1 = j0 + per_block < R ? j0 + per_block : R;
+  for (uint32_t jb = j0; jb < j1; jb += 256) {  // uniform over the block
+    const uint32_t j = jb + threadIdx.x;
+    const uint32_t SL = j < j1 ? run_pairs[j + 1] - run_pairs[j] : 0u;
     const bool medium = SL >= static_cast<uint32_t>(kMediumRun) &&
                         SL < static_cast<uint32_t>(kLongThreshold);
-    const unsigned mm = __ballot_sync(kFull, medium);
-    if (mm) {
-      const unsigned lane = lane_id();
-      const int leader = __ffs(mm) - 1;
-      uint32_t first = 0;
-      if (static_cast<int>(lane) == leader) first = atomicAdd(&counters[kCntMedium], __popc(mm));
-      first = __shfl_sync(kFull, first, leader);
-      if (medium) medium_run[first + __popc(mm & ((1u << lane) - 1u))] = j;
+    const bool lng = SL >= static_cast<uint32_t>(kLongThreshold);
+    const uint32_t nch = lng ? (SL + kChunk - 1) / kChunk : 0u;
+    const uint32_t nodes = lng ? static_cast<uint32_t>(tree_nodes(nch)) : 0u;
+    // medium count in the low half, long count in the high half (<= 256 each)
+    const uint32_t f = (medium ? 1u : 0u) | (lng ? 1u << 16 : 0u);
+    uint32_t ftot;
+    const uint32_t fex = block_inclusive_scan(f, OpSum(), 0u, sm32, &ftot) - f;
+    const unsigned long long c = nch | (static_cast<unsigned long long>(nodes) << 32);
+    unsigned long long ctot;
+    const unsigned long long cex = block_inclusive_scan(c, OpSum(), 0ull, sm64, &ctot) - c;
+    if (threadIdx.x == 0) {
+      base[0] = (ftot & 0xffffu) ? atomicAdd(&counters[kCntMedium], ftot & 0xffffu) : 0u;
+      base[1] = (ftot >> 16) ? atomicAdd(&counters[kCntLong], ftot >> 16) : 0u;
+      base[2] = static_cast<uint32_t>(ctot)
+                    ? atomicAdd(&counters[kCntChunks], static_cast<uint32_t>(ctot)) : 0u;
+      base[3] = static_cast<uint32_t>(ctot >> 32)
+                    ? atomicAdd(&counters[kCntTree], static_cast<uint32_t>(ctot >> 32)) : 0u;
     }
-    if (SL >= static_cast<uint32_t>(kLongThreshold)) {
-      const uint32_t nch = (SL + kChunk - 1) / kChunk;
-      const uint32_t slot = atomicAdd(&counters[kCntLong], 1u);
+    __syncthreads();
+    if (medium) medium_run[base[0] + (fex & 0xffffu)] = j;
+    if (lng) {
+      const uint32_t slot = base[1] + (fex >> 16);
       long_run[slot] = j;
-      long_chunk0[slot] = atomicAdd(&counters[kCntChunks], nch);
-      long_tree0[slot] = atomicAdd(&counters[kCntTree], static_cast<uint32_t>(tree_nodes(nch)));
+      long_chunk0[slot] = base[2] + static_cast<uint32_t>(cex);
+      long_tree0[slot] = base[3] + static_cast<uint32_t>(cex >> 32);
     }
+    __syncthreads();  // base is rewritten by the next pass
   }
 }
 
