@@ -775,6 +775,9 @@ __global__ void __launch_bounds__(kRleThreads)
                      uint32_t* __restrict__ run_pairs, uint32_t* __restrict__ pair_starts,
                      uint32_t* __restrict__ pair_bags, uint32_t* __restrict__ counters) {
   __shared__ uint32_t sm[33];
+  // the tile's pairs and runs, in order, before their coalesced write-out
+  __shared__ uint32_t s_pstart[kRleTile], s_pbag[kRleTile];
+  __shared__ uint32_t s_ukey[kRleTile], s_rstart[kRleTile], s_rpair[kRleTile];
   const int64_t n = geom_n(g);
   int64_t b, e;
   cta_range(g, n, &b, &e);
@@ -799,18 +802,18 @@ __global__ void __launch_bounds__(kRleThreads)
     uint32_t total;
     const uint32_t inc = block_inclusive_scan(c, OpSum(), 0u, sm, &total);
     const uint32_t exc = inc - c;
-    uint32_t rr = r + (exc >> 16);
-    uint32_t pp = p + (exc & 0xffffu);
+    uint32_t rr = exc >> 16;      // within the tile
+    uint32_t pp = exc & 0xffffu;
 #pragma unroll
     for (int j = 0; j < kRleItems; ++j) {
       const int64_t i = i0 + j;
       if (it.pair_head[j]) {
-        pair_starts[pp] = static_cast<uint32_t>(i);
-        pair_bags[pp] = it.b[j];
+        s_pstart[pp] = static_cast<uint32_t>(i);
+        s_pbag[pp] = it.b[j];
         if (it.run_head[j]) {
-          unique_keys[rr] = it.k[j];
-          run_starts[rr] = static_cast<uint32_t>(i);
-          run_pairs[rr] = pp;
+          s_ukey[rr] = it.k[j];
+          s_rstart[rr] = static_cast<uint32_t>(i);
+          s_rpair[rr] = p + pp;
           ++rr;
         }
         ++pp;
@@ -830,8 +833,20 @@ __global__ void __launch_bounds__(kRleThreads)
         }
       }
     }
-    r += total >> 16;
-    p += total & 0xffffu;
+    __syncthreads();
+    const uint32_t nr = total >> 16, np = total & 0xffffu;
+    for (uint32_t k = threadIdx.x; k < np; k += kRleThreads) {
+      pair_starts[p + k] = s_pstart[k];
+      pair_bags[p + k] = s_pbag[k];
+    }
+    for (uint32_t k = threadIdx.x; k < nr; k += kRleThreads) {
+      unique_keys[r + k] = s_ukey[k];
+      run_starts[r + k] = s_rstart[k];
+      run_pairs[r + k] = s_rpair[k];
+    }
+    __syncthreads();  // the staging arrays are rewritten by the next tile
+    r += nr;
+    p += np;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     counters[kCntRuns] = R;
