@@ -349,8 +349,11 @@ __device__ __forceinline__ void warp_run(const UpdArgs& a, const Meta& m, int t,
 
 // Medium runs (kMediumRun <= pairs < kLongThreshold, listed by the
 // preprocess): one warp per run.
-template <bool kWeighted>
-__global__ void __launch_bounds__(256, 2) medium_runs_kernel(UpdArgs a, const uint32_t* __restrict__ medium_run) {
+// kNarrow: every table of the launch is at most 128 wide (one vector per
+// lane), so the wider paths, which set the register budget, are left out.
+template <bool kWeighted, bool kNarrow>
+__global__ void __launch_bounds__(256, kNarrow ? 3 : 2)
+    medium_runs_kernel(UpdArgs a, const uint32_t* __restrict__ medium_run) {
   __shared__ MetaSmem msm;
   const Meta m = load_meta(a, msm, true);
   const uint32_t nmed = a.counters[kCntMedium];
@@ -372,7 +375,7 @@ __global__ void __launch_bounds__(256, 2) medium_runs_kernel(UpdArgs a, const ui
     if (nv <= 4) warp_run<4, 1, kWeighted>(a, m, t, p0, np, key);
     else if (nv <= 8) warp_run<8, 1, kWeighted>(a, m, t, p0, np, key);
     else if (nv <= 16) warp_run<16, 1, kWeighted>(a, m, t, p0, np, key);
-    else if (nv <= 32) warp_run<32, 1, kWeighted>(a, m, t, p0, np, key);
+    else if (kNarrow || nv <= 32) warp_run<32, 1, kWeighted>(a, m, t, p0, np, key);
     else if (nv <= 64) warp_run<32, 2, kWeighted>(a, m, t, p0, np, key);
     else if (nv <= 128) warp_run<32, 4, kWeighted>(a, m, t, p0, np, key);
     else warp_run<32, 8, kWeighted>(a, m, t, p0, np, key);
@@ -959,8 +962,16 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   if (weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   else { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   const uint32_t* medium = reinterpret_cast<const uint32_t*>(ws + W.medium_run);
-  if (weighted) { probe_begin(TBE_PROBE_MEDIUM_RUNS, L.s); medium_runs_kernel<true><<<blocks, 256, 0, L.s>>>(a, medium); note_launch(); probe_end(TBE_PROBE_MEDIUM_RUNS, L.s); }
-  else { probe_begin(TBE_PROBE_MEDIUM_RUNS, L.s); medium_runs_kernel<false><<<blocks, 256, 0, L.s>>>(a, medium); note_launch(); probe_end(TBE_PROBE_MEDIUM_RUNS, L.s); }
+  {
+    const bool narrow = d->max_D <= 128;
+    probe_begin(TBE_PROBE_MEDIUM_RUNS, L.s);
+    if (weighted && narrow) medium_runs_kernel<true, true><<<blocks, 256, 0, L.s>>>(a, medium);
+    else if (weighted) medium_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a, medium);
+    else if (narrow) medium_runs_kernel<false, true><<<blocks, 256, 0, L.s>>>(a, medium);
+    else medium_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a, medium);
+    note_launch();
+    probe_end(TBE_PROBE_MEDIUM_RUNS, L.s);
+  }
   if (wide && weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   if (wide && !weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   if (weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, false><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
