@@ -284,32 +284,55 @@ def run_native(args, world, rank, local):
     if not args.no_e2e:
         # End to end through the public API: per step, this step's inputs go
         # host -> device from pinned memory and the pooled output comes back.
+        # Two device input slots: step k+1's uploads (copy stream) overlap
+        # step k's compute, and step k's output download (a third stream)
+        # overlaps its backward; every copy stays inside the timed region.
         h_idx = w.indices.cpu().pin_memory()
         h_off = w.offsets.cpu().pin_memory()
         h_grad = w.grad_out.cpu().pin_memory()
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        d_idx, d_off, d_grad = (torch.empty_like(w.indices), torch.empty_like(w.offsets),
-                                torch.empty_like(w.grad_out))
+        slots = [(torch.empty_like(w.indices), torch.empty_like(w.offsets),
+                  torch.empty_like(w.grad_out)) for _ in range(2)]
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        copied = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
+        fwd_done, out_read = torch.cuda.Event(), torch.cuda.Event()
 
-        def e2e_step():
-            d_idx.copy_(h_idx, non_blocking=True)
-            d_off.copy_(h_off, non_blocking=True)
-            d_grad.copy_(h_grad, non_blocking=True)
+        def e2e_step(k):
+            d_idx, d_off, d_grad = slots[k % 2]
+            with torch.cuda.stream(up):
+                if k >= 2:
+                    up.wait_event(consumed[k % 2])
+                d_idx.copy_(h_idx, non_blocking=True)
+                d_off.copy_(h_off, non_blocking=True)
+                d_grad.copy_(h_grad, non_blocking=True)
+                copied[k % 2].record(up)
+            stream.wait_event(copied[k % 2])
+            if k >= 1:
+                stream.wait_event(out_read)  # the previous output was read back
             tbe.tbe_preprocess(desc, d_idx, d_off, None, ws)
             tbe.tbe_forward(desc, weights, d_idx, d_off, None, out, ws, PRE)
+            fwd_done.record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(fwd_done)
+                h_out.copy_(out, non_blocking=True)
+                out_read.record(down)
             tbe.tbe_backward_rowwise_adagrad(desc, d_grad, d_idx, d_off, None, weights, momentum,
                                              w.lr, w.eps, ws, PRE)
-            h_out.copy_(out, non_blocking=True)
+            consumed[k % 2].record(stream)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        for k in range(max(1, args.warmup)):
+            e2e_step(k)
         torch.cuda.synchronize()
         barrier(world)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        up.wait_event(a)
+        down.wait_event(a)
+        for k in range(args.steps):
+            e2e_step(k + 2 * args.warmup)  # the slot pattern continues past the warm-up
+        stream.wait_event(out_read)
         b.record(stream)
         torch.cuda.synchronize()
         barrier(world)
