@@ -182,9 +182,10 @@ tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indic
  * runs into short and long with the long-run task list compacted on the
  * device.  Hot rows: the workspace keeps, per table, up to hot_slots rows
  * chosen by the previous backward on it (none at first); lookups of those
- * rows are not sorted but summed per bag into a histogram (counts, or sums of
- * per-sample weights), and the remaining (cold) lookups are also kept per bag
- * in lookup order.  Results stay in the workspace (see tbe_workspace_view); a
+ * rows are not sorted but summed per bag into a histogram (counts, stored as
+ * bytes for every 128-bag tile whose counts all fit one; otherwise, and for
+ * sums of per-sample weights, fp32 with a per-bag power-of-two scale), and
+ * the remaining (cold) lookups are also kept per bag in lookup order.  Results stay in the workspace (see tbe_workspace_view); a
  * later tbe_forward or tbe_backward_rowwise_adagrad with TBE_F_PREPROCESSED
  * consumes them.  The sort chain runs on a stream of the library's own, so
  * that a forward enqueued next runs concurrently with it; the library's
@@ -210,8 +211,8 @@ tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* of
  * fp32 sums whose rounding order differs, so a row's result can differ in the
  * last bits between a call where it is hot and one where it is cold.  The call
  * then chooses the next hot set: per table, the most looked-up rows of this
- * batch with at least max(B/8, 32) lookups (tables with D_t <= 256 only, and
- * only while T * hot_slots * B * 4 bytes stay within 2 GiB).
+ * batch with at least max(B/64, 32) lookups (tables with D_t <= 256 only, and
+ * only while the histograms, T * hot_slots * B * 5 bytes, stay within 2 GiB).
  * No host synchronisation, no device-to-host copy.  Errors as tbe_forward. */
 tbe_status tbe_backward_rowwise_adagrad(const tbe_desc* d, const float* grad_out,
                                         const void* indices, const void* offsets, int64_t n,
