@@ -193,6 +193,29 @@ def forward_problem_bytes(w, rows_touched):
             + w.B * int(w.D.sum()) * 4)
 
 
+def problem_roofline(w, rows_touched, r, peak):
+    """Compulsory bytes of the forward, the backward and the whole step (each
+    index and offset read once, every distinct row once, the output written
+    once, grad_out read once, each touched row's weights and momentum read and
+    written once) over their measured time, against the HBM peak.  The
+    preprocess reads the indices for both passes, so its time counts in both."""
+    nb = w.T * w.B
+    D = int(w.D[0])
+    idx = w.n * INDEX_BYTES + (nb + 1) * INDEX_BYTES
+    out = w.B * int(w.D.sum()) * 4
+    fwd = idx + rows_touched * D * 2 + out
+    bwd = idx + out + rows_touched * (4 * D + 8)  # grad_out has the output's size
+    step = idx + 2 * out + rows_touched * (4 * D + 8)
+    t = {"forward": r["pre_ms"] + r["fwd_ms"], "backward": r["pre_ms"] + r["upd_ms"],
+         "step": r["ms"] / r["steps"]}
+    res = {}
+    for k, b in (("forward", fwd), ("backward", bwd), ("step", step)):
+        gbs = b / (t[k] / 1e3) / 1e9
+        res[k] = {"min_bytes": b, "ms": t[k], "GBps": gbs, "frac": gbs / peak}
+    res["note"] = "compulsory bytes over time; preprocess time counted in forward and backward"
+    return res
+
+
 def run_native(args, world, rank, local):
     import table_embedding_bag_gb300 as tbe
     import workloads
@@ -455,6 +478,7 @@ def main():
                                "long_runs": r["n_long"]}},
         "forward_context": {"phase_ms": r["fwd_ms"],
                             "problem_min_GBps": fwd_problem / (r["fwd_ms"] / 1e3) / 1e9},
+        "problem_roofline": problem_roofline(w, r["R"] + r["n_hot"], dict(r, steps=args.steps), hbm),
         "clocks": r["clocks"],
         "gpu_launches": r["launches"],
     }
