@@ -45,14 +45,15 @@ def _load():
         lib.oracle_half_to_double.restype = ctypes.c_double
         lib.oracle_double_to_half.argtypes = [ctypes.c_double]
         lib.oracle_double_to_half.restype = ctypes.c_uint16
-        lib.oracle_forward.argtypes = [i32, i32, P, P, P, P, i32, P, P, i64, P, P]
+        lib.oracle_forward.argtypes = [i32, i32, P, P, P, P, i32, P, P, i64, P, i32, P]
         lib.oracle_pool_gathered.argtypes = [i64, i32, P, P, P, P]
         lib.oracle_preprocess.argtypes = [i32, i32, P, i32, P, P, i64, P, P, P, P, P, P, P]
-        lib.oracle_row_gradients.argtypes = [i32, i32, P, P, i32, P, P, i64, P, P, i32, P, P, P]
+        lib.oracle_row_gradients.argtypes = [i32, i32, P, P, i32, P, P, i64, P, P, i32, i32, P,
+                                             P, P]
         lib.oracle_backward_rowwise_adagrad.argtypes = [i32, i32, P, P, P, i32, P, P, i64, P, P,
-                                                        f32, f32, P, P]
-        lib.oracle_backward_selected.argtypes = [i32, i32, P, P, i32, P, P, i64, P, P, f32, f32,
-                                                 i64, P, i32, P, P, P]
+                                                        i32, f32, f32, P, P]
+        lib.oracle_backward_selected.argtypes = [i32, i32, P, P, i32, P, P, i64, P, P, i32, f32,
+                                                 f32, i64, P, i32, P, P, P]
         lib.oracle_repair_offsets.argtypes = [i32, P, i64, i64, P]
         lib.oracle_repair_offsets.restype = i64
         _lib = lib
@@ -101,8 +102,9 @@ class Tables:
         self.w_offsets = np.concatenate([[0], np.cumsum(self.E * self.D)]).astype(np.int64)
 
 
-def forward(tables: Tables, B, weights, indices, offsets, psw=None):
-    """Pooled forward; returns fp32 [B, sum D]."""
+def forward(tables: Tables, B, weights, indices, offsets, psw=None, mean=False):
+    """Pooled forward; returns fp32 [B, sum D].  mean: each bag's sum times
+    1/L for its L > 1 lookups (HugeCTR's mean combiner)."""
     lib = _load()
     indices, offsets, bits = _idx(indices, offsets)
     w = np.ascontiguousarray(weights, dtype=np.float16).view(np.uint16)
@@ -110,7 +112,7 @@ def forward(tables: Tables, B, weights, indices, offsets, psw=None):
     out = np.zeros((B, int(tables.D_offsets[-1])), dtype=np.float32)
     rc = lib.oracle_forward(tables.T, B, _p(tables.D_offsets), _p(tables.hash_base),
                             _p(tables.w_offsets), _p(w), bits, _p(indices), _p(offsets),
-                            len(indices), _p(psw), _p(out))
+                            len(indices), _p(psw), int(bool(mean)), _p(out))
     _check(rc, "forward")
     return out
 
@@ -149,8 +151,9 @@ def preprocess(tables: Tables, B, indices, offsets):
                 unique_keys=uk[:R], run_starts=rs[:R + 1])
 
 
-def row_gradients(tables: Tables, B, indices, offsets, grad_out, psw=None):
-    """Summed gradient (double) of every touched row: (keys[R], g[R, maxD])."""
+def row_gradients(tables: Tables, B, indices, offsets, grad_out, psw=None, mean=False):
+    """Summed gradient (double) of every touched row: (keys[R], g[R, maxD]).
+    mean: each bag's gradient times 1/L for its L > 1 lookups, before grouping."""
     lib = _load()
     indices, offsets, bits = _idx(indices, offsets)
     n = len(indices)
@@ -161,16 +164,17 @@ def row_gradients(tables: Tables, B, indices, offsets, grad_out, psw=None):
     grad_out = _c(grad_out, np.float32)
     psw = _c(psw, np.float32)
     rc = lib.oracle_row_gradients(tables.T, B, _p(tables.D_offsets), _p(tables.hash_base), bits,
-                                  _p(indices), _p(offsets), n, _p(psw), _p(grad_out), maxD,
-                                  _p(keys), _p(g), _p(R))
+                                  _p(indices), _p(offsets), n, _p(psw), _p(grad_out),
+                                  int(bool(mean)), maxD, _p(keys), _p(g), _p(R))
     _check(rc, "row_gradients")
     R = int(R[0])
     return keys[:R], g[:R]
 
 
 def backward_rowwise_adagrad(tables: Tables, B, indices, offsets, grad_out, weights, momentum,
-                             lr, eps, psw=None):
-    """Returns (new_weights fp16, new_momentum fp32); inputs are not modified."""
+                             lr, eps, psw=None, mean=False):
+    """Returns (new_weights fp16, new_momentum fp32); inputs are not modified.
+    mean: each bag's gradient times 1/L for its L > 1 lookups, before grouping."""
     lib = _load()
     indices, offsets, bits = _idx(indices, offsets)
     w = np.array(weights, dtype=np.float16, copy=True)
@@ -180,14 +184,14 @@ def backward_rowwise_adagrad(tables: Tables, B, indices, offsets, grad_out, weig
     rc = lib.oracle_backward_rowwise_adagrad(tables.T, B, _p(tables.D_offsets),
                                              _p(tables.hash_base), _p(tables.w_offsets), bits,
                                              _p(indices), _p(offsets), len(indices), _p(psw),
-                                             _p(grad_out), float(lr), float(eps),
-                                             _p(w.view(np.uint16)), _p(m))
+                                             _p(grad_out), int(bool(mean)), float(lr),
+                                             float(eps), _p(w.view(np.uint16)), _p(m))
     _check(rc, "backward")
     return w, m
 
 
 def backward_selected(tables: Tables, B, indices, offsets, grad_out, lr, eps, sel_keys, w_rows,
-                      m_rows, psw=None):
+                      m_rows, psw=None, mean=False):
     """Row-wise Adagrad for selected linear keys only.
 
     w_rows [nsel, maxD] fp16 and m_rows [nsel] fp32 hold the rows' values before
@@ -203,7 +207,8 @@ def backward_selected(tables: Tables, B, indices, offsets, grad_out, lr, eps, se
     psw = _c(psw, np.float32)
     rc = lib.oracle_backward_selected(tables.T, B, _p(tables.D_offsets), _p(tables.hash_base),
                                       bits, _p(indices), _p(offsets), len(indices), _p(psw),
-                                      _p(grad_out), float(lr), float(eps), len(sel), _p(sel),
+                                      _p(grad_out), int(bool(mean)), float(lr), float(eps),
+                                      len(sel), _p(sel),
                                       maxD, _p(w.view(np.uint16)), _p(m), _p(cnt))
     _check(rc, "backward_selected")
     return w, m, cnt

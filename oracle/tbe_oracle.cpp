@@ -23,6 +23,13 @@
 //    square root.  The row-wise form replaces the element-wise accumulator
 //    increment g_d^2 by the row mean (1/D) sum_d g_d^2.
 //
+//  * same HugeCTR page, the combiner note (sum, or mean = the sum kernel then
+//    a scaling kernel) and the mean backward kernel: with mean pooling a
+//    bag's gradient is multiplied by 1/L, L the bag's number of lookups by
+//    the row offsets, when L > 1, before the regrouping.  The forward scaling
+//    kernel is not printed: the oracle takes the plainest reading, the pooled
+//    sum times the same factor.
+//
 // Readings where the pages are silent (each is listed in the design notes):
 //  * bags are table-major: bag (t,b) has id t*B+b, offsets has T*B+1 entries;
 //  * a lookup whose row is outside [0, E_t) contributes nothing (skipped);
@@ -88,30 +95,35 @@ int64_t load_int(const void* p, int bits, int64_t i) {
   return static_cast<const int64_t*>(p)[i];
 }
 
-// Sum-pool one bag: out[d] = (float) sum_k coef_k * row_k[d], summed in double
-// in ascending k.  coef == nullptr means every coefficient is 1.
-void pool_rows(int64_t L, int D, const uint16_t* const* rows, const float* coef, float* out) {
+// Pool one bag: out[d] = (float) (scale * sum_k coef_k * row_k[d]), summed in
+// double in ascending k.  coef == nullptr means every coefficient is 1.
+void pool_rows(int64_t L, int D, const uint16_t* const* rows, const float* coef, float* out,
+               double scale = 1.0) {
   for (int d = 0; d < D; ++d) {
     double s = 0.0;
     for (int64_t k = 0; k < L; ++k) {
       const double w = coef ? static_cast<double>(coef[k]) : 1.0;
       s += w * half_bits_to_double(rows[k][d]);
     }
-    out[d] = static_cast<float>(s);
+    out[d] = static_cast<float>(s * scale);
   }
 }
 
-// Sum one run's gradient: g[d] = sum_k coef_k * grad_k[d] in double, ascending k.
-void sum_run_gradient(int64_t SL, int D, const float* const* grads, const float* coef, double* g) {
+// Sum one run's gradient: g[d] = sum_k coef_k * bag_scale_k * grad_k[d] in
+// double, ascending k (bag_scale == nullptr: every factor is 1).
+void sum_run_gradient(int64_t SL, int D, const float* const* grads, const float* coef,
+                      double* g, const double* bag_scale = nullptr) {
   for (int d = 0; d < D; ++d) {
     double s = 0.0;
     for (int64_t k = 0; k < SL; ++k) {
-      const double w = coef ? static_cast<double>(coef[k]) : 1.0;
+      double w = coef ? static_cast<double>(coef[k]) : 1.0;
+      if (bag_scale) w *= bag_scale[k];
       s += w * static_cast<double>(grads[k][d]);
     }
     g[d] = s;
   }
 }
+
 
 // Exact row-wise Adagrad on one row, given its summed gradient g[0..D):
 //   m <- m + (1/D) sum_d g_d^2          (stored as fp32)
@@ -144,6 +156,12 @@ struct Problem {
   int64_t off(int64_t bag) const { return load_int(offsets, index_bits, bag); }
   int64_t idx(int64_t i) const { return load_int(indices, index_bits, i); }
   bool valid(int t, int64_t r) const { return r >= 0 && r < E(t); }
+  // Mean pooling's factor for bag `bag`: 1/L when its L lookups (by the
+  // offsets, rows out of range included) number more than one, else 1.
+  double mean_scale(int64_t bag) const {
+    const int64_t L = off(bag + 1) - off(bag);
+    return L > 1 ? 1.0 / static_cast<double>(L) : 1.0;
+  }
 };
 
 // Offsets must satisfy 0 = o[0] <= o[1] <= ... <= o[T*B] <= n; lookups at or
@@ -159,6 +177,7 @@ bool offsets_ok(const Problem& p) {
 struct Contribution {
   int64_t pos;   // lookup position in indices[]
   uint32_t bag;  // b, the bag within its table
+  double mean_scale;  // the bag's mean-pooling factor
 };
 
 // One std::map entry per touched (table,row), keyed by the linear key
@@ -171,7 +190,8 @@ std::map<uint64_t, std::vector<Contribution>> group_by_row(const Problem& p) {
       for (int64_t i = p.off(bag); i < p.off(bag + 1); ++i) {
         const int64_t r = p.idx(i);
         if (!p.valid(t, r)) continue;
-        runs[static_cast<uint64_t>(p.hash_base[t] + r)].push_back({i, static_cast<uint32_t>(b)});
+        runs[static_cast<uint64_t>(p.hash_base[t] + r)].push_back(
+            {i, static_cast<uint32_t>(b), p.mean_scale(bag)});
       }
     }
   }
@@ -199,7 +219,7 @@ uint16_t oracle_double_to_half(double x) { return double_to_half_bits(x); }
 int oracle_forward(int T, int B, const int64_t* D_offsets, const int64_t* hash_base,
                    const int64_t* w_offsets, const uint16_t* weights, int index_bits,
                    const void* indices, const void* offsets, int64_t n, const float* psw,
-                   float* out) {
+                   int mean, float* out) {
   Problem p{T, B, D_offsets, hash_base, w_offsets, index_bits, indices, offsets, n, psw};
   if (!offsets_ok(p)) return ORACLE_EINVAL;
   const int64_t sumD = D_offsets[T];
@@ -218,7 +238,7 @@ int oracle_forward(int T, int B, const int64_t* D_offsets, const int64_t* hash_b
         coef.push_back(psw ? psw[i] : 1.0f);
       }
       pool_rows(static_cast<int64_t>(rows.size()), D, rows.data(), coef.data(),
-                out + b * sumD + D_offsets[t]);
+                out + b * sumD + D_offsets[t], mean ? p.mean_scale(bag) : 1.0);
     }
   }
   return ORACLE_OK;
@@ -291,12 +311,12 @@ int oracle_preprocess(int T, int B, const int64_t* hash_base, int index_bits,
 }
 
 // Summed gradient of every touched row, in ascending key order:
-// g[j*maxD + d] = sum over the run's lookups i of psw_i * grad_out[b_i, D_offsets[t]+d]
-// (double).  keys[j] receives the run's linear key.  Sized for n runs.
+// g[j*maxD + d] = sum over the run's lookups i of psw_i * s_i * grad_out[b_i, D_offsets[t]+d]
+// (double; s_i the bag's mean-pooling factor when mean != 0, else 1).  keys[j] receives the run's linear key.  Sized for n runs.
 int oracle_row_gradients(int T, int B, const int64_t* D_offsets, const int64_t* hash_base,
                          int index_bits, const void* indices, const void* offsets, int64_t n,
-                         const float* psw, const float* grad_out, int maxD, uint32_t* keys,
-                         double* g, int64_t* R_out) {
+                         const float* psw, const float* grad_out, int mean, int maxD,
+                         uint32_t* keys, double* g, int64_t* R_out) {
   Problem p{T, B, D_offsets, hash_base, nullptr, index_bits, indices, offsets, n, psw};
   if (!offsets_ok(p)) return ORACLE_EINVAL;
   const int64_t sumD = D_offsets[T];
@@ -304,18 +324,22 @@ int oracle_row_gradients(int T, int B, const int64_t* D_offsets, const int64_t* 
   int64_t j = 0;
   std::vector<const float*> gp;
   std::vector<float> coef;
+  std::vector<double> bs;  // the lookups' bag factors (mean pooling)
   for (const auto& kv : runs) {
     const int t = table_of_key(p, kv.first);
     const int D = static_cast<int>(p.D(t));
     gp.clear();
     coef.clear();
+    bs.clear();
     for (const Contribution& c : kv.second) {
       gp.push_back(grad_out + static_cast<int64_t>(c.bag) * sumD + D_offsets[t]);
       coef.push_back(psw ? psw[c.pos] : 1.0f);
+      bs.push_back(c.mean_scale);
     }
     keys[j] = static_cast<uint32_t>(kv.first);
     std::fill(g + j * maxD, g + (j + 1) * maxD, 0.0);
-    sum_run_gradient(static_cast<int64_t>(gp.size()), D, gp.data(), coef.data(), g + j * maxD);
+    sum_run_gradient(static_cast<int64_t>(gp.size()), D, gp.data(), coef.data(), g + j * maxD,
+                     mean ? bs.data() : nullptr);
     ++j;
   }
   *R_out = j;
@@ -328,13 +352,15 @@ int oracle_backward_rowwise_adagrad(int T, int B, const int64_t* D_offsets,
                                     const int64_t* hash_base, const int64_t* w_offsets,
                                     int index_bits, const void* indices, const void* offsets,
                                     int64_t n, const float* psw, const float* grad_out,
-                                    float lr, float eps, uint16_t* weights, float* momentum) {
+                                    int mean, float lr, float eps, uint16_t* weights,
+                                    float* momentum) {
   Problem p{T, B, D_offsets, hash_base, w_offsets, index_bits, indices, offsets, n, psw};
   if (!offsets_ok(p)) return ORACLE_EINVAL;
   const int64_t sumD = D_offsets[T];
   auto runs = group_by_row(p);
   std::vector<const float*> gp;
   std::vector<float> coef;
+  std::vector<double> bs;  // the lookups' bag factors (mean pooling)
   std::vector<double> g;
   for (const auto& kv : runs) {
     const int t = table_of_key(p, kv.first);
@@ -342,12 +368,15 @@ int oracle_backward_rowwise_adagrad(int T, int B, const int64_t* D_offsets,
     const int64_t r = static_cast<int64_t>(kv.first) - hash_base[t];
     gp.clear();
     coef.clear();
+    bs.clear();
     for (const Contribution& c : kv.second) {
       gp.push_back(grad_out + static_cast<int64_t>(c.bag) * sumD + D_offsets[t]);
       coef.push_back(psw ? psw[c.pos] : 1.0f);
+      bs.push_back(c.mean_scale);
     }
     g.assign(D, 0.0);
-    sum_run_gradient(static_cast<int64_t>(gp.size()), D, gp.data(), coef.data(), g.data());
+    sum_run_gradient(static_cast<int64_t>(gp.size()), D, gp.data(), coef.data(), g.data(),
+                     mean ? bs.data() : nullptr);
     rowwise_adagrad(D, g.data(), lr, eps, weights + w_offsets[t] + r * D, momentum + kv.first);
   }
   return ORACLE_OK;
@@ -360,8 +389,9 @@ int oracle_backward_rowwise_adagrad(int T, int B, const int64_t* D_offsets,
 // contrib_out[j] (nullable) receives each selected row's run length.
 int oracle_backward_selected(int T, int B, const int64_t* D_offsets, const int64_t* hash_base,
                              int index_bits, const void* indices, const void* offsets, int64_t n,
-                             const float* psw, const float* grad_out, float lr, float eps,
-                             int64_t nsel, const uint32_t* sel_keys, int maxD, uint16_t* w_rows,
+                             const float* psw, const float* grad_out, int mean, float lr,
+                             float eps, int64_t nsel, const uint32_t* sel_keys, int maxD,
+                             uint16_t* w_rows,
                              float* m_rows, int64_t* contrib_out) {
   Problem p{T, B, D_offsets, hash_base, nullptr, index_bits, indices, offsets, n, psw};
   if (!offsets_ok(p)) return ORACLE_EINVAL;
@@ -376,11 +406,13 @@ int oracle_backward_selected(int T, int B, const int64_t* D_offsets, const int64
         const int64_t r = p.idx(i);
         if (!p.valid(t, r)) continue;
         auto it = slot.find(static_cast<uint64_t>(hash_base[t] + r));
-        if (it != slot.end()) lists[it->second].push_back({i, static_cast<uint32_t>(b)});
+        if (it != slot.end())
+          lists[it->second].push_back({i, static_cast<uint32_t>(b), p.mean_scale(bag)});
       }
     }
   std::vector<const float*> gp;
   std::vector<float> coef;
+  std::vector<double> bs;  // the lookups' bag factors (mean pooling)
   std::vector<double> g;
   for (int64_t j = 0; j < nsel; ++j) {
     if (contrib_out) contrib_out[j] = static_cast<int64_t>(lists[j].size());
@@ -390,12 +422,15 @@ int oracle_backward_selected(int T, int B, const int64_t* D_offsets, const int64
     const int D = static_cast<int>(p.D(t));
     gp.clear();
     coef.clear();
+    bs.clear();
     for (const Contribution& c : lists[j]) {
       gp.push_back(grad_out + static_cast<int64_t>(c.bag) * sumD + D_offsets[t]);
       coef.push_back(psw ? psw[c.pos] : 1.0f);
+      bs.push_back(c.mean_scale);
     }
     g.assign(D, 0.0);
-    sum_run_gradient(static_cast<int64_t>(gp.size()), D, gp.data(), coef.data(), g.data());
+    sum_run_gradient(static_cast<int64_t>(gp.size()), D, gp.data(), coef.data(), g.data(),
+                     mean ? bs.data() : nullptr);
     rowwise_adagrad(D, g.data(), lr, eps, w_rows + j * maxD, m_rows + j);
   }
   return ORACLE_OK;

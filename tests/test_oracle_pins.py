@@ -359,3 +359,90 @@ def test_oracle_rejects_bad_offsets(oracle_lib):
     with pytest.raises(ValueError):
         oracle.forward(tab, 2, np.zeros(32, np.float16), np.zeros(3, np.int64),
                        np.array([0, 2, 1], np.int64))
+
+
+# -------------------------------------------------------------- mean pooling
+# HugeCTR page, combiner note and mean backward kernel: with mean pooling a
+# bag of L > 1 lookups is scaled by 1/L (L by the row offsets), bags of 0 or 1
+# lookups are not scaled, and the backward scales the bag's gradient before
+# the regrouping.
+def test_mean_forward_of_identical_rows_is_the_row(oracle_lib):
+    tab = oracle.Tables([6], [8])
+    rng = np.random.default_rng(21)
+    W = rng.normal(0, 1, 48).astype(np.float16)
+    bags = [[3] * 7, [5], [], [0, 0, 0, 0]]
+    idx = np.array([r for b in bags for r in b], np.int64)
+    off = np.concatenate([[0], np.cumsum([len(b) for b in bags])]).astype(np.int64)
+    out = oracle.forward(tab, 4, W, idx, off, mean=True)
+    row = lambda r: W[r * 8:(r + 1) * 8].astype(np.float32)
+    # 7 copies summed in double then divided by 7: the row exactly
+    assert np.array_equal(out[0], row(3))
+    assert np.array_equal(out[1], row(5))        # L = 1: unscaled
+    assert np.array_equal(out[2], np.zeros(8, np.float32))
+    assert np.array_equal(out[3], row(0))
+    # and the sum pooling of the same bags is L times larger
+    s = oracle.forward(tab, 4, W, idx, off)
+    assert np.array_equal(s[0], (7 * W[24:32].astype(np.float64)).astype(np.float32))
+
+
+def test_mean_counts_out_of_range_lookups_in_L(oracle_lib):
+    # a bag [r, invalid] has L = 2: its mean is half the row; the invalid
+    # lookup adds nothing but still counts
+    tab = oracle.Tables([4], [8])
+    W = np.arange(32, dtype=np.float16) / 8
+    idx = np.array([1, 9], np.int64)
+    off = np.array([0, 2], np.int64)
+    out = oracle.forward(tab, 1, W, idx, off, mean=True)
+    assert np.array_equal(out[0], (W[8:16].astype(np.float64) / 2).astype(np.float32))
+
+
+@pytest.mark.parametrize("L", [1, 2, 5, 64])
+def test_mean_backward_of_one_bag_equals_the_single_lookup_update(oracle_lib, L):
+    # one bag of L lookups of one row: the row's gradient is L * g / L = g,
+    # the update of a single (sum-pooled) lookup of that row
+    D = 16
+    rng = np.random.default_rng(L)
+    g = rng.normal(0, 1, D).astype(np.float32)
+    w0 = rng.normal(0, 0.1, D).astype(np.float16)
+    tab = oracle.Tables([3], [D])
+    W = np.zeros(3 * D, np.float16)
+    W[D:2 * D] = w0
+    m = np.full(3, 0.25, np.float32)
+    G = g.reshape(1, D)
+    W1, m1 = oracle.backward_rowwise_adagrad(tab, 1, np.array([1] * L, np.int64),
+                                             np.array([0, L], np.int64), G, W, m, 0.05, 1e-8,
+                                             mean=True)
+    W2, m2 = oracle.backward_rowwise_adagrad(tab, 1, np.array([1], np.int64),
+                                             np.array([0, 1], np.int64), G, W, m, 0.05, 1e-8)
+    if L in (1, 2, 64):  # L * (g / L) is exact for powers of two
+        assert np.array_equal(W1, W2) and np.array_equal(m1, m2)
+    else:
+        assert np.allclose(m1, m2, rtol=1e-6)
+        assert np.max(np.abs(W1.astype(np.float64) - W2.astype(np.float64))) <= \
+            np.max(np.spacing(np.abs(W2.astype(np.float16)))).astype(np.float64)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_mean_gradients_equal_sum_gradients_of_scaled_grad_out(oracle_lib, seed):
+    # scaling each bag's grad_out row by its L and pooling with mean gives the
+    # sum-pooling gradients (L a power of two: every product exact)
+    rng = np.random.default_rng(40 + seed)
+    E, D, B = [9, 5], [8, 16], 6
+    T = 2
+    lens = rng.choice([0, 1, 2, 4, 8], size=T * B)
+    idx = np.concatenate([rng.integers(0, E[t], int(lens[t * B + b]))
+                          for t in range(T) for b in range(B)]).astype(np.int64)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    tab = oracle.Tables(E, D)
+    G = rng.normal(0, 1, (B, sum(D))).astype(np.float32)
+    Gs = G.copy()
+    for t in range(T):
+        d0 = int(tab.D_offsets[t])
+        for b in range(B):
+            L = int(lens[t * B + b])
+            if L > 1:
+                Gs[b, d0:d0 + D[t]] *= L
+    k1, g1 = oracle.row_gradients(tab, B, idx, off, Gs, mean=True)
+    k2, g2 = oracle.row_gradients(tab, B, idx, off, G)
+    assert np.array_equal(k1, k2)
+    assert np.array_equal(g1, g2)
