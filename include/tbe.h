@@ -84,9 +84,22 @@ enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3 };
                                            indices/offsets/per-sample weights (same
                                            stream); see tbe_forward for when the
                                            forward still reads the indices */
+#define TBE_F_MEAN (1u << 5)            /* forward and backward: mean pooling (the HugeCTR
+                                           page's mean combiner): a bag of L > 1 lookups
+                                           (L by the offsets, rows out of range included)
+                                           pools to its sum times 1/L, and its gradient
+                                           row is scaled by 1/L before the regrouping
+                                           (into the workspace: the backward needs one
+                                           sized with TBE_WS_MEAN); bags of 0 or 1
+                                           lookups are not scaled.  The small-table path
+                                           is not taken. */
 
 /* workspace-size flags */
 #define TBE_WS_WEIGHTED (1u << 0)       /* reserve room for per-sample weights */
+#define TBE_WS_MEAN (1u << 1)           /* reserve room for the mean-scaled gradient
+                                           (B x total_D floats, at the end of the
+                                           layout): needed by a backward with
+                                           TBE_F_MEAN */
 
 /* device status bits (tbe_read_status) */
 #define TBE_ERR_INDEX_RANGE (1 << 0)    /* a lookup's row was outside [0, E_t) */
@@ -258,9 +271,9 @@ tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits);
  * overlaps on the GPU (different streams, or several host threads) race on
  * the array: serialise them.
  *
- * Arguments as tbe_backward_rowwise_adagrad without workspace; flags may be 0
- * or TBE_F_LONG_TWO_LAUNCH (no bounds reporting: the status word lives in the
- * caller's workspace elsewhere; invalid rows are still skipped).
+ * Arguments as tbe_backward_rowwise_adagrad without workspace; flags may hold
+ * TBE_F_LONG_TWO_LAUNCH and TBE_F_MEAN (no bounds reporting: the status word
+ * lives in the caller's workspace elsewhere; invalid rows are still skipped).
  * Errors: TBE_EINVAL, TBE_EUNSUPPORTED, TBE_ETOO_LARGE, TBE_ECUDA. */
 tbe_status tbe_backward_rowwise_adagrad_noalloc(const tbe_desc* d, const float* grad_out,
                                                 const void* indices, const void* offsets,

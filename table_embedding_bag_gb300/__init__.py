@@ -23,7 +23,7 @@ __all__ = [
     "TableBatchedEmbedding", "lib_path", "tbe_backward_rowwise_adagrad_noalloc",
     "TBE_NOALLOC_SCRATCH_BYTES", "TBE_ETOO_LARGE",
     "TBE_F_CHECK_BOUNDS", "TBE_F_REPAIR_OFFSETS", "TBE_F_FORCE_GENERIC", "TBE_F_LONG_TWO_LAUNCH",
-    "TBE_F_PREPROCESSED", "TBE_WS_WEIGHTED", "TBE_ERR_INDEX_RANGE", "TBE_ERR_OFFSETS",
+    "TBE_F_PREPROCESSED", "TBE_F_MEAN", "TBE_WS_WEIGHTED", "TBE_WS_MEAN", "TBE_ERR_INDEX_RANGE", "TBE_ERR_OFFSETS",
 ]
 
 TBE_OK, TBE_EINVAL, TBE_EWORKSPACE, TBE_EUNSUPPORTED, TBE_ECUDA, TBE_ETOO_LARGE = range(6)
@@ -34,6 +34,8 @@ TBE_F_REPAIR_OFFSETS = 1 << 1
 TBE_F_FORCE_GENERIC = 1 << 2
 TBE_F_LONG_TWO_LAUNCH = 1 << 3
 TBE_F_PREPROCESSED = 1 << 4
+TBE_F_MEAN = 1 << 5
+TBE_WS_MEAN = 1 << 1
 TBE_WS_WEIGHTED = 1 << 0
 TBE_ERR_INDEX_RANGE = 1 << 0
 TBE_ERR_OFFSETS = 1 << 1
@@ -166,18 +168,21 @@ class TBEDesc:
         return ctypes.byref(self.c)
 
 
-def tbe_workspace_size(desc: TBEDesc, n_max: int, weighted: bool = False) -> int:
+def tbe_workspace_size(desc: TBEDesc, n_max: int, weighted: bool = False,
+                       mean: bool = False) -> int:
     out = ctypes.c_size_t(0)
+    ws_flags = (TBE_WS_WEIGHTED if weighted else 0) | (TBE_WS_MEAN if mean else 0)
     _ok("tbe_workspace_size", _load().tbe_workspace_size(
-        desc.ref, int(n_max), TBE_WS_WEIGHTED if weighted else 0, ctypes.byref(out)))
+        desc.ref, int(n_max), ws_flags, ctypes.byref(out)))
     return out.value
 
 
 class Workspace:
     """Device workspace for calls with at most n_max lookups."""
 
-    def __init__(self, desc: TBEDesc, n_max: int, weighted: bool = False, device="cuda"):
-        self.nbytes = tbe_workspace_size(desc, n_max, weighted)
+    def __init__(self, desc: TBEDesc, n_max: int, weighted: bool = False, device="cuda",
+                 mean: bool = False):
+        self.nbytes = tbe_workspace_size(desc, n_max, weighted, mean)
         self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
         self.weighted = weighted
 

@@ -184,6 +184,8 @@ struct WsLayout {
   size_t hot_scale;    // int8 [T*B] wide tiles: histogram row x 2^scale peaks below 2^15
   size_t tile_kind;    // uint8 [hot_tiles] kTileBytes / kTileWide / kTileNoHot
   size_t cold_off;     // uint32 [T*B + 1] first cold-list entry of each bag
+  size_t inv_len;      // float [T*B] mean pooling's factor per bag: 1/L for L > 1 lookups, else 1
+                       // (written by mean-mode calls before their use)
   size_t hot_part;     // float [T][hot_parts][kHot][kHotMaxD] partial hot gradients
   size_t bag_cold;     // uint32 [T*B] cold lookups per bag
   size_t tile_cold;    // uint32 [hot_tiles + 1] cold lookups per expand tile, then prefix
@@ -193,6 +195,7 @@ struct WsLayout {
   size_t sel_n;        // uint32 [T]
   size_t offsets_fix;  // index type [T*B+1] repaired offsets
   size_t fix_scratch;  // int64 [blocks] block maxima for the repair scan
+  size_t grad_mean;    // float [B][total_D] mean-scaled gradient (TBE_WS_MEAN only; last)
   size_t total;
   int64_t max_long, max_chunks, max_tree, max_medium;
   int64_t hot_tiles;   // expand CTAs: T * ceil(B / kHotTileBags)

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256, TBE_FWD_MINB)
                            const int64_t* __restrict__ w_offsets,
                            const IndexT* __restrict__ indices, const IndexT* __restrict__ offsets,
                            const float* __restrict__ psw, int64_t n, int T, int B,
-                           int64_t total_D, float* __restrict__ out, int* status) {
+                           int64_t total_D, float* __restrict__ out, int* status, bool mean) {
   const int warps = blockDim.x >> 5;
   const int64_t nbags = static_cast<int64_t>(T) * B;
   for (int64_t bag = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5); bag < nbags;
@@ -44,22 +44,24 @@ __global__ void __launch_bounds__(256, TBE_FWD_MINB)
     const __half* Wt = W + __ldg(w_offsets + t);
     int64_t s, e;
     bag_range(offsets, bag, n, &s, &e);
+    // mean pooling: the sum times 1/L for L > 1 lookups
+    const float scale = mean && e - s > 1 ? 1.f / static_cast<float>(e - s) : 1.f;
     float* orow = out + b * total_D + d0;
     const int nvec = D >> 3;
     if (nvec <= 1)
-      pool_bag<1, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status);
+      pool_bag<1, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else if (nvec <= 2)
-      pool_bag<2, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status);
+      pool_bag<2, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else if (nvec <= 4)
-      pool_bag<4, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status);
+      pool_bag<4, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else if (nvec <= 8)
-      pool_bag<8, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status);
+      pool_bag<8, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else if (nvec <= 16)
-      pool_bag<16, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status);
+      pool_bag<16, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else
       for (int vec0 = 0; vec0 < nvec; vec0 += 32)
         pool_bag<32, IndexT, kWeighted>(Wt, E, rbase, D, vec0, indices, psw, s, e, orow, mode,
-                                          status);
+                                          status, scale);
   }
 }
 
@@ -77,7 +79,8 @@ __global__ void __launch_bounds__(256, TBE_FWD_MINB)
                         const int64_t* __restrict__ hash_base, const int64_t* __restrict__ w_offsets,
                         const uint32_t* __restrict__ keys, const uint32_t* __restrict__ cold_off,
                         const float* __restrict__ psw, int T, int B, int64_t total_D,
-                        float* __restrict__ out, const uint32_t* __restrict__ hot_n) {
+                        float* __restrict__ out, const uint32_t* __restrict__ hot_n,
+                        const float* __restrict__ inv_len) {
   constexpr int G = 32 / S;
   constexpr int U = S < TBE_FWD_UNROLL ? S : TBE_FWD_UNROLL;
   const int lane = static_cast<int>(lane_id());
@@ -168,11 +171,30 @@ __global__ void __launch_bounds__(256, TBE_FWD_MINB)
         p += S;
       }
       if (col_ok) {
+        if (inv_len) {  // mean pooling: this kernel writes every bag last
+          const float sc = __ldg(inv_len + bag);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] *= sc;
+        }
         float4* o = reinterpret_cast<float4*>(orow + vec * 8);
         __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
         __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
       }
     }
+  }
+}
+
+// Mean pooling's factor of every bag, from its offsets clamped as every
+// kernel reads them: 1/L for L > 1 lookups (rows out of range included), else 1.
+template <typename IndexT>
+__global__ void __launch_bounds__(256)
+    mean_factor_kernel(const IndexT* __restrict__ offsets, int64_t nbags, int64_t n,
+                       float* __restrict__ inv_len) {
+  for (int64_t bag = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; bag < nbags;
+       bag += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int64_t s, e;
+    bag_range(offsets, bag, n, &s, &e);
+    inv_len[bag] = e - s > 1 ? 1.f / static_cast<float>(e - s) : 1.f;
   }
 }
 
@@ -264,7 +286,8 @@ __global__ void __launch_bounds__(kFixThreads)
 
 template <typename IndexT>
 cudaError_t launch_forward_t(const Launch& L, const __half* W, const IndexT* indices,
-                             const IndexT* offsets, const float* psw, float* out, int* status) {
+                             const IndexT* offsets, const float* psw, float* out, int* status,
+                             bool mean) {
   const tbe_desc* d = L.d;
   const int64_t nbags = static_cast<int64_t>(d->T) * d->B;
   const int warps = 8;
@@ -274,11 +297,11 @@ cudaError_t launch_forward_t(const Launch& L, const __half* W, const IndexT* ind
   if (psw)
     { forward_generic_kernel<IndexT, true><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
         W, d->D_offsets, d->hash_base, d->weights_offsets, indices, offsets, psw, L.n, d->T,
-        d->B, d->total_D, out, status); note_launch(); }
+        d->B, d->total_D, out, status, mean); note_launch(); }
   else
     { forward_generic_kernel<IndexT, false><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
         W, d->D_offsets, d->hash_base, d->weights_offsets, indices, offsets, psw, L.n, d->T,
-        d->B, d->total_D, out, status); note_launch(); }
+        d->B, d->total_D, out, status, mean); note_launch(); }
   return cudaGetLastError();
 }
 
@@ -304,19 +327,19 @@ cudaError_t launch_offsets_t(const Launch& L, const IndexT* offsets, bool repair
 
 cudaError_t launch_forward_generic(const Launch& L, const void* weights, const void* indices,
                                    const void* offsets, const float* psw, float* out,
-                                   int* status) {
+                                   int* status, bool mean) {
   const __half* W = static_cast<const __half*>(weights);
   if (L.d->index_dtype == TBE_DT_I32)
     return launch_forward_t<int32_t>(L, W, static_cast<const int32_t*>(indices),
-                                     static_cast<const int32_t*>(offsets), psw, out, status);
+                                     static_cast<const int32_t*>(offsets), psw, out, status, mean);
   return launch_forward_t<int64_t>(L, W, static_cast<const int64_t*>(indices),
-                                   static_cast<const int64_t*>(offsets), psw, out, status);
+                                   static_cast<const int64_t*>(offsets), psw, out, status, mean);
 }
 
 template <int S>
 cudaError_t launch_cold_s(const Launch& L, const __half* W, const uint32_t* keys,
                           const uint32_t* cold_off, const float* psw, float* out,
-                          const uint32_t* hot_n) {
+                          const uint32_t* hot_n, const float* inv_len) {
   const tbe_desc* d = L.d;
   const int64_t tasks = (static_cast<int64_t>(d->T) * d->B + (32 / S) - 1) / (32 / S);
   const int warps = 8;
@@ -326,25 +349,40 @@ cudaError_t launch_cold_s(const Launch& L, const __half* W, const uint32_t* keys
   if (psw)
     { probe_begin(TBE_PROBE_FORWARD_COLD, L.s); forward_cold_kernel<S, true><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
         W, d->D_offsets, d->hash_base, d->weights_offsets, keys, cold_off, psw, d->T, d->B,
-        d->total_D, out, hot_n); note_launch(); probe_end(TBE_PROBE_FORWARD_COLD, L.s); }
+        d->total_D, out, hot_n, inv_len); note_launch(); probe_end(TBE_PROBE_FORWARD_COLD, L.s); }
   else
     { probe_begin(TBE_PROBE_FORWARD_COLD, L.s); forward_cold_kernel<S, false><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
         W, d->D_offsets, d->hash_base, d->weights_offsets, keys, cold_off, psw, d->T, d->B,
-        d->total_D, out, hot_n); note_launch(); probe_end(TBE_PROBE_FORWARD_COLD, L.s); }
+        d->total_D, out, hot_n, inv_len); note_launch(); probe_end(TBE_PROBE_FORWARD_COLD, L.s); }
   return cudaGetLastError();
 }
 
 cudaError_t launch_forward_cold(const Launch& L, const void* weights, const uint32_t* cold_keys,
                                 const uint32_t* cold_off, const float* cold_psw, float* out,
-                                const uint32_t* hot_n) {
+                                const uint32_t* hot_n, const float* inv_len) {
   const __half* W = static_cast<const __half*>(weights);
   const int64_t nvec = L.d->max_D / 8;  // lanes per row for the widest table
-  if (nvec <= 1) return launch_cold_s<1>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
-  if (nvec <= 2) return launch_cold_s<2>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
-  if (nvec <= 4) return launch_cold_s<4>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
-  if (nvec <= 8) return launch_cold_s<8>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
-  if (nvec <= 16) return launch_cold_s<16>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
-  return launch_cold_s<32>(L, W, cold_keys, cold_off, cold_psw, out, hot_n);
+  if (nvec <= 1) return launch_cold_s<1>(L, W, cold_keys, cold_off, cold_psw, out, hot_n, inv_len);
+  if (nvec <= 2) return launch_cold_s<2>(L, W, cold_keys, cold_off, cold_psw, out, hot_n, inv_len);
+  if (nvec <= 4) return launch_cold_s<4>(L, W, cold_keys, cold_off, cold_psw, out, hot_n, inv_len);
+  if (nvec <= 8) return launch_cold_s<8>(L, W, cold_keys, cold_off, cold_psw, out, hot_n, inv_len);
+  if (nvec <= 16) return launch_cold_s<16>(L, W, cold_keys, cold_off, cold_psw, out, hot_n, inv_len);
+  return launch_cold_s<32>(L, W, cold_keys, cold_off, cold_psw, out, hot_n, inv_len);
+}
+
+cudaError_t launch_mean_factors(const Launch& L, const void* offsets, float* inv_len) {
+  const int64_t nbags = static_cast<int64_t>(L.d->T) * L.d->B;
+  int64_t blocks = (nbags + 255) / 256;
+  if (blocks > 8LL * L.num_sms) blocks = 8LL * L.num_sms;
+  if (blocks < 1) blocks = 1;
+  if (L.d->index_dtype == TBE_DT_I32)
+    mean_factor_kernel<int32_t><<<static_cast<unsigned>(blocks), 256, 0, L.s>>>(
+        static_cast<const int32_t*>(offsets), nbags, L.n, inv_len);
+  else
+    mean_factor_kernel<int64_t><<<static_cast<unsigned>(blocks), 256, 0, L.s>>>(
+        static_cast<const int64_t*>(offsets), nbags, L.n, inv_len);
+  note_launch();
+  return cudaGetLastError();
 }
 
 int64_t repair_scratch_blocks(int64_t nb1) { return (nb1 + kFixTile - 1) / kFixTile; }

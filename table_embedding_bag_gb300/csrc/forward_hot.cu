@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
 }  // namespace
 
 cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, const void* weights,
-                               const float* psw, float* out) {
+                               const float* psw, float* out, bool mean) {
   const tbe_desc* d = L.d;
   const uint32_t* hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_cur));
   if (W.hot_enabled) {
@@ -685,7 +685,8 @@ cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, con
   return launch_forward_cold(L, weights, reinterpret_cast<const uint32_t*>(ws + W.keys[2]),
                              reinterpret_cast<const uint32_t*>(ws + W.cold_off),
                              psw ? reinterpret_cast<const float*>(ws + W.psw[2]) : nullptr, out,
-                             W.hot_enabled ? hot_n : nullptr);
+                             W.hot_enabled ? hot_n : nullptr,
+                             mean ? reinterpret_cast<const float*>(ws + W.inv_len) : nullptr);
 }
 
 }  // namespace tbe

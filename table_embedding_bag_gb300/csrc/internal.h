@@ -46,12 +46,15 @@ struct Launch {
 // forward.cu
 cudaError_t launch_forward_generic(const Launch& L, const void* weights, const void* indices,
                                    const void* offsets, const float* psw, float* out,
-                                   int* status);
+                                   int* status, bool mean);
 // The generic kernel over tbe_preprocess's per-bag cold lists (linear keys);
-// with hot_n, bags of tables with hot rows are added to out.
+// with hot_n, bags of tables with hot rows are added to out; with inv_len
+// (mean pooling) every bag's result is scaled by its factor.
 cudaError_t launch_forward_cold(const Launch& L, const void* weights, const uint32_t* cold_keys,
                                 const uint32_t* cold_off, const float* cold_psw, float* out,
-                                const uint32_t* hot_n);
+                                const uint32_t* hot_n, const float* inv_len);
+// Mean pooling's per-bag factors (1/L for L > 1 lookups, else 1) into inv_len.
+cudaError_t launch_mean_factors(const Launch& L, const void* offsets, float* inv_len);
 cudaError_t launch_check_offsets(const Launch& L, const void* offsets, bool repair, void* fixed,
                                  int64_t* scratch, int* status);
 int64_t repair_scratch_blocks(int64_t nb1);
@@ -64,7 +67,7 @@ cudaError_t launch_forward_small(const Launch& L, const void* weights, const voi
 // forward_hot.cu: forward from tbe_preprocess's results (hot rows on the
 // tensor cores, cold lookups gathered).
 cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, const void* weights,
-                               const float* psw, float* out);
+                               const float* psw, float* out, bool mean);
 
 // preprocess.cu: expand, radix sort, run-length encode, classify.
 cudaError_t launch_preprocess(const Launch& L, const WsLayout& W, char* ws, const void* indices,
@@ -78,5 +81,9 @@ cudaError_t launch_hot_grad(const Launch& L, const WsLayout& W, char* ws, const 
 // update.cu: short-run and long-run row-wise Adagrad.
 cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const float* grad_out,
                           void* weights, float* momentum, float lr, float eps, bool two_launch);
+// Mean pooling's backward input: out[b, D_off[t] + c] = grad_out[b, D_off[t] + c]
+// times bag (t, b)'s factor from inv_len.
+cudaError_t launch_scale_grad(const Launch& L, const float* grad_out, const float* inv_len,
+                              float* out);
 
 }  // namespace tbe

@@ -80,8 +80,10 @@ extern "C" tbe_status tbe_backward_rowwise_adagrad_noalloc(
   if (!grad_out || !weights || !momentum) return TBE_EINVAL;
   if ((reinterpret_cast<uintptr_t>(grad_out) & 15u) || (reinterpret_cast<uintptr_t>(weights) & 15u))
     return TBE_EINVAL;
-  if (flags & ~TBE_F_LONG_TWO_LAUNCH) return TBE_EINVAL;
-  const WsLayout W = make_layout(d, n, per_sample_weights ? TBE_WS_WEIGHTED : 0u);
+  if (flags & ~(TBE_F_LONG_TWO_LAUNCH | TBE_F_MEAN)) return TBE_EINVAL;
+  const bool mean = (flags & TBE_F_MEAN) != 0;
+  const WsLayout W = make_layout(d, n, (per_sample_weights ? TBE_WS_WEIGHTED : 0u) |
+                                           (mean ? TBE_WS_MEAN : 0u));
   if (W.total > TBE_NOALLOC_SCRATCH_BYTES) return TBE_ETOO_LARGE;
   char* scratch = scratch_ptr();
   if (!scratch) return TBE_ECUDA;
@@ -97,6 +99,15 @@ extern "C" tbe_status tbe_backward_rowwise_adagrad_noalloc(
     return TBE_ECUDA;
   cudaError_t e = launch_preprocess(L, W, scratch, indices, offsets, per_sample_weights, false);
   if (e != cudaSuccess) return TBE_ECUDA;
+  if (mean) {
+    float* inv_len = reinterpret_cast<float*>(scratch + W.inv_len);
+    float* scaled = reinterpret_cast<float*>(scratch + W.grad_mean);
+    e = launch_mean_factors(L, offsets, inv_len);
+    if (e != cudaSuccess) return TBE_ECUDA;
+    e = launch_scale_grad(L, grad_out, inv_len, scaled);
+    if (e != cudaSuccess) return TBE_ECUDA;
+    grad_out = scaled;
+  }
   e = launch_update(L, W, scratch, grad_out, weights, momentum, lr, eps,
                     (flags & TBE_F_LONG_TWO_LAUNCH) != 0);
   return e == cudaSuccess ? TBE_OK : TBE_ECUDA;

@@ -30,7 +30,7 @@ __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t 
                                          int D, int vec0, const IndexT* __restrict__ indices,
                                          const float* __restrict__ psw, int64_t start,
                                          int64_t end, float* __restrict__ out_row, int mode,
-                                         int* status) {
+                                         int* status, float scale = 1.f) {
   constexpr int G = 32 / S;
   constexpr int U = S < kUnroll ? S : kUnroll;  // row vectors in flight per lane
   const int lane = static_cast<int>(lane_id());
@@ -104,6 +104,9 @@ __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t 
       acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
       acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
     }
+    if (scale != 1.f)  // mean pooling
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] *= scale;
     // written once, not read back: evict first
     __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
     __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));

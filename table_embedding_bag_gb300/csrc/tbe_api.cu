@@ -129,6 +129,7 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   L.hot_scale = take(static_cast<size_t>(T) * B);
   L.bag_cold = take(static_cast<size_t>(T) * B * 4);
   L.cold_off = take((static_cast<size_t>(T) * B + 1) * 4);
+  L.inv_len = take(static_cast<size_t>(T) * B * 4);
   L.tile_cold = take((L.hot_tiles + 1) * 4);
   L.sel_hist = take(T * kHotBuckets * 4);
   L.sel_thresh = take(T * 4);
@@ -137,6 +138,8 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   const int64_t nb1 = T * B + 1;
   L.offsets_fix = take(nb1 * index_bytes(d));
   L.fix_scratch = take(repair_scratch_blocks(nb1) * sizeof(int64_t));
+  // last, so layouts with and without it agree on every other offset
+  L.grad_mean = (ws_flags & TBE_WS_MEAN) ? take(static_cast<size_t>(B) * d->total_D * 4) : 0;
   L.total = off;
   return L;
 }
@@ -199,14 +202,15 @@ tbe_status run_checks(const Launch& L, const WsLayout& W, char* ws, const void* 
 }
 
 tbe_status common_args(const tbe_desc* d, const void* indices, const void* offsets, int64_t n,
-                       void* workspace, size_t ws_bytes, bool weighted, WsLayout* W) {
+                       void* workspace, size_t ws_bytes, bool weighted, WsLayout* W,
+                       bool mean = false) {
   tbe_status st = check_desc(d);
   if (st != TBE_OK) return st;
   st = check_n(n);
   if (st != TBE_OK) return st;
   if (!offsets || (n > 0 && !indices)) return TBE_EINVAL;
   if (!workspace || !aligned16(workspace)) return TBE_EWORKSPACE;
-  *W = make_layout(d, n, weighted ? TBE_WS_WEIGHTED : 0u);
+  *W = make_layout(d, n, (weighted ? TBE_WS_WEIGHTED : 0u) | (mean ? TBE_WS_MEAN : 0u));
   if (ws_bytes < W->total) return TBE_EWORKSPACE;
   return TBE_OK;
 }
@@ -246,17 +250,24 @@ tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indic
   char* ws = static_cast<char*>(workspace);
   // The preprocessed path pays off when a bag holds enough lookups for its
   // hot rows to matter; shorter bags are pooled straight from the indices.
-  if (pre && n >= static_cast<int64_t>(kHotFwdMinBagLen) * d->T * d->B)
-    return from_cuda(launch_forward_hot(L, W, ws, weights, per_sample_weights, out));
+  const bool mean = (flags & TBE_F_MEAN) != 0;
+  if (pre && n >= static_cast<int64_t>(kHotFwdMinBagLen) * d->T * d->B) {
+    if (mean) {
+      st = from_cuda(launch_mean_factors(L, offsets, reinterpret_cast<float*>(ws + W.inv_len)));
+      if (st != TBE_OK) return st;
+    }
+    return from_cuda(launch_forward_hot(L, W, ws, weights, per_sample_weights, out, mean));
+  }
   const void* off_eff;
   int* status;
   st = run_checks(L, W, ws, offsets, flags, &off_eff, &status);
   if (st != TBE_OK) return st;
-  if (!(flags & TBE_F_FORCE_GENERIC) && small_table_eligible(d, n, per_sample_weights != nullptr))
+  if (!(flags & TBE_F_FORCE_GENERIC) && !mean &&
+      small_table_eligible(d, n, per_sample_weights != nullptr))
     return from_cuda(launch_forward_small(L, weights, indices, off_eff, out, status,
                                           reinterpret_cast<int*>(ws + W.status)));
   return from_cuda(
-      launch_forward_generic(L, weights, indices, off_eff, per_sample_weights, out, status));
+      launch_forward_generic(L, weights, indices, off_eff, per_sample_weights, out, status, mean));
 }
 
 tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* offsets, int64_t n,
@@ -282,21 +293,32 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_desc* d, const float* grad_out
                                         float* momentum, float lr, float eps, void* workspace,
                                         size_t ws_bytes, void* stream, uint32_t flags) {
   WsLayout W;
+  const bool mean = (flags & TBE_F_MEAN) != 0;
   tbe_status st = common_args(d, indices, offsets, n, workspace, ws_bytes,
-                              per_sample_weights != nullptr, &W);
+                              per_sample_weights != nullptr, &W, mean);
   if (st != TBE_OK) return st;
   if (!grad_out || !weights || !momentum || !aligned16(grad_out) || !aligned16(weights))
     return TBE_EINVAL;
   const Launch L{d, n, static_cast<cudaStream_t>(stream), device_sms()};
   char* ws = static_cast<char*>(workspace);
+  const void* off_eff = offsets;
   if (!(flags & TBE_F_PREPROCESSED)) {
-    const void* off_eff;
     int* status;
     st = run_checks(L, W, ws, offsets, flags, &off_eff, &status);
     if (st != TBE_OK) return st;
     st = from_cuda(launch_preprocess(L, W, ws, indices, off_eff, per_sample_weights,
                                      status != nullptr));
     if (st != TBE_OK) return st;
+  }
+  if (mean) {
+    // each bag's gradient row times its factor, as the bags' gradients
+    float* inv_len = reinterpret_cast<float*>(ws + W.inv_len);
+    float* scaled = reinterpret_cast<float*>(ws + W.grad_mean);
+    st = from_cuda(launch_mean_factors(L, off_eff, inv_len));
+    if (st != TBE_OK) return st;
+    st = from_cuda(launch_scale_grad(L, grad_out, inv_len, scaled));
+    if (st != TBE_OK) return st;
+    grad_out = scaled;
   }
   return from_cuda(launch_update(L, W, ws, grad_out, weights, momentum, lr, eps,
                                  (flags & TBE_F_LONG_TWO_LAUNCH) != 0));

@@ -894,6 +894,29 @@ __global__ void __launch_bounds__(kHot)
   }
 }
 
+// Mean pooling's backward input (the HugeCTR page's mean backward step): the
+// gradient row of bag (t, b) times the bag's factor, 1/L for L > 1 lookups,
+// before the regrouping.  Grid: x over the table's B x D_t/4 vectors, y = t.
+__global__ void __launch_bounds__(256)
+    scale_grad_kernel(const float* __restrict__ grad, const float* __restrict__ inv_len,
+                      const int64_t* __restrict__ D_offsets, int B, int64_t total_D,
+                      float* __restrict__ out) {
+  const int t = blockIdx.y;
+  const int64_t d0 = D_offsets[t];
+  const int nv = static_cast<int>((D_offsets[t + 1] - d0) >> 2);
+  const int64_t nvec = static_cast<int64_t>(B) * nv;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t b = i / nv;
+    const int v = static_cast<int>(i - b * nv);
+    const float sc = __ldg(inv_len + static_cast<int64_t>(t) * B + b);
+    const int64_t at = b * total_D + d0 + v * 4;
+    float4 g = ldg_f4(grad + at);
+    g.x *= sc; g.y *= sc; g.z *= sc; g.w *= sc;
+    *reinterpret_cast<float4*>(out + at) = g;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const float* grad_out,
@@ -1007,6 +1030,21 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
       reinterpret_cast<uint32_t*>(ws + W.hot_n(W.hot_next)),
       reinterpret_cast<uint32_t*>(ws + W.hot_m1(W.hot_next)),
       reinterpret_cast<uint32_t*>(ws + W.hot_m2(W.hot_next))); note_launch(); }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_grad(const Launch& L, const float* grad_out, const float* inv_len,
+                              float* out) {
+  const tbe_desc* d = L.d;
+  const int64_t vecs = static_cast<int64_t>(d->B) * (d->max_D / 4);
+  int64_t bx = (vecs + 255) / 256;
+  const int64_t cap = 8LL * L.num_sms;
+  if (bx > cap) bx = cap;
+  if (bx < 1) bx = 1;
+  if (d->T > 65535) return cudaErrorInvalidConfiguration;
+  scale_grad_kernel<<<dim3(static_cast<unsigned>(bx), static_cast<unsigned>(d->T)), 256, 0, L.s>>>(
+      grad_out, inv_len, d->D_offsets, d->B, d->total_D, out);
+  note_launch();
   return cudaGetLastError();
 }
 

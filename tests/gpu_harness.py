@@ -31,10 +31,10 @@ def host(w):
 class Run:
     """One TBE problem on the GPU through the C ABI."""
 
-    def __init__(self, w, device="cuda"):
+    def __init__(self, w, device="cuda", mean=False):
         self.w = w
         self.desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, device)
-        self.ws = tbe.Workspace(self.desc, max(w.n, 1), w.psw is not None, device)
+        self.ws = tbe.Workspace(self.desc, max(w.n, 1), w.psw is not None, device, mean=mean)
         d = lambda x: None if x is None else x.to(device).contiguous()
         self.indices, self.offsets, self.psw = d(w.indices), d(w.offsets), d(w.psw)
         self.weights = d(w.weights).clone()
