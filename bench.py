@@ -50,6 +50,8 @@ def parse():
                    help="bags of table 0 in the CPU-oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--pooling", choices=["sum", "mean"], default="sum",
+                   help="pooling mode of the step (the recorded workload is sum)")
     # smaller variants of the hot-row recipe, for profiling captures only
     p.add_argument("--tables", type=int, default=None)
     p.add_argument("--rows", type=int, default=None)
@@ -224,12 +226,13 @@ def run_native(args, world, rank, local):
     E_scale = None if args.rows is None else args.rows / workloads.SPECS["hot"].E
     w = workloads.make("hot", device=dev, seed=rank, T=args.tables, B=args.bags, E_scale=E_scale)
     desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, dev)
-    ws = tbe.Workspace(desc, w.n, False, dev)
+    mean = args.pooling == "mean"
+    ws = tbe.Workspace(desc, w.n, False, dev, mean=mean)
     weights, momentum = w.weights, w.momentum
     out = torch.empty(w.B, desc.total_D, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    PRE = tbe.TBE_F_PREPROCESSED
+    PRE = tbe.TBE_F_PREPROCESSED | (tbe.TBE_F_MEAN if mean else 0)
 
     def step(ev=None):
         # one preprocess of the batch's indices serves forward and backward
@@ -455,8 +458,10 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD if (args.tables, args.rows, args.bags) == (None,) * 3 else
-                   f"reduced hot-row recipe T={w.T} E={int(w.E[0])} B={w.B} (profiling case)",
+        "config": {"workload": (WORKLOAD if (args.tables, args.rows, args.bags) == (None,) * 3 else
+                                f"reduced hot-row recipe T={w.T} E={int(w.E[0])} B={w.B} "
+                                "(profiling case)") +
+                               (", mean pooling" if args.pooling == "mean" else ""),
                    "n_lookups": w.n, "global_batch": w.B * world,
                    "parallelism": f"replicas x{world} (independent batches)",
                    "l2": f"inputs larger than L2 (indices {w.n * INDEX_BYTES / 1e9:.2f} GB, "
