@@ -45,13 +45,17 @@ def _load():
         lib.oracle_half_to_double.restype = ctypes.c_double
         lib.oracle_double_to_half.argtypes = [ctypes.c_double]
         lib.oracle_double_to_half.restype = ctypes.c_uint16
-        lib.oracle_forward.argtypes = [i32, i32, P, P, P, P, i32, P, P, i64, P, i32, P]
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_forward.argtypes = [i32, i32, P, P, P, P, i32, P, P, i64, P, i32, i32, P]
         lib.oracle_pool_gathered.argtypes = [i64, i32, P, P, P, P]
         lib.oracle_preprocess.argtypes = [i32, i32, P, i32, P, P, i64, P, P, P, P, P, P, P]
         lib.oracle_row_gradients.argtypes = [i32, i32, P, P, i32, P, P, i64, P, P, i32, i32, P,
                                              P, P]
         lib.oracle_backward_rowwise_adagrad.argtypes = [i32, i32, P, P, P, i32, P, P, i64, P, P,
-                                                        i32, f32, f32, P, P]
+                                                        i32, i32, f32, f32, P, P]
         lib.oracle_backward_selected.argtypes = [i32, i32, P, P, i32, P, P, i64, P, P, i32, f32,
                                                  f32, i64, P, i32, P, P, P]
         lib.oracle_repair_offsets.argtypes = [i32, P, i64, i64, P]
@@ -81,6 +85,14 @@ def _check(rc, what):
         raise ValueError(f"oracle {what}: invalid input (status {rc})")
 
 
+def bf16_to_double(h: int) -> float:
+    return _load().oracle_bf16_to_double(h)
+
+
+def double_to_bf16(x: float) -> int:
+    return _load().oracle_double_to_bf16(x)
+
+
 def half_to_double(h: int) -> float:
     return _load().oracle_half_to_double(int(h))
 
@@ -102,17 +114,26 @@ class Tables:
         self.w_offsets = np.concatenate([[0], np.cumsum(self.E * self.D)]).astype(np.int64)
 
 
-def forward(tables: Tables, B, weights, indices, offsets, psw=None, mean=False):
+def _weight_bits(weights, bf16):
+    """16-bit weight patterns: fp16 values (numpy float16), or, with bf16,
+    bfloat16 bit patterns given as uint16."""
+    if bf16:
+        return np.ascontiguousarray(weights, dtype=np.uint16), 1
+    return np.ascontiguousarray(weights, dtype=np.float16).view(np.uint16), 0
+
+
+def forward(tables: Tables, B, weights, indices, offsets, psw=None, mean=False, bf16=False):
     """Pooled forward; returns fp32 [B, sum D].  mean: each bag's sum times
-    1/L for its L > 1 lookups (HugeCTR's mean combiner)."""
+    1/L for its L > 1 lookups (HugeCTR's mean combiner).  bf16: weights are
+    bfloat16 bit patterns (uint16)."""
     lib = _load()
     indices, offsets, bits = _idx(indices, offsets)
-    w = np.ascontiguousarray(weights, dtype=np.float16).view(np.uint16)
+    w, wtype = _weight_bits(weights, bf16)
     psw = _c(psw, np.float32)
     out = np.zeros((B, int(tables.D_offsets[-1])), dtype=np.float32)
     rc = lib.oracle_forward(tables.T, B, _p(tables.D_offsets), _p(tables.hash_base),
                             _p(tables.w_offsets), _p(w), bits, _p(indices), _p(offsets),
-                            len(indices), _p(psw), int(bool(mean)), _p(out))
+                            len(indices), _p(psw), int(bool(mean)), wtype, _p(out))
     _check(rc, "forward")
     return out
 
@@ -172,20 +193,21 @@ def row_gradients(tables: Tables, B, indices, offsets, grad_out, psw=None, mean=
 
 
 def backward_rowwise_adagrad(tables: Tables, B, indices, offsets, grad_out, weights, momentum,
-                             lr, eps, psw=None, mean=False):
-    """Returns (new_weights fp16, new_momentum fp32); inputs are not modified.
-    mean: each bag's gradient times 1/L for its L > 1 lookups, before grouping."""
+                             lr, eps, psw=None, mean=False, bf16=False):
+    """Returns (new_weights, new_momentum fp32); inputs are not modified.
+    mean: each bag's gradient times 1/L for its L > 1 lookups, before grouping.
+    bf16: weights (in and out) are bfloat16 bit patterns (uint16), else fp16."""
     lib = _load()
     indices, offsets, bits = _idx(indices, offsets)
-    w = np.array(weights, dtype=np.float16, copy=True)
+    w = np.array(weights, dtype=np.uint16 if bf16 else np.float16, copy=True)
     m = np.array(momentum, dtype=np.float32, copy=True)
     grad_out = _c(grad_out, np.float32)
     psw = _c(psw, np.float32)
     rc = lib.oracle_backward_rowwise_adagrad(tables.T, B, _p(tables.D_offsets),
                                              _p(tables.hash_base), _p(tables.w_offsets), bits,
                                              _p(indices), _p(offsets), len(indices), _p(psw),
-                                             _p(grad_out), int(bool(mean)), float(lr),
-                                             float(eps), _p(w.view(np.uint16)), _p(m))
+                                             _p(grad_out), int(bool(mean)), int(bool(bf16)),
+                                             float(lr), float(eps), _p(w.view(np.uint16)), _p(m))
     _check(rc, "backward")
     return w, m
 

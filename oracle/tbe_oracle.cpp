@@ -33,7 +33,7 @@
 // Readings where the pages are silent (each is listed in the design notes):
 //  * bags are table-major: bag (t,b) has id t*B+b, offsets has T*B+1 entries;
 //  * a lookup whose row is outside [0, E_t) contributes nothing (skipped);
-//  * weights are fp16, rounded to nearest-even from the double result;
+//  * weights are fp16 (or bf16), rounded to nearest-even from the double result;
 //  * momentum is fp32, rounded from the double sum m_old + mean_d(g_d^2).
 //
 // Parity pins for every function live in tests/test_oracle_*.py.
@@ -90,6 +90,55 @@ uint16_t double_to_half_bits(double x) {
   return sign | static_cast<uint16_t>(((e + 15) << 10) | (static_cast<int>(q) - 1024));
 }
 
+// --------------------------------------------------------------- bf16 bits
+// bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits -- the
+// upper half of a binary32.
+double bf16_bits_to_double(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int expo = (h >> 7) & 0xff;
+  const int frac = h & 0x7f;
+  double v;
+  if (expo == 0) {
+    v = std::ldexp(static_cast<double>(frac), -133);  // subnormal: frac * 2^-133
+  } else if (expo == 255) {
+    v = frac ? NAN : INFINITY;
+  } else {
+    v = std::ldexp(static_cast<double>(128 + frac), expo - 134);
+  }
+  return sign ? -v : v;
+}
+
+// Round a double to the nearest bfloat16, ties to even.
+uint16_t double_to_bf16_bits(double x) {
+  if (std::isnan(x)) return 0x7fc0;
+  const uint16_t sign = std::signbit(x) ? 0x8000 : 0;
+  const double a = std::fabs(x);
+  if (a == 0.0) return sign;
+  if (a < std::ldexp(1.0, -126)) {
+    // subnormal range, unit 2^-133; q == 128 is the smallest normal 0x0080
+    const double q = std::nearbyint(std::ldexp(a, 133));
+    return sign | static_cast<uint16_t>(q);
+  }
+  int e2;
+  std::frexp(a, &e2);
+  int e = e2 - 1;                                    // a in [2^e, 2^(e+1))
+  double q = std::nearbyint(std::ldexp(a, 7 - e));   // in [128, 256]
+  if (q == 256.0) {
+    q = 128.0;
+    e += 1;
+  }
+  if (e + 127 >= 255) return sign | 0x7f80;          // overflow to infinity
+  return sign | static_cast<uint16_t>(((e + 127) << 7) | (static_cast<int>(q) - 128));
+}
+
+// The weights' element type: 0 fp16, 1 bf16.
+double weight_to_double(uint16_t h, int wtype) {
+  return wtype ? bf16_bits_to_double(h) : half_bits_to_double(h);
+}
+uint16_t double_to_weight(double x, int wtype) {
+  return wtype ? double_to_bf16_bits(x) : double_to_half_bits(x);
+}
+
 int64_t load_int(const void* p, int bits, int64_t i) {
   if (bits == 32) return static_cast<const int32_t*>(p)[i];
   return static_cast<const int64_t*>(p)[i];
@@ -98,12 +147,12 @@ int64_t load_int(const void* p, int bits, int64_t i) {
 // Pool one bag: out[d] = (float) (scale * sum_k coef_k * row_k[d]), summed in
 // double in ascending k.  coef == nullptr means every coefficient is 1.
 void pool_rows(int64_t L, int D, const uint16_t* const* rows, const float* coef, float* out,
-               double scale = 1.0) {
+               double scale = 1.0, int wtype = 0) {
   for (int d = 0; d < D; ++d) {
     double s = 0.0;
     for (int64_t k = 0; k < L; ++k) {
       const double w = coef ? static_cast<double>(coef[k]) : 1.0;
-      s += w * half_bits_to_double(rows[k][d]);
+      s += w * weight_to_double(rows[k][d], wtype);
     }
     out[d] = static_cast<float>(s * scale);
   }
@@ -128,15 +177,16 @@ void sum_run_gradient(int64_t SL, int D, const float* const* grads, const float*
 // Exact row-wise Adagrad on one row, given its summed gradient g[0..D):
 //   m <- m + (1/D) sum_d g_d^2          (stored as fp32)
 //   w_d <- w_d - lr * g_d / (sqrt(m) + eps)   (stored as fp16, nearest-even)
-void rowwise_adagrad(int D, const double* g, float lr, float eps, uint16_t* w, float* m) {
+void rowwise_adagrad(int D, const double* g, float lr, float eps, uint16_t* w, float* m,
+                     int wtype = 0) {
   double ss = 0.0;
   for (int d = 0; d < D; ++d) ss += g[d] * g[d];
   const float m_new = static_cast<float>(static_cast<double>(*m) + ss / static_cast<double>(D));
   *m = m_new;
   const double denom = std::sqrt(static_cast<double>(m_new)) + static_cast<double>(eps);
   for (int d = 0; d < D; ++d) {
-    const double w_old = half_bits_to_double(w[d]);
-    w[d] = double_to_half_bits(w_old - static_cast<double>(lr) * g[d] / denom);
+    const double w_old = weight_to_double(w[d], wtype);
+    w[d] = double_to_weight(w_old - static_cast<double>(lr) * g[d] / denom, wtype);
   }
 }
 
@@ -213,13 +263,15 @@ enum { ORACLE_OK = 0, ORACLE_EINVAL = 1 };
 
 double oracle_half_to_double(uint16_t h) { return half_bits_to_double(h); }
 uint16_t oracle_double_to_half(double x) { return double_to_half_bits(x); }
+double oracle_bf16_to_double(uint16_t h) { return bf16_bits_to_double(h); }
+uint16_t oracle_double_to_bf16(double x) { return double_to_bf16_bits(x); }
 
 // Pooled forward over every bag: out[b, D_offsets[t] + d] for all t, b, d.
 // out is fp32 row-major [B, D_offsets[T]].
 int oracle_forward(int T, int B, const int64_t* D_offsets, const int64_t* hash_base,
                    const int64_t* w_offsets, const uint16_t* weights, int index_bits,
                    const void* indices, const void* offsets, int64_t n, const float* psw,
-                   int mean, float* out) {
+                   int mean, int wtype, float* out) {
   Problem p{T, B, D_offsets, hash_base, w_offsets, index_bits, indices, offsets, n, psw};
   if (!offsets_ok(p)) return ORACLE_EINVAL;
   const int64_t sumD = D_offsets[T];
@@ -238,7 +290,7 @@ int oracle_forward(int T, int B, const int64_t* D_offsets, const int64_t* hash_b
         coef.push_back(psw ? psw[i] : 1.0f);
       }
       pool_rows(static_cast<int64_t>(rows.size()), D, rows.data(), coef.data(),
-                out + b * sumD + D_offsets[t], mean ? p.mean_scale(bag) : 1.0);
+                out + b * sumD + D_offsets[t], mean ? p.mean_scale(bag) : 1.0, wtype);
     }
   }
   return ORACLE_OK;
@@ -352,7 +404,7 @@ int oracle_backward_rowwise_adagrad(int T, int B, const int64_t* D_offsets,
                                     const int64_t* hash_base, const int64_t* w_offsets,
                                     int index_bits, const void* indices, const void* offsets,
                                     int64_t n, const float* psw, const float* grad_out,
-                                    int mean, float lr, float eps, uint16_t* weights,
+                                    int mean, int wtype, float lr, float eps, uint16_t* weights,
                                     float* momentum) {
   Problem p{T, B, D_offsets, hash_base, w_offsets, index_bits, indices, offsets, n, psw};
   if (!offsets_ok(p)) return ORACLE_EINVAL;
@@ -377,7 +429,8 @@ int oracle_backward_rowwise_adagrad(int T, int B, const int64_t* D_offsets,
     g.assign(D, 0.0);
     sum_run_gradient(static_cast<int64_t>(gp.size()), D, gp.data(), coef.data(), g.data(),
                      mean ? bs.data() : nullptr);
-    rowwise_adagrad(D, g.data(), lr, eps, weights + w_offsets[t] + r * D, momentum + kv.first);
+    rowwise_adagrad(D, g.data(), lr, eps, weights + w_offsets[t] + r * D, momentum + kv.first,
+                    wtype);
   }
   return ORACLE_OK;
 }

@@ -446,3 +446,78 @@ def test_mean_gradients_equal_sum_gradients_of_scaled_grad_out(oracle_lib, seed)
     k2, g2 = oracle.row_gradients(tab, B, idx, off, G)
     assert np.array_equal(k1, k2)
     assert np.array_equal(g1, g2)
+
+
+# ------------------------------------------------------------- bf16 weights
+def test_bf16_to_double_matches_torch_for_every_bit_pattern(oracle_lib):
+    torch = pytest.importorskip("torch")
+    bits = np.arange(65536, dtype=np.int64).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    got = np.array([oracle.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_double_to_bf16_matches_torch_rounding(oracle_lib):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    fin = np.arange(0, 0x7f80, dtype=np.int64).astype(np.uint16)
+    vals16 = torch.from_numpy(fin.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    mids = ((vals16[:-1].astype(np.float64) + vals16[1:]) / 2).astype(np.float32)  # exact ties
+    vals = np.concatenate([
+        vals16, mids, -mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1)),
+        rng.normal(0, 0.01, 20000).astype(np.float32), rng.normal(0, 1e30, 2000).astype(np.float32),
+        np.float32([3.3895314e38, 3.3961775e38, 3.4e38, 1e-40, 1e-45, 0.0, -0.0]),
+    ]).astype(np.float32)
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.double_to_bf16(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_forward_bf16_brute_force_exact_rational(oracle_lib, seed):
+    tab, B, idx, off, W, G, psw = _tiny_problem(seed, weighted=True, dtype=np.int64)
+    rng = np.random.default_rng(100 + seed)
+    Wb = rng.integers(0, 0x7f00, len(W)).astype(np.uint16) | \
+        (rng.integers(0, 2, len(W)).astype(np.uint16) << 15)
+    Wb &= np.uint16(0xbfff)  # keep exponents moderate (top exponent bit clear)
+    out = oracle.forward(tab, B, Wb, idx, off, psw, bf16=True)
+    exp = np.zeros_like(out, dtype=object)
+    exp[:] = Fraction(0)
+    for t, b, i, r in _lookups(tab, B, idx, off):
+        if not 0 <= r < tab.E[t]:
+            continue
+        c = Fraction(float(psw[i]))
+        base = int(tab.w_offsets[t]) + r * int(tab.D[t])
+        for d in range(int(tab.D[t])):
+            exp[b, int(tab.D_offsets[t]) + d] += c * Fraction(oracle.bf16_to_double(int(Wb[base + d])))
+    exact = np.array([[float(x) for x in row] for row in exp])
+    ulp = np.spacing(np.abs(exact).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(out.astype(np.float64) - exact) <= 0.5 * ulp + 1e-300)
+
+
+@pytest.mark.parametrize("c", [0.75, -2.5])
+def test_adagrad_bf16_constant_gradient_closed_form(oracle_lib, c):
+    torch = pytest.importorskip("torch")
+    D, lr, eps = 12, 0.01, 1e-8
+    tab = oracle.Tables([3], [D])
+    w0 = oracle.double_to_bf16(0.125)
+    W = np.zeros(3 * D, np.uint16)
+    W[D:2 * D] = w0
+    m = np.zeros(3, np.float32)
+    G = np.full((1, D), c, np.float32)
+    W2, m2 = oracle.backward_rowwise_adagrad(tab, 1, np.array([1], np.int64), np.array([0, 1]),
+                                             G, W, m, lr, eps, bf16=True)
+    c32 = np.float64(np.float32(c))
+    assert m2[1] == np.float32(c32 * c32)
+    step = 0.125 - lr * c32 / (np.sqrt(np.float64(np.float32(c32 * c32))) + eps)
+    # closed form rounded by the oracle; where the double step is an fp32
+    # value, torch's fp32 -> bf16 rounding must give the same bits
+    ref = torch.tensor([step], dtype=torch.float64).float().to(torch.bfloat16)
+    want = oracle.double_to_bf16(step)
+    assert np.all(W2[D:2 * D] == want)
+    assert np.all(W2[:D] == 0) and np.all(W2[2 * D:] == 0)
+    # the rounding agrees with torch's where the fp32 value is exact
+    if np.float64(np.float32(step)) == step:
+        assert int(ref.view(torch.int16).item()) & 0xffff == want
