@@ -68,7 +68,7 @@ typedef enum tbe_status {
 } tbe_status;
 
 /* element types */
-enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3 };
+enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3, TBE_DT_BF16 = 4 };
 
 /* call flags */
 #define TBE_F_CHECK_BOUNDS (1u << 0)    /* validate offsets (separate kernel) and indices,
@@ -113,7 +113,10 @@ enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3 };
 typedef struct tbe_desc {
   int32_t T;                        /* number of tables, >= 1 */
   int32_t B;                        /* bags per table (batch size), >= 1 */
-  int32_t weights_dtype;            /* TBE_DT_F16 */
+  int32_t weights_dtype;            /* TBE_DT_F16, or TBE_DT_BF16 (accumulated in fp32
+                                       like fp16; the tensor-core paths -- hot rows and
+                                       the small table -- are fp16 only, so bf16 tables
+                                       take the gather paths throughout) */
   int32_t index_dtype;              /* TBE_DT_I32 or TBE_DT_I64; offsets use it too */
   const int64_t* D_offsets;         /* device [T+1]: sum of D_t' for t' < t */
   const int64_t* hash_base;         /* device [T+1]: sum of E_t' for t' < t */

@@ -28,7 +28,7 @@ __all__ = [
 
 TBE_OK, TBE_EINVAL, TBE_EWORKSPACE, TBE_EUNSUPPORTED, TBE_ECUDA, TBE_ETOO_LARGE = range(6)
 TBE_NOALLOC_SCRATCH_BYTES = 32 << 20
-TBE_DT_F16, TBE_DT_I32, TBE_DT_I64 = 1, 2, 3
+TBE_DT_F16, TBE_DT_I32, TBE_DT_I64, TBE_DT_BF16 = 1, 2, 3, 4
 TBE_F_CHECK_BOUNDS = 1 << 0
 TBE_F_REPAIR_OFFSETS = 1 << 1
 TBE_F_FORCE_GENERIC = 1 << 2
@@ -135,9 +135,11 @@ def _stream(stream):
 
 class TBEDesc:
     """Problem description: per-table rows E_t and widths D_t, bags per table B,
-    index dtype.  Holds the three cumulative int64 arrays on the device."""
+    index dtype and weight dtype (torch.float16 or torch.bfloat16).  Holds the
+    three cumulative int64 arrays on the device."""
 
-    def __init__(self, E, D, B, index_dtype=torch.int64, device="cuda"):
+    def __init__(self, E, D, B, index_dtype=torch.int64, device="cuda",
+                 weights_dtype=torch.float16):
         self.E = np.asarray(E, dtype=np.int64)
         self.D = np.asarray(D, dtype=np.int64)
         if self.E.ndim != 1 or self.E.shape != self.D.shape or len(self.E) == 0:
@@ -146,6 +148,9 @@ class TBEDesc:
             raise ValueError("every D_t must be a multiple of 8 in [8, 1024]")
         self.T, self.B = len(self.E), int(B)
         self.index_dtype = index_dtype
+        if weights_dtype not in (torch.float16, torch.bfloat16):
+            raise ValueError("weights_dtype must be torch.float16 or torch.bfloat16")
+        self.weights_dtype = weights_dtype
         cum = lambda a: np.concatenate([[0], np.cumsum(a)]).astype(np.int64)
         self.D_offsets_h = cum(self.D)
         self.hash_base_h = cum(self.E)
@@ -157,7 +162,8 @@ class TBEDesc:
         self.total_D = int(self.D_offsets_h[-1])
         self.total_E = int(self.hash_base_h[-1])
         self.num_weights = int(self.weights_offsets_h[-1])
-        self.c = tbe_desc(self.T, self.B, TBE_DT_F16,
+        self.c = tbe_desc(self.T, self.B,
+                          TBE_DT_BF16 if weights_dtype == torch.bfloat16 else TBE_DT_F16,
                           TBE_DT_I32 if index_dtype == torch.int32 else TBE_DT_I64,
                           self.D_offsets.data_ptr(), self.hash_base.data_ptr(),
                           self.weights_offsets.data_ptr(), self.total_D, self.total_E,
@@ -200,10 +206,16 @@ def _check_tensors(desc, indices, offsets):
         raise ValueError("indices and offsets must be contiguous")
 
 
+def _check_weights(desc, weights):
+    if isinstance(weights, torch.Tensor) and weights.dtype != desc.weights_dtype:
+        raise TypeError(f"weights must be {desc.weights_dtype}")
+
+
 def tbe_forward(desc: TBEDesc, weights, indices, offsets, per_sample_weights, out, ws: Workspace,
                 flags: int = 0, stream=None):
     """Pooled forward into out (fp32 [B, sum D]); see tbe_forward in include/tbe.h."""
     _check_tensors(desc, indices, offsets)
+    _check_weights(desc, weights)
     _ok("tbe_forward", _load().tbe_forward(
         desc.ref, _ptr(weights), _ptr(indices), _ptr(offsets), indices.numel(),
         _ptr(per_sample_weights), _ptr(out), ws.ptr, ws.nbytes, _stream(stream), flags))
@@ -224,6 +236,7 @@ def tbe_backward_rowwise_adagrad(desc: TBEDesc, grad_out, indices, offsets, per_
     """Backward with one exact row-wise Adagrad update per touched row, in place
     on weights and momentum; see include/tbe.h."""
     _check_tensors(desc, indices, offsets)
+    _check_weights(desc, weights)
     _ok("tbe_backward_rowwise_adagrad", _load().tbe_backward_rowwise_adagrad(
         desc.ref, _ptr(grad_out), _ptr(indices), _ptr(offsets), indices.numel(),
         _ptr(per_sample_weights), _ptr(weights), _ptr(momentum), float(lr), float(eps), ws.ptr,
@@ -237,6 +250,7 @@ def tbe_backward_rowwise_adagrad_noalloc(desc: TBEDesc, grad_out, indices, offse
     device memory at call time (see tbe_backward_rowwise_adagrad_noalloc in
     include/tbe.h for the scratch limit and the rules on overlapping calls)."""
     _check_tensors(desc, indices, offsets)
+    _check_weights(desc, weights)
     _ok("tbe_backward_rowwise_adagrad_noalloc", _load().tbe_backward_rowwise_adagrad_noalloc(
         desc.ref, _ptr(grad_out), _ptr(indices), _ptr(offsets), indices.numel(),
         _ptr(per_sample_weights), _ptr(weights), _ptr(momentum), float(lr), float(eps),
@@ -281,15 +295,15 @@ def tbe_probe_read():
 
 
 class TableBatchedEmbedding:
-    """Owns fp16 weights, fp32 row-wise momentum and a workspace for one
-    problem shape; forward() and backward() call the C ABI."""
+    """Owns 16-bit weights (fp16, or bf16), fp32 row-wise momentum and a
+    workspace for one problem shape; forward() and backward() call the C ABI."""
 
     def __init__(self, E, D, B, n_max, index_dtype=torch.int64, weighted=False, weights=None,
-                 momentum=None, lr=0.01, eps=1e-8, device="cuda"):
-        self.desc = TBEDesc(E, D, B, index_dtype, device)
+                 momentum=None, lr=0.01, eps=1e-8, device="cuda", weights_dtype=torch.float16):
+        self.desc = TBEDesc(E, D, B, index_dtype, device, weights_dtype)
         self.ws = Workspace(self.desc, n_max, weighted, device)
         self.weights = weights if weights is not None else torch.zeros(
-            self.desc.num_weights, dtype=torch.float16, device=device)
+            self.desc.num_weights, dtype=weights_dtype, device=device)
         self.momentum = momentum if momentum is not None else torch.zeros(
             self.desc.total_E, dtype=torch.float32, device=device)
         self.lr, self.eps = lr, eps

@@ -1,6 +1,7 @@
 // Internal helpers shared by the CUDA translation units of the TBE library.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -290,6 +291,36 @@ __device__ __forceinline__ void add_half8(float* acc, uint4 v) {
         "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
         : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
         : "r"(w[i]));
+}
+
+// Eight bf16 values packed in a uint4 -> fp32 (a bf16 is the upper half of
+// an fp32), accumulated, optionally scaled.
+__device__ __forceinline__ void add_bf16x8(float* acc, uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] += __uint_as_float(w[i] << 16);
+    acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void acc_bf16x8(float* acc, uint4 v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = fmaf(s, __uint_as_float(w[i] << 16), acc[2 * i]);
+    acc[2 * i + 1] = fmaf(s, __uint_as_float(w[i] & 0xffff0000u), acc[2 * i + 1]);
+  }
+}
+// The forward's accumulation of eight 16-bit weights of either type.
+template <bool kBf16, bool kWeighted>
+__device__ __forceinline__ void acc_row8(float* acc, uint4 v, float s) {
+  if constexpr (kBf16) {
+    if constexpr (kWeighted) acc_bf16x8(acc, v, s);
+    else add_bf16x8(acc, v);
+  } else {
+    if constexpr (kWeighted) acc_half8(acc, v, s);
+    else add_half8(acc, v);
+  }
 }
 
 __device__ __forceinline__ uint4 ldg_u4(const void* p) {

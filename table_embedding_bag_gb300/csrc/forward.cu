@@ -3,10 +3,10 @@
 // "Modernizing Table Batched Embeddings with FBTriton", section "Forward:
 // keep a narrowly specialized path beside the general one": one launch covers
 // every table; each bag gathers the rows its lookups index and sums them,
-// fp16 weights accumulating in fp32; the bounds / offset check is a separate
-// small kernel and is off by default.
+// fp16 (or bf16) weights accumulating in fp32; the bounds / offset check is a
+// separate small kernel and is off by default.
 //
-// GB300 mapping: one warp per bag.  A row of D_t fp16 values is D_t/8 16-byte
+// GB300 mapping: one warp per bag.  A row of D_t 16-bit values is D_t/8 16-byte
 // vectors; S = next_pow2(D_t/8) lanes (at most 32) cover one row, so a warp
 // holds G = 32/S lookups of the bag at once and every lane keeps U row
 // vectors in flight.  The G partial sums meet through a shuffle butterfly.
@@ -20,7 +20,7 @@
 namespace tbe {
 namespace {
 
-template <typename IndexT, bool kWeighted>
+template <typename IndexT, bool kWeighted, bool kBf16>
 __global__ void __launch_bounds__(256, TBE_FWD_MINB)
     forward_generic_kernel(const __half* __restrict__ W, const int64_t* __restrict__ D_offsets,
                            const int64_t* __restrict__ hash_base,
@@ -49,18 +49,18 @@ __global__ void __launch_bounds__(256, TBE_FWD_MINB)
     float* orow = out + b * total_D + d0;
     const int nvec = D >> 3;
     if (nvec <= 1)
-      pool_bag<1, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
+      pool_bag<1, IndexT, kWeighted, TBE_FWD_UNROLL, kBf16>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else if (nvec <= 2)
-      pool_bag<2, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
+      pool_bag<2, IndexT, kWeighted, TBE_FWD_UNROLL, kBf16>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else if (nvec <= 4)
-      pool_bag<4, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
+      pool_bag<4, IndexT, kWeighted, TBE_FWD_UNROLL, kBf16>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else if (nvec <= 8)
-      pool_bag<8, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
+      pool_bag<8, IndexT, kWeighted, TBE_FWD_UNROLL, kBf16>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else if (nvec <= 16)
-      pool_bag<16, IndexT, kWeighted>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
+      pool_bag<16, IndexT, kWeighted, TBE_FWD_UNROLL, kBf16>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else
       for (int vec0 = 0; vec0 < nvec; vec0 += 32)
-        pool_bag<32, IndexT, kWeighted>(Wt, E, rbase, D, vec0, indices, psw, s, e, orow, mode,
+        pool_bag<32, IndexT, kWeighted, TBE_FWD_UNROLL, kBf16>(Wt, E, rbase, D, vec0, indices, psw, s, e, orow, mode,
                                           status, scale);
   }
 }
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(256, TBE_FWD_MINB)
 // when the bag's hot rows were already pooled into out (hot_n given, the
 // table has hot rows, D_t <= kHotMaxD) the out row is read at the start and
 // added to.  Rows wider than 8 S values take several column passes.
-template <int S, bool kWeighted>
+template <int S, bool kWeighted, bool kBf16>
 __global__ void __launch_bounds__(256, TBE_FWD_MINB)
     forward_cold_kernel(const __half* __restrict__ W, const int64_t* __restrict__ D_offsets,
                         const int64_t* __restrict__ hash_base, const int64_t* __restrict__ w_offsets,
@@ -163,10 +163,7 @@ __global__ void __launch_bounds__(256, TBE_FWD_MINB)
             v[uu] = ldg_u4(reinterpret_cast<const __half*>(ad) + col);
           }
 #pragma unroll
-          for (int uu = 0; uu < U; ++uu) {
-            if (kWeighted) acc_half8(acc, v[uu], wv[uu]);
-            else add_half8(acc, v[uu]);
-          }
+          for (int uu = 0; uu < U; ++uu) acc_row8<kBf16, kWeighted>(acc, v[uu], kWeighted ? wv[uu] : 1.f);
         }
         p += S;
       }
@@ -294,14 +291,20 @@ cudaError_t launch_forward_t(const Launch& L, const __half* W, const IndexT* ind
   int64_t blocks = (nbags + warps - 1) / warps;
   if (blocks > (1 << 22)) blocks = 1 << 22;
   if (blocks < 1) blocks = 1;
-  if (psw)
-    { forward_generic_kernel<IndexT, true><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
+  auto go = [&](auto kernel) {
+    kernel<<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
         W, d->D_offsets, d->hash_base, d->weights_offsets, indices, offsets, psw, L.n, d->T,
-        d->B, d->total_D, out, status, mean); note_launch(); }
-  else
-    { forward_generic_kernel<IndexT, false><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
-        W, d->D_offsets, d->hash_base, d->weights_offsets, indices, offsets, psw, L.n, d->T,
-        d->B, d->total_D, out, status, mean); note_launch(); }
+        d->B, d->total_D, out, status, mean);
+    note_launch();
+  };
+  const bool bf16 = d->weights_dtype == TBE_DT_BF16;
+  if (psw) {
+    if (bf16) go(forward_generic_kernel<IndexT, true, true>);
+    else go(forward_generic_kernel<IndexT, true, false>);
+  } else {
+    if (bf16) go(forward_generic_kernel<IndexT, false, true>);
+    else go(forward_generic_kernel<IndexT, false, false>);
+  }
   return cudaGetLastError();
 }
 
@@ -346,14 +349,22 @@ cudaError_t launch_cold_s(const Launch& L, const __half* W, const uint32_t* keys
   int64_t blocks = (tasks + warps - 1) / warps;
   if (blocks > (1 << 22)) blocks = 1 << 22;
   if (blocks < 1) blocks = 1;
-  if (psw)
-    { probe_begin(TBE_PROBE_FORWARD_COLD, L.s); forward_cold_kernel<S, true><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
+  auto go = [&](auto kernel) {
+    probe_begin(TBE_PROBE_FORWARD_COLD, L.s);
+    kernel<<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
         W, d->D_offsets, d->hash_base, d->weights_offsets, keys, cold_off, psw, d->T, d->B,
-        d->total_D, out, hot_n, inv_len); note_launch(); probe_end(TBE_PROBE_FORWARD_COLD, L.s); }
-  else
-    { probe_begin(TBE_PROBE_FORWARD_COLD, L.s); forward_cold_kernel<S, false><<<static_cast<unsigned>(blocks), warps * 32, 0, L.s>>>(
-        W, d->D_offsets, d->hash_base, d->weights_offsets, keys, cold_off, psw, d->T, d->B,
-        d->total_D, out, hot_n, inv_len); note_launch(); probe_end(TBE_PROBE_FORWARD_COLD, L.s); }
+        d->total_D, out, hot_n, inv_len);
+    note_launch();
+    probe_end(TBE_PROBE_FORWARD_COLD, L.s);
+  };
+  const bool bf16 = d->weights_dtype == TBE_DT_BF16;
+  if (psw) {
+    if (bf16) go(forward_cold_kernel<S, true, true>);
+    else go(forward_cold_kernel<S, true, false>);
+  } else {
+    if (bf16) go(forward_cold_kernel<S, false, true>);
+    else go(forward_cold_kernel<S, false, false>);
+  }
   return cudaGetLastError();
 }
 

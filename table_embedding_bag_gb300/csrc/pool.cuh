@@ -25,7 +25,7 @@ __device__ __align__(16) uint4 g_zero_row[kMaxD / 8];
 // per-lookup branch (a skipped lookup also gets weight 0).  Row r of the
 // table is the lookup value minus `rbase` (0 for raw indices, the table's
 // first linear key for lists of linear keys).
-template <int S, typename IndexT, bool kWeighted, int kUnroll = TBE_FWD_UNROLL>
+template <int S, typename IndexT, bool kWeighted, int kUnroll = TBE_FWD_UNROLL, bool kBf16 = false>
 __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t E, int64_t rbase,
                                          int D, int vec0, const IndexT* __restrict__ indices,
                                          const float* __restrict__ psw, int64_t start,
@@ -84,10 +84,7 @@ __device__ __forceinline__ void pool_bag(const __half* __restrict__ Wt, int64_t 
         v[uu] = ldg_u4(reinterpret_cast<const __half*>(a) + col);
       }
 #pragma unroll
-      for (int uu = 0; uu < U; ++uu) {
-        if (kWeighted) acc_half8(acc, v[uu], wv[uu]);
-        else add_half8(acc, v[uu]);
-      }
+      for (int uu = 0; uu < U; ++uu) acc_row8<kBf16, kWeighted>(acc, v[uu], kWeighted ? wv[uu] : 1.f);
     }
   }
 

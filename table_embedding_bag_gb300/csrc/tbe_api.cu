@@ -120,7 +120,9 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   L.hot_parts = static_cast<int>(kHotCtaTarget / T > 0 ? kHotCtaTarget / T : 1);
   const int64_t max_parts = (B + kHotMinPartBags - 1) / kHotMinPartBags;
   if (L.hot_parts > max_parts) L.hot_parts = static_cast<int>(max_parts);
-  L.hot_enabled = static_cast<size_t>(T) * kHot * B * (sizeof(float) + 1) <= kHotBudgetBytes;
+  // the hot rows' tensor-core kernels take fp16 weights only
+  L.hot_enabled = d->weights_dtype == TBE_DT_F16 &&
+                  static_cast<size_t>(T) * kHot * B * (sizeof(float) + 1) <= kHotBudgetBytes;
   L.hot_cnt = take(T * kHot * 4);
   L.hot_hist8 = L.hot_enabled ? take(static_cast<size_t>(T) * kHot * B) : 0;
   L.hot_hist = L.hot_enabled ? take(static_cast<size_t>(T) * kHot * B * sizeof(float)) : 0;
@@ -150,7 +152,7 @@ tbe_status check_desc(const tbe_desc* d) {
   if (!d) return TBE_EINVAL;
   if (d->T < 1 || d->B < 1 || !d->D_offsets || !d->hash_base || !d->weights_offsets)
     return TBE_EINVAL;
-  if (d->weights_dtype != TBE_DT_F16) return TBE_EUNSUPPORTED;
+  if (d->weights_dtype != TBE_DT_F16 && d->weights_dtype != TBE_DT_BF16) return TBE_EUNSUPPORTED;
   if (d->index_dtype != TBE_DT_I32 && d->index_dtype != TBE_DT_I64) return TBE_EUNSUPPORTED;
   if (d->min_D < 8 || d->max_D > kMaxD || d->min_D > d->max_D || (d->min_D & 7) ||
       (d->max_D & 7) || d->total_D < d->max_D || (d->total_D & 7))

@@ -70,6 +70,7 @@ struct UpdArgs {
   int max_D;
   float lr;
   float eps;
+  bool bf16;  // weights are bf16 rather than fp16
 };
 
 // Table metadata, in shared memory when the problem has few enough tables.
@@ -169,7 +170,8 @@ __device__ __forceinline__ void load_row(const __half* row, int nv, uint2 (&w_ra
 
 // Row-wise Adagrad on one row with the summed gradient held by the S lanes
 // of a group (lane sl owns vectors sl + c*S).  w_raw / m_old are the row's
-// fp16 weights (4 per vector) and momentum, already loaded.  Every lane of
+// 16-bit weights (4 per vector; fp16, or bf16 when a.bf16) and momentum,
+// already loaded; the new weight is rounded to nearest even in its own type.  Every lane of
 // the warp must call it (the sum of squares is a group shuffle).
 template <int S, int NC>
 __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4], int D,
@@ -193,11 +195,19 @@ __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4
     const int vec = sl + c * S;
     if (vec < nv) {
       uint2 raw = w_raw[c];
-      __half2* h = reinterpret_cast<__half2*>(&raw);
-      const float2 w01 = __half22float2(h[0]);
-      const float2 w23 = __half22float2(h[1]);
-      h[0] = __floats2half2_rn(w01.x - a.lr * g[c][0] / denom, w01.y - a.lr * g[c][1] / denom);
-      h[1] = __floats2half2_rn(w23.x - a.lr * g[c][2] / denom, w23.y - a.lr * g[c][3] / denom);
+      if (a.bf16) {
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+        const float2 w01 = __bfloat1622float2(h[0]);
+        const float2 w23 = __bfloat1622float2(h[1]);
+        h[0] = __floats2bfloat162_rn(w01.x - a.lr * g[c][0] / denom, w01.y - a.lr * g[c][1] / denom);
+        h[1] = __floats2bfloat162_rn(w23.x - a.lr * g[c][2] / denom, w23.y - a.lr * g[c][3] / denom);
+      } else {
+        __half2* h = reinterpret_cast<__half2*>(&raw);
+        const float2 w01 = __half22float2(h[0]);
+        const float2 w23 = __half22float2(h[1]);
+        h[0] = __floats2half2_rn(w01.x - a.lr * g[c][0] / denom, w01.y - a.lr * g[c][1] / denom);
+        h[1] = __floats2half2_rn(w23.x - a.lr * g[c][2] / denom, w23.y - a.lr * g[c][3] / denom);
+      }
       *reinterpret_cast<uint2*>(row + vec * 4) = raw;
     }
   }
@@ -925,7 +935,8 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   const int fin = radix_passes(d) & 1;
   UpdArgs a;
   a.grad_out = grad_out;
-  a.W = static_cast<__half*>(weights);
+  a.W = static_cast<__half*>(weights);  // 16-bit rows; a.bf16 picks the codec
+  a.bf16 = d->weights_dtype == TBE_DT_BF16;
   a.momentum = momentum;
   a.D_offsets = d->D_offsets;
   a.hash_base = d->hash_base;

@@ -31,13 +31,14 @@ def host(w):
 class Run:
     """One TBE problem on the GPU through the C ABI."""
 
-    def __init__(self, w, device="cuda", mean=False):
+    def __init__(self, w, device="cuda", mean=False, weights_dtype=torch.float16):
         self.w = w
-        self.desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, device)
+        self.desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, device, weights_dtype)
         self.ws = tbe.Workspace(self.desc, max(w.n, 1), w.psw is not None, device, mean=mean)
         d = lambda x: None if x is None else x.to(device).contiguous()
         self.indices, self.offsets, self.psw = d(w.indices), d(w.offsets), d(w.psw)
         self.weights = d(w.weights).clone()
+        assert self.weights.dtype == weights_dtype, "the workload's weights have another dtype"
         self.momentum = d(w.momentum).clone()
         self.grad_out = d(w.grad_out)
         self.out = torch.empty(w.B, self.desc.total_D, dtype=torch.float32, device=device)
@@ -73,7 +74,13 @@ class Run:
                                          self.psw, self.weights, self.momentum, self.w.lr,
                                          self.w.eps, self.ws, flags)
         torch.cuda.synchronize()
-        return self.weights.cpu().numpy(), self.momentum.cpu().numpy()
+        return self.host_weights(), self.momentum.cpu().numpy()
+
+    def host_weights(self):
+        """The weights on the host: fp16 values, or bf16 bit patterns (uint16)."""
+        if self.weights.dtype == torch.bfloat16:
+            return bf16_bits(self.weights)
+        return self.weights.cpu().numpy()
 
     def status(self):
         return tbe.tbe_read_status(self.ws)
@@ -112,6 +119,55 @@ def assert_momentum_close(m, ref, rel=1e-5):
     tol = rel * np.abs(ref.astype(np.float64)) + 1e-30
     bad = err > tol
     assert not bad.any(), f"{bad.sum()} momentum values off; worst rel {np.max(err / (tol / rel)):.3e}"
+
+
+def bf16_bits(t):
+    """A bfloat16 tensor's bit patterns as numpy uint16."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_values(bits):
+    """bf16 bit patterns as float64 (a bf16 is the upper half of an fp32)."""
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def assert_bf16_step_close(bits, ref_bits, old_bits, upd_rel=2.0 ** -12, max_frac=1e-5):
+    """bf16 weights after an Adagrad step against the oracle's.  The kernel
+    forms w - lr*g/(sqrt(m)+eps) in fp32 and rounds once to bf16; the oracle
+    does the same in fp64.  Where the step nearly cancels the weight the
+    result is far smaller than its operands, and because bf16 keeps fp32's
+    exponent range (fp16 bottoms out at 2^-24) its ulp there can be below the
+    fp32 error of the operands.  So each weight must lie within 1 ulp of the
+    oracle's or within the fp32 error budget of the operands: 2^-12 of the
+    step (an fp32 gradient summed over runs of up to a few thousand pairs,
+    then divided) plus 2^-23 of the old weight; and at most max_frac of all
+    weights may need more than the 1 ulp."""
+    a, b = bf16_values(bits), bf16_values(ref_bits)
+    old = bf16_values(old_bits)
+    assert np.isfinite(a).all()
+    err = np.abs(a - b)
+    ulp = np.spacing(np.abs(b).astype(np.float32)).astype(np.float64) * 65536.0
+    beyond = err > ulp
+    tol = ulp + upd_rel * np.abs(old - b) + 2.0 ** -23 * np.abs(old)
+    bad = err > tol
+    worst = int(np.argmax(err - tol)) if err.size else 0
+    detail = (f"{beyond.sum()} of {err.size} beyond 1 ulp, {bad.sum()} beyond the fp32 budget; "
+              f"worst at {worst}: gpu {a[worst]:.9e} oracle {b[worst]:.9e} old {old[worst]:.9e}")
+    print("bf16 step:", detail)
+    assert not bad.any(), detail
+    assert beyond.sum() <= max_frac * err.size, detail
+
+
+def assert_bf16_within_ulp(bits, ref_bits, ulps=1):
+    """bf16 patterns within `ulps` steps of the oracle's (steps counted along
+    the ordered sequence of finite bf16 values; +0 and -0 are the same step)."""
+    def order(x):
+        x = np.asarray(x, np.int64)
+        return np.where(x & 0x8000, -(x & 0x7fff), x)
+    a, b = np.asarray(bits, np.uint16), np.asarray(ref_bits, np.uint16)
+    assert not np.isnan(bf16_values(a)).any() and not np.isinf(bf16_values(a)).any()
+    bad = np.abs(order(a) - order(b)) > ulps
+    assert not bad.any(), f"{bad.sum()} of {bad.size} bf16 weights beyond {ulps} ulp"
 
 
 def assert_weights_within_ulp(w, ref, ulps=1):

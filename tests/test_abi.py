@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import table_embedding_bag_gb300 as tbe
 
@@ -74,6 +75,28 @@ def test_bad_descriptors_rejected(lib, field, value, code):
     d = _desc()
     setattr(d, field, value)
     assert _ws_size(lib, d, 100)[0] == code
+
+
+def test_bf16_weights_accepted_without_hot_row_buffers(lib):
+    # bf16 tables are supported; the hot rows' histograms (fp16 only) are not
+    # laid out for them, so their workspace is the smaller one
+    d16, dbf = _desc(B=4096), _desc(B=4096)
+    dbf.weights_dtype = tbe.TBE_DT_BF16
+    rc16, s16 = _ws_size(lib, d16, 1 << 16)
+    rcbf, sbf = _ws_size(lib, dbf, 1 << 16)
+    assert rc16 == rcbf == tbe.TBE_OK
+    assert sbf < s16
+
+
+def test_binding_checks_the_weight_dtype():
+    with pytest.raises(ValueError):
+        tbe.TBEDesc([10], [8], 2, device="cpu", weights_dtype=torch.float32)
+    desc = tbe.TBEDesc([10], [8], 2, device="cpu", weights_dtype=torch.bfloat16)
+    idx = torch.zeros(3, dtype=torch.int64)
+    off = torch.tensor([0, 1, 3], dtype=torch.int64)
+    out = torch.empty(2, 8)
+    with pytest.raises(TypeError):  # fp16 weights for a bf16 problem, refused before any call
+        tbe.tbe_forward(desc, torch.zeros(80, dtype=torch.float16), idx, off, None, out, None)
 
 
 def test_bad_sizes_rejected(lib):

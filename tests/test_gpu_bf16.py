@@ -1,0 +1,155 @@
+"""bf16 weights (TBE_DT_BF16): rows of bfloat16 values, pooled in fp32, and
+the row-wise Adagrad step computed in fp32 and rounded to the nearest bf16
+(ties to even), compared within 1 bf16 ulp of the oracle or, where the step
+nearly cancels a weight, within the fp32 error of its operands.  The CUDA path against the oracle's bf16 mode, weights passed
+to the oracle as bit patterns: the plain forward (a one-table problem too,
+where fp16 would take the small-table path), the preprocessed forward, the
+backward over short, medium and long runs with either long-run variant, mean
+pooling, the no-alloc entry point and bags at the edges.  Hot rows are an
+fp16 feature: a bf16 problem keeps an empty hot set and pools every lookup
+on the gather path."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+tbe = H.tbe
+BF16 = torch.bfloat16
+
+CASES = {
+    "tiny": dict(name="tiny"),
+    "hot": dict(name="hot", B=2048, E_scale=0.01),
+    "weighted": dict(name="weighted", B=1024, T=16, E_scale=0.01),
+    "small": dict(name="small", B=4096),
+    "mixed": dict(name="mixed", B=2048, E_scale=0.05),
+}
+
+
+def make(case, seed=0):
+    kw = dict(CASES[case])
+    return workloads.make(kw.pop("name"), seed=seed, weights_dtype=BF16, **kw)
+
+
+def host(w):
+    t = lambda x: None if x is None else x.detach().cpu().numpy()
+    return dict(indices=t(w.indices), offsets=t(w.offsets), psw=t(w.psw),
+                weights=H.bf16_bits(w.weights), momentum=t(w.momentum), grad_out=t(w.grad_out))
+
+
+def oracle_forward(w, mean=False):
+    hw = host(w)
+    tab = H.tables(w)
+    ref = oracle.forward(tab, w.B, hw["weights"], hw["indices"], hw["offsets"], hw["psw"],
+                         mean=mean, bf16=True)
+    absp = None if hw["psw"] is None else np.abs(hw["psw"])
+    terms = oracle.forward(tab, w.B, hw["weights"] & np.uint16(0x7fff), hw["indices"],
+                           hw["offsets"], absp, mean=mean, bf16=True)
+    return ref, terms
+
+
+def oracle_backward(w, mean=False):
+    hw = host(w)
+    return oracle.backward_rowwise_adagrad(H.tables(w), w.B, hw["indices"], hw["offsets"],
+                                           hw["grad_out"], hw["weights"], hw["momentum"], w.lr,
+                                           w.eps, hw["psw"], mean=mean, bf16=True)
+
+
+def check_backward(run, w, flags=0, mean=False):
+    W_ref, m_ref = oracle_backward(w, mean)
+    W_gpu, m_gpu = run.backward(flags)
+    H.assert_momentum_close(m_gpu, m_ref)
+    W_old = host(w)["weights"]
+    H.assert_bf16_step_close(W_gpu, W_ref, W_old)
+    assert (W_ref != W_old).any()  # the step moved weights
+    return W_gpu, W_ref
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_bf16_forward_matches_oracle(case):
+    w = make(case)
+    run = H.Run(w, weights_dtype=BF16)
+    ref, terms = oracle_forward(w)
+    H.assert_forward_close(run.forward(), ref, terms)
+
+
+@pytest.mark.parametrize("case", ["hot", "weighted", "mixed"])
+def test_bf16_preprocessed_forward_and_backward_match_oracle(case):
+    w = make(case)
+    run = H.Run(w, weights_dtype=BF16)
+    ref, terms = oracle_forward(w)
+    tbe.tbe_preprocess(run.desc, run.indices, run.offsets, run.psw, run.ws)
+    H.assert_forward_close(run.forward(tbe.TBE_F_PREPROCESSED), ref, terms)
+    check_backward(run, w, tbe.TBE_F_PREPROCESSED)
+    # no hot set is learned for bf16 weights; the next step is still exact
+    assert sum(len(h) for h in run.hot_set()) == 0
+    run.reset_state()
+    tbe.tbe_preprocess(run.desc, run.indices, run.offsets, run.psw, run.ws)
+    H.assert_forward_close(run.forward(tbe.TBE_F_PREPROCESSED), ref, terms)
+    check_backward(run, w, tbe.TBE_F_PREPROCESSED)
+
+
+@pytest.mark.parametrize("two_launch", [False, True])
+def test_bf16_backward_short_medium_and_long_runs(two_launch):
+    # the hot recipe's skew gives runs of every class at this size
+    w = make("hot", seed=2)
+    run = H.Run(w, weights_dtype=BF16)
+    pre = run.preprocess()
+    lens = np.diff(pre["run_pairs"].astype(np.int64))
+    assert (lens < 16).any() and ((lens >= 16) & (lens < 128)).any() and pre["n_long"] > 0
+    check_backward(run, w, tbe.TBE_F_LONG_TWO_LAUNCH if two_launch else 0)
+
+
+@pytest.mark.parametrize("case", ["weighted", "mixed"])
+def test_bf16_mean_pooling(case):
+    w = make(case, seed=4)
+    run = H.Run(w, mean=True, weights_dtype=BF16)
+    ref, terms = oracle_forward(w, mean=True)
+    H.assert_forward_close(run.forward(tbe.TBE_F_MEAN), ref, terms)
+    check_backward(run, w, tbe.TBE_F_MEAN, mean=True)
+
+
+def test_bf16_edge_bags():
+    # empty bags, single lookups, one row repeated, out-of-range rows (they
+    # add nothing and get no update), widths 8 and 1024 in one problem
+    rng = np.random.default_rng(7)
+    E, D, B = [50, 9], [8, 1024], 6
+    bags = [[[], [49], [3] * 40, [0, 50, -1, 7], list(rng.integers(0, 50, 300)), [2, 2]],
+            [[8], [], [4] * 5, list(rng.integers(0, 9, 33)), [9, 0], [1, 2, 3]]]
+    idx, off = [], [0]
+    for t in range(2):
+        for b in range(B):
+            idx.extend(bags[t][b])
+            off.append(len(idx))
+    W = (torch.from_numpy(rng.standard_normal(int(np.dot(E, D)))) * 0.01).to(BF16)
+    G = rng.standard_normal((B, sum(D))).astype(np.float32)
+    w = workloads.from_arrays(E, D, B, np.asarray(idx, np.int64), np.asarray(off, np.int64), W, G)
+    run = H.Run(w, weights_dtype=BF16)
+    ref, terms = oracle_forward(w)
+    H.assert_forward_close(run.forward(), ref, terms)
+    check_backward(run, w)
+
+
+def test_bf16_noalloc_matches_oracle():
+    w = make("tiny", seed=1)
+    run = H.Run(w, weights_dtype=BF16)
+    W_ref, m_ref = oracle_backward(w)
+    tbe.tbe_backward_rowwise_adagrad_noalloc(run.desc, run.grad_out, run.indices, run.offsets,
+                                             run.psw, run.weights, run.momentum, w.lr, w.eps)
+    torch.cuda.synchronize()
+    H.assert_momentum_close(run.momentum.cpu().numpy(), m_ref)
+    H.assert_bf16_step_close(H.bf16_bits(run.weights), W_ref, host(w)["weights"])
+
+
+def test_bf16_step_differs_from_fp16_step():
+    # the same drawn weights stored as fp16 and as bf16 give different
+    # results, so the bf16 tests are not passing on the fp16 codec
+    w16 = workloads.make("tiny", seed=3)
+    wb = workloads.make("tiny", seed=3, weights_dtype=BF16)
+    r16, rb = H.Run(w16), H.Run(wb, weights_dtype=BF16)
+    assert not np.array_equal(r16.forward(), rb.forward())
+    ref, terms = oracle_forward(wb)
+    H.assert_forward_close(rb.forward(), ref, terms)

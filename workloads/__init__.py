@@ -65,7 +65,7 @@ class Workload:
     indices: torch.Tensor    # [n] int32/int64
     offsets: torch.Tensor    # [T*B+1], same dtype as indices, table-major bags
     psw: torch.Tensor | None # [n] fp32 or None
-    weights: torch.Tensor    # flat fp16, table t rows contiguous with stride D_t
+    weights: torch.Tensor    # flat fp16 or bf16, table t rows contiguous with stride D_t
     momentum: torch.Tensor   # fp32 [sum E]
     grad_out: torch.Tensor   # fp32 [B, sum D]
     lr: float
@@ -138,12 +138,15 @@ def _rows(spec: Spec, E: int, count: int, g, device):
 
 
 def make(name: str, device="cpu", seed: int = 0, B: int | None = None, T: int | None = None,
-         E_scale: float | None = None, compact: bool = False) -> Workload:
+         E_scale: float | None = None, compact: bool = False,
+         weights_dtype: torch.dtype = torch.float16) -> Workload:
     """Draw a workload.  B, T and E_scale shrink a recipe for oracle-sized tests
     (E_scale multiplies every table's row count, keeping at least one row).
     compact=True keeps only the rows the lookups touch, renumbered per table
     in increasing order (the lookups are drawn from the full tables first), so
-    that a few bags of a huge table need no huge weight array."""
+    that a few bags of a huge table need no huge weight array.  weights_dtype
+    (torch.float16 or torch.bfloat16) is the type the N(0, 0.01^2) weight
+    draws are stored in."""
     spec = SPECS[name]
     T = spec.T if T is None else T
     B = spec.B if B is None else B
@@ -173,11 +176,11 @@ def make(name: str, device="cpu", seed: int = 0, B: int | None = None, T: int | 
     psw = torch.cat(psws) if spec.weighted else None
     gw = _gen(device, seed * 1000 + 999)
     nW = int((E * D).sum())
-    weights = torch.empty(nW, dtype=torch.float16, device=device)
+    weights = torch.empty(nW, dtype=weights_dtype, device=device)
     chunk = 1 << 27
     for s in range(0, nW, chunk):
         e = min(nW, s + chunk)
-        weights[s:e] = (torch.randn(e - s, generator=gw, device=device) * 0.01).to(torch.float16)
+        weights[s:e] = (torch.randn(e - s, generator=gw, device=device) * 0.01).to(weights_dtype)
     momentum = torch.zeros(int(E.sum()), dtype=torch.float32, device=device)
     grad_out = torch.randn(B, int(D.sum()), generator=gw, device=device)
     return Workload(name, T, B, E, D, indices, offsets, psw, weights, momentum, grad_out,
@@ -186,7 +189,8 @@ def make(name: str, device="cpu", seed: int = 0, B: int | None = None, T: int | 
 
 def from_arrays(E, D, B, indices, offsets, weights, grad_out, psw=None, momentum=None,
                 lr=0.01, eps=1e-8, name="custom") -> Workload:
-    """Wrap hand-made arrays (numpy or torch, on the host) as a Workload."""
+    """Wrap hand-made arrays (numpy or torch, on the host) as a Workload
+    (weights: fp16, or a bfloat16 tensor, which is kept as it is)."""
     t = lambda x, dt=None: None if x is None else torch.as_tensor(np.asarray(x) if not
                                                                    torch.is_tensor(x) else x,
                                                                    dtype=dt)
@@ -196,4 +200,5 @@ def from_arrays(E, D, B, indices, offsets, weights, grad_out, psw=None, momentum
     off = t(offsets, idx.dtype)
     m = t(momentum, torch.float32) if momentum is not None else torch.zeros(int(E.sum()))
     return Workload(name, len(E), int(B), E, D, idx, off, t(psw, torch.float32),
-                    t(weights, torch.float16), m, t(grad_out, torch.float32), lr, eps)
+                    weights if torch.is_tensor(weights) and weights.dtype == torch.bfloat16
+                    else t(weights, torch.float16), m, t(grad_out, torch.float32), lr, eps)
