@@ -55,7 +55,7 @@ def _load():
         lib.oracle_row_gradients.argtypes = [i32, i32, P, P, i32, P, P, i64, P, P, i32, i32, P,
                                              P, P]
         lib.oracle_backward_rowwise_adagrad.argtypes = [i32, i32, P, P, P, i32, P, P, i64, P, P,
-                                                        i32, i32, f32, f32, P, P]
+                                                        i32, i32, i32, f32, f32, P, P]
         lib.oracle_backward_selected.argtypes = [i32, i32, P, P, i32, P, P, i64, P, P, i32, f32,
                                                  f32, i64, P, i32, P, P, P]
         lib.oracle_repair_offsets.argtypes = [i32, P, i64, i64, P]
@@ -193,21 +193,26 @@ def row_gradients(tables: Tables, B, indices, offsets, grad_out, psw=None, mean=
 
 
 def backward_rowwise_adagrad(tables: Tables, B, indices, offsets, grad_out, weights, momentum,
-                             lr, eps, psw=None, mean=False, bf16=False):
+                             lr, eps, psw=None, mean=False, bf16=False, elementwise=False):
     """Returns (new_weights, new_momentum fp32); inputs are not modified.
     mean: each bag's gradient times 1/L for its L > 1 lookups, before grouping.
-    bf16: weights (in and out) are bfloat16 bit patterns (uint16), else fp16."""
+    bf16: weights (in and out) are bfloat16 bit patterns (uint16), else fp16.
+    elementwise: HugeCTR's element-wise Adagrad, momentum shaped like the
+    flat weights (one accumulator per element), instead of one per row."""
     lib = _load()
     indices, offsets, bits = _idx(indices, offsets)
     w = np.array(weights, dtype=np.uint16 if bf16 else np.float16, copy=True)
     m = np.array(momentum, dtype=np.float32, copy=True)
+    if m.size != (int(tables.w_offsets[-1]) if elementwise else int(tables.hash_base[-1])):
+        raise ValueError("momentum has one entry per weight element (elementwise) or per row")
     grad_out = _c(grad_out, np.float32)
     psw = _c(psw, np.float32)
     rc = lib.oracle_backward_rowwise_adagrad(tables.T, B, _p(tables.D_offsets),
                                              _p(tables.hash_base), _p(tables.w_offsets), bits,
                                              _p(indices), _p(offsets), len(indices), _p(psw),
                                              _p(grad_out), int(bool(mean)), int(bool(bf16)),
-                                             float(lr), float(eps), _p(w.view(np.uint16)), _p(m))
+                                             int(bool(elementwise)), float(lr), float(eps),
+                                             _p(w.view(np.uint16)), _p(m))
     _check(rc, "backward")
     return w, m
 

@@ -21,7 +21,9 @@
 //    (row, sample) pairs, run starts with a sentinel, accumulator updated
 //    first and the weight step using the new accumulator with eps outside the
 //    square root.  The row-wise form replaces the element-wise accumulator
-//    increment g_d^2 by the row mean (1/D) sum_d g_d^2.
+//    increment g_d^2 by the row mean (1/D) sum_d g_d^2; the element-wise
+//    form itself (one accumulator per weight element, at the weight's own
+//    flat position) is offered beside it.
 //
 //  * same HugeCTR page, the combiner note (sum, or mean = the sum kernel then
 //    a scaling kernel) and the mean backward kernel: with mean pooling a
@@ -34,7 +36,8 @@
 //  * bags are table-major: bag (t,b) has id t*B+b, offsets has T*B+1 entries;
 //  * a lookup whose row is outside [0, E_t) contributes nothing (skipped);
 //  * weights are fp16 (or bf16), rounded to nearest-even from the double result;
-//  * momentum is fp32, rounded from the double sum m_old + mean_d(g_d^2).
+//  * momentum is fp32, rounded from the double sum m_old + mean_d(g_d^2)
+//    (element-wise: m_old_d + g_d^2 per element).
 //
 // Parity pins for every function live in tests/test_oracle_*.py.
 
@@ -398,14 +401,30 @@ int oracle_row_gradients(int T, int B, const int64_t* D_offsets, const int64_t* 
   return ORACLE_OK;
 }
 
-// Backward with exactly one row-wise Adagrad update per touched row, in place
-// on weights (fp16 bits, flat) and momentum (fp32, [hash_base[T]]).
+// Element-wise Adagrad on one row (the HugeCTR page's Adagrad kernel: the
+// accumulator is per weight element), given its summed gradient g[0..D):
+//   m_d <- m_d + g_d^2                          (stored as fp32)
+//   w_d <- w_d - lr * g_d / (sqrt(m_d) + eps)   (stored in the weight type)
+void elementwise_adagrad(int D, const double* g, float lr, float eps, uint16_t* w, float* m,
+                         int wtype) {
+  for (int d = 0; d < D; ++d) {
+    const float m_new = static_cast<float>(static_cast<double>(m[d]) + g[d] * g[d]);
+    m[d] = m_new;
+    const double denom = std::sqrt(static_cast<double>(m_new)) + static_cast<double>(eps);
+    const double w_old = weight_to_double(w[d], wtype);
+    w[d] = double_to_weight(w_old - static_cast<double>(lr) * g[d] / denom, wtype);
+  }
+}
+
+// Backward with exactly one Adagrad update per touched row, in place on
+// weights (16-bit patterns, flat) and momentum: row-wise, fp32 [hash_base[T]];
+// element-wise (elementwise != 0), fp32 laid out like the weights.
 int oracle_backward_rowwise_adagrad(int T, int B, const int64_t* D_offsets,
                                     const int64_t* hash_base, const int64_t* w_offsets,
                                     int index_bits, const void* indices, const void* offsets,
                                     int64_t n, const float* psw, const float* grad_out,
-                                    int mean, int wtype, float lr, float eps, uint16_t* weights,
-                                    float* momentum) {
+                                    int mean, int wtype, int elementwise, float lr, float eps,
+                                    uint16_t* weights, float* momentum) {
   Problem p{T, B, D_offsets, hash_base, w_offsets, index_bits, indices, offsets, n, psw};
   if (!offsets_ok(p)) return ORACLE_EINVAL;
   const int64_t sumD = D_offsets[T];
@@ -429,8 +448,11 @@ int oracle_backward_rowwise_adagrad(int T, int B, const int64_t* D_offsets,
     g.assign(D, 0.0);
     sum_run_gradient(static_cast<int64_t>(gp.size()), D, gp.data(), coef.data(), g.data(),
                      mean ? bs.data() : nullptr);
-    rowwise_adagrad(D, g.data(), lr, eps, weights + w_offsets[t] + r * D, momentum + kv.first,
-                    wtype);
+    uint16_t* w = weights + w_offsets[t] + r * D;
+    if (elementwise)
+      elementwise_adagrad(D, g.data(), lr, eps, w, momentum + w_offsets[t] + r * D, wtype);
+    else
+      rowwise_adagrad(D, g.data(), lr, eps, w, momentum + kv.first, wtype);
   }
   return ORACLE_OK;
 }

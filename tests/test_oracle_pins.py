@@ -521,3 +521,109 @@ def test_adagrad_bf16_constant_gradient_closed_form(oracle_lib, c):
     # the rounding agrees with torch's where the fp32 value is exact
     if np.float64(np.float32(step)) == step:
         assert int(ref.view(torch.int16).item()) & 0xffff == want
+
+
+# ------------------------------------------------ element-wise Adagrad
+# HugeCTR's Adagrad kernel keeps one accumulator per weight element:
+# acc_d += g_d^2, w_d -= lr * g_d / (sqrt(acc_d) + eps).  The oracle's
+# element-wise mode keeps that accumulator at the weight's own flat position.
+
+def _elementwise_row_problem(D, v, K, w0, m0, lr, eps, E=3, row=1):
+    """K identical bags, each looking up `row` once with gradient row v."""
+    tab = oracle.Tables([E], [D])
+    W = np.zeros(E * D, np.float16)
+    W[row * D:(row + 1) * D] = w0
+    m = np.zeros(E * D, np.float32)
+    m[row * D:(row + 1) * D] = m0
+    G = np.tile(np.asarray(v, np.float32), (K, 1))
+    idx = np.full(K, row, np.int64)
+    off = np.arange(K + 1, dtype=np.int64)
+    W2, m2 = oracle.backward_rowwise_adagrad(tab, K, idx, off, G, W, m, lr, eps,
+                                             elementwise=True)
+    return W2.reshape(E, D), m2.reshape(E, D)
+
+
+def test_elementwise_first_step_with_eps_zero_moves_each_element_by_lr():
+    # From acc = 0 with eps = 0 the step is lr * g/|g| = lr * sign(g) for every
+    # element, whatever its magnitude; acc becomes g^2 with g = K v (exact).
+    v = np.array([3.0, -0.015625, 1e-3, -250.0, 0.5, -7.25, 40.0, -1.0], np.float32)
+    K, lr = 3, 0.125
+    W2, m2 = _elementwise_row_problem(8, v, K, np.float16(0.5), 0.0, lr, 0.0)
+    assert np.array_equal(W2[1], np.where(v > 0, np.float16(0.375), np.float16(0.625)))
+    g = K * v.astype(np.float64)
+    assert np.array_equal(m2[1], (g * g).astype(np.float32))
+    # other rows untouched, their accumulators too
+    assert not W2[0].any() and not W2[2].any() and not m2[0].any() and not m2[2].any()
+
+
+def test_elementwise_second_step_divides_by_sqrt_two():
+    # From acc = g^2 with the same gradient: acc = 2 g^2, step = lr/sqrt(2)
+    v = np.array([2.0, -0.25, 64.0, -3.0, 0.75, -1e-2, 9.0, -5.5], np.float32)
+    lr = 0.125
+    g2 = (v.astype(np.float64)) ** 2
+    W2, m2 = _elementwise_row_problem(8, v, 1, np.float16(0.375), g2.astype(np.float32), lr, 0.0)
+    assert np.array_equal(m2[1], (2 * g2).astype(np.float32))
+    exp = (0.375 - np.sign(v) * lr / np.sqrt(2.0)).astype(np.float16)
+    assert np.array_equal(W2[1], exp)
+
+
+def test_elementwise_equals_rowwise_when_every_element_has_the_same_magnitude():
+    # |g_d| = c for all d: the row mean of g^2 is c^2, the element-wise
+    # accumulators all equal it, and the two rules give the same step.
+    D, c, lr, eps = 16, 0.375, 0.05, 1e-3
+    v = np.where(np.arange(D) % 3 == 0, -c, c).astype(np.float32)
+    W_el, m_el = _elementwise_row_problem(D, v, 2, np.float16(0.25), 0.5, lr, eps)
+    W_rw, m_rw = _single_row_problem(D, 2 * v, np.float16(0.25), m0=0.5, lr=lr, eps=eps)
+    assert np.array_equal(W_el, W_rw)
+    assert np.array_equal(m_el[1], np.full(D, m_rw[1], np.float32))
+
+
+def test_elementwise_D1_equals_rowwise():
+    # For D = 1 the two rules coincide (the row-wise D = 1 case is pinned to
+    # the HugeCTR rule above), over several steps and per-sample weights.
+    rng = np.random.default_rng(11)
+    tab = oracle.Tables([5, 3], [1, 1])
+    W = rng.normal(0, 1, 8).astype(np.float16)
+    m = rng.uniform(0, 1, 8).astype(np.float32)
+    We, me, Wr, mr = W.copy(), m.copy(), W.copy(), m.copy()
+    for step in range(3):
+        idx = np.concatenate([rng.integers(0, 5, 7), rng.integers(0, 3, 5)]).astype(np.int64)
+        off = np.array([0, 3, 7, 9, 12], np.int64)
+        G = rng.normal(0, 1, (2, 2)).astype(np.float32)
+        psw = rng.uniform(0.5, 2, 12).astype(np.float32)
+        We, me = oracle.backward_rowwise_adagrad(tab, 2, idx, off, G, We, me, 0.05, 1e-3, psw,
+                                                 elementwise=True)
+        Wr, mr = oracle.backward_rowwise_adagrad(tab, 2, idx, off, G, Wr, mr, 0.05, 1e-3, psw)
+        assert np.array_equal(We, Wr) and np.array_equal(me, mr)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_elementwise_invariants(oracle_lib, seed):
+    # untouched elements bit-identical; each touched element's accumulator
+    # grows by exactly its own summed gradient squared, once
+    tab, B, idx, off, W, G, psw = _tiny_problem(seed + 70, weighted=seed != 1)
+    rng = np.random.default_rng(seed)
+    nW = int(tab.w_offsets[-1])
+    m0 = rng.uniform(0, 2, nW).astype(np.float32)
+    W2, m2 = oracle.backward_rowwise_adagrad(tab, B, idx, off, G, W, m0, 0.01, 1e-8, psw,
+                                             elementwise=True)
+    keys, g = oracle.row_gradients(tab, B, idx, off, G, psw)
+    touched = np.zeros(nW, bool)
+    for j, k in enumerate(keys):
+        t = int(np.searchsorted(tab.hash_base, k, side="right") - 1)
+        D = int(tab.D[t])
+        s = int(tab.w_offsets[t]) + (int(k) - int(tab.hash_base[t])) * D
+        touched[s:s + D] = True
+        exp = m0[s:s + D].astype(np.float64) + g[j, :D] ** 2
+        assert np.all(np.abs(m2[s:s + D] - exp) <= 2 ** -23 * exp)
+    assert np.array_equal(W2.view(np.uint16)[~touched], W.view(np.uint16)[~touched])
+    assert np.array_equal(m2.view(np.uint32)[~touched], m0.view(np.uint32)[~touched])
+    assert (W2.view(np.uint16)[touched] != W.view(np.uint16)[touched]).any()
+
+
+def test_elementwise_momentum_must_be_shaped_like_the_weights():
+    tab = oracle.Tables([4], [8])
+    with pytest.raises(ValueError):
+        oracle.backward_rowwise_adagrad(tab, 1, np.array([1]), np.array([0, 1]),
+                                        np.ones((1, 8), np.float32), np.zeros(32, np.float16),
+                                        np.zeros(4, np.float32), 0.1, 1e-8, elementwise=True)
