@@ -52,6 +52,10 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--pooling", choices=["sum", "mean"], default="sum",
                    help="pooling mode of the step (the recorded workload is sum)")
+    p.add_argument("--weights", choices=["fp16", "bf16"], default="fp16",
+                   help="weight type (the recorded workload is fp16)")
+    p.add_argument("--optimizer", choices=["rowwise", "elementwise"], default="rowwise",
+                   help="Adagrad form (the recorded workload is row-wise)")
     # smaller variants of the hot-row recipe, for profiling captures only
     p.add_argument("--tables", type=int, default=None)
     p.add_argument("--rows", type=int, default=None)
@@ -176,14 +180,21 @@ def profiled_traffic():
     return int(fields["traffic_bytes_per_launch"])
 
 
-def long_chunk_bytes(D, long_pairs, chunks, long_runs):
+def momentum_bytes(D, elementwise):
+    """Momentum bytes a row's update reads and writes: one fp32 per row, or
+    one per element with element-wise Adagrad."""
+    return 8 * D if elementwise else 8
+
+
+def long_chunk_bytes(D, long_pairs, chunks, long_runs, elementwise=False):
     """Algorithmic bytes of one long_chunks_kernel launch, counted per use (the
     per-unit figures of the design notes): per long pair its gradient row
     (4 D) and pair data (8); per chunk its partial written and read back
     (2 x 4 D) and its descriptor (16); per long run the weights row read and
-    written (2 x 2 D), the momentum (8) and the run record (32)."""
+    written (2 x 2 D), the momentum (8, or 8 D element-wise) and the run
+    record (32)."""
     return (long_pairs * (4 * D + 8) + chunks * (2 * 4 * D + 16)
-            + long_runs * (2 * 2 * D + 8 + 32))
+            + long_runs * (2 * 2 * D + momentum_bytes(D, elementwise) + 32))
 
 
 def forward_problem_bytes(w, rows_touched):
@@ -195,7 +206,7 @@ def forward_problem_bytes(w, rows_touched):
             + w.B * int(w.D.sum()) * 4)
 
 
-def problem_roofline(w, rows_touched, r, peak):
+def problem_roofline(w, rows_touched, r, peak, elementwise=False):
     """Compulsory bytes of the forward, the backward and the whole step (each
     index and offset read once, every distinct row once, the output written
     once, grad_out read once, each touched row's weights and momentum read and
@@ -206,8 +217,9 @@ def problem_roofline(w, rows_touched, r, peak):
     idx = w.n * INDEX_BYTES + (nb + 1) * INDEX_BYTES
     out = w.B * int(w.D.sum()) * 4
     fwd = idx + rows_touched * D * 2 + out
-    bwd = idx + out + rows_touched * (4 * D + 8)  # grad_out has the output's size
-    step = idx + 2 * out + rows_touched * (4 * D + 8)
+    upd = rows_touched * (4 * D + momentum_bytes(D, elementwise))
+    bwd = idx + out + upd  # grad_out has the output's size
+    step = idx + 2 * out + upd
     t = {"forward": r["pre_ms"] + r["fwd_ms"], "backward": r["pre_ms"] + r["upd_ms"],
          "step": r["ms"] / r["steps"]}
     res = {}
@@ -224,15 +236,21 @@ def run_native(args, world, rank, local):
 
     dev = torch.device("cuda", torch.cuda.current_device())
     E_scale = None if args.rows is None else args.rows / workloads.SPECS["hot"].E
-    w = workloads.make("hot", device=dev, seed=rank, T=args.tables, B=args.bags, E_scale=E_scale)
-    desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, dev)
+    wdt = torch.bfloat16 if args.weights == "bf16" else torch.float16
+    w = workloads.make("hot", device=dev, seed=rank, T=args.tables, B=args.bags, E_scale=E_scale,
+                       weights_dtype=wdt)
+    desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, dev, wdt)
     mean = args.pooling == "mean"
+    ew = args.optimizer == "elementwise"
     ws = tbe.Workspace(desc, w.n, False, dev, mean=mean)
-    weights, momentum = w.weights, w.momentum
+    weights = w.weights
+    momentum = (torch.zeros(desc.num_weights, dtype=torch.float32, device=dev) if ew
+                else w.momentum)
     out = torch.empty(w.B, desc.total_D, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     PRE = tbe.TBE_F_PREPROCESSED | (tbe.TBE_F_MEAN if mean else 0)
+    UPD = PRE | (tbe.TBE_F_ELEMENTWISE if ew else 0)
 
     def step(ev=None):
         # one preprocess of the batch's indices serves forward and backward
@@ -245,7 +263,7 @@ def run_native(args, world, rank, local):
         if ev is not None:
             ev[2].record(stream)
         tbe.tbe_backward_rowwise_adagrad(desc, w.grad_out, w.indices, w.offsets, None, weights,
-                                         momentum, w.lr, w.eps, ws, PRE)
+                                         momentum, w.lr, w.eps, ws, UPD)
         if ev is not None:
             ev[3].record(stream)
 
@@ -449,7 +467,8 @@ def main():
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     D = int(w.D[0])
-    kb = long_chunk_bytes(D, r["long_pairs"], r["n_chunks"], r["n_long"])
+    ew = args.optimizer == "elementwise"
+    kb = long_chunk_bytes(D, r["long_pairs"], r["n_chunks"], r["n_long"], ew)
     k_launch_ms = r["probe_ms"] / max(r["probe_launches"], 1)
     achieved = kb / (k_launch_ms / 1e3) / 1e9
     fwd_problem = forward_problem_bytes(w, r["R"] + r["n_hot"])
@@ -460,13 +479,18 @@ def main():
         "data": "synthetic",
         "config": {"workload": (WORKLOAD if (args.tables, args.rows, args.bags) == (None,) * 3 else
                                 f"reduced hot-row recipe T={w.T} E={int(w.E[0])} B={w.B} "
-                                "(profiling case)") +
+                                "(profiling case)").replace(
+                                    "fp16 weights", f"{args.weights} weights").replace(
+                                    "row-wise momentum",
+                                    "per-element momentum (element-wise Adagrad)" if ew
+                                    else "row-wise momentum") +
                                (", mean pooling" if args.pooling == "mean" else ""),
                    "n_lookups": w.n, "global_batch": w.B * world,
                    "parallelism": f"replicas x{world} (independent batches)",
                    "l2": f"inputs larger than L2 (indices {w.n * INDEX_BYTES / 1e9:.2f} GB, "
                          f"weights {w.weights.numel() * 2 / 1e9:.1f} GB); no flush",
-                   "storage": "fp16 weights, fp32 momentum/gradients"},
+                   "storage": f"{args.weights} weights, fp32 "
+                              f"{'per-element' if ew else 'per-row'} momentum, fp32 gradients"},
         "phases_ms": {"forward": r["fwd_ms"], "preprocess": r["pre_ms"], "update": r["upd_ms"]},
         "runs": {"R": r["R"], "long_runs": r["n_long"], "long_chunks": r["n_chunks"],
                  "cold_lookups": r["n_cold"], "hot_rows": r["n_hot"]},
@@ -483,7 +507,8 @@ def main():
                                "long_runs": r["n_long"]}},
         "forward_context": {"phase_ms": r["fwd_ms"],
                             "problem_min_GBps": fwd_problem / (r["fwd_ms"] / 1e3) / 1e9},
-        "problem_roofline": problem_roofline(w, r["R"] + r["n_hot"], dict(r, steps=args.steps), hbm),
+        "problem_roofline": problem_roofline(w, r["R"] + r["n_hot"], dict(r, steps=args.steps), hbm,
+                                             ew),
         "clocks": r["clocks"],
         "gpu_launches": r["launches"],
     }

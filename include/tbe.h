@@ -93,6 +93,16 @@ enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3, TBE_DT_BF16 = 4 };
                                            sized with TBE_WS_MEAN); bags of 0 or 1
                                            lookups are not scaled.  The small-table path
                                            is not taken. */
+#define TBE_F_ELEMENTWISE (1u << 6)     /* backward: element-wise Adagrad (the HugeCTR
+                                           page's Adagrad kernel, one accumulator per
+                                           weight element): momentum is fp32 laid out
+                                           like the weights (weights_offsets[T]
+                                           entries, 16-byte aligned), and every element
+                                           takes m_c <- m_c + g_c^2 and
+                                           W[r, c] <- rn(W[r, c] - lr * g_c /
+                                           (sqrt(m_c) + eps)).  The rows, runs, hot
+                                           rows and summation are as in the row-wise
+                                           update. */
 
 /* workspace-size flags */
 #define TBE_WS_WEIGHTED (1u << 0)       /* reserve room for per-sample weights */
@@ -218,9 +228,12 @@ tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* of
  *   g_c   = sum_i psw_i * grad_out[b_i, D_offsets[t] + c]        (fp32)
  *   m_r  <- m_r + (1/D_t) * sum_c g_c^2
  *   W_t[r, c] <- fp16_rn(W_t[r, c] - lr * g_c / (sqrt(m_r) + eps))
- * exactly once per touched row; untouched rows are not written.
- * grad_out: fp32 device [B, total_D]; weights (fp16) and momentum (fp32
- * [total_E]) are updated in place.  Without TBE_F_PREPROCESSED the call runs
+ * exactly once per touched row; untouched rows are not written (fp16_rn is
+ * bf16_rn for TBE_DT_BF16 weights; TBE_F_ELEMENTWISE replaces the row
+ * accumulator by one per element, see the flag).
+ * grad_out: fp32 device [B, total_D]; weights (16-bit) and momentum (fp32
+ * [total_E], or [weights_offsets[T]] with TBE_F_ELEMENTWISE) are updated in
+ * place.  Without TBE_F_PREPROCESSED the call runs
  * tbe_preprocess first.  The gradient of a hot row (see tbe_preprocess) is
  * its histogram column times grad_out, summed over bag partitions in a fixed
  * order; every other row's gradient is summed over its sorted run.  Both are
@@ -275,7 +288,7 @@ tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits);
  * the array: serialise them.
  *
  * Arguments as tbe_backward_rowwise_adagrad without workspace; flags may hold
- * TBE_F_LONG_TWO_LAUNCH and TBE_F_MEAN (no bounds reporting: the status word
+ * TBE_F_LONG_TWO_LAUNCH, TBE_F_MEAN and TBE_F_ELEMENTWISE (no bounds reporting: the status word
  * lives in the caller's workspace elsewhere; invalid rows are still skipped).
  * Errors: TBE_EINVAL, TBE_EUNSUPPORTED, TBE_ETOO_LARGE, TBE_ECUDA. */
 tbe_status tbe_backward_rowwise_adagrad_noalloc(const tbe_desc* d, const float* grad_out,

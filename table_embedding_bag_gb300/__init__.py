@@ -23,7 +23,7 @@ __all__ = [
     "TableBatchedEmbedding", "lib_path", "tbe_backward_rowwise_adagrad_noalloc",
     "TBE_NOALLOC_SCRATCH_BYTES", "TBE_ETOO_LARGE",
     "TBE_F_CHECK_BOUNDS", "TBE_F_REPAIR_OFFSETS", "TBE_F_FORCE_GENERIC", "TBE_F_LONG_TWO_LAUNCH",
-    "TBE_F_PREPROCESSED", "TBE_F_MEAN", "TBE_WS_WEIGHTED", "TBE_WS_MEAN", "TBE_ERR_INDEX_RANGE", "TBE_ERR_OFFSETS",
+    "TBE_F_PREPROCESSED", "TBE_F_MEAN", "TBE_F_ELEMENTWISE", "TBE_WS_WEIGHTED", "TBE_WS_MEAN", "TBE_ERR_INDEX_RANGE", "TBE_ERR_OFFSETS",
 ]
 
 TBE_OK, TBE_EINVAL, TBE_EWORKSPACE, TBE_EUNSUPPORTED, TBE_ECUDA, TBE_ETOO_LARGE = range(6)
@@ -35,6 +35,7 @@ TBE_F_FORCE_GENERIC = 1 << 2
 TBE_F_LONG_TWO_LAUNCH = 1 << 3
 TBE_F_PREPROCESSED = 1 << 4
 TBE_F_MEAN = 1 << 5
+TBE_F_ELEMENTWISE = 1 << 6
 TBE_WS_MEAN = 1 << 1
 TBE_WS_WEIGHTED = 1 << 0
 TBE_ERR_INDEX_RANGE = 1 << 0
@@ -295,17 +296,23 @@ def tbe_probe_read():
 
 
 class TableBatchedEmbedding:
-    """Owns 16-bit weights (fp16, or bf16), fp32 row-wise momentum and a
-    workspace for one problem shape; forward() and backward() call the C ABI."""
+    """Owns 16-bit weights (fp16, or bf16), fp32 Adagrad momentum (one value
+    per row, or per weight element with elementwise=True) and a workspace for
+    one problem shape; forward() and backward() call the C ABI."""
 
     def __init__(self, E, D, B, n_max, index_dtype=torch.int64, weighted=False, weights=None,
-                 momentum=None, lr=0.01, eps=1e-8, device="cuda", weights_dtype=torch.float16):
+                 momentum=None, lr=0.01, eps=1e-8, device="cuda", weights_dtype=torch.float16,
+                 elementwise=False):
         self.desc = TBEDesc(E, D, B, index_dtype, device, weights_dtype)
         self.ws = Workspace(self.desc, n_max, weighted, device)
         self.weights = weights if weights is not None else torch.zeros(
             self.desc.num_weights, dtype=weights_dtype, device=device)
+        self.elementwise = elementwise
+        n_mom = self.desc.num_weights if elementwise else self.desc.total_E
         self.momentum = momentum if momentum is not None else torch.zeros(
-            self.desc.total_E, dtype=torch.float32, device=device)
+            n_mom, dtype=torch.float32, device=device)
+        if self.momentum.numel() != n_mom:
+            raise ValueError(f"momentum must have {n_mom} entries")
         self.lr, self.eps = lr, eps
         self.out = torch.empty(self.desc.B, self.desc.total_D, dtype=torch.float32, device=device)
 
@@ -316,4 +323,4 @@ class TableBatchedEmbedding:
     def backward(self, grad_out, indices, offsets, per_sample_weights=None, flags=0):
         tbe_backward_rowwise_adagrad(self.desc, grad_out, indices, offsets, per_sample_weights,
                                      self.weights, self.momentum, self.lr, self.eps, self.ws,
-                                     flags)
+                                     flags | (TBE_F_ELEMENTWISE if self.elementwise else 0))

@@ -80,7 +80,8 @@ cudaError_t launch_hot_grad(const Launch& L, const WsLayout& W, char* ws, const 
 
 // update.cu: short-run and long-run row-wise Adagrad.
 cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const float* grad_out,
-                          void* weights, float* momentum, float lr, float eps, bool two_launch);
+                          void* weights, float* momentum, float lr, float eps, bool two_launch,
+                          bool elementwise = false);
 // Mean pooling's backward input: out[b, D_off[t] + c] = grad_out[b, D_off[t] + c]
 // times bag (t, b)'s factor from inv_len.
 cudaError_t launch_scale_grad(const Launch& L, const float* grad_out, const float* inv_len,

@@ -80,7 +80,9 @@ extern "C" tbe_status tbe_backward_rowwise_adagrad_noalloc(
   if (!grad_out || !weights || !momentum) return TBE_EINVAL;
   if ((reinterpret_cast<uintptr_t>(grad_out) & 15u) || (reinterpret_cast<uintptr_t>(weights) & 15u))
     return TBE_EINVAL;
-  if (flags & ~(TBE_F_LONG_TWO_LAUNCH | TBE_F_MEAN)) return TBE_EINVAL;
+  if (flags & ~(TBE_F_LONG_TWO_LAUNCH | TBE_F_MEAN | TBE_F_ELEMENTWISE)) return TBE_EINVAL;
+  const bool elementwise = (flags & TBE_F_ELEMENTWISE) != 0;
+  if (elementwise && (reinterpret_cast<uintptr_t>(momentum) & 15u)) return TBE_EINVAL;
   const bool mean = (flags & TBE_F_MEAN) != 0;
   const WsLayout W = make_layout(d, n, (per_sample_weights ? TBE_WS_WEIGHTED : 0u) |
                                            (mean ? TBE_WS_MEAN : 0u));
@@ -109,6 +111,6 @@ extern "C" tbe_status tbe_backward_rowwise_adagrad_noalloc(
     grad_out = scaled;
   }
   e = launch_update(L, W, scratch, grad_out, weights, momentum, lr, eps,
-                    (flags & TBE_F_LONG_TWO_LAUNCH) != 0);
+                    (flags & TBE_F_LONG_TWO_LAUNCH) != 0, elementwise);
   return e == cudaSuccess ? TBE_OK : TBE_ECUDA;
 }

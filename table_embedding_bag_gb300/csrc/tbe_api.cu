@@ -301,6 +301,8 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_desc* d, const float* grad_out
   if (st != TBE_OK) return st;
   if (!grad_out || !weights || !momentum || !aligned16(grad_out) || !aligned16(weights))
     return TBE_EINVAL;
+  const bool elementwise = (flags & TBE_F_ELEMENTWISE) != 0;
+  if (elementwise && !aligned16(momentum)) return TBE_EINVAL;  // float4 accumulator rows
   const Launch L{d, n, static_cast<cudaStream_t>(stream), device_sms()};
   char* ws = static_cast<char*>(workspace);
   const void* off_eff = offsets;
@@ -323,7 +325,7 @@ tbe_status tbe_backward_rowwise_adagrad(const tbe_desc* d, const float* grad_out
     grad_out = scaled;
   }
   return from_cuda(launch_update(L, W, ws, grad_out, weights, momentum, lr, eps,
-                                 (flags & TBE_F_LONG_TWO_LAUNCH) != 0));
+                                 (flags & TBE_F_LONG_TWO_LAUNCH) != 0, elementwise));
 }
 
 tbe_status tbe_workspace_view(const tbe_desc* d, int64_t n, uint32_t ws_flags, void* workspace,

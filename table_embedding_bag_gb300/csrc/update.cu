@@ -168,17 +168,61 @@ __device__ __forceinline__ void load_row(const __half* row, int nv, uint2 (&w_ra
   }
 }
 
-// Row-wise Adagrad on one row with the summed gradient held by the S lanes
-// of a group (lane sl owns vectors sl + c*S).  w_raw / m_old are the row's
-// 16-bit weights (4 per vector; fp16, or bf16 when a.bf16) and momentum,
-// already loaded; the new weight is rounded to nearest even in its own type.  Every lane of
-// the warp must call it (the sum of squares is a group shuffle).
-template <int S, int NC>
+// Four weights of a row after their Adagrad step w - lr * g / den, each
+// rounded to nearest even in the weights' own 16-bit type (bf16 when a.bf16).
+__device__ __forceinline__ uint2 adagrad_step4(const UpdArgs& a, uint2 raw, const float (&g)[4],
+                                               const float (&den)[4]) {
+  if (a.bf16) {
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+    const float2 w01 = __bfloat1622float2(h[0]);
+    const float2 w23 = __bfloat1622float2(h[1]);
+    h[0] = __floats2bfloat162_rn(w01.x - a.lr * g[0] / den[0], w01.y - a.lr * g[1] / den[1]);
+    h[1] = __floats2bfloat162_rn(w23.x - a.lr * g[2] / den[2], w23.y - a.lr * g[3] / den[3]);
+  } else {
+    __half2* h = reinterpret_cast<__half2*>(&raw);
+    const float2 w01 = __half22float2(h[0]);
+    const float2 w23 = __half22float2(h[1]);
+    h[0] = __floats2half2_rn(w01.x - a.lr * g[0] / den[0], w01.y - a.lr * g[1] / den[1]);
+    h[1] = __floats2half2_rn(w23.x - a.lr * g[2] / den[2], w23.y - a.lr * g[3] / den[3]);
+  }
+  return raw;
+}
+
+// Adagrad on one row with the summed gradient held by the S lanes of a group
+// (lane sl owns vectors sl + c*S).  w_raw / m_old are the row's 16-bit
+// weights (4 per vector; fp16, or bf16 when a.bf16) and row momentum, already
+// loaded; the new weight is rounded to nearest even in its own type.
+// Row-wise (default): m += mean_d g_d^2, one denominator for the row; every
+// lane of the warp must call it (the sum of squares is a group shuffle).
+// Element-wise (kEw): momentum holds
+// one accumulator per weight element at the weight's own flat position, each
+// element takes m_d += g_d^2 and its own denominator; m_old is unused.
+template <int S, int NC, bool kEw>
 __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4], int D,
                                               uint32_t key, __half* row, const uint2 (&w_raw)[NC],
                                               float m_old, bool active) {
   const int sl = static_cast<int>(lane_id()) % S;
   const int nv = D >> 2;
+  if constexpr (kEw) {
+    if (!active) return;
+    float* mrow = a.momentum + (row - a.W);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const int vec = sl + c * S;
+      if (vec < nv) {
+        float4 m = *reinterpret_cast<const float4*>(mrow + vec * 4);
+        m.x = fmaf(g[c][0], g[c][0], m.x);
+        m.y = fmaf(g[c][1], g[c][1], m.y);
+        m.z = fmaf(g[c][2], g[c][2], m.z);
+        m.w = fmaf(g[c][3], g[c][3], m.w);
+        const float den[4] = {sqrtf(m.x) + a.eps, sqrtf(m.y) + a.eps, sqrtf(m.z) + a.eps,
+                              sqrtf(m.w) + a.eps};
+        *reinterpret_cast<uint2*>(row + vec * 4) = adagrad_step4(a, w_raw[c], g[c], den);
+        *reinterpret_cast<float4*>(mrow + vec * 4) = m;
+      }
+    }
+    return;
+  }
   float ss = 0.f;
 #pragma unroll
   for (int c = 0; c < NC; ++c)
@@ -190,26 +234,11 @@ __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4
   if (!active) return;
   const float m_new = m_old + ss / static_cast<float>(D);
   const float denom = sqrtf(m_new) + a.eps;
+  const float den[4] = {denom, denom, denom, denom};
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     const int vec = sl + c * S;
-    if (vec < nv) {
-      uint2 raw = w_raw[c];
-      if (a.bf16) {
-        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
-        const float2 w01 = __bfloat1622float2(h[0]);
-        const float2 w23 = __bfloat1622float2(h[1]);
-        h[0] = __floats2bfloat162_rn(w01.x - a.lr * g[c][0] / denom, w01.y - a.lr * g[c][1] / denom);
-        h[1] = __floats2bfloat162_rn(w23.x - a.lr * g[c][2] / denom, w23.y - a.lr * g[c][3] / denom);
-      } else {
-        __half2* h = reinterpret_cast<__half2*>(&raw);
-        const float2 w01 = __half22float2(h[0]);
-        const float2 w23 = __half22float2(h[1]);
-        h[0] = __floats2half2_rn(w01.x - a.lr * g[c][0] / denom, w01.y - a.lr * g[c][1] / denom);
-        h[1] = __floats2half2_rn(w23.x - a.lr * g[c][2] / denom, w23.y - a.lr * g[c][3] / denom);
-      }
-      *reinterpret_cast<uint2*>(row + vec * 4) = raw;
-    }
+    if (vec < nv) *reinterpret_cast<uint2*>(row + vec * 4) = adagrad_step4(a, w_raw[c], g[c], den);
   }
   if (sl == 0) a.momentum[key] = m_new;
 }
@@ -247,7 +276,7 @@ __device__ __forceinline__ ShortTask fetch_task(const UpdArgs& a, const Meta& m,
 
 // Group g of the warp owns one run: its pairs are loaded S at a time, one
 // per lane of the group, and gathered U at a time.
-template <int S, int NC, bool kWeighted>
+template <int S, int NC, bool kWeighted, bool kEw>
 __device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, const ShortTask& st) {
   // Row vectors in flight per lane: short runs hold few pairs, so the warp's
   // G concurrent runs, not a deep unroll, hide the latency.
@@ -293,7 +322,7 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, cons
       for (int uu = 0; uu < U; ++uu) fma_rows<NC>(acc, v[uu], wv[uu]);
     }
   }
-  adagrad_apply<S, NC>(a, acc, D, key, row, w_raw, m_old, active);
+  adagrad_apply<S, NC, kEw>(a, acc, D, key, row, w_raw, m_old, active);
 }
 
 // kWide: the instantiation for rows wider than 512 values (eight vectors per
@@ -306,7 +335,7 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, cons
 // U = 8 / NC rows in flight per lane, and a butterfly adds the groups' sums
 // (each group sums its pairs in order; the groups are combined in a fixed
 // pattern).  A run of many pairs costs one round trip per G U pairs.
-template <int R, int NC, bool kWeighted>
+template <int R, int NC, bool kWeighted, bool kEw>
 __device__ __forceinline__ void warp_run(const UpdArgs& a, const Meta& m, int t, uint32_t p0,
                                          uint32_t np, uint32_t key) {
   constexpr int G = 32 / R;
@@ -354,14 +383,14 @@ __device__ __forceinline__ void warp_run(const UpdArgs& a, const Meta& m, int t,
     for (int c = 0; c < NC; ++c)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[c][i] += __shfl_xor_sync(kFull, acc[c][i], off);
-  adagrad_apply<R, NC>(a, acc, D, key, row, w_raw, m_old, g == 0);
+  adagrad_apply<R, NC, kEw>(a, acc, D, key, row, w_raw, m_old, g == 0);
 }
 
 // Medium runs (kMediumRun <= pairs < kLongThreshold, listed by the
 // preprocess): one warp per run.
 // kNarrow: every table of the launch is at most 128 wide (one vector per
 // lane), so the wider paths, which set the register budget, are left out.
-template <bool kWeighted, bool kNarrow>
+template <bool kWeighted, bool kNarrow, bool kEw>
 __global__ void __launch_bounds__(256, kNarrow ? 3 : 2)
     medium_runs_kernel(UpdArgs a, const uint32_t* __restrict__ medium_run) {
   __shared__ MetaSmem msm;
@@ -382,17 +411,17 @@ __global__ void __launch_bounds__(256, kNarrow ? 3 : 2)
     const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
     if (D < 8 || D > kMaxD || (D & 7)) continue;  // widths the vector path cannot move
     const int nv = D >> 2;
-    if (nv <= 4) warp_run<4, 1, kWeighted>(a, m, t, p0, np, key);
-    else if (nv <= 8) warp_run<8, 1, kWeighted>(a, m, t, p0, np, key);
-    else if (nv <= 16) warp_run<16, 1, kWeighted>(a, m, t, p0, np, key);
-    else if (kNarrow || nv <= 32) warp_run<32, 1, kWeighted>(a, m, t, p0, np, key);
-    else if (nv <= 64) warp_run<32, 2, kWeighted>(a, m, t, p0, np, key);
-    else if (nv <= 128) warp_run<32, 4, kWeighted>(a, m, t, p0, np, key);
-    else warp_run<32, 8, kWeighted>(a, m, t, p0, np, key);
+    if (nv <= 4) warp_run<4, 1, kWeighted, kEw>(a, m, t, p0, np, key);
+    else if (nv <= 8) warp_run<8, 1, kWeighted, kEw>(a, m, t, p0, np, key);
+    else if (nv <= 16) warp_run<16, 1, kWeighted, kEw>(a, m, t, p0, np, key);
+    else if (kNarrow || nv <= 32) warp_run<32, 1, kWeighted, kEw>(a, m, t, p0, np, key);
+    else if (nv <= 64) warp_run<32, 2, kWeighted, kEw>(a, m, t, p0, np, key);
+    else if (nv <= 128) warp_run<32, 4, kWeighted, kEw>(a, m, t, p0, np, key);
+    else warp_run<32, 8, kWeighted, kEw>(a, m, t, p0, np, key);
   }
 }
 
-template <bool kWeighted, bool kWide>
+template <bool kWeighted, bool kWide, bool kEw>
 __global__ void __launch_bounds__(256, TBE_SHORT_MINB) short_runs_kernel(UpdArgs a) {
   __shared__ MetaSmem msm;
   const Meta m = load_meta(a, msm, true);
@@ -404,14 +433,14 @@ __global__ void __launch_bounds__(256, TBE_SHORT_MINB) short_runs_kernel(UpdArgs
     const ShortTask next = fetch_task(a, m, task + warps, ntasks);  // one task ahead
     const int nv = cur.nv;
     if (cur.t >= 0 && (nv > 128) == kWide) {
-      if (kWide) short_task<32, 8, kWeighted>(a, m, cur);
-      else if (nv <= 2) short_task<2, 1, kWeighted>(a, m, cur);
-      else if (nv <= 4) short_task<4, 1, kWeighted>(a, m, cur);
-      else if (nv <= 8) short_task<8, 1, kWeighted>(a, m, cur);
-      else if (nv <= 16) short_task<8, 2, kWeighted>(a, m, cur);
-      else if (nv <= 32) short_task<8, 4, kWeighted>(a, m, cur);
-      else if (nv <= 64) short_task<16, 4, kWeighted>(a, m, cur);
-      else short_task<32, 4, kWeighted>(a, m, cur);
+      if (kWide) short_task<32, 8, kWeighted, kEw>(a, m, cur);
+      else if (nv <= 2) short_task<2, 1, kWeighted, kEw>(a, m, cur);
+      else if (nv <= 4) short_task<4, 1, kWeighted, kEw>(a, m, cur);
+      else if (nv <= 8) short_task<8, 1, kWeighted, kEw>(a, m, cur);
+      else if (nv <= 16) short_task<8, 2, kWeighted, kEw>(a, m, cur);
+      else if (nv <= 32) short_task<8, 4, kWeighted, kEw>(a, m, cur);
+      else if (nv <= 64) short_task<16, 4, kWeighted, kEw>(a, m, cur);
+      else short_task<32, 4, kWeighted, kEw>(a, m, cur);
     }
     cur = next;
   }
@@ -533,7 +562,7 @@ __device__ __forceinline__ bool arrive_last(uint32_t* counter) {
 
 // The whole warp applies the update of one long run's row (every lane holds
 // the summed gradient; group 0's lanes write).
-template <int S, int NC>
+template <int S, int NC, bool kEw>
 __device__ __forceinline__ void finish_long_row(const UpdArgs& a, const Meta& m,
                                                 const LongRunInfo& ri, float (&acc)[NC][4]) {
   const int t = static_cast<int>(ri.table);
@@ -543,10 +572,10 @@ __device__ __forceinline__ void finish_long_row(const UpdArgs& a, const Meta& m,
   uint2 w_raw[NC];
   load_row<S, NC>(row, D >> 2, w_raw, writer);
   const float m_old = a.momentum[ri.key];
-  adagrad_apply<S, NC>(a, acc, D, ri.key, row, w_raw, m_old, writer);
+  adagrad_apply<S, NC, kEw>(a, acc, D, ri.key, row, w_raw, m_old, writer);
 }
 
-template <int S, int NC, bool kWeighted>
+template <int S, int NC, bool kWeighted, bool kEw>
 __device__ __forceinline__ void long_chunk(const UpdArgs& a, const Meta& m, const ChunkDesc& cd,
                                            const LongRunInfo& ri, bool two_launch) {
   const int t = static_cast<int>(ri.table);
@@ -556,7 +585,7 @@ __device__ __forceinline__ void long_chunk(const UpdArgs& a, const Meta& m, cons
   float acc[NC][4];
   sum_pairs<S, NC, kWeighted>(a, d0, nv, cd.first, cd.end, acc);
   if (ri.nch == 1 && !two_launch) {
-    finish_long_row<S, NC>(a, m, ri, acc);
+    finish_long_row<S, NC, kEw>(a, m, ri, acc);
     return;
   }
   store_partial<S, NC>(a.partials + static_cast<int64_t>(ri.chunk0 + cd.c) * a.max_D, nv, acc);
@@ -576,7 +605,7 @@ __device__ __forceinline__ void long_chunk(const UpdArgs& a, const Meta& m, cons
                                                a.max_D;
     sum_partials<S, NC>(src, a.max_D, kids, nv, acc);
     if (here == 1) {
-      finish_long_row<S, NC>(a, m, ri, acc);
+      finish_long_row<S, NC, kEw>(a, m, ri, acc);
       return;
     }
     store_partial<S, NC>(a.tree_part + static_cast<int64_t>(ri.tree0 + level_off + i) * a.max_D, nv,
@@ -587,7 +616,7 @@ __device__ __forceinline__ void long_chunk(const UpdArgs& a, const Meta& m, cons
   }
 }
 
-template <bool kWeighted, bool kWide>
+template <bool kWeighted, bool kWide, bool kEw>
 __global__ void __launch_bounds__(256, TBE_LONG_MINB) long_chunks_kernel(UpdArgs a, bool two_launch) {
   __shared__ MetaSmem msm;
   const Meta m = load_meta(a, msm, false);
@@ -601,30 +630,30 @@ __global__ void __launch_bounds__(256, TBE_LONG_MINB) long_chunks_kernel(UpdArgs
     if (D < 8 || D > kMaxD || (D & 7)) continue;
     const int nv = D >> 2;
     if ((nv > 128) != kWide) continue;
-    if (kWide) long_chunk<32, 8, kWeighted>(a, m, cd, ri, two_launch);
-    else if (nv <= 2) long_chunk<2, 1, kWeighted>(a, m, cd, ri, two_launch);
-    else if (nv <= 4) long_chunk<4, 1, kWeighted>(a, m, cd, ri, two_launch);
-    else if (nv <= 8) long_chunk<8, 1, kWeighted>(a, m, cd, ri, two_launch);
-    else if (nv <= 16) long_chunk<8, 2, kWeighted>(a, m, cd, ri, two_launch);
-    else if (nv <= 32) long_chunk<8, 4, kWeighted>(a, m, cd, ri, two_launch);
-    else if (nv <= 64) long_chunk<16, 4, kWeighted>(a, m, cd, ri, two_launch);
-    else long_chunk<32, 4, kWeighted>(a, m, cd, ri, two_launch);
+    if (kWide) long_chunk<32, 8, kWeighted, kEw>(a, m, cd, ri, two_launch);
+    else if (nv <= 2) long_chunk<2, 1, kWeighted, kEw>(a, m, cd, ri, two_launch);
+    else if (nv <= 4) long_chunk<4, 1, kWeighted, kEw>(a, m, cd, ri, two_launch);
+    else if (nv <= 8) long_chunk<8, 1, kWeighted, kEw>(a, m, cd, ri, two_launch);
+    else if (nv <= 16) long_chunk<8, 2, kWeighted, kEw>(a, m, cd, ri, two_launch);
+    else if (nv <= 32) long_chunk<8, 4, kWeighted, kEw>(a, m, cd, ri, two_launch);
+    else if (nv <= 64) long_chunk<16, 4, kWeighted, kEw>(a, m, cd, ri, two_launch);
+    else long_chunk<32, 4, kWeighted, kEw>(a, m, cd, ri, two_launch);
   }
 }
 
 // Two-launch variant, second kernel: one warp per long run sums the run's
 // chunk partials in chunk order and applies the update.
-template <int S, int NC>
+template <int S, int NC, bool kEw>
 __device__ __forceinline__ void finish_run(const UpdArgs& a, const Meta& m, const LongRunInfo& ri) {
   const int t = static_cast<int>(ri.table);
   const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
   float acc[NC][4];
   sum_partials<S, NC>(a.partials + static_cast<int64_t>(ri.chunk0) * a.max_D, a.max_D, ri.nch,
                       D >> 2, acc);
-  finish_long_row<S, NC>(a, m, ri, acc);
+  finish_long_row<S, NC, kEw>(a, m, ri, acc);
 }
 
-template <bool kWide>
+template <bool kWide, bool kEw>
 __global__ void __launch_bounds__(256, 3) long_finish_kernel(UpdArgs a) {
   __shared__ MetaSmem msm;
   const Meta m = load_meta(a, msm, false);
@@ -637,14 +666,14 @@ __global__ void __launch_bounds__(256, 3) long_finish_kernel(UpdArgs a) {
     if (D < 8 || D > kMaxD || (D & 7)) continue;
     const int nv = D >> 2;
     if ((nv > 128) != kWide) continue;
-    if (kWide) finish_run<32, 8>(a, m, ri);
-    else if (nv <= 2) finish_run<2, 1>(a, m, ri);
-    else if (nv <= 4) finish_run<4, 1>(a, m, ri);
-    else if (nv <= 8) finish_run<8, 1>(a, m, ri);
-    else if (nv <= 16) finish_run<8, 2>(a, m, ri);
-    else if (nv <= 32) finish_run<8, 4>(a, m, ri);
-    else if (nv <= 64) finish_run<16, 4>(a, m, ri);
-    else finish_run<32, 4>(a, m, ri);
+    if (kWide) finish_run<32, 8, kEw>(a, m, ri);
+    else if (nv <= 2) finish_run<2, 1, kEw>(a, m, ri);
+    else if (nv <= 4) finish_run<4, 1, kEw>(a, m, ri);
+    else if (nv <= 8) finish_run<8, 1, kEw>(a, m, ri);
+    else if (nv <= 16) finish_run<8, 2, kEw>(a, m, ri);
+    else if (nv <= 32) finish_run<8, 4, kEw>(a, m, ri);
+    else if (nv <= 64) finish_run<16, 4, kEw>(a, m, ri);
+    else finish_run<32, 4, kEw>(a, m, ri);
   }
 }
 
@@ -655,6 +684,7 @@ __global__ void __launch_bounds__(256, 3) long_finish_kernel(UpdArgs a) {
 // partitions w, w + 8, ... in order, warp 0 adds the eight warp sums in order
 // (a fixed order, so the result is reproducible), then applies the row-wise
 // Adagrad step.
+template <bool kEw>
 __global__ void __launch_bounds__(256)
     hot_finish_kernel(UpdArgs a, const uint32_t* __restrict__ hot_keys,
                       const uint32_t* __restrict__ hot_n, const uint32_t* __restrict__ hot_cnt,
@@ -703,7 +733,7 @@ __global__ void __launch_bounds__(256)
   uint2 w_raw[2];
   load_row<32, 2>(row, nv, w_raw, true);
   const float m_old = a.momentum[key];
-  adagrad_apply<32, 2>(a, acc, D, key, row, w_raw, m_old, true);
+  adagrad_apply<32, 2, kEw>(a, acc, D, key, row, w_raw, m_old, true);
 }
 
 // ------------------------------------------------------ hot set refresh
@@ -927,10 +957,40 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The cold runs' update kernels (short, medium, long chunks, and the second
+// long-run kernel in the two-launch variant) on L's stream, in that order.
+template <bool kEw>
+void launch_runs(const Launch& L, const UpdArgs& a, const uint32_t* medium, unsigned blocks,
+                 bool weighted, bool wide, bool two_launch) {
+  if (weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, false, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  else { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, false, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  {
+    const bool narrow = a.max_D <= 128;
+    probe_begin(TBE_PROBE_MEDIUM_RUNS, L.s);
+    if (weighted && narrow) medium_runs_kernel<true, true, kEw><<<blocks, 256, 0, L.s>>>(a, medium);
+    else if (weighted) medium_runs_kernel<true, false, kEw><<<blocks, 256, 0, L.s>>>(a, medium);
+    else if (narrow) medium_runs_kernel<false, true, kEw><<<blocks, 256, 0, L.s>>>(a, medium);
+    else medium_runs_kernel<false, false, kEw><<<blocks, 256, 0, L.s>>>(a, medium);
+    note_launch();
+    probe_end(TBE_PROBE_MEDIUM_RUNS, L.s);
+  }
+  if (wide && weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, true, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  if (wide && !weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, true, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  if (weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, false, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  else { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, false, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  if (wide && weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, true, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  if (wide && !weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, true, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  if (two_launch) {
+    { long_finish_kernel<false, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
+    if (wide) { long_finish_kernel<true, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const float* grad_out,
-                          void* weights, float* momentum, float lr, float eps, bool two_launch) {
+                          void* weights, float* momentum, float lr, float eps, bool two_launch,
+                          bool elementwise) {
   const tbe_desc* d = L.d;
   const int fin = radix_passes(d) & 1;
   UpdArgs a;
@@ -981,8 +1041,13 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
     const float* part = reinterpret_cast<const float*>(ws + W.hot_part);
     e = launch_hot_grad(Ls, W, ws, grad_out);
     if (e != cudaSuccess) return e;
-    { hot_finish_kernel<<<static_cast<unsigned>(d->T) * kHot, 256, 0, Ls.s>>>(
-        a, hot_keys, hot_n, hot_cnt, W.hot_parts, part); note_launch(); }
+    if (elementwise)
+      hot_finish_kernel<true><<<static_cast<unsigned>(d->T) * kHot, 256, 0, Ls.s>>>(
+          a, hot_keys, hot_n, hot_cnt, W.hot_parts, part);
+    else
+      hot_finish_kernel<false><<<static_cast<unsigned>(d->T) * kHot, 256, 0, Ls.s>>>(
+          a, hot_keys, hot_n, hot_cnt, W.hot_parts, part);
+    note_launch();
     e = cudaEventRecord(sf->hot, Ls.s);
     if (e != cudaSuccess) return e;
     e = cudaEventRecord(sf->done, Ls.s);
@@ -993,29 +1058,9 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
     cudaError_t e = cudaStreamWaitEvent(L.s, sf->sorted, 0);
     if (e != cudaSuccess) return e;
   }
-  if (weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
-  else { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   const uint32_t* medium = reinterpret_cast<const uint32_t*>(ws + W.medium_run);
-  {
-    const bool narrow = d->max_D <= 128;
-    probe_begin(TBE_PROBE_MEDIUM_RUNS, L.s);
-    if (weighted && narrow) medium_runs_kernel<true, true><<<blocks, 256, 0, L.s>>>(a, medium);
-    else if (weighted) medium_runs_kernel<true, false><<<blocks, 256, 0, L.s>>>(a, medium);
-    else if (narrow) medium_runs_kernel<false, true><<<blocks, 256, 0, L.s>>>(a, medium);
-    else medium_runs_kernel<false, false><<<blocks, 256, 0, L.s>>>(a, medium);
-    note_launch();
-    probe_end(TBE_PROBE_MEDIUM_RUNS, L.s);
-  }
-  if (wide && weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
-  if (wide && !weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, true><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
-  if (weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, false><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
-  else { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, false><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
-  if (wide && weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, true><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
-  if (wide && !weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, true><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
-  if (two_launch) {
-    { long_finish_kernel<false><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
-    if (wide) { long_finish_kernel<true><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
-  }
+  if (elementwise) launch_runs<true>(L, a, medium, blocks, weighted, wide, two_launch);
+  else launch_runs<false>(L, a, medium, blocks, weighted, wide, two_launch);
   if (!W.hot_enabled) return cudaGetLastError();  // no histogram: the hot set stays empty
   // Choose the next hot set, once the hot rows' update has read this one.
   cudaError_t e = cudaStreamWaitEvent(L.s, sf->hot, 0);

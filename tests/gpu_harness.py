@@ -31,8 +31,10 @@ def host(w):
 class Run:
     """One TBE problem on the GPU through the C ABI."""
 
-    def __init__(self, w, device="cuda", mean=False, weights_dtype=torch.float16):
+    def __init__(self, w, device="cuda", mean=False, weights_dtype=torch.float16,
+                 elementwise=False):
         self.w = w
+        self.ew_flag = tbe.TBE_F_ELEMENTWISE if elementwise else 0
         self.desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, device, weights_dtype)
         self.ws = tbe.Workspace(self.desc, max(w.n, 1), w.psw is not None, device, mean=mean)
         d = lambda x: None if x is None else x.to(device).contiguous()
@@ -72,7 +74,7 @@ class Run:
     def backward(self, flags=0):
         tbe.tbe_backward_rowwise_adagrad(self.desc, self.grad_out, self.indices, self.offsets,
                                          self.psw, self.weights, self.momentum, self.w.lr,
-                                         self.w.eps, self.ws, flags)
+                                         self.w.eps, self.ws, flags | self.ew_flag)
         torch.cuda.synchronize()
         return self.host_weights(), self.momentum.cpu().numpy()
 
@@ -156,6 +158,89 @@ def assert_bf16_step_close(bits, ref_bits, old_bits, upd_rel=2.0 ** -12, max_fra
     print("bf16 step:", detail)
     assert not bad.any(), detail
     assert beyond.sum() <= max_frac * err.size, detail
+
+
+def _touched_elements(tab, B, indices, offsets):
+    """Per touched row (ascending linear key): its lookups' count, and the
+    flat weight positions of its elements with their column numbers."""
+    offsets = np.asarray(offsets, np.int64)
+    idx = np.asarray(indices, np.int64)
+    bag = np.repeat(np.arange(len(offsets) - 1), np.diff(offsets))
+    t = bag // B
+    E = np.asarray(tab.E, np.int64)
+    ok = (idx >= 0) & (idx < E[t])
+    keys = np.asarray(tab.hash_base, np.int64)[t[ok]] + idx[ok]
+    ukeys, count = np.unique(keys, return_counts=True)
+    kt = np.searchsorted(np.asarray(tab.hash_base, np.int64), ukeys, side="right") - 1
+    D = np.asarray(tab.D, np.int64)[kt]
+    base = np.asarray(tab.w_offsets, np.int64)[kt] + (ukeys - np.asarray(tab.hash_base)[kt]) * D
+    row = np.repeat(np.arange(len(ukeys)), D)
+    col = np.arange(row.size) - np.repeat(np.cumsum(D) - D, D)
+    return ukeys, count, row, np.repeat(base, D) + col, col
+
+
+def assert_elementwise_step_close(tab, B, indices, offsets, grad_out, psw, mean, lr, eps,
+                                  w_old, m_old, w_gpu, m_gpu, w_ref, m_ref, bf16=False,
+                                  max_loose=1e-3):
+    """Element-wise Adagrad results against the oracle's, with an error bound
+    derived from the arithmetic.  Each element's gradient g is an fp32 sum of
+    n terms; whatever the order, it lies within d = (n + 10) 2^-24 S of the
+    exact sum, S the sum of the terms' magnitudes (from the oracle on |grad|,
+    |psw|): n - 1 additions, the products with per-sample weights and mean
+    factors, and for hot rows the tensor-core products, whose split operands
+    drop a remainder term of about 2^-21 of each product.  The accumulator m = m_old + g^2 is then off by at most
+    (2|g| + d) d plus two fp32 roundings, and the step lr g / (sqrt(m) + eps)
+    by what those two errors move it, plus its own fp32 rounding; the stored
+    weight may differ by that plus one unit in the last place.  Touched
+    elements must meet the bound, at most max_loose of them may need more
+    than 1e-5 (momentum) or 1 ulp (weights), and untouched elements must be
+    bit-identical to the inputs."""
+    u = 2.0 ** -24
+    ukeys, count, row, flat, col = _touched_elements(tab, B, indices, offsets)
+    keys, g = oracle.row_gradients(tab, B, indices, offsets, grad_out, psw, mean)
+    absp = None if psw is None else np.abs(psw)
+    keys_a, S = oracle.row_gradients(tab, B, indices, offsets, np.abs(grad_out), absp, mean)
+    assert np.array_equal(keys.astype(np.int64), ukeys) and np.array_equal(keys_a, keys)
+    g = g[row, col]
+    S = S[row, col]
+    d = (count[row] + 10) * u * S
+    # momentum
+    mr = m_ref[flat].astype(np.float64)
+    mg = m_gpu[flat].astype(np.float64)
+    dm = 4 * u * mr + (2 * np.abs(g) + d) * d
+    bad = np.abs(mg - mr) > dm
+    assert not bad.any(), f"{bad.sum()} of {flat.size} accumulators beyond the fp32 bound"
+    loose = np.abs(mg - mr) > 1e-5 * mr
+    assert loose.sum() <= max_loose * flat.size, f"{loose.sum()} accumulators beyond 1e-5"
+    # weights
+    if bf16:
+        val = lambda x: bf16_values(x)
+        spacing = lambda v: np.spacing(np.abs(v).astype(np.float32)).astype(np.float64) * 65536.0
+    else:
+        val = lambda x: np.asarray(x, np.float16).astype(np.float64)
+        spacing = lambda v: np.spacing(np.abs(v).astype(np.float16)).astype(np.float64)
+    wo = val(w_old)[flat]
+    wr = val(w_ref)[flat]
+    wg = val(w_gpu)[flat]
+    lo = np.sqrt(np.maximum(mr - dm, 0.0)) + eps
+    hi = np.sqrt(mr + dm) + eps
+    step = lr * np.abs(g) / lo
+    ds = lr * d / lo + lr * np.abs(g) * (1.0 / lo - 1.0 / hi) + 8 * u * step
+    tol = ds + 2 * u * (np.abs(wo) + step) + np.maximum(spacing(wr), spacing(wg))
+    err = np.abs(wg - wr)
+    bad = err > tol
+    assert not bad.any(), f"{bad.sum()} of {flat.size} weights beyond the fp32 bound"
+    loose = err > spacing(wr)
+    assert loose.sum() <= max_loose * flat.size, f"{loose.sum()} weights beyond 1 ulp"
+    # untouched elements unchanged
+    mask = np.ones(np.asarray(m_gpu).size, bool)
+    mask[flat] = False
+    assert np.array_equal(np.asarray(m_gpu).view(np.uint32)[mask],
+                          np.asarray(m_old, np.float32).view(np.uint32)[mask])
+    assert np.array_equal(np.asarray(w_gpu).view(np.uint16)[mask],
+                          np.asarray(w_old).view(np.uint16)[mask])
+    print(f"element-wise step: {flat.size} touched elements; beyond 1e-5 / 1 ulp: "
+          f"{int((np.abs(mg - mr) > 1e-5 * mr).sum())} / {int(loose.sum())}")
 
 
 def assert_bf16_within_ulp(bits, ref_bits, ulps=1):

@@ -140,3 +140,15 @@ def test_probe_selection_and_empty_record(lib):
     assert lib.tbe_probe_set(tbe.TBE_PROBE_LONG_CHUNKS) == tbe.TBE_OK
     assert tbe.tbe_probe_read() == (0, 0.0)
     assert lib.tbe_probe_set(tbe.TBE_PROBE_OFF) == tbe.TBE_OK
+
+
+def test_binding_constants_match_the_header():
+    import re
+    text = open(os.path.join(ROOT, "include", "tbe.h")).read()
+    defs = dict(re.findall(r"#define (TBE_(?:F|WS|ERR)_\w+) \((1u? << \d+)\)", text))
+    assert defs, "no flag definitions found"
+    for name, expr in defs.items():
+        assert getattr(tbe, name) == eval(expr.replace("1u", "1")), name
+    enum = re.search(r"enum \{ (TBE_DT_[^}]*)\}", text).group(1)
+    for name, val in re.findall(r"(TBE_DT_\w+) = (\d+)", enum):
+        assert getattr(tbe, name) == int(val), name
