@@ -298,13 +298,15 @@ def tbe_probe_read():
 class TableBatchedEmbedding:
     """Owns 16-bit weights (fp16, or bf16), fp32 Adagrad momentum (one value
     per row, or per weight element with elementwise=True) and a workspace for
-    one problem shape; forward() and backward() call the C ABI."""
+    one problem shape; forward() and backward() call the C ABI, with mean
+    pooling throughout when mean=True."""
 
     def __init__(self, E, D, B, n_max, index_dtype=torch.int64, weighted=False, weights=None,
                  momentum=None, lr=0.01, eps=1e-8, device="cuda", weights_dtype=torch.float16,
-                 elementwise=False):
+                 elementwise=False, mean=False):
         self.desc = TBEDesc(E, D, B, index_dtype, device, weights_dtype)
-        self.ws = Workspace(self.desc, n_max, weighted, device)
+        self.ws = Workspace(self.desc, n_max, weighted, device, mean=mean)
+        self.mean = mean
         self.weights = weights if weights is not None else torch.zeros(
             self.desc.num_weights, dtype=weights_dtype, device=device)
         self.elementwise = elementwise
@@ -318,9 +320,10 @@ class TableBatchedEmbedding:
 
     def forward(self, indices, offsets, per_sample_weights=None, flags=0):
         return tbe_forward(self.desc, self.weights, indices, offsets, per_sample_weights,
-                           self.out, self.ws, flags)
+                           self.out, self.ws, flags | (TBE_F_MEAN if self.mean else 0))
 
     def backward(self, grad_out, indices, offsets, per_sample_weights=None, flags=0):
         tbe_backward_rowwise_adagrad(self.desc, grad_out, indices, offsets, per_sample_weights,
                                      self.weights, self.momentum, self.lr, self.eps, self.ws,
-                                     flags | (TBE_F_ELEMENTWISE if self.elementwise else 0))
+                                     flags | (TBE_F_ELEMENTWISE if self.elementwise else 0) |
+                                     (TBE_F_MEAN if self.mean else 0))

@@ -152,3 +152,26 @@ def test_binding_constants_match_the_header():
     enum = re.search(r"enum \{ (TBE_DT_[^}]*)\}", text).group(1)
     for name, val in re.findall(r"(TBE_DT_\w+) = (\d+)", enum):
         assert getattr(tbe, name) == int(val), name
+
+
+def test_module_sizes_state_and_passes_its_flags(monkeypatch):
+    # built on the host (no device memory needed); the C calls are captured
+    emb = tbe.TableBatchedEmbedding([10, 4], [8, 16], 3, 64, device="cpu",
+                                    weights_dtype=torch.bfloat16, elementwise=True, mean=True)
+    assert emb.weights.dtype == torch.bfloat16 and emb.weights.numel() == 10 * 8 + 4 * 16
+    assert emb.momentum.numel() == emb.weights.numel()  # one accumulator per element
+    assert emb.ws.nbytes == tbe.tbe_workspace_size(emb.desc, 64, mean=True)
+    assert tbe.TableBatchedEmbedding([10, 4], [8, 16], 3, 64, device="cpu").momentum.numel() == 14
+    with pytest.raises(ValueError):
+        tbe.TableBatchedEmbedding([10], [8], 3, 64, device="cpu", elementwise=True,
+                                  momentum=torch.zeros(10))
+    seen = {}
+    monkeypatch.setattr(tbe, "tbe_forward", lambda *a: seen.setdefault("fwd", a[-1]))
+    monkeypatch.setattr(tbe, "tbe_backward_rowwise_adagrad",
+                        lambda *a: seen.setdefault("bwd", a[-1]))
+    idx = torch.zeros(2, dtype=torch.int64)
+    off = torch.tensor([0, 1, 1, 1, 2, 2, 2], dtype=torch.int64)
+    emb.forward(idx, off)
+    emb.backward(torch.zeros(3, 24), idx, off, flags=tbe.TBE_F_PREPROCESSED)
+    assert seen["fwd"] == tbe.TBE_F_MEAN
+    assert seen["bwd"] == tbe.TBE_F_PREPROCESSED | tbe.TBE_F_ELEMENTWISE | tbe.TBE_F_MEAN
