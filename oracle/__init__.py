@@ -114,21 +114,27 @@ class Tables:
         self.w_offsets = np.concatenate([[0], np.cumsum(self.E * self.D)]).astype(np.int64)
 
 
-def _weight_bits(weights, bf16):
-    """16-bit weight patterns: fp16 values (numpy float16), or, with bf16,
-    bfloat16 bit patterns given as uint16."""
+def _weight_bits(weights, bf16, fp32=False):
+    """The weights as the oracle reads them: fp16 values (numpy float16) as
+    16-bit patterns; with bf16, bfloat16 bit patterns given as uint16; with
+    fp32, float32 values."""
+    if bf16 and fp32:
+        raise ValueError("one weight type at a time")
+    if fp32:
+        return np.ascontiguousarray(weights, dtype=np.float32), 2
     if bf16:
         return np.ascontiguousarray(weights, dtype=np.uint16), 1
     return np.ascontiguousarray(weights, dtype=np.float16).view(np.uint16), 0
 
 
-def forward(tables: Tables, B, weights, indices, offsets, psw=None, mean=False, bf16=False):
+def forward(tables: Tables, B, weights, indices, offsets, psw=None, mean=False, bf16=False,
+            fp32=False):
     """Pooled forward; returns fp32 [B, sum D].  mean: each bag's sum times
     1/L for its L > 1 lookups (HugeCTR's mean combiner).  bf16: weights are
-    bfloat16 bit patterns (uint16)."""
+    bfloat16 bit patterns (uint16); fp32: weights are float32."""
     lib = _load()
     indices, offsets, bits = _idx(indices, offsets)
-    w, wtype = _weight_bits(weights, bf16)
+    w, wtype = _weight_bits(weights, bf16, fp32)
     psw = _c(psw, np.float32)
     out = np.zeros((B, int(tables.D_offsets[-1])), dtype=np.float32)
     rc = lib.oracle_forward(tables.T, B, _p(tables.D_offsets), _p(tables.hash_base),
@@ -193,15 +199,18 @@ def row_gradients(tables: Tables, B, indices, offsets, grad_out, psw=None, mean=
 
 
 def backward_rowwise_adagrad(tables: Tables, B, indices, offsets, grad_out, weights, momentum,
-                             lr, eps, psw=None, mean=False, bf16=False, elementwise=False):
+                             lr, eps, psw=None, mean=False, bf16=False, elementwise=False,
+                             fp32=False):
     """Returns (new_weights, new_momentum fp32); inputs are not modified.
     mean: each bag's gradient times 1/L for its L > 1 lookups, before grouping.
-    bf16: weights (in and out) are bfloat16 bit patterns (uint16), else fp16.
+    bf16: weights (in and out) are bfloat16 bit patterns (uint16); fp32:
+    float32 weights; else fp16.
     elementwise: HugeCTR's element-wise Adagrad, momentum shaped like the
     flat weights (one accumulator per element), instead of one per row."""
     lib = _load()
     indices, offsets, bits = _idx(indices, offsets)
-    w = np.array(weights, dtype=np.uint16 if bf16 else np.float16, copy=True)
+    w, wtype = _weight_bits(weights, bf16, fp32)
+    w = w.copy()
     m = np.array(momentum, dtype=np.float32, copy=True)
     if m.size != (int(tables.w_offsets[-1]) if elementwise else int(tables.hash_base[-1])):
         raise ValueError("momentum has one entry per weight element (elementwise) or per row")
@@ -210,11 +219,11 @@ def backward_rowwise_adagrad(tables: Tables, B, indices, offsets, grad_out, weig
     rc = lib.oracle_backward_rowwise_adagrad(tables.T, B, _p(tables.D_offsets),
                                              _p(tables.hash_base), _p(tables.w_offsets), bits,
                                              _p(indices), _p(offsets), len(indices), _p(psw),
-                                             _p(grad_out), int(bool(mean)), int(bool(bf16)),
+                                             _p(grad_out), int(bool(mean)), wtype,
                                              int(bool(elementwise)), float(lr), float(eps),
-                                             _p(w.view(np.uint16)), _p(m))
+                                             _p(w), _p(m))
     _check(rc, "backward")
-    return w, m
+    return (w.view(np.float16) if wtype == 0 else w), m
 
 
 def backward_selected(tables: Tables, B, indices, offsets, grad_out, lr, eps, sel_keys, w_rows,

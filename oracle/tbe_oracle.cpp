@@ -35,7 +35,10 @@
 // Readings where the pages are silent (each is listed in the design notes):
 //  * bags are table-major: bag (t,b) has id t*B+b, offsets has T*B+1 entries;
 //  * a lookup whose row is outside [0, E_t) contributes nothing (skipped);
-//  * weights are fp16 (or bf16), rounded to nearest-even from the double result;
+//  * weights are fp16 (or bf16, or fp32), rounded to nearest-even from the
+//    double result; every type is pooled in double (the page pools fp32
+//    weights in fp64 and 16-bit ones in fp32: both are within the double
+//    sum's rounding of the exact sum);
 //  * momentum is fp32, rounded from the double sum m_old + mean_d(g_d^2)
 //    (element-wise: m_old_d + g_d^2 per element).
 //
@@ -134,13 +137,26 @@ uint16_t double_to_bf16_bits(double x) {
   return sign | static_cast<uint16_t>(((e + 127) << 7) | (static_cast<int>(q) - 128));
 }
 
-// The weights' element type: 0 fp16, 1 bf16.
-double weight_to_double(uint16_t h, int wtype) {
-  return wtype ? bf16_bits_to_double(h) : half_bits_to_double(h);
-}
-uint16_t double_to_weight(double x, int wtype) {
-  return wtype ? double_to_bf16_bits(x) : double_to_half_bits(x);
-}
+// A flat weight array of one element type (wtype): 0 fp16 and 1 bf16 (16-bit
+// patterns), 2 fp32.  Elements are read exactly as doubles and written
+// rounded to nearest even in the array's own type (fp32 by the language's
+// double-to-float conversion, which rounds to nearest even).
+struct WeightArray {
+  void* base;
+  int wtype;
+  double get(int64_t i) const {
+    if (wtype == 2) return static_cast<double>(static_cast<const float*>(base)[i]);
+    const uint16_t h = static_cast<const uint16_t*>(base)[i];
+    return wtype == 1 ? bf16_bits_to_double(h) : half_bits_to_double(h);
+  }
+  void set(int64_t i, double x) const {
+    if (wtype == 2) {
+      static_cast<float*>(base)[i] = static_cast<float>(x);
+      return;
+    }
+    static_cast<uint16_t*>(base)[i] = wtype == 1 ? double_to_bf16_bits(x) : double_to_half_bits(x);
+  }
+};
 
 int64_t load_int(const void* p, int bits, int64_t i) {
   if (bits == 32) return static_cast<const int32_t*>(p)[i];
@@ -148,14 +164,15 @@ int64_t load_int(const void* p, int bits, int64_t i) {
 }
 
 // Pool one bag: out[d] = (float) (scale * sum_k coef_k * row_k[d]), summed in
-// double in ascending k.  coef == nullptr means every coefficient is 1.
-void pool_rows(int64_t L, int D, const uint16_t* const* rows, const float* coef, float* out,
-               double scale = 1.0, int wtype = 0) {
+// double in ascending k; row k starts at element row_start[k] of W.
+// coef == nullptr means every coefficient is 1.
+void pool_rows(int64_t L, int D, const WeightArray& W, const int64_t* row_start,
+               const float* coef, float* out, double scale = 1.0) {
   for (int d = 0; d < D; ++d) {
     double s = 0.0;
     for (int64_t k = 0; k < L; ++k) {
       const double w = coef ? static_cast<double>(coef[k]) : 1.0;
-      s += w * weight_to_double(rows[k][d], wtype);
+      s += w * W.get(row_start[k] + d);
     }
     out[d] = static_cast<float>(s * scale);
   }
@@ -179,17 +196,19 @@ void sum_run_gradient(int64_t SL, int D, const float* const* grads, const float*
 
 // Exact row-wise Adagrad on one row, given its summed gradient g[0..D):
 //   m <- m + (1/D) sum_d g_d^2          (stored as fp32)
-//   w_d <- w_d - lr * g_d / (sqrt(m) + eps)   (stored as fp16, nearest-even)
-void rowwise_adagrad(int D, const double* g, float lr, float eps, uint16_t* w, float* m,
-                     int wtype = 0) {
+//   w_d <- w_d - lr * g_d / (sqrt(m) + eps)   (stored in the weight type,
+//                                              nearest-even); the row starts
+//                                              at element w0 of W
+void rowwise_adagrad(int D, const double* g, float lr, float eps, const WeightArray& W,
+                     int64_t w0, float* m) {
   double ss = 0.0;
   for (int d = 0; d < D; ++d) ss += g[d] * g[d];
   const float m_new = static_cast<float>(static_cast<double>(*m) + ss / static_cast<double>(D));
   *m = m_new;
   const double denom = std::sqrt(static_cast<double>(m_new)) + static_cast<double>(eps);
   for (int d = 0; d < D; ++d) {
-    const double w_old = weight_to_double(w[d], wtype);
-    w[d] = double_to_weight(w_old - static_cast<double>(lr) * g[d] / denom, wtype);
+    const double w_old = W.get(w0 + d);
+    W.set(w0 + d, w_old - static_cast<double>(lr) * g[d] / denom);
   }
 }
 
@@ -272,13 +291,15 @@ uint16_t oracle_double_to_bf16(double x) { return double_to_bf16_bits(x); }
 // Pooled forward over every bag: out[b, D_offsets[t] + d] for all t, b, d.
 // out is fp32 row-major [B, D_offsets[T]].
 int oracle_forward(int T, int B, const int64_t* D_offsets, const int64_t* hash_base,
-                   const int64_t* w_offsets, const uint16_t* weights, int index_bits,
+                   const int64_t* w_offsets, const void* weights, int index_bits,
                    const void* indices, const void* offsets, int64_t n, const float* psw,
                    int mean, int wtype, float* out) {
   Problem p{T, B, D_offsets, hash_base, w_offsets, index_bits, indices, offsets, n, psw};
   if (!offsets_ok(p)) return ORACLE_EINVAL;
+  if (wtype < 0 || wtype > 2) return ORACLE_EINVAL;
+  const WeightArray W{const_cast<void*>(weights), wtype};
   const int64_t sumD = D_offsets[T];
-  std::vector<const uint16_t*> rows;
+  std::vector<int64_t> rows;
   std::vector<float> coef;
   for (int t = 0; t < T; ++t) {
     const int D = static_cast<int>(p.D(t));
@@ -289,11 +310,11 @@ int oracle_forward(int T, int B, const int64_t* D_offsets, const int64_t* hash_b
       for (int64_t i = p.off(bag); i < p.off(bag + 1); ++i) {
         const int64_t r = p.idx(i);
         if (!p.valid(t, r)) continue;
-        rows.push_back(weights + w_offsets[t] + r * D);
+        rows.push_back(w_offsets[t] + r * D);
         coef.push_back(psw ? psw[i] : 1.0f);
       }
-      pool_rows(static_cast<int64_t>(rows.size()), D, rows.data(), coef.data(),
-                out + b * sumD + D_offsets[t], mean ? p.mean_scale(bag) : 1.0, wtype);
+      pool_rows(static_cast<int64_t>(rows.size()), D, W, rows.data(), coef.data(),
+                out + b * sumD + D_offsets[t], mean ? p.mean_scale(bag) : 1.0);
     }
   }
   return ORACLE_OK;
@@ -305,13 +326,14 @@ int oracle_forward(int T, int B, const int64_t* D_offsets, const int64_t* hash_b
 // workloads too large to hold on the host.
 int oracle_pool_gathered(int64_t nbags, int D, const int64_t* bag_off, const uint16_t* rows,
                          const float* coef, float* out) {
-  std::vector<const uint16_t*> rp;
+  const WeightArray W{const_cast<uint16_t*>(rows), 0};
+  std::vector<int64_t> rp;
   for (int64_t j = 0; j < nbags; ++j) {
     const int64_t L = bag_off[j + 1] - bag_off[j];
     if (L < 0) return ORACLE_EINVAL;
     rp.resize(L);
-    for (int64_t k = 0; k < L; ++k) rp[k] = rows + (bag_off[j] + k) * D;
-    pool_rows(L, D, rp.data(), coef ? coef + bag_off[j] : nullptr, out + j * D);
+    for (int64_t k = 0; k < L; ++k) rp[k] = (bag_off[j] + k) * D;
+    pool_rows(L, D, W, rp.data(), coef ? coef + bag_off[j] : nullptr, out + j * D);
   }
   return ORACLE_OK;
 }
@@ -405,14 +427,14 @@ int oracle_row_gradients(int T, int B, const int64_t* D_offsets, const int64_t* 
 // accumulator is per weight element), given its summed gradient g[0..D):
 //   m_d <- m_d + g_d^2                          (stored as fp32)
 //   w_d <- w_d - lr * g_d / (sqrt(m_d) + eps)   (stored in the weight type)
-void elementwise_adagrad(int D, const double* g, float lr, float eps, uint16_t* w, float* m,
-                         int wtype) {
+void elementwise_adagrad(int D, const double* g, float lr, float eps, const WeightArray& W,
+                         int64_t w0, float* m) {
   for (int d = 0; d < D; ++d) {
     const float m_new = static_cast<float>(static_cast<double>(m[d]) + g[d] * g[d]);
     m[d] = m_new;
     const double denom = std::sqrt(static_cast<double>(m_new)) + static_cast<double>(eps);
-    const double w_old = weight_to_double(w[d], wtype);
-    w[d] = double_to_weight(w_old - static_cast<double>(lr) * g[d] / denom, wtype);
+    const double w_old = W.get(w0 + d);
+    W.set(w0 + d, w_old - static_cast<double>(lr) * g[d] / denom);
   }
 }
 
@@ -424,9 +446,11 @@ int oracle_backward_rowwise_adagrad(int T, int B, const int64_t* D_offsets,
                                     int index_bits, const void* indices, const void* offsets,
                                     int64_t n, const float* psw, const float* grad_out,
                                     int mean, int wtype, int elementwise, float lr, float eps,
-                                    uint16_t* weights, float* momentum) {
+                                    void* weights, float* momentum) {
   Problem p{T, B, D_offsets, hash_base, w_offsets, index_bits, indices, offsets, n, psw};
   if (!offsets_ok(p)) return ORACLE_EINVAL;
+  if (wtype < 0 || wtype > 2) return ORACLE_EINVAL;
+  const WeightArray W{weights, wtype};
   const int64_t sumD = D_offsets[T];
   auto runs = group_by_row(p);
   std::vector<const float*> gp;
@@ -448,11 +472,11 @@ int oracle_backward_rowwise_adagrad(int T, int B, const int64_t* D_offsets,
     g.assign(D, 0.0);
     sum_run_gradient(static_cast<int64_t>(gp.size()), D, gp.data(), coef.data(), g.data(),
                      mean ? bs.data() : nullptr);
-    uint16_t* w = weights + w_offsets[t] + r * D;
+    const int64_t w0 = w_offsets[t] + r * D;
     if (elementwise)
-      elementwise_adagrad(D, g.data(), lr, eps, w, momentum + w_offsets[t] + r * D, wtype);
+      elementwise_adagrad(D, g.data(), lr, eps, W, w0, momentum + w0);
     else
-      rowwise_adagrad(D, g.data(), lr, eps, w, momentum + kv.first, wtype);
+      rowwise_adagrad(D, g.data(), lr, eps, W, w0, momentum + kv.first);
   }
   return ORACLE_OK;
 }
@@ -506,7 +530,7 @@ int oracle_backward_selected(int T, int B, const int64_t* D_offsets, const int64
     g.assign(D, 0.0);
     sum_run_gradient(static_cast<int64_t>(gp.size()), D, gp.data(), coef.data(), g.data(),
                      mean ? bs.data() : nullptr);
-    rowwise_adagrad(D, g.data(), lr, eps, w_rows + j * maxD, m_rows + j);
+    rowwise_adagrad(D, g.data(), lr, eps, WeightArray{w_rows, 0}, j * maxD, m_rows + j);
   }
   return ORACLE_OK;
 }

@@ -627,3 +627,70 @@ def test_elementwise_momentum_must_be_shaped_like_the_weights():
         oracle.backward_rowwise_adagrad(tab, 1, np.array([1]), np.array([0, 1]),
                                         np.ones((1, 8), np.float32), np.zeros(32, np.float16),
                                         np.zeros(4, np.float32), 0.1, 1e-8, elementwise=True)
+
+
+# -------------------------------------------------------------- fp32 weights
+# The FBTriton page pools fp32 weights in fp64.  The oracle reads fp32
+# weights exactly, sums in double and rounds the result once.
+
+@pytest.mark.parametrize("seed", range(3))
+def test_forward_fp32_brute_force_exact_rational(oracle_lib, seed):
+    # fp32 weights with full 24-bit significands (not representable in 16-bit
+    # types); the exact rational sum rounded once to fp32 is the answer
+    tab, B, idx, off, W, G, psw = _tiny_problem(seed + 60, weighted=seed != 2)
+    rng = np.random.default_rng(200 + seed)
+    Wf = (rng.standard_normal(len(W)) * (1 + rng.random(len(W)) * 2.0 ** -12)).astype(np.float32)
+    out = oracle.forward(tab, B, Wf, idx, off, psw, fp32=True)
+    exp = np.zeros_like(out, dtype=object)
+    exp[:] = Fraction(0)
+    for t, b, i, r in _lookups(tab, B, idx, off):
+        if not 0 <= r < tab.E[t]:
+            continue
+        c = Fraction(float(psw[i])) if psw is not None else Fraction(1)
+        base = int(tab.w_offsets[t]) + r * int(tab.D[t])
+        for d in range(int(tab.D[t])):
+            exp[b, int(tab.D_offsets[t]) + d] += c * Fraction(float(Wf[base + d]))
+    exact = np.array([[float(x) for x in row] for row in exp])
+    ulp = np.spacing(np.abs(exact).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(out.astype(np.float64) - exact) <= 0.5 * ulp + 1e-300)
+    # the 16-bit readings of the same bits would not give this result
+    assert not np.array_equal(out, oracle.forward(tab, B, Wf.astype(np.float16), idx, off, psw))
+
+
+@pytest.mark.parametrize("elementwise", [False, True])
+def test_adagrad_fp32_keeps_full_precision(oracle_lib, elementwise):
+    # From m = 0 with eps = 0 and a row of equal |g|, both Adagrad forms step
+    # every element by exactly lr against the sign of g.  w0 = 1 + 2^-20 and
+    # lr = 2^-10 make w0 -+ lr exact in fp32 but not in fp16 or bf16.
+    D = 8
+    tab = oracle.Tables([3], [D])
+    w0 = np.float32(1 + 2.0 ** -20)
+    W = np.full(3 * D, np.float32(0.3), np.float32)
+    W[D:2 * D] = w0
+    m = np.zeros(3 * D if elementwise else 3, np.float32)
+    v = np.array([0.5, -0.5, 0.5, 0.5, -0.5, -0.5, 0.5, -0.5], np.float32)
+    W2, m2 = oracle.backward_rowwise_adagrad(tab, 1, np.array([1], np.int64), np.array([0, 1]),
+                                             v.reshape(1, D), W, m, 2.0 ** -10, 0.0,
+                                             elementwise=elementwise, fp32=True)
+    assert W2.dtype == np.float32
+    exp = np.where(v > 0, 1 + 2.0 ** -20 - 2.0 ** -10, 1 + 2.0 ** -20 + 2.0 ** -10)
+    assert np.array_equal(W2[D:2 * D].astype(np.float64), exp)
+    # untouched rows keep their (non-16-bit) values bit for bit
+    assert np.array_equal(W2[:D].view(np.uint32), W[:D].view(np.uint32))
+    assert np.array_equal(W2[2 * D:].view(np.uint32), W[2 * D:].view(np.uint32))
+
+
+def test_backward_fp32_agrees_with_fp16_on_fp16_values_when_nothing_rounds():
+    # Weights and steps that are exact in fp16 give the same result whichever
+    # type holds them: w0 = 0.5, lr = 0.125, eps = 0, |g| equal in the row.
+    D = 16
+    tab = oracle.Tables([2], [D])
+    rng = np.random.default_rng(4)
+    v = np.where(rng.random(D) < 0.5, -2.0, 2.0).astype(np.float32).reshape(1, D)
+    W16 = np.full(2 * D, np.float16(0.5))
+    W16[:D] = np.float16(0.25)
+    args = (tab, 1, np.array([1], np.int64), np.array([0, 1]), v)
+    Wa, ma = oracle.backward_rowwise_adagrad(*args, W16, np.zeros(2, np.float32), 0.125, 0.0)
+    Wb, mb = oracle.backward_rowwise_adagrad(*args, W16.astype(np.float32),
+                                             np.zeros(2, np.float32), 0.125, 0.0, fp32=True)
+    assert np.array_equal(Wa.astype(np.float32), Wb) and np.array_equal(ma, mb)
