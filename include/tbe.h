@@ -3,13 +3,14 @@
  *
  * Table Batched Embedding (TBE) pools lookups from many embedding tables in
  * one launch and trains them with a backward that regroups lookups by row and
- * applies exactly one exact row-wise Adagrad update per touched row.
+ * applies exactly one Adagrad update (row-wise, or element-wise) per touched
+ * row.
  *
  * Sources (page titles and sections):
  *  - "Modernizing Table Batched Embeddings with FBTriton", sections
  *    "Why redesign a sparse operator?" (what TBE combines), "Forward: keep a
  *    narrowly specialized path beside the general one" (generic gather-pool,
- *    fp32 accumulation of fp16 weights, int32 index option, small-table
+ *    fp32 accumulation of fp16/bf16 weights, int32 index option, small-table
  *    histogram path and its eligibility, bounds checks off by default),
  *    "Backward: invert 'which rows did this sample use?'" (transpose, sort,
  *    run-length encoding into runs, short/long runs, fenced last-chunk
@@ -20,14 +21,18 @@
  *  - "HugeCTR DistributedSlotSparseEmbeddingHash backward" (eqicode.com):
  *    CSR bags (row_offset / value), the sample-id expansion, radix sort by
  *    row with end_bit, run flags + prefix sum + run starts with a sentinel,
- *    and the Adagrad accumulator-then-weight order with eps outside the root.
+ *    and the Adagrad accumulator-then-weight order with eps outside the root
+ *    (one accumulator per element there; row-wise here by default), and the
+ *    sum/mean combiners with the mean backward's 1/L scaling.
  *
  * Data layout (all device buffers are owned by the caller):
  *  - T tables; table t has E_t rows of width D_t (D_t a multiple of 8, at
- *    most 1024).  Weights are fp16, one flat buffer; table t starts at element
- *    weights_offsets[t], its rows are contiguous with stride D_t.
+ *    most 1024).  Weights are fp16 or bf16 (weights_dtype), one flat buffer;
+ *    table t starts at element weights_offsets[t], its rows are contiguous
+ *    with stride D_t.
  *  - Momentum: fp32 [sum E_t], one value per row, row r of table t at
- *    hash_base[t] + r.
+ *    hash_base[t] + r; with TBE_F_ELEMENTWISE fp32 [weights_offsets[T]], one
+ *    value per weight element at the element's own position.
  *  - Bags are table-major: bag (t,b) has id t*B+b.  offsets: [T*B+1] of the
  *    index type, indices: [n], lookups of bag (t,b) at positions
  *    offsets[t*B+b] .. offsets[t*B+b+1]-1.  A lookup's row must lie in
@@ -186,12 +191,14 @@ tbe_status tbe_workspace_size(const tbe_desc* d, int64_t n_max, uint32_t ws_flag
  * (n >= 64 T B; shorter bags are pooled from the indices as without the
  * flag) the forward reads tbe_preprocess's results instead of the indices:
  * each table's hot rows are pooled as the per-bag histogram
- * times those rows on the tensor cores (tf32 with an exact remainder term:
- * the products are exact), the cold lookups are gathered from the per-bag
- * cold lists; the bounds/offsets flags are then ignored (the preprocess
+ * times those rows on the tensor cores (fp16 MMAs: counts up to 255 are exact
+ * fp16 values, larger or weighted counts are scaled per bag and split exactly
+ * into three fp16 parts, so only the fp32 accumulation rounds), the cold
+ * lookups are gathered from the per-bag cold lists (bf16 problems have no
+ * hot rows: every lookup is a cold one); the bounds/offsets flags are then ignored (the preprocess
  * checked them) and per_sample_weights must be NULL exactly when it was NULL
  * for the preprocess.
- * weights: fp16 device; indices/offsets: device, index_dtype; n: lookups
+ * weights: device, weights_dtype; indices/offsets: device, index_dtype; n: lookups
  * (length of indices); per_sample_weights: fp32 device [n] or NULL;
  * out: fp32 device [B, total_D], fully overwritten.  Workspace: the status
  * word plus (TBE_F_REPAIR_OFFSETS) the repaired offsets; ws_bytes must be at
