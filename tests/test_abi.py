@@ -175,3 +175,41 @@ def test_module_sizes_state_and_passes_its_flags(monkeypatch):
     emb.backward(torch.zeros(3, 24), idx, off, flags=tbe.TBE_F_PREPROCESSED)
     assert seen["fwd"] == tbe.TBE_F_MEAN
     assert seen["bwd"] == tbe.TBE_F_PREPROCESSED | tbe.TBE_F_ELEMENTWISE | tbe.TBE_F_MEAN
+
+
+@pytest.mark.parametrize("dims", [dict(T=2, B=4, E=(10, 20), D=(8, 16)),
+                                  dict(T=3, B=4096, E=(1000, 5, 70000), D=(128, 8, 1024))])
+def test_workspace_layout_invariants(lib, dims):
+    # Host arithmetic only (a fake base address, nothing dereferenced): every
+    # region lies inside the reported size at 256-byte alignment; the hot-row
+    # state sits at offsets that depend on the tables alone, so one workspace
+    # serves calls of any n, weighted or not, with or without mean pooling;
+    # the mean region is the last one.
+    d = _desc(**dims)
+    base = 1 << 40
+    lib.tbe_workspace_view.argtypes = [ctypes.POINTER(tbe.tbe_desc), ctypes.c_int64,
+                                       ctypes.c_uint32, ctypes.c_void_p,
+                                       ctypes.POINTER(tbe.tbe_ws_view)]
+    state = None
+    for n in (0, 1000, 1 << 20):
+        sizes = {}
+        for flags in (0, tbe.TBE_WS_WEIGHTED, tbe.TBE_WS_MEAN,
+                      tbe.TBE_WS_WEIGHTED | tbe.TBE_WS_MEAN):
+            rc, size = _ws_size(lib, d, n, flags)
+            assert rc == tbe.TBE_OK
+            sizes[flags] = size
+            v = tbe.tbe_ws_view()
+            assert lib.tbe_workspace_view(ctypes.byref(d), n, flags, base,
+                                          ctypes.byref(v)) == tbe.TBE_OK
+            ptrs = {name: getattr(v, name) for name, t in tbe.tbe_ws_view._fields_
+                    if t is ctypes.c_void_p and getattr(v, name)}
+            for name, p in ptrs.items():
+                assert base <= p < base + size, name
+                assert (p - base) % 256 == 0, name
+            assert ("sorted_psw" in ptrs) == bool(flags & tbe.TBE_WS_WEIGHTED)
+            here = (v.hot_keys, v.hot_n, v.counts)
+            state = state or here
+            assert here == state
+        grad = ((4 * dims["B"] * sum(dims["D"]) + 255) // 256) * 256
+        assert sizes[tbe.TBE_WS_MEAN] - sizes[0] == grad
+        assert sizes[tbe.TBE_WS_WEIGHTED | tbe.TBE_WS_MEAN] - sizes[tbe.TBE_WS_WEIGHTED] == grad
