@@ -180,6 +180,16 @@ def profiled_traffic():
     return int(fields["traffic_bytes_per_launch"])
 
 
+def workload_name(args, base=WORKLOAD):
+    """The workload string with the step's weight type, Adagrad form and
+    pooling."""
+    ew = args.optimizer == "elementwise"
+    return (base.replace("fp16 weights", f"{args.weights} weights").replace(
+        "row-wise momentum",
+        "per-element momentum (element-wise Adagrad)" if ew else "row-wise momentum") +
+        (", mean pooling" if args.pooling == "mean" else ""))
+
+
 def momentum_bytes(D, elementwise):
     """Momentum bytes a row's update reads and writes: one fp32 per row, or
     one per element with element-wise Adagrad."""
@@ -396,30 +406,40 @@ def cpu_sample(w_dev, bags):
     idx_dev = w_dev.indices[:int(off[-1])]
     uniq, inv = torch.unique(idx_dev, return_inverse=True)
     D0 = int(w_dev.D[0])
-    rows = w_dev.weights[:int(w_dev.E[0]) * D0].view(-1, D0)[uniq].cpu().numpy().reshape(-1)
+    rows = w_dev.weights[:int(w_dev.E[0]) * D0].view(-1, D0)[uniq].cpu().reshape(-1)
+    if rows.dtype != torch.bfloat16:
+        rows = rows.numpy()
     G0 = w_dev.grad_out[:bags, :D0].cpu().numpy()
     E0 = int(uniq.numel())
     return workloads.from_arrays([E0], [D0], bags, inv.cpu().numpy(), off, rows, G0,
                                  momentum=np.zeros(E0, np.float32), lr=w_dev.lr, eps=w_dev.eps)
 
 
-def time_oracle(s):
+def time_oracle(s, mean=False, elementwise=False):
+    """Seconds the oracle takes for one forward and backward of sample s, in
+    the step's pooling, weight type and Adagrad form."""
     import oracle
     oracle.build()
     tab = oracle.Tables(s.E, s.D)
     idx, off = s.indices.numpy(), s.offsets.numpy()
-    W, G, m = s.weights.numpy(), s.grad_out.numpy(), s.momentum.numpy()
+    bf16 = s.weights.dtype == torch.bfloat16
+    W = s.weights.view(torch.int16).numpy().view(np.uint16) if bf16 else s.weights.numpy()
+    G = s.grad_out.numpy()
+    m = (np.zeros(int(tab.w_offsets[-1]), np.float32) if elementwise
+         else s.momentum.numpy())
     t = time.perf_counter()
-    oracle.forward(tab, s.B, W, idx, off)
-    oracle.backward_rowwise_adagrad(tab, s.B, idx, off, G, W, m, s.lr, s.eps)
+    oracle.forward(tab, s.B, W, idx, off, mean=mean, bf16=bf16)
+    oracle.backward_rowwise_adagrad(tab, s.B, idx, off, G, W, m, s.lr, s.eps, mean=mean,
+                                    bf16=bf16, elementwise=elementwise)
     return time.perf_counter() - t
 
 
-def reference_sample(bags, seed=0):
+def reference_sample(bags, seed=0, weights_dtype=torch.float16):
     """The same recipe's table 0, drawn on the host: bags x 200 lookups, with
     only the touched rows materialised."""
     import workloads
-    return workloads.make("hot", device="cpu", seed=seed, B=bags, T=1, compact=True)
+    return workloads.make("hot", device="cpu", seed=seed, B=bags, T=1, compact=True,
+                          weights_dtype=weights_dtype)
 
 
 def main():
@@ -431,8 +451,9 @@ def main():
         bags = 2048
         times, lookups = [], 0
         for k in range(args.warmup + args.steps):
-            s = reference_sample(bags, seed=k)
-            dt = time_oracle(s)
+            s = reference_sample(bags, seed=k, weights_dtype=torch.bfloat16
+                                 if args.weights == "bf16" else torch.float16)
+            dt = time_oracle(s, args.pooling == "mean", args.optimizer == "elementwise")
             if k >= args.warmup:
                 times.append(dt)
                 lookups += s.n
@@ -443,7 +464,7 @@ def main():
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": f"table 0, {bags} bags x 200 lookups "
+            "config": {"workload": workload_name(args), "sample": f"table 0, {bags} bags x 200 lookups "
                                                      "per step (same recipe, host-drawn, "
                                                      "touched rows only)"},
             "cpu_baseline": {"value": value, "unit": "lookups/s", "cores": 1, "kind": "oracle",
@@ -477,14 +498,10 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": (WORKLOAD if (args.tables, args.rows, args.bags) == (None,) * 3 else
-                                f"reduced hot-row recipe T={w.T} E={int(w.E[0])} B={w.B} "
-                                "(profiling case)").replace(
-                                    "fp16 weights", f"{args.weights} weights").replace(
-                                    "row-wise momentum",
-                                    "per-element momentum (element-wise Adagrad)" if ew
-                                    else "row-wise momentum") +
-                               (", mean pooling" if args.pooling == "mean" else ""),
+        "config": {"workload": workload_name(
+                       args, WORKLOAD if (args.tables, args.rows, args.bags) == (None,) * 3
+                       else f"reduced hot-row recipe T={w.T} E={int(w.E[0])} B={w.B} "
+                            "(profiling case)"),
                    "n_lookups": w.n, "global_batch": w.B * world,
                    "parallelism": f"replicas x{world} (independent batches)",
                    "l2": f"inputs larger than L2 (indices {w.n * INDEX_BYTES / 1e9:.2f} GB, "
@@ -517,7 +534,7 @@ def main():
                        "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = cpu_sample(w, args.cpu_bags)
-        dt = time_oracle(s)
+        dt = time_oracle(s, args.pooling == "mean", args.optimizer == "elementwise")
         line["cpu_baseline"] = {"value": s.n / dt, "unit": "lookups/s", "cores": 1,
                                 "kind": "oracle",
                                 "sample": f"table 0, first {args.cpu_bags} bags "
