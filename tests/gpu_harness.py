@@ -184,11 +184,13 @@ def assert_elementwise_step_close(tab, B, indices, offsets, grad_out, psw, mean,
                                   max_loose=1e-3):
     """Element-wise Adagrad results against the oracle's, with an error bound
     derived from the arithmetic.  Each element's gradient g is an fp32 sum of
-    n terms; whatever the order, it lies within d = (n + 10) 2^-24 S of the
+    n terms; whatever the order, it lies within d = (2 n + 10) 2^-24 S of the
     exact sum, S the sum of the terms' magnitudes (from the oracle on |grad|,
-    |psw|): n - 1 additions, the products with per-sample weights and mean
-    factors, and for hot rows the tensor-core products, whose split operands
-    drop a remainder term of about 2^-21 of each product.  The accumulator m = m_old + g^2 is then off by at most
+    |psw|): n - 1 additions (each within 2^-23 of its result, which also
+    covers a tensor core's accumulator if it truncates rather than rounds),
+    the products with per-sample weights and mean factors, and for hot rows
+    the tensor-core products, whose split operands drop a remainder term of
+    about 2^-21 of each product.  The accumulator m = m_old + g^2 is then off by at most
     (2|g| + d) d plus two fp32 roundings, and the step lr g / (sqrt(m) + eps)
     by what those two errors move it, plus its own fp32 rounding; the stored
     weight may differ by that plus one unit in the last place.  Touched
@@ -203,7 +205,7 @@ def assert_elementwise_step_close(tab, B, indices, offsets, grad_out, psw, mean,
     assert np.array_equal(keys.astype(np.int64), ukeys) and np.array_equal(keys_a, keys)
     g = g[row, col]
     S = S[row, col]
-    d = (count[row] + 10) * u * S
+    d = (2 * count[row] + 10) * u * S
     # momentum
     mr = m_ref[flat].astype(np.float64)
     mg = m_gpu[flat].astype(np.float64)
