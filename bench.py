@@ -372,7 +372,7 @@ def run_native(args, world, rank, local):
                 h_out.copy_(out, non_blocking=True)
                 out_read.record(down)
             tbe.tbe_backward_rowwise_adagrad(desc, d_grad, d_idx, d_off, None, weights, momentum,
-                                             w.lr, w.eps, ws, PRE)
+                                             w.lr, w.eps, ws, UPD)
             consumed[k % 2].record(stream)
 
         for k in range(max(1, args.warmup)):
