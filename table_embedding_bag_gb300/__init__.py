@@ -208,8 +208,20 @@ def _check_tensors(desc, indices, offsets):
 
 
 def _check_weights(desc, weights):
-    if isinstance(weights, torch.Tensor) and weights.dtype != desc.weights_dtype:
-        raise TypeError(f"weights must be {desc.weights_dtype}")
+    if isinstance(weights, torch.Tensor):
+        if weights.dtype != desc.weights_dtype:
+            raise TypeError(f"weights must be {desc.weights_dtype}")
+        if weights.numel() < desc.num_weights:
+            raise ValueError(f"weights must hold {desc.num_weights} elements")
+
+
+def _check_momentum(desc, momentum, flags):
+    """The accumulators the update writes: one per row, or one per weight
+    element with TBE_F_ELEMENTWISE."""
+    if isinstance(momentum, torch.Tensor):
+        need = desc.num_weights if flags & TBE_F_ELEMENTWISE else desc.total_E
+        if momentum.dtype != torch.float32 or momentum.numel() < need:
+            raise ValueError(f"momentum must be float32 with {need} entries")
 
 
 def tbe_forward(desc: TBEDesc, weights, indices, offsets, per_sample_weights, out, ws: Workspace,
@@ -238,6 +250,7 @@ def tbe_backward_rowwise_adagrad(desc: TBEDesc, grad_out, indices, offsets, per_
     on weights and momentum; see include/tbe.h."""
     _check_tensors(desc, indices, offsets)
     _check_weights(desc, weights)
+    _check_momentum(desc, momentum, flags)
     _ok("tbe_backward_rowwise_adagrad", _load().tbe_backward_rowwise_adagrad(
         desc.ref, _ptr(grad_out), _ptr(indices), _ptr(offsets), indices.numel(),
         _ptr(per_sample_weights), _ptr(weights), _ptr(momentum), float(lr), float(eps), ws.ptr,
@@ -252,6 +265,7 @@ def tbe_backward_rowwise_adagrad_noalloc(desc: TBEDesc, grad_out, indices, offse
     include/tbe.h for the scratch limit and the rules on overlapping calls)."""
     _check_tensors(desc, indices, offsets)
     _check_weights(desc, weights)
+    _check_momentum(desc, momentum, flags)
     _ok("tbe_backward_rowwise_adagrad_noalloc", _load().tbe_backward_rowwise_adagrad_noalloc(
         desc.ref, _ptr(grad_out), _ptr(indices), _ptr(offsets), indices.numel(),
         _ptr(per_sample_weights), _ptr(weights), _ptr(momentum), float(lr), float(eps),

@@ -213,3 +213,23 @@ def test_workspace_layout_invariants(lib, dims):
         grad = ((4 * dims["B"] * sum(dims["D"]) + 255) // 256) * 256
         assert sizes[tbe.TBE_WS_MEAN] - sizes[0] == grad
         assert sizes[tbe.TBE_WS_WEIGHTED | tbe.TBE_WS_MEAN] - sizes[tbe.TBE_WS_WEIGHTED] == grad
+
+
+def test_binding_checks_state_sizes_before_any_call():
+    # a row-sized accumulator with the element-wise flag (or short weights)
+    # would be written past its end: refused on the host
+    desc = tbe.TBEDesc([10, 4], [8, 16], 2, device="cpu")
+    idx = torch.zeros(1, dtype=torch.int64)
+    off = torch.tensor([0, 1, 1, 1, 1], dtype=torch.int64)
+    W = torch.zeros(desc.num_weights, dtype=torch.float16)
+    G = torch.zeros(2, 24)
+    rows, elems = torch.zeros(desc.total_E), torch.zeros(desc.num_weights)
+    for fn, extra in ((tbe.tbe_backward_rowwise_adagrad, (None,)),
+                      (tbe.tbe_backward_rowwise_adagrad_noalloc, ())):
+        with pytest.raises(ValueError):
+            fn(desc, G, idx, off, None, W, rows, 0.1, 1e-8, *extra, flags=tbe.TBE_F_ELEMENTWISE)
+        with pytest.raises(ValueError):
+            fn(desc, G, idx, off, None, W[:-1], elems, 0.1, 1e-8, *extra,
+               flags=tbe.TBE_F_ELEMENTWISE)
+        with pytest.raises(ValueError):
+            fn(desc, G, idx, off, None, W, rows.double(), 0.1, 1e-8, *extra)
