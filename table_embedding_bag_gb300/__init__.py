@@ -215,6 +215,21 @@ def _check_weights(desc, weights):
             raise ValueError(f"weights must hold {desc.num_weights} elements")
 
 
+def _check_dense(desc, t, name):
+    """out / grad_out: fp32, contiguous, B x total_D elements."""
+    if isinstance(t, torch.Tensor):
+        if t.dtype != torch.float32 or not t.is_contiguous() or \
+                t.numel() != desc.B * desc.total_D:
+            raise ValueError(f"{name} must be contiguous float32 [{desc.B}, {desc.total_D}]")
+
+
+def _check_psw(indices, psw):
+    if isinstance(psw, torch.Tensor):
+        if psw.dtype != torch.float32 or not psw.is_contiguous() or \
+                psw.numel() != indices.numel():
+            raise ValueError("per_sample_weights must be contiguous float32, one per lookup")
+
+
 def _check_momentum(desc, momentum, flags):
     """The accumulators the update writes: one per row, or one per weight
     element with TBE_F_ELEMENTWISE."""
@@ -229,6 +244,8 @@ def tbe_forward(desc: TBEDesc, weights, indices, offsets, per_sample_weights, ou
     """Pooled forward into out (fp32 [B, sum D]); see tbe_forward in include/tbe.h."""
     _check_tensors(desc, indices, offsets)
     _check_weights(desc, weights)
+    _check_dense(desc, out, "out")
+    _check_psw(indices, per_sample_weights)
     _ok("tbe_forward", _load().tbe_forward(
         desc.ref, _ptr(weights), _ptr(indices), _ptr(offsets), indices.numel(),
         _ptr(per_sample_weights), _ptr(out), ws.ptr, ws.nbytes, _stream(stream), flags))
@@ -238,6 +255,7 @@ def tbe_forward(desc: TBEDesc, weights, indices, offsets, per_sample_weights, ou
 def tbe_preprocess(desc: TBEDesc, indices, offsets, per_sample_weights, ws: Workspace,
                    flags: int = 0, stream=None):
     _check_tensors(desc, indices, offsets)
+    _check_psw(indices, per_sample_weights)
     _ok("tbe_preprocess", _load().tbe_preprocess(
         desc.ref, _ptr(indices), _ptr(offsets), indices.numel(), _ptr(per_sample_weights),
         ws.ptr, ws.nbytes, _stream(stream), flags))
@@ -251,6 +269,8 @@ def tbe_backward_rowwise_adagrad(desc: TBEDesc, grad_out, indices, offsets, per_
     _check_tensors(desc, indices, offsets)
     _check_weights(desc, weights)
     _check_momentum(desc, momentum, flags)
+    _check_dense(desc, grad_out, "grad_out")
+    _check_psw(indices, per_sample_weights)
     _ok("tbe_backward_rowwise_adagrad", _load().tbe_backward_rowwise_adagrad(
         desc.ref, _ptr(grad_out), _ptr(indices), _ptr(offsets), indices.numel(),
         _ptr(per_sample_weights), _ptr(weights), _ptr(momentum), float(lr), float(eps), ws.ptr,
@@ -266,6 +286,8 @@ def tbe_backward_rowwise_adagrad_noalloc(desc: TBEDesc, grad_out, indices, offse
     _check_tensors(desc, indices, offsets)
     _check_weights(desc, weights)
     _check_momentum(desc, momentum, flags)
+    _check_dense(desc, grad_out, "grad_out")
+    _check_psw(indices, per_sample_weights)
     _ok("tbe_backward_rowwise_adagrad_noalloc", _load().tbe_backward_rowwise_adagrad_noalloc(
         desc.ref, _ptr(grad_out), _ptr(indices), _ptr(offsets), indices.numel(),
         _ptr(per_sample_weights), _ptr(weights), _ptr(momentum), float(lr), float(eps),

@@ -233,3 +233,19 @@ def test_binding_checks_state_sizes_before_any_call():
                flags=tbe.TBE_F_ELEMENTWISE)
         with pytest.raises(ValueError):
             fn(desc, G, idx, off, None, W, rows.double(), 0.1, 1e-8, *extra)
+
+
+def test_binding_checks_dense_arrays_before_any_call():
+    desc = tbe.TBEDesc([10, 4], [8, 16], 2, device="cpu")
+    idx = torch.zeros(3, dtype=torch.int64)
+    off = torch.tensor([0, 1, 2, 2, 3], dtype=torch.int64)
+    W = torch.zeros(desc.num_weights, dtype=torch.float16)
+    with pytest.raises(ValueError):  # out of the wrong size
+        tbe.tbe_forward(desc, W, idx, off, None, torch.empty(2, 23), None)
+    with pytest.raises(ValueError):  # non-contiguous out
+        tbe.tbe_forward(desc, W, idx, off, None, torch.empty(24, 2).t(), None)
+    with pytest.raises(ValueError):  # one per-sample weight short
+        tbe.tbe_forward(desc, W, idx, off, torch.ones(2), torch.empty(2, 24), None)
+    with pytest.raises(ValueError):  # grad_out in fp64
+        tbe.tbe_backward_rowwise_adagrad(desc, torch.zeros(2, 24, dtype=torch.float64), idx, off,
+                                         None, W, torch.zeros(desc.total_E), 0.1, 1e-8, None)
