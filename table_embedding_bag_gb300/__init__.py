@@ -264,8 +264,9 @@ def tbe_preprocess(desc: TBEDesc, indices, offsets, per_sample_weights, ws: Work
 def tbe_backward_rowwise_adagrad(desc: TBEDesc, grad_out, indices, offsets, per_sample_weights,
                                  weights, momentum, lr, eps, ws: Workspace, flags: int = 0,
                                  stream=None):
-    """Backward with one exact row-wise Adagrad update per touched row, in place
-    on weights and momentum; see include/tbe.h."""
+    """Backward with one Adagrad update per touched row (row-wise, or
+    element-wise with TBE_F_ELEMENTWISE), in place on weights and momentum;
+    see include/tbe.h."""
     _check_tensors(desc, indices, offsets)
     _check_weights(desc, weights)
     _check_momentum(desc, momentum, flags)
