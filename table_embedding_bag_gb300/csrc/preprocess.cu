@@ -858,10 +858,10 @@ __global__ void __launch_bounds__(kRleThreads)
 // One CTA: first run of every table (binary search of its first key among
 // the unique keys) and the prefix of short-run warp tasks per table.
 __global__ void __launch_bounds__(1024)
-    table_runs_kernel(const uint32_t* __restrict__ unique_keys, const uint32_t* __restrict__ counters,
+    table_runs_kernel(const uint32_t* __restrict__ unique_keys, const uint32_t* counters,
                       const int64_t* __restrict__ hash_base, const int64_t* __restrict__ D_offsets,
                       int T, uint32_t* __restrict__ table_runs, uint32_t* __restrict__ table_tasks,
-                      uint32_t* __restrict__ counters_out) {
+                      uint32_t* counters_out) {  // counters and counters_out: the same array
   __shared__ uint32_t sm[33];
   const uint32_t R = counters[kCntRuns];
   for (int t = threadIdx.x; t <= T; t += blockDim.x) {
