@@ -694,3 +694,23 @@ def test_backward_fp32_agrees_with_fp16_on_fp16_values_when_nothing_rounds():
     Wb, mb = oracle.backward_rowwise_adagrad(*args, W16.astype(np.float32),
                                              np.zeros(2, np.float32), 0.125, 0.0, fp32=True)
     assert np.array_equal(Wa.astype(np.float32), Wb) and np.array_equal(ma, mb)
+
+
+def test_elementwise_closed_form_with_bf16_weights_and_mean_pooling():
+    # One bag looking up row 1 three times, mean pooling: the row's gradient is
+    # 3 x (1/3) x grad_out = grad_out (exactly 1 in double only up to
+    # rounding of 1/3; eps = 0 makes the step lr * sign(g) regardless).  bf16
+    # weights 0.5 and lr = 0.125 keep 0.375 / 0.625 exact.
+    D = 8
+    tab = oracle.Tables([3], [D])
+    w0 = oracle.double_to_bf16(0.5)
+    W = np.full(3 * D, w0, np.uint16)
+    m = np.zeros(3 * D, np.float32)
+    v = np.array([[1.5, -0.25, 4.0, -8.0, 0.5, -1.0, 2.0, -3.0]], np.float32)
+    W2, m2 = oracle.backward_rowwise_adagrad(tab, 1, np.array([1, 1, 1], np.int64),
+                                             np.array([0, 3]), v, W, m, 0.125, 0.0, mean=True,
+                                             bf16=True, elementwise=True)
+    want = [oracle.double_to_bf16(0.375 if x > 0 else 0.625) for x in v[0]]
+    assert W2[D:2 * D].tolist() == want
+    assert np.allclose(m2[D:2 * D], v[0].astype(np.float64) ** 2, rtol=2 ** -22)
+    assert (W2[:D] == w0).all() and (W2[2 * D:] == w0).all() and not m2[:D].any()
