@@ -51,3 +51,20 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("variant,words", [
+    (["--weights", "bf16"], ["bf16 weights", "row-wise momentum"]),
+    (["--optimizer", "elementwise"], ["fp16 weights", "per-element momentum"]),
+    (["--pooling", "mean"], ["fp16 weights", "mean pooling"]),
+])
+def test_reference_arm_names_the_variant_it_timed(variant, words):
+    # the oracle sample follows the step's options, and the line says which
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0",
+           *variant]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    assert line["value"] > 0
+    for w in words:
+        assert w in line["config"]["workload"]
