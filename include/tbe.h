@@ -50,7 +50,11 @@
  * Errors: argument problems are reported synchronously through tbe_status
  * before anything is enqueued.  Data problems found on the device (indices
  * out of range, malformed offsets) set bits in a status word that lives in
- * the workspace; tbe_read_status copies it to the host.
+ * the workspace; tbe_read_status copies it to the host.  Without
+ * TBE_F_REPAIR_OFFSETS, malformed offsets give unspecified results but every
+ * kernel stays inside its buffers: each bag is read over its own offsets
+ * clamped into [0, n] (bags may then overlap), and the backward keeps at
+ * most n of the lookups such bags name.
  */
 #ifndef TBE_H_
 #define TBE_H_
@@ -220,9 +224,11 @@ tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indic
  * sums of per-sample weights, fp32 with a per-bag power-of-two scale), and
  * the remaining (cold) lookups are also kept per bag in lookup order.  Results stay in the workspace (see tbe_workspace_view); a
  * later tbe_forward or tbe_backward_rowwise_adagrad with TBE_F_PREPROCESSED
- * consumes them.  The sort chain runs on a stream of the library's own, so
- * that a forward enqueued next runs concurrently with it; the library's
- * calls order themselves against it (through events), but reading the
+ * consumes them.  The sort chain runs on a stream the library keeps for this
+ * workspace (created at the workspace's first use, one per workspace and
+ * device), so that a forward enqueued next runs concurrently with it; the
+ * library's calls on this workspace order themselves against it (through
+ * events), calls on other workspaces never wait on it, and reading the
  * sorted arrays directly needs a device synchronisation first.
  * Errors as tbe_forward. */
 tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* offsets, int64_t n,
@@ -262,7 +268,8 @@ tbe_status tbe_workspace_view(const tbe_desc* d, int64_t n, uint32_t ws_flags, v
                               tbe_ws_view* view);
 
 /* Copy the device status word to *status_bits (a TBE_ERR_* mask) and clear it.
- * Synchronises the stream: never call it inside a timed or captured region.
+ * Synchronises the stream and the workspace's own side stream (see
+ * tbe_preprocess): never call it inside a timed or captured region.
  * Errors: TBE_EINVAL, TBE_ECUDA. */
 tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits);
 
@@ -277,22 +284,25 @@ tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits);
  * and code that cannot afford cudaMalloc/cudaFree, which may synchronise the
  * whole device and fragment such a plan.
  *
- * It computes exactly what tbe_backward_rowwise_adagrad computes, with the
- * same kernels, but its scratch is a fixed array of TBE_NOALLOC_SCRATCH_BYTES
- * (32 MiB) inside the library, held by every GPU that loads the library until
- * the process exits.  Problems whose scratch would be larger -- roughly more
- * than 300k lookups of 128-wide rows at 200 lookups per bag, fewer for wider
- * rows, shorter bags or per-sample weights -- are rejected with
+ * It computes what tbe_backward_rowwise_adagrad computes on a fresh
+ * workspace, with the same sort and run kernels, but its scratch is a fixed
+ * array of TBE_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library, held by
+ * every GPU that loads the library until the process exits.  The hot-row
+ * path is off here (its histograms would fill most of the array), so every
+ * touched row is updated from its sorted run, and no kernel of this call
+ * waits on anything: no call can end in a time-out.  Problems whose scratch
+ * would be larger -- about 366k lookups of 128-wide rows (321k with
+ * per-sample weights, 249k for 256-wide rows) -- are rejected with
  * TBE_ETOO_LARGE before anything is enqueued.  No cudaMalloc, cudaFree or
  * other allocating call is made.
  *
  * The first call on each device does the set-up (looks up the device address
- * of the array); make that first call before any stream capture.  Every call
- * shares the one array and it keeps the previous call's contents; everything
- * that must start at zero is cleared by the call itself, including the
- * hot-row set (see tbe_backward_rowwise_adagrad), so each call stands alone.  Calls whose work
- * overlaps on the GPU (different streams, or several host threads) race on
- * the array: serialise them.
+ * of the array; a set-up that fails is tried again by the next call); make
+ * that first call before any stream capture.  Every call shares the one
+ * array and it keeps the previous call's contents; everything that must
+ * start at zero is cleared by the call itself, so each call stands alone.
+ * Calls whose work overlaps on the GPU (different streams, or several host
+ * threads) race on the array: serialise them.
  *
  * Arguments as tbe_backward_rowwise_adagrad without workspace; flags may hold
  * TBE_F_LONG_TWO_LAUNCH, TBE_F_MEAN and TBE_F_ELEMENTWISE (no bounds reporting: the status word

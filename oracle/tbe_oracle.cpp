@@ -32,7 +32,7 @@
 //    kernel is not printed: the oracle takes the plainest reading, the pooled
 //    sum times the same factor.
 //
-// Readings where the pages are silent (each is listed in the design notes):
+// Readings where the pages are silent:
 //  * bags are table-major: bag (t,b) has id t*B+b, offsets has T*B+1 entries;
 //  * a lookup whose row is outside [0, E_t) contributes nothing (skipped);
 //  * weights are fp16 (or bf16, or fp32), rounded to nearest-even from the

@@ -241,7 +241,9 @@ __host__ __device__ inline int64_t tree_nodes(int64_t nch) {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags);
+// allow_hot = false lays out no hot-row histograms or partials and turns the
+// hot-row path off (the no-allocation entry point's fixed scratch).
+WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags, bool allow_hot = true);
 
 inline int index_bytes(const tbe_desc* d) { return d->index_dtype == TBE_DT_I32 ? 4 : 8; }
 

@@ -18,20 +18,26 @@ void note_launch();
 void probe_begin(uint32_t kernel, cudaStream_t s);
 void probe_end(uint32_t kernel, cudaStream_t s);
 
-// Side stream of the current device, created once (with the device's
-// set-up): the preprocess runs its sort chain there, concurrently with the
-// forward, and the backward its hot-row gradient, concurrently with the cold
-// rows.  Events join the streams:
+// Side stream of one workspace (one per workspace and device, created at the
+// workspace's first use): the preprocess runs its sort chain there,
+// concurrently with the forward, and the backward its hot-row gradient,
+// concurrently with the cold rows.  Events join the streams:
 //   sorted  recorded on the side stream after the sort chain,
 //   hot     recorded on it after the hot-row update,
 //   done    recorded after every side segment (the latest side work),
 //   fork    recorded on the caller's stream before a side segment.
+// Because the flow belongs to the workspace, calls on different workspaces
+// (other streams, other host threads) never wait on each other's events.
 struct SideFlow {
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, sorted = nullptr, hot = nullptr, done = nullptr;
 };
-// nullptr if the stream or events could not be created.
-SideFlow* side_flow();
+// The flow of workspace `ws` on the current device, created on first use;
+// nullptr if the stream or events could not be created (the next call
+// tries again).
+SideFlow* side_flow(const void* ws);
+// The flow of `ws` if one exists, else nullptr (creates nothing).
+SideFlow* find_side_flow(const void* ws);
 // Makes `side` wait for everything enqueued on `s` so far.
 cudaError_t fork_to(SideFlow* f, cudaStream_t s);
 

@@ -22,20 +22,22 @@ constexpr int kMaxDevices = 64;
 cudaError_t prepare_preprocess_kernels();
 namespace {
 
-// Set-up, once per device and with that device current: the device address
-// of the scratch, and the shared-memory attributes of the sort kernels.
-// Returns the scratch address on the current device, or nullptr on failure.
+// Set-up, per device and with that device current: the device address of
+// the scratch, and the shared-memory attributes of the sort kernels.  Returns
+// the scratch address on the current device, or nullptr on failure; a failed
+// set-up is not remembered, so the next call on that device tries again.
 char* scratch_ptr() {
   static char* ptrs[kMaxDevices] = {nullptr};
-  static std::once_flag once[kMaxDevices];
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::call_once(once[dev], [dev]() {
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return;
-    if (prepare_preprocess_kernels() != cudaSuccess) return;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    if (prepare_preprocess_kernels() != cudaSuccess) return nullptr;
     ptrs[dev] = static_cast<char*>(p);
-  });
+  }
   return ptrs[dev];
 }
 
@@ -84,18 +86,21 @@ extern "C" tbe_status tbe_backward_rowwise_adagrad_noalloc(
   const bool elementwise = (flags & TBE_F_ELEMENTWISE) != 0;
   if (elementwise && (reinterpret_cast<uintptr_t>(momentum) & 15u)) return TBE_EINVAL;
   const bool mean = (flags & TBE_F_MEAN) != 0;
+  // The hot-row path is off here: its per-bag histograms would take most of
+  // the fixed array, and without it no kernel of this call waits on
+  // anything (every bounded wait of the library is in the hot-row and
+  // small-table tensor-core kernels), so no call can end in a time-out.
   const WsLayout W = make_layout(d, n, (per_sample_weights ? TBE_WS_WEIGHTED : 0u) |
-                                           (mean ? TBE_WS_MEAN : 0u));
+                                           (mean ? TBE_WS_MEAN : 0u), /*allow_hot=*/false);
   if (W.total > TBE_NOALLOC_SCRATCH_BYTES) return TBE_ETOO_LARGE;
   char* scratch = scratch_ptr();
   if (!scratch) return TBE_ECUDA;
   const Launch L{d, n, static_cast<cudaStream_t>(stream), sm_count()};
-  // Each call stands alone: the hot-row set a previous call left in the
-  // scratch (possibly for another problem) is cleared, so no call's result
-  // depends on an earlier one.  Everything else the kernels read before
-  // writing is reset by launch_preprocess (counters, first run and pair
-  // entries, band counts); the status word is not used because bounds
-  // reporting is not offered here.
+  // Each call stands alone: the hot-row set is cleared (the path is off, so
+  // nothing reads it, but no stale set is kept), and everything else the
+  // kernels read before writing is reset by launch_preprocess (counters,
+  // first run and pair entries, band counts); the status word is not used
+  // because bounds reporting is not offered here.
   if (cudaMemsetAsync(scratch + W.hot_n(W.hot_next), 0, static_cast<size_t>(d->T) * sizeof(uint32_t),
                       L.s) != cudaSuccess)
     return TBE_ECUDA;

@@ -146,7 +146,7 @@ template <typename IndexT, bool kWeighted>
 struct ExpandSmem {
   HotHash hash;
   int64_t bag_off[kHotTileBags + 1];  // the tile's offsets, clamped to [0, n]
-  uint32_t warp_cold[8];
+  unsigned long long warp_cold[8];
   uint32_t wide_bags[kHotTileBags / 32];  // bit lb: bag lb has an fp32 row
   uint32_t slot_cnt[kHot];
   // the bag each warp is on: per-slot weight (exact sums: integer counts, or
@@ -197,7 +197,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int j = 0; j < kPerLane; ++j) cnt[j] = 0;
   bool bad = false;
-  uint32_t cold_w = 0;
+  // this warp's cold lookups over its bags: 64-bit, because bags of malformed
+  // (overlapping) offsets can together hold more than n lookups
+  unsigned long long cold_w = 0;
   const unsigned lt = (1u << lane) - 1u;
   for (int lb = warp; lb < ti.nbags; lb += 8) {
     const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
@@ -306,9 +308,12 @@ __global__ void __launch_bounds__(256)
     if (cnt[j]) atomicAdd(&sm.slot_cnt[kWeighted ? lane + 32 * j : 8 * lane + j], cnt[j]);
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t c = 0;
+    // saturated at n: with well-formed offsets the tile holds at most n cold
+    // lookups; overlapping bags may count more, and only the first n of all
+    // cold lookups are kept (see capped_scan_kernel)
+    unsigned long long c = 0;
     for (int w = 0; w < 8; ++w) c += sm.warp_cold[w];
-    tile_cold[blockIdx.x] = c;
+    tile_cold[blockIdx.x] = static_cast<uint32_t>(c < static_cast<unsigned long long>(n) ? c : n);
   }
   if (nh_pad) {
     bool wide = kWeighted;
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(256)
                         const float* __restrict__ sp_psw, uint32_t* __restrict__ keys,
                         uint32_t* __restrict__ vals, float* __restrict__ psw_out) {
   __shared__ uint32_t bag_base[kHotTileBags];
-  __shared__ uint32_t scan[33];
+  __shared__ unsigned long long scan[33];
   __shared__ int64_t bag_off[kHotTileBags + 1];
   const TileInfo ti = tile_info(B);
   const int warp = threadIdx.x >> 5;
@@ -357,30 +362,66 @@ __global__ void __launch_bounds__(256)
   load_tile_offsets(offsets, ti, B, n, bag_off);  // read after the scan's barriers
   {
     // exclusive prefix of the tile's per-bag cold counts = the bags' first
-    // entries in the dense list
+    // entries in the dense list.  In 64 bits and capped at n: with
+    // well-formed offsets no cap applies; bags of malformed (overlapping)
+    // offsets can hold more than n cold lookups in all, and then only
+    // positions below n are written (every one of them, since positions are
+    // a dense prefix), so the dense list never leaves its n entries.
     const int lb = threadIdx.x;
-    const uint32_t c =
-        lb < ti.nbags ? bag_cold[static_cast<int64_t>(ti.t) * B + ti.b0 + lb] : 0u;
-    uint32_t total;
-    const uint32_t inc = block_inclusive_scan(c, OpSum(), 0u, scan, &total);
-    const uint32_t first = tile_base[blockIdx.x] + inc - c;
-    if (lb < kHotTileBags) bag_base[lb] = first;
-    if (lb < ti.nbags) cold_off[static_cast<int64_t>(ti.t) * B + ti.b0 + lb] = first;
-    if (lb == 0 && blockIdx.x == gridDim.x - 1)
-      cold_off[static_cast<int64_t>(ti.t) * B + ti.b0 + ti.nbags] = tile_base[blockIdx.x] + total;
+    const unsigned long long c =
+        lb < ti.nbags ? bag_cold[static_cast<int64_t>(ti.t) * B + ti.b0 + lb] : 0ull;
+    unsigned long long total;
+    const unsigned long long inc = block_inclusive_scan(c, OpSum(), 0ull, scan, &total);
+    const unsigned long long cap = static_cast<unsigned long long>(n);
+    const unsigned long long first = tile_base[blockIdx.x] + inc - c;
+    const uint32_t first_c = static_cast<uint32_t>(first < cap ? first : cap);
+    if (lb < kHotTileBags) bag_base[lb] = first_c;
+    if (lb < ti.nbags) cold_off[static_cast<int64_t>(ti.t) * B + ti.b0 + lb] = first_c;
+    if (lb == 0 && blockIdx.x == gridDim.x - 1) {
+      const unsigned long long last = tile_base[blockIdx.x] + total;
+      cold_off[static_cast<int64_t>(ti.t) * B + ti.b0 + ti.nbags] =
+          static_cast<uint32_t>(last < cap ? last : cap);
+    }
   }
   __syncthreads();
   for (int lb = warp; lb < ti.nbags; lb += 8) {
     const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
     const int64_t s = bag_off[lb];
-    const uint32_t c = bag_cold[bag];
     const uint32_t pos = bag_base[lb];
+    // entries at or past n are dropped (malformed offsets only; see above)
+    const int64_t room = n - static_cast<int64_t>(pos);
+    const uint32_t c = static_cast<uint32_t>(
+        min(static_cast<int64_t>(bag_cold[bag]), room > 0 ? room : int64_t(0)));
     for (uint32_t i = lane; i < c; i += 32) {
       keys[pos + i] = __ldg(sp_keys + s + i);
       vals[pos + i] = __ldg(sp_vals + s + i);
       if (kWeighted) psw_out[pos + i] = __ldg(sp_psw + s + i);
     }
   }
+}
+
+// Single CTA: exclusive scan of the expand tiles' cold counts in place,
+// capped at `cap` (= n): entry i becomes min(sum of the counts before i, cap)
+// and *sum_out min(sum of all, cap), the number of entries the sort takes.
+// Sums are formed in 64 bits, so counts of malformed offsets cannot wrap.
+__global__ void __launch_bounds__(1024)
+    capped_scan_kernel(uint32_t* __restrict__ data, int64_t total, uint32_t cap,
+                       uint32_t* sum_out) {
+  __shared__ unsigned long long sm[33];
+  const int64_t per = (total + blockDim.x - 1) / blockDim.x;
+  const int64_t b = threadIdx.x * per;
+  const int64_t e = b + per < total ? b + per : total;
+  unsigned long long s = 0;
+  for (int64_t i = b; i < e; ++i) s += data[i];
+  unsigned long long agg;
+  const unsigned long long inc = block_inclusive_scan(s, OpSum(), 0ull, sm, &agg);
+  unsigned long long run = inc - s;
+  for (int64_t i = b; i < e; ++i) {
+    const uint32_t v = data[i];
+    data[i] = static_cast<uint32_t>(run < cap ? run : cap);
+    run += v;
+  }
+  if (threadIdx.x == 0) *sum_out = static_cast<uint32_t>(agg < cap ? agg : cap);
 }
 
 // -------------------------------------------------------------- radix sort
@@ -1071,7 +1112,7 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
   uint32_t* uk = reinterpret_cast<uint32_t*>(ws + W.unique_keys);
   uint32_t* rs = reinterpret_cast<uint32_t*>(ws + W.run_starts);
 
-  SideFlow* sf = side_flow();
+  SideFlow* sf = side_flow(ws);
   if (!sf) return cudaErrorNotReady;
   // the previous call's side work (sort chain, hot-row update) still reads
   // the buffers this one rewrites
@@ -1120,7 +1161,8 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
       { probe_begin(TBE_PROBE_EXPAND_COUNT, s); expand_count_kernel<IndexT, false><<<tiles, 256, sizeof(ExpandSmem<IndexT, false>), s>>>(
           indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh8, hh, hsc, tk, hc, bc,
           tile_cold, keys[0], vals[0], pw[0], status); note_launch(); probe_end(TBE_PROBE_EXPAND_COUNT, s); }
-    { exclusive_scan_kernel<<<1, 1024, 0, s>>>(tile_cold, W.hot_tiles, counters + kCntSortN); note_launch(); }
+    { capped_scan_kernel<<<1, 1024, 0, s>>>(tile_cold, W.hot_tiles, static_cast<uint32_t>(n),
+                                            counters + kCntSortN); note_launch(); }
     if (weighted)
       { expand_write_kernel<IndexT, true><<<tiles, 256, 0, s>>>(
           offsets, n, d->B, bc, tile_cold, co, keys[0], vals[0], pw[0], keys[2], vals[2],

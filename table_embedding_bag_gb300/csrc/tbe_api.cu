@@ -1,7 +1,9 @@
 // C ABI entry points: argument validation, workspace layout and launch order.
 // The operations themselves are specified in include/tbe.h.
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
@@ -12,23 +14,44 @@ std::atomic<uint64_t> g_kernel_launches{0};
 
 void note_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 
-SideFlow* side_flow() {
-  static SideFlow flows[64];
-  static std::once_flag once[64];
-  static bool ok[64] = {false};
+namespace {
+// Side flows by (device, workspace address).  Entries live until the process
+// exits (a stream and four events each); a workspace freed and another
+// allocated at the same address shares the entry, which only orders the new
+// workspace's calls after the old one's.
+std::mutex g_flow_mu;
+std::map<std::pair<int, const void*>, SideFlow*> g_flows;
+
+SideFlow* lookup_flow(const void* ws, bool create) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::call_once(once[dev], [dev]() {
-    SideFlow& f = flows[dev];
-    const unsigned ef = cudaEventDisableTiming;
-    ok[dev] = cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) == cudaSuccess &&
-              cudaEventCreateWithFlags(&f.fork, ef) == cudaSuccess &&
-              cudaEventCreateWithFlags(&f.sorted, ef) == cudaSuccess &&
-              cudaEventCreateWithFlags(&f.hot, ef) == cudaSuccess &&
-              cudaEventCreateWithFlags(&f.done, ef) == cudaSuccess;
-  });
-  return ok[dev] ? &flows[dev] : nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lk(g_flow_mu);
+  const auto key = std::make_pair(dev, ws);
+  auto it = g_flows.find(key);
+  if (it != g_flows.end()) return it->second;
+  if (!create) return nullptr;
+  SideFlow f;
+  const unsigned ef = cudaEventDisableTiming;
+  const bool ok = cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&f.fork, ef) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&f.sorted, ef) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&f.hot, ef) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&f.done, ef) == cudaSuccess;
+  if (!ok) {
+    // give back what was created; the next call tries again
+    for (cudaEvent_t e : {f.fork, f.sorted, f.hot, f.done})
+      if (e) cudaEventDestroy(e);
+    if (f.side) cudaStreamDestroy(f.side);
+    return nullptr;
+  }
+  SideFlow* p = new SideFlow(f);
+  g_flows.emplace(key, p);
+  return p;
 }
+}  // namespace
+
+SideFlow* side_flow(const void* ws) { return lookup_flow(ws, true); }
+SideFlow* find_side_flow(const void* ws) { return lookup_flow(ws, false); }
 
 cudaError_t fork_to(SideFlow* f, cudaStream_t s) {
   cudaError_t e = cudaEventRecord(f->fork, s);
@@ -66,7 +89,7 @@ void probe_end(uint32_t kernel, cudaStream_t s) {
 
 cudaError_t prepare_preprocess_kernels();
 
-WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
+WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags, bool allow_hot) {
   WsLayout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -121,7 +144,7 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags) {
   const int64_t max_parts = (B + kHotMinPartBags - 1) / kHotMinPartBags;
   if (L.hot_parts > max_parts) L.hot_parts = static_cast<int>(max_parts);
   // the hot rows' tensor-core kernels take fp16 weights only
-  L.hot_enabled = d->weights_dtype == TBE_DT_F16 &&
+  L.hot_enabled = allow_hot && d->weights_dtype == TBE_DT_F16 &&
                   static_cast<size_t>(T) * kHot * B * (sizeof(float) + 1) <= kHotBudgetBytes;
   L.hot_cnt = take(T * kHot * 4);
   L.hot_hist8 = L.hot_enabled ? take(static_cast<size_t>(T) * kHot * B) : 0;
@@ -170,18 +193,22 @@ tbe_status check_n(int64_t n) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SM count of the current device, and the device's kernel set-up (shared
+// memory attributes), done once per device; a set-up that fails is tried
+// again by the next call.
 int device_sms() {
   static int sms[64] = {0};
-  static std::once_flag once[64];
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  std::call_once(once[dev], [dev]() {
+  std::lock_guard<std::mutex> lk(mu);
+  if (sms[dev] == 0) {
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
-      v = 148;
+      return 148;
+    if (prepare_preprocess_kernels() != cudaSuccess) return v;
     sms[dev] = v;
-    prepare_preprocess_kernels();
-  });
+  }
   return sms[dev];
 }
 
@@ -360,7 +387,12 @@ tbe_status tbe_read_status(void* workspace, void* stream, int32_t* status_bits) 
   if (!workspace || !status_bits) return TBE_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t v = 0;
-  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  // the workspace's side work (sort chain, hot-row gradient) may also set
+  // bits: it is finished first
+  cudaError_t e = cudaSuccess;
+  if (SideFlow* f = find_side_flow(workspace)) e = cudaStreamSynchronize(f->side);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&v, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
   if (e != cudaSuccess) return TBE_ECUDA;

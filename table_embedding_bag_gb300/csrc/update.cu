@@ -1021,7 +1021,7 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   a.lr = lr;
   a.eps = eps;
   if (L.n == 0) return cudaSuccess;
-  SideFlow* sf = side_flow();
+  SideFlow* sf = side_flow(ws);
   if (!sf) return cudaErrorNotReady;
   const unsigned blocks = static_cast<unsigned>(L.num_sms) * 8u;
   const bool weighted = a.sorted_psw != nullptr;

@@ -290,3 +290,71 @@ def pair_structure(sorted_keys, sorted_bags, run_starts):
     ps = np.concatenate([np.nonzero(head)[0], [n]]).astype(np.int64)
     rp = np.searchsorted(ps, np.asarray(run_starts, dtype=np.int64))
     return ps, b[ps[:-1]], rp
+
+
+# ------------------------------------------------- sampled checks (any size)
+def host_inputs(w):
+    """indices, offsets, psw of a (device) workload as host numpy arrays."""
+    return (w.indices.cpu().numpy(), w.offsets.cpu().numpy(),
+            None if w.psw is None else w.psw.cpu().numpy())
+
+
+def check_sampled_bags(w, weights_dev, out, nsample=300, seed=1, inputs=None):
+    """Pooled outputs of sampled bags (the first, the last and `nsample`
+    random ones) against oracle.pool_gathered on rows gathered from the
+    device weights by index (no TBE arithmetic here)."""
+    idx, off, psw = inputs if inputs is not None else host_inputs(w)
+    rng = np.random.default_rng(seed)
+    nb = w.T * w.B
+    bags = np.unique(np.concatenate([[0, nb - 1], rng.integers(0, nb, nsample)]))
+    D_off = np.concatenate([[0], np.cumsum(w.D)])
+    W_off = np.concatenate([[0], np.cumsum(w.E * w.D)])
+    checked = 0
+    for t in np.unique(bags // w.B):
+        tb = bags[bags // w.B == t]
+        D = int(w.D[t])
+        seg = [np.arange(off[b], off[b + 1]) for b in tb]
+        pos = np.concatenate(seg) if seg else np.zeros(0, np.int64)
+        rows = idx[pos].astype(np.int64)
+        flat = torch.as_tensor(W_off[t] + rows[:, None] * D + np.arange(D)[None, :],
+                               device=weights_dev.device)
+        gathered = weights_dev[flat.reshape(-1)].reshape(len(rows), D).cpu().numpy()
+        bo = np.concatenate([[0], np.cumsum([len(s) for s in seg])])
+        coef = None if psw is None else psw[pos]
+        ref = oracle.pool_gathered(bo, gathered, coef)
+        terms = oracle.pool_gathered(bo, np.abs(gathered), None if coef is None else np.abs(coef))
+        got = out[tb % w.B, D_off[t]:D_off[t] + D]
+        assert_forward_close(got, ref, terms)
+        checked += len(tb)
+    return checked
+
+
+def selected_rows(w, weights_dev, momentum_dev, sel):
+    """fp16 weights [len(sel), max D] and momentum of the rows with linear keys sel."""
+    hb = np.concatenate([[0], np.cumsum(w.E)])
+    W_off = np.concatenate([[0], np.cumsum(w.E * w.D)])
+    maxD = int(w.D.max())
+    t_sel = np.searchsorted(hb, sel, side="right") - 1
+    out = np.zeros((len(sel), maxD), np.float16)
+    for j, (k, t) in enumerate(zip(sel, t_sel)):
+        D = int(w.D[t])
+        s = int(W_off[t] + (int(k) - hb[t]) * D)
+        out[j, :D] = weights_dev[s:s + D].cpu().numpy()
+    m = momentum_dev[torch.as_tensor(np.asarray(sel, np.int64), device=momentum_dev.device)]
+    return out, m.cpu().numpy()
+
+
+def check_selected_rows(w, sel, w0, m0, w1, m1, inputs=None):
+    """Rows sel after one backward (w1, m1; before: w0, m0) against
+    oracle.backward_selected: momentum within 1e-5 relative, weights within
+    1 fp16 ulp, rows without lookups bit-identical.  Returns the rows'
+    lookup counts."""
+    idx, off, psw = inputs if inputs is not None else host_inputs(w)
+    ws, ms, cnt = oracle.backward_selected(tables(w), w.B, idx, off, w.grad_out.cpu().numpy(),
+                                           w.lr, w.eps, sel, w0, m0, psw)
+    assert_momentum_close(m1, ms)
+    assert_weights_within_ulp(w1, ws)
+    free = cnt == 0
+    assert np.array_equal(w1[free].view(np.uint16), w0[free].view(np.uint16))
+    assert np.array_equal(m1[free].view(np.uint32), m0[free].view(np.uint32))
+    return cnt

@@ -149,3 +149,93 @@ def test_preprocessed_flag_reuses_runs():
                                                    w.lr, w.eps, hw["psw"])
     H.assert_momentum_close(m_gpu, m_ref)
     H.assert_weights_within_ulp(W_gpu, W_ref)
+
+
+def _clamped_bags(off, n):
+    """Each bag as the kernels read it without repair: [s, max(e, s)) with s
+    and e clamped into [0, n] one by one (bags may overlap)."""
+    o = np.clip(np.asarray(off, np.int64), 0, n)
+    return [(int(o[i]), int(max(o[i + 1], o[i]))) for i in range(len(o) - 1)]
+
+
+def test_malformed_offsets_without_repair_stay_in_bounds():
+    """Offsets that are not monotone (overlapping bags whose lookups add up
+    to far more than n), negative or beyond n, with no repair flag: every
+    path (plain forward, preprocess, preprocessed forward with hot rows,
+    backward, the no-allocation backward) must finish, report the bad
+    offsets when asked, leave every row that no index names untouched, and
+    leave the workspace fit for a well-formed batch afterwards.  The plain
+    forward pools each bag over its own clamped range, which is checked
+    against the oracle on rows gathered by numpy."""
+    # E = 2000 rows per table: about 90 hot rows each, the rest of the lookups cold
+    w = workloads.make("hot", B=256, E_scale=2e-4, T=2, seed=5)
+    n = w.n
+    good = w.offsets.numpy().copy()
+    bad = good.copy()
+    nb = len(bad) - 1
+    bad[1:nb:2] = n          # bags 0, 2, 4, ...: [prev, n); bags 1, 3, ...: [n, 0) -> empty
+    bad[2:nb:2] = 0
+    bad[5], bad[9], bad[nb] = -7, n + 1000, n // 3
+    wb = workloads.from_arrays(w.E, w.D, w.B, w.indices, bad, w.weights, w.grad_out,
+                               momentum=w.momentum, lr=w.lr, eps=w.eps)
+    run = H.Run(w)
+    run.backward()  # a well-formed batch first: a hot set for the preprocessed paths
+    run.reset_state()
+    learned = run.hot_set()
+    assert sum(len(h) for h in learned) > 0
+    runb = H.Run(wb)
+    runb.ws = run.ws  # same workspace, hot set included
+    # plain forward: per-bag clamped ranges
+    out = runb.forward(tbe.TBE_F_CHECK_BOUNDS)
+    assert runb.status() == tbe.TBE_ERR_OFFSETS
+    idx = w.indices.numpy().astype(np.int64)
+    W = w.weights.numpy()
+    W_off = np.concatenate([[0], np.cumsum(w.E * w.D)])
+    D = int(w.D[0])
+    for bag, (s, e) in enumerate(_clamped_bags(bad, n)):
+        t, b = divmod(bag, w.B)
+        rows = idx[s:e]
+        rows = rows[(rows >= 0) & (rows < w.E[t])]
+        g = W[W_off[t] + rows[:, None] * D + np.arange(D)[None, :]].reshape(len(rows), D)
+        ref = oracle.pool_gathered([0, len(rows)], g)
+        terms = oracle.pool_gathered([0, len(rows)], np.abs(g))
+        H.assert_forward_close(out[b:b + 1, t * D:(t + 1) * D], ref, terms)
+    # preprocess + preprocessed forward + backward, and the plain backward
+    named = np.zeros(int(w.E.sum()), bool)
+    for t in range(w.T):
+        r = idx[(idx >= 0) & (idx < w.E[t])]
+        named[int(np.sum(w.E[:t])) + r] = True
+    W0 = runb.host_weights().copy()
+    m0 = runb.momentum.cpu().numpy().copy()
+    pre = runb.preprocess(tbe.TBE_F_CHECK_BOUNDS)
+    assert runb.status() == tbe.TBE_ERR_OFFSETS
+    assert pre["n_valid"] <= n and pre["R"] <= n and pre["P"] <= n
+    runb.forward(tbe.TBE_F_PREPROCESSED)
+    for flags in (tbe.TBE_F_PREPROCESSED, 0, tbe.TBE_F_LONG_TWO_LAUNCH):
+        W1, m1 = runb.backward(flags)
+        assert runb.status() == 0
+        assert np.isfinite(W1.astype(np.float32)).all() and np.isfinite(m1).all()
+        rowmask = np.repeat(~named, D)
+        assert np.array_equal(W1.view(np.uint16)[rowmask], W0.view(np.uint16)[rowmask])
+        assert np.array_equal(m1.view(np.uint32)[~named], m0.view(np.uint32)[~named])
+    tbe.tbe_backward_rowwise_adagrad_noalloc(runb.desc, runb.grad_out, runb.indices,
+                                             runb.offsets, None, runb.weights, runb.momentum,
+                                             w.lr, w.eps, 0)
+    torch.cuda.synchronize()
+    W1 = runb.host_weights()
+    assert np.array_equal(W1.view(np.uint16)[np.repeat(~named, D)],
+                          W0.view(np.uint16)[np.repeat(~named, D)])
+    # the workspace still serves a well-formed batch exactly
+    run.reset_state()
+    hw = H.host(w)
+    tab = H.tables(w)
+    ref = oracle.forward(tab, w.B, hw["weights"], hw["indices"], hw["offsets"])
+    terms = oracle.forward(tab, w.B, np.abs(hw["weights"]), hw["indices"], hw["offsets"])
+    tbe.tbe_preprocess(run.desc, run.indices, run.offsets, None, run.ws)
+    H.assert_forward_close(run.forward(tbe.TBE_F_PREPROCESSED), ref, terms)
+    W_ref, m_ref = oracle.backward_rowwise_adagrad(tab, w.B, hw["indices"], hw["offsets"],
+                                                   hw["grad_out"], hw["weights"], hw["momentum"],
+                                                   w.lr, w.eps)
+    W_gpu, m_gpu = run.backward(tbe.TBE_F_PREPROCESSED)
+    H.assert_momentum_close(m_gpu, m_ref)
+    H.assert_weights_within_ulp(W_gpu, W_ref)

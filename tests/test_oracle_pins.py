@@ -135,6 +135,44 @@ def test_forward_brute_force_exact_rational(oracle_lib, seed, weighted):
     assert np.all(np.abs(out.astype(np.float64) - exact) <= 0.5 * ulp + 1e-300)
 
 
+@pytest.mark.parametrize("seed", range(3))
+@pytest.mark.parametrize("weighted", [False, True])
+def test_pool_gathered_exact_and_equal_to_forward(oracle_lib, seed, weighted):
+    """pool_gathered (the checker of the full-size forward tests) pools rows
+    that the caller gathered itself.  Against the definition: each bag's sum,
+    computed in exact rationals from rows gathered here with numpy and
+    rounded once to fp32.  And bit for bit against oracle.forward on the same
+    bags.  Bags are ragged (lengths 0..9, never equal to D, some empty) and
+    every coefficient differs, so an offset coefficient or a row stride of
+    the wrong length changes the result."""
+    tab, B, idx, off, W, G, psw = _tiny_problem(seed, weighted=weighted, dtype=np.int64)
+    rng = np.random.default_rng(100 + seed)
+    # re-draw ragged bags over table 0 only
+    T, D = 1, int(tab.D[0])
+    tab1 = oracle.Tables([int(tab.E[0])], [D])
+    lens = rng.integers(0, 10, B)
+    lens[1] = 0
+    off1 = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    n = int(off1[-1])
+    idx1 = rng.integers(0, int(tab.E[0]), n).astype(np.int64)
+    W1 = W[:int(tab.E[0]) * D]
+    coef = rng.uniform(0.1, 2.0, n).astype(np.float32) if weighted else None
+    rows = W1.reshape(-1, D)[idx1]                      # gathered here, by numpy
+    got = oracle.pool_gathered(off1, rows, coef)
+    assert got.shape == (B, D)
+    for b in range(B):
+        for d in range(D):
+            acc = Fraction(0)
+            for i in range(off1[b], off1[b + 1]):
+                c = Fraction(float(coef[i])) if weighted else Fraction(1)
+                acc += c * Fraction(float(rows[i, d]))
+            exact = float(acc)
+            ulp = float(np.spacing(np.float32(abs(exact))))
+            assert abs(float(got[b, d]) - exact) <= 0.5 * ulp + 1e-300, (b, d)
+    ref = oracle.forward(tab1, B, W1, idx1, off1, coef)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
 def test_forward_closed_forms(oracle_lib):
     tab = oracle.Tables([5, 3], [8, 16])
     rng = np.random.default_rng(0)
