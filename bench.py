@@ -1,20 +1,29 @@
 """TBE training-step benchmark: pooled forward + backward with row-wise Adagrad.
 
-One step = tbe_forward (pooled lookup) + tbe_preprocess (expand, radix sort,
-run-length encode, classify) + tbe_backward_rowwise_adagrad on the
-preprocessed runs (short-run and long-run update kernels), over one batch of
-the hot-row workload: T=8 tables of E=1e7 rows, D=128, fp16 weights (20.5 GB)
-+ fp32 row-wise momentum, B=131072 bags per table, L=200 lookups per bag
-(209.7M lookups), Zipf(1.4) rows over a per-table random permutation.  Inputs
-are drawn on the device once (seeded) and stay resident; every timed step
-applies a real optimizer update.  Indices (1.7 GB) and weights (20.5 GB) are
-far larger than the 129 MB L2, so no flush is needed between steps.
+One step = tbe_preprocess (expand, radix sort, run-length encode, classify)
++ tbe_forward from the preprocessed workspace + tbe_backward_rowwise_adagrad
+on the preprocessed runs (hot rows on the tensor cores, short-, medium- and
+long-run update kernels), over one batch of the hot-row workload: T=8 tables
+of E=1e7 rows, D=128, fp16 weights (20.5 GB) + fp32 row-wise momentum,
+B=131072 bags per table, L=200 lookups per bag (209.7M lookups), Zipf(1.4)
+rows over a per-table random permutation.  Several distinct batches are drawn
+over the same tables (one table seed, per-batch draw seeds) and cycled, so
+each step uses the hot set the backward learned on a different batch.
+Inputs are drawn on the device once (seeded) and stay resident; every timed
+step applies a real optimizer update.  Indices (1.7 GB per batch) and weights
+(20.5 GB) are far larger than the 129 MB L2, so no flush is needed between
+steps.
+
+Besides the headline line it reports, per recipe of the workload set (tiny,
+small, mixed, weighted, hot), forward / backward / step times in both
+arrangements of the preprocessing, lookups/s and compulsory-byte roofline
+fractions, and the long runs' fused and two-launch updates.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
 Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs its own
-independent batch (different seed): weak scaling with no collective on the
-data path; value = lookups of all ranks / max-over-ranks time.
+independent batches (table seed = rank): weak scaling with no collective on
+the data path; value = lookups of all ranks / max-over-ranks time.
 """
 from __future__ import annotations
 
@@ -50,6 +59,12 @@ def parse():
                    help="bags of table 0 in the CPU-oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--batches", type=int, default=4,
+                   help="distinct batches of the recipe cycled through the steps")
+    p.add_argument("--configs", default="tiny,small,mixed,weighted,hot",
+                   help="recipes measured for the per-config figures")
+    p.add_argument("--config-steps", type=int, default=10)
+    p.add_argument("--no-configs", action="store_true")
     p.add_argument("--pooling", choices=["sum", "mean"], default="sum",
                    help="pooling mode of the step (the recorded workload is sum)")
     p.add_argument("--weights", choices=["fp16", "bf16"], default="fp16",
@@ -146,12 +161,20 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# The step's dominant kernel (largest share of the ncu launch list of this
-# workload, profiles/launches_hot_row_step.md): the long-run chunk kernel of
-# the backward.  Its launches are timed live by the library's kernel probe.
-ROOFLINE_KERNEL = "long_chunks_kernel (tbe_backward_rowwise_adagrad, long runs)"
+# The roofline kernel: the largest steady-state share of the step's kernels in
+# the ncu launch list of this workload (distinct batches, hot set learned on
+# the batch before): the short-run update kernel of the backward.  Its
+# launches are timed live by the library's kernel probe.
+ROOFLINE_KERNEL = "short_runs_kernel (tbe_backward_rowwise_adagrad, runs of fewer than 16 pairs)"
 ROOFLINE_KERNEL_SOURCES = ("update.cu", "common.cuh")
-ROOFLINE_PROFILE = "long_chunks_hot_row.md"
+# DRAM bytes per short-run pair of one short_runs_kernel launch, from a
+# one-kernel ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of
+# this recipe reduced to one table (each table of the recipe is an
+# independent draw and the kernel takes the tables' runs in key order), and
+# the sha1 of the kernel's sources it was taken on: the bench scales it by
+# the pairs of a full launch while the sources are unchanged, else reports
+# null.  None until a capture of the current sources exists.
+TRAFFIC_RECORD = None
 
 
 def source_sha1():
@@ -163,21 +186,14 @@ def source_sha1():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes of one launch of the roofline kernel on this workload, from
-    the committed ncu summary, if the kernel's sources are unchanged since
-    the capture (else None)."""
-    path = os.path.join(ROOT, "profiles", ROOFLINE_PROFILE)
-    try:
-        text = open(path).read()
-        digest = source_sha1()
-    except OSError:
+def recorded_traffic(units):
+    """DRAM bytes of one roofline-kernel launch over `units` short-run pairs,
+    scaled from the recorded capture; None without a record of the current
+    sources."""
+    rec = TRAFFIC_RECORD
+    if rec is None or rec["source_sha1"] != source_sha1():
         return None
-    fields = dict(line.split(":", 1) for line in text.splitlines()
-                  if line.startswith(("traffic_bytes_per_launch:", "source_sha1:")))
-    if fields.get("source_sha1", "").strip() != digest:
-        return None
-    return int(fields["traffic_bytes_per_launch"])
+    return int(rec["bytes_per_pair"] * units)
 
 
 def workload_name(args, base=WORKLOAD):
@@ -196,89 +212,245 @@ def momentum_bytes(D, elementwise):
     return 8 * D if elementwise else 8
 
 
-def long_chunk_bytes(D, long_pairs, chunks, long_runs, elementwise=False):
-    """Algorithmic bytes of one long_chunks_kernel launch, counted per use (the
-    per-unit figures of the design notes): per long pair its gradient row
-    (4 D) and pair data (8); per chunk its partial written and read back
-    (2 x 4 D) and its descriptor (16); per long run the weights row read and
-    written (2 x 2 D), the momentum (8, or 8 D element-wise) and the run
-    record (32)."""
-    return (long_pairs * (4 * D + 8) + chunks * (2 * 4 * D + 16)
-            + long_runs * (2 * 2 * D + momentum_bytes(D, elementwise) + 32))
+def short_run_bytes(D, pairs, runs, all_runs, elementwise=False):
+    """Algorithmic bytes of one short_runs_kernel launch, counted per use: per
+    short-run pair its bag (4), pair start (8) and gradient row (4 D); per
+    short run the weights row read and written (2 x 2 D) and the momentum (8,
+    or 8 D element-wise); per run of the batch its run data (8: the kernel
+    walks every run to pick the short ones)."""
+    return (pairs * (4 + 8 + 4 * D) + runs * (2 * 2 * D + momentum_bytes(D, elementwise))
+            + all_runs * 8)
 
 
-def forward_problem_bytes(w, rows_touched):
-    """Compulsory bytes of the forward problem: indices, offsets, every
-    distinct row once, the pooled output."""
+def compulsory_bytes(w, rows_touched, index_bytes, elementwise=False):
+    """Compulsory bytes of the forward, the backward and the whole step of
+    batch w: every index, offset and per-sample weight read once, every
+    distinct row once (rows_touched[t] rows of table t), the pooled output
+    written once and its gradient read once, each touched row's weights and
+    momentum read and written once."""
     nb = w.T * w.B
-    D = int(w.D[0])
-    return (w.n * INDEX_BYTES + (nb + 1) * INDEX_BYTES + rows_touched * D * 2
-            + w.B * int(w.D.sum()) * 4)
+    idx = w.n * index_bytes + (nb + 1) * index_bytes + (4 * w.n if w.psw is not None else 0)
+    dense = w.B * int(w.D.sum()) * 4
+    rows_w = sum(int(r) * int(d) * 2 for r, d in zip(rows_touched, w.D))
+    rows_m = sum(int(r) * momentum_bytes(int(d), elementwise) for r, d in zip(rows_touched, w.D))
+    return {"forward": idx + rows_w + dense,
+            "backward": idx + dense + 2 * rows_w + rows_m,
+            "step": idx + 2 * dense + 2 * rows_w + rows_m}
 
 
-def problem_roofline(w, rows_touched, r, peak, elementwise=False):
-    """Compulsory bytes of the forward, the backward and the whole step (each
-    index and offset read once, every distinct row once, the output written
-    once, grad_out read once, each touched row's weights and momentum read and
-    written once) over their measured time, against the HBM peak.  The
-    preprocess reads the indices for both passes, so its time counts in both."""
-    nb = w.T * w.B
-    D = int(w.D[0])
-    idx = w.n * INDEX_BYTES + (nb + 1) * INDEX_BYTES
-    out = w.B * int(w.D.sum()) * 4
-    fwd = idx + rows_touched * D * 2 + out
-    upd = rows_touched * (4 * D + momentum_bytes(D, elementwise))
-    bwd = idx + out + upd  # grad_out has the output's size
-    step = idx + 2 * out + upd
-    t = {"forward": r["pre_ms"] + r["fwd_ms"], "backward": r["pre_ms"] + r["upd_ms"],
-         "step": r["ms"] / r["steps"]}
+def rows_touched(w):
+    """Distinct valid rows each table's lookups touch (on the device)."""
+    L = (w.offsets[1:] - w.offsets[:-1]).long()
+    t_of = torch.repeat_interleave(torch.arange(w.T * w.B, device=L.device) // w.B, L)
+    E = torch.as_tensor(w.E, device=L.device)
+    r = w.indices.long()
+    ok = (r >= 0) & (r < E[t_of])
+    hb = torch.as_tensor(np.concatenate([[0], np.cumsum(w.E)]), device=L.device)
+    keys = torch.unique(hb[t_of[ok]] + r[ok])
+    return torch.bincount(torch.searchsorted(hb[1:], keys, right=True), minlength=w.T).cpu().numpy()
+
+
+def draw_batches(name, dev, rank, K, **kw):
+    """K distinct batches over one set of tables (table seed = rank): the
+    first drawn with its weights, the others sharing them."""
+    import workloads
+    w0 = workloads.make(name, device=dev, seed=1000 * rank, table_seed=rank, **kw)
+    return [w0] + [workloads.batch(w0, 1000 * rank + k) for k in range(1, K)]
+
+
+class Stepper:
+    """One problem's state (descriptor, workspace, weights, momentum, output)
+    and its training step through the public API."""
+
+    def __init__(self, tbe, batches, dev, wdt=torch.float16, mean=False, elementwise=False,
+                 momentum=None):
+        w = batches[0]
+        self.tbe = tbe
+        self.weighted = w.psw is not None
+        self.desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, dev, wdt)
+        self.n_max = max(b.n for b in batches)
+        self.ws = tbe.Workspace(self.desc, max(self.n_max, 1), self.weighted, dev, mean=mean)
+        self.weights = w.weights
+        self.momentum = momentum if momentum is not None else (
+            torch.zeros(self.desc.num_weights, dtype=torch.float32, device=dev) if elementwise
+            else w.momentum)
+        self.out = torch.empty(w.B, self.desc.total_D, dtype=torch.float32, device=dev)
+        self.pre_flags = tbe.TBE_F_PREPROCESSED | (tbe.TBE_F_MEAN if mean else 0)
+        self.upd_flags = self.pre_flags | (tbe.TBE_F_ELEMENTWISE if elementwise else 0)
+        self.mean = mean
+        self.elementwise = elementwise
+
+    def step(self, w, ev=None, arrangement="pre_in_fwd", two_launch=False):
+        """One training step on batch w.  pre_in_fwd (the timed step): one
+        preprocess of the batch serves the forward and the backward;
+        pre_in_bwd: the plain forward from the indices, and the backward
+        with its own preprocess.  ev: four events recorded around the
+        phases (pre_in_bwd: its first two coincide)."""
+        tbe = self.tbe
+        s = torch.cuda.current_stream()
+        extra = tbe.TBE_F_LONG_TWO_LAUNCH if two_launch else 0
+        rec = (lambda i: ev[i].record(s)) if ev is not None else (lambda i: None)
+        rec(0)
+        if arrangement == "pre_in_fwd":
+            tbe.tbe_preprocess(self.desc, w.indices, w.offsets, w.psw, self.ws)
+            rec(1)
+            tbe.tbe_forward(self.desc, self.weights, w.indices, w.offsets, w.psw, self.out,
+                            self.ws, self.pre_flags)
+            rec(2)
+            tbe.tbe_backward_rowwise_adagrad(self.desc, w.grad_out, w.indices, w.offsets, w.psw,
+                                             self.weights, self.momentum, w.lr, w.eps, self.ws,
+                                             self.upd_flags | extra)
+        else:
+            rec(1)
+            plain = (tbe.TBE_F_MEAN if self.mean else 0)
+            tbe.tbe_forward(self.desc, self.weights, w.indices, w.offsets, w.psw, self.out,
+                            self.ws, plain)
+            rec(2)
+            tbe.tbe_backward_rowwise_adagrad(
+                self.desc, w.grad_out, w.indices, w.offsets, w.psw, self.weights, self.momentum,
+                w.lr, w.eps, self.ws, plain | (tbe.TBE_F_ELEMENTWISE if self.elementwise else 0)
+                | extra)
+        rec(3)
+
+    def counters(self):
+        """The workspace's device counters after the last preprocess (syncs)."""
+        torch.cuda.synchronize()
+        v = self.tbe.tbe_workspace_view(self.desc, self.n_max, self.ws)
+        o = v["counts"] - self.ws.buf.data_ptr()
+        return self.ws.buf[o:o + 36].view(torch.int32).cpu().numpy().view(np.uint32), v
+
+    def ws_u32(self, ptr, count):
+        o = ptr - self.ws.buf.data_ptr()
+        return self.ws.buf[o:o + 4 * count].view(torch.int32)
+
+    def clear_hot_set(self):
+        """Empty the hot set the next preprocess takes (as in a fresh workspace)."""
+        torch.cuda.synchronize()
+        v = self.tbe.tbe_workspace_view(self.desc, self.n_max, self.ws)
+        self.ws_u32(v["hot_n"], self.desc.T).zero_()
+        torch.cuda.synchronize()
+
+
+def run_units(st, w):
+    """Work units of the last backward on batch w (counters of its
+    preprocess): cold lookups, runs by class, short-run pairs, and the
+    distinct (table, bag) gradient rows the short runs gather."""
+    c, v = st.counters()
+    R, n_long, n_chunks, n_cold = int(c[0]), int(c[2]), int(c[3]), int(c[7])
+    rp = st.ws_u32(v["run_pairs"], R + 1).long()
+    sl = rp[1:] - rp[:-1]
+    short = sl < int(v["medium_threshold"])
+    lng = sl >= int(v["long_threshold"])
+    P = int(c[6])
+    pair_run = torch.repeat_interleave(torch.arange(R, device=rp.device), sl)
+    pb = st.ws_u32(v["pair_bags"], P).long()
+    uk = st.ws_u32(v["unique_keys"], R).long() & 0xffffffff
+    hb = torch.as_tensor(np.concatenate([[0], np.cumsum(w.E)]), device=rp.device)
+    t_run = torch.searchsorted(hb[1:], uk, right=True)
+    sp = short[pair_run]
+    short_bag_rows = int(torch.unique(t_run[pair_run[sp]] * w.B + pb[sp]).numel())
+    hn = int(st.ws_u32(v["hot_n"], w.T).sum().item())
+    return {"R": R, "long_runs": n_long, "long_chunks": n_chunks, "cold_lookups": n_cold,
+            "short_runs": int(short.sum().item()), "short_pairs": int(sl[short].sum().item()),
+            "long_pairs": int(sl[lng].sum().item()), "short_bag_rows": short_bag_rows,
+            "hot_rows_next": hn, "hit_rate": 1.0 - n_cold / max(w.n, 1)}
+
+
+def l2_flush(buf):
+    """Overwrite a buffer larger than L2 (outside the timed events)."""
+    if buf is not None:
+        buf.add_(1)
+
+
+def time_phases(st, batches, steps, warmup, arrangement="pre_in_fwd", two_launch=False,
+                flush=None, first=0):
+    """Median phase times (ms) over `steps` timed steps cycling the batches
+    (warm-up steps first; every step's hot set comes from the step before)."""
+    K = len(batches)
+    for k in range(warmup):
+        st.step(batches[(first + k) % K], arrangement=arrangement, two_launch=two_launch)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for k in range(steps):
+        l2_flush(flush)
+        st.step(batches[(first + warmup + k) % K], evs[k], arrangement, two_launch)
+    torch.cuda.synchronize()
+    ph = lambda a, b: statistics.median(e[a].elapsed_time(e[b]) for e in evs)
+    return {"pre_ms": ph(0, 1), "fwd_ms": ph(0, 2), "bwd_ms": ph(2, 3), "step_ms": ph(0, 3),
+            "next": first + warmup + steps}
+
+
+CONFIG_KW = {"tiny": {}, "small": {}, "mixed": {}, "weighted": {}, "hot": {}}
+
+
+def measure_configs(tbe, dev, rank, args, hbm, main=None):
+    """Per recipe at its stated size: forward, backward and step ms in both
+    arrangements of the preprocessing (in the forward: one preprocess serves
+    both passes; in the backward: the plain forward from the indices and a
+    backward that sorts for itself), lookups/s, and the compulsory bytes of
+    each phase as a fraction of the HBM peak; for the hot and weighted
+    recipes also the long runs' fused and two-launch updates.  L2 is flushed
+    before every timed step.  main: the hot recipe's batches and stepper of
+    the headline run, reused."""
     res = {}
-    for k, b in (("forward", fwd), ("backward", bwd), ("step", step)):
-        gbs = b / (t[k] / 1e3) / 1e9
-        res[k] = {"min_bytes": b, "ms": t[k], "GBps": gbs, "frac": gbs / peak}
-    res["note"] = "compulsory bytes over time; preprocess time counted in forward and backward"
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 2x L2
+    for name in args.configs.split(","):
+        if name == "hot" and main is not None:
+            batches, st = main
+        else:
+            batches = draw_batches(name, dev, rank, 2, **CONFIG_KW[name])
+            st = Stepper(tbe, batches, dev)
+        w = batches[0]
+        ib = w.indices.element_size()
+        steps, warm = args.config_steps, 3
+        r = {"n_lookups": w.n, "T": w.T, "B": w.B}
+        touched = rows_touched(w)
+        cb = compulsory_bytes(w, touched, ib)
+        first = 0
+        for arr in ("pre_in_fwd", "pre_in_bwd"):
+            ph = time_phases(st, batches, steps, warm, arr, flush=flush, first=first)
+            first = ph["next"]
+            r[arr] = {"fwd_ms": ph["fwd_ms"], "bwd_ms": ph["bwd_ms"], "sum_ms": ph["step_ms"],
+                      "lookups_per_s": w.n / (ph["step_ms"] / 1e3),
+                      "roofline_frac": {k: cb[k] / (t / 1e3) / 1e9 / hbm for k, t in
+                                        (("forward", ph["fwd_ms"]), ("backward", ph["bwd_ms"]),
+                                         ("step", ph["step_ms"]))}}
+        if name in ("hot", "weighted"):
+            ph2 = time_phases(st, batches, steps, warm, "pre_in_fwd", two_launch=True,
+                              flush=flush, first=first)
+            r["long_runs_update"] = {"fused_bwd_ms": r["pre_in_fwd"]["bwd_ms"],
+                                     "two_launch_bwd_ms": ph2["bwd_ms"],
+                                     "two_launch_sum_ms": ph2["step_ms"]}
+        r["compulsory_bytes"] = cb
+        res[name] = r
+        if not (name == "hot" and main is not None):
+            del st, batches, w
+            torch.cuda.empty_cache()
+    r0 = {"note": "median of timed steps over 2 distinct batches per recipe (the hot recipe: "
+                  "the headline batches); fractions are compulsory bytes over time against "
+                  "the measured HBM peak; L2 flushed before each timed step"}
+    res.update(r0)
     return res
 
 
 def run_native(args, world, rank, local):
     import table_embedding_bag_gb300 as tbe
-    import workloads
 
     dev = torch.device("cuda", torch.cuda.current_device())
+    import workloads
     E_scale = None if args.rows is None else args.rows / workloads.SPECS["hot"].E
     wdt = torch.bfloat16 if args.weights == "bf16" else torch.float16
-    w = workloads.make("hot", device=dev, seed=rank, T=args.tables, B=args.bags, E_scale=E_scale,
-                       weights_dtype=wdt)
-    desc = tbe.TBEDesc(w.E, w.D, w.B, w.indices.dtype, dev, wdt)
     mean = args.pooling == "mean"
     ew = args.optimizer == "elementwise"
-    ws = tbe.Workspace(desc, w.n, False, dev, mean=mean)
-    weights = w.weights
-    momentum = (torch.zeros(desc.num_weights, dtype=torch.float32, device=dev) if ew
-                else w.momentum)
-    out = torch.empty(w.B, desc.total_D, dtype=torch.float32, device=dev)
+    K = max(1, args.batches)
+    batches = draw_batches("hot", dev, rank, K, T=args.tables, B=args.bags, E_scale=E_scale,
+                           weights_dtype=wdt)
+    w = batches[0]
+    st = Stepper(tbe, batches, dev, wdt, mean=mean, elementwise=ew)
     stream = torch.cuda.current_stream()
 
-    PRE = tbe.TBE_F_PREPROCESSED | (tbe.TBE_F_MEAN if mean else 0)
-    UPD = PRE | (tbe.TBE_F_ELEMENTWISE if ew else 0)
-
-    def step(ev=None):
-        # one preprocess of the batch's indices serves forward and backward
-        if ev is not None:
-            ev[0].record(stream)
-        tbe.tbe_preprocess(desc, w.indices, w.offsets, None, ws)
-        if ev is not None:
-            ev[1].record(stream)
-        tbe.tbe_forward(desc, weights, w.indices, w.offsets, None, out, ws, PRE)
-        if ev is not None:
-            ev[2].record(stream)
-        tbe.tbe_backward_rowwise_adagrad(desc, w.grad_out, w.indices, w.offsets, None, weights,
-                                         momentum, w.lr, w.eps, ws, UPD)
-        if ev is not None:
-            ev[3].record(stream)
-
-    for _ in range(args.warmup):
-        step()
+    for k in range(args.warmup):
+        st.step(batches[k % K])
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = Clocks(local)
@@ -286,11 +458,11 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    tbe.tbe_probe_set(tbe.TBE_PROBE_LONG_CHUNKS)
+    tbe.tbe_probe_set(tbe.TBE_PROBE_SHORT_RUNS)
     launches0 = tbe.tbe_kernel_launches()
     t0.record(stream)
     for k in range(args.steps):
-        step(evs[k])
+        st.step(batches[(args.warmup + k) % K], evs[k])
     t1.record(stream)
     launches = tbe.tbe_kernel_launches() - launches0
     probe_launches, probe_ms = tbe.tbe_probe_read()
@@ -298,7 +470,7 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    status = tbe.tbe_read_status(ws)
+    status = tbe.tbe_read_status(st.ws)
     if status & tbe.TBE_ERR_TIMEOUT:
         raise SystemExit("bench: a kernel's bounded wait timed out during the timed steps "
                          f"(status {status:#x}); the measurement is invalid")
@@ -307,43 +479,44 @@ def run_native(args, world, rank, local):
     pre = [e[0].elapsed_time(e[1]) for e in evs]
     fwd = [e[1].elapsed_time(e[2]) for e in evs]
     upd = [e[2].elapsed_time(e[3]) for e in evs]
+    lookups = sum(batches[(args.warmup + k) % K].n for k in range(args.steps))
 
-    view = tbe.tbe_workspace_view(desc, w.n, ws)
-    off = view["counts"] - ws.buf.data_ptr()
-    counts = ws.buf[off:off + 32].view(torch.int32).cpu().numpy().view(np.uint32)
-    R, n_long, n_chunks = int(counts[0]), int(counts[2]), int(counts[3])
-    n_cold = int(counts[7])  # lookups left to the sort after the hot rows
-    # hot rows per table (the set the next step uses; the same batch repeats,
-    # so it is also the set the timed steps used)
-    hoff = view["hot_n"] - ws.buf.data_ptr()
-    n_hot = int(ws.buf[hoff:hoff + 4 * w.T].view(torch.int32).cpu().numpy().sum())
-
-    def ws_u32(ptr, count):
-        o = ptr - ws.buf.data_ptr()
-        return ws.buf[o:o + 4 * count].view(torch.int32).cpu().numpy().view(np.uint32)
-
-    # pairs of the long runs (the units of the long-run kernel)
-    run_pairs = ws_u32(view["run_pairs"], R + 1).astype(np.int64)
-    long_idx = ws_u32(view["long_runs"], n_long).astype(np.int64)
-    long_pairs = int((run_pairs[long_idx + 1] - run_pairs[long_idx]).sum()) if n_long else 0
+    # work units per batch, continuing the cycle (each hot set from the batch before)
+    nxt = args.warmup + args.steps
+    units = []
+    for j in range(K):
+        b = batches[(nxt + j) % K]
+        st.step(b)
+        units.append(run_units(st, b))
+    nxt += K
+    avg = {k: float(np.mean([u[k] for u in units])) for k in units[0]}
+    # first step with an empty hot set (a fresh workspace's first batch)
+    st.clear_hot_set()
+    ce = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    b = batches[nxt % K]
+    st.step(b, ce)
+    torch.cuda.synchronize()
+    cold = {"step_ms": ce[0].elapsed_time(ce[3]), "fwd_ms": ce[0].elapsed_time(ce[2]),
+            "bwd_ms": ce[2].elapsed_time(ce[3])}
+    nxt += 1
     result = {
         "ms": ms, "ms_local": ms_local, "fwd_ms": statistics.median(fwd),
         "pre_ms": statistics.median(pre), "upd_ms": statistics.median(upd),
-        "n": w.n, "R": R, "n_long": n_long, "n_chunks": n_chunks, "n_cold": n_cold,
-        "n_hot": n_hot, "long_pairs": long_pairs, "clocks": clk,
-        "probe_launches": probe_launches, "probe_ms": probe_ms,
-        "launches": launches, "w": w,
+        "lookups": lookups, "units": avg, "units_per_batch": units, "cold_start": cold,
+        "clocks": clk, "probe_launches": probe_launches, "probe_ms": probe_ms,
+        "launches": launches, "w": w, "batches": batches, "stepper": st, "next": nxt,
     }
 
     if not args.no_e2e:
         # End to end through the public API: per step, this step's inputs go
         # host -> device from pinned memory and the pooled output comes back.
-        # Two device input slots: step k+1's uploads (copy stream) overlap
-        # step k's compute, and step k's output download (a third stream)
-        # overlaps its backward; every copy stays inside the timed region.
-        h_idx = w.indices.cpu().pin_memory()
-        h_off = w.offsets.cpu().pin_memory()
-        h_grad = w.grad_out.cpu().pin_memory()
+        # Two distinct batches alternate on the host.  Two device input slots:
+        # step k+1's uploads (copy stream) overlap step k's compute, and step
+        # k's output download (a third stream) overlaps its backward; every
+        # copy stays inside the timed region.
+        hb = [(b.indices.cpu().pin_memory(), b.offsets.cpu().pin_memory(),
+               b.grad_out.cpu().pin_memory()) for b in batches[:2]]
+        out = st.out
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         slots = [(torch.empty_like(w.indices), torch.empty_like(w.offsets),
                   torch.empty_like(w.grad_out)) for _ in range(2)]
@@ -354,6 +527,7 @@ def run_native(args, world, rank, local):
 
         def e2e_step(k):
             d_idx, d_off, d_grad = slots[k % 2]
+            h_idx, h_off, h_grad = hb[k % len(hb)]
             with torch.cuda.stream(up):
                 if k >= 2:
                     up.wait_event(consumed[k % 2])
@@ -364,15 +538,15 @@ def run_native(args, world, rank, local):
             stream.wait_event(copied[k % 2])
             if k >= 1:
                 stream.wait_event(out_read)  # the previous output was read back
-            tbe.tbe_preprocess(desc, d_idx, d_off, None, ws)
-            tbe.tbe_forward(desc, weights, d_idx, d_off, None, out, ws, PRE)
+            tbe.tbe_preprocess(st.desc, d_idx, d_off, None, st.ws)
+            tbe.tbe_forward(st.desc, st.weights, d_idx, d_off, None, out, st.ws, st.pre_flags)
             fwd_done.record(stream)
             with torch.cuda.stream(down):
                 down.wait_event(fwd_done)
                 h_out.copy_(out, non_blocking=True)
                 out_read.record(down)
-            tbe.tbe_backward_rowwise_adagrad(desc, d_grad, d_idx, d_off, None, weights, momentum,
-                                             w.lr, w.eps, ws, UPD)
+            tbe.tbe_backward_rowwise_adagrad(st.desc, d_grad, d_idx, d_off, None, st.weights,
+                                             st.momentum, w.lr, w.eps, st.ws, st.upd_flags)
             consumed[k % 2].record(stream)
 
         for k in range(max(1, args.warmup)):
@@ -380,21 +554,25 @@ def run_native(args, world, rank, local):
         torch.cuda.synchronize()
         barrier(world)
         a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
+        bev = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         up.wait_event(a)
         down.wait_event(a)
         for k in range(args.steps):
             e2e_step(k + 2 * args.warmup)  # the slot pattern continues past the warm-up
         stream.wait_event(out_read)
-        b.record(stream)
+        bev.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        e2e_ms = max_over_ranks(a.elapsed_time(bev), world, dev)
         result["e2e_ms"] = e2e_ms
-        result["h2d"] = h_idx.numel() * h_idx.element_size() + h_off.numel() * 8 + \
-            h_grad.numel() * 4
+        result["e2e_lookups"] = sum(batches[(k + 2 * args.warmup) % len(hb)].n
+                                    for k in range(args.steps))
+        hidx, hoff, hgrad = hb[0]
+        result["h2d"] = (hidx.numel() * hidx.element_size() + hoff.numel() * hoff.element_size()
+                         + hgrad.numel() * 4)
         result["d2h"] = h_out.numel() * 4
+        del hb, slots
     return result
 
 
@@ -478,7 +656,7 @@ def main():
 
     r = run_native(args, world, rank, local)
     w = r["w"]
-    total_lookups = w.n * world * args.steps
+    total_lookups = r["lookups"] * world
     value = total_lookups / (r["ms"] / 1e3)
     peaks = {}
     try:
@@ -489,49 +667,81 @@ def main():
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     D = int(w.D[0])
     ew = args.optimizer == "elementwise"
-    kb = long_chunk_bytes(D, r["long_pairs"], r["n_chunks"], r["n_long"], ew)
+    u = r["units"]
+    kb = short_run_bytes(D, u["short_pairs"], u["short_runs"], u["R"], ew)
     k_launch_ms = r["probe_ms"] / max(r["probe_launches"], 1)
     achieved = kb / (k_launch_ms / 1e3) / 1e9
-    fwd_problem = forward_problem_bytes(w, r["R"] + r["n_hot"])
+    # compulsory bytes of the kernel: each short run's row and momentum read
+    # and written once, its pair data once, each gradient row it gathers once
+    k_min = (u["short_runs"] * (2 * 2 * D + momentum_bytes(D, ew)) + u["R"] * 8
+             + u["short_pairs"] * 12 + u["short_bag_rows"] * 4 * D)
+    reduced = (args.tables, args.rows, args.bags) != (None,) * 3
+    touched = rows_touched(w)
+    cb = compulsory_bytes(w, touched, w.indices.element_size(), ew)
+    t_fwd = r["pre_ms"] + r["fwd_ms"]
+    t_step = r["ms_local"] / args.steps
+    t_bwd = r["upd_ms"]
     line = {
         "metric": METRIC, "value": value, "unit": "lookups/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": workload_name(
-                       args, WORKLOAD if (args.tables, args.rows, args.bags) == (None,) * 3
+                       args, WORKLOAD if not reduced
                        else f"reduced hot-row recipe T={w.T} E={int(w.E[0])} B={w.B} "
                             "(profiling case)"),
                    "n_lookups": w.n, "global_batch": w.B * world,
+                   "batches": f"{len(r['batches'])} distinct batches over the same tables "
+                              "(table seed = rank), cycled; each step's hot set was learned "
+                              "on the batch before",
                    "parallelism": f"replicas x{world} (independent batches)",
-                   "l2": f"inputs larger than L2 (indices {w.n * INDEX_BYTES / 1e9:.2f} GB, "
-                         f"weights {w.weights.numel() * 2 / 1e9:.1f} GB); no flush",
+                   "l2": f"inputs larger than L2 (indices {w.n * INDEX_BYTES / 1e9:.2f} GB "
+                         f"per batch, weights {w.weights.numel() * 2 / 1e9:.1f} GB); no flush",
                    "storage": f"{args.weights} weights, fp32 "
                               f"{'per-element' if ew else 'per-row'} momentum, fp32 gradients"},
-        "phases_ms": {"forward": r["fwd_ms"], "preprocess": r["pre_ms"], "update": r["upd_ms"]},
-        "runs": {"R": r["R"], "long_runs": r["n_long"], "long_chunks": r["n_chunks"],
-                 "cold_lookups": r["n_cold"], "hot_rows": r["n_hot"]},
+        "phases_ms": {"preprocess": r["pre_ms"], "forward": r["fwd_ms"], "update": r["upd_ms"],
+                      "note": "median per step; the sort chain runs on a side stream during "
+                              "the forward and is waited for by the update"},
+        "hot_rows": {"hit_rate": u["hit_rate"], "cold_lookups": u["cold_lookups"],
+                     "hot_rows": u["hot_rows_next"],
+                     "hit_rate_per_batch": [x["hit_rate"] for x in r["units_per_batch"]],
+                     "note": "fraction of lookups served by hot rows learned on the previous "
+                             "batch"},
+        "cold_start_ms": dict(r["cold_start"], note="one step whose hot set is empty (a "
+                                                    "fresh workspace's first batch)"),
+        "runs": {k: u[k] for k in ("R", "long_runs", "long_chunks", "short_runs",
+                                   "short_pairs", "long_pairs")},
         "roofline": {"kernel": ROOFLINE_KERNEL, "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": profiled_traffic() if args.tables is None else None,
+                     "traffic": None if reduced else recorded_traffic(u["short_pairs"]),
                      "peak_source": peak_src,
-                     "bytes_model": "per use: gradient row + pair data per long pair, "
-                                    "partial write+read per chunk, weights row r/w + "
-                                    "momentum per long run",
+                     "bytes_model": "per use: bag + pair start + gradient row per short-run "
+                                    "pair, weights row r/w + momentum per short run, run data "
+                                    "per run",
                      "bytes_per_launch": kb, "launch_ms": k_launch_ms,
                      "launches_timed": r["probe_launches"],
-                     "units": {"long_pairs": r["long_pairs"], "chunks": r["n_chunks"],
-                               "long_runs": r["n_long"]}},
-        "forward_context": {"phase_ms": r["fwd_ms"],
-                            "problem_min_GBps": fwd_problem / (r["fwd_ms"] / 1e3) / 1e9},
-        "problem_roofline": problem_roofline(w, r["R"] + r["n_hot"], dict(r, steps=args.steps), hbm,
-                                             ew),
+                     "compulsory_bytes_per_launch": k_min,
+                     "compulsory_frac": k_min / (k_launch_ms / 1e3) / 1e9 / hbm,
+                     "units": {"short_pairs": u["short_pairs"], "short_runs": u["short_runs"],
+                               "runs": u["R"], "short_bag_rows": u["short_bag_rows"]}},
+        "problem_roofline": {
+            k: {"min_bytes": cb[k], "ms": t, "GBps": cb[k] / (t / 1e3) / 1e9,
+                "frac": cb[k] / (t / 1e3) / 1e9 / hbm}
+            for k, t in (("forward", t_fwd), ("backward", t_bwd), ("step", t_step))},
         "clocks": r["clocks"],
         "gpu_launches": r["launches"],
     }
+    line["problem_roofline"]["note"] = ("compulsory bytes over time: forward = preprocess + "
+                                        "forward phases, backward = update phase")
     if "e2e_ms" in r:
-        line["e2e"] = {"value": total_lookups / (r["e2e_ms"] / 1e3), "unit": "lookups/s",
-                       "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}
+        line["e2e"] = {"value": r["e2e_lookups"] * world / (r["e2e_ms"] / 1e3),
+                       "unit": "lookups/s", "h2d_bytes_per_step": r["h2d"],
+                       "d2h_bytes_per_step": r["d2h"]}
+    if not args.no_configs and not reduced and world == 1 and args.weights == "fp16" \
+            and not ew and args.pooling == "sum":
+        import table_embedding_bag_gb300 as tbe
+        line["configs"] = measure_configs(tbe, w.indices.device, rank, args, hbm,
+                                          main=(r["batches"], r["stepper"]))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = cpu_sample(w, args.cpu_bags)
         dt = time_oracle(s, args.pooling == "mean", args.optimizer == "elementwise")

@@ -27,9 +27,9 @@
  *
  * Data layout (all device buffers are owned by the caller):
  *  - T tables; table t has E_t rows of width D_t (D_t a multiple of 8, at
- *    most 1024).  Weights are fp16 or bf16 (weights_dtype), one flat buffer;
- *    table t starts at element weights_offsets[t], its rows are contiguous
- *    with stride D_t.
+ *    most 1024).  Weights are fp16, bf16 or fp32 (weights_dtype), one flat
+ *    buffer; table t starts at element weights_offsets[t], its rows are
+ *    contiguous with stride D_t.
  *  - Momentum: fp32 [sum E_t], one value per row, row r of table t at
  *    hash_base[t] + r; with TBE_F_ELEMENTWISE fp32 [weights_offsets[T]], one
  *    value per weight element at the element's own position.
@@ -77,7 +77,7 @@ typedef enum tbe_status {
 } tbe_status;
 
 /* element types */
-enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3, TBE_DT_BF16 = 4 };
+enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3, TBE_DT_BF16 = 4, TBE_DT_F32 = 5 };
 
 /* call flags */
 #define TBE_F_CHECK_BOUNDS (1u << 0)    /* validate offsets (separate kernel) and indices,
@@ -132,10 +132,13 @@ enum { TBE_DT_F16 = 1, TBE_DT_I32 = 2, TBE_DT_I64 = 3, TBE_DT_BF16 = 4 };
 typedef struct tbe_desc {
   int32_t T;                        /* number of tables, >= 1 */
   int32_t B;                        /* bags per table (batch size), >= 1 */
-  int32_t weights_dtype;            /* TBE_DT_F16, or TBE_DT_BF16 (accumulated in fp32
-                                       like fp16; the tensor-core paths -- hot rows and
-                                       the small table -- are fp16 only, so bf16 tables
-                                       take the gather paths throughout) */
+  int32_t weights_dtype;            /* TBE_DT_F16, TBE_DT_BF16 (accumulated in fp32
+                                       like fp16) or TBE_DT_F32 (the forward accumulates
+                                       each output as a compensated two-float sum: as
+                                       accurate as an fp64 accumulation rounded once to
+                                       fp32, see tbe_forward).  The small-table path
+                                       takes fp16 only and the hot rows fp16 only, so
+                                       other types take the gather paths there */
   int32_t index_dtype;              /* TBE_DT_I32 or TBE_DT_I64; offsets use it too */
   const int64_t* D_offsets;         /* device [T+1]: sum of D_t' for t' < t */
   const int64_t* hash_base;         /* device [T+1]: sum of E_t' for t' < t */
@@ -171,6 +174,8 @@ typedef struct tbe_ws_view {
   const uint32_t* hot_keys;     /* [T][hot_slots] hot rows of each table (linear keys, sorted) */
   const uint32_t* hot_n;        /* [T] hot rows per table */
   int32_t hot_slots;            /* hot rows a table can have */
+  int32_t medium_threshold;     /* pairs from which a run below long_threshold is updated
+                                   by a whole warp (fewer pairs: several runs per warp) */
 } tbe_ws_view;
 
 /* Bytes of workspace needed for calls with at most n_max lookups.
@@ -187,7 +192,13 @@ tbe_status tbe_workspace_size(const tbe_desc* d, int64_t n_max, uint32_t ws_flag
  * general one"):
  *   out[b, D_offsets[t] + c] = sum over lookups i of bag (t,b) with a valid row
  *                              of psw_i * W_t[indices[i], c]   (psw_i = 1 if NULL)
- * accumulated in fp32.  An empty bag yields zeros.  One table with E <= 64,
+ * accumulated in fp32 for 16-bit weights.  fp32 weights are accumulated as
+ * an unevaluated sum hi + lo of two fp32 values (each addition an exact
+ * two-sum, each weighted product exact through a fused multiply-add), rounded
+ * once at the end; its error is the final rounding plus at most about
+ * n^2 2^-48 of the sum of |terms| for a bag of n lookups, below 1e-9 of
+ * it up to n = 250, as with the fp64 accumulation the pages name for fp32
+ * weights.  An empty bag yields zeros.  One table with E <= 64,
  * 64 <= D <= 128, no per-sample weights and an average bag length >= 64 takes
  * the tensor-core histogram path (counts per bag times the table) unless
  * TBE_F_FORCE_GENERIC; every other problem takes the generic gather-pool.
@@ -201,7 +212,8 @@ tbe_status tbe_workspace_size(const tbe_desc* d, int64_t n_max, uint32_t ws_flag
  * lookups are gathered from the per-bag cold lists (bf16 problems have no
  * hot rows: every lookup is a cold one); the bounds/offsets flags are then ignored (the preprocess
  * checked them) and per_sample_weights must be NULL exactly when it was NULL
- * for the preprocess.
+ * for the preprocess.  fp32 weights are always pooled from the indices, as
+ * without the flag.
  * weights: device, weights_dtype; indices/offsets: device, index_dtype; n: lookups
  * (length of indices); per_sample_weights: fp32 device [n] or NULL;
  * out: fp32 device [B, total_D], fully overwritten.  Workspace: the status
@@ -242,9 +254,10 @@ tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* of
  *   m_r  <- m_r + (1/D_t) * sum_c g_c^2
  *   W_t[r, c] <- fp16_rn(W_t[r, c] - lr * g_c / (sqrt(m_r) + eps))
  * exactly once per touched row; untouched rows are not written (fp16_rn is
- * bf16_rn for TBE_DT_BF16 weights; TBE_F_ELEMENTWISE replaces the row
- * accumulator by one per element, see the flag).
- * grad_out: fp32 device [B, total_D]; weights (16-bit) and momentum (fp32
+ * bf16_rn for TBE_DT_BF16 weights, and the fp32 rounding of the step formed
+ * in fp32 for TBE_DT_F32; TBE_F_ELEMENTWISE replaces the row accumulator by
+ * one per element, see the flag).
+ * grad_out: fp32 device [B, total_D]; weights (weights_dtype) and momentum (fp32
  * [total_E], or [weights_offsets[T]] with TBE_F_ELEMENTWISE) are updated in
  * place.  Without TBE_F_PREPROCESSED the call runs
  * tbe_preprocess first.  The gradient of a hot row (see tbe_preprocess) is

@@ -28,7 +28,7 @@ __all__ = [
 
 TBE_OK, TBE_EINVAL, TBE_EWORKSPACE, TBE_EUNSUPPORTED, TBE_ECUDA, TBE_ETOO_LARGE = range(6)
 TBE_NOALLOC_SCRATCH_BYTES = 32 << 20
-TBE_DT_F16, TBE_DT_I32, TBE_DT_I64, TBE_DT_BF16 = 1, 2, 3, 4
+TBE_DT_F16, TBE_DT_I32, TBE_DT_I64, TBE_DT_BF16, TBE_DT_F32 = 1, 2, 3, 4, 5
 TBE_F_CHECK_BOUNDS = 1 << 0
 TBE_F_REPAIR_OFFSETS = 1 << 1
 TBE_F_FORCE_GENERIC = 1 << 2
@@ -81,7 +81,7 @@ class tbe_ws_view(ctypes.Structure):
                 ("chunk", ctypes.c_int32), ("run_pairs", ctypes.c_void_p),
                 ("pair_starts", ctypes.c_void_p), ("pair_bags", ctypes.c_void_p),
                 ("hot_keys", ctypes.c_void_p), ("hot_n", ctypes.c_void_p),
-                ("hot_slots", ctypes.c_int32)]
+                ("hot_slots", ctypes.c_int32), ("medium_threshold", ctypes.c_int32)]
 
 
 _lib = None
@@ -134,9 +134,13 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+_WEIGHT_DT = {torch.float16: TBE_DT_F16, torch.bfloat16: TBE_DT_BF16,
+              torch.float32: TBE_DT_F32}
+
+
 class TBEDesc:
     """Problem description: per-table rows E_t and widths D_t, bags per table B,
-    index dtype and weight dtype (torch.float16 or torch.bfloat16).  Holds the
+    index dtype and weight dtype (torch.float16, torch.bfloat16 or torch.float32).  Holds the
     three cumulative int64 arrays on the device."""
 
     def __init__(self, E, D, B, index_dtype=torch.int64, device="cuda",
@@ -149,8 +153,9 @@ class TBEDesc:
             raise ValueError("every D_t must be a multiple of 8 in [8, 1024]")
         self.T, self.B = len(self.E), int(B)
         self.index_dtype = index_dtype
-        if weights_dtype not in (torch.float16, torch.bfloat16):
-            raise ValueError("weights_dtype must be torch.float16 or torch.bfloat16")
+        if weights_dtype not in _WEIGHT_DT:
+            raise ValueError("weights_dtype must be torch.float16, torch.bfloat16 or "
+                             "torch.float32")
         self.weights_dtype = weights_dtype
         cum = lambda a: np.concatenate([[0], np.cumsum(a)]).astype(np.int64)
         self.D_offsets_h = cum(self.D)
@@ -163,8 +168,7 @@ class TBEDesc:
         self.total_D = int(self.D_offsets_h[-1])
         self.total_E = int(self.hash_base_h[-1])
         self.num_weights = int(self.weights_offsets_h[-1])
-        self.c = tbe_desc(self.T, self.B,
-                          TBE_DT_BF16 if weights_dtype == torch.bfloat16 else TBE_DT_F16,
+        self.c = tbe_desc(self.T, self.B, _WEIGHT_DT[weights_dtype],
                           TBE_DT_I32 if index_dtype == torch.int32 else TBE_DT_I64,
                           self.D_offsets.data_ptr(), self.hash_base.data_ptr(),
                           self.weights_offsets.data_ptr(), self.total_D, self.total_E,

@@ -20,9 +20,13 @@
 namespace tbe {
 namespace {
 
-template <typename IndexT, bool kWeighted, bool kBf16>
+// Weight types of the generic forward: fp16, bf16 (fp32 accumulation) and
+// fp32 (compensated accumulation, pool_bag_f32).
+constexpr int kWF16 = 0, kWBF16 = 1, kWF32 = 2;
+
+template <typename IndexT, bool kWeighted, int kWT>
 __global__ void __launch_bounds__(256, TBE_FWD_MINB)
-    forward_generic_kernel(const __half* __restrict__ W, const int64_t* __restrict__ D_offsets,
+    forward_generic_kernel(const void* __restrict__ Wv, const int64_t* __restrict__ D_offsets,
                            const int64_t* __restrict__ hash_base,
                            const int64_t* __restrict__ w_offsets,
                            const IndexT* __restrict__ indices, const IndexT* __restrict__ offsets,
@@ -41,13 +45,32 @@ __global__ void __launch_bounds__(256, TBE_FWD_MINB)
     const int64_t E = __ldg(hash_base + t + 1) - h0;
     const int64_t rbase = 0;
     const int mode = kPoolStore;
-    const __half* Wt = W + __ldg(w_offsets + t);
     int64_t s, e;
     bag_range(offsets, bag, n, &s, &e);
     // mean pooling: the sum times 1/L for L > 1 lookups
     const float scale = mean && e - s > 1 ? 1.f / static_cast<float>(e - s) : 1.f;
     float* orow = out + b * total_D + d0;
     const int nvec = D >> 3;
+    if constexpr (kWT == kWF32) {
+      const float* Wt = static_cast<const float*>(Wv) + __ldg(w_offsets + t);
+      if (nvec <= 1)
+        pool_bag_f32<1, IndexT, kWeighted>(Wt, E, D, 0, indices, psw, s, e, orow, status, scale);
+      else if (nvec <= 2)
+        pool_bag_f32<2, IndexT, kWeighted>(Wt, E, D, 0, indices, psw, s, e, orow, status, scale);
+      else if (nvec <= 4)
+        pool_bag_f32<4, IndexT, kWeighted>(Wt, E, D, 0, indices, psw, s, e, orow, status, scale);
+      else if (nvec <= 8)
+        pool_bag_f32<8, IndexT, kWeighted>(Wt, E, D, 0, indices, psw, s, e, orow, status, scale);
+      else if (nvec <= 16)
+        pool_bag_f32<16, IndexT, kWeighted>(Wt, E, D, 0, indices, psw, s, e, orow, status, scale);
+      else
+        for (int vec0 = 0; vec0 < nvec; vec0 += 32)
+          pool_bag_f32<32, IndexT, kWeighted>(Wt, E, D, vec0, indices, psw, s, e, orow, status,
+                                              scale);
+      continue;
+    }
+    constexpr bool kBf16 = kWT == kWBF16;
+    const __half* Wt = static_cast<const __half*>(Wv) + __ldg(w_offsets + t);
     if (nvec <= 1)
       pool_bag<1, IndexT, kWeighted, TBE_FWD_UNROLL, kBf16>(Wt, E, rbase, D, 0, indices, psw, s, e, orow, mode, status, scale);
     else if (nvec <= 2)
@@ -282,7 +305,7 @@ __global__ void __launch_bounds__(kFixThreads)
 }
 
 template <typename IndexT>
-cudaError_t launch_forward_t(const Launch& L, const __half* W, const IndexT* indices,
+cudaError_t launch_forward_t(const Launch& L, const void* W, const IndexT* indices,
                              const IndexT* offsets, const float* psw, float* out, int* status,
                              bool mean) {
   const tbe_desc* d = L.d;
@@ -297,13 +320,15 @@ cudaError_t launch_forward_t(const Launch& L, const __half* W, const IndexT* ind
         d->B, d->total_D, out, status, mean);
     note_launch();
   };
-  const bool bf16 = d->weights_dtype == TBE_DT_BF16;
+  const int wt = d->weights_dtype;
   if (psw) {
-    if (bf16) go(forward_generic_kernel<IndexT, true, true>);
-    else go(forward_generic_kernel<IndexT, true, false>);
+    if (wt == TBE_DT_F32) go(forward_generic_kernel<IndexT, true, kWF32>);
+    else if (wt == TBE_DT_BF16) go(forward_generic_kernel<IndexT, true, kWBF16>);
+    else go(forward_generic_kernel<IndexT, true, kWF16>);
   } else {
-    if (bf16) go(forward_generic_kernel<IndexT, false, true>);
-    else go(forward_generic_kernel<IndexT, false, false>);
+    if (wt == TBE_DT_F32) go(forward_generic_kernel<IndexT, false, kWF32>);
+    else if (wt == TBE_DT_BF16) go(forward_generic_kernel<IndexT, false, kWBF16>);
+    else go(forward_generic_kernel<IndexT, false, kWF16>);
   }
   return cudaGetLastError();
 }
@@ -331,7 +356,7 @@ cudaError_t launch_offsets_t(const Launch& L, const IndexT* offsets, bool repair
 cudaError_t launch_forward_generic(const Launch& L, const void* weights, const void* indices,
                                    const void* offsets, const float* psw, float* out,
                                    int* status, bool mean) {
-  const __half* W = static_cast<const __half*>(weights);
+  const void* W = weights;
   if (L.d->index_dtype == TBE_DT_I32)
     return launch_forward_t<int32_t>(L, W, static_cast<const int32_t*>(indices),
                                      static_cast<const int32_t*>(offsets), psw, out, status, mean);

@@ -47,7 +47,9 @@ tbe_status check_args(const tbe_desc* d, const void* indices, const void* offset
   if (!d) return TBE_EINVAL;
   if (d->T < 1 || d->B < 1 || !d->D_offsets || !d->hash_base || !d->weights_offsets)
     return TBE_EINVAL;
-  if (d->weights_dtype != TBE_DT_F16 && d->weights_dtype != TBE_DT_BF16) return TBE_EUNSUPPORTED;
+  if (d->weights_dtype != TBE_DT_F16 && d->weights_dtype != TBE_DT_BF16 &&
+      d->weights_dtype != TBE_DT_F32)
+    return TBE_EUNSUPPORTED;
   if (d->index_dtype != TBE_DT_I32 && d->index_dtype != TBE_DT_I64) return TBE_EUNSUPPORTED;
   if (d->min_D < 8 || d->max_D > kMaxD || d->min_D > d->max_D || (d->min_D & 7) ||
       (d->max_D & 7) || d->total_D < d->max_D || (d->total_D & 7))

@@ -175,7 +175,9 @@ tbe_status check_desc(const tbe_desc* d) {
   if (!d) return TBE_EINVAL;
   if (d->T < 1 || d->B < 1 || !d->D_offsets || !d->hash_base || !d->weights_offsets)
     return TBE_EINVAL;
-  if (d->weights_dtype != TBE_DT_F16 && d->weights_dtype != TBE_DT_BF16) return TBE_EUNSUPPORTED;
+  if (d->weights_dtype != TBE_DT_F16 && d->weights_dtype != TBE_DT_BF16 &&
+      d->weights_dtype != TBE_DT_F32)
+    return TBE_EUNSUPPORTED;
   if (d->index_dtype != TBE_DT_I32 && d->index_dtype != TBE_DT_I64) return TBE_EUNSUPPORTED;
   if (d->min_D < 8 || d->max_D > kMaxD || d->min_D > d->max_D || (d->min_D & 7) ||
       (d->max_D & 7) || d->total_D < d->max_D || (d->total_D & 7))
@@ -280,7 +282,9 @@ tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indic
   // The preprocessed path pays off when a bag holds enough lookups for its
   // hot rows to matter; shorter bags are pooled straight from the indices.
   const bool mean = (flags & TBE_F_MEAN) != 0;
-  if (pre && n >= static_cast<int64_t>(kHotFwdMinBagLen) * d->T * d->B) {
+  // fp32 weights are always pooled from the indices (no hot rows for them)
+  if (pre && n >= static_cast<int64_t>(kHotFwdMinBagLen) * d->T * d->B &&
+      d->weights_dtype != TBE_DT_F32) {
     if (mean) {
       st = from_cuda(launch_mean_factors(L, offsets, reinterpret_cast<float*>(ws + W.inv_len)));
       if (st != TBE_OK) return st;
@@ -379,6 +383,7 @@ tbe_status tbe_workspace_view(const tbe_desc* d, int64_t n, uint32_t ws_flags, v
   view->hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_next));
   view->hot_slots = kHot;
   view->long_threshold = kLongThreshold;
+  view->medium_threshold = kMediumRun;
   view->chunk = kChunk;
   return TBE_OK;
 }

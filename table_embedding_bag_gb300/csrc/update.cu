@@ -71,6 +71,7 @@ struct UpdArgs {
   float lr;
   float eps;
   bool bf16;  // weights are bf16 rather than fp16
+  bool f32;   // weights are fp32 (W then points at floats)
 };
 
 // Table metadata, in shared memory when the problem has few enough tables.
@@ -157,14 +158,18 @@ __device__ __forceinline__ void fma_rows(float (&acc)[NC][4], const float4 (&v)[
   }
 }
 
+// This lane's 16-bit weights of the row at element offset woff, fetched
+// ahead of the gradient gathers (fp32 rows are read by the update itself).
 template <int S, int NC>
-__device__ __forceinline__ void load_row(const __half* row, int nv, uint2 (&w_raw)[NC], bool active) {
+__device__ __forceinline__ void load_row(const UpdArgs& a, int64_t woff, int nv,
+                                         uint2 (&w_raw)[NC], bool active) {
   const int sl = static_cast<int>(lane_id()) % S;
+  const __half* row = a.W + woff;
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     const int vec = sl + c * S;
-    w_raw[c] = (active && vec < nv) ? *reinterpret_cast<const uint2*>(row + vec * 4)
-                                    : make_uint2(0u, 0u);
+    w_raw[c] = (active && !a.f32 && vec < nv) ? *reinterpret_cast<const uint2*>(row + vec * 4)
+                                              : make_uint2(0u, 0u);
   }
 }
 
@@ -188,6 +193,24 @@ __device__ __forceinline__ uint2 adagrad_step4(const UpdArgs& a, uint2 raw, cons
   return raw;
 }
 
+// Stores the four weights at element offset off after their step: 16-bit
+// weights from raw (see adagrad_step4); fp32 weights are read here and the
+// step w - lr * g / den is formed and stored in fp32.
+__device__ __forceinline__ void store_step4(const UpdArgs& a, int64_t off, uint2 raw,
+                                            const float (&g)[4], const float (&den)[4]) {
+  if (a.f32) {
+    float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.W) + off);
+    float4 w = *p;
+    w.x = w.x - a.lr * g[0] / den[0];
+    w.y = w.y - a.lr * g[1] / den[1];
+    w.z = w.z - a.lr * g[2] / den[2];
+    w.w = w.w - a.lr * g[3] / den[3];
+    *p = w;
+  } else {
+    *reinterpret_cast<uint2*>(a.W + off) = adagrad_step4(a, raw, g, den);
+  }
+}
+
 // Adagrad on one row with the summed gradient held by the S lanes of a group
 // (lane sl owns vectors sl + c*S).  w_raw / m_old are the row's 16-bit
 // weights (4 per vector; fp16, or bf16 when a.bf16) and row momentum, already
@@ -199,13 +222,13 @@ __device__ __forceinline__ uint2 adagrad_step4(const UpdArgs& a, uint2 raw, cons
 // element takes m_d += g_d^2 and its own denominator; m_old is unused.
 template <int S, int NC, bool kEw>
 __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4], int D,
-                                              uint32_t key, __half* row, const uint2 (&w_raw)[NC],
-                                              float m_old, bool active) {
+                                              uint32_t key, int64_t woff,
+                                              const uint2 (&w_raw)[NC], float m_old, bool active) {
   const int sl = static_cast<int>(lane_id()) % S;
   const int nv = D >> 2;
   if constexpr (kEw) {
     if (!active) return;
-    float* mrow = a.momentum + (row - a.W);
+    float* mrow = a.momentum + woff;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const int vec = sl + c * S;
@@ -217,7 +240,7 @@ __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4
         m.w = fmaf(g[c][3], g[c][3], m.w);
         const float den[4] = {sqrtf(m.x) + a.eps, sqrtf(m.y) + a.eps, sqrtf(m.z) + a.eps,
                               sqrtf(m.w) + a.eps};
-        *reinterpret_cast<uint2*>(row + vec * 4) = adagrad_step4(a, w_raw[c], g[c], den);
+        store_step4(a, woff + vec * 4, w_raw[c], g[c], den);
         *reinterpret_cast<float4*>(mrow + vec * 4) = m;
       }
     }
@@ -238,7 +261,7 @@ __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     const int vec = sl + c * S;
-    if (vec < nv) *reinterpret_cast<uint2*>(row + vec * 4) = adagrad_step4(a, w_raw[c], g[c], den);
+    if (vec < nv) store_step4(a, woff + vec * 4, w_raw[c], g[c], den);
   }
   if (sl == 0) a.momentum[key] = m_new;
 }
@@ -293,9 +316,9 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, cons
   // chunked path
   const uint32_t np = st.np >= static_cast<uint32_t>(kMediumRun) ? 0u : st.np;
   const bool active = np > 0;
-  __half* row = a.W + m.w_off[t] + (active ? (static_cast<int64_t>(key) - m.hb[t]) * D : 0);
+  const int64_t woff = m.w_off[t] + (active ? (static_cast<int64_t>(key) - m.hb[t]) * D : 0);
   uint2 w_raw[NC];
-  load_row<S, NC>(row, nv, w_raw, active);
+  load_row<S, NC>(a, woff, nv, w_raw, active);
   const float m_old = active ? a.momentum[key] : 0.f;
   const uint32_t max_np = __reduce_max_sync(kFull, np);
   float acc[NC][4];
@@ -322,7 +345,7 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, cons
       for (int uu = 0; uu < U; ++uu) fma_rows<NC>(acc, v[uu], wv[uu]);
     }
   }
-  adagrad_apply<S, NC, kEw>(a, acc, D, key, row, w_raw, m_old, active);
+  adagrad_apply<S, NC, kEw>(a, acc, D, key, woff, w_raw, m_old, active);
 }
 
 // kWide: the instantiation for rows wider than 512 values (eight vectors per
@@ -345,9 +368,9 @@ __device__ __forceinline__ void warp_run(const UpdArgs& a, const Meta& m, int t,
   const int64_t d0 = m.d_off[t];
   const int D = static_cast<int>(m.d_off[t + 1] - d0);
   const int nv = D >> 2;
-  __half* row = a.W + m.w_off[t] + (static_cast<int64_t>(key) - m.hb[t]) * D;
+  const int64_t woff = m.w_off[t] + (static_cast<int64_t>(key) - m.hb[t]) * D;
   uint2 w_raw[NC];
-  load_row<R, NC>(row, nv, w_raw, true);
+  load_row<R, NC>(a, woff, nv, w_raw, true);
   const float m_old = a.momentum[key];
   float acc[NC][4];
 #pragma unroll
@@ -383,7 +406,7 @@ __device__ __forceinline__ void warp_run(const UpdArgs& a, const Meta& m, int t,
     for (int c = 0; c < NC; ++c)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[c][i] += __shfl_xor_sync(kFull, acc[c][i], off);
-  adagrad_apply<R, NC, kEw>(a, acc, D, key, row, w_raw, m_old, g == 0);
+  adagrad_apply<R, NC, kEw>(a, acc, D, key, woff, w_raw, m_old, g == 0);
 }
 
 // Medium runs (kMediumRun <= pairs < kLongThreshold, listed by the
@@ -567,12 +590,12 @@ __device__ __forceinline__ void finish_long_row(const UpdArgs& a, const Meta& m,
                                                 const LongRunInfo& ri, float (&acc)[NC][4]) {
   const int t = static_cast<int>(ri.table);
   const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
-  __half* row = a.W + m.w_off[t] + (static_cast<int64_t>(ri.key) - m.hb[t]) * D;
+  const int64_t woff = m.w_off[t] + (static_cast<int64_t>(ri.key) - m.hb[t]) * D;
   const bool writer = static_cast<int>(lane_id()) < S;
   uint2 w_raw[NC];
-  load_row<S, NC>(row, D >> 2, w_raw, writer);
+  load_row<S, NC>(a, woff, D >> 2, w_raw, writer);
   const float m_old = a.momentum[ri.key];
-  adagrad_apply<S, NC, kEw>(a, acc, D, ri.key, row, w_raw, m_old, writer);
+  adagrad_apply<S, NC, kEw>(a, acc, D, ri.key, woff, w_raw, m_old, writer);
 }
 
 template <int S, int NC, bool kWeighted, bool kEw>
@@ -729,11 +752,11 @@ __global__ void __launch_bounds__(256)
   }
   const uint32_t key = hot_keys[blockIdx.x];
   if (key < a.hash_base[t] || key >= a.hash_base[t + 1]) return;  // not this table's row
-  __half* row = a.W + a.w_offsets[t] + (static_cast<int64_t>(key) - a.hash_base[t]) * D;
+  const int64_t woff = a.w_offsets[t] + (static_cast<int64_t>(key) - a.hash_base[t]) * D;
   uint2 w_raw[2];
-  load_row<32, 2>(row, nv, w_raw, true);
+  load_row<32, 2>(a, woff, nv, w_raw, true);
   const float m_old = a.momentum[key];
-  adagrad_apply<32, 2, kEw>(a, acc, D, key, row, w_raw, m_old, true);
+  adagrad_apply<32, 2, kEw>(a, acc, D, key, woff, w_raw, m_old, true);
 }
 
 // ------------------------------------------------------ hot set refresh
@@ -997,6 +1020,7 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   a.grad_out = grad_out;
   a.W = static_cast<__half*>(weights);  // 16-bit rows; a.bf16 picks the codec
   a.bf16 = d->weights_dtype == TBE_DT_BF16;
+  a.f32 = d->weights_dtype == TBE_DT_F32;
   a.momentum = momentum;
   a.D_offsets = d->D_offsets;
   a.hash_base = d->hash_base;

@@ -358,3 +358,86 @@ def check_selected_rows(w, sel, w0, m0, w1, m1, inputs=None):
     assert np.array_equal(w1[free].view(np.uint16), w0[free].view(np.uint16))
     assert np.array_equal(m1[free].view(np.uint32), m0[free].view(np.uint32))
     return cnt
+
+
+def assert_f32_forward_close(out, ref, abs_terms, n_max, mean=False):
+    """fp32 weights: the kernel's compensated sum is within its final
+    rounding plus (n u)^2 of the sum of |terms| of the exact sum, u = 2^-24,
+    n the bag length (Ogita, Rump and Oishi, Sum2 / Dot2); the oracle's double
+    sum, rounded once, within half an ulp.  So |out - ref| <= 1 ulp (2 with
+    the mean factor's rounding) + 2 (n u)^2 sum|terms|, which for the bags
+    here is below 1e-9 of sum|terms|: a plain fp32 accumulation, off by up to
+    about n u of it, would not pass."""
+    u = 2.0 ** -24
+    ref64 = ref.astype(np.float64)
+    ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    tol = (2 if mean else 1) * ulp + 2 * (n_max * u) ** 2 * abs_terms.astype(np.float64) + 1e-45
+    err = np.abs(out.astype(np.float64) - ref64)
+    bad = err > tol
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} fp32 forward outputs off; worst err "
+                           f"{err.max():.3e}, tol there {tol.flat[np.argmax(err - tol)]:.3e}")
+    return float(np.max(err / np.maximum(abs_terms.astype(np.float64), 1e-300)))
+
+
+def assert_f32_step_close(tab, B, indices, offsets, grad_out, psw, mean, lr, eps, w_old, m_old,
+                          w_gpu, m_gpu, w_ref, m_ref, elementwise=False):
+    """fp32 weights after one Adagrad step against the oracle's (which forms
+    the step in fp64 and rounds once).  Each element's gradient g is an fp32
+    sum of its row's n terms: within d = (2 n + 10) 2^-24 S of the exact sum,
+    S the sum of the terms' magnitudes (as in assert_elementwise_step_close).
+    The accumulator (one per row, m = m_old + mean g^2, or one per element)
+    is then off by what d moves it plus its fp32 roundings, and the step
+    lr g / (sqrt(m) + eps) by what both errors move it plus its own three
+    fp32 roundings; the weight may further differ by the rounding of the
+    subtraction and one ulp.  Untouched rows must be bit-identical.  Row-wise
+    momentum must also be within 1e-5 relative."""
+    u = 2.0 ** -24
+    ukeys, count, row, flat, col = _touched_elements(tab, B, indices, offsets)
+    keys, g = oracle.row_gradients(tab, B, indices, offsets, grad_out, psw, mean)
+    absp = None if psw is None else np.abs(psw)
+    _, S = oracle.row_gradients(tab, B, indices, offsets, np.abs(grad_out), absp, mean)
+    assert np.array_equal(keys.astype(np.int64), ukeys)
+    g = g[row, col]
+    S = S[row, col]
+    d = (2 * count[row] + 10) * u * S
+    if elementwise:
+        mr = m_ref[flat].astype(np.float64)
+        mg = m_gpu[flat].astype(np.float64)
+        dm = 4 * u * mr + (2 * np.abs(g) + d) * d
+    else:
+        Drow = np.asarray(tab.D, np.int64)[np.searchsorted(tab.hash_base, ukeys, side="right") - 1]
+        per_row = np.zeros(len(ukeys))
+        np.add.at(per_row, row, (2 * np.abs(g) + d) * d)
+        mr_row = m_ref[ukeys].astype(np.float64)
+        dm_row = 4 * u * mr_row + per_row / Drow
+        mg_row = m_gpu[ukeys].astype(np.float64)
+        assert np.all(np.abs(mg_row - mr_row) <= dm_row), "row momentum beyond the fp32 bound"
+        assert_momentum_close(m_gpu[ukeys], m_ref[ukeys])
+        mr, mg, dm = mr_row[row], mg_row[row], dm_row[row]
+    assert np.all(np.abs(mg - mr) <= dm), "momentum beyond the fp32 bound"
+    wo = np.asarray(w_old, np.float64)[flat]
+    wr = np.asarray(w_ref, np.float64)[flat]
+    wg = np.asarray(w_gpu, np.float64)[flat]
+    lo = np.sqrt(np.maximum(mr - dm, 0.0)) + eps
+    hi = np.sqrt(mr + dm) + eps
+    step = lr * np.abs(g) / lo
+    ds = lr * d / lo + lr * np.abs(g) * (1.0 / lo - 1.0 / hi) + 8 * u * step
+    spacing = lambda v: np.spacing(np.abs(v).astype(np.float32)).astype(np.float64)
+    tol = ds + 2 * u * (np.abs(wo) + step) + np.maximum(spacing(wr), spacing(wg))
+    err = np.abs(wg - wr)
+    bad = err > tol
+    assert not bad.any(), f"{bad.sum()} of {flat.size} fp32 weights beyond the fp32 bound"
+    beyond = int((err > spacing(wr)).sum())
+    mask = np.ones(np.asarray(w_gpu).size, bool)
+    mask[flat] = False
+    assert np.array_equal(np.asarray(w_gpu, np.float32).view(np.uint32)[mask],
+                          np.asarray(w_old, np.float32).view(np.uint32)[mask])
+    if elementwise:
+        assert np.array_equal(np.asarray(m_gpu).view(np.uint32)[mask],
+                              np.asarray(m_old, np.float32).view(np.uint32)[mask])
+    else:
+        free = np.ones(np.asarray(m_gpu).size, bool)
+        free[ukeys] = False
+        assert np.array_equal(np.asarray(m_gpu).view(np.uint32)[free],
+                              np.asarray(m_old, np.float32).view(np.uint32)[free])
+    print(f"fp32 step: {flat.size} touched elements, {beyond} beyond 1 ulp of the oracle")

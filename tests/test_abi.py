@@ -88,9 +88,21 @@ def test_bf16_weights_accepted_without_hot_row_buffers(lib):
     assert sbf < s16
 
 
+def test_fp32_weights_accepted_without_hot_row_buffers(lib):
+    # fp32 tables take the gather paths: no hot-row histograms are laid out
+    d16, d32 = _desc(B=4096), _desc(B=4096)
+    d32.weights_dtype = tbe.TBE_DT_F32
+    rc16, s16 = _ws_size(lib, d16, 1 << 16)
+    rc32, s32 = _ws_size(lib, d32, 1 << 16)
+    assert rc16 == rc32 == tbe.TBE_OK
+    assert s32 < s16
+
+
 def test_binding_checks_the_weight_dtype():
     with pytest.raises(ValueError):
-        tbe.TBEDesc([10], [8], 2, device="cpu", weights_dtype=torch.float32)
+        tbe.TBEDesc([10], [8], 2, device="cpu", weights_dtype=torch.float64)
+    d32 = tbe.TBEDesc([10], [8], 2, device="cpu", weights_dtype=torch.float32)
+    assert d32.c.weights_dtype == tbe.TBE_DT_F32
     desc = tbe.TBEDesc([10], [8], 2, device="cpu", weights_dtype=torch.bfloat16)
     idx = torch.zeros(3, dtype=torch.int64)
     off = torch.tensor([0, 1, 3], dtype=torch.int64)

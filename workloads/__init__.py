@@ -124,7 +124,11 @@ def zipf_cdf(E: int, alpha: float, device):
     return c.div_(c[-1].clone()).to(device)
 
 
-def _rows(spec: Spec, E: int, count: int, g, device):
+def _rows(spec: Spec, E: int, count: int, g, device, gperm=None):
+    """Rows of `count` lookups.  Zipf ranks are drawn from g and mapped
+    through a random permutation of the table's rows, drawn from gperm when
+    given (a table seed of its own, so batches with other draw seeds share
+    the table's row popularity) and else from g after the ranks."""
     if count == 0:
         return torch.zeros(0, dtype=torch.int64, device=device)
     if spec.rows == "uniform":
@@ -133,46 +137,59 @@ def _rows(spec: Spec, E: int, count: int, g, device):
     cdf = zipf_cdf(E, alpha, device)
     u = torch.rand(count, dtype=torch.float64, generator=g, device=device)
     rank = torch.searchsorted(cdf, u, right=True).clamp_(max=E - 1)
-    perm = torch.randperm(E, generator=g, device=device)
+    perm = torch.randperm(E, generator=gperm if gperm is not None else g, device=device)
     return perm[rank]
+
+
+def _lookups(spec: Spec, T: int, B: int, E, device, seed: int, table_seed: int | None):
+    """Bag lengths, rows and per-sample weights of one batch, per table."""
+    lengths, rows, psws = [], [], []
+    for t in range(T):
+        g = _gen(device, seed * 1000 + t)
+        gperm = None if table_seed is None else _gen(device, table_seed * 1000 + 500 + t)
+        L = _lengths(spec, B, g, device)
+        cnt = int(L.sum().item())
+        lengths.append(L)
+        rows.append(_rows(spec, int(E[t]), cnt, g, device, gperm))
+        if spec.weighted:
+            psws.append(torch.rand(cnt, dtype=torch.float32, generator=g, device=device))
+    return lengths, rows, psws
+
+
+def _csr(spec: Spec, T: int, B: int, lengths, rows, device):
+    L = torch.cat(lengths)
+    offsets = torch.zeros(T * B + 1, dtype=torch.int64, device=device)
+    torch.cumsum(L, 0, out=offsets[1:])
+    return torch.cat(rows).to(spec.index_dtype), offsets.to(spec.index_dtype)
 
 
 def make(name: str, device="cpu", seed: int = 0, B: int | None = None, T: int | None = None,
          E_scale: float | None = None, compact: bool = False,
-         weights_dtype: torch.dtype = torch.float16) -> Workload:
+         weights_dtype: torch.dtype = torch.float16, table_seed: int | None = None) -> Workload:
     """Draw a workload.  B, T and E_scale shrink a recipe for oracle-sized tests
     (E_scale multiplies every table's row count, keeping at least one row).
     compact=True keeps only the rows the lookups touch, renumbered per table
     in increasing order (the lookups are drawn from the full tables first), so
     that a few bags of a huge table need no huge weight array.  weights_dtype
     (torch.float16 or torch.bfloat16) is the type the N(0, 0.01^2) weight
-    draws are stored in."""
+    draws are stored in.  table_seed, when given, seeds the tables (sizes and
+    each table's row permutation) apart from the batch draws, so that
+    workloads of one table_seed and different seeds are distinct batches over
+    the same tables (see batch()); without it both come from seed."""
     spec = SPECS[name]
     T = spec.T if T is None else T
     B = spec.B if B is None else B
     device = torch.device(device)
-    E, D = _table_sizes(spec, T, seed)
+    E, D = _table_sizes(spec, T, seed if table_seed is None else table_seed)
     if E_scale is not None:
         E = np.maximum(1, np.rint(E * E_scale)).astype(np.int64)
-    lengths, rows, psws = [], [], []
-    for t in range(T):
-        g = _gen(device, seed * 1000 + t)
-        L = _lengths(spec, B, g, device)
-        cnt = int(L.sum().item())
-        lengths.append(L)
-        rows.append(_rows(spec, int(E[t]), cnt, g, device))
-        if spec.weighted:
-            psws.append(torch.rand(cnt, dtype=torch.float32, generator=g, device=device))
+    lengths, rows, psws = _lookups(spec, T, B, E, device, seed, table_seed)
     if compact:
         for t in range(T):
             uniq, inv = torch.unique(rows[t], return_inverse=True)
             rows[t] = inv
             E[t] = max(1, int(uniq.numel()))
-    L = torch.cat(lengths)
-    offsets = torch.zeros(T * B + 1, dtype=torch.int64, device=device)
-    torch.cumsum(L, 0, out=offsets[1:])
-    indices = torch.cat(rows).to(spec.index_dtype)
-    offsets = offsets.to(spec.index_dtype)
+    indices, offsets = _csr(spec, T, B, lengths, rows, device)
     psw = torch.cat(psws) if spec.weighted else None
     gw = _gen(device, seed * 1000 + 999)
     nW = int((E * D).sum())
@@ -184,7 +201,26 @@ def make(name: str, device="cpu", seed: int = 0, B: int | None = None, T: int | 
     momentum = torch.zeros(int(E.sum()), dtype=torch.float32, device=device)
     grad_out = torch.randn(B, int(D.sum()), generator=gw, device=device)
     return Workload(name, T, B, E, D, indices, offsets, psw, weights, momentum, grad_out,
-                    spec.lr, spec.eps)
+                    spec.lr, spec.eps, dict(table_seed=table_seed))
+
+
+def batch(w: Workload, seed: int) -> Workload:
+    """Another batch over the tables of w (drawn with a table_seed): new
+    bags, lookups, per-sample weights and gradients from `seed`, the same
+    tables, row popularity, weights and momentum (shared tensors, not
+    copies)."""
+    table_seed = w.extra.get("table_seed")
+    if table_seed is None:
+        raise ValueError("batch() needs a workload drawn with a table_seed")
+    spec = SPECS[w.name]
+    device = w.indices.device
+    lengths, rows, psws = _lookups(spec, w.T, w.B, w.E, device, seed, table_seed)
+    indices, offsets = _csr(spec, w.T, w.B, lengths, rows, device)
+    psw = torch.cat(psws) if spec.weighted else None
+    gw = _gen(device, seed * 1000 + 998)
+    grad_out = torch.randn(w.B, int(w.D.sum()), generator=gw, device=device)
+    return Workload(w.name, w.T, w.B, w.E, w.D, indices, offsets, psw, w.weights, w.momentum,
+                    grad_out, w.lr, w.eps, dict(w.extra))
 
 
 def from_arrays(E, D, B, indices, offsets, weights, grad_out, psw=None, momentum=None,
