@@ -133,12 +133,13 @@ typedef struct tbe_desc {
   int32_t T;                        /* number of tables, >= 1 */
   int32_t B;                        /* bags per table (batch size), >= 1 */
   int32_t weights_dtype;            /* TBE_DT_F16, TBE_DT_BF16 (accumulated in fp32
-                                       like fp16) or TBE_DT_F32 (the forward accumulates
+                                       like fp16; hot rows with bf16 tensor-core
+                                       operands) or TBE_DT_F32 (the forward accumulates
                                        each output as a compensated two-float sum: as
                                        accurate as an fp64 accumulation rounded once to
                                        fp32, see tbe_forward).  The small-table path
-                                       takes fp16 only and the hot rows fp16 only, so
-                                       other types take the gather paths there */
+                                       takes fp16 only, and fp32 tables take no hot
+                                       rows: they take the gather paths there */
   int32_t index_dtype;              /* TBE_DT_I32 or TBE_DT_I64; offsets use it too */
   const int64_t* D_offsets;         /* device [T+1]: sum of D_t' for t' < t */
   const int64_t* hash_base;         /* device [T+1]: sum of E_t' for t' < t */
@@ -196,8 +197,8 @@ tbe_status tbe_workspace_size(const tbe_desc* d, int64_t n_max, uint32_t ws_flag
  * an unevaluated sum hi + lo of two fp32 values (each addition an exact
  * two-sum, each weighted product exact through a fused multiply-add), rounded
  * once at the end; its error is the final rounding plus at most about
- * n^2 2^-48 of the sum of |terms| for a bag of n lookups, below 1e-9 of
- * it up to n = 250, as with the fp64 accumulation the pages name for fp32
+ * 4 n^2 2^-48 of the sum of |terms| for a bag of n lookups (about 1e-9 of
+ * it at n = 200), as with the fp64 accumulation the pages name for fp32
  * weights.  An empty bag yields zeros.  One table with E <= 64,
  * 64 <= D <= 128, no per-sample weights and an average bag length >= 64 takes
  * the tensor-core histogram path (counts per bag times the table) unless
@@ -208,9 +209,10 @@ tbe_status tbe_workspace_size(const tbe_desc* d, int64_t n_max, uint32_t ws_flag
  * each table's hot rows are pooled as the per-bag histogram
  * times those rows on the tensor cores (fp16 MMAs: counts up to 255 are exact
  * fp16 values, larger or weighted counts are scaled per bag and split exactly
- * into three fp16 parts, so only the fp32 accumulation rounds), the cold
- * lookups are gathered from the per-bag cold lists (bf16 problems have no
- * hot rows: every lookup is a cold one); the bounds/offsets flags are then ignored (the preprocess
+ * into three fp16 parts, so only the fp32 accumulation rounds; bf16 weights
+ * take bf16 operands the same way: counts up to 255 are exact bf16 values and
+ * three bf16 parts hold any fp32 value), the cold lookups are gathered from
+ * the per-bag cold lists; the bounds/offsets flags are then ignored (the preprocess
  * checked them) and per_sample_weights must be NULL exactly when it was NULL
  * for the preprocess.  fp32 weights are always pooled from the indices, as
  * without the flag.

@@ -153,7 +153,23 @@ __device__ __forceinline__ void stage_hot_rows(const FwdHotArgs& a, int t, int D
   }
 }
 
+// 16-bit operand values of either weight type (kBf16: bf16, else fp16): the
+// round-to-nearest conversion from fp32 and back.
+template <bool kBf16>
+__device__ __forceinline__ uint16_t to16(float v) {
+  if constexpr (kBf16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  else return __half_as_ushort(__float2half_rn(v));
+}
+template <bool kBf16>
+__device__ __forceinline__ float from16(uint16_t h) {
+  if constexpr (kBf16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  else return __half2float(__ushort_as_half(h));
+}
+
 // Wide tiles only (per-sample weights, or counts above 255 in some bag).
+// kBf16: bf16 weights, and the histogram split into bf16 parts (three 8-bit
+// significands hold any fp32 value exactly, as three fp16 parts do).
+template <bool kBf16>
 __global__ void __launch_bounds__(kFThreads, 2) forward_hot_kernel(FwdHotArgs a, uint32_t tmem_cols) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -225,20 +241,21 @@ __global__ void __launch_bounds__(kFThreads, 2) forward_hot_kernel(FwdHotArgs a,
         const int mg = cm % (kFM / 8), kg = cm / (kFM / 8);
         const float mul = pow2(tl.scale[mg * 8 + lr]);
         const float v[2] = {x[j].x * mul, x[j].y * mul};
-        __half p[3][2];
+        uint16_t p[3][2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          p[0][q] = __float2half_rn(v[q]);
-          const float r1 = v[q] - __half2float(p[0][q]);
-          p[1][q] = __float2half_rn(r1);
-          const float r2 = r1 - __half2float(p[1][q]);
-          p[2][q] = __float2half_rn(r2);
+          p[0][q] = to16<kBf16>(v[q]);
+          const float r1 = v[q] - from16<kBf16>(p[0][q]);
+          p[1][q] = to16<kBf16>(r1);
+          const float r2 = r1 - from16<kBf16>(p[1][q]);
+          p[2][q] = to16<kBf16>(r2);
           need |= (r1 != 0.f ? 1 : 0) | (r2 != 0.f ? 2 : 0);
         }
         const uint32_t off = static_cast<uint32_t>(mg * kFSBOA + kg * kFLBO) + lane * 4;
 #pragma unroll
         for (int part = 0; part < 3; ++part)
-          *reinterpret_cast<__half2*>(a_part[part] + off) = __halves2half2(p[part][0], p[part][1]);
+          *reinterpret_cast<uint32_t*>(a_part[part] + off) =
+              static_cast<uint32_t>(p[part][0]) | (static_cast<uint32_t>(p[part][1]) << 16);
       }
       // the next chunk's histogram loads overlap this chunk's MMAs
       if (c + 1 < nchunks) load_chunk(a, t, b0, nbags, nh, c + 1, warp, lr, lk, x);
@@ -249,7 +266,7 @@ __global__ void __launch_bounds__(kFThreads, 2) forward_hot_kernel(FwdHotArgs a,
       __syncthreads();
       fence_after_sync();
       if (tid == 0) {
-        const uint32_t idesc = make_idesc(kFmtF16, kFM, n_pad);
+        const uint32_t idesc = make_idesc(kBf16 ? kFmtBF16 : kFmtF16, kFM, n_pad);
         const int parts = need_lo ? 3 : (need_mid ? 2 : 1);
         for (int part = 0; part < parts; ++part) {
 #pragma unroll
@@ -354,11 +371,27 @@ __device__ __forceinline__ uint32_t bytes_to_half2(uint32_t w, uint32_t sel) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// The same for bf16: 2^23 + b is exact in fp32, minus 2^23 exactly gives b,
+// whose upper 16 bits are its bf16 value (b has at most 8 significant bits).
+__device__ __forceinline__ uint32_t bytes_to_bf162(uint32_t w, uint32_t sel) {
+  const uint32_t x = __byte_perm(w, 0u, sel);  // the two bytes in bits 0-7 and 16-23
+  const float f0 = __uint_as_float(0x4b000000u | (x & 0xffu)) - 8388608.f;
+  const float f1 = __uint_as_float(0x4b000000u | (x >> 16)) - 8388608.f;
+  return __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint32_t bytes_to_16x2(uint32_t w, uint32_t sel) {
+  if constexpr (kBf16) return bytes_to_bf162(w, sel);
+  else return bytes_to_half2(w, sel);
+}
+
 // kXpose: the epilogue goes through a per-warp shared buffer so that every
 // global store instruction writes 8 rows x 64 contiguous bytes (full
 // sectors); without it (no room for the buffer: D_t > 128) a lane stores its
 // own row.
-template <bool kXpose>
+// kBf16: bf16 weights and counts (counts up to 255 are exact bf16 values).
+template <bool kXpose, bool kBf16>
 __global__ void __launch_bounds__(kBThreads, 1)
     forward_bytes_kernel(FwdHotArgs a, uint32_t tmem_cols, int stages) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -516,14 +549,14 @@ __global__ void __launch_bounds__(kBThreads, 1)
       const int k0 = ((kq + p) & 15) * 16;
       const uint4 w = *reinterpret_cast<const uint4*>(rt + m * kHot + k0);
       uint4 h0, h1;
-      h0.x = bytes_to_half2(w.x, 0x4140u);
-      h0.y = bytes_to_half2(w.x, 0x4342u);
-      h0.z = bytes_to_half2(w.y, 0x4140u);
-      h0.w = bytes_to_half2(w.y, 0x4342u);
-      h1.x = bytes_to_half2(w.z, 0x4140u);
-      h1.y = bytes_to_half2(w.z, 0x4342u);
-      h1.z = bytes_to_half2(w.w, 0x4140u);
-      h1.w = bytes_to_half2(w.w, 0x4342u);
+      h0.x = bytes_to_16x2<kBf16>(w.x, 0x4140u);
+      h0.y = bytes_to_16x2<kBf16>(w.x, 0x4342u);
+      h0.z = bytes_to_16x2<kBf16>(w.y, 0x4140u);
+      h0.w = bytes_to_16x2<kBf16>(w.y, 0x4342u);
+      h1.x = bytes_to_16x2<kBf16>(w.z, 0x4140u);
+      h1.y = bytes_to_16x2<kBf16>(w.z, 0x4342u);
+      h1.z = bytes_to_16x2<kBf16>(w.w, 0x4140u);
+      h1.w = bytes_to_16x2<kBf16>(w.w, 0x4342u);
       unsigned char* dst = a_op + (k0 >> 6) * kAPartBytes + mg * kFSBOA + ((k0 & 63) >> 3) * kFLBO + p * 16;
       *reinterpret_cast<uint4*>(dst) = h0;
       *reinterpret_cast<uint4*>(dst + kFLBO) = h1;
@@ -534,7 +567,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     fence_after_sync();
     const uint32_t acc_col = (committed & 1u) * tmem_cols;
     if (tid == 0) {
-      const uint32_t idesc = make_idesc(kFmtF16, kFM, n_pad);
+      const uint32_t idesc = make_idesc(kBf16 ? kFmtBF16 : kFmtF16, kFM, n_pad);
       for (int c = 0; c < nchunks; ++c)
 #pragma unroll
         for (int ks = 0; ks < kFChunk / 16; ++ks)
@@ -608,19 +641,23 @@ cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, con
     while (tmem_cols < static_cast<uint32_t>(a.n_max)) tmem_cols <<= 1;
     const size_t smem = fwd_hot_smem_bytes(a.n_max);
 
-    static size_t attr_bytes[64] = {};
-    static int ctas_per_sm[64] = {};
+    const bool bf16 = d->weights_dtype == TBE_DT_BF16;
+    const int ti = bf16 ? 1 : 0;  // weight type: index of the per-type attribute caches
+    const void* hot_k = bf16 ? reinterpret_cast<const void*>(forward_hot_kernel<true>)
+                             : reinterpret_cast<const void*>(forward_hot_kernel<false>);
+    static size_t attr_bytes[64][2] = {};
+    static int ctas_per_sm[64][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (attr_bytes[dev] != smem) {
-      e = cudaFuncSetAttribute(forward_hot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (attr_bytes[dev][ti] != smem) {
+      e = cudaFuncSetAttribute(hot_k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       // all of the unified L1 / shared storage as shared memory, so that two
       // CTAs fit when the operands allow
-      e = cudaFuncSetAttribute(forward_hot_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+      e = cudaFuncSetAttribute(hot_k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
       int smem_per_sm = 0;
@@ -629,11 +666,11 @@ cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, con
       // 1 KB of each CTA's shared memory is reserved by the driver
       int per_sm = static_cast<int>(static_cast<size_t>(smem_per_sm) / (smem + 1024));
       if (per_sm > 2) per_sm = 2;
-      ctas_per_sm[dev] = per_sm < 1 ? 1 : per_sm;
-      attr_bytes[dev] = smem;
+      ctas_per_sm[dev][ti] = per_sm < 1 ? 1 : per_sm;
+      attr_bytes[dev][ti] = smem;
     }
     // resident CTAs x tensor-memory columns must fit the SM's 512
-    int per_sm = ctas_per_sm[dev];
+    int per_sm = ctas_per_sm[dev][ti];
     if (per_sm * static_cast<int>(tmem_cols) > 512) per_sm = static_cast<int>(512 / tmem_cols);
     const int64_t tiles = static_cast<int64_t>(d->T) * ((d->B + kFM - 1) / kFM);
     int64_t grid = static_cast<int64_t>(per_sm) * L.num_sms;
@@ -642,11 +679,11 @@ cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, con
 
     // byte tiles: one CTA per SM, as many ring stages as shared memory holds
     // (the transpose buffer when at least two stages fit beside it)
-    static size_t bytes_attr[64] = {};
-    static int bytes_stages[64] = {};
-    static int bytes_nmax[64] = {};
-    static bool bytes_xpose[64] = {};
-    if (bytes_nmax[dev] != a.n_max) {
+    static size_t bytes_attr[64][2] = {};
+    static int bytes_stages[64][2] = {};
+    static int bytes_nmax[64][2] = {};
+    static bool bytes_xpose[64][2] = {};
+    if (bytes_nmax[dev][ti] != a.n_max) {
       int optin = 0;
       e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
       if (e != cudaSuccess) return e;
@@ -655,28 +692,36 @@ cudaError_t launch_forward_hot(const Launch& L, const WsLayout& W, char* ws, con
       while (stages > 1 && fwd_bytes_smem_bytes(a.n_max, stages, xpose) > static_cast<size_t>(optin))
         --stages;
       const size_t bsmem = fwd_bytes_smem_bytes(a.n_max, stages, xpose);
-      e = cudaFuncSetAttribute(xpose ? forward_bytes_kernel<true> : forward_bytes_kernel<false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bsmem));
+      const void* k = xpose ? (bf16 ? reinterpret_cast<const void*>(forward_bytes_kernel<true, true>)
+                                    : reinterpret_cast<const void*>(forward_bytes_kernel<true, false>))
+                            : (bf16 ? reinterpret_cast<const void*>(forward_bytes_kernel<false, true>)
+                                    : reinterpret_cast<const void*>(forward_bytes_kernel<false, false>));
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bsmem));
       if (e != cudaSuccess) return e;
-      bytes_attr[dev] = bsmem;
-      bytes_stages[dev] = stages;
-      bytes_xpose[dev] = xpose;
-      bytes_nmax[dev] = a.n_max;
+      bytes_attr[dev][ti] = bsmem;
+      bytes_stages[dev][ti] = stages;
+      bytes_xpose[dev][ti] = xpose;
+      bytes_nmax[dev][ti] = a.n_max;
     }
     int64_t bgrid = L.num_sms < tiles ? L.num_sms : tiles;
     if (bgrid < 1) bgrid = 1;
     // both kernels together are the hot part of the forward
     probe_begin(TBE_PROBE_FORWARD_HOT, L.s);
-    if (bytes_xpose[dev])
-      forward_bytes_kernel<true><<<static_cast<unsigned>(bgrid), kBThreads, bytes_attr[dev], L.s>>>(
-          a, tmem_cols, bytes_stages[dev]);
-    else
-      forward_bytes_kernel<false><<<static_cast<unsigned>(bgrid), kBThreads, bytes_attr[dev], L.s>>>(
-          a, tmem_cols, bytes_stages[dev]);
+    const unsigned bg = static_cast<unsigned>(bgrid);
+    const size_t bs = bytes_attr[dev][ti];
+    const int st = bytes_stages[dev][ti];
+    if (bytes_xpose[dev][ti]) {
+      if (bf16) forward_bytes_kernel<true, true><<<bg, kBThreads, bs, L.s>>>(a, tmem_cols, st);
+      else forward_bytes_kernel<true, false><<<bg, kBThreads, bs, L.s>>>(a, tmem_cols, st);
+    } else {
+      if (bf16) forward_bytes_kernel<false, true><<<bg, kBThreads, bs, L.s>>>(a, tmem_cols, st);
+      else forward_bytes_kernel<false, false><<<bg, kBThreads, bs, L.s>>>(a, tmem_cols, st);
+    }
     note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    forward_hot_kernel<<<static_cast<unsigned>(grid), kFThreads, smem, L.s>>>(a, tmem_cols);
+    if (bf16) forward_hot_kernel<true><<<static_cast<unsigned>(grid), kFThreads, smem, L.s>>>(a, tmem_cols);
+    else forward_hot_kernel<false><<<static_cast<unsigned>(grid), kFThreads, smem, L.s>>>(a, tmem_cols);
     note_launch();
     probe_end(TBE_PROBE_FORWARD_HOT, L.s);
     e = cudaGetLastError();

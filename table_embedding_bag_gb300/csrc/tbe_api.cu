@@ -143,8 +143,9 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags, bool allow
   L.hot_parts = static_cast<int>(kHotCtaTarget / T > 0 ? kHotCtaTarget / T : 1);
   const int64_t max_parts = (B + kHotMinPartBags - 1) / kHotMinPartBags;
   if (L.hot_parts > max_parts) L.hot_parts = static_cast<int>(max_parts);
-  // the hot rows' tensor-core kernels take fp16 weights only
-  L.hot_enabled = allow_hot && d->weights_dtype == TBE_DT_F16 &&
+  // the hot rows' tensor-core kernels take 16-bit weights (fp16 or bf16)
+  L.hot_enabled = allow_hot &&
+                  (d->weights_dtype == TBE_DT_F16 || d->weights_dtype == TBE_DT_BF16) &&
                   static_cast<size_t>(T) * kHot * B * (sizeof(float) + 1) <= kHotBudgetBytes;
   L.hot_cnt = take(T * kHot * 4);
   L.hot_hist8 = L.hot_enabled ? take(static_cast<size_t>(T) * kHot * B) : 0;

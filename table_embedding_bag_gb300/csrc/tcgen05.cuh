@@ -31,9 +31,11 @@ __device__ __forceinline__ uint64_t make_smem_desc(const void* smem_ptr, uint32_
 }
 
 // Instruction descriptor for kind::f16 / kind::tf32: fp32 accumulator (bit 4),
-// A and B format at bits 7 and 10 (f16 = 0, tf32 = 2), both K-major,
+// A and B format at bits 7 and 10 (f16 = 0, bf16 = 1 under kind::f16; tf32 = 2
+// under kind::tf32; A and B always of one type here), both K-major,
 // N >> 3 at bit 17, M >> 4 at bit 24.
 constexpr uint32_t kFmtF16 = 0;
+constexpr uint32_t kFmtBF16 = 1;  // kind::f16 with bf16 A and B
 constexpr uint32_t kFmtTF32 = 2;
 __device__ __forceinline__ uint32_t make_idesc(uint32_t fmt, int m, int n) {
   return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(n >> 3) << 17) |

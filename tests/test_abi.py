@@ -77,15 +77,14 @@ def test_bad_descriptors_rejected(lib, field, value, code):
     assert _ws_size(lib, d, 100)[0] == code
 
 
-def test_bf16_weights_accepted_without_hot_row_buffers(lib):
-    # bf16 tables are supported; the hot rows' histograms (fp16 only) are not
-    # laid out for them, so their workspace is the smaller one
+def test_bf16_weights_take_the_same_layout_as_fp16(lib):
+    # bf16 tables have hot rows too: the same workspace as fp16 tables
     d16, dbf = _desc(B=4096), _desc(B=4096)
     dbf.weights_dtype = tbe.TBE_DT_BF16
     rc16, s16 = _ws_size(lib, d16, 1 << 16)
     rcbf, sbf = _ws_size(lib, dbf, 1 << 16)
     assert rc16 == rcbf == tbe.TBE_OK
-    assert sbf < s16
+    assert sbf == s16
 
 
 def test_fp32_weights_accepted_without_hot_row_buffers(lib):

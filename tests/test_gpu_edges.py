@@ -199,7 +199,10 @@ def test_malformed_offsets_without_repair_stay_in_bounds():
         g = W[W_off[t] + rows[:, None] * D + np.arange(D)[None, :]].reshape(len(rows), D)
         ref = oracle.pool_gathered([0, len(rows)], g)
         terms = oracle.pool_gathered([0, len(rows)], np.abs(g))
-        H.assert_forward_close(out[b:b + 1, t * D:(t + 1) * D], ref, terms)
+        # an fp32 sum of m terms is within (m - 1) 2^-24 of the sum of their
+        # magnitudes: beyond 1e-5 for these bags of up to n lookups
+        rel = max(1e-5, 1.1 * len(rows) * 2.0 ** -24)
+        H.assert_forward_close(out[b:b + 1, t * D:(t + 1) * D], ref, terms, rel=rel)
     # preprocess + preprocessed forward + backward, and the plain backward
     named = np.zeros(int(w.E.sum()), bool)
     for t in range(w.T):
