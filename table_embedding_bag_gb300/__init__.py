@@ -87,35 +87,40 @@ class tbe_ws_view(ctypes.Structure):
 _lib = None
 
 
+def configure(lib):
+    """Declare the C signatures of the entry points on a loaded libtbe (a
+    ctypes.CDLL); returns lib."""
+    P, i64, u32, f32, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint32,
+                            ctypes.c_float, ctypes.c_size_t)
+    D = ctypes.POINTER(tbe_desc)
+    lib.tbe_workspace_size.argtypes = [D, i64, u32, ctypes.POINTER(sz)]
+    lib.tbe_forward.argtypes = [D, P, P, P, i64, P, P, P, sz, P, u32]
+    lib.tbe_preprocess.argtypes = [D, P, P, i64, P, P, sz, P, u32]
+    lib.tbe_backward_rowwise_adagrad.argtypes = [D, P, P, P, i64, P, P, P, f32, f32, P, sz, P,
+                                                 u32]
+    lib.tbe_workspace_view.argtypes = [D, i64, u32, P, ctypes.POINTER(tbe_ws_view)]
+    lib.tbe_backward_rowwise_adagrad_noalloc.argtypes = [D, P, P, P, i64, P, P, P, f32, f32,
+                                                         P, u32]
+    lib.tbe_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+    lib.tbe_version.restype = ctypes.c_char_p
+    lib.tbe_kernel_launches.restype = ctypes.c_uint64
+    lib.tbe_kernel_launches.argtypes = []
+    lib.tbe_probe_set.argtypes = [u32]
+    lib.tbe_probe_read.argtypes = [ctypes.POINTER(ctypes.c_uint32),
+                                   ctypes.POINTER(ctypes.c_float)]
+    for f in ("tbe_workspace_size", "tbe_forward", "tbe_preprocess",
+              "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status",
+              "tbe_backward_rowwise_adagrad_noalloc", "tbe_probe_set", "tbe_probe_read"):
+        getattr(lib, f).restype = ctypes.c_int
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
         if not os.path.exists(lib_path):
             raise RuntimeError(f"{lib_path} is not built; run table_embedding_bag_gb300.build()")
-        lib = ctypes.CDLL(lib_path)
-        P, i64, u32, f32, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint32,
-                                ctypes.c_float, ctypes.c_size_t)
-        D = ctypes.POINTER(tbe_desc)
-        lib.tbe_workspace_size.argtypes = [D, i64, u32, ctypes.POINTER(sz)]
-        lib.tbe_forward.argtypes = [D, P, P, P, i64, P, P, P, sz, P, u32]
-        lib.tbe_preprocess.argtypes = [D, P, P, i64, P, P, sz, P, u32]
-        lib.tbe_backward_rowwise_adagrad.argtypes = [D, P, P, P, i64, P, P, P, f32, f32, P, sz, P,
-                                                     u32]
-        lib.tbe_workspace_view.argtypes = [D, i64, u32, P, ctypes.POINTER(tbe_ws_view)]
-        lib.tbe_backward_rowwise_adagrad_noalloc.argtypes = [D, P, P, P, i64, P, P, P, f32, f32,
-                                                             P, u32]
-        lib.tbe_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
-        lib.tbe_version.restype = ctypes.c_char_p
-        lib.tbe_kernel_launches.restype = ctypes.c_uint64
-        lib.tbe_kernel_launches.argtypes = []
-        lib.tbe_probe_set.argtypes = [u32]
-        lib.tbe_probe_read.argtypes = [ctypes.POINTER(ctypes.c_uint32),
-                                       ctypes.POINTER(ctypes.c_float)]
-        for f in ("tbe_workspace_size", "tbe_forward", "tbe_preprocess",
-                  "tbe_backward_rowwise_adagrad", "tbe_workspace_view", "tbe_read_status",
-                  "tbe_backward_rowwise_adagrad_noalloc", "tbe_probe_set", "tbe_probe_read"):
-            getattr(lib, f).restype = ctypes.c_int
-        _lib = lib
+        _lib = configure(ctypes.CDLL(lib_path))
     return _lib
 
 

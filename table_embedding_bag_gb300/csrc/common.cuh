@@ -35,6 +35,12 @@
 #ifndef TBE_FWD_UNROLL
 #define TBE_FWD_UNROLL 4
 #endif
+// TBE_DYNAMIC_RUNS: the short-, medium- and long-run update kernels take
+// their next task from a counter (in task order) instead of a fixed stride,
+// so that the warps in flight stay on a narrow window of runs.
+#ifndef TBE_DYNAMIC_RUNS
+#define TBE_DYNAMIC_RUNS 0
+#endif
 
 namespace tbe {
 
@@ -133,7 +139,10 @@ enum Counter : int {
   kCntPairs = 6,     // P: distinct (key, bag) pairs among the valid sorted lookups
   kCntSortN = 7,     // entries in the sort (written on the device before the sort)
   kCntMedium = 8,    // medium runs (kMediumRun <= pairs < kLongThreshold)
-  kNumCounters = 9,
+  kCntNextShort = 9,   // work cursors of the update kernels (TBE_DYNAMIC_RUNS):
+  kCntNextMedium = 10, // the next short-run task, medium run and long-run chunk
+  kCntNextLong = 11,   // to hand out
+  kNumCounters = 12,
 };
 
 struct WsLayout {

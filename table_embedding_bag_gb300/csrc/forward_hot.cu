@@ -347,6 +347,7 @@ static_assert(kHot == 256 && kBAOpBytes == 4 * kAPartBytes, "byte tiles: 256 slo
 struct FwdBytesTail {
   alignas(8) unsigned long long full[kBMaxStages];
   alignas(8) unsigned long long mma_done;
+  alignas(8) unsigned long long never;  // test-only builds: nothing arrives on it
   uint32_t tmem_base;
   int timed_out;
   int b_table;
@@ -430,6 +431,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < stages; ++i) mbar_init(&tl.full[i], 1);
     mbar_init(&tl.mma_done, 1);
+    mbar_init(&tl.never, 1);
     tl.timed_out = 0;
     tl.b_table = -1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -519,7 +521,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
     }
     const int slot = static_cast<int>(consumed % static_cast<uint32_t>(stages));
     // this tile's bytes, and the previous tile's MMAs (A and B are rewritten)
-    bool ok = mbar_wait(&tl.full[slot], (consumed / static_cast<uint32_t>(stages)) & 1u);
+    bool ok = (TBE_TEST_STUCK_WAIT > 0 && consumed == 0)
+                  ? mbar_wait(&tl.never, 0u, TBE_TEST_STUCK_WAIT)
+                  : mbar_wait(&tl.full[slot], (consumed / static_cast<uint32_t>(stages)) & 1u);
     ++consumed;
     if (committed > done) {
       const bool mma_ok = mbar_wait(&tl.mma_done, done & 1u);

@@ -20,8 +20,12 @@
 // counts of 2^11 and up).  The next stage's loads are issued before waiting
 // for the current stage's MMAs.  The dropped lo*lo term and the MMA's
 // truncation of the remainders leave a relative error of about 2^-21 per
-// product, below fp32 accumulation error over a bag partition.  The
-// accumulator goes to hot_part[t][p][slot][c]; the finishing kernel sums the
+// product, below fp32 accumulation error over a bag partition.  The tensor
+// core's accumulation into tensor memory does not round to nearest, and its
+// error grows with the number of MMAs summed into one accumulator (hundreds
+// over a long partition); so every kHotFlushStages stages the accumulator is
+// added (fp32, round to nearest) into the partition's partial sums in
+// hot_part[t][p][slot][c] and restarted.  The finishing kernel sums the
 // partitions in order.  Every mbarrier wait is bounded (time-out:
 // TBE_ERR_TIMEOUT in the status word, drain, free).
 #include "common.cuh"
@@ -41,6 +45,36 @@ constexpr int kGATileBytes = kGM * kGStage * 4;  // 16 KB
 constexpr int kGBBytes = kHot * kGStage * 4;     // 32 KB for 256 slots
 constexpr int kGAItems = kGM * kGStage / kGThreads;    // 16 per M tile
 constexpr int kGBItems = kHot * kGStage / kGThreads;   // up to 32
+// Stages summed into the tensor-memory accumulator between two flushes into
+// the partials (at most 8 x 4 x 3 MMAs of 8 products each).
+#ifndef TBE_HOT_FLUSH_STAGES
+#define TBE_HOT_FLUSH_STAGES 8
+#endif
+constexpr int kHotFlushStages = TBE_HOT_FLUSH_STAGES;
+
+// The accumulator D^T[c][slot] of this CTA stored (add: added) into
+// hot_part[t][p][slot][c]: warp w reads TMEM lanes 32 (w % 4) .. + 31
+// (columns) of M tile w / 4, the slots in blocks of 32.  The caller orders
+// the MMAs before and after it.
+__device__ __forceinline__ void flush_partials(uint32_t tmem, float* dst, int mtiles, int D,
+                                               int nh, int n_slots, bool add) {
+  const int warp = threadIdx.x >> 5;
+  const int q = warp & 3;
+  const int mt = warp >> 2;
+  if (mt >= mtiles) return;
+  const int c = mt * 128 + q * 32 + static_cast<int>(lane_id());
+  for (int s0 = 0; s0 < n_slots; s0 += 32) {
+    float v[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 256 + s0), v);
+    if (c < D)
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (s0 + j < nh) {
+          float* o = dst + (s0 + j) * kHotMaxD + c;
+          *o = add ? *o + v[j] : v[j];
+        }
+  }
+}
 
 static_assert(kHot % 16 == 0 && kHot <= 256, "MMA N");
 static_assert(kGStage / 4 == kGWarps, "B items: the k group of core matrix warp + 8 j is the warp");
@@ -215,6 +249,9 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_tc_kernel(HotGradArgs a
     load_stage<kMixed>(a, t, d0, D, mtiles, nh, n_slots, b_begin,
                static_cast<int>(b_end - b_begin < kGStage ? b_end - b_begin : kGStage),
                kind_at(b_begin) == kTileBytes, warp, lr, lk, r);
+  float* dst = a.hot_part + (static_cast<int64_t>(t) * a.parts + p) * kHot * kHotMaxD;
+  int flushed = 0;  // flushes of the accumulator into dst so far
+  int in_acc = 0;   // stages summed in the accumulator since the last flush
   for (int64_t c0 = b_begin; c0 < b_end; c0 += kGStage) {
     // stage the loaded values: core matrix cm sits at (cm % groups) * SBO +
     // (cm / groups) * LBO; inside it element (row % 8, k % 4) is at 4 lane
@@ -293,32 +330,23 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_tc_kernel(HotGradArgs a
     fence_after_sync();
     __syncthreads();
     if (tl.timed_out) break;
+    if (++in_acc == kHotFlushStages && c0 + kGStage < b_end) {
+      // into the partials; the next stage restarts the accumulator
+      flush_partials(tmem, dst, mtiles, D, nh, n_slots, flushed > 0);
+      ++flushed;
+      in_acc = 0;
+      first = true;
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+    }
   }
 
-  float* dst = a.hot_part + (static_cast<int64_t>(t) * a.parts + p) * kHot * kHotMaxD;
-  if (!tl.timed_out && first) {
+  if (!tl.timed_out && first && flushed == 0) {
     // no bags in this partition: its partial sums are zero
     for (int i = tid; i < nh * kHotMaxD; i += kGThreads) dst[i] = 0.f;
   }
-  if (!tl.timed_out && !first) {
-    // D^T[c][slot] -> hot_part[t][p][slot][c]: warp w reads TMEM lanes
-    // 32 (w % 4) .. + 31 (columns) of M tile w / 4, the slots in blocks of 32
-    const int q = warp & 3;
-    const int mt = warp >> 2;
-    if (mt < mtiles) {
-      const int c = mt * kGM + q * 32 + static_cast<int>(lane);
-      for (int s0 = 0; s0 < n_slots; s0 += 32) {
-        float v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                      static_cast<uint32_t>(mt * 256 + s0),
-                  v);
-        if (c < D)
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (s0 + j < nh) dst[(s0 + j) * kHotMaxD + c] = v[j];
-      }
-    }
-  }
+  if (!tl.timed_out && !first) flush_partials(tmem, dst, mtiles, D, nh, n_slots, flushed > 0);
   if (tl.timed_out) {
     if (tid == 0) {
       atomicOr(a.error_word, TBE_ERR_TIMEOUT);
@@ -421,6 +449,7 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_bytes_kernel(HotGradArg
   if (warp == 0)
     for (int i = 0; i < kGRing && i < nstages; ++i) issue(i);
 
+  float* dst = a.hot_part + (static_cast<int64_t>(t) * a.parts + p) * kHot * kHotMaxD;
   int consumed = 0, committed = 0, done = 0;
   for (int i = 0; i < nstages; ++i) {
     const int slot = i % kGRing;
@@ -494,7 +523,8 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_bytes_kernel(HotGradArg
         for (int ks = 0; ks < kGStage / 8; ++ks) {
           const uint32_t off = ks * 2 * kGLBO;
           mma_tf32(acc_tmem, make_smem_desc(a_hi[mt] + off, kGLBO, kGSBO),
-                   make_smem_desc(b_op + off, kGLBO, kGSBO), idesc, (i | ks) != 0 ? 1u : 0u);
+                   make_smem_desc(b_op + off, kGLBO, kGSBO), idesc,
+                   ((i % kHotFlushStages) | ks) != 0 ? 1u : 0u);
           mma_tf32(acc_tmem, make_smem_desc(a_lo[mt] + off, kGLBO, kGSBO),
                    make_smem_desc(b_op + off, kGLBO, kGSBO), idesc, 1u);
         }
@@ -507,6 +537,19 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_bytes_kernel(HotGradArg
       fence_proxy_async();
       issue(i + kGRing);
     }
+    if ((i + 1) % kHotFlushStages == 0 && i + 1 < nstages) {
+      // into the partials; stage i + 1 restarts the accumulator
+      const bool ok = mbar_wait(&tl.mma_done, static_cast<uint32_t>(done) & 1u);
+      if (ok) ++done;
+      fence_after_sync();
+      if (!ok) atomicOr(&tl.timed_out, 1);
+      __syncthreads();
+      if (tl.timed_out) break;
+      flush_partials(tmem, dst, mtiles, D, nh, n_slots, (i + 1) > kHotFlushStages);
+      fence_before_sync();
+      __syncthreads();
+      fence_after_sync();
+    }
   }
   if (!tl.timed_out && committed > done) {
     const bool ok = mbar_wait(&tl.mma_done, static_cast<uint32_t>(done) & 1u);
@@ -515,22 +558,8 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_bytes_kernel(HotGradArg
     if (!ok) atomicOr(&tl.timed_out, 1);
   }
   __syncthreads();
-  float* dst = a.hot_part + (static_cast<int64_t>(t) * a.parts + p) * kHot * kHotMaxD;
   if (!tl.timed_out) {
-    // D^T[c][slot] -> hot_part[t][p][slot][c], as in the register-staged kernel
-    const int q = warp & 3;
-    const int mt = warp >> 2;
-    if (mt < mtiles) {
-      const int c = mt * kGM + q * 32 + static_cast<int>(lane);
-      for (int s0 = 0; s0 < n_slots; s0 += 32) {
-        float v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 256 + s0), v);
-        if (c < D)
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (s0 + j < nh) dst[(s0 + j) * kHotMaxD + c] = v[j];
-      }
-    }
+    flush_partials(tmem, dst, mtiles, D, nh, n_slots, nstages > kHotFlushStages);
   } else if (tid == 0) {
     atomicOr(a.error_word, TBE_ERR_TIMEOUT);
     // drain (bounded): committed MMAs, issued copies (the stage that timed

@@ -58,14 +58,25 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
   return ok != 0;
 }
 
-// Bounded wait; false if the phase did not complete within the limit.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+// Bounded wait; false if the phase did not complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity,
+                                          uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (i > 64) __nanosleep(64);
   }
   return false;
 }
+
+// Test-only builds (-DTBE_TEST_STUCK_WAIT=polls): forward_bytes_kernel's
+// first ring wait is made on an mbarrier that nothing arrives on, bounded by
+// that many polls, so that it always runs out and the time-out path (status
+// bit, drain of the copies in flight under the normal bound, tensor memory
+// freed) runs without any fault or hang.  0 (every regular build): no such
+// wait.
+#ifndef TBE_TEST_STUCK_WAIT
+#define TBE_TEST_STUCK_WAIT 0
+#endif
 
 // Arms the barrier's current phase for `bytes` of asynchronous copies (one
 // arrival, by the thread that issues them).

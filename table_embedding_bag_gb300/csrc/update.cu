@@ -62,6 +62,7 @@ struct UpdArgs {
   const LongRunInfo* long_info;
   const ChunkDesc* chunk_order;
   uint32_t* tree_cnt;
+  uint32_t* cursors;  // counters + kCntNextShort: the update kernels' work cursors
   float* partials;
   float* tree_part;
   int64_t total_D;
@@ -105,6 +106,14 @@ __device__ __forceinline__ Meta load_meta(const UpdArgs& a, MetaSmem& sm, bool w
   }
   __syncthreads();
   return Meta{sm.d_off, sm.hb, sm.w_off, sm.tasks, sm.runs};
+}
+
+// The next work item of a warp from cursor `c` (TBE_DYNAMIC_RUNS): one
+// atomic by lane 0, broadcast.
+__device__ __forceinline__ uint32_t grab(uint32_t* c) {
+  uint32_t v = 0;
+  if (lane_id() == 0) v = atomicAdd(c, 1u);
+  return __shfl_sync(kFull, v, 0);
 }
 
 // Largest t with first[t] <= x (first has T+1 ascending entries).
@@ -419,8 +428,13 @@ __global__ void __launch_bounds__(256, kNarrow ? 3 : 2)
   __shared__ MetaSmem msm;
   const Meta m = load_meta(a, msm, true);
   const uint32_t nmed = a.counters[kCntMedium];
+#if TBE_DYNAMIC_RUNS
+  uint32_t* cur = a.cursors + (kCntNextMedium - kCntNextShort);
+  for (uint32_t i = grab(cur); i < nmed; i = grab(cur)) {
+#else
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   for (uint32_t i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < nmed; i += warps) {
+#endif
     const uint32_t j = __ldg(medium_run + i);
     const uint32_t key = __ldg(a.unique_keys + j);
     const uint32_t p0 = __ldg(a.run_pairs + j);
@@ -449,11 +463,20 @@ __global__ void __launch_bounds__(256, TBE_SHORT_MINB) short_runs_kernel(UpdArgs
   __shared__ MetaSmem msm;
   const Meta m = load_meta(a, msm, true);
   const uint32_t ntasks = a.counters[kCntTasks];
+#if TBE_DYNAMIC_RUNS
+  uint32_t task = grab(a.cursors);
+  ShortTask cur = fetch_task(a, m, task, ntasks);
+  while (task < ntasks) {
+    const uint32_t task_next = grab(a.cursors);
+    const ShortTask next = fetch_task(a, m, task_next, ntasks);  // one task ahead
+    task = task_next;
+#else
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   uint32_t task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   ShortTask cur = fetch_task(a, m, task, ntasks);
   for (; task < ntasks; task += warps) {
     const ShortTask next = fetch_task(a, m, task + warps, ntasks);  // one task ahead
+#endif
     const int nv = cur.nv;
     if (cur.t >= 0 && (nv > 128) == kWide) {
       if (kWide) short_task<32, 8, kWeighted, kEw>(a, m, cur);
@@ -644,8 +667,13 @@ __global__ void __launch_bounds__(256, TBE_LONG_MINB) long_chunks_kernel(UpdArgs
   __shared__ MetaSmem msm;
   const Meta m = load_meta(a, msm, false);
   const uint32_t nchunks = a.counters[kCntChunks];
+#if TBE_DYNAMIC_RUNS
+  uint32_t* cur = a.cursors + (kCntNextLong - kCntNextShort);
+  for (uint32_t qi = grab(cur); qi < nchunks; qi = grab(cur)) {
+#else
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   for (uint32_t qi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; qi < nchunks; qi += warps) {
+#endif
     const ChunkDesc cd = a.chunk_order[qi];
     const LongRunInfo ri = a.long_info[cd.run];
     const int t = static_cast<int>(ri.table);
@@ -997,10 +1025,17 @@ void launch_runs(const Launch& L, const UpdArgs& a, const uint32_t* medium, unsi
     note_launch();
     probe_end(TBE_PROBE_MEDIUM_RUNS, L.s);
   }
+  // a second launch of a kernel with a work cursor (rows wider than 512
+  // values) starts its cursor afresh
+  auto reset = [&](int c) {
+    if (TBE_DYNAMIC_RUNS && wide) cudaMemsetAsync(a.cursors + (c - kCntNextShort), 0, 4, L.s);
+  };
+  reset(kCntNextShort);
   if (wide && weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, true, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   if (wide && !weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, true, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   if (weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, false, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
   else { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, false, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  reset(kCntNextLong);
   if (wide && weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, true, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
   if (wide && !weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, true, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
   if (two_launch) {
@@ -1036,6 +1071,7 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   a.long_info = reinterpret_cast<const LongRunInfo*>(ws + W.long_info);
   a.chunk_order = reinterpret_cast<const ChunkDesc*>(ws + W.chunk_order);
   a.tree_cnt = reinterpret_cast<uint32_t*>(ws + W.tree_cnt);
+  a.cursors = reinterpret_cast<uint32_t*>(ws + W.counts) + kCntNextShort;
   a.partials = reinterpret_cast<float*>(ws + W.partials);
   a.tree_part = reinterpret_cast<float*>(ws + W.tree_part);
   a.total_D = d->total_D;
@@ -1077,9 +1113,11 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
     e = cudaEventRecord(sf->done, Ls.s);
     if (e != cudaSuccess) return e;
   }
-  // the cold rows need the sort chain
+  // the cold rows need the sort chain; their work cursors start at zero
   {
     cudaError_t e = cudaStreamWaitEvent(L.s, sf->sorted, 0);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(a.cursors, 0, 3 * sizeof(uint32_t), L.s);
     if (e != cudaSuccess) return e;
   }
   const uint32_t* medium = reinterpret_cast<const uint32_t*>(ws + W.medium_run);

@@ -92,9 +92,11 @@ def test_elementwise_hot_rows(case):
     assert sum(len(h) for h in run.hot_set()) > 0
     run.reset_state()
     tbe.tbe_preprocess(run.desc, run.indices, run.offsets, run.psw, run.ws)
-    # the hot rows' tensor-core gradient rounds each product to about 2^-21,
-    # so more of their accumulators leave the 1e-5 band (the bound still holds)
-    check(run, w, tbe.TBE_F_PREPROCESSED, max_loose=1e-2)
+    # the hot rows' tensor-core gradient is held to the same allowance as the
+    # cold rows' fp32 sums: its accumulator is flushed into fp32 partials
+    # every few stages, so the tensor core's own accumulation error stays
+    # within that of an fp32 sum
+    check(run, w, tbe.TBE_F_PREPROCESSED, max_loose=1e-3)
 
 
 def test_elementwise_with_mean_pooling():
