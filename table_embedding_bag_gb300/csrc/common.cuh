@@ -39,7 +39,7 @@
 // their next task from a counter (in task order) instead of a fixed stride,
 // so that the warps in flight stay on a narrow window of runs.
 #ifndef TBE_DYNAMIC_RUNS
-#define TBE_DYNAMIC_RUNS 0
+#define TBE_DYNAMIC_RUNS 1
 #endif
 
 namespace tbe {
@@ -88,7 +88,12 @@ constexpr uint8_t kTileWide = 1;
 constexpr uint8_t kTileNoHot = 2;
 constexpr int kHotMaxD = 256;
 constexpr size_t kHotBudgetBytes = size_t(2) << 30;
-constexpr int kHotCtaTarget = 304;  // CTAs of the hot-gradient kernel: one wave at 2 per SM on 152 SMs
+// CTAs of the hot-gradient kernels (bag partitions over all tables): one
+// wave at 2 per SM on 152 SMs
+#ifndef TBE_HOT_CTA_TARGET
+#define TBE_HOT_CTA_TARGET 304
+#endif
+constexpr int kHotCtaTarget = TBE_HOT_CTA_TARGET;
 constexpr int kHotMinPartBags = 256;  // fewest bags per hot-gradient CTA
 constexpr int kHotFwdMinBagLen = 64;  // preprocessed forward: mean lookups per bag to use it
 constexpr int kHotBuckets = 256;    // log-scale buckets of lookup counts (8 per octave)

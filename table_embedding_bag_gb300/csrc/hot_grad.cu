@@ -53,17 +53,23 @@ constexpr int kGBItems = kHot * kGStage / kGThreads;   // up to 32
 constexpr int kHotFlushStages = TBE_HOT_FLUSH_STAGES;
 
 // The accumulator D^T[c][slot] of this CTA stored (add: added) into
-// hot_part[t][p][slot][c]: warp w reads TMEM lanes 32 (w % 4) .. + 31
-// (columns) of M tile w / 4, the slots in blocks of 32.  The caller orders
-// the MMAs before and after it.
+// hot_part[t][p][slot][c].  Warps w and w + 4 read TMEM lanes 32 (w % 4) ..
+// + 31 (columns): with two M tiles warp w takes tile w / 4, with one the two
+// warps share the slot blocks of 32.  Additions are reductions at L2
+// (red.global.add.f32: fire and forget, rounded to nearest); each element is
+// written by one thread, so a CTA's flushes reach it in program order and
+// the result does not depend on timing.  The caller orders the MMAs before
+// and after it.
 __device__ __forceinline__ void flush_partials(uint32_t tmem, float* dst, int mtiles, int D,
                                                int nh, int n_slots, bool add) {
   const int warp = threadIdx.x >> 5;
   const int q = warp & 3;
-  const int mt = warp >> 2;
-  if (mt >= mtiles) return;
+  const int half = warp >> 2;
+  const int mt = mtiles == 2 ? half : 0;
+  const int s_first = mtiles == 2 ? 0 : 32 * half;
+  const int s_step = mtiles == 2 ? 32 : 64;
   const int c = mt * 128 + q * 32 + static_cast<int>(lane_id());
-  for (int s0 = 0; s0 < n_slots; s0 += 32) {
+  for (int s0 = s_first; s0 < n_slots; s0 += s_step) {
     float v[32];
     tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 256 + s0), v);
     if (c < D)
@@ -71,13 +77,11 @@ __device__ __forceinline__ void flush_partials(uint32_t tmem, float* dst, int mt
       for (int j = 0; j < 32; ++j)
         if (s0 + j < nh) {
           float* o = dst + (s0 + j) * kHotMaxD + c;
-          *o = add ? *o + v[j] : v[j];
+          if (add) atomicAdd(o, v[j]);
+          else *o = v[j];
         }
   }
 }
-
-static_assert(kHot % 16 == 0 && kHot <= 256, "MMA N");
-static_assert(kGStage / 4 == kGWarps, "B items: the k group of core matrix warp + 8 j is the warp");
 
 __device__ __forceinline__ void split_tf32(float v, float* hi, float* lo) {
   *hi = __uint_as_float(__float_as_uint(v) & 0xffffe000u);

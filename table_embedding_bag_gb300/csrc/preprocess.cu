@@ -939,15 +939,29 @@ __global__ void __launch_bounds__(1024)
 // kLongThreshold pairs) compacted into lists on the device, each long run
 // with a contiguous range of chunk slots and of tree nodes.  Each block takes
 // a contiguous range of runs in passes of 256; a pass places its runs by
-// block scans and takes its list ranges with one atomic per counter (the
-// lists' order across blocks is arbitrary; every run is independent).
+// block scans.  kMode 0: each pass takes its list ranges with one atomic per
+// counter (the lists' order across blocks is arbitrary).  With
+// TBE_ORDERED_CLASSIFY the lists follow the run order (table-major, so the
+// medium-run kernel works through one table's gradient rows at a time):
+// kMode 1 only counts each block's medium runs, long runs, chunks and tree
+// nodes into blk[4][grid], an exclusive scan of each turns them into the
+// blocks' list bases, and kMode 2 writes the lists from those bases.
+#ifndef TBE_ORDERED_CLASSIFY
+#define TBE_ORDERED_CLASSIFY 0
+#endif
+template <int kMode>
 __global__ void __launch_bounds__(256)
     classify_kernel(const uint32_t* __restrict__ run_pairs, uint32_t* __restrict__ counters,
                     uint32_t* __restrict__ long_run, uint32_t* __restrict__ long_chunk0,
-                    uint32_t* __restrict__ long_tree0, uint32_t* __restrict__ medium_run) {
+                    uint32_t* __restrict__ long_tree0, uint32_t* __restrict__ medium_run,
+                    uint32_t* __restrict__ blk) {
   __shared__ uint32_t sm32[33];
   __shared__ unsigned long long sm64[33];
   __shared__ uint32_t base[4];
+  __shared__ uint32_t run_base[4];  // kMode 1: the block's totals; 2: its next list slots
+  if (threadIdx.x < 4)
+    run_base[threadIdx.x] = kMode == 2 ? blk[threadIdx.x * gridDim.x + blockIdx.x] : 0u;
+  __syncthreads();
   const uint32_t R = counters[kCntRuns];
   const uint32_t per_block = ((R + gridDim.x - 1) / gridDim.x + 255u) & ~255u;
   const uint32_t j0 = blockIdx.x * per_block;
@@ -968,14 +982,22 @@ __global__ void __launch_bounds__(256)
     unsigned long long ctot;
     const unsigned long long cex = block_inclusive_scan(c, OpSum(), 0ull, sm64, &ctot) - c;
     if (threadIdx.x == 0) {
-      base[0] = (ftot & 0xffffu) ? atomicAdd(&counters[kCntMedium], ftot & 0xffffu) : 0u;
-      base[1] = (ftot >> 16) ? atomicAdd(&counters[kCntLong], ftot >> 16) : 0u;
-      base[2] = static_cast<uint32_t>(ctot)
-                    ? atomicAdd(&counters[kCntChunks], static_cast<uint32_t>(ctot)) : 0u;
-      base[3] = static_cast<uint32_t>(ctot >> 32)
-                    ? atomicAdd(&counters[kCntTree], static_cast<uint32_t>(ctot >> 32)) : 0u;
+      const uint32_t tot[4] = {ftot & 0xffffu, ftot >> 16, static_cast<uint32_t>(ctot),
+                               static_cast<uint32_t>(ctot >> 32)};
+      if (kMode == 0) {
+        base[0] = tot[0] ? atomicAdd(&counters[kCntMedium], tot[0]) : 0u;
+        base[1] = tot[1] ? atomicAdd(&counters[kCntLong], tot[1]) : 0u;
+        base[2] = tot[2] ? atomicAdd(&counters[kCntChunks], tot[2]) : 0u;
+        base[3] = tot[3] ? atomicAdd(&counters[kCntTree], tot[3]) : 0u;
+      } else {
+        for (int k = 0; k < 4; ++k) {
+          base[k] = run_base[k];
+          run_base[k] += tot[k];
+        }
+      }
     }
     __syncthreads();
+    if (kMode == 1) continue;  // uniform; the next pass's barriers follow
     if (medium) medium_run[base[0] + (fex & 0xffffu)] = j;
     if (lng) {
       const uint32_t slot = base[1] + (fex >> 16);
@@ -985,6 +1007,7 @@ __global__ void __launch_bounds__(256)
     }
     __syncthreads();  // base is rewritten by the next pass
   }
+  if (kMode == 1 && threadIdx.x < 4) blk[threadIdx.x * gridDim.x + blockIdx.x] = run_base[threadIdx.x];
 }
 
 // One warp per long run: its info record, the descriptors of its chunks, and
@@ -1046,14 +1069,27 @@ __global__ void __launch_bounds__(256)
 
 // Processing order of the long-run chunks: binned by the first bag each
 // chunk gathers (counting sort over bag bands; order within a band is free).
+// With TBE_TABLE_BANDS the bins are (table, band) in table-major order,
+// bands_per_table bins per table: the chunks in flight then gather from one
+// table's gradient rows at a time instead of every table's.
+#ifndef TBE_TABLE_BANDS
+#define TBE_TABLE_BANDS 0
+#endif
 __global__ void __launch_bounds__(256)
     chunk_band_count_kernel(const uint32_t* __restrict__ counters,
                             const ChunkDesc* __restrict__ chunk_desc,
+                            const LongRunInfo* __restrict__ info,
                             const uint32_t* __restrict__ pair_bags, int band_shift,
+                            int bands_per_table,
                             uint32_t* __restrict__ chunk_band, uint32_t* __restrict__ band_count) {
   const uint32_t nchunks = counters[kCntChunks];
   for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < nchunks; q += gridDim.x * blockDim.x) {
-    uint32_t band = pair_bags[chunk_desc[q].first] >> band_shift;
+    const ChunkDesc cd = chunk_desc[q];
+    uint32_t band = pair_bags[cd.first] >> band_shift;
+    if (TBE_TABLE_BANDS) {
+      const uint32_t bpt = static_cast<uint32_t>(bands_per_table);
+      band = info[cd.run].table * bpt + (band < bpt ? band : bpt - 1);
+    }
     band = band < kBagBands ? band : kBagBands - 1;
     chunk_band[q] = band;
     atomicAdd(&band_count[band], 1u);
@@ -1223,11 +1259,30 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
   if (n > 0) {
     int64_t blocks = (n + 255) / 256;
     if (blocks > 8LL * L.num_sms) blocks = 8LL * L.num_sms;
-    { classify_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        reinterpret_cast<uint32_t*>(ws + W.run_pairs), counters, reinterpret_cast<uint32_t*>(ws + W.long_run),
-        reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
-        reinterpret_cast<uint32_t*>(ws + W.long_tree0),
-        reinterpret_cast<uint32_t*>(ws + W.medium_run)); note_launch(); }
+    uint32_t* cl_args[5] = {reinterpret_cast<uint32_t*>(ws + W.long_run),
+                            reinterpret_cast<uint32_t*>(ws + W.long_chunk0),
+                            reinterpret_cast<uint32_t*>(ws + W.long_tree0),
+                            reinterpret_cast<uint32_t*>(ws + W.medium_run),
+                            reinterpret_cast<uint32_t*>(ws + W.radix_counts)};  // sort done: free
+    const uint32_t* rp = reinterpret_cast<uint32_t*>(ws + W.run_pairs);
+    const unsigned cb0 = static_cast<unsigned>(blocks);
+    if (TBE_ORDERED_CLASSIFY) {
+      classify_kernel<1><<<cb0, 256, 0, s>>>(rp, counters, cl_args[0], cl_args[1], cl_args[2],
+                                              cl_args[3], cl_args[4]);
+      note_launch();
+      const int dest[4] = {kCntMedium, kCntLong, kCntChunks, kCntTree};
+      for (int k = 0; k < 4; ++k) {
+        exclusive_scan_kernel<<<1, 1024, 0, s>>>(cl_args[4] + k * cb0, cb0, counters + dest[k]);
+        note_launch();
+      }
+      classify_kernel<2><<<cb0, 256, 0, s>>>(rp, counters, cl_args[0], cl_args[1], cl_args[2],
+                                              cl_args[3], cl_args[4]);
+      note_launch();
+    } else {
+      classify_kernel<0><<<cb0, 256, 0, s>>>(rp, counters, cl_args[0], cl_args[1], cl_args[2],
+                                              cl_args[3], cl_args[4]);
+      note_launch();
+    }
     int64_t fb = (W.max_long * 32 + 255) / 256;
     if (fb > 8LL * L.num_sms) fb = 8LL * L.num_sms;
     if (fb < 1) fb = 1;
@@ -1239,8 +1294,10 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
         reinterpret_cast<LongRunInfo*>(ws + W.long_info),
         reinterpret_cast<ChunkDesc*>(ws + W.chunk_desc),
         reinterpret_cast<uint32_t*>(ws + W.tree_cnt)); note_launch(); }
+    const int bands_per_table =
+        TBE_TABLE_BANDS ? (d->T < kBagBands ? kBagBands / d->T : 1) : kBagBands;
     int band_shift = 0;
-    while ((static_cast<int64_t>(d->B - 1) >> band_shift) >= kBagBands) ++band_shift;
+    while ((static_cast<int64_t>(d->B - 1) >> band_shift) >= bands_per_table) ++band_shift;
     uint32_t* band_count = reinterpret_cast<uint32_t*>(ws + W.band_count);
     err = cudaMemsetAsync(band_count, 0, kBagBands * sizeof(uint32_t), s);
     if (err != cudaSuccess) return err;
@@ -1249,7 +1306,8 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     if (cb < 1) cb = 1;
     { chunk_band_count_kernel<<<static_cast<unsigned>(cb), 256, 0, s>>>(
         counters, reinterpret_cast<ChunkDesc*>(ws + W.chunk_desc),
-        reinterpret_cast<uint32_t*>(ws + W.pair_bags), band_shift,
+        reinterpret_cast<const LongRunInfo*>(ws + W.long_info),
+        reinterpret_cast<uint32_t*>(ws + W.pair_bags), band_shift, bands_per_table,
         reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count); note_launch(); }
     { exclusive_scan_kernel<<<1, 1024, 0, s>>>(band_count, kBagBands, nullptr); note_launch(); }
     { chunk_band_scatter_kernel<<<static_cast<unsigned>(cb), 256, 0, s>>>(
