@@ -67,7 +67,7 @@ def parse():
     p.add_argument("--no-configs", action="store_true")
     p.add_argument("--pooling", choices=["sum", "mean"], default="sum",
                    help="pooling mode of the step (the recorded workload is sum)")
-    p.add_argument("--weights", choices=["fp16", "bf16"], default="fp16",
+    p.add_argument("--weights", choices=["fp16", "bf16", "fp32"], default="fp16",
                    help="weight type (the recorded workload is fp16)")
     p.add_argument("--optimizer", choices=["rowwise", "elementwise"], default="rowwise",
                    help="Adagrad form (the recorded workload is row-wise)")
@@ -212,13 +212,13 @@ def momentum_bytes(D, elementwise):
     return 8 * D if elementwise else 8
 
 
-def short_run_bytes(D, pairs, runs, all_runs, elementwise=False):
+def short_run_bytes(D, pairs, runs, all_runs, elementwise=False, wb=2):
     """Algorithmic bytes of one short_runs_kernel launch, counted per use: per
     short-run pair its bag (4), pair start (8) and gradient row (4 D); per
-    short run the weights row read and written (2 x 2 D) and the momentum (8,
-    or 8 D element-wise); per run of the batch its run data (8: the kernel
-    walks every run to pick the short ones)."""
-    return (pairs * (4 + 8 + 4 * D) + runs * (2 * 2 * D + momentum_bytes(D, elementwise))
+    short run the weights row read and written (2 x wb D, wb bytes per
+    weight) and the momentum (8, or 8 D element-wise); per run of the batch
+    its run data (8: the kernel walks every run to pick the short ones)."""
+    return (pairs * (4 + 8 + 4 * D) + runs * (2 * wb * D + momentum_bytes(D, elementwise))
             + all_runs * 8)
 
 
@@ -231,7 +231,7 @@ def compulsory_bytes(w, rows_touched, index_bytes, elementwise=False):
     nb = w.T * w.B
     idx = w.n * index_bytes + (nb + 1) * index_bytes + (4 * w.n if w.psw is not None else 0)
     dense = w.B * int(w.D.sum()) * 4
-    rows_w = sum(int(r) * int(d) * 2 for r, d in zip(rows_touched, w.D))
+    rows_w = sum(int(r) * int(d) * w.weights.element_size() for r, d in zip(rows_touched, w.D))
     rows_m = sum(int(r) * momentum_bytes(int(d), elementwise) for r, d in zip(rows_touched, w.D))
     return {"forward": idx + rows_w + dense,
             "backward": idx + dense + 2 * rows_w + rows_m,
@@ -439,7 +439,7 @@ def run_native(args, world, rank, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     import workloads
     E_scale = None if args.rows is None else args.rows / workloads.SPECS["hot"].E
-    wdt = torch.bfloat16 if args.weights == "bf16" else torch.float16
+    wdt = {"bf16": torch.bfloat16, "fp32": torch.float32}.get(args.weights, torch.float16)
     mean = args.pooling == "mean"
     ew = args.optimizer == "elementwise"
     K = max(1, args.batches)
@@ -602,14 +602,15 @@ def time_oracle(s, mean=False, elementwise=False):
     tab = oracle.Tables(s.E, s.D)
     idx, off = s.indices.numpy(), s.offsets.numpy()
     bf16 = s.weights.dtype == torch.bfloat16
+    fp32 = s.weights.dtype == torch.float32
     W = s.weights.view(torch.int16).numpy().view(np.uint16) if bf16 else s.weights.numpy()
     G = s.grad_out.numpy()
     m = (np.zeros(int(tab.w_offsets[-1]), np.float32) if elementwise
          else s.momentum.numpy())
     t = time.perf_counter()
-    oracle.forward(tab, s.B, W, idx, off, mean=mean, bf16=bf16)
+    oracle.forward(tab, s.B, W, idx, off, mean=mean, bf16=bf16, fp32=fp32)
     oracle.backward_rowwise_adagrad(tab, s.B, idx, off, G, W, m, s.lr, s.eps, mean=mean,
-                                    bf16=bf16, elementwise=elementwise)
+                                    bf16=bf16, elementwise=elementwise, fp32=fp32)
     return time.perf_counter() - t
 
 
@@ -660,8 +661,8 @@ def main():
         bags = 2048
         times, lookups = [], 0
         for k in range(args.warmup + args.steps):
-            s = reference_sample(bags, seed=k, weights_dtype=torch.bfloat16
-                                 if args.weights == "bf16" else torch.float16)
+            s = reference_sample(bags, seed=k, weights_dtype={
+                "bf16": torch.bfloat16, "fp32": torch.float32}.get(args.weights, torch.float16))
             dt = time_oracle(s, args.pooling == "mean", args.optimizer == "elementwise")
             if k >= args.warmup:
                 times.append(dt)
@@ -699,12 +700,13 @@ def main():
     D = int(w.D[0])
     ew = args.optimizer == "elementwise"
     u = r["units"]
-    kb = short_run_bytes(D, u["short_pairs"], u["short_runs"], u["R"], ew)
+    wb = w.weights.element_size()
+    kb = short_run_bytes(D, u["short_pairs"], u["short_runs"], u["R"], ew, wb)
     k_launch_ms = r["probe_ms"] / max(r["probe_launches"], 1)
     achieved = kb / (k_launch_ms / 1e3) / 1e9
     # compulsory bytes of the kernel: each short run's row and momentum read
     # and written once, its pair data once, each gradient row it gathers once
-    k_min = (u["short_runs"] * (2 * 2 * D + momentum_bytes(D, ew)) + u["R"] * 8
+    k_min = (u["short_runs"] * (2 * wb * D + momentum_bytes(D, ew)) + u["R"] * 8
              + u["short_pairs"] * 12 + u["short_bag_rows"] * 4 * D)
     reduced = (args.tables, args.rows, args.bags) != (None,) * 3
     touched = rows_touched(w)
@@ -727,7 +729,8 @@ def main():
                               "on the batch before",
                    "parallelism": f"replicas x{world} (independent batches)",
                    "l2": f"inputs larger than L2 (indices {w.n * INDEX_BYTES / 1e9:.2f} GB "
-                         f"per batch, weights {w.weights.numel() * 2 / 1e9:.1f} GB); no flush",
+                         f"per batch, weights "
+                         f"{w.weights.numel() * w.weights.element_size() / 1e9:.1f} GB); no flush",
                    "storage": f"{args.weights} weights, fp32 "
                               f"{'per-element' if ew else 'per-row'} momentum, fp32 gradients"},
         "phases_ms": {"preprocess": r["pre_ms"], "forward": r["fwd_ms"], "update": r["upd_ms"],

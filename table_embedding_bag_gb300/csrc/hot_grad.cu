@@ -23,8 +23,9 @@
 // product, below fp32 accumulation error over a bag partition.  The tensor
 // core's accumulation into tensor memory does not round to nearest, and its
 // error grows with the number of MMAs summed into one accumulator (hundreds
-// over a long partition); so every kHotFlushStages stages the accumulator is
-// added (fp32, round to nearest) into the partition's partial sums in
+// over a long partition); so every few stages (kHotFlushStages,
+// kHotFlushStagesWide) the accumulator is added (fp32, round to nearest,
+// reductions at L2) into the partition's partial sums in
 // hot_part[t][p][slot][c] and restarted.  The finishing kernel sums the
 // partitions in order.  Every mbarrier wait is bounded (time-out:
 // TBE_ERR_TIMEOUT in the status word, drain, free).
@@ -46,11 +47,21 @@ constexpr int kGBBytes = kHot * kGStage * 4;     // 32 KB for 256 slots
 constexpr int kGAItems = kGM * kGStage / kGThreads;    // 16 per M tile
 constexpr int kGBItems = kHot * kGStage / kGThreads;   // up to 32
 // Stages summed into the tensor-memory accumulator between two flushes into
-// the partials (at most 8 x 4 x 3 MMAs of 8 products each).
+// the partials: byte tiles (hot_grad_bytes_kernel, 2 MMAs per K step of 8
+// bags) every 8 stages, wide tiles (hot_grad_tc_kernel, up to 3 MMAs per K
+// step, fp32 histogram values with remainders) every 2 stages.  Measured on
+// GB300: at 8 stages the wide tiles of the weighted recipe left 0.4 % of the
+// element-wise accumulators beyond 1e-5 of the oracle, at 2 stages none
+// beyond the 0.1 % the cold rows' fp32 sums allow; the hot-row recipe's byte
+// tiles meet 1e-5 (row-wise) at 8.
 #ifndef TBE_HOT_FLUSH_STAGES
 #define TBE_HOT_FLUSH_STAGES 8
 #endif
+#ifndef TBE_HOT_FLUSH_STAGES_WIDE
+#define TBE_HOT_FLUSH_STAGES_WIDE 2
+#endif
 constexpr int kHotFlushStages = TBE_HOT_FLUSH_STAGES;
+constexpr int kHotFlushStagesWide = TBE_HOT_FLUSH_STAGES_WIDE;
 
 // The accumulator D^T[c][slot] of this CTA stored (add: added) into
 // hot_part[t][p][slot][c].  Warps w and w + 4 read TMEM lanes 32 (w % 4) ..
@@ -334,7 +345,7 @@ __global__ void __launch_bounds__(kGThreads, 2) hot_grad_tc_kernel(HotGradArgs a
     fence_after_sync();
     __syncthreads();
     if (tl.timed_out) break;
-    if (++in_acc == kHotFlushStages && c0 + kGStage < b_end) {
+    if (++in_acc == kHotFlushStagesWide && c0 + kGStage < b_end) {
       // into the partials; the next stage restarts the accumulator
       flush_partials(tmem, dst, mtiles, D, nh, n_slots, flushed > 0);
       ++flushed;

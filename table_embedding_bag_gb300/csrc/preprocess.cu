@@ -947,7 +947,7 @@ __global__ void __launch_bounds__(1024)
 // nodes into blk[4][grid], an exclusive scan of each turns them into the
 // blocks' list bases, and kMode 2 writes the lists from those bases.
 #ifndef TBE_ORDERED_CLASSIFY
-#define TBE_ORDERED_CLASSIFY 0
+#define TBE_ORDERED_CLASSIFY 1
 #endif
 template <int kMode>
 __global__ void __launch_bounds__(256)
@@ -1073,7 +1073,7 @@ __global__ void __launch_bounds__(256)
 // bands_per_table bins per table: the chunks in flight then gather from one
 // table's gradient rows at a time instead of every table's.
 #ifndef TBE_TABLE_BANDS
-#define TBE_TABLE_BANDS 0
+#define TBE_TABLE_BANDS 1
 #endif
 __global__ void __launch_bounds__(256)
     chunk_band_count_kernel(const uint32_t* __restrict__ counters,

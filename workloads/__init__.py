@@ -226,7 +226,8 @@ def batch(w: Workload, seed: int) -> Workload:
 def from_arrays(E, D, B, indices, offsets, weights, grad_out, psw=None, momentum=None,
                 lr=0.01, eps=1e-8, name="custom") -> Workload:
     """Wrap hand-made arrays (numpy or torch, on the host) as a Workload
-    (weights: fp16, or a bfloat16 tensor, which is kept as it is)."""
+    (weights: fp16; a bfloat16 tensor or float32 weights are kept as they
+    are)."""
     t = lambda x, dt=None: None if x is None else torch.as_tensor(np.asarray(x) if not
                                                                    torch.is_tensor(x) else x,
                                                                    dtype=dt)
@@ -235,6 +236,11 @@ def from_arrays(E, D, B, indices, offsets, weights, grad_out, psw=None, momentum
     idx = t(indices)
     off = t(offsets, idx.dtype)
     m = t(momentum, torch.float32) if momentum is not None else torch.zeros(int(E.sum()))
-    return Workload(name, len(E), int(B), E, D, idx, off, t(psw, torch.float32),
-                    weights if torch.is_tensor(weights) and weights.dtype == torch.bfloat16
-                    else t(weights, torch.float16), m, t(grad_out, torch.float32), lr, eps)
+    if torch.is_tensor(weights) and weights.dtype in (torch.bfloat16, torch.float32):
+        W = weights
+    elif not torch.is_tensor(weights) and np.asarray(weights).dtype == np.float32:
+        W = t(weights, torch.float32)
+    else:
+        W = t(weights, torch.float16)
+    return Workload(name, len(E), int(B), E, D, idx, off, t(psw, torch.float32), W, m,
+                    t(grad_out, torch.float32), lr, eps)
