@@ -780,12 +780,13 @@ def main():
         mean, ew_ = args.pooling == "mean", args.optimizer == "elementwise"
         s = cpu_sample(w, args.cpu_bags)
         dt = time_oracle(s, mean, ew_)
-        cores = max(1, min(os.cpu_count() or 1, w.B // args.cpu_bags))
-        v, n_all, secs = cpu_baseline_parallel(w, args.cpu_bags, cores, mean, ew_)
+        cores = max(1, os.cpu_count() or 1)
+        per = max(1, min(args.cpu_bags, w.B // cores))  # bags of table 0 per core
+        v, n_all, secs = cpu_baseline_parallel(w, per, cores, mean, ew_)
         line["cpu_baseline"] = {"value": v, "unit": "lookups/s", "cores": cores,
                                 "kind": "oracle",
                                 "sample": f"table 0 of the first batch, {cores} disjoint ranges "
-                                          f"of {args.cpu_bags} bags ({n_all} lookups), forward + "
+                                          f"of {per} bags ({n_all} lookups), forward + "
                                           f"backward, one oracle process per core, "
                                           f"{secs:.1f} s wall",
                                 "single_core": {"value": s.n / dt, "cores": 1,

@@ -172,7 +172,8 @@ typedef struct tbe_ws_view {
   const uint32_t* run_pairs;    /* [R+1] first pair of each run; [R] = P */
   const uint32_t* pair_starts;  /* [P+1] first sorted position of each pair; [P] = n_valid */
   const uint32_t* pair_bags;    /* [P] bag of each pair */
-  const uint32_t* hot_keys;     /* [T][hot_slots] hot rows of each table (linear keys, sorted) */
+  const uint32_t* hot_keys;     /* [T][hot_slots] hot rows of each table (linear keys, the
+                                   most looked-up first) */
   const uint32_t* hot_n;        /* [T] hot rows per table */
   int32_t hot_slots;            /* hot rows a table can have */
   int32_t medium_threshold;     /* pairs from which a run below long_threshold is updated

@@ -179,7 +179,8 @@ struct WsLayout {
   size_t tree_cnt;     // uint32 [max_tree] arrivals still expected at each tree node
   size_t partials;     // float [max_chunks * max_D]
   size_t tree_part;    // float [max_tree * max_D]
-  // Two hot sets, each uint32 keys [T][kHot] (sorted linear keys), place
+  // Two hot sets, each uint32 keys [T][kHot] (linear keys, the most looked-up
+  // first, ties by key), place
   // [T][kHot] (each key's cuckoo entry), n [T], m1 [T], m2 [T], kept across
   // calls: `hot_next` is written by the backward's refresh and copied to
   // `hot_cur` at the start of every preprocess; the preprocess, the forward
@@ -207,6 +208,7 @@ struct WsLayout {
   size_t sel_hist;     // uint32 [T][kHotBuckets] refresh: count buckets per table
   size_t sel_thresh;   // uint32 [T] refresh: lowest bucket kept
   size_t sel_keys;     // uint32 [T][kHot] refresh: the next hot set
+  size_t sel_cnt;      // uint32 [T][kHot] refresh: each selected key's lookups
   size_t sel_n;        // uint32 [T]
   size_t offsets_fix;  // index type [T*B+1] repaired offsets
   size_t fix_scratch;  // int64 [blocks] block maxima for the repair scan

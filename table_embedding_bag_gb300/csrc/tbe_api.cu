@@ -160,6 +160,7 @@ WsLayout make_layout(const tbe_desc* d, int64_t n, uint32_t ws_flags, bool allow
   L.sel_hist = take(T * kHotBuckets * 4);
   L.sel_thresh = take(T * 4);
   L.sel_keys = take(T * kHot * 4);
+  L.sel_cnt = take(T * kHot * 4);
   L.sel_n = take(T * 4);
   const int64_t nb1 = T * B + 1;
   L.offsets_fix = take(nb1 * index_bytes(d));

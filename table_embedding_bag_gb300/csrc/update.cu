@@ -866,7 +866,7 @@ __global__ void __launch_bounds__(256)
                       const uint32_t* __restrict__ hot_keys, const uint32_t* __restrict__ hot_n,
                       const uint32_t* __restrict__ hot_cnt, uint32_t min_count,
                       const uint32_t* __restrict__ sel_thresh, uint32_t* __restrict__ sel_keys,
-                      uint32_t* __restrict__ sel_n) {
+                      uint32_t* __restrict__ sel_cnt, uint32_t* __restrict__ sel_n) {
   __shared__ MetaSmem msm;
   const Meta m = load_meta(a, msm, false);
   const uint32_t R = a.counters[kCntRuns];
@@ -877,14 +877,19 @@ __global__ void __launch_bounds__(256)
     if (hot_candidate(a, m, i, R, run_starts, hot_keys, hot_n, hot_cnt, min_count, &t, &key, &cnt) &&
         static_cast<uint32_t>(count_bucket(cnt)) >= sel_thresh[t]) {
       const uint32_t slot = atomicAdd(&sel_n[t], 1u);
-      if (slot < static_cast<uint32_t>(kHot)) sel_keys[t * kHot + slot] = key;
+      if (slot < static_cast<uint32_t>(kHot)) {
+        sel_keys[t * kHot + slot] = key;
+        sel_cnt[t * kHot + slot] = cnt;
+      }
     }
   }
 }
 
-// The selected keys, sorted per table, become the hot set, together with a
-// place for each key in the two-choice hash (see kCuckooHalf): one CTA per
-// table sorts the keys (bitonic), then one thread inserts them with
+// The selected keys, ordered per table by lookups (most first, ties by key:
+// the expand counts the first slots by warp votes), become the hot set,
+// together with a place for each key in the two-choice hash (see
+// kCuckooHalf): one CTA per table sorts them (bitonic), then one thread
+// inserts them with
 // displacement under the first multiplier pair of a fixed sequence for which
 // every insertion succeeds within kCuckooKicks moves.  At a load of 1/4 the
 // first pair almost always succeeds; if kCuckooTries pairs fail, keys that
@@ -919,29 +924,36 @@ __device__ bool cuckoo_insert(uint32_t* tab, uint32_t key, uint32_t m1, uint32_t
 }
 
 __global__ void __launch_bounds__(kHot)
-    hot_commit_kernel(const uint32_t* __restrict__ sel_keys, const uint32_t* __restrict__ sel_n,
+    hot_commit_kernel(const uint32_t* __restrict__ sel_keys, const uint32_t* __restrict__ sel_cnt,
+                      const uint32_t* __restrict__ sel_n,
                       uint32_t* __restrict__ hot_keys, uint32_t* __restrict__ hot_place,
                       uint32_t* __restrict__ hot_n, uint32_t* __restrict__ hot_m1,
                       uint32_t* __restrict__ hot_m2) {
   __shared__ uint32_t k[kHot];
+  __shared__ unsigned long long order[kHot];  // (~count) << 32 | key: ascending = most first
   __shared__ uint32_t tab[kCuckooSize];
   __shared__ uint32_t scan[33];
   __shared__ uint32_t mults[2];
   const int t = blockIdx.x;
   const int i = threadIdx.x;
   const uint32_t nsel = min(sel_n[t], static_cast<uint32_t>(kHot));
-  k[i] = i < static_cast<int>(nsel) ? sel_keys[t * kHot + i] : kEmptyKey;
-  // bitonic sort of kHot keys, ascending (padding kEmptyKey sorts last)
+  order[i] = i < static_cast<int>(nsel)
+                 ? (static_cast<unsigned long long>(~sel_cnt[t * kHot + i]) << 32) |
+                       sel_keys[t * kHot + i]
+                 : ~0ull;  // padding sorts last
+  // bitonic sort of kHot entries, ascending
   for (int size = 2; size <= kHot; size <<= 1)
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       __syncthreads();
       const int j = i ^ stride;
       if (j > i) {
         const bool up = (i & size) == 0;
-        const uint32_t a = k[i], b = k[j];
-        if ((a > b) == up) { k[i] = b; k[j] = a; }
+        const unsigned long long a = order[i], b = order[j];
+        if ((a > b) == up) { order[i] = b; order[j] = a; }
       }
     }
+  __syncthreads();
+  k[i] = i < static_cast<int>(nsel) ? static_cast<uint32_t>(order[i]) : kEmptyKey;
   __syncthreads();
   if (i == 0) {
     bool ok = false;
@@ -1137,13 +1149,14 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   uint32_t* sel_hist = reinterpret_cast<uint32_t*>(ws + W.sel_hist);
   uint32_t* sel_thresh = reinterpret_cast<uint32_t*>(ws + W.sel_thresh);
   uint32_t* sel_keys = reinterpret_cast<uint32_t*>(ws + W.sel_keys);
+  uint32_t* sel_cnt = reinterpret_cast<uint32_t*>(ws + W.sel_cnt);
   uint32_t* sel_n = reinterpret_cast<uint32_t*>(ws + W.sel_n);
   { hot_hist_kernel<<<blocks, 256, 0, L.s>>>(a, rs, hot_keys, hot_n, hot_cnt, min_count, sel_hist); note_launch(); }
   { hot_thresh_kernel<<<(d->T + 127) / 128, 128, 0, L.s>>>(d->T, sel_hist, sel_thresh); note_launch(); }
   { hot_select_kernel<<<blocks, 256, 0, L.s>>>(a, rs, hot_keys, hot_n, hot_cnt, min_count,
-                                             sel_thresh, sel_keys, sel_n); note_launch(); }
+                                             sel_thresh, sel_keys, sel_cnt, sel_n); note_launch(); }
   { hot_commit_kernel<<<static_cast<unsigned>(d->T), kHot, 0, L.s>>>(
-      sel_keys, sel_n, reinterpret_cast<uint32_t*>(ws + W.hot_keys(W.hot_next)),
+      sel_keys, sel_cnt, sel_n, reinterpret_cast<uint32_t*>(ws + W.hot_keys(W.hot_next)),
       reinterpret_cast<uint32_t*>(ws + W.hot_place(W.hot_next)),
       reinterpret_cast<uint32_t*>(ws + W.hot_n(W.hot_next)),
       reinterpret_cast<uint32_t*>(ws + W.hot_m1(W.hot_next)),
