@@ -162,11 +162,13 @@ struct ExpandSmem {
 constexpr int kExpandLoads = TBE_EXPAND_LOADS;  // index loads in flight per lane
 // Unweighted lookups of a table's first kTopVoteSlots hot slots (the set is
 // ordered by lookups, so these are its most looked-up rows: about 60 % of
-// the hot lookups under Zipf(1.4)) are counted by one warp vote per slot
-// instead of shared atomics that many lanes of a warp would aim at the same
-// counter.
+// the hot lookups under Zipf(1.4) for four slots) can be counted by one warp
+// vote per slot instead of shared atomics that many lanes of a warp aim at
+// the same counter.  Off: on GB300 the votes cost more than the contention
+// they remove (hot-row preprocess 0.83 ms without, 0.95 ms with four slots,
+// 1.05 ms with eight).
 #ifndef TBE_TOP_VOTE_SLOTS
-#define TBE_TOP_VOTE_SLOTS 4
+#define TBE_TOP_VOTE_SLOTS 0
 #endif
 constexpr int kTopVoteSlots = TBE_TOP_VOTE_SLOTS;
 
