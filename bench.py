@@ -71,7 +71,9 @@ def parse():
                    help="weight type (the recorded workload is fp16)")
     p.add_argument("--optimizer", choices=["rowwise", "elementwise"], default="rowwise",
                    help="Adagrad form (the recorded workload is row-wise)")
-    # smaller variants of the hot-row recipe, for profiling captures only
+    # other recipes and smaller variants of one, for profiling captures only
+    p.add_argument("--recipe", choices=["hot", "weighted", "mixed", "small", "tiny"],
+                   default="hot")
     p.add_argument("--tables", type=int, default=None)
     p.add_argument("--rows", type=int, default=None)
     p.add_argument("--bags", type=int, default=None)
@@ -174,7 +176,10 @@ ROOFLINE_KERNEL_SOURCES = ("update.cu", "common.cuh")
 # the sha1 of the kernel's sources it was taken on: the bench scales it by
 # the pairs of a full launch while the sources are unchanged, else reports
 # null.  None until a capture of the current sources exists.
-TRAFFIC_RECORD = None
+TRAFFIC_RECORD = {"bytes_per_pair": 496.46, "source_sha1": "9d13953be01dd9e6",
+                  "capture": "hot-row recipe reduced to one table (E=1e7, D=128, B=131072), "
+                             "two timed launches, dram__bytes_read.sum + dram__bytes_write.sum "
+                             "= 220.6 MB per launch over 442 434 short-run pairs"}
 
 
 def source_sha1():
@@ -439,12 +444,14 @@ def run_native(args, world, rank, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     import workloads
     E_scale = None if args.rows is None else args.rows / workloads.SPECS["hot"].E
+    if args.recipe != "hot" and args.rows is not None:
+        raise SystemExit("--rows applies to the hot-row recipe only")
     wdt = {"bf16": torch.bfloat16, "fp32": torch.float32}.get(args.weights, torch.float16)
     mean = args.pooling == "mean"
     ew = args.optimizer == "elementwise"
     K = max(1, args.batches)
-    batches = draw_batches("hot", dev, rank, K, T=args.tables, B=args.bags, E_scale=E_scale,
-                           weights_dtype=wdt)
+    batches = draw_batches(args.recipe, dev, rank, K, T=args.tables, B=args.bags,
+                           E_scale=E_scale, weights_dtype=wdt)
     w = batches[0]
     st = Stepper(tbe, batches, dev, wdt, mean=mean, elementwise=ew)
     stream = torch.cuda.current_stream()
@@ -697,7 +704,10 @@ def main():
         pass
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    D = int(w.D[0])
+    # row width of the byte models: the recipe's D, or (mixed widths) the
+    # lookup-weighted mean width
+    L_t = (w.offsets[1:].long() - w.offsets[:-1].long()).view(w.T, w.B).sum(1).cpu().numpy()
+    D = int(round(float((L_t * w.D).sum() / max(L_t.sum(), 1))))
     ew = args.optimizer == "elementwise"
     u = r["units"]
     wb = w.weights.element_size()
@@ -708,7 +718,7 @@ def main():
     # and written once, its pair data once, each gradient row it gathers once
     k_min = (u["short_runs"] * (2 * wb * D + momentum_bytes(D, ew)) + u["R"] * 8
              + u["short_pairs"] * 12 + u["short_bag_rows"] * 4 * D)
-    reduced = (args.tables, args.rows, args.bags) != (None,) * 3
+    reduced = (args.tables, args.rows, args.bags) != (None,) * 3 or args.recipe != "hot"
     touched = rows_touched(w)
     cb = compulsory_bytes(w, touched, w.indices.element_size(), ew)
     t_fwd = r["pre_ms"] + r["fwd_ms"]
@@ -721,8 +731,9 @@ def main():
         "data": "synthetic",
         "config": {"workload": workload_name(
                        args, WORKLOAD if not reduced
-                       else f"reduced hot-row recipe T={w.T} E={int(w.E[0])} B={w.B} "
-                            "(profiling case)"),
+                       else f"{args.recipe} recipe T={w.T} B={w.B} n={w.n}"
+                            + (" (reduced)" if args.recipe == "hot" else "")
+                            + " (profiling case)"),
                    "n_lookups": w.n, "global_batch": w.B * world,
                    "batches": f"{len(r['batches'])} distinct batches over the same tables "
                               "(table seed = rank), cycled; each step's hot set was learned "

@@ -220,36 +220,50 @@ __global__ void __launch_bounds__(256)
     uint32_t top[kTopVoteSlots > 0 ? kTopVoteSlots : 1];  // votes of the first slots (uniform)
 #pragma unroll
     for (int j = 0; j < kTopVoteSlots; ++j) top[j] = 0;
-    for (int64_t base = s; base < e; base += 32 * kExpandLoads) {
-      int64_t r[kExpandLoads];
+    // 32-bit arithmetic relative to the bag's start (a bag holds fewer than
+    // 2^32 lookups, and keys are below 2^32): the lane's position o, the
+    // sparse-list position `cold + ...`, the key h0 + row
+    const uint32_t len = static_cast<uint32_t>(e - s);
+    const IndexT* __restrict__ ib = indices + s;
+    const float* __restrict__ pb = kWeighted ? psw + s : nullptr;
+    uint32_t* __restrict__ kb = sp_keys + s;
+    uint32_t* __restrict__ vb = sp_vals + s;
+    float* __restrict__ wb = kWeighted ? sp_psw + s : nullptr;
+    const uint32_t bag_in_table = static_cast<uint32_t>(ti.b0 + lb);
+    const uint32_t h0_32 = static_cast<uint32_t>(h0);
+    for (uint32_t base = 0; base < len; base += 32 * kExpandLoads) {
+      IndexT r[kExpandLoads];
 #pragma unroll
       for (int u = 0; u < kExpandLoads; ++u) {
-        const int64_t i = base + u * 32 + lane;
-        r[u] = i < e ? load_index(indices, i) : -2;  // -2: past the bag's end
+        const uint32_t o = base + u * 32 + lane;
+        r[u] = o < len ? __ldg(ib + o) : IndexT(0);
       }
 #pragma unroll
       for (int u = 0; u < kExpandLoads; ++u) {
-        if (base + u * 32 >= e) break;  // warp-uniform
-        const bool inside = r[u] != -2;
-        const bool ok = static_cast<uint64_t>(r[u]) < static_cast<uint64_t>(E);  // -2 fails too
+        if (base + u * 32 >= len) break;  // warp-uniform
+        const uint32_t o = base + u * 32 + lane;
+        const bool inside = o < len;
+        // a row outside [0, E) (negative ones too, as unsigned) is skipped
+        const bool ok = inside && static_cast<uint64_t>(static_cast<int64_t>(r[u])) <
+                                      static_cast<uint64_t>(E);
         bad |= inside && !ok;
-        const uint32_t key = static_cast<uint32_t>(h0 + r[u]);
+        const uint32_t key = h0_32 + static_cast<uint32_t>(r[u]);
         const int slot = ok && nh ? hot_lookup(sm.hash, m1, m2, key) : -1;
         // cold lookups go, in lookup order, to the front of the bag's own
         // range [s, e) of the sparse list
         const bool is_cold = ok && slot < 0;
         const unsigned cm = __ballot_sync(kFull, is_cold);
         if (is_cold) {
-          const int64_t at = s + cold + __popc(cm & lt);
-          sp_keys[at] = key;
-          sp_vals[at] = static_cast<uint32_t>(ti.b0 + lb);
-          if (kWeighted) sp_psw[at] = __ldg(psw + base + u * 32 + lane);
+          const uint32_t at = cold + __popc(cm & lt);
+          kb[at] = key;
+          vb[at] = bag_in_table;
+          if (kWeighted) wb[at] = __ldg(pb + o);
         }
         cold += __popc(cm);
         if constexpr (kWeighted) {
           // double sums of fp32 weights are exact: atomic order does not matter
           if (slot >= 0) {
-            atomicAdd(&sm.row[warp][slot], static_cast<double>(__ldg(psw + base + u * 32 + lane)));
+            atomicAdd(&sm.row[warp][slot], static_cast<double>(__ldg(pb + o)));
             atomicAdd(&sm.cnt_row[warp][slot], 1u);
           }
         } else {
@@ -420,6 +434,33 @@ __global__ void __launch_bounds__(256)
       if (kWeighted) psw_out[pos + i] = __ldg(sp_psw + s + i);
     }
   }
+}
+
+// One CTA per array (blockIdx.x = k): exclusive scan in place of the
+// classify blocks' totals blk[k][0 .. nblk) and the array's total into
+// counters[dest[k]] (medium runs, long runs, chunks, tree nodes).
+struct ScanDests {
+  int d[4];
+};
+__global__ void __launch_bounds__(1024)
+    block_totals_scan_kernel(uint32_t* __restrict__ blk, int nblk, uint32_t* counters,
+                             ScanDests dest) {
+  __shared__ uint32_t sm[33];
+  uint32_t* data = blk + static_cast<int64_t>(blockIdx.x) * nblk;
+  const int per = (nblk + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+  const int b = static_cast<int>(threadIdx.x) * per;
+  const int e = b + per < nblk ? b + per : nblk;
+  uint32_t s = 0;
+  for (int i = b; i < e; ++i) s += data[i];
+  uint32_t agg;
+  const uint32_t inc = block_inclusive_scan(s, OpSum(), 0u, sm, &agg);
+  uint32_t run = inc - s;
+  for (int i = b; i < e; ++i) {
+    const uint32_t v = data[i];
+    data[i] = run;
+    run += v;
+  }
+  if (threadIdx.x == 0) counters[dest.d[blockIdx.x]] = agg;
 }
 
 // Single CTA: exclusive scan of the expand tiles' cold counts in place,
@@ -1292,11 +1333,10 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
       classify_kernel<1><<<cb0, 256, 0, s>>>(rp, counters, cl_args[0], cl_args[1], cl_args[2],
                                               cl_args[3], cl_args[4]);
       note_launch();
-      const int dest[4] = {kCntMedium, kCntLong, kCntChunks, kCntTree};
-      for (int k = 0; k < 4; ++k) {
-        exclusive_scan_kernel<<<1, 1024, 0, s>>>(cl_args[4] + k * cb0, cb0, counters + dest[k]);
-        note_launch();
-      }
+      const ScanDests dest{{kCntMedium, kCntLong, kCntChunks, kCntTree}};
+      block_totals_scan_kernel<<<4, 1024, 0, s>>>(cl_args[4], static_cast<int>(cb0), counters,
+                                                 dest);
+      note_launch();
       classify_kernel<2><<<cb0, 256, 0, s>>>(rp, counters, cl_args[0], cl_args[1], cl_args[2],
                                               cl_args[3], cl_args[4]);
       note_launch();

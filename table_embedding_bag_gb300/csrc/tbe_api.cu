@@ -14,6 +14,10 @@ std::atomic<uint64_t> g_kernel_launches{0};
 
 void note_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 
+#ifndef TBE_SIDE_PRIORITY
+#define TBE_SIDE_PRIORITY 0
+#endif
+
 namespace {
 // Side flows by (device, workspace address).  Entries live until the process
 // exits (a stream and four events each); a workspace freed and another
@@ -32,7 +36,13 @@ SideFlow* lookup_flow(const void* ws, bool create) {
   if (!create) return nullptr;
   SideFlow f;
   const unsigned ef = cudaEventDisableTiming;
-  const bool ok = cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) == cudaSuccess &&
+  // TBE_SIDE_PRIORITY: the side stream at the device's greatest priority
+  // (its blocks are scheduled ahead of the caller's default-priority ones)
+  int prio_least = 0, prio_greatest = 0;
+  if (TBE_SIDE_PRIORITY && cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest) != cudaSuccess)
+    prio_greatest = 0;
+  const int prio = TBE_SIDE_PRIORITY ? prio_greatest : 0;
+  const bool ok = cudaStreamCreateWithPriority(&f.side, cudaStreamNonBlocking, prio) == cudaSuccess &&
                   cudaEventCreateWithFlags(&f.fork, ef) == cudaSuccess &&
                   cudaEventCreateWithFlags(&f.sorted, ef) == cudaSuccess &&
                   cudaEventCreateWithFlags(&f.hot, ef) == cudaSuccess &&

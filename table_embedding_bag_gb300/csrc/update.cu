@@ -1020,6 +1020,10 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+#ifndef TBE_HOT_GRAD_SIDE
+#define TBE_HOT_GRAD_SIDE 1
+#endif
+
 // The cold runs' update kernels (short, medium, long chunks, and the second
 // long-run kernel in the two-launch variant) on L's stream, in that order.
 template <bool kEw>
@@ -1106,10 +1110,11 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   const uint32_t* hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_cur));
   const uint32_t* hot_cnt = reinterpret_cast<const uint32_t*>(ws + W.hot_cnt);
   if (W.hot_enabled) {
-    cudaError_t e = fork_to(sf, L.s);
+    // TBE_HOT_GRAD_SIDE 0: on the caller's stream, before the cold rows
+    cudaError_t e = TBE_HOT_GRAD_SIDE ? fork_to(sf, L.s) : cudaSuccess;
     if (e != cudaSuccess) return e;
     Launch Ls = L;
-    Ls.s = sf->side;
+    if (TBE_HOT_GRAD_SIDE) Ls.s = sf->side;
     const float* part = reinterpret_cast<const float*>(ws + W.hot_part);
     e = launch_hot_grad(Ls, W, ws, grad_out);
     if (e != cudaSuccess) return e;
