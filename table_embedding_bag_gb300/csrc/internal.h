@@ -88,6 +88,15 @@ cudaError_t launch_hot_grad(const Launch& L, const WsLayout& W, char* ws, const 
 cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const float* grad_out,
                           void* weights, float* momentum, float lr, float eps, bool two_launch,
                           bool elementwise = false);
+// The next call's hot set, chosen from this call's cold runs and hot-row
+// counts (after the sort chain), written to the workspace's second set.
+cudaError_t launch_hot_refresh(const Launch& L, const WsLayout& W, char* ws);
+// Where the refresh runs: 0, at the end of the backward on the caller's
+// stream; 1, at the end of the preprocess's sort chain on the side stream
+// (beside the forward).
+#ifndef TBE_REFRESH_IN_PREPROCESS
+#define TBE_REFRESH_IN_PREPROCESS 0
+#endif
 // Mean pooling's backward input: out[b, D_off[t] + c] = grad_out[b, D_off[t] + c]
 // times bag (t, b)'s factor from inv_len.
 cudaError_t launch_scale_grad(const Launch& L, const float* grad_out, const float* inv_len,

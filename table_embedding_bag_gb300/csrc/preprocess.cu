@@ -1379,6 +1379,14 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
   }
   err = cudaEventRecord(sf->sorted, s);
   if (err != cudaSuccess) return err;
+  if (TBE_REFRESH_IN_PREPROCESS) {
+    // the next hot set needs only this batch's runs and hot-row counts;
+    // the backward does not wait for it (only the next preprocess does)
+    Launch Ls = L;
+    Ls.s = s;
+    err = launch_hot_refresh(Ls, W, ws);
+    if (err != cudaSuccess) return err;
+  }
   err = cudaEventRecord(sf->done, s);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();

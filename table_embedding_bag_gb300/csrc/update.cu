@@ -1141,10 +1141,33 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   if (elementwise) launch_runs<true>(L, a, medium, blocks, weighted, wide, two_launch);
   else launch_runs<false>(L, a, medium, blocks, weighted, wide, two_launch);
   if (!W.hot_enabled) return cudaGetLastError();  // no histogram: the hot set stays empty
-  // Choose the next hot set, once the hot rows' update has read this one.
+  // the caller's stream joins the hot rows' update
   cudaError_t e = cudaStreamWaitEvent(L.s, sf->hot, 0);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(ws + W.sel_hist, 0, static_cast<size_t>(d->T) * kHotBuckets * 4, L.s);
+  if (TBE_REFRESH_IN_PREPROCESS) return cudaGetLastError();  // the preprocess chose it
+  return launch_hot_refresh(L, W, ws);
+}
+
+// The next call's hot set, chosen from this call's lookups: the cold runs'
+// lengths and the hot rows' counts (none of the gradients), written to the
+// workspace's second hot set on L's stream.
+cudaError_t launch_hot_refresh(const Launch& L, const WsLayout& W, char* ws) {
+  const tbe_desc* d = L.d;
+  if (L.n == 0 || !W.hot_enabled) return cudaSuccess;
+  UpdArgs a{};
+  a.D_offsets = d->D_offsets;
+  a.hash_base = d->hash_base;
+  a.w_offsets = d->weights_offsets;
+  a.unique_keys = reinterpret_cast<const uint32_t*>(ws + W.unique_keys);
+  a.counters = reinterpret_cast<const uint32_t*>(ws + W.counts);
+  a.T = d->T;
+  a.B = d->B;
+  a.max_D = d->max_D;
+  const unsigned blocks = static_cast<unsigned>(L.num_sms) * 8u;
+  const uint32_t* hot_keys = reinterpret_cast<const uint32_t*>(ws + W.hot_keys(W.hot_cur));
+  const uint32_t* hot_n = reinterpret_cast<const uint32_t*>(ws + W.hot_n(W.hot_cur));
+  const uint32_t* hot_cnt = reinterpret_cast<const uint32_t*>(ws + W.hot_cnt);
+  cudaError_t e = cudaMemsetAsync(ws + W.sel_hist, 0, static_cast<size_t>(d->T) * kHotBuckets * 4, L.s);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(ws + W.sel_n, 0, static_cast<size_t>(d->T) * 4, L.s);
   if (e != cudaSuccess) return e;
