@@ -237,7 +237,12 @@ tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indic
  * rows are not sorted but summed per bag into a histogram (counts, stored as
  * bytes for every 128-bag tile whose counts all fit one; otherwise, and for
  * sums of per-sample weights, fp32 with a per-bag power-of-two scale), and
- * the remaining (cold) lookups are also kept per bag in lookup order.  Results stay in the workspace (see tbe_workspace_view); a
+ * the remaining (cold) lookups are also kept per bag in lookup order.  After
+ * the sort the call chooses the next hot set from this batch: per table, the
+ * most looked-up rows with at least max(B/64, 32) lookups (tables with D_t <=
+ * 256 only, and only while the histograms, T * hot_slots * B * 5 bytes, stay
+ * within 2 GiB; fp32 tables have none); the next preprocess on this
+ * workspace takes it.  Results stay in the workspace (see tbe_workspace_view); a
  * later tbe_forward or tbe_backward_rowwise_adagrad with TBE_F_PREPROCESSED
  * consumes them.  The sort chain runs on a stream the library keeps for this
  * workspace (created at the workspace's first use, one per workspace and
@@ -267,11 +272,10 @@ tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* of
  * its histogram column times grad_out, summed over bag partitions in a fixed
  * order; every other row's gradient is summed over its sorted run.  Both are
  * fp32 sums whose rounding order differs, so a row's result can differ in the
- * last bits between a call where it is hot and one where it is cold.  The call
- * then chooses the next hot set: per table, the most looked-up rows of this
- * batch with at least max(B/64, 32) lookups (tables with D_t <= 256 only, and
- * only while the histograms, T * hot_slots * B * 5 bytes, stay within 2 GiB).
- * No host synchronisation, no device-to-host copy.  Errors as tbe_forward. */
+ * last bits between a call where it is hot and one where it is cold (the hot
+ * set comes from the previous preprocess on this workspace; see
+ * tbe_preprocess).  No host synchronisation, no device-to-host copy.  Errors
+ * as tbe_forward. */
 tbe_status tbe_backward_rowwise_adagrad(const tbe_desc* d, const float* grad_out,
                                         const void* indices, const void* offsets, int64_t n,
                                         const float* per_sample_weights, void* weights,

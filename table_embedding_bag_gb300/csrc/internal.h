@@ -95,7 +95,7 @@ cudaError_t launch_hot_refresh(const Launch& L, const WsLayout& W, char* ws);
 // stream; 1, at the end of the preprocess's sort chain on the side stream
 // (beside the forward).
 #ifndef TBE_REFRESH_IN_PREPROCESS
-#define TBE_REFRESH_IN_PREPROCESS 0
+#define TBE_REFRESH_IN_PREPROCESS 1
 #endif
 // Mean pooling's backward input: out[b, D_off[t] + c] = grad_out[b, D_off[t] + c]
 // times bag (t, b)'s factor from inv_len.

@@ -15,7 +15,7 @@ std::atomic<uint64_t> g_kernel_launches{0};
 void note_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 
 #ifndef TBE_SIDE_PRIORITY
-#define TBE_SIDE_PRIORITY 0
+#define TBE_SIDE_PRIORITY 1
 #endif
 
 namespace {

@@ -1021,7 +1021,7 @@ __global__ void __launch_bounds__(256)
 }
 
 #ifndef TBE_HOT_GRAD_SIDE
-#define TBE_HOT_GRAD_SIDE 1
+#define TBE_HOT_GRAD_SIDE 0
 #endif
 
 // The cold runs' update kernels (short, medium, long chunks, and the second
