@@ -204,6 +204,176 @@ __global__ void __launch_bounds__(256, TBE_FWD_MINB)
   }
 }
 
+// The same pooling with persistent warps that loop over their bag groups
+// through a software pipeline whose intermediate data lives in shared
+// memory: while bag group i is pooled, the first S cold keys (and weights)
+// of each bag of group i + 1 and the list offsets of group i + 2 are copied
+// there by cp.async.  A group then waits for its rows only, not for its
+// offsets and keys.
+#ifndef TBE_COLD_PIPE
+#define TBE_COLD_PIPE 1
+#endif
+
+template <int S>
+struct ColdPipe {  // one per warp
+  uint32_t off[3][32 / S + 1];  // slot: cold_off of the group's bags and the end
+  uint32_t key[2][32];          // slot: the first S keys of bag g at [g S + sl]
+  float w[2][32];               // and their per-sample weights
+};
+
+template <int S, bool kWeighted, bool kBf16>
+__global__ void __launch_bounds__(256, TBE_FWD_MINB)
+    forward_cold_piped_kernel(const __half* __restrict__ W, const int64_t* __restrict__ D_offsets,
+                              const int64_t* __restrict__ hash_base,
+                              const int64_t* __restrict__ w_offsets,
+                              const uint32_t* __restrict__ keys, const uint32_t* __restrict__ cold_off,
+                              const float* __restrict__ psw, int T, int B, int64_t total_D,
+                              float* __restrict__ out, const uint32_t* __restrict__ hot_n,
+                              const float* __restrict__ inv_len) {
+  constexpr int G = 32 / S;
+  constexpr int U = S < TBE_FWD_UNROLL ? S : TBE_FWD_UNROLL;
+  __shared__ ColdPipe<S> pipes[8];
+  ColdPipe<S>& cp = pipes[threadIdx.x >> 5];
+  const int lane = static_cast<int>(lane_id());
+  const int g = lane / S;
+  const int sl = lane % S;
+  const int64_t nbags = static_cast<int64_t>(T) * B;
+  const int64_t ngroups = (nbags + G - 1) / G;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  // list offsets of group q into slot os: lanes 0 .. G copy cold_off[q G + l]
+  auto stage_off = [&](int64_t q, int os) {
+    if (q >= ngroups) return;  // warp-uniform
+    if (lane <= G) {
+      const int64_t bb = q * G + lane;
+      const bool v = bb <= nbags;
+      cp_async4(&cp.off[os][lane], cold_off + (v ? bb : 0), v);
+    }
+  };
+  // the first S keys of each bag of group q (offsets in slot os) into slot ks
+  auto stage_keys = [&](int64_t q, int os, int ks) {
+    if (q >= ngroups) return;
+    const bool live = q * G + g < nbags;
+    const uint32_t s = cp.off[os][g];
+    const uint32_t e = cp.off[os][g + 1];
+    const bool v = live && s + static_cast<uint32_t>(sl) < e;
+    const uint32_t at = v ? s + static_cast<uint32_t>(sl) : 0u;
+    cp_async4(&cp.key[ks][lane], keys + at, v);
+    if (kWeighted) cp_async4(&cp.w[ks][lane], psw + at, v);
+  };
+  const int64_t q0 = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  stage_off(q0, 0);
+  cp_async_commit();
+  stage_off(q0 + stride, 1);
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncwarp();
+  stage_keys(q0, 0, 0);
+  cp_async_commit();
+  for (uint32_t it = 0;; ++it) {
+    const int64_t q = q0 + static_cast<int64_t>(it) * stride;
+    if (q >= ngroups) break;
+    const int os0 = static_cast<int>(it % 3u), ks0 = static_cast<int>(it & 1u);
+    const int os1 = os0 == 2 ? 0 : os0 + 1, os2 = os1 == 2 ? 0 : os1 + 1;
+    __syncwarp();  // every lane is done reading the slots refilled below
+    stage_off(q + 2 * stride, os2);
+    cp_async_commit();
+    cp_async_wait<1>();  // group q + 1's offsets and group q's keys are in
+    __syncwarp();
+    stage_keys(q + stride, os1, ks0 ^ 1);
+    cp_async_commit();
+
+    const int64_t bag = q * G + g;  // this group's bag
+    const bool live = bag < nbags;
+    const int t = live ? static_cast<int>(bag / B) : 0;
+    const int64_t b = bag - static_cast<int64_t>(t) * B;
+    const int64_t d0 = __ldg(D_offsets + t);
+    const int D = static_cast<int>(__ldg(D_offsets + t + 1) - d0);
+    const int64_t h0 = __ldg(hash_base + t);
+    const int64_t E = __ldg(hash_base + t + 1) - h0;
+    const __half* Wt = W + __ldg(w_offsets + t);
+    const bool add = live && hot_n && D <= kHotMaxD && hot_n[t] != 0;
+    const int64_t s = live ? static_cast<int64_t>(cp.off[os0][g]) : 0;
+    const int64_t e = live ? static_cast<int64_t>(cp.off[os0][g + 1]) : 0;
+    float* orow = out + b * total_D + d0;
+    const int nvec = D >> 3;
+    int nvec_max = nvec;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) nvec_max = max(nvec_max, __shfl_xor_sync(kFull, nvec_max, o));
+    for (int vec0 = 0; vec0 < nvec_max; vec0 += S) {  // warp-uniform
+      const int vec = vec0 + sl;
+      const bool col_ok = live && vec < nvec;
+      const int col = col_ok ? vec * 8 : 0;
+      float acc[8];
+      if (add && col_ok) {
+        const float4 o0 = reinterpret_cast<const float4*>(orow + col)[0];
+        const float4 o1 = reinterpret_cast<const float4*>(orow + col)[1];
+        acc[0] = o0.x; acc[1] = o0.y; acc[2] = o0.z; acc[3] = o0.w;
+        acc[4] = o1.x; acc[5] = o1.y; acc[6] = o1.z; acc[7] = o1.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      }
+      int64_t p = s;
+      // the first batch of keys is in shared memory (zero past the bag)
+      uint32_t nx_key = cp.key[ks0][lane];
+      float nx_w = kWeighted ? cp.w[ks0][lane] : 0.f;
+      for (;;) {
+        const int cnt = static_cast<int>(e - p < S ? (e - p > 0 ? e - p : 0) : S);
+        int cmax = cnt;
+#pragma unroll
+        for (int o = S; o < 32; o <<= 1) cmax = max(cmax, __shfl_xor_sync(kFull, cmax, o));
+        if (cmax == 0) break;  // warp-uniform
+        const uint32_t key = nx_key;
+        const float w_in = nx_w;
+        if (p + S + sl < e) {
+          nx_key = __ldg(keys + p + S + sl);
+          if (kWeighted) nx_w = __ldg(psw + p + S + sl);
+        }
+        const __half* my_row = reinterpret_cast<const __half*>(g_zero_row);
+        float my_w = 0.f;
+        if (sl < cnt) {
+          const int64_t r = static_cast<int64_t>(key) - h0;
+          if (r >= 0 && r < E) {
+            my_row = Wt + r * D;
+            if (kWeighted) my_w = w_in;
+          }
+        }
+        const uint64_t my_addr = reinterpret_cast<uint64_t>(my_row);
+        const uint32_t my_lo = static_cast<uint32_t>(my_addr);
+        const uint32_t my_hi = static_cast<uint32_t>(my_addr >> 32);
+#pragma unroll
+        for (int u0 = 0; u0 < S; u0 += U) {
+          if (u0 >= cmax) break;  // warp-uniform
+          uint4 v[U];
+          float wv[U];
+#pragma unroll
+          for (int uu = 0; uu < U; ++uu) {
+            const int src = g * S + u0 + uu;  // lane of this group holding lookup u0 + uu
+            const uint64_t ad = static_cast<uint64_t>(__shfl_sync(kFull, my_lo, src)) |
+                                (static_cast<uint64_t>(__shfl_sync(kFull, my_hi, src)) << 32);
+            if (kWeighted) wv[uu] = __shfl_sync(kFull, my_w, src);
+            v[uu] = ldg_u4(reinterpret_cast<const __half*>(ad) + col);
+          }
+#pragma unroll
+          for (int uu = 0; uu < U; ++uu) acc_row8<kBf16, kWeighted>(acc, v[uu], kWeighted ? wv[uu] : 1.f);
+        }
+        p += S;
+      }
+      if (col_ok) {
+        if (inv_len) {  // mean pooling: this kernel writes every bag last
+          const float sc = __ldg(inv_len + bag);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] *= sc;
+        }
+        float4* o = reinterpret_cast<float4*>(orow + vec * 8);
+        __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+      }
+    }
+  }
+  cp_async_wait<0>();  // no copy outlives the block's shared memory
+}
+
 // Mean pooling's factor of every bag, from its offsets clamped as every
 // kernel reads them: 1/L for L > 1 lookups (rows out of range included), else 1.
 template <typename IndexT>
@@ -373,6 +543,9 @@ cudaError_t launch_cold_s(const Launch& L, const __half* W, const uint32_t* keys
   const int warps = 8;
   int64_t blocks = (tasks + warps - 1) / warps;
   if (blocks > (1 << 22)) blocks = 1 << 22;
+  // persistent warps for the pipelined kernel: the CTAs the SMs hold at once
+  if (TBE_COLD_PIPE && blocks > static_cast<int64_t>(L.num_sms) * TBE_FWD_MINB)
+    blocks = static_cast<int64_t>(L.num_sms) * TBE_FWD_MINB;
   if (blocks < 1) blocks = 1;
   auto go = [&](auto kernel) {
     probe_begin(TBE_PROBE_FORWARD_COLD, L.s);
@@ -383,6 +556,15 @@ cudaError_t launch_cold_s(const Launch& L, const __half* W, const uint32_t* keys
     probe_end(TBE_PROBE_FORWARD_COLD, L.s);
   };
   const bool bf16 = d->weights_dtype == TBE_DT_BF16;
+#if TBE_COLD_PIPE
+  if (psw) {
+    if (bf16) go(forward_cold_piped_kernel<S, true, true>);
+    else go(forward_cold_piped_kernel<S, true, false>);
+  } else {
+    if (bf16) go(forward_cold_piped_kernel<S, false, true>);
+    else go(forward_cold_piped_kernel<S, false, false>);
+  }
+#else
   if (psw) {
     if (bf16) go(forward_cold_kernel<S, true, true>);
     else go(forward_cold_kernel<S, true, false>);
@@ -390,6 +572,7 @@ cudaError_t launch_cold_s(const Launch& L, const __half* W, const uint32_t* keys
     if (bf16) go(forward_cold_kernel<S, false, true>);
     else go(forward_cold_kernel<S, false, false>);
   }
+#endif
   return cudaGetLastError();
 }
 

@@ -248,7 +248,10 @@ __global__ void __launch_bounds__(256)
                                       static_cast<uint64_t>(E);
         bad |= inside && !ok;
         const uint32_t key = h0_32 + static_cast<uint32_t>(r[u]);
-        const int slot = ok && nh ? hot_lookup(sm.hash, m1, m2, key) : -1;
+        // the probe is always in bounds and finds nothing in an empty set
+        // (every entry then holds kEmptyKey, never a key): no branch
+        const int hit = hot_lookup(sm.hash, m1, m2, key);
+        const int slot = ok ? hit : -1;
         // cold lookups go, in lookup order, to the front of the bag's own
         // range [s, e) of the sparse list
         const bool is_cold = ok && slot < 0;
@@ -598,20 +601,6 @@ __global__ void __launch_bounds__(1024)
     run += v;
   }
   if (sum_out && threadIdx.x == 0) *sum_out = agg;
-}
-
-// 16-byte asynchronous global -> shared copy; bytes beyond src_bytes are
-// zero-filled and not read from global memory.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
-  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
 template <bool kWeighted>

@@ -116,6 +116,17 @@ __device__ __forceinline__ uint32_t grab(uint32_t* c) {
   return __shfl_sync(kFull, v, 0);
 }
 
+// grab() in two halves, for loops that take their next work item one
+// iteration ahead: lane 0's atomic (grab_raw), whose result the warp reads
+// (ticket) in the next iteration, so that the atomic's round trip does not
+// stall the warp (it issues in order and would wait at the broadcast).
+__device__ __forceinline__ uint32_t grab_raw(uint32_t* c) {
+  uint32_t v = 0;
+  if (lane_id() == 0) v = atomicAdd(c, 1u);
+  return v;
+}
+__device__ __forceinline__ uint32_t ticket(uint32_t raw) { return __shfl_sync(kFull, raw, 0); }
+
 // Largest t with first[t] <= x (first has T+1 ascending entries).
 __device__ __forceinline__ int find_table(const uint32_t* first, int T, uint32_t x) {
   int lo = 0, hi = T - 1;
@@ -182,41 +193,44 @@ __device__ __forceinline__ void load_row(const UpdArgs& a, int64_t woff, int nv,
   }
 }
 
-// Four weights of a row after their Adagrad step w - lr * g / den, each
-// rounded to nearest even in the weights' own 16-bit type (bf16 when a.bf16).
+// Four weights of a row after their Adagrad step w - lr * g / den, formed as
+// fma(-g, q, w) with q = lr / den (one rounding of the quotient, then one of
+// the fused product and difference), each rounded to nearest even in the
+// weights' own 16-bit type (bf16 when a.bf16).  The row-wise step shares q
+// over the row, so a row costs one division instead of one per element.
 __device__ __forceinline__ uint2 adagrad_step4(const UpdArgs& a, uint2 raw, const float (&g)[4],
-                                               const float (&den)[4]) {
+                                               const float (&q)[4]) {
   if (a.bf16) {
     __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
     const float2 w01 = __bfloat1622float2(h[0]);
     const float2 w23 = __bfloat1622float2(h[1]);
-    h[0] = __floats2bfloat162_rn(w01.x - a.lr * g[0] / den[0], w01.y - a.lr * g[1] / den[1]);
-    h[1] = __floats2bfloat162_rn(w23.x - a.lr * g[2] / den[2], w23.y - a.lr * g[3] / den[3]);
+    h[0] = __floats2bfloat162_rn(fmaf(-g[0], q[0], w01.x), fmaf(-g[1], q[1], w01.y));
+    h[1] = __floats2bfloat162_rn(fmaf(-g[2], q[2], w23.x), fmaf(-g[3], q[3], w23.y));
   } else {
     __half2* h = reinterpret_cast<__half2*>(&raw);
     const float2 w01 = __half22float2(h[0]);
     const float2 w23 = __half22float2(h[1]);
-    h[0] = __floats2half2_rn(w01.x - a.lr * g[0] / den[0], w01.y - a.lr * g[1] / den[1]);
-    h[1] = __floats2half2_rn(w23.x - a.lr * g[2] / den[2], w23.y - a.lr * g[3] / den[3]);
+    h[0] = __floats2half2_rn(fmaf(-g[0], q[0], w01.x), fmaf(-g[1], q[1], w01.y));
+    h[1] = __floats2half2_rn(fmaf(-g[2], q[2], w23.x), fmaf(-g[3], q[3], w23.y));
   }
   return raw;
 }
 
 // Stores the four weights at element offset off after their step: 16-bit
-// weights from raw (see adagrad_step4); fp32 weights are read here and the
-// step w - lr * g / den is formed and stored in fp32.
+// weights from raw (see adagrad_step4); fp32 weights are read here and
+// fma(-g, q, w) is stored in fp32.
 __device__ __forceinline__ void store_step4(const UpdArgs& a, int64_t off, uint2 raw,
-                                            const float (&g)[4], const float (&den)[4]) {
+                                            const float (&g)[4], const float (&q)[4]) {
   if (a.f32) {
     float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.W) + off);
     float4 w = *p;
-    w.x = w.x - a.lr * g[0] / den[0];
-    w.y = w.y - a.lr * g[1] / den[1];
-    w.z = w.z - a.lr * g[2] / den[2];
-    w.w = w.w - a.lr * g[3] / den[3];
+    w.x = fmaf(-g[0], q[0], w.x);
+    w.y = fmaf(-g[1], q[1], w.y);
+    w.z = fmaf(-g[2], q[2], w.z);
+    w.w = fmaf(-g[3], q[3], w.w);
     *p = w;
   } else {
-    *reinterpret_cast<uint2*>(a.W + off) = adagrad_step4(a, raw, g, den);
+    *reinterpret_cast<uint2*>(a.W + off) = adagrad_step4(a, raw, g, q);
   }
 }
 
@@ -247,9 +261,9 @@ __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4
         m.y = fmaf(g[c][1], g[c][1], m.y);
         m.z = fmaf(g[c][2], g[c][2], m.z);
         m.w = fmaf(g[c][3], g[c][3], m.w);
-        const float den[4] = {sqrtf(m.x) + a.eps, sqrtf(m.y) + a.eps, sqrtf(m.z) + a.eps,
-                              sqrtf(m.w) + a.eps};
-        store_step4(a, woff + vec * 4, w_raw[c], g[c], den);
+        const float q[4] = {a.lr / (sqrtf(m.x) + a.eps), a.lr / (sqrtf(m.y) + a.eps),
+                            a.lr / (sqrtf(m.z) + a.eps), a.lr / (sqrtf(m.w) + a.eps)};
+        store_step4(a, woff + vec * 4, w_raw[c], g[c], q);
         *reinterpret_cast<float4*>(mrow + vec * 4) = m;
       }
     }
@@ -265,12 +279,12 @@ __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4
   for (int off = 1; off < S; off <<= 1) ss += __shfl_xor_sync(kFull, ss, off);
   if (!active) return;
   const float m_new = m_old + ss / static_cast<float>(D);
-  const float denom = sqrtf(m_new) + a.eps;
-  const float den[4] = {denom, denom, denom, denom};
+  const float qr = a.lr / (sqrtf(m_new) + a.eps);
+  const float q[4] = {qr, qr, qr, qr};
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
     const int vec = sl + c * S;
-    if (vec < nv) store_step4(a, woff + vec * 4, w_raw[c], g[c], den);
+    if (vec < nv) store_step4(a, woff + vec * 4, w_raw[c], g[c], q);
   }
   if (sl == 0) a.momentum[key] = m_new;
 }
@@ -281,9 +295,12 @@ __device__ __forceinline__ void adagrad_apply(const UpdArgs& a, float (&g)[NC][4
 struct ShortTask {
   int t;       // table, -1 when there is no task
   int nv;      // float4 vectors per gradient row
-  uint32_t p0; // this lane group's first pair
-  uint32_t np; // and pair count (0: no run, or a long run)
+  uint32_t p0; // this lane group's pairs [p0, p1) (none: no run)
+  uint32_t p1;
   uint32_t key;
+  // The pair count.  Read where it is used: the loads of p0 and p1 then
+  // need not have arrived when the task is fetched.
+  __device__ __forceinline__ uint32_t np() const { return p1 - p0; }
 };
 
 __device__ __forceinline__ ShortTask fetch_task(const UpdArgs& a, const Meta& m, uint32_t task,
@@ -292,7 +309,8 @@ __device__ __forceinline__ ShortTask fetch_task(const UpdArgs& a, const Meta& m,
   if (task >= ntasks) return st;
   const int t = find_table(m.tasks, a.T, task);
   const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
-  if (D < 8 || D > kMaxD || (D & 7)) return st;  // widths the vector path cannot move
+  // widths the vector path cannot move, or columns off the 32-byte grid
+  if (D < 8 || D > kMaxD || (D & 7) || (m.d_off[t] & 7)) return st;
   st.t = t;
   st.nv = D >> 2;
   const int S = update_lanes(st.nv);
@@ -300,7 +318,7 @@ __device__ __forceinline__ ShortTask fetch_task(const UpdArgs& a, const Meta& m,
   const uint32_t j = m.runs[t] + (task - m.tasks[t]) * G + lane_id() / S;
   if (j < m.runs[t + 1]) {
     st.p0 = __ldg(a.run_pairs + j);
-    st.np = __ldg(a.run_pairs + j + 1) - st.p0;
+    st.p1 = __ldg(a.run_pairs + j + 1);
     st.key = __ldg(a.unique_keys + j);
   }
   return st;
@@ -323,7 +341,7 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, cons
   const uint32_t key = st.key;
   // runs of kMediumRun pairs or more belong to medium_runs_kernel and the
   // chunked path
-  const uint32_t np = st.np >= static_cast<uint32_t>(kMediumRun) ? 0u : st.np;
+  const uint32_t np = st.np() >= static_cast<uint32_t>(kMediumRun) ? 0u : st.np();
   const bool active = np > 0;
   const int64_t woff = m.w_off[t] + (active ? (static_cast<int64_t>(key) - m.hb[t]) * D : 0);
   uint2 w_raw[NC];
@@ -353,6 +371,129 @@ __device__ __forceinline__ void short_task(const UpdArgs& a, const Meta& m, cons
 #pragma unroll
       for (int uu = 0; uu < U; ++uu) fma_rows<NC>(acc, v[uu], wv[uu]);
     }
+  }
+  adagrad_apply<S, NC, kEw>(a, acc, D, key, woff, w_raw, m_old, active);
+}
+
+// ------------------------------------------------------ short runs, piped
+// The short-run kernel's tasks (without per-sample weights) through a
+// software pipeline per warp whose intermediate data lives in shared
+// memory, not registers: while task i is updated, the run data of task i + 2
+// and the pair data of task i + 1 are copied there by cp.async (4-byte
+// copies, no registers held while they are in flight), and the index of task
+// i + 3 is taken.  A task of the tables whose rows take lane groups of S = 8
+// (5 to 32 float4 vectors) then waits for its gradient rows only; other
+// widths run short_task as it is.  Measured on GB300 (hot-row recipe, short
+// runs): 0.618 ms with the register path, 0.567 ms piped.  Per-sample
+// weights would add a dependent load of the weights to each pair; those
+// launches keep the register path (0.48 ms against 0.57 ms piped, weighted
+// recipe), as does a variant that gathered the four runs' rows as one stream
+// with a lane per vector (0.81 ms: the per-row accumulator choice and the
+// per-run reductions cost more instructions than the latency it saved).
+#ifndef TBE_SHORT_PIPE
+#define TBE_SHORT_PIPE 1
+#endif
+static_assert(kMediumRun <= 16, "a short run has at most 15 pairs");
+
+struct ShortPipe {             // one per warp
+  uint32_t run[3][16][4];      // slot, run of the task (G = 32 / S <= 16): p0, p1, key
+  uint32_t bag[2][4][16];      // slot, run (four for S = 8), pair: its bag
+  uint32_t start[2][4][16];    // and its first lookup; start[np] is the run's end
+};
+
+// Table of a task, and whether the vector path can move its rows.
+__device__ __forceinline__ bool task_table(const UpdArgs& a, const Meta& m, uint32_t task, int* t,
+                                           int* D) {
+  *t = find_table(m.tasks, a.T, task);
+  *D = static_cast<int>(m.d_off[*t + 1] - m.d_off[*t]);
+  return *D >= 8 && *D <= kMaxD && !(*D & 7) && !(m.d_off[*t] & 7);
+}
+
+// Run data of task `task` into run slot rs: lane l < G copies run j0 + l.
+__device__ __forceinline__ void pipe_runs(const UpdArgs& a, const Meta& m, uint32_t task,
+                                          uint32_t ntasks, uint32_t (*rs)[4]) {
+  if (task >= ntasks) return;  // warp-uniform
+  int t, D;
+  const bool ok = task_table(a, m, task, &t, &D);
+  const uint32_t G = 32u / static_cast<uint32_t>(update_lanes(D >> 2));
+  const uint32_t l = lane_id();
+  if (l < G) {
+    const uint32_t j = m.runs[t] + (task - m.tasks[t]) * G + l;
+    const bool v = ok && j < m.runs[t + 1];
+    const uint32_t jj = v ? j : 0u;
+    cp_async4(&rs[l][0], a.run_pairs + jj, v);
+    cp_async4(&rs[l][1], a.run_pairs + jj + 1, v);
+    cp_async4(&rs[l][2], a.unique_keys + jj, v);
+  }
+}
+
+// Pair data of an S = 8 task (run slot rs, complete) into pair slot
+// (bag, start): lane (g, sl) copies pairs sl and sl + 8 of run g.
+__device__ __forceinline__ void pipe_pairs(const UpdArgs& a, const Meta& m, uint32_t task,
+                                           uint32_t ntasks, const uint32_t (*rs)[4],
+                                           uint32_t (*bag)[16], uint32_t (*start)[16]) {
+  if (task >= ntasks) return;
+  int t, D;
+  if (!task_table(a, m, task, &t, &D)) return;
+  const int nv = D >> 2;
+  if (nv <= 4 || nv > 32) return;  // not an S = 8 task (warp-uniform)
+  const uint32_t g = lane_id() >> 3, sl = lane_id() & 7u;
+  const uint32_t p0 = rs[g][0];
+  uint32_t np = rs[g][1] - p0;
+  if (np >= static_cast<uint32_t>(kMediumRun)) np = 0u;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t k = sl + 8u * h;
+    const bool vb = k < np, vs = np > 0 && k <= np;
+    cp_async4(&bag[g][k], a.pair_bags + (vb ? p0 + k : 0u), vb);
+    cp_async4(&start[g][k], a.pair_starts + (vs ? p0 + k : 0u), vs);
+  }
+}
+
+// Coefficient of pair k of a run: its lookup count (as load_pair forms it).
+__device__ __forceinline__ float pipe_coef(const uint32_t* start, uint32_t k) {
+  return static_cast<float>(start[k + 1] - start[k]);
+}
+
+// S = 8 lane groups (rows of 5 to 32 vectors), pair data from the pipe.
+template <int NC, bool kEw>
+__device__ __forceinline__ void short_task_piped(const UpdArgs& a, const Meta& m, int t,
+                                                 const uint32_t (*rs)[4], const uint32_t (*bag)[16],
+                                                 const uint32_t (*start)[16]) {
+  constexpr int S = 8;
+  constexpr int U = TBE_SHORT_VECS / NC > 0 ? TBE_SHORT_VECS / NC : 1;
+  const int g = static_cast<int>(lane_id()) >> 3;
+  const int64_t d0 = m.d_off[t];
+  const int D = static_cast<int>(m.d_off[t + 1] - d0);
+  const int nv = D >> 2;
+  const uint32_t p0 = rs[g][0];
+  const uint32_t key = rs[g][2];
+  uint32_t np = rs[g][1] - p0;
+  if (np >= static_cast<uint32_t>(kMediumRun)) np = 0u;
+  const bool active = np > 0;
+  const int64_t woff = m.w_off[t] + (active ? (static_cast<int64_t>(key) - m.hb[t]) * D : 0);
+  uint2 w_raw[NC];
+  load_row<S, NC>(a, woff, nv, w_raw, active);
+  const float m_old = (active && !kEw) ? a.momentum[key] : 0.f;
+  const uint32_t max_np = __reduce_max_sync(kFull, np);
+  float acc[NC][4];
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[c][i] = 0.f;
+  for (uint32_t k0 = 0; k0 < max_np; k0 += U) {
+    float4 v[U][NC];
+    float w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool has = k0 + u < np;
+      const uint32_t k = has ? k0 + u : 0u;  // in-bounds index either way
+      const uint32_t b = has ? bag[g][k] : 0xffffffffu;
+      w[u] = has ? pipe_coef(start[g], k) : 0.f;
+      gather_row<S, NC>(a, d0, nv, b, v[u], b < static_cast<uint32_t>(a.B));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) fma_rows<NC>(acc, v[u], w[u]);
   }
   adagrad_apply<S, NC, kEw>(a, acc, D, key, woff, w_raw, m_old, active);
 }
@@ -446,7 +587,8 @@ __global__ void __launch_bounds__(256, kNarrow ? 3 : 2)
     }
     const int t = lo;
     const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
-    if (D < 8 || D > kMaxD || (D & 7)) continue;  // widths the vector path cannot move
+    // widths the vector path cannot move, or columns off the 32-byte grid
+    if (D < 8 || D > kMaxD || (D & 7) || (m.d_off[t] & 7)) continue;
     const int nv = D >> 2;
     if (nv <= 4) warp_run<4, 1, kWeighted, kEw>(a, m, t, p0, np, key);
     else if (nv <= 8) warp_run<8, 1, kWeighted, kEw>(a, m, t, p0, np, key);
@@ -463,11 +605,83 @@ __global__ void __launch_bounds__(256, TBE_SHORT_MINB) short_runs_kernel(UpdArgs
   __shared__ MetaSmem msm;
   const Meta m = load_meta(a, msm, true);
   const uint32_t ntasks = a.counters[kCntTasks];
+  if constexpr (!kWide && !kWeighted && TBE_SHORT_PIPE) {
+    __shared__ ShortPipe pipes[8];
+    ShortPipe& sp = pipes[threadIdx.x >> 5];
+#if TBE_DYNAMIC_RUNS
+    auto take = [&]() { return grab_raw(a.cursors); };
+    auto index = [&](uint32_t raw) { return ticket(raw); };
+#else
+    const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
+    uint32_t stride_task = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    auto take = [&]() {
+      const uint32_t v = stride_task;
+      stride_task += warps;
+      return v;
+    };
+    auto index = [&](uint32_t raw) { return raw; };
+#endif
+    // prologue: run data of tasks 0 and 1, pair data of task 0
+    uint32_t task0 = index(take());
+    pipe_runs(a, m, task0, ntasks, sp.run[0]);
+    cp_async_commit();
+    uint32_t task1 = index(take());
+    pipe_runs(a, m, task1, ntasks, sp.run[1]);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
+    pipe_pairs(a, m, task0, ntasks, sp.run[0], sp.bag[0], sp.start[0]);
+    cp_async_commit();
+    uint32_t raw = take();
+    int rs0 = 0, ps0 = 0;  // slots of task 0
+    while (task0 < ntasks) {
+      __syncwarp();  // every lane is done reading the slots refilled below
+      const uint32_t task2 = index(raw);
+      raw = take();
+      const int rs1 = rs0 == 2 ? 0 : rs0 + 1, rs2 = rs1 == 2 ? 0 : rs1 + 1;
+      pipe_runs(a, m, task2, ntasks, sp.run[rs2]);
+      cp_async_commit();
+      cp_async_wait<1>();  // task 1's run data and task 0's pair data are in
+      __syncwarp();
+      pipe_pairs(a, m, task1, ntasks, sp.run[rs1], sp.bag[ps0 ^ 1], sp.start[ps0 ^ 1]);
+      cp_async_commit();
+      int t, D;
+      if (task_table(a, m, task0, &t, &D)) {
+        const int nv = D >> 2;
+        const uint32_t (*rs)[4] = sp.run[rs0];
+        if (nv > 4 && nv <= 32) {
+          if (nv <= 8) short_task_piped<1, kEw>(a, m, t, rs, sp.bag[ps0], sp.start[ps0]);
+          else if (nv <= 16) short_task_piped<2, kEw>(a, m, t, rs, sp.bag[ps0], sp.start[ps0]);
+          else short_task_piped<4, kEw>(a, m, t, rs, sp.bag[ps0], sp.start[ps0]);
+        } else if (nv <= 128) {
+          ShortTask st;
+          st.t = t;
+          st.nv = nv;
+          const int grp = static_cast<int>(lane_id()) / update_lanes(nv);
+          st.p0 = rs[grp][0];
+          st.p1 = rs[grp][1];
+          st.key = rs[grp][2];
+          if (nv <= 2) short_task<2, 1, false, kEw>(a, m, st);
+          else if (nv <= 4) short_task<4, 1, false, kEw>(a, m, st);
+          else if (nv <= 64) short_task<16, 4, false, kEw>(a, m, st);
+          else short_task<32, 4, false, kEw>(a, m, st);
+        }
+      }
+      task0 = task1;
+      task1 = task2;
+      rs0 = rs1;
+      ps0 ^= 1;
+    }
+    cp_async_wait<0>();  // no copy outlives the block's shared memory
+    return;
+  }
 #if TBE_DYNAMIC_RUNS
   uint32_t task = grab(a.cursors);
   ShortTask cur = fetch_task(a, m, task, ntasks);
+  uint32_t raw = grab_raw(a.cursors);  // the next task's index, read next iteration
   while (task < ntasks) {
-    const uint32_t task_next = grab(a.cursors);
+    const uint32_t task_next = ticket(raw);
+    raw = grab_raw(a.cursors);
     const ShortTask next = fetch_task(a, m, task_next, ntasks);  // one task ahead
     task = task_next;
 #else
@@ -678,7 +892,7 @@ __global__ void __launch_bounds__(256, TBE_LONG_MINB) long_chunks_kernel(UpdArgs
     const LongRunInfo ri = a.long_info[cd.run];
     const int t = static_cast<int>(ri.table);
     const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
-    if (D < 8 || D > kMaxD || (D & 7)) continue;
+    if (D < 8 || D > kMaxD || (D & 7) || (m.d_off[t] & 7)) continue;
     const int nv = D >> 2;
     if ((nv > 128) != kWide) continue;
     if (kWide) long_chunk<32, 8, kWeighted, kEw>(a, m, cd, ri, two_launch);
@@ -714,7 +928,7 @@ __global__ void __launch_bounds__(256, 3) long_finish_kernel(UpdArgs a) {
     const LongRunInfo ri = a.long_info[k];
     const int t = static_cast<int>(ri.table);
     const int D = static_cast<int>(m.d_off[t + 1] - m.d_off[t]);
-    if (D < 8 || D > kMaxD || (D & 7)) continue;
+    if (D < 8 || D > kMaxD || (D & 7) || (m.d_off[t] & 7)) continue;
     const int nv = D >> 2;
     if ((nv > 128) != kWide) continue;
     if (kWide) finish_run<32, 8, kEw>(a, m, ri);
@@ -746,7 +960,7 @@ __global__ void __launch_bounds__(256)
       hot_cnt[blockIdx.x] == 0)
     return;  // uniform over the CTA
   const int D = static_cast<int>(a.D_offsets[t + 1] - a.D_offsets[t]);
-  if (D > kHotMaxD || (D & 7)) return;
+  if (D > kHotMaxD || (D & 7) || (a.D_offsets[t] & 7)) return;
   const int warp = threadIdx.x >> 5;
   const int lane = static_cast<int>(lane_id());
   const int nv = D >> 2;
