@@ -59,6 +59,8 @@ def parse():
                    help="bags of table 0 in the CPU-oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-copy-streams", type=int, default=1,
+                   help="copy streams sharing each step's host-to-device uploads in the e2e loop")
     p.add_argument("--batches", type=int, default=4,
                    help="distinct batches of the recipe cycled through the steps")
     p.add_argument("--configs", default="tiny,small,mixed,weighted,hot",
@@ -176,10 +178,10 @@ ROOFLINE_KERNEL_SOURCES = ("update.cu", "common.cuh")
 # the sha1 of the kernel's sources it was taken on: the bench scales it by
 # the pairs of a full launch while the sources are unchanged, else reports
 # null.  None until a capture of the current sources exists.
-TRAFFIC_RECORD = {"bytes_per_pair": 496.33, "source_sha1": "3882ed91e82eb354",
+TRAFFIC_RECORD = {"bytes_per_pair": 495.54, "source_sha1": "902dae0c8b232161",
                   "capture": "hot-row recipe reduced to one table (E=1e7, D=128, B=131072), "
                              "two timed launches, dram__bytes_read.sum + dram__bytes_write.sum "
-                             "= 219.6 MB per launch over 442 434 short-run pairs"}
+                             "= 219.2 MB per launch over 442 434 short-run pairs"}
 
 
 def source_sha1():
@@ -527,22 +529,35 @@ def run_native(args, world, rank, local):
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         slots = [(torch.empty_like(w.indices), torch.empty_like(w.offsets),
                   torch.empty_like(w.grad_out)) for _ in range(2)]
-        up, down = torch.cuda.Stream(), torch.cuda.Stream()
-        copied = [torch.cuda.Event() for _ in range(2)]
+        # the uploads are split into contiguous pieces on several copy
+        # streams, so that several copy engines share the host link
+        nup = max(1, args.e2e_copy_streams)
+        ups = [torch.cuda.Stream() for _ in range(nup)]
+        down = torch.cuda.Stream()
+        copied = [[torch.cuda.Event() for _ in range(nup)] for _ in range(2)]
         consumed = [torch.cuda.Event() for _ in range(2)]
         fwd_done, out_read = torch.cuda.Event(), torch.cuda.Event()
+
+        def pieces(t):
+            f = t.view(-1)
+            step = (f.numel() + nup - 1) // nup
+            return [f[i * step:(i + 1) * step] for i in range(nup)]
 
         def e2e_step(k):
             d_idx, d_off, d_grad = slots[k % 2]
             h_idx, h_off, h_grad = hb[k % len(hb)]
-            with torch.cuda.stream(up):
-                if k >= 2:
-                    up.wait_event(consumed[k % 2])
-                d_idx.copy_(h_idx, non_blocking=True)
-                d_off.copy_(h_off, non_blocking=True)
-                d_grad.copy_(h_grad, non_blocking=True)
-                copied[k % 2].record(up)
-            stream.wait_event(copied[k % 2])
+            parts = [list(zip(pieces(d), pieces(h)))
+                     for d, h in ((d_idx, h_idx), (d_off, h_off), (d_grad, h_grad))]
+            for j, up in enumerate(ups):
+                with torch.cuda.stream(up):
+                    if k >= 2:
+                        up.wait_event(consumed[k % 2])
+                    for pr in parts:
+                        if pr[j][0].numel():
+                            pr[j][0].copy_(pr[j][1], non_blocking=True)
+                    copied[k % 2][j].record(up)
+            for ev in copied[k % 2]:
+                stream.wait_event(ev)
             if k >= 1:
                 stream.wait_event(out_read)  # the previous output was read back
             tbe.tbe_preprocess(st.desc, d_idx, d_off, None, st.ws)
@@ -563,7 +578,8 @@ def run_native(args, world, rank, local):
         a = torch.cuda.Event(enable_timing=True)
         bev = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        up.wait_event(a)
+        for up in ups:
+            up.wait_event(a)
         down.wait_event(a)
         for k in range(args.steps):
             e2e_step(k + 2 * args.warmup)  # the slot pattern continues past the warm-up
@@ -579,6 +595,7 @@ def run_native(args, world, rank, local):
         result["h2d"] = (hidx.numel() * hidx.element_size() + hoff.numel() * hoff.element_size()
                          + hgrad.numel() * 4)
         result["d2h"] = h_out.numel() * 4
+        result["e2e_copy_streams"] = nup
         del hb, slots
     return result
 
@@ -795,7 +812,8 @@ def main():
     if "e2e_ms" in r:
         line["e2e"] = {"value": r["e2e_lookups"] * world / (r["e2e_ms"] / 1e3),
                        "unit": "lookups/s", "h2d_bytes_per_step": r["h2d"],
-                       "d2h_bytes_per_step": r["d2h"]}
+                       "d2h_bytes_per_step": r["d2h"],
+                       "copy_streams": r["e2e_copy_streams"]}
     if not args.no_configs and not reduced and world == 1 and args.weights == "fp16" \
             and not ew and args.pooling == "sum":
         import table_embedding_bag_gb300 as tbe

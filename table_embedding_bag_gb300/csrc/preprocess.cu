@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(256)
                         int8_t* __restrict__ hot_scale, uint8_t* __restrict__ tile_kind,
                         uint32_t* __restrict__ hot_cnt, uint32_t* __restrict__ bag_cold,
                         uint32_t* __restrict__ tile_cold, uint32_t* __restrict__ sp_keys,
-                        uint32_t* __restrict__ sp_vals, float* __restrict__ sp_psw, int* status) {
+                        float* __restrict__ sp_psw, int* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   ExpandSmem<IndexT, kWeighted>& sm = *reinterpret_cast<ExpandSmem<IndexT, kWeighted>*>(smem_raw);
   const TileInfo ti = tile_info(B);
@@ -227,9 +227,7 @@ __global__ void __launch_bounds__(256)
     const IndexT* __restrict__ ib = indices + s;
     const float* __restrict__ pb = kWeighted ? psw + s : nullptr;
     uint32_t* __restrict__ kb = sp_keys + s;
-    uint32_t* __restrict__ vb = sp_vals + s;
     float* __restrict__ wb = kWeighted ? sp_psw + s : nullptr;
-    const uint32_t bag_in_table = static_cast<uint32_t>(ti.b0 + lb);
     const uint32_t h0_32 = static_cast<uint32_t>(h0);
     for (uint32_t base = 0; base < len; base += 32 * kExpandLoads) {
       IndexT r[kExpandLoads];
@@ -256,10 +254,9 @@ __global__ void __launch_bounds__(256)
         // range [s, e) of the sparse list
         const bool is_cold = ok && slot < 0;
         const unsigned cm = __ballot_sync(kFull, is_cold);
-        if (is_cold) {
+        if (is_cold) {  // the bag of each entry is its range's: expand_write adds it
           const uint32_t at = cold + __popc(cm & lt);
           kb[at] = key;
-          vb[at] = bag_in_table;
           if (kWeighted) wb[at] = __ldg(pb + o);
         }
         cold += __popc(cm);
@@ -379,17 +376,18 @@ __global__ void __launch_bounds__(256)
   if (status && __any_sync(kFull, bad) && lane == 0) set_status(status, TBE_ERR_INDEX_RANGE);
 }
 
-// Compaction of the cold lookups: each bag's cold entries, which the count
+// Compaction of the cold lookups: each bag's cold keys, which the count
 // kernel left at the front of the bag's own range of the sparse list, move to
 // the dense list at the bag's first cold entry (tile base + in-tile prefix of
-// the per-bag counts), keeping lookup order; cold_off gets each bag's first
+// the per-bag counts), keeping lookup order, each with its bag (the range's
+// own, so the sparse list holds no bags); cold_off gets each bag's first
 // entry.  Only the cold entries are read, not the indices.
 template <typename IndexT, bool kWeighted>
 __global__ void __launch_bounds__(256)
     expand_write_kernel(const IndexT* __restrict__ offsets, int64_t n, int B,
                         const uint32_t* __restrict__ bag_cold,
                         const uint32_t* __restrict__ tile_base, uint32_t* __restrict__ cold_off,
-                        const uint32_t* __restrict__ sp_keys, const uint32_t* __restrict__ sp_vals,
+                        const uint32_t* __restrict__ sp_keys,
                         const float* __restrict__ sp_psw, uint32_t* __restrict__ keys,
                         uint32_t* __restrict__ vals, float* __restrict__ psw_out) {
   __shared__ uint32_t bag_base[kHotTileBags];
@@ -431,9 +429,10 @@ __global__ void __launch_bounds__(256)
     const int64_t room = n - static_cast<int64_t>(pos);
     const uint32_t c = static_cast<uint32_t>(
         min(static_cast<int64_t>(bag_cold[bag]), room > 0 ? room : int64_t(0)));
+    const uint32_t bag_in_table = static_cast<uint32_t>(ti.b0 + lb);
     for (uint32_t i = lane; i < c; i += 32) {
       keys[pos + i] = __ldg(sp_keys + s + i);
-      vals[pos + i] = __ldg(sp_vals + s + i);
+      vals[pos + i] = bag_in_table;
       if (kWeighted) psw_out[pos + i] = __ldg(sp_psw + s + i);
     }
   }
@@ -1244,20 +1243,20 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     if (weighted)
       { probe_begin(TBE_PROBE_EXPAND_COUNT, s); expand_count_kernel<IndexT, true><<<tiles, 256, sizeof(ExpandSmem<IndexT, true>), s>>>(
           indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh8, hh, hsc, tk, hc, bc,
-          tile_cold, keys[0], vals[0], pw[0], status); note_launch(); probe_end(TBE_PROBE_EXPAND_COUNT, s); }
+          tile_cold, keys[0], pw[0], status); note_launch(); probe_end(TBE_PROBE_EXPAND_COUNT, s); }
     else
       { probe_begin(TBE_PROBE_EXPAND_COUNT, s); expand_count_kernel<IndexT, false><<<tiles, 256, sizeof(ExpandSmem<IndexT, false>), s>>>(
           indices, offsets, psw, d->hash_base, d->D_offsets, n, d->B, hs, hh8, hh, hsc, tk, hc, bc,
-          tile_cold, keys[0], vals[0], pw[0], status); note_launch(); probe_end(TBE_PROBE_EXPAND_COUNT, s); }
+          tile_cold, keys[0], pw[0], status); note_launch(); probe_end(TBE_PROBE_EXPAND_COUNT, s); }
     { capped_scan_kernel<<<1, 1024, 0, s>>>(tile_cold, W.hot_tiles, static_cast<uint32_t>(n),
                                             counters + kCntSortN); note_launch(); }
     if (weighted)
       { expand_write_kernel<IndexT, true><<<tiles, 256, 0, s>>>(
-          offsets, n, d->B, bc, tile_cold, co, keys[0], vals[0], pw[0], keys[2], vals[2],
+          offsets, n, d->B, bc, tile_cold, co, keys[0], pw[0], keys[2], vals[2],
           pw[2]); note_launch(); }
     else
       { expand_write_kernel<IndexT, false><<<tiles, 256, 0, s>>>(
-          offsets, n, d->B, bc, tile_cold, co, keys[0], vals[0], pw[0], keys[2], vals[2],
+          offsets, n, d->B, bc, tile_cold, co, keys[0], pw[0], keys[2], vals[2],
           pw[2]); note_launch(); }
   }
   // The sort chain (sort, run-length encoding, classification) goes to the
