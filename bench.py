@@ -165,42 +165,69 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# The roofline kernel: the largest steady-state share of the step's kernels in
-# the ncu launch list of this workload (distinct batches, hot set learned on
-# the batch before): the short-run update kernel of the backward.  Its
-# launches are timed live by the library's kernel probe.
-ROOFLINE_KERNEL = "short_runs_kernel (tbe_backward_rowwise_adagrad, runs of fewer than 16 pairs)"
-ROOFLINE_KERNEL_SOURCES = ("update.cu", "common.cuh")
-# DRAM bytes per short-run pair of one short_runs_kernel launch, from a
-# one-kernel ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of
-# this recipe reduced to one table (each table of the recipe is an
-# independent draw and the kernel takes the tables' runs in key order), and
-# the sha1 of the kernel's sources it was taken on: the bench scales it by
-# the pairs of a full launch while the sources are unchanged, else reports
-# null.  None until a capture of the current sources exists.
-TRAFFIC_RECORD = {"bytes_per_pair": 495.54, "source_sha1": "902dae0c8b232161",
-                  "capture": "hot-row recipe reduced to one table (E=1e7, D=128, B=131072), "
-                             "two timed launches, dram__bytes_read.sum + dram__bytes_write.sum "
-                             "= 219.2 MB per launch over 442 434 short-run pairs"}
+# The roofline kernels: the largest steady-state shares of the step's
+# kernels in the ncu launch list of this workload (distinct batches, hot set
+# learned on the batch before; --cache-control none, so that the serialised
+# per-launch times match the live probes): the expand of the preprocess
+# (15.3 %), the cold-list forward (15.0 %) and the short-run update
+# (14.6 %).  `roofline` reports the first, `roofline_kernels` the others.
+# Each is timed live by the library's kernel probe.  A traffic record holds
+# the DRAM bytes per work unit of one launch from a one-kernel ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum) of this recipe reduced to
+# one table (each table is an independent draw and the kernels take the
+# tables one after another), with the sha1 of the kernel's sources it was
+# taken on: the bench scales it by the units of a full launch while the
+# sources are unchanged, else reports null.
+ROOFLINE_DOMINANT = "expand_count_kernel"
+ROOFLINE_KERNELS = {
+    "expand_count_kernel": {
+        "what": "expand of tbe_preprocess: reads every index, writes the hot rows' byte "
+                "histogram and the cold keys",
+        "probe": "TBE_PROBE_EXPAND_COUNT", "sources": ("preprocess.cu", "common.cuh"),
+        "record": {"bytes_per_unit": 9.301, "unit": "lookup",
+                   "source_sha1": "51c846f9ce11c1b8",
+                   "capture": "hot-row recipe reduced to one table (E=1e7, D=128, B=131072), "
+                              "two launches, dram__bytes_read.sum + dram__bytes_write.sum = "
+                              "243.8 MB per launch over 26.21 M lookups"}},
+    "forward_cold_piped_kernel": {
+        "what": "cold-list forward of tbe_forward(TBE_F_PREPROCESSED): gathers the cold "
+                "rows and adds them to the hot sums",
+        "probe": "TBE_PROBE_FORWARD_COLD", "sources": ("forward.cu", "pool.cuh", "common.cuh"),
+        "record": {"bytes_per_unit": 74.03, "unit": "cold lookup",
+                   "source_sha1": "ad5f48928d886de1",
+                   "capture": "hot-row recipe reduced to one table (E=1e7, D=128, B=131072), "
+                              "two launches, dram__bytes_read.sum + dram__bytes_write.sum = "
+                              "167.6 MB per launch over 2.263 M cold lookups"}},
+    "short_runs_kernel": {
+        "what": "short-run update of tbe_backward_rowwise_adagrad (runs of fewer than 16 "
+                "pairs)",
+        "probe": "TBE_PROBE_SHORT_RUNS", "sources": ("update.cu", "common.cuh"),
+        "record": {"bytes_per_unit": 495.54, "unit": "short-run pair",
+                   "source_sha1": "902dae0c8b232161",
+                   "capture": "hot-row recipe reduced to one table (E=1e7, D=128, B=131072), "
+                              "two launches, dram__bytes_read.sum + dram__bytes_write.sum = "
+                              "219.2 MB per launch over 442 434 short-run pairs"}},
+}
 
 
-def source_sha1():
-    """First 16 hex digits of the sha1 over the roofline kernel's sources."""
+def source_sha1(files):
+    """First 16 hex digits of the sha1 over a kernel's source files."""
     import hashlib
     h = hashlib.sha1()
-    for f in ROOFLINE_KERNEL_SOURCES:
+    for f in files:
         h.update(open(os.path.join(ROOT, "table_embedding_bag_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(units):
-    """DRAM bytes of one roofline-kernel launch over `units` short-run pairs,
-    scaled from the recorded capture; None without a record of the current
+def recorded_traffic(name, units):
+    """DRAM bytes of one launch of kernel `name` over `units` work units,
+    scaled from its recorded capture; None without a record of the current
     sources."""
-    rec = TRAFFIC_RECORD
-    if rec is None or rec["source_sha1"] != source_sha1():
+    k = ROOFLINE_KERNELS[name]
+    rec = k["record"]
+    if rec is None or rec["source_sha1"] != source_sha1(k["sources"]):
         return None
-    return int(rec["bytes_per_pair"] * units)
+    return int(rec["bytes_per_unit"] * units)
 
 
 def workload_name(args, base=WORKLOAD):
@@ -227,6 +254,36 @@ def short_run_bytes(D, pairs, runs, all_runs, elementwise=False, wb=2):
     its run data (8: the kernel walks every run to pick the short ones)."""
     return (pairs * (4 + 8 + 4 * D) + runs * (2 * wb * D + momentum_bytes(D, elementwise))
             + all_runs * 8)
+
+
+def expand_bytes(w, units, per_use=True):
+    """Bytes of one expand_count_kernel launch: every index (and per-sample
+    weight) read once and each bag's offset; the hot rows' histogram row of
+    every bag of a table with hot rows written (a byte per slot, fp32 with
+    per-sample weights); each cold key (and weight) and each bag's cold count
+    written.  Per use it adds each CTA's read of its table's hot set (kHot
+    keys and places), which L2 serves after the first."""
+    nb = w.T * w.B
+    psw = w.psw is not None
+    b = (w.n * w.indices.element_size() + (nb + 1) * w.offsets.element_size()
+         + (4 * w.n if psw else 0))
+    b += units["hot_tables"] * w.B * 256 * (4 if psw else 1)
+    b += units["cold_lookups"] * (8 if psw else 4) + nb * 4
+    if per_use:
+        b += w.T * ((w.B + 127) // 128) * 256 * 8
+    return int(b)
+
+
+def cold_forward_bytes(w, units, D):
+    """Per-use bytes of one forward_cold_piped_kernel launch: per cold lookup
+    its key (4, + 4 weight) and its row (D weights); per bag its list offset
+    (4) and its fp32 output row, read and written where the bag's table has
+    hot rows (the hot forward pooled them first), else written."""
+    nb = w.T * w.B
+    wb = w.weights.element_size()
+    per = 4 + (4 if w.psw is not None else 0) + wb * D
+    return int(units["cold_lookups"] * per + (nb + 1) * 4
+               + units["hot_tables"] * w.B * 8 * D + (w.T - units["hot_tables"]) * w.B * 4 * D)
 
 
 def compulsory_bytes(w, rows_touched, index_bytes, elementwise=False):
@@ -356,8 +413,10 @@ def run_units(st, w):
     t_run = torch.searchsorted(hb[1:], uk, right=True)
     sp = short[pair_run]
     short_bag_rows = int(torch.unique(t_run[pair_run[sp]] * w.B + pb[sp]).numel())
-    hn = int(st.ws_u32(v["hot_n"], w.T).sum().item())
+    hot_n = st.ws_u32(v["hot_n"], w.T)
+    hn = int(hot_n.sum().item())
     return {"R": R, "long_runs": n_long, "long_chunks": n_chunks, "cold_lookups": n_cold,
+            "hot_tables": int((hot_n > 0).sum().item()),
             "short_runs": int(short.sum().item()), "short_pairs": int(sl[short].sum().item()),
             "long_pairs": int(sl[lng].sum().item()), "short_bag_rows": short_bag_rows,
             "hot_rows_next": hn, "hit_rate": 1.0 - n_cold / max(w.n, 1)}
@@ -499,6 +558,16 @@ def run_native(args, world, rank, local):
         units.append(run_units(st, b))
     nxt += K
     avg = {k: float(np.mean([u[k] for u in units])) for k in units[0]}
+    # the other roofline kernels timed live by the probe (2 K steps each,
+    # continuing the cycle)
+    probes = {"short_runs_kernel": (probe_launches, probe_ms)}
+    for name in ("expand_count_kernel", "forward_cold_piped_kernel"):
+        tbe.tbe_probe_set(getattr(tbe, ROOFLINE_KERNELS[name]["probe"]))
+        for j in range(2 * K):
+            st.step(batches[(nxt + j) % K])
+        nxt += 2 * K
+        probes[name] = tbe.tbe_probe_read()
+        tbe.tbe_probe_set(tbe.TBE_PROBE_OFF)
     # first step with an empty hot set (a fresh workspace's first batch)
     st.clear_hot_set()
     ce = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
@@ -512,7 +581,7 @@ def run_native(args, world, rank, local):
         "ms": ms, "ms_local": ms_local, "fwd_ms": statistics.median(fwd),
         "pre_ms": statistics.median(pre), "upd_ms": statistics.median(upd),
         "lookups": lookups, "units": avg, "units_per_batch": units, "cold_start": cold,
-        "clocks": clk, "probe_launches": probe_launches, "probe_ms": probe_ms,
+        "clocks": clk, "probe_launches": probe_launches, "probe_ms": probe_ms, "probes": probes,
         "launches": launches, "w": w, "batches": batches, "stepper": st, "next": nxt,
     }
 
@@ -742,14 +811,46 @@ def main():
     ew = args.optimizer == "elementwise"
     u = r["units"]
     wb = w.weights.element_size()
-    kb = short_run_bytes(D, u["short_pairs"], u["short_runs"], u["R"], ew, wb)
-    k_launch_ms = r["probe_ms"] / max(r["probe_launches"], 1)
-    achieved = kb / (k_launch_ms / 1e3) / 1e9
-    # compulsory bytes of the kernel: each short run's row and momentum read
-    # and written once, its pair data once, each gradient row it gathers once
+    reduced = (args.tables, args.rows, args.bags) != (None,) * 3 or args.recipe != "hot"
+
+    def kernel_entry(name, per_use, minimum, units, unit_name, model):
+        launches, total_ms = r["probes"][name]
+        launch_ms = total_ms / max(launches, 1)
+        ach = per_use / (launch_ms / 1e3) / 1e9
+        e = {"kernel": name, "what": ROOFLINE_KERNELS[name]["what"], "bound": "hbm",
+             "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+             "traffic": None if reduced else recorded_traffic(name, units),
+             "peak_source": peak_src, "bytes_model": model, "bytes_per_launch": per_use,
+             "launch_ms": launch_ms, "launches_timed": launches, "units": {unit_name: units}}
+        if minimum is not None:
+            e["compulsory_bytes_per_launch"] = minimum
+            e["compulsory_frac"] = minimum / (launch_ms / 1e3) / 1e9 / hbm
+        return e
+
+    # compulsory bytes of the short runs: each short run's row and momentum
+    # read and written once, its pair data once, each gradient row it
+    # gathers once
     k_min = (u["short_runs"] * (2 * wb * D + momentum_bytes(D, ew)) + u["R"] * 8
              + u["short_pairs"] * 12 + u["short_bag_rows"] * 4 * D)
-    reduced = (args.tables, args.rows, args.bags) != (None,) * 3 or args.recipe != "hot"
+    kernels = {
+        "expand_count_kernel": kernel_entry(
+            "expand_count_kernel", expand_bytes(w, u), expand_bytes(w, u, per_use=False), w.n,
+            "lookups", "per use: every index and offset, the histogram row of every bag of a "
+                       "table with hot rows, the cold keys and counts, each CTA's hot-set "
+                       "read"),
+        "forward_cold_piped_kernel": kernel_entry(
+            "forward_cold_piped_kernel", cold_forward_bytes(w, u, D), None, u["cold_lookups"],
+            "cold_lookups", "per use: key and row per cold lookup, list offset and output "
+                            "row read and written per bag"),
+        "short_runs_kernel": kernel_entry(
+            "short_runs_kernel", short_run_bytes(D, u["short_pairs"], u["short_runs"], u["R"],
+                                                 ew, wb),
+            k_min, u["short_pairs"], "short_pairs",
+            "per use: bag + pair start + gradient row per short-run pair, weights row r/w + "
+            "momentum per short run, run data per run"),
+    }
+    kernels["short_runs_kernel"]["units"].update(
+        {"short_runs": u["short_runs"], "runs": u["R"], "short_bag_rows": u["short_bag_rows"]})
     touched = rows_touched(w)
     cb = compulsory_bytes(w, touched, w.indices.element_size(), ew)
     t_fwd = r["pre_ms"] + r["fwd_ms"]
@@ -787,19 +888,8 @@ def main():
                                                     "fresh workspace's first batch)"),
         "runs": {k: u[k] for k in ("R", "long_runs", "long_chunks", "short_runs",
                                    "short_pairs", "long_pairs")},
-        "roofline": {"kernel": ROOFLINE_KERNEL, "bound": "hbm", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None if reduced else recorded_traffic(u["short_pairs"]),
-                     "peak_source": peak_src,
-                     "bytes_model": "per use: bag + pair start + gradient row per short-run "
-                                    "pair, weights row r/w + momentum per short run, run data "
-                                    "per run",
-                     "bytes_per_launch": kb, "launch_ms": k_launch_ms,
-                     "launches_timed": r["probe_launches"],
-                     "compulsory_bytes_per_launch": k_min,
-                     "compulsory_frac": k_min / (k_launch_ms / 1e3) / 1e9 / hbm,
-                     "units": {"short_pairs": u["short_pairs"], "short_runs": u["short_runs"],
-                               "runs": u["R"], "short_bag_rows": u["short_bag_rows"]}},
+        "roofline": kernels[ROOFLINE_DOMINANT],
+        "roofline_kernels": {k: v for k, v in kernels.items() if k != ROOFLINE_DOMINANT},
         "problem_roofline": {
             k: {"min_bytes": cb[k], "ms": t, "GBps": cb[k] / (t / 1e3) / 1e9,
                 "frac": cb[k] / (t / 1e3) / 1e9 / hbm}
