@@ -1243,15 +1243,21 @@ __global__ void __launch_bounds__(256)
 template <bool kEw>
 void launch_runs(const Launch& L, const UpdArgs& a, const uint32_t* medium, unsigned blocks,
                  bool weighted, bool wide, bool two_launch) {
-  if (weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, false, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
-  else { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, false, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  // with work cursors, the CTAs the SMs hold at once take every task: a
+  // larger grid only adds CTAs that start late and find the cursor spent
+  const unsigned sms = static_cast<unsigned>(L.num_sms);
+  const unsigned short_blocks = TBE_DYNAMIC_RUNS ? sms * TBE_SHORT_MINB : blocks;
+  const unsigned medium_blocks = TBE_DYNAMIC_RUNS ? sms * (a.max_D <= 128 ? 3u : 2u) : blocks;
+  const unsigned long_blocks = TBE_DYNAMIC_RUNS ? sms * TBE_LONG_MINB : blocks;
+  if (weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, false, kEw><<<short_blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  else { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, false, kEw><<<short_blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
   {
     const bool narrow = a.max_D <= 128;
     probe_begin(TBE_PROBE_MEDIUM_RUNS, L.s);
-    if (weighted && narrow) medium_runs_kernel<true, true, kEw><<<blocks, 256, 0, L.s>>>(a, medium);
-    else if (weighted) medium_runs_kernel<true, false, kEw><<<blocks, 256, 0, L.s>>>(a, medium);
-    else if (narrow) medium_runs_kernel<false, true, kEw><<<blocks, 256, 0, L.s>>>(a, medium);
-    else medium_runs_kernel<false, false, kEw><<<blocks, 256, 0, L.s>>>(a, medium);
+    if (weighted && narrow) medium_runs_kernel<true, true, kEw><<<medium_blocks, 256, 0, L.s>>>(a, medium);
+    else if (weighted) medium_runs_kernel<true, false, kEw><<<medium_blocks, 256, 0, L.s>>>(a, medium);
+    else if (narrow) medium_runs_kernel<false, true, kEw><<<medium_blocks, 256, 0, L.s>>>(a, medium);
+    else medium_runs_kernel<false, false, kEw><<<medium_blocks, 256, 0, L.s>>>(a, medium);
     note_launch();
     probe_end(TBE_PROBE_MEDIUM_RUNS, L.s);
   }
@@ -1261,13 +1267,13 @@ void launch_runs(const Launch& L, const UpdArgs& a, const uint32_t* medium, unsi
     if (TBE_DYNAMIC_RUNS && wide) cudaMemsetAsync(a.cursors + (c - kCntNextShort), 0, 4, L.s);
   };
   reset(kCntNextShort);
-  if (wide && weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, true, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
-  if (wide && !weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, true, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
-  if (weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, false, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
-  else { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, false, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  if (wide && weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<true, true, kEw><<<short_blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  if (wide && !weighted) { probe_begin(TBE_PROBE_SHORT_RUNS, L.s); short_runs_kernel<false, true, kEw><<<short_blocks, 256, 0, L.s>>>(a); note_launch(); probe_end(TBE_PROBE_SHORT_RUNS, L.s); }
+  if (weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, false, kEw><<<long_blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  else { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, false, kEw><<<long_blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
   reset(kCntNextLong);
-  if (wide && weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, true, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
-  if (wide && !weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, true, kEw><<<blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  if (wide && weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<true, true, kEw><<<long_blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
+  if (wide && !weighted) { probe_begin(TBE_PROBE_LONG_CHUNKS, L.s); long_chunks_kernel<false, true, kEw><<<long_blocks, 256, 0, L.s>>>(a, two_launch); note_launch(); probe_end(TBE_PROBE_LONG_CHUNKS, L.s); }
   if (two_launch) {
     { long_finish_kernel<false, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
     if (wide) { long_finish_kernel<true, kEw><<<blocks, 256, 0, L.s>>>(a); note_launch(); }
