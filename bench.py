@@ -449,6 +449,36 @@ def time_phases(st, batches, steps, warmup, arrangement="pre_in_fwd", two_launch
 CONFIG_KW = {"tiny": {}, "small": {}, "mixed": {}, "weighted": {}, "hot": {}}
 
 
+def time_graph_steps(st, batches, steps, warmup, flush=None):
+    """Median step time (ms) with each batch's whole step (preprocess,
+    forward, backward) captured once into a CUDA graph and the graphs
+    replayed in turn: the same kernels without the host's per-launch cost."""
+    K = len(batches)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    for b in batches:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                st.step(b)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    for k in range(warmup):
+        graphs[k % K].replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for k in range(steps):
+        l2_flush(flush)
+        evs[k][0].record(s)
+        graphs[k % K].replay()
+        evs[k][1].record(s)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
 def measure_configs(tbe, dev, rank, args, hbm, main=None):
     """Per recipe at its stated size: forward, backward and step ms in both
     arrangements of the preprocessing (in the forward: one preprocess serves
@@ -481,6 +511,12 @@ def measure_configs(tbe, dev, rank, args, hbm, main=None):
                       "roofline_frac": {k: cb[k] / (t / 1e3) / 1e9 / hbm for k, t in
                                         (("forward", ph["fwd_ms"]), ("backward", ph["bwd_ms"]),
                                          ("step", ph["step_ms"]))}}
+        if name in ("tiny", "small", "mixed"):
+            # launch-bound recipes: the same step replayed as a CUDA graph
+            g_ms = time_graph_steps(st, batches, steps, warm, flush=flush)
+            r["graph"] = {"sum_ms": g_ms, "lookups_per_s": w.n / (g_ms / 1e3),
+                          "note": "each batch's step captured once into a CUDA graph "
+                                  "and replayed"}
         if name in ("hot", "weighted"):
             ph2 = time_phases(st, batches, steps, warm, "pre_in_fwd", two_launch=True,
                               flush=flush, first=first)

@@ -249,7 +249,13 @@ tbe_status tbe_forward(const tbe_desc* d, const void* weights, const void* indic
  * device), so that a forward enqueued next runs concurrently with it; the
  * library's calls on this workspace order themselves against it (through
  * events), calls on other workspaces never wait on it, and reading the
- * sorted arrays directly needs a device synchronisation first.
+ * sorted arrays directly needs a device synchronisation first.  Every
+ * tbe_backward_rowwise_adagrad joins the workspace's side-stream work into
+ * its stream before it returns, so whole training steps (preprocess,
+ * forward, backward) can be captured into a CUDA graph and replayed; a
+ * capture must end with a backward (a preprocess alone leaves its sort chain
+ * unjoined), and the first call on a workspace, which creates its stream,
+ * must come before any capture.
  * Errors as tbe_forward. */
 tbe_status tbe_preprocess(const tbe_desc* d, const void* indices, const void* offsets, int64_t n,
                           const float* per_sample_weights, void* workspace, size_t ws_bytes,

@@ -18,6 +18,16 @@ void note_launch();
 void probe_begin(uint32_t kernel, cudaStream_t s);
 void probe_end(uint32_t kernel, cudaStream_t s);
 
+// An event of the flow and whether its latest record was made while its
+// stream was being captured into a CUDA graph (such a record is a
+// dependency inside that graph, not a point in any stream: a wait outside
+// the capture may not name it, and a capture may not wait on a record made
+// outside it).
+struct FlowEvent {
+  cudaEvent_t ev = nullptr;
+  bool captured = false;
+};
+
 // Side stream of one workspace (one per workspace and device, created at the
 // workspace's first use): the preprocess runs its sort chain there,
 // concurrently with the forward, and the backward its hot-row gradient,
@@ -30,7 +40,8 @@ void probe_end(uint32_t kernel, cudaStream_t s);
 // (other streams, other host threads) never wait on each other's events.
 struct SideFlow {
   cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, sorted = nullptr, hot = nullptr, done = nullptr;
+  cudaEvent_t fork = nullptr;
+  FlowEvent sorted, hot, done;
 };
 // The flow of workspace `ws` on the current device, created on first use;
 // nullptr if the stream or events could not be created (the next call
@@ -40,6 +51,13 @@ SideFlow* side_flow(const void* ws);
 SideFlow* find_side_flow(const void* ws);
 // Makes `side` wait for everything enqueued on `s` so far.
 cudaError_t fork_to(SideFlow* f, cudaStream_t s);
+// Records e on s, noting whether s is being captured.
+cudaError_t flow_record(FlowEvent& e, cudaStream_t s);
+// Makes s wait for e's latest record when both lie on the same side of a
+// capture; otherwise the wait is left out: a record made inside a graph is
+// ordered by the graph's replays on the caller's stream, and one made
+// before a capture by the synchronisation that precedes it.
+cudaError_t flow_wait(cudaStream_t s, const FlowEvent& e);
 
 // One call's launch context.
 struct Launch {

@@ -1201,9 +1201,11 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
 
   SideFlow* sf = side_flow(ws);
   if (!sf) return cudaErrorNotReady;
-  // the previous call's side work (sort chain, hot-row update) still reads
-  // the buffers this one rewrites
-  cudaError_t err = cudaStreamWaitEvent(s, sf->done, 0);
+  // the previous call's side work (sort chain, hot-set refresh) still reads
+  // the buffers this one rewrites (a record on the other side of a graph
+  // capture is not waited for: every backward joins its side work into the
+  // caller's stream before it returns)
+  cudaError_t err = flow_wait(s, sf->done);
   if (err != cudaSuccess) return err;
   err = cudaMemsetAsync(counters, 0, kNumCounters * sizeof(uint32_t), s);
   if (err != cudaSuccess) return err;
@@ -1365,7 +1367,7 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
         reinterpret_cast<uint32_t*>(ws + W.chunk_band), band_count,
         reinterpret_cast<ChunkDesc*>(ws + W.chunk_order)); note_launch(); }
   }
-  err = cudaEventRecord(sf->sorted, s);
+  err = flow_record(sf->sorted, s);
   if (err != cudaSuccess) return err;
   if (TBE_REFRESH_IN_PREPROCESS) {
     // the next hot set needs only this batch's runs and hot-row counts;
@@ -1375,7 +1377,7 @@ cudaError_t preprocess_t(const Launch& L, const WsLayout& W, char* ws, const Ind
     err = launch_hot_refresh(Ls, W, ws);
     if (err != cudaSuccess) return err;
   }
-  err = cudaEventRecord(sf->done, s);
+  err = flow_record(sf->done, s);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

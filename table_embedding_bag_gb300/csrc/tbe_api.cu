@@ -44,12 +44,12 @@ SideFlow* lookup_flow(const void* ws, bool create) {
   const int prio = TBE_SIDE_PRIORITY ? prio_greatest : 0;
   const bool ok = cudaStreamCreateWithPriority(&f.side, cudaStreamNonBlocking, prio) == cudaSuccess &&
                   cudaEventCreateWithFlags(&f.fork, ef) == cudaSuccess &&
-                  cudaEventCreateWithFlags(&f.sorted, ef) == cudaSuccess &&
-                  cudaEventCreateWithFlags(&f.hot, ef) == cudaSuccess &&
-                  cudaEventCreateWithFlags(&f.done, ef) == cudaSuccess;
+                  cudaEventCreateWithFlags(&f.sorted.ev, ef) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&f.hot.ev, ef) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&f.done.ev, ef) == cudaSuccess;
   if (!ok) {
     // give back what was created; the next call tries again
-    for (cudaEvent_t e : {f.fork, f.sorted, f.hot, f.done})
+    for (cudaEvent_t e : {f.fork, f.sorted.ev, f.hot.ev, f.done.ev})
       if (e) cudaEventDestroy(e);
     if (f.side) cudaStreamDestroy(f.side);
     return nullptr;
@@ -67,6 +67,31 @@ cudaError_t fork_to(SideFlow* f, cudaStream_t s) {
   cudaError_t e = cudaEventRecord(f->fork, s);
   if (e != cudaSuccess) return e;
   return cudaStreamWaitEvent(f->side, f->fork, 0);
+}
+
+namespace {
+cudaError_t capturing(cudaStream_t s, bool* yes) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  *yes = cs != cudaStreamCaptureStatusNone;
+  return e;
+}
+}  // namespace
+
+cudaError_t flow_record(FlowEvent& e, cudaStream_t s) {
+  bool cap = false;
+  const cudaError_t err = capturing(s, &cap);
+  if (err != cudaSuccess) return err;
+  e.captured = cap;
+  return cudaEventRecord(e.ev, s);
+}
+
+cudaError_t flow_wait(cudaStream_t s, const FlowEvent& e) {
+  bool cap = false;
+  const cudaError_t err = capturing(s, &cap);
+  if (err != cudaSuccess) return err;
+  if (cap != e.captured) return cudaSuccess;
+  return cudaStreamWaitEvent(s, e.ev, 0);
 }
 
 

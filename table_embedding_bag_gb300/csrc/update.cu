@@ -1345,14 +1345,16 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
       hot_finish_kernel<false><<<static_cast<unsigned>(d->T) * kHot, 256, 0, Ls.s>>>(
           a, hot_keys, hot_n, hot_cnt, W.hot_parts, part);
     note_launch();
-    e = cudaEventRecord(sf->hot, Ls.s);
+    e = flow_record(sf->hot, Ls.s);
     if (e != cudaSuccess) return e;
-    e = cudaEventRecord(sf->done, Ls.s);
-    if (e != cudaSuccess) return e;
+    if (TBE_HOT_GRAD_SIDE) {  // the side stream's latest work (after the refresh)
+      e = flow_record(sf->done, Ls.s);
+      if (e != cudaSuccess) return e;
+    }
   }
   // the cold rows need the sort chain; their work cursors start at zero
   {
-    cudaError_t e = cudaStreamWaitEvent(L.s, sf->sorted, 0);
+    cudaError_t e = flow_wait(L.s, sf->sorted);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(a.cursors, 0, 3 * sizeof(uint32_t), L.s);
     if (e != cudaSuccess) return e;
@@ -1360,12 +1362,23 @@ cudaError_t launch_update(const Launch& L, const WsLayout& W, char* ws, const fl
   const uint32_t* medium = reinterpret_cast<const uint32_t*>(ws + W.medium_run);
   if (elementwise) launch_runs<true>(L, a, medium, blocks, weighted, wide, two_launch);
   else launch_runs<false>(L, a, medium, blocks, weighted, wide, two_launch);
-  if (!W.hot_enabled) return cudaGetLastError();  // no histogram: the hot set stays empty
-  // the caller's stream joins the hot rows' update
-  cudaError_t e = cudaStreamWaitEvent(L.s, sf->hot, 0);
+  cudaError_t e = cudaSuccess;
+  if (W.hot_enabled) {  // without a histogram the hot set stays empty
+    // the caller's stream joins the hot rows' update
+    e = flow_wait(L.s, sf->hot);
+    if (e != cudaSuccess) return e;
+    if (!TBE_REFRESH_IN_PREPROCESS) {  // else the preprocess chose the next set
+      e = launch_hot_refresh(L, W, ws);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  // and every side-stream segment of this call and of its preprocess (the
+  // sort chain, the hot-set refresh): once the call's work on the caller's
+  // stream is done, all of it is, and a CUDA graph that captures whole steps
+  // has no unjoined work
+  e = flow_wait(L.s, sf->done);
   if (e != cudaSuccess) return e;
-  if (TBE_REFRESH_IN_PREPROCESS) return cudaGetLastError();  // the preprocess chose it
-  return launch_hot_refresh(L, W, ws);
+  return cudaGetLastError();
 }
 
 // The next call's hot set, chosen from this call's lookups: the cold runs'
