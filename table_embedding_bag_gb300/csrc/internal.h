@@ -18,14 +18,14 @@ void note_launch();
 void probe_begin(uint32_t kernel, cudaStream_t s);
 void probe_end(uint32_t kernel, cudaStream_t s);
 
-// An event of the flow and whether its latest record was made while its
-// stream was being captured into a CUDA graph (such a record is a
-// dependency inside that graph, not a point in any stream: a wait outside
-// the capture may not name it, and a capture may not wait on a record made
-// outside it).
+// An event of the flow and the stream capture its latest record was made
+// in (0: none).  A record made while a stream is captured into a CUDA graph
+// is a dependency inside that graph, not a point in any stream: only the
+// same capture may wait on it, and a capture may wait on no record made
+// outside it.
 struct FlowEvent {
   cudaEvent_t ev = nullptr;
-  bool captured = false;
+  unsigned long long capture = 0;
 };
 
 // Side stream of one workspace (one per workspace and device, created at the
@@ -51,12 +51,12 @@ SideFlow* side_flow(const void* ws);
 SideFlow* find_side_flow(const void* ws);
 // Makes `side` wait for everything enqueued on `s` so far.
 cudaError_t fork_to(SideFlow* f, cudaStream_t s);
-// Records e on s, noting whether s is being captured.
+// Records e on s, noting the capture s is in.
 cudaError_t flow_record(FlowEvent& e, cudaStream_t s);
-// Makes s wait for e's latest record when both lie on the same side of a
-// capture; otherwise the wait is left out: a record made inside a graph is
-// ordered by the graph's replays on the caller's stream, and one made
-// before a capture by the synchronisation that precedes it.
+// Makes s wait for e's latest record when both belong to the same capture
+// (or to none); otherwise the wait is left out: a record made inside a
+// graph is ordered by that graph's replays on the caller's stream, and one
+// made before a capture by the synchronisation that precedes it.
 cudaError_t flow_wait(cudaStream_t s, const FlowEvent& e);
 
 // One call's launch context.

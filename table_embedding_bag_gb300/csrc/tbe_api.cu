@@ -70,27 +70,29 @@ cudaError_t fork_to(SideFlow* f, cudaStream_t s) {
 }
 
 namespace {
-cudaError_t capturing(cudaStream_t s, bool* yes) {
+// The id of the capture s is in, 0 when it is not being captured.
+cudaError_t capture_id(cudaStream_t s, unsigned long long* id) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  const cudaError_t e = cudaStreamIsCapturing(s, &cs);
-  *yes = cs != cudaStreamCaptureStatusNone;
+  unsigned long long v = 0;
+  const cudaError_t e = cudaStreamGetCaptureInfo(s, &cs, &v);
+  *id = cs == cudaStreamCaptureStatusActive ? v : 0ull;
   return e;
 }
 }  // namespace
 
 cudaError_t flow_record(FlowEvent& e, cudaStream_t s) {
-  bool cap = false;
-  const cudaError_t err = capturing(s, &cap);
+  unsigned long long id = 0;
+  const cudaError_t err = capture_id(s, &id);
   if (err != cudaSuccess) return err;
-  e.captured = cap;
+  e.capture = id;
   return cudaEventRecord(e.ev, s);
 }
 
 cudaError_t flow_wait(cudaStream_t s, const FlowEvent& e) {
-  bool cap = false;
-  const cudaError_t err = capturing(s, &cap);
+  unsigned long long id = 0;
+  const cudaError_t err = capture_id(s, &id);
   if (err != cudaSuccess) return err;
-  if (cap != e.captured) return cudaSuccess;
+  if (id != e.capture) return cudaSuccess;
   return cudaStreamWaitEvent(s, e.ev, 0);
 }
 

@@ -3,10 +3,12 @@
 Every backward joins the workspace's side-stream work (sort chain, hot-set
 refresh) into its stream before it returns, so a step -- tbe_preprocess,
 tbe_forward(TBE_F_PREPROCESSED), tbe_backward_rowwise_adagrad(TBE_F_PREPROCESSED)
--- can be captured.  Replaying the graph must give bit for bit what the same
-steps give when launched one by one from the same state (weights, momentum,
-workspace with its hot set): the kernels sum in a fixed order whichever warp
-takes which task.  The first replayed step is also checked against the oracle.
+-- can be captured, again and again on one workspace.  Replaying the graphs
+must give bit for bit what the same steps give when launched one by one from
+the same state (weights, momentum, workspace with its hot set): the kernels
+sum in a fixed order whichever warp takes which task.  A step launched after
+a replay, on the same workspace, continues from it.  The first replayed step
+is also checked against the oracle.
 """
 import numpy as np
 import pytest
@@ -65,20 +67,23 @@ def test_graph_replay_matches_eager_steps(case):
     torch.cuda.synchronize()
     W_e, m_e = run.weights.clone(), run.momentum.clone()
 
-    # graph: the same two steps from the same state
+    # graphs: the same two steps from the same state, each captured into a
+    # graph of its own on the same workspace (a later capture must not wait
+    # on an earlier one's records), replayed in turn
     _restore(run, s0)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
+    graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g, stream=side):
-            _step(run)
+    for g in graphs:
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                _step(run)
     torch.cuda.synchronize()
     _restore(run, s0)  # capture ran nothing, but start from the saved state all the same
     torch.cuda.synchronize()
     outs_g = []
-    for _ in range(2):
+    for g in graphs:
         g.replay()
         torch.cuda.synchronize()
         outs_g.append(run.out.clone())
@@ -93,7 +98,7 @@ def test_graph_replay_matches_eager_steps(case):
     W1, m1 = oracle.backward_rowwise_adagrad(tab, w.B, hw["indices"], hw["offsets"],
                                              hw["grad_out"], W0, m0, w.lr, w.eps, hw["psw"])
     _restore(run, s0)
-    g.replay()
+    graphs[0].replay()
     torch.cuda.synchronize()
     ref = oracle.forward(tab, w.B, W0, hw["indices"], hw["offsets"], hw["psw"])
     terms = oracle.forward(tab, w.B, np.abs(W0), hw["indices"], hw["offsets"],
@@ -101,3 +106,11 @@ def test_graph_replay_matches_eager_steps(case):
     H.assert_forward_close(run.out.cpu().numpy(), ref, terms)
     H.assert_momentum_close(run.momentum.cpu().numpy(), m1)
     H.assert_weights_within_ulp(run.host_weights(), W1)
+    # a step launched after the replay continues from it: replayed first
+    # step plus launched second step = the two launched steps
+    _step(run)
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    assert torch.equal(run.out, outs_e[1])
+    assert torch.equal(run.weights.view(torch.int16), W_e.view(torch.int16))
+    assert torch.equal(run.momentum, m_e)
