@@ -183,9 +183,12 @@ ROOFLINE_KERNELS = {
     "expand_count_kernel": {
         "what": "expand of tbe_preprocess: reads every index, writes the hot rows' byte "
                 "histogram and the cold keys",
-        "probe": "TBE_PROBE_EXPAND_COUNT", "sources": ("preprocess.cu", "common.cuh"),
+        "probe": "TBE_PROBE_EXPAND_COUNT",
+        # the part of preprocess.cu up to the end of the kernel (its helpers
+        # come before it), and common.cuh
+        "sources": (("preprocess.cu", "// Compaction of the cold lookups"), "common.cuh"),
         "record": {"bytes_per_unit": 9.306, "unit": "lookup",
-                   "source_sha1": "e126eddae0d0fad3",
+                   "source_sha1": "0f27c5bf3f9aaa36",
                    "capture": "hot-row recipe reduced to one table (E=1e7, D=128, B=131072), "
                               "two launches, dram__bytes_read.sum + dram__bytes_write.sum = "
                               "243.9 MB per launch over 26.21 M lookups"}},
@@ -211,11 +214,19 @@ ROOFLINE_KERNELS = {
 
 
 def source_sha1(files):
-    """First 16 hex digits of the sha1 over a kernel's source files."""
+    """First 16 hex digits of the sha1 over a kernel's sources: whole files,
+    or (file, marker) for the part of a file before the marker line."""
     import hashlib
     h = hashlib.sha1()
     for f in files:
-        h.update(open(os.path.join(ROOT, "table_embedding_bag_gb300", "csrc", f), "rb").read())
+        name, marker = (f, None) if isinstance(f, str) else f
+        text = open(os.path.join(ROOT, "table_embedding_bag_gb300", "csrc", name), "rb").read()
+        if marker is not None:
+            cut = text.find(marker.encode())
+            if cut < 0:
+                raise SystemExit(f"bench: marker {marker!r} not found in {name}")
+            text = text[:cut]
+        h.update(text)
     return h.hexdigest()[:16]
 
 

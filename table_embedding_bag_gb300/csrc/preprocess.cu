@@ -390,13 +390,12 @@ __global__ void __launch_bounds__(256)
                         const uint32_t* __restrict__ sp_keys,
                         const float* __restrict__ sp_psw, uint32_t* __restrict__ keys,
                         uint32_t* __restrict__ vals, float* __restrict__ psw_out) {
-  __shared__ uint32_t bag_base[kHotTileBags];
+  __shared__ uint32_t rel[kHotTileBags + 1];  // each bag's first entry relative to the tile's
   __shared__ unsigned long long scan[33];
   __shared__ int64_t bag_off[kHotTileBags + 1];
   const TileInfo ti = tile_info(B);
-  const int warp = threadIdx.x >> 5;
-  const unsigned lane = lane_id();
   load_tile_offsets(offsets, ti, B, n, bag_off);  // read after the scan's barriers
+  unsigned long long tile_total = 0;
   {
     // exclusive prefix of the tile's per-bag cold counts = the bags' first
     // entries in the dense list.  In 64 bits and capped at n: with
@@ -412,8 +411,12 @@ __global__ void __launch_bounds__(256)
     const unsigned long long cap = static_cast<unsigned long long>(n);
     const unsigned long long first = tile_base[blockIdx.x] + inc - c;
     const uint32_t first_c = static_cast<uint32_t>(first < cap ? first : cap);
-    if (lb < kHotTileBags) bag_base[lb] = first_c;
+    // relative starts saturate at 2^32 - 1: the entries copied below lie
+    // below n - tile base < 2^32, where the saturated values still order them
+    const unsigned long long r = inc - c;
+    if (lb < kHotTileBags) rel[lb] = static_cast<uint32_t>(r < 0xffffffffull ? r : 0xffffffffull);
     if (lb < ti.nbags) cold_off[static_cast<int64_t>(ti.t) * B + ti.b0 + lb] = first_c;
+    tile_total = total;
     if (lb == 0 && blockIdx.x == gridDim.x - 1) {
       const unsigned long long last = tile_base[blockIdx.x] + total;
       cold_off[static_cast<int64_t>(ti.t) * B + ti.b0 + ti.nbags] =
@@ -421,20 +424,27 @@ __global__ void __launch_bounds__(256)
     }
   }
   __syncthreads();
-  for (int lb = warp; lb < ti.nbags; lb += 8) {
-    const int64_t bag = static_cast<int64_t>(ti.t) * B + ti.b0 + lb;
-    const int64_t s = bag_off[lb];
-    const uint32_t pos = bag_base[lb];
-    // entries at or past n are dropped (malformed offsets only; see above)
-    const int64_t room = n - static_cast<int64_t>(pos);
-    const uint32_t c = static_cast<uint32_t>(
-        min(static_cast<int64_t>(bag_cold[bag]), room > 0 ? room : int64_t(0)));
-    const uint32_t bag_in_table = static_cast<uint32_t>(ti.b0 + lb);
-    for (uint32_t i = lane; i < c; i += 32) {
-      keys[pos + i] = __ldg(sp_keys + s + i);
-      vals[pos + i] = bag_in_table;
-      if (kWeighted) psw_out[pos + i] = __ldg(sp_psw + s + i);
+  // The tile's entries as one dense range, the threads striding over it
+  // (a bag holds about as many cold entries as a warp has lanes, so a
+  // warp per bag left lanes idle and waited on each bag's loads in turn).
+  // Entry i belongs to the last bag whose relative start is at most i;
+  // entries at or past n are dropped (malformed offsets only; see above).
+  const unsigned long long tb = tile_base[blockIdx.x];
+  const unsigned long long un = static_cast<unsigned long long>(n);
+  const unsigned long long room = tb < un ? un - tb : 0ull;
+  const uint32_t lim = static_cast<uint32_t>(tile_total < room ? tile_total : room);
+  const uint64_t pos0 = tb;
+#pragma unroll 4
+  for (uint32_t i = threadIdx.x; i < lim; i += blockDim.x) {
+    int lo = 0, hi = ti.nbags - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (rel[mid] <= i) lo = mid; else hi = mid - 1;
     }
+    const int64_t src = bag_off[lo] + static_cast<int64_t>(i - rel[lo]);
+    keys[pos0 + i] = __ldg(sp_keys + src);
+    vals[pos0 + i] = static_cast<uint32_t>(ti.b0 + lo);
+    if (kWeighted) psw_out[pos0 + i] = __ldg(sp_psw + src);
   }
 }
 
