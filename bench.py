@@ -712,6 +712,28 @@ def run_native(args, world, rank, local):
                          + hgrad.numel() * 4)
         result["d2h"] = h_out.numel() * 4
         result["e2e_copy_streams"] = nup
+        # the host link as this process sees it, for context: one step's
+        # uploads (all on one stream) and its download, each alone, best of
+        # three; the e2e step cannot be shorter than the slower direction
+        d_idx, d_off, d_grad = slots[0]
+        h_idx, h_off, h_grad = hb[0]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        up_ms, down_ms = [], []
+        for _ in range(3):
+            ev[0].record(stream)
+            for d, h in ((d_idx, h_idx), (d_off, h_off), (d_grad, h_grad)):
+                d.copy_(h, non_blocking=True)
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            up_ms.append(ev[0].elapsed_time(ev[1]))
+            ev[0].record(stream)
+            h_out.copy_(out, non_blocking=True)
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            down_ms.append(ev[0].elapsed_time(ev[1]))
+        result["link"] = {"h2d_GBps": result["h2d"] / min(up_ms) / 1e6,
+                          "d2h_GBps": result["d2h"] / min(down_ms) / 1e6,
+                          "h2d_ms": min(up_ms), "d2h_ms": min(down_ms)}
         del hb, slots
     return result
 
@@ -954,7 +976,7 @@ def main():
         line["e2e"] = {"value": r["e2e_lookups"] * world / (r["e2e_ms"] / 1e3),
                        "unit": "lookups/s", "h2d_bytes_per_step": r["h2d"],
                        "d2h_bytes_per_step": r["d2h"],
-                       "copy_streams": r["e2e_copy_streams"]}
+                       "copy_streams": r["e2e_copy_streams"], "link": r["link"]}
     if not args.no_configs and not reduced and world == 1 and args.weights == "fp16" \
             and not ew and args.pooling == "sum":
         import table_embedding_bag_gb300 as tbe
