@@ -806,6 +806,55 @@ def cpu_baseline_parallel(w, bags, cores, mean=False, elementwise=False):
     return n / secs, n, secs
 
 
+def _openmp_worker(job):
+    """The oracle's OpenMP form on one sample with `threads` threads, timed
+    in this (spawned) process: (seconds, lookups, threads) or (None, reason,
+    0) if it could not be built or run here."""
+    threads, E, D, B, idx, off, W, G, lr, eps, mean, ew, bf16, fp32 = job
+    try:
+        import oracle
+        import oracle.openmp as omp
+        omp.build()
+        omp.set_threads(threads)
+        tab = oracle.Tables(E, D)
+        m = np.zeros(int(tab.w_offsets[-1]) if ew else int(tab.hash_base[-1]), np.float32)
+        t = time.perf_counter()
+        omp.forward(tab, B, W, idx, off, mean=mean, bf16=bf16, fp32=fp32)
+        omp.backward_rowwise_adagrad(tab, B, idx, off, G, W, m, lr, eps, mean=mean, bf16=bf16,
+                                     elementwise=ew, fp32=fp32)
+        return time.perf_counter() - t, len(idx), omp.threads()
+    except Exception as e:  # a host without OpenMP: reported, not fatal
+        return None, f"{type(e).__name__}: {e}"[:200], 0
+
+
+def cpu_baseline_openmp(w, bags, cores, mean=False, elementwise=False):
+    """The oracle's OpenMP form (forward parallel over bags, backward over the
+    rows of the run map after a parallel sort) on bags [0, bags) of table 0
+    of batch w, with one thread per host core, in a spawned process."""
+    try:
+        return _cpu_baseline_openmp(w, bags, cores, mean, elementwise)
+    except Exception as e:  # reported, not fatal: the line is printed either way
+        return {"value": None, "reason": f"{type(e).__name__}: {e}"[:200]}
+
+
+def _cpu_baseline_openmp(w, bags, cores, mean, elementwise):
+    import multiprocessing as mp
+    s = cpu_sample(w, bags)
+    bf16 = s.weights.dtype == torch.bfloat16
+    fp32 = s.weights.dtype == torch.float32
+    W = s.weights.view(torch.int16).numpy().view(np.uint16) if bf16 else s.weights.numpy()
+    job = (cores, s.E, s.D, s.B, s.indices.numpy(), s.offsets.numpy(), W, s.grad_out.numpy(),
+           s.lr, s.eps, mean, elementwise, bf16, fp32)
+    with mp.get_context("spawn").Pool(1) as pool:  # left with terminate() on a time-out
+        secs, n, threads = pool.apply_async(_openmp_worker, (job,)).get(timeout=300)
+    if secs is None:
+        return {"value": None, "reason": n}
+    return {"value": n / secs, "unit": "lookups/s", "threads": threads,
+            "kind": "oracle, OpenMP form (bit-identical results)",
+            "sample": f"table 0 of the first batch, bags [0, {bags}) ({n} lookups), forward "
+                      f"+ backward, {secs:.1f} s wall"}
+
+
 def _reference_worker(job):
     """One host core's share of a reference-arm step: draw its own sample of
     the recipe and time the oracle on it (the draw is not timed)."""
@@ -997,7 +1046,8 @@ def main():
                                           f"{secs:.1f} s wall",
                                 "single_core": {"value": s.n / dt, "cores": 1,
                                                 "sample": f"the first {args.cpu_bags} bags "
-                                                          f"({s.n} lookups)"}}
+                                                          f"({s.n} lookups)"},
+                                "openmp": cpu_baseline_openmp(w, per * cores, cores, mean, ew_)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
