@@ -846,7 +846,7 @@ def _cpu_baseline_openmp(w, bags, cores, mean, elementwise):
     job = (cores, s.E, s.D, s.B, s.indices.numpy(), s.offsets.numpy(), W, s.grad_out.numpy(),
            s.lr, s.eps, mean, elementwise, bf16, fp32)
     with mp.get_context("spawn").Pool(1) as pool:  # left with terminate() on a time-out
-        secs, n, threads = pool.apply_async(_openmp_worker, (job,)).get(timeout=300)
+        secs, n, threads = pool.apply_async(_openmp_worker, (job,)).get(timeout=120)
     if secs is None:
         return {"value": None, "reason": n}
     return {"value": n / secs, "unit": "lookups/s", "threads": threads,
